@@ -114,10 +114,17 @@ def topk_row(scores_row, k: int) -> np.ndarray:
     Total order: larger score first, equal scores by lower index; -0.0 and
     +0.0 compare equal; NaN ranks below every number.
     """
-    s = _f64(scores_row)
-    key = np.where(np.isnan(s), np.inf, -s)      # ascending key; NaN last
-    order = np.argsort(key, kind="stable")        # stable => lower index first on ties
-    return np.sort(order[:k])
+    return np.sort(_rank_order(_f64(scores_row)[None, :])[0, :k])
+
+
+def _rank_order(S2: np.ndarray) -> np.ndarray:
+    """Per row, indices from best to worst under the total order above."""
+    nan = np.isnan(S2)
+    key = np.where(nan, np.inf, -S2)                           # larger score first
+    order = np.argsort(key, axis=1, kind="stable")            # stable => lower index first on ties
+    # NaN after every number, -inf included (second stable pass keeps index order)
+    back = np.argsort(np.take_along_axis(nan, order, axis=1), axis=1, kind="stable")
+    return np.take_along_axis(order, back, axis=1)
 
 
 def topk_lists(S, k_per_head: Sequence[int]) -> Tuple[np.ndarray, np.ndarray]:
@@ -130,9 +137,7 @@ def topk_lists(S, k_per_head: Sequence[int]) -> Tuple[np.ndarray, np.ndarray]:
     for b in range(B):
         for h in range(H):
             k = int(k_per_head[h])
-            key = np.where(np.isnan(S[b, h]), np.inf, -S[b, h])
-            order = np.argsort(key, axis=1, kind="stable")[:, :k]
-            sel = np.sort(order, axis=1)
+            sel = np.sort(_rank_order(S[b, h])[:, :k], axis=1)
             for g in range(G):
                 cols.append(sel[g])
                 ptr[row + 1] = ptr[row] + k

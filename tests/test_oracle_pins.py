@@ -128,6 +128,8 @@ def test_topk_constructed_ties():
     assert oracle.topk_row([2.0] * 9, 4).tolist() == [0, 1, 2, 3]
     assert oracle.topk_row([np.nan, 1.0, 2.0, np.nan], 3).tolist() == [0, 1, 2]
     assert oracle.topk_row([-np.inf, np.nan, -1.0], 2).tolist() == [0, 2]
+    assert oracle.topk_row([np.nan, -np.inf], 1).tolist() == [1]          # NaN below -inf
+    assert oracle.topk_row([np.nan, -np.inf, np.nan, -np.inf], 3).tolist() == [0, 1, 3]
 
 
 def test_topk_lists_invariants(rng):
