@@ -1,0 +1,252 @@
+"""Thin Python binding of libdsv.so (the C ABI declared in include/dsv.h).
+
+Argument marshalling only: torch tensors supply device memory and the current
+CUDA stream; every step of the hot path runs in the library's kernels.  There
+is no fallback: if the library has not been built (``__graft_entry__.build()``
+or ``python -m dynamic_block_sparse_projection_gb300.build``) importing this
+module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+_LIB_PATH = Path(__file__).resolve().parent / "_build" / "libdsv.so"
+
+DSV_OK, DSV_ERR_INVALID_ARG, DSV_ERR_UNSUPPORTED, DSV_ERR_CUDA, DSV_ERR_BAD_INDEX, DSV_ERR_TIMEOUT = range(6)
+
+# Every symbol the header declares; checked at load time.
+EXPORTS = (
+    "dsv_predict_workspace_bytes", "dsv_predict_scores",
+    "dsv_topk_workspace_bytes", "dsv_topk_blocks",
+    "dsv_sparse_attn_fwd",
+    "dsv_attn_bwd_workspace_bytes", "dsv_sparse_attn_bwd",
+    "dsv_status_string", "dsv_get_device_error", "dsv_clear_device_error",
+    "dsv_set_wait_limit_ns", "dsv_version",
+)
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("N", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("block", ctypes.c_int32), ("r", ctypes.c_int32)]
+
+
+class DsvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def _load() -> ctypes.CDLL:
+    if not _LIB_PATH.exists():
+        raise ImportError(f"libdsv.so is not built ({_LIB_PATH}); run __graft_entry__.build() first")
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    missing = [s for s in EXPORTS if not hasattr(lib, s)]
+    if missing:
+        raise ImportError(f"libdsv.so lacks symbols: {missing}")
+    vp, sz, i32, u32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.POINTER(ctypes.c_uint32)
+    lib.dsv_predict_workspace_bytes.argtypes = [Shape]
+    lib.dsv_predict_workspace_bytes.restype = sz
+    lib.dsv_predict_scores.argtypes = [vp, vp, vp, vp, Shape, vp, vp, sz, vp]
+    lib.dsv_predict_scores.restype = ctypes.c_int
+    lib.dsv_topk_workspace_bytes.argtypes = [Shape]
+    lib.dsv_topk_workspace_bytes.restype = sz
+    lib.dsv_topk_blocks.argtypes = [vp, Shape, ctypes.POINTER(i32), vp, vp, vp, vp, vp, sz, vp]
+    lib.dsv_topk_blocks.restype = ctypes.c_int
+    lib.dsv_sparse_attn_fwd.argtypes = [vp, vp, vp, Shape, vp, vp, ctypes.c_float, vp, vp, vp]
+    lib.dsv_sparse_attn_fwd.restype = ctypes.c_int
+    lib.dsv_attn_bwd_workspace_bytes.argtypes = [Shape]
+    lib.dsv_attn_bwd_workspace_bytes.restype = sz
+    lib.dsv_sparse_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, Shape, vp, vp, vp, vp, ctypes.c_float,
+                                        vp, vp, vp, vp, sz, vp]
+    lib.dsv_sparse_attn_bwd.restype = ctypes.c_int
+    lib.dsv_status_string.argtypes = [ctypes.c_int]
+    lib.dsv_status_string.restype = ctypes.c_char_p
+    lib.dsv_get_device_error.argtypes = [vp, u32p]
+    lib.dsv_get_device_error.restype = ctypes.c_int
+    lib.dsv_clear_device_error.argtypes = [vp]
+    lib.dsv_clear_device_error.restype = ctypes.c_int
+    lib.dsv_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.dsv_set_wait_limit_ns.restype = ctypes.c_int
+    lib.dsv_version.argtypes = []
+    lib.dsv_version.restype = i32
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.dsv_status_string(status).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != DSV_OK:
+        raise DsvError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device, stream=None) -> Optional[int]:
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return s.cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, device: Optional[torch.device] = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def nnz_of(B: int, G: int, k_per_head: Sequence[int]) -> int:
+    return B * G * int(sum(int(k) for k in k_per_head))
+
+
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.Tensor:
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError(f"workspace needs {nbytes} bytes")
+        return workspace
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+
+
+def predict_workspace_bytes(B: int, H: int, N: int, d: int, block: int, r: int) -> int:
+    return lib.dsv_predict_workspace_bytes(Shape(B, H, N, d, block, r))
+
+
+def topk_workspace_bytes(B: int, H: int, N: int, d: int, block: int) -> int:
+    return lib.dsv_topk_workspace_bytes(Shape(B, H, N, d, block, 8))
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, N: int, d: int, block: int) -> int:
+    return lib.dsv_attn_bwd_workspace_bytes(Shape(B, H, N, d, block, 8))
+
+
+# ---------------------------------------------------------------------------
+# The four calls of the hot path
+# ---------------------------------------------------------------------------
+
+def predict_scores(Q, K, Wq, Wk, block: int, *, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """scores[b,h,g,j] = qbar_g . kbar_j (fp32 [B,H,G,nb]); see dsv_predict_scores."""
+    _need(Q, "Q", torch.bfloat16)
+    dev = Q.device
+    _need(K, "K", torch.bfloat16, dev)
+    _need(Wq, "Wq", torch.float32, dev)
+    _need(Wk, "Wk", torch.float32, dev)
+    B, H, N, d = Q.shape
+    r = Wq.shape[-1]
+    s = Shape(B, H, N, d, block, r)
+    G = N // block if block else 0
+    if out is None:
+        out = torch.empty(B, H, G, G, dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, dev)
+    nbytes = lib.dsv_predict_workspace_bytes(s)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(lib.dsv_predict_scores(_ptr(Q), _ptr(K), _ptr(Wq), _ptr(Wk), s, _ptr(out), _ptr(ws), nbytes,
+                                  _stream(dev, stream)), "dsv_predict_scores")
+    return out
+
+
+def topk_blocks(scores, k_per_head: Sequence[int], block: int, N: int, d: int = 128, *, outs=None,
+                workspace=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(fwd_ptr, fwd_col, bwd_ptr, bwd_col) int32 CSR lists; see dsv_topk_blocks."""
+    _need(scores, "scores", torch.float32)
+    dev = scores.device
+    B, H, G, nb = scores.shape
+    s = Shape(B, H, N, d, block, 8)
+    nnz = nnz_of(B, G, k_per_head)
+    if outs is None:
+        outs = (torch.empty(B * H * G + 1, dtype=torch.int32, device=dev),
+                torch.empty(max(nnz, 1), dtype=torch.int32, device=dev),
+                torch.empty(B * H * nb + 1, dtype=torch.int32, device=dev),
+                torch.empty(max(nnz, 1), dtype=torch.int32, device=dev))
+    for name, t in zip(("fwd_ptr", "fwd_col", "bwd_ptr", "bwd_col"), outs):
+        _need(t, name, torch.int32, dev)
+    karr = (ctypes.c_int32 * max(H, 1))(*[int(k) for k in k_per_head])
+    nbytes = lib.dsv_topk_workspace_bytes(s)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(lib.dsv_topk_blocks(_ptr(scores), s, karr, *[_ptr(t) for t in outs], _ptr(ws), nbytes,
+                               _stream(dev, stream)), "dsv_topk_blocks")
+    fp, fc, bp, bc = outs
+    return fp, fc[:nnz], bp, bc[:nnz]
+
+
+def sparse_attn_fwd(Q, K, V, fwd_ptr, fwd_col, block: int, softmax_scale: float = 0.0, *, out=None, lse=None,
+                    stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(O bf16 [B,H,N,d], lse fp32 [B,H,N]); see dsv_sparse_attn_fwd."""
+    _need(Q, "Q", torch.bfloat16)
+    dev = Q.device
+    for name, t in (("K", K), ("V", V)):
+        _need(t, name, torch.bfloat16, dev)
+    for name, t in (("fwd_ptr", fwd_ptr), ("fwd_col", fwd_col)):
+        _need(t, name, torch.int32, dev)
+    B, H, N, d = Q.shape
+    s = Shape(B, H, N, d, block, 8)
+    if out is None:
+        out = torch.empty_like(Q)
+    if lse is None:
+        lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    _check(lib.dsv_sparse_attn_fwd(_ptr(Q), _ptr(K), _ptr(V), s, _ptr(fwd_ptr), _ptr(fwd_col),
+                                   float(softmax_scale), _ptr(out), _ptr(lse), _stream(dev, stream)),
+           "dsv_sparse_attn_fwd")
+    return out, lse
+
+
+def sparse_attn_bwd(Q, K, V, O, dO, lse, fwd_ptr, fwd_col, bwd_ptr, bwd_col, block: int,
+                    softmax_scale: float = 0.0, *, outs=None, workspace=None, stream=None):
+    """(dQ, dK, dV) bf16 [B,H,N,d]; see dsv_sparse_attn_bwd."""
+    _need(Q, "Q", torch.bfloat16)
+    dev = Q.device
+    for name, t in (("K", K), ("V", V), ("O", O), ("dO", dO)):
+        _need(t, name, torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    for name, t in (("fwd_ptr", fwd_ptr), ("fwd_col", fwd_col), ("bwd_ptr", bwd_ptr), ("bwd_col", bwd_col)):
+        _need(t, name, torch.int32, dev)
+    B, H, N, d = Q.shape
+    s = Shape(B, H, N, d, block, 8)
+    if outs is None:
+        outs = (torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V))
+    for name, t in zip(("dQ", "dK", "dV"), outs):
+        _need(t, name, torch.bfloat16, dev)
+    nbytes = lib.dsv_attn_bwd_workspace_bytes(s)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(lib.dsv_sparse_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse), s,
+                                   _ptr(fwd_ptr), _ptr(fwd_col), _ptr(bwd_ptr), _ptr(bwd_col),
+                                   float(softmax_scale), *[_ptr(t) for t in outs], _ptr(ws), nbytes,
+                                   _stream(dev, stream)), "dsv_sparse_attn_bwd")
+    return outs
+
+
+# ---------------------------------------------------------------------------
+# Device-side error word
+# ---------------------------------------------------------------------------
+
+def device_error(stream=None, device=None) -> Tuple[int, int]:
+    """(status, info) recorded by the kernels on the current device; synchronises."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    info = ctypes.c_uint32(0)
+    st = lib.dsv_get_device_error(_stream(dev, stream), ctypes.byref(info))
+    return st, info.value
+
+
+def clear_device_error(stream=None, device=None) -> None:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _check(lib.dsv_clear_device_error(_stream(dev, stream)), "dsv_clear_device_error")
+
+
+def set_wait_limit_ns(limit_ns: int) -> None:
+    _check(lib.dsv_set_wait_limit_ns(int(limit_ns)), "dsv_set_wait_limit_ns")

@@ -1,0 +1,326 @@
+// attn_fwd.cu — block-sparse softmax attention forward on tcgen05 tensor cores.
+//
+// DSV page [nl], "Technische samenvatting" 2A (stage 2: only the critical
+// subset of KV pairs is computed) and 2B (a query group shares its critical
+// KV indices); [hi] 2B (grouping maximises coalescing and tensor-core use).
+//
+// One CTA per query group (b, h, g): the group's `block` query rows form the
+// M = 128 rows of every MMA (for block = 64 the upper 64 rows are zero
+// padding).  For each key block j in the group's list:
+//   S = Q K_j^T            tcgen05.mma, A = Q (smem), B = K_j (smem), D in TMEM
+//   P = exp2(S*c - m)      softmax warpgroup, P written back to TMEM as bf16
+//   O += P V_j             tcgen05.mma, A = P (TMEM), B = V_j (smem, MN-major)
+// with an online (running-max) softmax; O is only rescaled when the running
+// max grows by more than 2^8 (values of P then stay below 256).
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: Q once, then K_j / V_j into an NST-deep ring.
+//   warp 1      TMEM allocator; lane 0 issues every MMA and commit.
+//   warps 2..5  softmax / epilogue; warp w owns TMEM lanes 32*(w%4)..+31,
+//               i.e. one query row per thread.
+// TMEM columns: S/P buffer 0 at [0,128), buffer 1 at [128,256), O at [256,256+d).
+// S is double-buffered so the MMA of block n+1 overlaps the softmax of block n.
+#include <math.h>
+
+#include "dsv_launch.h"
+
+namespace dsv {
+
+namespace {
+
+template <int BETA, int D>
+struct FwdTraits {
+  static constexpr int BM = 128;                 // MMA M (query rows incl. padding)
+  static constexpr int NCH = D / 64;             // 64-column (128-byte) chunks along d
+  static constexpr int Q_CHUNK = BM * 128;       // bytes of one Q chunk
+  static constexpr int KV_CHUNK = BETA * 128;    // bytes of one K or V chunk
+  static constexpr int Q_BYTES = NCH * Q_CHUNK;
+  static constexpr int KV_BYTES = NCH * KV_CHUNK;
+  static constexpr int NST = (Q_BYTES + 6 * KV_BYTES + 2048 <= 227 * 1024) ? 3 : 2;
+  static constexpr int NBAR = 1 + 3 * NST + 2 + 2 + 2 + 1;
+  static constexpr int SMEM_USED = 1024 + Q_BYTES + 2 * NST * KV_BYTES + NBAR * 8 + 16;
+  // at least 120 KB so that one CTA owns an SM (and its 512 TMEM columns)
+  static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  static constexpr uint32_t S_COL = 128;         // column stride of the two S/P buffers
+  static constexpr uint32_t O_COL = 256;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TX_BYTES = BETA * D * 2;   // one K or V tile (and the Q tile)
+};
+
+enum : unsigned int { W_Q = 1, W_KEMPTY, W_K, W_P, W_V, W_S, W_O, W_OFINAL, W_DRAIN };
+
+template <int BETA, int D>
+__global__ void __launch_bounds__(192, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ fwd_ptr,
+                    const int32_t* __restrict__ fwd_col, int N, int G, int nb, float scale_log2,
+                    __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, Ctl ctl) {
+  using T = FwdTraits<BETA, D>;
+  constexpr int NST = T::NST;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sbase = align_up_ptr<uint8_t>(smem_raw, 1024);
+  uint8_t* sQ = sbase;
+  uint8_t* sK = sQ + T::Q_BYTES;
+  uint8_t* sV = sK + NST * T::KV_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NST * T::KV_BYTES);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + NST;
+  uint64_t* kv_empty = v_full + NST;
+  uint64_t* s_full = kv_empty + NST;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 2;   // [2]: PV of block n arrives on o_done[n & 1]
+  uint64_t* o_final = o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_final + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = blockIdx.x;  // (b*H + h)*G + g
+  const long long bh = row / G;
+  const int g = (int)(row - bh * G);
+  const int start = fwd_ptr[row];
+  const int cnt = fwd_ptr[row + 1] - start;
+  const unsigned int kid = (unsigned int)KID_FWD << 8;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], 128);
+      mbar_init(&o_done[b], 1);
+    }
+    mbar_init(o_final, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (BETA < T::BM) {
+    // rows BETA..127 of every Q chunk are never loaded: make them zero
+    for (int c = 0; c < T::NCH; ++c) {
+      uint4* z = reinterpret_cast<uint4*>(sQ + c * T::Q_CHUNK + BETA * 128);
+      for (int i = threadIdx.x; i < (T::BM - BETA) * 128 / 16; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, T::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (cnt <= 0) {
+    // empty (or malformed) list: O = 0, lse = -inf
+    if (cnt < 0 && threadIdx.x == 0) set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
+    for (int i = threadIdx.x; i < BETA * D / 8; i += blockDim.x) {
+      reinterpret_cast<uint4*>(O + (bh * N + (long long)g * BETA) * D)[i] = make_uint4(0, 0, 0, 0);
+    }
+    for (int i = threadIdx.x; i < BETA; i += blockDim.x) LSE[bh * N + (long long)g * BETA + i] = -INFINITY;
+  } else if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const int qrow = (int)(bh * N + (long long)g * BETA);
+      mbar_arrive_expect_tx(q_full, T::TX_BYTES);
+      for (int c = 0; c < T::NCH; ++c) tma_load_2d(sQ + c * T::Q_CHUNK, &tmQ, q_full, c * 64, qrow);
+      int issued = 0;
+      int jn = fwd_col[start];
+      for (int n = 0; n < cnt; ++n) {
+        const int s = n % NST;
+        const uint32_t ph = (uint32_t)(n / NST) & 1u;
+        int j = jn;
+        if (n + 1 < cnt) jn = fwd_col[start + n + 1];
+        if (!mbar_wait(&kv_empty[s], ph ^ 1u, abort_flag, ctl, kid | W_KEMPTY)) break;
+        if ((unsigned)j >= (unsigned)nb) {
+          set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
+          j = 0;
+        }
+        const int krow = (int)(bh * N + (long long)j * BETA);
+        mbar_arrive_expect_tx(&k_full[s], T::TX_BYTES);
+        for (int c = 0; c < T::NCH; ++c)
+          tma_load_2d(sK + s * T::KV_BYTES + c * T::KV_CHUNK, &tmK, &k_full[s], c * 64, krow);
+        mbar_arrive_expect_tx(&v_full[s], T::TX_BYTES);
+        for (int c = 0; c < T::NCH; ++c)
+          tma_load_2d(sV + s * T::KV_BYTES + c * T::KV_CHUNK, &tmV, &v_full[s], c * 64, krow);
+        issued = n + 1;
+      }
+      // every copy this thread started must land before the CTA exits
+      mbar_wait(q_full, 0, nullptr, ctl, kid | W_DRAIN);
+      for (int n = (issued > NST ? issued - NST : 0); n < issued; ++n) {
+        const uint32_t ph = (uint32_t)(n / NST) & 1u;
+        mbar_wait(&k_full[n % NST], ph, nullptr, ctl, kid | W_DRAIN);
+        mbar_wait(&v_full[n % NST], ph, nullptr, ctl, kid | W_DRAIN);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t IDS = idesc_bf16_f32(T::BM, BETA, false, false);
+      constexpr uint32_t IDO = idesc_bf16_f32(T::BM, D, false, true);
+      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+      bool ok = mbar_wait(q_full, 0, abort_flag, ctl, kid | W_Q);
+      auto issue_S = [&](int n) -> bool {
+        const int s = n % NST;
+        if (!mbar_wait(&k_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_K)) return false;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(n & 1) * T::S_COL;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = sdesc_sw128(aQ + (kk >> 2) * T::Q_CHUNK + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(aK + s * T::KV_BYTES + (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32, 16, 1024);
+          mma_ss(d_tmem, a, b, IDS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[n & 1]);
+        return true;
+      };
+      if (ok) ok = issue_S(0);
+      for (int n = 0; ok && n < cnt; ++n) {
+        if (n + 1 < cnt && !issue_S(n + 1)) break;
+        if (!mbar_wait(&p_full[n & 1], (uint32_t)(n >> 1) & 1u, abort_flag, ctl, kid | W_P)) break;
+        const int s = n % NST;
+        if (!mbar_wait(&v_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_V)) break;
+        tc_fence_after();
+        const uint32_t p_tmem = tmem + (uint32_t)(n & 1) * T::S_COL;
+#pragma unroll
+        for (int kk = 0; kk < BETA / 16; ++kk) {
+          const uint64_t b = sdesc_sw128(aV + s * T::KV_BYTES + kk * 16 * 128, T::KV_CHUNK, 1024);
+          mma_ts(tmem + T::O_COL, p_tmem + kk * 8, b, IDO, (n > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&kv_empty[s]);
+        mma_commit(&o_done[n & 1]);
+      }
+      mma_commit(o_final);
+      // TMEM is freed after the closing CTA-wide sync only once every MMA is done
+      mbar_wait(o_final, 0, nullptr, ctl, kid | W_DRAIN);
+    }
+  } else {
+    // ---------------- softmax warpgroup (warps 2..5) ----------------
+    const int sp = warp & 3;
+    const int r = sp * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int n = 0; n < cnt; ++n) {
+      if (!mbar_wait_warp(&s_full[n & 1], (uint32_t)(n >> 1) & 1u, abort_flag, ctl, kid | W_S)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sb = tmem + lane_off + (uint32_t)(n & 1) * T::S_COL;
+      uint32_t xr[BETA];
+#pragma unroll
+      for (int c = 0; c < BETA / 32; ++c) tmem_ld32(sb + c * 32, xr + c * 32);
+      tmem_ld_wait();
+      float mx = __uint_as_float(xr[0]);
+#pragma unroll
+      for (int j = 1; j < BETA; ++j) mx = fmaxf(mx, __uint_as_float(xr[j]));
+      const float m_new = fmaxf(m, mx * scale_log2);
+      if (n == 0) {
+        m = m_new;
+      } else if (__any_sync(0xffffffffu, m_new > m + 8.0f)) {
+        // rescale this warp's O rows once the previous PV product has landed
+        if (!mbar_wait_warp(&o_done[(n - 1) & 1], (uint32_t)((n - 1) >> 1) & 1u, abort_flag, ctl, kid | W_O)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float alpha = ex2(m - m_new);
+        l *= alpha;
+        m = m_new;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + T::O_COL + c * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+          tmem_st32(tmem + lane_off + T::O_COL + c * 32, o);
+        }
+        tmem_st_wait();
+      }
+      const float neg_m = -m;
+      float rs = 0.f;
+      uint32_t pk[BETA / 2];
+#pragma unroll
+      for (int j = 0; j < BETA / 2; ++j) {
+        const float p0 = ex2(fmaf(__uint_as_float(xr[2 * j]), scale_log2, neg_m));
+        const float p1 = ex2(fmaf(__uint_as_float(xr[2 * j + 1]), scale_log2, neg_m));
+        rs += p0 + p1;
+        pk[j] = pack_bf16x2(p0, p1);
+      }
+      l += rs;
+#pragma unroll
+      for (int c = 0; c < BETA / 32; ++c) tmem_st16(sb + c * 16, pk + c * 16);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[n & 1]);
+    }
+    if (ok) ok = mbar_wait_warp(o_final, 0, abort_flag, ctl, kid | W_OFINAL);
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.0f / l;
+      const long long orow = bh * N + (long long)g * BETA + r;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + T::O_COL + c * 32, o);
+        tmem_ld_wait();
+        if (r < BETA) {
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(O + orow * D + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
+      }
+      if (r < BETA) LSE[orow] = (m + log2f(l)) * 0.69314718055994530942f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, T::TMEM_COLS);
+}
+
+template <int BETA, int D>
+cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const dsv_shape& s,
+                         const int32_t* fwd_ptr, const int32_t* fwd_col, float scale, void* O, float* lse,
+                         const Ctl& ctl, cudaStream_t st) {
+  using T = FwdTraits<BETA, D>;
+  auto kern = attn_fwd_kernel<BETA, D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
+  if (e != cudaSuccess) return e;
+  const int G = s.N / s.block;
+  const long long rows = (long long)s.B * s.H * G;
+  const float scale_log2 = scale * 1.4426950408889634f;
+  kern<<<(unsigned)rows, 192, T::SMEM, st>>>(tmQ, tmK, tmV, fwd_ptr, fwd_col, s.N, G, G, scale_log2,
+                                             static_cast<__nv_bfloat16*>(O), lse, ctl);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                            const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col, float scale,
+                            void* O, float* lse, const Ctl& ctl, cudaStream_t st) {
+  if (s.block == 128 && s.d == 128)
+    return launch_fwd_t<128, 128>(tmQ, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
+  if (s.block == 128 && s.d == 64)
+    return launch_fwd_t<128, 64>(tmQ, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
+  if (s.block == 64 && s.d == 128)
+    return launch_fwd_t<64, 128>(tmQ, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
+  return launch_fwd_t<64, 64>(tmQ, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
+}
+
+}  // namespace dsv

@@ -1,0 +1,171 @@
+/*
+ * dsv.h — C ABI of the DSV dynamic sparse 3D attention hot path on GB300 (sm_103a).
+ *
+ * Source pages (cited by title and section):
+ *   [nl] "DSV: Exploiting Dynamic Sparsity to Accelerate Large-Scale Video DiT
+ *        Training", gist.science/nl/paper/2502.07590, "Technische samenvatting".
+ *   [hi] the same title, gist.science/hi/paper/2502.07590, technical summary.
+ *
+ * The path: a low-rank predictor scores (query group, key block) pairs
+ * ([nl] 2A, 2B), a per-group top-k picks the critical key blocks ([nl] 2B,
+ * [hi] 2A "critical KV"), and block-sparse softmax attention runs forward and
+ * backward over only those blocks ([nl] 2A stage 2, [hi] 2A/2B).
+ *
+ * Conventions shared by every call
+ *   - Tensors Q, K, V, O, dO, dQ, dK, dV are bf16, shape [B, H, N, d],
+ *     contiguous (d fastest).  Token n of a video latent t x Hl x Wl is in
+ *     raster order n = (t*Hl + y)*Wl + x.
+ *   - A group (queries) and a key block are `block` consecutive tokens:
+ *     G = nb = N / block per (b, h).
+ *   - All pointers except `k_per_head` are DEVICE pointers owned by the
+ *     caller.  The library allocates no device memory; scratch space is
+ *     passed in as `workspace` (size from the *_workspace_bytes query).
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream) and never synchronises the host.
+ *   - Argument errors are detected on the host before any launch and
+ *     returned as DSV_ERR_INVALID_ARG / DSV_ERR_UNSUPPORTED; nothing is
+ *     written then.  A failed launch returns DSV_ERR_CUDA.  Errors found by
+ *     the kernels themselves (an out-of-range index in a caller's list, a
+ *     wait that ran out of time) are recorded in a per-device error word read
+ *     by dsv_get_device_error().
+ *   - Empty problems (B*H*N == 0) are valid: only the CSR row-pointer heads
+ *     are written.
+ *   - Outputs are fully overwritten and bit-identical from run to run (no
+ *     atomics on any output).
+ */
+#ifndef DSV_H_
+#define DSV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-compatible with cudaStream_t. */
+typedef struct CUstream_st* dsv_stream_t;
+
+typedef enum {
+  DSV_OK = 0,
+  DSV_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, k out of range */
+  DSV_ERR_UNSUPPORTED = 2,  /* a size this build has no kernel for */
+  DSV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  DSV_ERR_BAD_INDEX = 4,    /* a kernel met an out-of-range CSR entry */
+  DSV_ERR_TIMEOUT = 5       /* a kernel wait ran past its time limit */
+} dsv_status;
+
+/* Problem shape.  Supported: d in {64, 128}; block in {64, 128};
+ * r a multiple of 8 in [8, 64]; N a multiple of block; H <= 1024;
+ * B*H <= 65535; B*H*N < 2^31; N / block <= 8192 for the top-k. */
+typedef struct {
+  int32_t B, H, N, d, block, r;
+} dsv_shape;
+
+/* ------------------------------------------------------------------------
+ * dsv_predict_scores — low-rank block-score predictor
+ * ([nl] 2A low-rank predictors W^Q_lr, W^K_lr; 2B query grouping / proxy query)
+ *
+ *   qbar[b,h,g] = mean over the `block` tokens i of group g of Q[b,h,i] W^Q[h]
+ *   kbar[b,h,j] = mean over the tokens of key block j of K[b,h,i] W^K[h]
+ *   scores[b,h,g,j] = qbar[b,h,g] . kbar[b,h,j]        (fp32, no scale)
+ *
+ * Q, K      bf16 [B,H,N,d], 16-byte aligned.
+ * Wq, Wk    fp32 [H,d,r] (row-major: r fastest), 16-byte aligned.
+ * scores    fp32 [B,H,G,nb] row-major, 16-byte aligned; overwritten.
+ * workspace >= dsv_predict_workspace_bytes(s) bytes, 256-byte aligned
+ *           (holds the pooled rank-r vectors).
+ * ------------------------------------------------------------------------ */
+size_t dsv_predict_workspace_bytes(dsv_shape s);
+dsv_status dsv_predict_scores(const void* Q, const void* K, const float* Wq, const float* Wk,
+                              dsv_shape s, float* scores, void* workspace, size_t workspace_bytes,
+                              dsv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * dsv_topk_blocks — per-group top-k critical key blocks and their transpose
+ * ([nl] 2B fused estimation & selection; [hi] 2B top-k selection)
+ *
+ * For every row (b,h,g): the k_per_head[h] block indices j with the largest
+ * scores[b,h,g,j]; equal scores go to the lower j; -0.0 equals +0.0; NaN
+ * ranks below every number.  Lists are written in ascending j.
+ *
+ * scores     fp32 [B,H,G,nb] (device), 16-byte aligned.
+ * k_per_head HOST array [H], 1 <= k <= nb.
+ * fwd_ptr    int32 [B*H*G + 1]: row (b*H + h)*G + g holds fwd_col[fwd_ptr[row] .. fwd_ptr[row+1]).
+ * fwd_col    int32 [nnz], nnz = B*G*sum_h k_per_head[h]: block index j within (b,h).
+ * bwd_ptr    int32 [B*H*nb + 1]: row (b*H + h)*nb + j lists the groups whose list holds j.
+ * bwd_col    int32 [nnz]: group index g within (b,h), ascending.
+ * workspace  >= dsv_topk_workspace_bytes(s) bytes, 256-byte aligned
+ *            (a G x nb bitmask per (b,h) and per-block counts).
+ * ------------------------------------------------------------------------ */
+size_t dsv_topk_workspace_bytes(dsv_shape s);
+dsv_status dsv_topk_blocks(const float* scores, dsv_shape s, const int32_t* k_per_head,
+                           int32_t* fwd_ptr, int32_t* fwd_col, int32_t* bwd_ptr, int32_t* bwd_col,
+                           void* workspace, size_t workspace_bytes, dsv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * dsv_sparse_attn_fwd — block-sparse softmax attention forward
+ * ([nl] 2A stage 2: only the critical KV subset is computed; [hi] 2A)
+ *
+ * For query i in group g, over the keys of the blocks in g's list only:
+ *   s_ij = scale * q_i . k_j,  O_i = sum_j softmax(s_i)_j v_j,
+ *   lse_i = ln sum_j exp(s_ij)  (natural log).
+ * A group with an empty list gets O_i = 0 and lse_i = -inf.
+ *
+ * Q, K, V   bf16 [B,H,N,d], 16-byte aligned.
+ * fwd_ptr/fwd_col  the forward CSR (any valid lists, e.g. from dsv_topk_blocks).
+ * softmax_scale    <= 0 selects 1/sqrt(d).
+ * O         bf16 [B,H,N,d]; lse fp32 [B,H,N]; both overwritten.
+ * ------------------------------------------------------------------------ */
+dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const void* V, dsv_shape s,
+                               const int32_t* fwd_ptr, const int32_t* fwd_col, float softmax_scale,
+                               void* O, float* lse, dsv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * dsv_sparse_attn_bwd — gradient of dsv_sparse_attn_fwd over the same blocks
+ *
+ *   D_i = sum_c dO_ic O_ic;  P_ij = exp(s_ij - lse_i);  dP_ij = dO_i . v_j;
+ *   dS_ij = P_ij (dP_ij - D_i);  dV_j = sum_i P_ij dO_i;
+ *   dQ_i = scale sum_j dS_ij k_j;  dK_j = scale sum_i dS_ij q_i.
+ * Sums run over the selected (group, block) pairs only; key blocks that no
+ * group selected get dK = dV = 0.  dQ uses the forward lists, dK/dV the
+ * transposed lists; every output tile has exactly one writer (no atomics).
+ *
+ * Q, K, V, O, dO bf16 [B,H,N,d]; lse fp32 [B,H,N] from the forward.
+ * dQ, dK, dV bf16 [B,H,N,d]; overwritten.
+ * workspace >= dsv_attn_bwd_workspace_bytes(s) bytes, 256-byte aligned (holds D).
+ * ------------------------------------------------------------------------ */
+size_t dsv_attn_bwd_workspace_bytes(dsv_shape s);
+dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, const void* O,
+                               const void* dO, const float* lse, dsv_shape s,
+                               const int32_t* fwd_ptr, const int32_t* fwd_col,
+                               const int32_t* bwd_ptr, const int32_t* bwd_col, float softmax_scale,
+                               void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                               dsv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Status and device-side error reporting.
+ * ------------------------------------------------------------------------ */
+const char* dsv_status_string(dsv_status status);
+
+/* Synchronises `stream`, then returns the first device-side error recorded
+ * on the current device since the last clear (DSV_OK if none).  `info`, if
+ * not NULL, receives a kernel-specific detail word (which wait or index). */
+dsv_status dsv_get_device_error(dsv_stream_t stream, uint32_t* info);
+
+/* Resets the current device's error word (asynchronous on `stream`). */
+dsv_status dsv_clear_device_error(dsv_stream_t stream);
+
+/* Time limit, in nanoseconds, of every wait inside the kernels on the
+ * current device (default 1e9).  A wait past it records DSV_ERR_TIMEOUT and
+ * the kernel returns without finishing.  0 restores the default. */
+dsv_status dsv_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t dsv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSV_H_ */

@@ -1,0 +1,105 @@
+"""The C-ABI library: builds, loads, exports every declared symbol, and rejects
+bad arguments on the host before any launch (CPU only; no compute calls)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dynamic_block_sparse_projection_gb300.build import build
+    build()
+    from dynamic_block_sparse_projection_gb300 import binding
+    return binding
+
+
+def _declared():
+    text = (ROOT / "include" / "dsv.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsv_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 12
+    raw = ctypes.CDLL(str(lib._LIB_PATH))
+    for n in names:
+        assert hasattr(raw, n), n
+    assert set(names) == set(lib.EXPORTS)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.status_string(0) == "ok"
+    assert "argument" in lib.status_string(1)
+    assert lib.lib.dsv_version() >= 10000
+    assert lib.status_string(99) == "unknown status"
+
+
+def _shape(lib, B=1, H=2, N=512, d=128, block=128, r=16):
+    return lib.Shape(B, H, N, d, block, r)
+
+
+def test_workspace_queries(lib):
+    s = _shape(lib)
+    G = 4
+    assert lib.lib.dsv_predict_workspace_bytes(s) >= 2 * 1 * 2 * G * 16 * 4
+    assert lib.lib.dsv_topk_workspace_bytes(s) >= 2 * G * 4
+    assert lib.lib.dsv_attn_bwd_workspace_bytes(s) >= 1 * 2 * 512 * 4
+    assert lib.lib.dsv_topk_workspace_bytes(_shape(lib, d=96)) == 0     # unsupported -> 0
+    assert lib.lib.dsv_predict_workspace_bytes(_shape(lib, N=0)) == 0
+
+
+FAKE = 1 << 20          # an aligned, never dereferenced address
+
+
+def test_host_validation_predict(lib):
+    L = lib.lib
+    ws = L.dsv_predict_workspace_bytes(_shape(lib))
+    ok = (FAKE, FAKE, FAKE, FAKE)
+    assert L.dsv_predict_scores(*ok, _shape(lib, d=96), FAKE, FAKE, ws, None) == lib.DSV_ERR_UNSUPPORTED
+    assert L.dsv_predict_scores(*ok, _shape(lib, block=32), FAKE, FAKE, ws, None) == lib.DSV_ERR_UNSUPPORTED
+    assert L.dsv_predict_scores(*ok, _shape(lib, r=12), FAKE, FAKE, ws, None) == lib.DSV_ERR_UNSUPPORTED
+    assert L.dsv_predict_scores(*ok, _shape(lib, N=500), FAKE, FAKE, ws, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_predict_scores(*ok, _shape(lib, B=-1), FAKE, FAKE, ws, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_predict_scores(None, FAKE, FAKE, FAKE, _shape(lib), FAKE, FAKE, ws, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_predict_scores(FAKE + 8, FAKE, FAKE, FAKE, _shape(lib), FAKE, FAKE, ws, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_predict_scores(*ok, _shape(lib), FAKE, FAKE + 16, ws, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_predict_scores(*ok, _shape(lib), FAKE, FAKE, ws - 1, None) == lib.DSV_ERR_INVALID_ARG
+    # an empty problem is valid and launches nothing
+    assert L.dsv_predict_scores(None, None, None, None, _shape(lib, N=0), None, None, 0, None) == lib.DSV_OK
+
+
+def test_host_validation_topk(lib):
+    L = lib.lib
+    s = _shape(lib)
+    ws = L.dsv_topk_workspace_bytes(s)
+    k = (ctypes.c_int32 * 2)(2, 3)
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE, ws)
+    assert L.dsv_topk_blocks(FAKE, s, (ctypes.c_int32 * 2)(0, 3), FAKE, *args, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_topk_blocks(FAKE, s, (ctypes.c_int32 * 2)(2, 5), FAKE, *args, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_topk_blocks(FAKE, s, None, FAKE, *args, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_topk_blocks(FAKE, s, k, FAKE, FAKE, FAKE, FAKE, FAKE, ws - 4, None) == lib.DSV_ERR_INVALID_ARG
+    big = _shape(lib, N=128 * 8193, H=1)
+    assert L.dsv_topk_blocks(FAKE, big, k, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == lib.DSV_ERR_UNSUPPORTED
+    assert L.dsv_topk_blocks(FAKE, _shape(lib, H=1025), k, *((FAKE,) * 5), ws, None) == lib.DSV_ERR_UNSUPPORTED
+
+
+def test_host_validation_attention(lib):
+    L = lib.lib
+    s = _shape(lib)
+    assert L.dsv_sparse_attn_fwd(FAKE, FAKE, FAKE, s, FAKE, None, 0.0, FAKE, FAKE, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_sparse_attn_fwd(FAKE, FAKE, FAKE + 2, s, FAKE, FAKE, 0.0, FAKE, FAKE, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_sparse_attn_fwd(FAKE, FAKE, FAKE, _shape(lib, d=32), FAKE, FAKE, 0.0, FAKE, FAKE, None) == \
+        lib.DSV_ERR_UNSUPPORTED
+    ws = L.dsv_attn_bwd_workspace_bytes(s)
+    p = (FAKE,) * 6
+    assert L.dsv_sparse_attn_bwd(*p, s, FAKE, FAKE, FAKE, FAKE, 0.0, FAKE, FAKE, FAKE, FAKE, ws - 1, None) == \
+        lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_sparse_attn_bwd(*p, s, FAKE, FAKE, None, FAKE, 0.0, FAKE, FAKE, FAKE, FAKE, ws, None) == \
+        lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_sparse_attn_bwd(*p, s, FAKE, FAKE, FAKE, FAKE, 0.0, FAKE, FAKE, FAKE, FAKE + 64, ws, None) == \
+        lib.DSV_ERR_INVALID_ARG
