@@ -27,6 +27,24 @@ def rel_l2(x, y) -> float:
     return float(np.linalg.norm((x - y).ravel()) / (den if den > 0 else 1.0))
 
 
+def bf16_half_ulp(ref) -> np.ndarray:
+    """Half the spacing of the bf16 grid at each reference value (|x| >= 2^-126)."""
+    r = np.abs(np.asarray(ref, np.float64)).astype(np.float32)
+    return np.spacing(r).astype(np.float64) * 2.0 ** 15
+
+
+def max_abs_beyond_rounding(gpu, ref) -> float:
+    """max |gpu - ref| less the half-ulp that storing ref in bf16 alone can cost.
+
+    O is a bf16 output: above |O| = 4 half a bf16 ulp is already 0.0156, and
+    above 8 it exceeds the 2e-2 bar by itself, so the max-abs bar is applied
+    to the error beyond the output format's own rounding.
+    """
+    g = np.asarray(gpu, np.float64)
+    r = np.asarray(ref, np.float64)
+    return float(np.max(np.abs(g - r) - bf16_half_ulp(r))) if g.size else 0.0
+
+
 def score_err(gpu: np.ndarray, ref: np.ndarray) -> float:
     """max |gpu - ref| / max(|ref|, rms(ref row)) over all entries."""
     rms = np.sqrt(np.mean(ref ** 2, axis=-1, keepdims=True))

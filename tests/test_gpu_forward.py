@@ -4,8 +4,9 @@ Every comparison is against the fp64 oracle on the same seeded inputs:
   * predictor scores: |dS| <= 1e-4 * max(|S_ref|, row rms);
   * top-k lists: bit-exact against the oracle's top-k of the GPU's own scores
     (the selection is an integer decision taken on fp32 keys on both sides);
-  * attention forward: O rel-L2 <= 1e-2 and max-abs <= 2e-2 against the
-    oracle run on lists the oracle computed itself.
+  * attention forward: O rel-L2 <= 1e-2 and max-abs <= 2e-2 beyond the
+    bf16 output's own rounding (half a bf16 ulp of the oracle value), against
+    the oracle run on lists the oracle computed itself.
 """
 import numpy as np
 import pytest
@@ -13,8 +14,8 @@ import torch
 
 import oracle
 from dynamic_block_sparse_projection_gb300 import workloads as wl
-from parity_util import (LSE_MAX_ABS, O_MAX_ABS, O_REL_L2, SCORE_REL, SMALL, csr_to_device, oracle_lists,
-                         random_lists, rel_l2, score_err, to64)
+from parity_util import (LSE_MAX_ABS, O_MAX_ABS, O_REL_L2, SCORE_REL, SMALL, csr_to_device,
+                         max_abs_beyond_rounding, oracle_lists, random_lists, rel_l2, score_err, to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -66,7 +67,7 @@ def test_forward_matches_oracle(dsv, name):
     O_ref, L_ref = oracle.attn_fwd_groups(Q, K, V, rfp, rfc, w.block)
     O_gpu = to64(O)
     assert rel_l2(O_gpu, O_ref) <= O_REL_L2
-    assert np.max(np.abs(O_gpu - O_ref)) <= O_MAX_ABS
+    assert max_abs_beyond_rounding(O_gpu, O_ref) <= O_MAX_ABS
     assert np.max(np.abs(to64(lse) - L_ref)) <= LSE_MAX_ABS
 
 
@@ -85,7 +86,7 @@ def test_forward_all_tile_shapes(dsv, block, d, k):
     torch.cuda.synchronize()
     O_ref, L_ref = oracle.attn_fwd_groups(to64(Qb), to64(Kb), to64(Vb), fp_, fc_, block)
     assert rel_l2(to64(O), O_ref) <= O_REL_L2
-    assert np.max(np.abs(to64(O) - O_ref)) <= O_MAX_ABS
+    assert max_abs_beyond_rounding(to64(O), O_ref) <= O_MAX_ABS
     assert np.max(np.abs(to64(lse) - L_ref)) <= LSE_MAX_ABS
 
 
