@@ -26,6 +26,7 @@ EXPORTS = (
     "dsv_attn_bwd_workspace_bytes", "dsv_sparse_attn_bwd",
     "dsv_status_string", "dsv_get_device_error", "dsv_clear_device_error",
     "dsv_set_wait_limit_ns", "dsv_version",
+    "dsv_topk_blocks_noalloc",
 )
 
 
@@ -71,6 +72,8 @@ def _load() -> ctypes.CDLL:
     lib.dsv_clear_device_error.restype = ctypes.c_int
     lib.dsv_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.dsv_set_wait_limit_ns.restype = ctypes.c_int
+    lib.dsv_topk_blocks_noalloc.argtypes = [vp, Shape, ctypes.POINTER(i32), vp, vp, vp, vp, vp]
+    lib.dsv_topk_blocks_noalloc.restype = ctypes.c_int
     lib.dsv_version.argtypes = []
     lib.dsv_version.restype = i32
     return lib
@@ -181,6 +184,24 @@ def topk_blocks(scores, k_per_head: Sequence[int], block: int, N: int, d: int = 
                                _stream(dev, stream)), "dsv_topk_blocks")
     fp, fc, bp, bc = outs
     return fp, fc[:nnz], bp, bc[:nnz]
+
+
+def topk_blocks_noalloc(scores, k_per_head: Sequence[int], block: int, N: int, d: int = 128, *, outs,
+                        stream=None) -> None:
+    """dsv_topk_blocks_noalloc into caller-provided `outs`; it allocates nothing.
+
+    For callers that cannot allocate device memory: the library's fixed
+    device scratch replaces the workspace.  Calls share that scratch, so do
+    not let two of them overlap on the GPU.
+    """
+    _need(scores, "scores", torch.float32)
+    dev = scores.device
+    B, H, G, nb = scores.shape
+    for name, t in zip(("fwd_ptr", "fwd_col", "bwd_ptr", "bwd_col"), outs):
+        _need(t, name, torch.int32, dev)
+    karr = (ctypes.c_int32 * max(H, 1))(*[int(k) for k in k_per_head])
+    _check(lib.dsv_topk_blocks_noalloc(_ptr(scores), Shape(B, H, N, d, block, 8), karr, *[_ptr(t) for t in outs],
+                                       _stream(dev, stream)), "dsv_topk_blocks_noalloc")
 
 
 def sparse_attn_fwd(Q, K, V, fwd_ptr, fwd_col, block: int, softmax_scale: float = 0.0, *, out=None, lse=None,

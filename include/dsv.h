@@ -104,6 +104,27 @@ dsv_status dsv_topk_blocks(const float* scores, dsv_shape s, const int32_t* k_pe
                            void* workspace, size_t workspace_bytes, dsv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * dsv_topk_blocks_noalloc — dsv_topk_blocks for callers that cannot allocate
+ * (the DSV pages have no counterpart: this is a deployment convenience)
+ *
+ * Same arguments, lists and results as dsv_topk_blocks, minus the workspace.
+ * For callers that must not call cudaMalloc or any allocating routine (for
+ * example while another thread captures a CUDA graph, inside a plug-in whose
+ * host framework owns the device heap, or in a loop where an allocation may
+ * block): the scratch comes from a fixed device array inside libdsv of
+ * DSV_TOPK_NOALLOC_SCRATCH_BYTES, held on every GPU that loads the library
+ * until the process exits.  Problems whose dsv_topk_workspace_bytes() exceed
+ * it return DSV_ERR_UNSUPPORTED before any launch.  The first call on a
+ * device looks up the array's device address (make it before any stream
+ * capture).  All calls share the array, so calls that overlap on the GPU race;
+ * serialise them (one stream, or events).
+ * ------------------------------------------------------------------------ */
+#define DSV_TOPK_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+dsv_status dsv_topk_blocks_noalloc(const float* scores, dsv_shape s, const int32_t* k_per_head,
+                                   int32_t* fwd_ptr, int32_t* fwd_col, int32_t* bwd_ptr, int32_t* bwd_col,
+                                   dsv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * dsv_sparse_attn_fwd — block-sparse softmax attention forward
  * ([nl] 2A stage 2: only the critical KV subset is computed; [hi] 2A)
  *
