@@ -12,30 +12,47 @@
 //   kv kernel  one CTA per key block (b, h, j), looping over the ascending
 //              transposed list of groups g that selected j:
 //                S^T = K_j Q_g^T, dP^T = V_j dO_g^T       (tcgen05, smem x smem)
-//                P^T, dS^T -> TMEM (bf16) by the compute warpgroup
+//                P^T, dS^T -> TMEM (bf16) by the compute warps
 //                dV += P^T dO_g, dK += dS^T Q_g           (tcgen05, TMEM x smem)
 //   q kernel   one CTA per group (b, h, g), looping over its forward list:
 //                S = Q_g K_j^T, dP = dO_g V_j^T; dS -> TMEM; dQ += dS K_j
 // The price of no atomics is recomputing S and dP in both kernels (7 MMAs
-// per pair instead of 5).  Warp roles and TMEM use mirror the forward kernel:
-// warp 0 TMA, warp 1 MMA issue, warps 2..5 one tile row per thread.
+// per pair instead of 5).
+//
+// Warp roles: warp 0 TMA producer (one lane), warp 1 TMEM allocator and MMA
+// issuer (the whole warp; one elected lane issues), warps 2..9 compute; the q
+// kernel adds warp 10 as the producer of its V ring.  A TMEM lane (tile row)
+// belongs to the sub-partition warp % 4, so two compute warps share each row
+// quarter and split its columns: two warps per SM sub-partition hide the
+// latency of the TMEM loads and the exponentials.
 #include <math.h>
 
 #include "dsv_launch.h"
 
 namespace dsv {
 
+#ifdef DSV_TRACE
+static __device__ int g_trace_cta;
+static __device__ unsigned long long g_trace_kv[96 * 16];
+static __device__ unsigned long long g_trace_q[96 * 16];
+#endif
+
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kThreads = 320;          // 2 control warps + 8 compute warps
+constexpr int kQVWarp = 10;            // q kernel: V producer warp
+constexpr int kQThreads = 352;         // q kernel: 3 control warps + 8 compute warps
+constexpr int kComputeThreads = 256;
 
 // ---------------------------------------------------------------------------
-// D_i = sum_c dO_ic * O_ic
+// Pre-pass: D_i = sum_c dO_ic O_ic and lse_i * log2(e) for the main kernels.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ O,
                                                          const __nv_bfloat16* __restrict__ dO,
-                                                         float* __restrict__ Dw, long long rows) {
+                                                         const float* __restrict__ lse, float* __restrict__ Dw,
+                                                         float* __restrict__ L2w, long long rows) {
   constexpr int TPR = D / 8;             // threads per row, 16 bytes each
   constexpr int RPC = 256 / TPR;         // rows per CTA
   const long long row = (long long)blockIdx.x * RPC + threadIdx.x / TPR;
@@ -53,10 +70,16 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __nv_bfloat16* __
   }
 #pragma unroll
   for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (row < rows && c == 0) Dw[row] = acc;
+  if (row < rows && c == 0) {
+    Dw[row] = acc;
+    L2w[row] = lse[row] * kLog2e;
+  }
 }
 
-enum : unsigned int { W_KV = 1, W_GFULL, W_GEMPTY, W_S, W_P, W_ACC, W_DRAIN, W_KFULL, W_VFULL, W_KVEMPTY };
+enum : unsigned int {
+  W_KV = 1, W_GFULL, W_GEMPTY, W_S, W_P, W_ACC, W_DRAIN, W_KFULL, W_VFULL, W_KVEMPTY, W_LD, W_SPFREE, W_DSFULL,
+  W_DSEMPTY
+};
 
 // ---------------------------------------------------------------------------
 // dK, dV: one CTA per key block
@@ -70,40 +93,51 @@ struct KVTraits {
   static constexpr int B_CHUNK = BETA * 128;       // Q_g / dO_g tiles
   static constexpr int B_BYTES = NCH * B_CHUNK;
   static constexpr int NST = 2;
-  static constexpr int VEC_BYTES = BETA * 4;       // lse_g or D_g
+  static constexpr int VEC_BYTES = BETA * 4;       // lse2_g or D_g
   static constexpr int STAGE_BYTES = (2 * B_BYTES + 2 * VEC_BYTES + 1023) / 1024 * 1024;  // keeps tiles 1024-aligned
-  static constexpr int NBAR = 1 + 2 * NST + 3;
+  static constexpr int NBAR = 1 + 2 * NST + 5;
   static constexpr int SMEM_USED = 1024 + 2 * A_BYTES + NST * STAGE_BYTES + NBAR * 8 + 16;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
-  static constexpr uint32_t ST_COL = 0, DPT_COL = 128, DV_COL = 256, DK_COL = 256 + D;
+  // Each pair (j, g) is processed as two halves of the query group, so the
+  // compute warps work on one half while the tensor core runs the other:
+  // half h owns columns [h*BETA, h*BETA + HALF) for S^T_h and the next HALF
+  // for dP^T_h; P^T_h / dS^T_h (bf16) are written back over them.
+  static constexpr int HALF = BETA / 2;            // queries per half
+  static constexpr int W = HALF / 2;               // columns of a half per compute warp
+  static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
+  __host__ __device__ static constexpr uint32_t st_col(int h) { return (uint32_t)(h * BETA); }
+  __host__ __device__ static constexpr uint32_t dpt_col(int h) { return (uint32_t)(h * BETA + HALF); }
 };
 
 template <int BETA, int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const float* __restrict__ lse, const float* __restrict__ Dw,
+                       const float* __restrict__ L2w, const float* __restrict__ Dw,
                        const int32_t* __restrict__ bwd_ptr, const int32_t* __restrict__ bwd_col, int N, int G,
                        float scale, __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, Ctl ctl) {
   using T = KVTraits<BETA, D>;
   constexpr int NST = T::NST;
+  constexpr int HALF = T::HALF;
+  constexpr int W = T::W;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = align_up_ptr<uint8_t>(smem_raw, 1024);
   uint8_t* sK = sbase;
   uint8_t* sV = sK + T::A_BYTES;
-  uint8_t* sStage = sV + T::A_BYTES;              // NST x [Q_g | dO_g | lse | D]
+  uint8_t* sStage = sV + T::A_BYTES;              // NST x [Q_g | dO_g | lse2 | D]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + NST * T::STAGE_BYTES);
   uint64_t* kv_full = bars;
   uint64_t* g_full = bars + 1;
   uint64_t* g_empty = g_full + NST;
-  uint64_t* s_full = g_empty + NST;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* acc_done = p_full + 1;
+  uint64_t* s_full = g_empty + NST;               // [2] S^T_h, dP^T_h in TMEM
+  uint64_t* p_full = s_full + 2;                  // [2] P^T_h, dS^T_h in TMEM
+  uint64_t* acc_done = p_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  DSV_TRACE_INIT;
   const long long row = blockIdx.x;               // (b*H + h)*nb + j
   const int nb = G;
   const long long bh = row / nb;
@@ -118,8 +152,10 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&g_full[s], 1);
       mbar_init(&g_empty[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&s_full[h], 1);
+      mbar_init(&p_full[h], kComputeThreads);
+    }
     mbar_init(acc_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -161,10 +197,12 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_2d(sV + c * T::A_CHUNK, &tmV, kv_full, c * 64, (int)krow0);
       }
       int issued = 0;
+      int gn = bwd_col[start];
       for (int n = 0; n < cnt; ++n) {
         const int s = n % NST;
         const uint32_t ph = (uint32_t)(n / NST) & 1u;
-        int g = bwd_col[start + n];
+        int g = gn;
+        if (n + 1 < cnt) gn = bwd_col[start + n + 1];
         if (!mbar_wait(&g_empty[s], ph ^ 1u, abort_flag, ctl, kid | W_GEMPTY)) break;
         if ((unsigned)g >= (unsigned)G) {
           set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
@@ -177,7 +215,7 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_2d(st + c * T::B_CHUNK, &tmQ, &g_full[s], c * 64, (int)qrow);
           tma_load_2d(st + T::B_BYTES + c * T::B_CHUNK, &tmdO, &g_full[s], c * 64, (int)qrow);
         }
-        bulk_load(st + 2 * T::B_BYTES, lse + qrow, T::VEC_BYTES, &g_full[s]);
+        bulk_load(st + 2 * T::B_BYTES, L2w + qrow, T::VEC_BYTES, &g_full[s]);
         bulk_load(st + 2 * T::B_BYTES + T::VEC_BYTES, Dw + qrow, T::VEC_BYTES, &g_full[s]);
         issued = n + 1;
       }
@@ -186,87 +224,140 @@ __global__ void __launch_bounds__(192, 1)
         mbar_wait(&g_full[n % NST], (uint32_t)(n / NST) & 1u, nullptr, ctl, kid | W_DRAIN);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      constexpr uint32_t ID_S = idesc_bf16_f32(T::BM, BETA, false, false);   // S^T, dP^T: N = queries
-      constexpr uint32_t ID_G = idesc_bf16_f32(T::BM, D, false, true);       // dV, dK: B MN-major
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aS = smem_u32(sStage);
-      bool ok = mbar_wait(kv_full, 0, abort_flag, ctl, kid | W_KV);
-      for (int n = 0; ok && n < cnt; ++n) {
+    {
+      // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+      // Order per pair n: S/dP(n, 1), dV/dK(n, 0), S/dP(n+1, 0), dV/dK(n, 1).
+      // Each S/dP half is issued once the compute warps have released that
+      // TMEM buffer (p_full of the previous use, awaited before its dV/dK).
+      constexpr uint32_t ID_S = idesc_bf16_f32(T::BM, HALF, false, false);  // S^T_h, dP^T_h: N = HALF queries
+      constexpr uint32_t ID_G = idesc_bf16_f32(T::BM, D, false, true);      // dV, dK: B MN-major
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t dS0 = sdesc_sw128(smem_u32(sStage), 16, 1024);           // K-major view of a stage
+      const uint64_t dSmn0 = sdesc_sw128(smem_u32(sStage), T::B_CHUNK, 1024);  // MN-major view
+      auto issue_sdp = [&](int n, int h) {
         const int s = n % NST;
-        if (!mbar_wait(&g_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_GFULL)) break;
-        tc_fence_after();
-        const uint32_t aQg = aS + s * T::STAGE_BYTES, adOg = aQg + T::B_BYTES;
+        const uint64_t qg = desc_off(dS0, (uint32_t)(s * T::STAGE_BYTES + h * HALF * 128));
+        const uint64_t dog = desc_off(qg, T::B_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ao = (kk >> 2) * T::A_CHUNK + (kk & 3) * 32;
           const uint32_t bo = (kk >> 2) * T::B_CHUNK + (kk & 3) * 32;
-          mma_ss(tmem + T::ST_COL, sdesc_sw128(aK + ao, 16, 1024), sdesc_sw128(aQg + bo, 16, 1024), ID_S,
-                 kk > 0 ? 1u : 0u);
+          mma_ss_w(tmem + T::st_col(h), desc_off(dK0, ao), desc_off(qg, bo), ID_S, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ao = (kk >> 2) * T::A_CHUNK + (kk & 3) * 32;
           const uint32_t bo = (kk >> 2) * T::B_CHUNK + (kk & 3) * 32;
-          mma_ss(tmem + T::DPT_COL, sdesc_sw128(aV + ao, 16, 1024), sdesc_sw128(adOg + bo, 16, 1024), ID_S,
-                 kk > 0 ? 1u : 0u);
+          mma_ss_w(tmem + T::dpt_col(h), desc_off(dV0, ao), desc_off(dog, bo), ID_S, kk > 0 ? 1u : 0u);
         }
-        mma_commit(s_full);
-        if (!mbar_wait(p_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_P)) break;
-        tc_fence_after();
+        mma_commit_w(&s_full[h]);
+      };
+      // dV += P^T_h dO_g[half h], dK += dS^T_h Q_g[half h].  Compute warp hf
+      // of a half packed its W queries into the first W/2 of its own W columns.
+      auto issue_grad = [&](int n, int h) {
+        const int s = n % NST;
+        const uint64_t qmn = desc_off(dSmn0, (uint32_t)(s * T::STAGE_BYTES + h * HALF * 128));
+        const uint64_t domn = desc_off(qmn, T::B_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BETA / 16; ++kk) {
-          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + T::DV_COL, tmem + T::ST_COL + kk * 8,
-                 sdesc_sw128(adOg + kk * 16 * 128, T::B_CHUNK, 1024), ID_G, acc);
-          mma_ts(tmem + T::DK_COL, tmem + T::DPT_COL + kk * 8,
-                 sdesc_sw128(aQg + kk * 16 * 128, T::B_CHUNK, 1024), ID_G, acc);
+        for (int kk = 0; kk < HALF / 16; ++kk) {
+          const uint32_t acc = (n > 0 || h > 0 || kk > 0) ? 1u : 0u;
+          const uint32_t pc = (uint32_t)(((kk * 16) / W) * W + ((kk * 16) % W) / 2);
+          mma_ts_w(tmem + T::DV_COL, tmem + T::st_col(h) + pc, desc_off(domn, kk * 16 * 128), ID_G, acc);
         }
-        mma_commit(&g_empty[s]);
+#pragma unroll
+        for (int kk = 0; kk < HALF / 16; ++kk) {
+          const uint32_t acc = (n > 0 || h > 0 || kk > 0) ? 1u : 0u;
+          const uint32_t pc = (uint32_t)(((kk * 16) / W) * W + ((kk * 16) % W) / 2);
+          mma_ts_w(tmem + T::DK_COL, tmem + T::dpt_col(h) + pc, desc_off(qmn, kk * 16 * 128), ID_G, acc);
+        }
+      };
+      bool ok = mbar_wait_warp(kv_full, 0, abort_flag, ctl, kid | W_KV) &&
+                mbar_wait_warp(&g_full[0], 0, abort_flag, ctl, kid | W_GFULL);
+      if (ok) {
+        tc_fence_after();
+        issue_sdp(0, 0);
       }
-      mma_commit(acc_done);
-      mbar_wait(acc_done, 0, nullptr, ctl, kid | W_DRAIN);
+      for (int n = 0; ok && n < cnt; ++n) {
+        DSV_TRACE_POINT(g_trace_kv, n, 0);
+        issue_sdp(n, 1);
+        DSV_TRACE_POINT(g_trace_kv, n, 1);
+        if (!mbar_wait_warp(&p_full[0], (uint32_t)n & 1u, abort_flag, ctl, kid | W_P)) break;
+        DSV_TRACE_POINT(g_trace_kv, n, 2);
+        tc_fence_after();
+        issue_grad(n, 0);
+        if (n + 1 < cnt) {
+          const int s1 = (n + 1) % NST;
+          if (!mbar_wait_warp(&g_full[s1], (uint32_t)((n + 1) / NST) & 1u, abort_flag, ctl, kid | W_GFULL)) break;
+          tc_fence_after();
+          issue_sdp(n + 1, 0);
+        }
+        if (!mbar_wait_warp(&p_full[1], (uint32_t)n & 1u, abort_flag, ctl, kid | W_P)) break;
+        tc_fence_after();
+        issue_grad(n, 1);
+        mma_commit_w(&g_empty[n % NST]);
+        DSV_TRACE_POINT(g_trace_kv, n, 3);
+      }
+      mma_commit_w(acc_done);
+      mbar_wait_warp(acc_done, 0, nullptr, ctl, kid | W_DRAIN);
     }
   } else {
-    // ---------------- compute warpgroup: one key row per thread ----------------
+    // ------------- compute warps: key row kr, W queries of each half -------------
     const int sp = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int kr = sp * 32 + lane;
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     const float scale_log2 = scale * kLog2e;
     bool ok = true;
-    for (int n = 0; n < cnt; ++n) {
+    for (int n = 0; ok && n < cnt; ++n) {
       const int s = n % NST;
-      if (!mbar_wait_warp(&g_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_GFULL) ||
-          !mbar_wait_warp(s_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_S)) {
+      if (!mbar_wait_warp(&g_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_GFULL)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      const float* lse_s = reinterpret_cast<const float*>(sStage + s * T::STAGE_BYTES + 2 * T::B_BYTES);
-      const float* dd_s = lse_s + BETA;
-#pragma unroll
-      for (int c = 0; c < BETA / 32; ++c) {
-        uint32_t xs[32], xp[32];
-        tmem_ld32(tmem + lane_off + T::ST_COL + c * 32, xs);
-        tmem_ld32(tmem + lane_off + T::DPT_COL + c * 32, xp);
-        tmem_ld_wait();
-        uint32_t pw[16], dw[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int q0 = c * 32 + 2 * i;
-          const float p0 = ex2(fmaf(__uint_as_float(xs[2 * i]), scale_log2, -lse_s[q0] * kLog2e));
-          const float p1 = ex2(fmaf(__uint_as_float(xs[2 * i + 1]), scale_log2, -lse_s[q0 + 1] * kLog2e));
-          const float d0 = p0 * (__uint_as_float(xp[2 * i]) - dd_s[q0]);
-          const float d1 = p1 * (__uint_as_float(xp[2 * i + 1]) - dd_s[q0 + 1]);
-          pw[i] = pack_bf16x2(p0, p1);
-          dw[i] = pack_bf16x2(d0, d1);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (!mbar_wait_warp(&s_full[h], (uint32_t)n & 1u, abort_flag, ctl, kid | W_S)) {
+          ok = false;
+          break;
         }
-        tmem_st16(tmem + lane_off + T::ST_COL + c * 16, pw);
-        tmem_st16(tmem + lane_off + T::DPT_COL + c * 16, dw);
+        if (warp == 2 && lane == 0 && h == 0) DSV_TRACE_POINT(g_trace_kv, n, 4);
+        tc_fence_after();
+        const uint32_t cs = tmem + lane_off + T::st_col(h) + hf * W;
+        const uint32_t cp = tmem + lane_off + T::dpt_col(h) + hf * W;
+        uint32_t xs[W], xp[W];
+        tmem_ld_w<W>(cs, xs);
+        tmem_ld_w<W>(cp, xp);
+        const int q0 = h * HALF + hf * W;            // first query of this warp's columns
+        const float4* l4 = reinterpret_cast<const float4*>(sStage + s * T::STAGE_BYTES + 2 * T::B_BYTES) + q0 / 4;
+        const float4* d4 = l4 + BETA / 4;
+        tmem_ld_wait();
+        if (warp == 2 && lane == 0 && h == 0) DSV_TRACE_POINT(g_trace_kv, n, 5);
+        uint32_t pw[W / 2], dw[W / 2];
+#pragma unroll
+        for (int q = 0; q < W / 4; ++q) {
+          const float4 L = l4[q], Dd = d4[q];
+          const float Lv[4] = {L.x, L.y, L.z, L.w}, Dv[4] = {Dd.x, Dd.y, Dd.z, Dd.w};
+          float p[4], ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            p[e] = ex2(fmaf(__uint_as_float(xs[4 * q + e]), scale_log2, -Lv[e]));
+            ds[e] = p[e] * (__uint_as_float(xp[4 * q + e]) - Dv[e]);
+          }
+          pw[2 * q] = pack_bf16x2(p[0], p[1]);
+          pw[2 * q + 1] = pack_bf16x2(p[2], p[3]);
+          dw[2 * q] = pack_bf16x2(ds[0], ds[1]);
+          dw[2 * q + 1] = pack_bf16x2(ds[2], ds[3]);
+        }
+        if (warp == 2 && lane == 0 && h == 0) DSV_TRACE_POINT(g_trace_kv, n, 6);
+        // each warp overwrites only the TMEM lanes and columns it has just read
+        tmem_st_w<W / 2>(cs, pw);
+        tmem_st_w<W / 2>(cp, dw);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[h]);
+        if (warp == 2 && lane == 0 && h == 0) DSV_TRACE_POINT(g_trace_kv, n, 7);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_full);
     }
     if (ok) ok = mbar_wait_warp(acc_done, 0, abort_flag, ctl, kid | W_ACC);
     if (ok) {
@@ -274,11 +365,11 @@ __global__ void __launch_bounds__(192, 1)
       const long long orow = krow0 + kr;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        const uint32_t col = t == 0 ? T::DV_COL : T::DK_COL;
+        const uint32_t col = (t == 0 ? T::DV_COL : T::DK_COL) + hf * (D / 2);
         const float mul = t == 0 ? 1.0f : scale;
-        __nv_bfloat16* outp = t == 0 ? dV : dK;
+        __nv_bfloat16* outp = (t == 0 ? dV : dK) + orow * D + hf * (D / 2);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t o[32];
           tmem_ld32(tmem + lane_off + col + c * 32, o);
           tmem_ld_wait();
@@ -287,7 +378,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i)
               w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * mul, __uint_as_float(o[2 * i + 1]) * mul);
-            uint4* dst = reinterpret_cast<uint4*>(outp + orow * D + c * 32);
+            uint4* dst = reinterpret_cast<uint4*>(outp + c * 32);
 #pragma unroll
             for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
           }
@@ -313,42 +404,51 @@ struct QTraits {
   static constexpr int A_BYTES = NCH * A_CHUNK;
   static constexpr int KV_CHUNK = BETA * 128;
   static constexpr int KV_BYTES = NCH * KV_CHUNK;
-  static constexpr int NST = (2 * A_BYTES + 6 * KV_BYTES + 2048 <= 227 * 1024) ? 3 : 2;
-  static constexpr int NBAR = 1 + 3 * NST + 3;
-  static constexpr int SMEM_USED = 1024 + 2 * A_BYTES + 2 * NST * KV_BYTES + NBAR * 8 + 16;
+  // K_j is read by S (early) and by dQ (late); V_j only by dP: separate rings,
+  // each slot released as soon as its last product is done.
+  static constexpr int NK = 3, NV = 2;
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 4 + 1;
+  static constexpr int SMEM_USED = 1024 + 2 * A_BYTES + (NK + NV) * KV_BYTES + NBAR * 8 + 16;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
-  static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256;
+  // S and dP (fp32), dQ (fp32), then two bf16 dS buffers of BETA/2 columns
+  static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256, DS_COL = 384, DS_STRIDE = 64;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TX_BYTES = BETA * D * 2;
+  static constexpr int HALF = BETA / 2;
 };
 
 template <int BETA, int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kQThreads, 1)
     attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                      const float* __restrict__ lse, const float* __restrict__ Dw,
+                      const float* __restrict__ L2w, const float* __restrict__ Dw,
                       const int32_t* __restrict__ fwd_ptr, const int32_t* __restrict__ fwd_col, int N, int G,
                       float scale, __nv_bfloat16* __restrict__ dQ, Ctl ctl) {
   using T = QTraits<BETA, D>;
-  constexpr int NST = T::NST;
+  constexpr int NK = T::NK, NV = T::NV;
+  constexpr int HALF = T::HALF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = align_up_ptr<uint8_t>(smem_raw, 1024);
   uint8_t* sQ = sbase;
   uint8_t* sdO = sQ + T::A_BYTES;
   uint8_t* sK = sdO + T::A_BYTES;
-  uint8_t* sV = sK + NST * T::KV_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NST * T::KV_BYTES);
+  uint8_t* sV = sK + NK * T::KV_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NV * T::KV_BYTES);
   uint64_t* qd_full = bars;
   uint64_t* k_full = bars + 1;
-  uint64_t* v_full = k_full + NST;
-  uint64_t* kv_empty = v_full + NST;
-  uint64_t* s_full = kv_empty + NST;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* acc_done = p_full + 1;
+  uint64_t* k_empty = k_full + NK;
+  uint64_t* v_full = k_empty + NK;
+  uint64_t* v_empty = v_full + NV;
+  uint64_t* s_full = v_empty + NV;
+  uint64_t* sp_free = s_full + 1;                 // compute threads have read S, dP
+  uint64_t* ds_full = sp_free + 1;                // [2]
+  uint64_t* ds_empty = ds_full + 2;               // [2]
+  uint64_t* acc_done = ds_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  DSV_TRACE_INIT;
   const long long row = blockIdx.x;               // (b*H + h)*G + g
   const long long bh = row / G;
   const int g = (int)(row - bh * G);
@@ -360,13 +460,20 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(qd_full, 1);
-    for (int s = 0; s < NST; ++s) {
+    for (int s = 0; s < NK; ++s) {
       mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < NV; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    mbar_init(sp_free, kComputeThreads);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ds_full[b], kComputeThreads);
+      mbar_init(&ds_empty[b], 1);
+    }
     mbar_init(acc_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -392,93 +499,118 @@ __global__ void __launch_bounds__(192, 1)
     if (cnt < 0 && threadIdx.x == 0) set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
     for (int i = threadIdx.x; i < BETA * D / 8; i += blockDim.x)
       reinterpret_cast<uint4*>(dQ + qrow0 * D)[i] = make_uint4(0, 0, 0, 0);
-  } else if (warp == 0) {
+  } else if (warp == 0 || warp == kQVWarp) {
+    // TMA producers, one per warp: warp 0 loads Q_g, dO_g and the K ring,
+    // warp 10 the V ring
     if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(qd_full, 2 * T::TX_BYTES);
-      for (int c = 0; c < T::NCH; ++c) {
-        tma_load_2d(sQ + c * T::A_CHUNK, &tmQ, qd_full, c * 64, (int)qrow0);
-        tma_load_2d(sdO + c * T::A_CHUNK, &tmdO, qd_full, c * 64, (int)qrow0);
+      const bool is_k = warp == 0;
+      const CUtensorMap* map = is_k ? &tmK : &tmV;
+      const int nst = is_k ? NK : NV;
+      uint8_t* ring = is_k ? sK : sV;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      tma_prefetch_desc(map);
+      if (is_k) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmdO);
+        mbar_arrive_expect_tx(qd_full, 2 * T::TX_BYTES);
+        for (int c = 0; c < T::NCH; ++c) {
+          tma_load_2d(sQ + c * T::A_CHUNK, &tmQ, qd_full, c * 64, (int)qrow0);
+          tma_load_2d(sdO + c * T::A_CHUNK, &tmdO, qd_full, c * 64, (int)qrow0);
+        }
       }
       int issued = 0;
       int jn = fwd_col[start];
       for (int n = 0; n < cnt; ++n) {
-        const int s = n % NST;
-        const uint32_t ph = (uint32_t)(n / NST) & 1u;
+        const int s = n % nst;
+        const uint32_t ph = (uint32_t)(n / nst) & 1u;
         int j = jn;
         if (n + 1 < cnt) jn = fwd_col[start + n + 1];
-        if (!mbar_wait(&kv_empty[s], ph ^ 1u, abort_flag, ctl, kid | W_KVEMPTY)) break;
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, ctl, kid | W_KVEMPTY)) break;
         if ((unsigned)j >= (unsigned)nb) {
-          set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
+          if (is_k) set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
           j = 0;
         }
         const int krow = (int)(bh * N + (long long)j * BETA);
-        mbar_arrive_expect_tx(&k_full[s], T::TX_BYTES);
+        mbar_arrive_expect_tx(&full[s], T::TX_BYTES);
         for (int c = 0; c < T::NCH; ++c)
-          tma_load_2d(sK + s * T::KV_BYTES + c * T::KV_CHUNK, &tmK, &k_full[s], c * 64, krow);
-        mbar_arrive_expect_tx(&v_full[s], T::TX_BYTES);
-        for (int c = 0; c < T::NCH; ++c)
-          tma_load_2d(sV + s * T::KV_BYTES + c * T::KV_CHUNK, &tmV, &v_full[s], c * 64, krow);
+          tma_load_2d(ring + s * T::KV_BYTES + c * T::KV_CHUNK, map, &full[s], c * 64, krow);
         issued = n + 1;
       }
-      mbar_wait(qd_full, 0, nullptr, ctl, kid | W_DRAIN);
-      for (int n = (issued > NST ? issued - NST : 0); n < issued; ++n) {
-        const uint32_t ph = (uint32_t)(n / NST) & 1u;
-        mbar_wait(&k_full[n % NST], ph, nullptr, ctl, kid | W_DRAIN);
-        mbar_wait(&v_full[n % NST], ph, nullptr, ctl, kid | W_DRAIN);
-      }
+      if (is_k) mbar_wait(qd_full, 0, nullptr, ctl, kid | W_DRAIN);
+      for (int n = (issued > nst ? issued - nst : 0); n < issued; ++n)
+        mbar_wait(&full[n % nst], (uint32_t)(n / nst) & 1u, nullptr, ctl, kid | W_DRAIN);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {
+      // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
       constexpr uint32_t ID_S = idesc_bf16_f32(T::BM, BETA, false, false);
       constexpr uint32_t ID_Q = idesc_bf16_f32(T::BM, D, false, true);
-      const uint32_t aQ = smem_u32(sQ), adO = smem_u32(sdO), aK = smem_u32(sK), aV = smem_u32(sV);
-      bool ok = mbar_wait(qd_full, 0, abort_flag, ctl, kid | W_KV);
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t ddO0 = sdesc_sw128(smem_u32(sdO), 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t dKmn0 = sdesc_sw128(smem_u32(sK), T::KV_CHUNK, 1024);
+      auto issue_sdp = [&](int n) -> bool {
+        const int sk = n % NK, sv = n % NV;
+        if (!mbar_wait_warp(&k_full[sk], (uint32_t)(n / NK) & 1u, abort_flag, ctl, kid | W_KFULL)) return false;
+        tc_fence_after();
+        const uint64_t kb = desc_off(dK0, (uint32_t)sk * T::KV_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ao = (kk >> 2) * T::A_CHUNK + (kk & 3) * 32;
+          const uint32_t bo = (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32;
+          mma_ss_w(tmem + T::S_COL, desc_off(dQ0, ao), desc_off(kb, bo), ID_S, kk > 0 ? 1u : 0u);
+        }
+        if (!mbar_wait_warp(&v_full[sv], (uint32_t)(n / NV) & 1u, abort_flag, ctl, kid | W_VFULL)) return false;
+        tc_fence_after();
+        const uint64_t vb = desc_off(dV0, (uint32_t)sv * T::KV_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ao = (kk >> 2) * T::A_CHUNK + (kk & 3) * 32;
+          const uint32_t bo = (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32;
+          mma_ss_w(tmem + T::DP_COL, desc_off(ddO0, ao), desc_off(vb, bo), ID_S, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_w(s_full);
+        mma_commit_w(&v_empty[sv]);   // V_j is only needed by dP
+        return true;
+      };
+      bool ok = mbar_wait_warp(qd_full, 0, abort_flag, ctl, kid | W_KV);
+      if (ok) ok = issue_sdp(0);
       for (int n = 0; ok && n < cnt; ++n) {
-        const int s = n % NST;
-        const uint32_t ph = (uint32_t)(n / NST) & 1u;
-        if (!mbar_wait(&k_full[s], ph, abort_flag, ctl, kid | W_KFULL)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ao = (kk >> 2) * T::A_CHUNK + (kk & 3) * 32;
-          const uint32_t bo = s * T::KV_BYTES + (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32;
-          mma_ss(tmem + T::S_COL, sdesc_sw128(aQ + ao, 16, 1024), sdesc_sw128(aK + bo, 16, 1024), ID_S,
-                 kk > 0 ? 1u : 0u);
+        DSV_TRACE_POINT(g_trace_q, n, 0);
+        if (n + 1 < cnt) {
+          // S and dP are single-buffered: overwrite them once the compute warps hold block n
+          if (!mbar_wait_warp(sp_free, (uint32_t)n & 1u, abort_flag, ctl, kid | W_SPFREE)) break;
+          tc_fence_after();
+          if (!issue_sdp(n + 1)) break;
         }
-        if (!mbar_wait(&v_full[s], ph, abort_flag, ctl, kid | W_VFULL)) break;
+        DSV_TRACE_POINT(g_trace_q, n, 1);
+        if (!mbar_wait_warp(&ds_full[n & 1], (uint32_t)(n >> 1) & 1u, abort_flag, ctl, kid | W_DSFULL)) break;
+        DSV_TRACE_POINT(g_trace_q, n, 2);
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ao = (kk >> 2) * T::A_CHUNK + (kk & 3) * 32;
-          const uint32_t bo = s * T::KV_BYTES + (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32;
-          mma_ss(tmem + T::DP_COL, sdesc_sw128(adO + ao, 16, 1024), sdesc_sw128(aV + bo, 16, 1024), ID_S,
-                 kk > 0 ? 1u : 0u);
-        }
-        mma_commit(s_full);
-        if (!mbar_wait(p_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_P)) break;
-        tc_fence_after();
+        const int s = n % NK;
+        const uint64_t kmn = desc_off(dKmn0, (uint32_t)s * T::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BETA / 16; ++kk) {
-          mma_ts(tmem + T::DQ_COL, tmem + T::S_COL + kk * 8,
-                 sdesc_sw128(aK + s * T::KV_BYTES + kk * 16 * 128, T::KV_CHUNK, 1024), ID_Q,
-                 (n > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_w(tmem + T::DQ_COL, tmem + T::DS_COL + (uint32_t)(n & 1) * T::DS_STRIDE + kk * 8,
+                 desc_off(kmn, kk * 16 * 128), ID_Q, (n > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&kv_empty[s]);
+        mma_commit_w(&k_empty[s]);
+        mma_commit_w(&ds_empty[n & 1]);
+        DSV_TRACE_POINT(g_trace_q, n, 3);
       }
-      mma_commit(acc_done);
-      mbar_wait(acc_done, 0, nullptr, ctl, kid | W_DRAIN);
+      mma_commit_w(acc_done);
+      mbar_wait_warp(acc_done, 0, nullptr, ctl, kid | W_DRAIN);
     }
-  } else {
-    // ---------------- compute warpgroup: one query row per thread ----------------
+  } else if (warp < kQVWarp) {
+    // ------------- compute warps: query row r, key half hf -------------
     const int sp = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int r = sp * 32 + lane;
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     const float scale_log2 = scale * kLog2e;
-    const float lse2 = (r < BETA) ? lse[qrow0 + r] * kLog2e : 0.f;
+    const float lse2 = (r < BETA) ? L2w[qrow0 + r] : 0.f;
     const float dd = (r < BETA) ? Dw[qrow0 + r] : 0.f;
     bool ok = true;
     for (int n = 0; n < cnt; ++n) {
@@ -486,41 +618,55 @@ __global__ void __launch_bounds__(192, 1)
         ok = false;
         break;
       }
+      if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 4);
+      tc_fence_after();
+      uint32_t xs[HALF], xp[HALF];
+#pragma unroll
+      for (int c = 0; c < HALF / 32; ++c) {
+        tmem_ld32(tmem + lane_off + T::S_COL + hf * HALF + c * 32, xs + c * 32);
+        tmem_ld32(tmem + lane_off + T::DP_COL + hf * HALF + c * 32, xp + c * 32);
+      }
+      tmem_ld_wait();
+      if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 5);
+      tc_fence_before();
+      mbar_arrive(sp_free);
+      uint32_t dw[HALF / 2];
+#pragma unroll
+      for (int i = 0; i < HALF / 2; ++i) {
+        const float p0 = ex2(fmaf(__uint_as_float(xs[2 * i]), scale_log2, -lse2));
+        const float p1 = ex2(fmaf(__uint_as_float(xs[2 * i + 1]), scale_log2, -lse2));
+        dw[i] = pack_bf16x2(p0 * (__uint_as_float(xp[2 * i]) - dd), p1 * (__uint_as_float(xp[2 * i + 1]) - dd));
+      }
+      if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 6);
+      if (!mbar_wait_warp(&ds_empty[n & 1], ((uint32_t)(n >> 1) & 1u) ^ 1u, abort_flag, ctl, kid | W_DSEMPTY)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < BETA / 32; ++c) {
-        uint32_t xs[32], xp[32];
-        tmem_ld32(tmem + lane_off + T::S_COL + c * 32, xs);
-        tmem_ld32(tmem + lane_off + T::DP_COL + c * 32, xp);
-        tmem_ld_wait();
-        uint32_t dw[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(__uint_as_float(xs[2 * i]), scale_log2, -lse2));
-          const float p1 = ex2(fmaf(__uint_as_float(xs[2 * i + 1]), scale_log2, -lse2));
-          dw[i] = pack_bf16x2(p0 * (__uint_as_float(xp[2 * i]) - dd), p1 * (__uint_as_float(xp[2 * i + 1]) - dd));
-        }
-        tmem_st16(tmem + lane_off + T::S_COL + c * 16, dw);
-      }
+      for (int c = 0; c < HALF / 32; ++c)
+        tmem_st16(tmem + lane_off + T::DS_COL + (uint32_t)(n & 1) * T::DS_STRIDE + hf * (HALF / 2) + c * 16,
+                  dw + c * 16);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&ds_full[n & 1]);
+      if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 7);
     }
     if (ok) ok = mbar_wait_warp(acc_done, 0, abort_flag, ctl, kid | W_ACC);
     if (ok) {
       tc_fence_after();
       const long long orow = qrow0 + r;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + T::DQ_COL + c * 32, o);
+        tmem_ld32(tmem + lane_off + T::DQ_COL + hf * (D / 2) + c * 32, o);
         tmem_ld_wait();
         if (r < BETA) {
           uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * scale, __uint_as_float(o[2 * i + 1]) * scale);
-          uint4* dst = reinterpret_cast<uint4*>(dQ + orow * D + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(dQ + orow * D + hf * (D / 2) + c * 32);
 #pragma unroll
           for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
         }
@@ -544,31 +690,34 @@ cudaError_t launch_bwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
   const long long rows = (long long)s.B * s.H * s.N;
   const long long groups = (long long)s.B * s.H * G;
   float* Dw = static_cast<float*>(ws);
+  float* L2w = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)rows * sizeof(float)));
   constexpr int RPC = 256 / (D / 8);
   bwd_rowdot_kernel<D><<<(unsigned)((rows + RPC - 1) / RPC), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), Dw, rows);
+      static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse, Dw, L2w, rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   auto kv = attn_bwd_kv_kernel<BETA, D>;
   if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KVTraits<BETA, D>::SMEM)) !=
       cudaSuccess)
     return e;
-  kv<<<(unsigned)groups, 192, KVTraits<BETA, D>::SMEM, st>>>(tmQ, tmK, tmV, tmdO, lse, Dw, bwd_ptr, bwd_col, s.N, G,
-                                                              scale, static_cast<__nv_bfloat16*>(dK),
-                                                              static_cast<__nv_bfloat16*>(dV), ctl);
+  kv<<<(unsigned)groups, kThreads, KVTraits<BETA, D>::SMEM, st>>>(tmQ, tmK, tmV, tmdO, L2w, Dw, bwd_ptr, bwd_col,
+                                                                   s.N, G, scale, static_cast<__nv_bfloat16*>(dK),
+                                                                   static_cast<__nv_bfloat16*>(dV), ctl);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto qk = attn_bwd_q_kernel<BETA, D>;
   if ((e = cudaFuncSetAttribute(qk, cudaFuncAttributeMaxDynamicSharedMemorySize, QTraits<BETA, D>::SMEM)) !=
       cudaSuccess)
     return e;
-  qk<<<(unsigned)groups, 192, QTraits<BETA, D>::SMEM, st>>>(tmQ, tmK, tmV, tmdO, lse, Dw, fwd_ptr, fwd_col, s.N, G,
-                                                            scale, static_cast<__nv_bfloat16*>(dQ), ctl);
+  qk<<<(unsigned)groups, kQThreads, QTraits<BETA, D>::SMEM, st>>>(tmQ, tmK, tmV, tmdO, L2w, Dw, fwd_ptr, fwd_col,
+                                                                 s.N, G, scale, static_cast<__nv_bfloat16*>(dQ), ctl);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t attn_bwd_ws_bytes(const dsv_shape& s) { return align256((size_t)s.B * s.H * s.N * sizeof(float)); }
+size_t attn_bwd_ws_bytes(const dsv_shape& s) {
+  return 2 * align256((size_t)s.B * s.H * s.N * sizeof(float));  // D and lse*log2(e)
+}
 
 cudaError_t launch_attn_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             const CUtensorMap& tmdO, const void* O, const void* dO, const float* lse,
@@ -586,3 +735,16 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
 }
 
 }  // namespace dsv
+
+#ifdef DSV_TRACE
+extern "C" int dsv_trace_bwd(int which, int cta, unsigned long long* host) {
+  if (host == nullptr) {
+    static const unsigned long long zero[96 * 16] = {};
+    cudaMemcpyToSymbol(dsv::g_trace_kv, zero, sizeof(zero));
+    cudaMemcpyToSymbol(dsv::g_trace_q, zero, sizeof(zero));
+    return (int)cudaMemcpyToSymbol(dsv::g_trace_cta, &cta, sizeof(int));
+  }
+  return which == 0 ? (int)cudaMemcpyFromSymbol(host, dsv::g_trace_kv, sizeof(dsv::g_trace_kv))
+                    : (int)cudaMemcpyFromSymbol(host, dsv::g_trace_q, sizeof(dsv::g_trace_q));
+}
+#endif

@@ -13,11 +13,13 @@
 // with an online (running-max) softmax; O is only rescaled when the running
 // max grows by more than 2^8 (values of P then stay below 256).
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, then K_j / V_j into an NST-deep ring.
-//   warp 1      TMEM allocator; lane 0 issues every MMA and commit.
+// Warp roles (224 threads):
+//   warp 0      TMA producer of Q and the K_j ring (one lane).
+//   warp 1      TMEM allocator and MMA issuer (the whole warp, one elected
+//               lane issues each MMA and commit).
 //   warps 2..5  softmax / epilogue; warp w owns TMEM lanes 32*(w%4)..+31,
 //               i.e. one query row per thread.
+//   warp 6      TMA producer of the V_j ring (one lane).
 // TMEM columns: S/P buffer 0 at [0,128), buffer 1 at [128,256), O at [256,256+d).
 // S is double-buffered so the MMA of block n+1 overlaps the softmax of block n.
 #include <math.h>
@@ -25,6 +27,11 @@
 #include "dsv_launch.h"
 
 namespace dsv {
+
+#ifdef DSV_TRACE
+static __device__ int g_trace_cta;
+static __device__ unsigned long long g_trace_fwd[96 * 16];
+#endif
 
 namespace {
 
@@ -37,7 +44,7 @@ struct FwdTraits {
   static constexpr int Q_BYTES = NCH * Q_CHUNK;
   static constexpr int KV_BYTES = NCH * KV_CHUNK;
   static constexpr int NST = (Q_BYTES + 6 * KV_BYTES + 2048 <= 227 * 1024) ? 3 : 2;
-  static constexpr int NBAR = 1 + 3 * NST + 2 + 2 + 2 + 1;
+  static constexpr int NBAR = 1 + 4 * NST + 2 + 2 + 2 + 1;
   static constexpr int SMEM_USED = 1024 + Q_BYTES + 2 * NST * KV_BYTES + NBAR * 8 + 16;
   // at least 120 KB so that one CTA owns an SM (and its 512 TMEM columns)
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
@@ -47,10 +54,13 @@ struct FwdTraits {
   static constexpr uint32_t TX_BYTES = BETA * D * 2;   // one K or V tile (and the Q tile)
 };
 
+constexpr int kVWarp = 6;                // V producer warp
+constexpr int kFwdThreads = 224;         // 7 warps
+
 enum : unsigned int { W_Q = 1, W_KEMPTY, W_K, W_P, W_V, W_S, W_O, W_OFINAL, W_DRAIN };
 
 template <int BETA, int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ fwd_ptr,
                     const int32_t* __restrict__ fwd_col, int N, int G, int nb, float scale_log2,
@@ -66,8 +76,9 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
   uint64_t* v_full = k_full + NST;
-  uint64_t* kv_empty = v_full + NST;
-  uint64_t* s_full = kv_empty + NST;
+  uint64_t* k_empty = v_full + NST;                // K slot free: its S product is done
+  uint64_t* v_empty = k_empty + NST;               // V slot free: its PV product is done
+  uint64_t* s_full = v_empty + NST;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;   // [2]: PV of block n arrives on o_done[n & 1]
   uint64_t* o_final = o_done + 2;
@@ -75,6 +86,7 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  DSV_TRACE_INIT;
   const long long row = blockIdx.x;  // (b*H + h)*G + g
   const long long bh = row / G;
   const int g = (int)(row - bh * G);
@@ -87,7 +99,8 @@ __global__ void __launch_bounds__(192, 1)
     for (int s = 0; s < NST; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
@@ -122,15 +135,25 @@ __global__ void __launch_bounds__(192, 1)
       reinterpret_cast<uint4*>(O + (bh * N + (long long)g * BETA) * D)[i] = make_uint4(0, 0, 0, 0);
     }
     for (int i = threadIdx.x; i < BETA; i += blockDim.x) LSE[bh * N + (long long)g * BETA + i] = -INFINITY;
-  } else if (warp == 0) {
+  } else if (warp == 0 || warp == kVWarp) {
+    // ---------------- TMA producers: warp 0 loads Q and the K ring, warp 6 the V ring ----------------
+    // K is consumed by S = Q K^T one block before V is consumed by O += P V, and each
+    // slot is released as soon as its own product is done, so K runs further ahead.
+    // One producer per warp: lanes of one warp spinning on different barriers
+    // would serialise each other.
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      const int qrow = (int)(bh * N + (long long)g * BETA);
-      mbar_arrive_expect_tx(q_full, T::TX_BYTES);
-      for (int c = 0; c < T::NCH; ++c) tma_load_2d(sQ + c * T::Q_CHUNK, &tmQ, q_full, c * 64, qrow);
+      const bool is_k = warp == 0;
+      const CUtensorMap* map = is_k ? &tmK : &tmV;
+      uint8_t* ring = is_k ? sK : sV;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      tma_prefetch_desc(map);
+      if (is_k) {
+        tma_prefetch_desc(&tmQ);
+        const int qrow = (int)(bh * N + (long long)g * BETA);
+        mbar_arrive_expect_tx(q_full, T::TX_BYTES);
+        for (int c = 0; c < T::NCH; ++c) tma_load_2d(sQ + c * T::Q_CHUNK, &tmQ, q_full, c * 64, qrow);
+      }
       int issued = 0;
       int jn = fwd_col[start];
       for (int n = 0; n < cnt; ++n) {
@@ -138,70 +161,74 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t ph = (uint32_t)(n / NST) & 1u;
         int j = jn;
         if (n + 1 < cnt) jn = fwd_col[start + n + 1];
-        if (!mbar_wait(&kv_empty[s], ph ^ 1u, abort_flag, ctl, kid | W_KEMPTY)) break;
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, ctl, kid | W_KEMPTY)) break;
         if ((unsigned)j >= (unsigned)nb) {
-          set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
+          if (is_k) set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
           j = 0;
         }
         const int krow = (int)(bh * N + (long long)j * BETA);
-        mbar_arrive_expect_tx(&k_full[s], T::TX_BYTES);
+        mbar_arrive_expect_tx(&full[s], T::TX_BYTES);
         for (int c = 0; c < T::NCH; ++c)
-          tma_load_2d(sK + s * T::KV_BYTES + c * T::KV_CHUNK, &tmK, &k_full[s], c * 64, krow);
-        mbar_arrive_expect_tx(&v_full[s], T::TX_BYTES);
-        for (int c = 0; c < T::NCH; ++c)
-          tma_load_2d(sV + s * T::KV_BYTES + c * T::KV_CHUNK, &tmV, &v_full[s], c * 64, krow);
+          tma_load_2d(ring + s * T::KV_BYTES + c * T::KV_CHUNK, map, &full[s], c * 64, krow);
         issued = n + 1;
       }
       // every copy this thread started must land before the CTA exits
-      mbar_wait(q_full, 0, nullptr, ctl, kid | W_DRAIN);
-      for (int n = (issued > NST ? issued - NST : 0); n < issued; ++n) {
-        const uint32_t ph = (uint32_t)(n / NST) & 1u;
-        mbar_wait(&k_full[n % NST], ph, nullptr, ctl, kid | W_DRAIN);
-        mbar_wait(&v_full[n % NST], ph, nullptr, ctl, kid | W_DRAIN);
-      }
+      if (is_k) mbar_wait(q_full, 0, nullptr, ctl, kid | W_DRAIN);
+      for (int n = (issued > NST ? issued - NST : 0); n < issued; ++n)
+        mbar_wait(&full[n % NST], (uint32_t)(n / NST) & 1u, nullptr, ctl, kid | W_DRAIN);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+    {
+      // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
       constexpr uint32_t IDS = idesc_bf16_f32(T::BM, BETA, false, false);
       constexpr uint32_t IDO = idesc_bf16_f32(T::BM, D, false, true);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-      bool ok = mbar_wait(q_full, 0, abort_flag, ctl, kid | W_Q);
+      // base descriptors; every MMA adds a compile-time offset
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(sV), T::KV_CHUNK, 1024);
+      bool ok = mbar_wait_warp(q_full, 0, abort_flag, ctl, kid | W_Q);
       auto issue_S = [&](int n) -> bool {
         const int s = n % NST;
-        if (!mbar_wait(&k_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_K)) return false;
+        DSV_TRACE_POINT(g_trace_fwd, n, 0);
+        if (!mbar_wait_warp(&k_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_K)) return false;
+        DSV_TRACE_POINT(g_trace_fwd, n, 1);
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(n & 1) * T::S_COL;
+        const uint64_t kb = desc_off(dK0, (uint32_t)s * T::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(aQ + (kk >> 2) * T::Q_CHUNK + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(aK + s * T::KV_BYTES + (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32, 16, 1024);
-          mma_ss(d_tmem, a, b, IDS, kk > 0 ? 1u : 0u);
+          mma_ss_w(d_tmem, desc_off(dQ0, (kk >> 2) * T::Q_CHUNK + (kk & 3) * 32),
+                 desc_off(kb, (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32), IDS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[n & 1]);
+        mma_commit_w(&s_full[n & 1]);
+        mma_commit_w(&k_empty[s]);
+        DSV_TRACE_POINT(g_trace_fwd, n, 2);
         return true;
       };
       if (ok) ok = issue_S(0);
       for (int n = 0; ok && n < cnt; ++n) {
         if (n + 1 < cnt && !issue_S(n + 1)) break;
-        if (!mbar_wait(&p_full[n & 1], (uint32_t)(n >> 1) & 1u, abort_flag, ctl, kid | W_P)) break;
+        if (!mbar_wait_warp(&p_full[n & 1], (uint32_t)(n >> 1) & 1u, abort_flag, ctl, kid | W_P)) break;
+        DSV_TRACE_POINT(g_trace_fwd, n, 3);
         const int s = n % NST;
-        if (!mbar_wait(&v_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_V)) break;
+        if (!mbar_wait_warp(&v_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_V)) break;
+        DSV_TRACE_POINT(g_trace_fwd, n, 4);
         tc_fence_after();
         const uint32_t p_tmem = tmem + (uint32_t)(n & 1) * T::S_COL;
+        const uint64_t vb = desc_off(dV0, (uint32_t)s * T::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BETA / 16; ++kk) {
-          const uint64_t b = sdesc_sw128(aV + s * T::KV_BYTES + kk * 16 * 128, T::KV_CHUNK, 1024);
-          mma_ts(tmem + T::O_COL, p_tmem + kk * 8, b, IDO, (n > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_w(tmem + T::O_COL, p_tmem + kk * 8, desc_off(vb, kk * 16 * 128), IDO, (n > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&kv_empty[s]);
-        mma_commit(&o_done[n & 1]);
+        mma_commit_w(&v_empty[s]);
+        mma_commit_w(&o_done[n & 1]);
+        DSV_TRACE_POINT(g_trace_fwd, n, 5);
       }
-      mma_commit(o_final);
+      mma_commit_w(o_final);
       // TMEM is freed after the closing CTA-wide sync only once every MMA is done
-      mbar_wait(o_final, 0, nullptr, ctl, kid | W_DRAIN);
+      mbar_wait_warp(o_final, 0, nullptr, ctl, kid | W_DRAIN);
     }
-  } else {
+  } else if (warp < kVWarp) {
     // ---------------- softmax warpgroup (warps 2..5) ----------------
     const int sp = warp & 3;
     const int r = sp * 32 + lane;
@@ -213,15 +240,24 @@ __global__ void __launch_bounds__(192, 1)
         ok = false;
         break;
       }
+      if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 8);
       tc_fence_after();
       const uint32_t sb = tmem + lane_off + (uint32_t)(n & 1) * T::S_COL;
       uint32_t xr[BETA];
 #pragma unroll
       for (int c = 0; c < BETA / 32; ++c) tmem_ld32(sb + c * 32, xr + c * 32);
       tmem_ld_wait();
-      float mx = __uint_as_float(xr[0]);
+      if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 9);
+      // row max as 8 independent partial maxima (short dependency chains)
+      float mx8[8];
 #pragma unroll
-      for (int j = 1; j < BETA; ++j) mx = fmaxf(mx, __uint_as_float(xr[j]));
+      for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(xr[i]);
+#pragma unroll
+      for (int j = 8; j < BETA; j += 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], __uint_as_float(xr[j + i]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m, mx * scale_log2);
       if (n == 0) {
         m = m_new;
@@ -247,21 +283,23 @@ __global__ void __launch_bounds__(192, 1)
         tmem_st_wait();
       }
       const float neg_m = -m;
-      float rs = 0.f;
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pk[BETA / 2];
 #pragma unroll
       for (int j = 0; j < BETA / 2; ++j) {
         const float p0 = ex2(fmaf(__uint_as_float(xr[2 * j]), scale_log2, neg_m));
         const float p1 = ex2(fmaf(__uint_as_float(xr[2 * j + 1]), scale_log2, neg_m));
-        rs += p0 + p1;
+        rs8[j & 7] += p0 + p1;
         pk[j] = pack_bf16x2(p0, p1);
       }
-      l += rs;
+      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 10);
 #pragma unroll
       for (int c = 0; c < BETA / 32; ++c) tmem_st16(sb + c * 16, pk + c * 16);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[n & 1]);
+      if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 11);
     }
     if (ok) ok = mbar_wait_warp(o_final, 0, abort_flag, ctl, kid | W_OFINAL);
     if (ok) {
@@ -304,7 +342,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
   const int G = s.N / s.block;
   const long long rows = (long long)s.B * s.H * G;
   const float scale_log2 = scale * 1.4426950408889634f;
-  kern<<<(unsigned)rows, 192, T::SMEM, st>>>(tmQ, tmK, tmV, fwd_ptr, fwd_col, s.N, G, G, scale_log2,
+  kern<<<(unsigned)rows, kFwdThreads, T::SMEM, st>>>(tmQ, tmK, tmV, fwd_ptr, fwd_col, s.N, G, G, scale_log2,
                                              static_cast<__nv_bfloat16*>(O), lse, ctl);
   return cudaGetLastError();
 }
@@ -324,3 +362,14 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
 }
 
 }  // namespace dsv
+
+#ifdef DSV_TRACE
+extern "C" int dsv_trace_fwd(int cta, unsigned long long* host) {
+  if (host == nullptr) {
+    static const unsigned long long zero[96 * 16] = {};
+    cudaMemcpyToSymbol(dsv::g_trace_fwd, zero, sizeof(zero));
+    return (int)cudaMemcpyToSymbol(dsv::g_trace_cta, &cta, sizeof(int));
+  }
+  return (int)cudaMemcpyFromSymbol(host, dsv::g_trace_fwd, sizeof(dsv::g_trace_fwd));
+}
+#endif

@@ -173,6 +173,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
   return d;
 }
 
+// Descriptor of the same matrix `byte_off` bytes further on.  The start
+// address field holds (address >> 4) in 14 bits and shared-memory addresses
+// stay below 2^18, so adding to the low bits never carries into LBO.  Used to
+// keep the single MMA-issuing thread at a few instructions per MMA: the
+// issue rate of tcgen05.mma from one thread is bounded by the scalar work
+// between MMAs, not by the tensor core, when descriptors are rebuilt per MMA.
+__device__ __forceinline__ uint64_t desc_off(uint64_t d, uint32_t byte_off) { return d + (uint64_t)(byte_off >> 4); }
+
 // D[tmem] (+)= A[smem] * B[smem]  (both operands via descriptors)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
@@ -199,6 +207,41 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// Warp-wide forms of the three calls above: the whole warp runs the issuing
+// code with converged control flow and elect.sync picks the one lane that
+// issues, so descriptors and TMEM addresses are computed warp-uniformly.
+// Measured on GB300: a converged warp issues one tcgen05.mma every ~35-48
+// clocks, under the 64 clocks an M=128, N=128, K=16 MMA takes, while a single
+// lane in a divergent branch needs ~100 clocks per MMA and starves the tensor
+// core.  Every lane of the warp must call these together.
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
 // TMEM -> registers: 32 lanes x 32 consecutive 32-bit columns (one row per thread).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
   asm volatile(
@@ -210,6 +253,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
+}
+// TMEM -> registers: 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+// registers -> TMEM: 32 lanes x 8 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
 }
 // registers -> TMEM: 32 lanes x 16 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
@@ -231,6 +289,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+// W consecutive columns (W = 16 or 32) into / out of registers.
+template <int W>
+__device__ __forceinline__ void tmem_ld_w(uint32_t taddr, uint32_t* r) {
+  static_assert(W == 16 || W == 32, "tmem_ld_w: W must be 16 or 32");
+  if constexpr (W == 32) tmem_ld32(taddr, r); else tmem_ld16(taddr, r);
+}
+template <int W>
+__device__ __forceinline__ void tmem_st_w(uint32_t taddr, const uint32_t* r) {
+  static_assert(W == 8 || W == 16 || W == 32, "tmem_st_w: W must be 8, 16 or 32");
+  if constexpr (W == 32) tmem_st32(taddr, r); else if constexpr (W == 16) tmem_st16(taddr, r); else tmem_st8(taddr, r);
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -254,6 +323,25 @@ __device__ __forceinline__ T* align_up_ptr(void* p, uintptr_t a) {
   uintptr_t v = reinterpret_cast<uintptr_t>(p);
   return reinterpret_cast<T*>((v + a - 1) & ~(a - 1));
 }
+
+// Optional timeline instrumentation, compiled only with -DDSV_TRACE (never in
+// the library build): DSV_TRACE_POINT(buf, step, k) stamps clock64() into
+// buf[step * 16 + k] for the one CTA selected by the translation unit's
+// g_trace_cta (read once by DSV_TRACE_INIT), for the first 96 steps.
+#ifdef DSV_TRACE
+#define DSV_TRACE_INIT const bool dsv_traced = (blockIdx.x == (unsigned)g_trace_cta)
+#define DSV_TRACE_POINT(buf, step, k)                                     \
+  do {                                                                    \
+    if (dsv_traced && (step) < 96) (buf)[(step) * 16 + (k)] = clock64(); \
+  } while (0)
+#else
+#define DSV_TRACE_INIT \
+  do {                 \
+  } while (0)
+#define DSV_TRACE_POINT(buf, step, k) \
+  do {                                \
+  } while (0)
+#endif
 
 // Where a wait gave up (detail word of DSV_ERR_TIMEOUT): kernel id << 8 | wait id.
 enum : unsigned int {

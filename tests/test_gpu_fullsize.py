@@ -1,0 +1,133 @@
+"""GPU parity at the full workload sizes, on sampled outputs (needs a GB300).
+
+The whole hot path runs at the benchmark's sizes and launch configuration;
+the fp64 oracle then checks what it can evaluate one item at a time:
+
+  scores    rows S[b,h,g,:] of sampled groups against the oracle's per-row form
+  lists     sampled forward rows bit-exact against the oracle's top-k fed the
+            GPU's own fp32 scores of that row; for sampled heads the whole
+            transposed CSR equal to the oracle's transpose of the GPU lists
+  forward   O and lse of sampled groups against the per-group oracle
+  backward  dQ of sampled groups and dK/dV of sampled key blocks (the most
+            selected block of the head, a random one and the least selected)
+            against the per-group / per-block oracle forms, on the GPU lists
+
+The oracle sees one (b, h) slice at a time, as fp32 copies of the bf16 inputs
+(exact), with the CSR rows of that slice re-based to (0, 0).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dynamic_block_sparse_projection_gb300 import workloads as wl
+from parity_util import (GRAD_REL_L2, LSE_MAX_ABS, O_MAX_ABS, O_REL_L2, SCORE_REL, max_abs_beyond_rounding,
+                         rel_l2, score_err)
+
+pytestmark = pytest.mark.gpu
+
+FULL = ["latent123k_global", "stress61k", "long518k"]
+MAX_GROUPS = 48
+
+
+@pytest.fixture(scope="module")
+def dsv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dynamic_block_sparse_projection_gb300 import binding
+    return binding
+
+
+def _head_csr(ptr, col, bh, G):
+    """CSR rows of one (b, h) slice, re-based so that the slice is (0, 0)."""
+    p = ptr[bh * G:(bh + 1) * G + 1]
+    return p - p[0], col[p[0]:p[-1]]
+
+
+def _f32(t):
+    return t.detach().float().cpu().numpy()[None, None]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_parity(dsv, name):
+    w = wl.WORKLOADS[name]
+    G = w.nb
+    x = wl.make_inputs(w, device="cuda")
+    S = dsv.predict_scores(x.Q, x.K, x.Wq, x.Wk, w.block)
+    fp, fc, bp, bc = dsv.topk_blocks(S, x.k_per_head, w.block, w.N, w.d)
+    O, lse = dsv.sparse_attn_fwd(x.Q, x.K, x.V, fp, fc, w.block)
+    dQ, dK, dV = dsv.sparse_attn_bwd(x.Q, x.K, x.V, O, x.dO, lse, fp, fc, bp, bc, w.block)
+    torch.cuda.synchronize()
+    assert dsv.device_error()[0] == 0
+    assert int(fp[-1]) == sum(x.k_per_head[h] for h in range(w.H)) * w.B * G
+
+    fpn, fcn = fp.cpu().numpy().astype(np.int64), fc.cpu().numpy().astype(np.int64)
+    bpn, bcn = bp.cpu().numpy().astype(np.int64), bc.cpu().numpy().astype(np.int64)
+    rng = np.random.default_rng(97 + w.seed)
+    heads = sorted({(0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))})
+    for (b, h) in heads:
+        bh = b * w.H + h
+        Qh, Kh, Vh, dOh = (_f32(t[b, h]) for t in (x.Q, x.K, x.V, x.dO))
+        Wq, Wk = x.Wq[h:h + 1].double().cpu().numpy(), x.Wk[h:h + 1].double().cpu().numpy()
+        groups = sorted({0, G - 1, int(rng.integers(G))})
+        hp, hc = _head_csr(fpn, fcn, bh, G)
+
+        # scores: sampled rows
+        ref = oracle.predict_scores_rows(Qh, Kh, Wq, Wk, w.block, [(0, 0, g) for g in groups])
+        got = S[b, h, groups].double().cpu().numpy()
+        assert score_err(got, ref) <= SCORE_REL, f"scores {name} head {(b, h)}"
+
+        # forward lists: the oracle's top-k on the GPU's scores of the same rows
+        k = int(x.k_per_head[h])
+        rows_gpu = S[b, h].double().cpu().numpy()
+        for g in list(groups) + [int(v) for v in rng.integers(G, size=16)]:
+            assert np.array_equal(hc[hp[g]:hp[g + 1]], oracle.topk_row(rows_gpu[g], k)), (name, b, h, g)
+
+        # transposed CSR of the head: the oracle's transpose of the GPU lists
+        tp, tc = oracle.transpose_lists(hp, hc, 1, 1, G, G)
+        gp, gc = _head_csr(bpn, bcn, bh, G)
+        assert np.array_equal(tp, gp) and np.array_equal(tc, gc), f"transposed lists {name} head {(b, h)}"
+
+        # forward: sampled groups
+        for g, (o_ref, l_ref) in zip(groups, oracle.attn_fwd_groups(Qh, Kh, Vh, hp, hc, w.block,
+                                                                     rows=[(0, 0, g) for g in groups])):
+            sl = slice(g * w.block, (g + 1) * w.block)
+            o = O[b, h, sl].double().cpu().numpy()
+            assert rel_l2(o, o_ref) <= O_REL_L2
+            assert max_abs_beyond_rounding(o, o_ref) <= O_MAX_ABS
+            assert np.max(np.abs(lse[b, h, sl].double().cpu().numpy() - l_ref)) <= LSE_MAX_ABS
+
+        # backward: dQ of sampled groups
+        for g, dq_ref in zip(groups, oracle.attn_bwd_dq_rows(Qh, Kh, Vh, dOh, hp, hc, w.block,
+                                                              [(0, 0, g) for g in groups])):
+            sl = slice(g * w.block, (g + 1) * w.block)
+            assert rel_l2(dQ[b, h, sl].double().cpu().numpy(), dq_ref) <= GRAD_REL_L2, f"dQ {name} {(b, h, g)}"
+
+        # backward: dK, dV of sampled key blocks.  The per-block oracle redoes
+        # the whole softmax of every group in the block's list, so only blocks
+        # with at most MAX_GROUPS groups are sampled (the least selected, the
+        # most selected among those, a random one); the gradient sums below
+        # cover every block.
+        lens = np.diff(gp)
+        cheap = np.nonzero((lens > 0) & (lens <= MAX_GROUPS))[0]
+        blocks = {int(np.argmin(lens))}
+        if cheap.size:
+            blocks |= {int(cheap[np.argmax(lens[cheap])]), int(rng.choice(cheap))}
+        blocks = sorted(blocks)
+        for j, (dk_ref, dv_ref) in zip(blocks, oracle.attn_bwd_kv_blocks(Qh, Kh, Vh, dOh, hp, hc, gp, gc, w.block,
+                                                                          [(0, 0, j) for j in blocks])):
+            sl = slice(j * w.block, (j + 1) * w.block)
+            dk = dK[b, h, sl].double().cpu().numpy()
+            dv = dV[b, h, sl].double().cpu().numpy()
+            if lens[j] == 0:
+                assert np.all(dk == 0) and np.all(dv == 0)
+            else:
+                assert rel_l2(dk, dk_ref) <= GRAD_REL_L2, f"dK {name} {(b, h, j)}"
+                assert rel_l2(dv, dv_ref) <= GRAD_REL_L2, f"dV {name} {(b, h, j)}"
+
+        # gradient sums over every key of the head: each query's softmax row sums
+        # to one, so sum_keys dV = sum_queries dO and sum_keys dK = 0 (every
+        # query group has a non-empty list here)
+        dKs = dK[b, h].double().sum(dim=0)
+        assert torch.all(dKs.abs() <= 2e-2 * dK[b, h].double().abs().sum(dim=0) + 1e-3)
+        assert rel_l2(dV[b, h].double().sum(dim=0).cpu().numpy(), x.dO[b, h].double().sum(dim=0).cpu().numpy()) <= 1e-2
