@@ -400,18 +400,21 @@ template <int BETA, int D>
 struct QTraits {
   static constexpr int BM = 128;
   static constexpr int NCH = D / 64;
-  static constexpr int A_CHUNK = BM * 128;         // Q_g / dO_g as A operands (padded rows)
+  static constexpr int A_CHUNK = BM * 128;         // dO_g as the A operand of dP (padded rows)
   static constexpr int A_BYTES = NCH * A_CHUNK;
   static constexpr int KV_CHUNK = BETA * 128;
   static constexpr int KV_BYTES = NCH * KV_CHUNK;
   // K_j is read by S (early) and by dQ (late); V_j only by dP: separate rings,
   // each slot released as soon as its last product is done.
-  static constexpr int NK = 3, NV = 2;
-  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 4 + 1;
-  static constexpr int SMEM_USED = 1024 + 2 * A_BYTES + (NK + NV) * KV_BYTES + NBAR * 8 + 16;
+  static constexpr int NK = 3;
+  static constexpr int NV = (A_BYTES + 6 * KV_BYTES + 2048 <= 227 * 1024) ? 3 : 2;
+  static constexpr int NBAR = 2 + 2 * NK + 2 * NV + 2 + 2 + 1;
+  static constexpr int SMEM_USED = 1024 + A_BYTES + (NK + NV) * KV_BYTES + NBAR * 8 + 16;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
-  // S and dP (fp32), dQ (fp32), then two bf16 dS buffers of BETA/2 columns
-  static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256, DS_COL = 384, DS_STRIDE = 64;
+  // TMEM: S and dP (fp32), dQ (fp32), dS (bf16 pairs, BETA/2 columns), and Q_g
+  // (bf16 pairs, D/2 columns) as the A operand of S, read in once per CTA: an
+  // M=128 MMA with both operands in shared memory takes all of its bandwidth.
+  static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256, DS_COL = 256 + D, Q_COL = 256 + D + 64;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TX_BYTES = BETA * D * 2;
   static constexpr int HALF = BETA / 2;
@@ -419,7 +422,7 @@ struct QTraits {
 
 template <int BETA, int D>
 __global__ void __launch_bounds__(kQThreads, 1)
-    attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    attn_bwd_q_kernel(const __nv_bfloat16* __restrict__ Qg, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                       const float* __restrict__ L2w, const float* __restrict__ Dw,
                       const int32_t* __restrict__ fwd_ptr, const int32_t* __restrict__ fwd_col, int N, int G,
@@ -429,21 +432,21 @@ __global__ void __launch_bounds__(kQThreads, 1)
   constexpr int HALF = T::HALF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = align_up_ptr<uint8_t>(smem_raw, 1024);
-  uint8_t* sQ = sbase;
-  uint8_t* sdO = sQ + T::A_BYTES;
+  uint8_t* sdO = sbase;
   uint8_t* sK = sdO + T::A_BYTES;
   uint8_t* sV = sK + NK * T::KV_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NV * T::KV_BYTES);
-  uint64_t* qd_full = bars;
-  uint64_t* k_full = bars + 1;
+  uint64_t* qd_full = bars;                       // dO_g landed in smem
+  uint64_t* q_tm = bars + 1;                      // Q_g written to TMEM by the compute threads
+  uint64_t* k_full = bars + 2;
   uint64_t* k_empty = k_full + NK;
   uint64_t* v_full = k_empty + NK;
   uint64_t* v_empty = v_full + NV;
   uint64_t* s_full = v_empty + NV;
   uint64_t* sp_free = s_full + 1;                 // compute threads have read S, dP
-  uint64_t* ds_full = sp_free + 1;                // [2]
-  uint64_t* ds_empty = ds_full + 2;               // [2]
-  uint64_t* acc_done = ds_empty + 2;
+  uint64_t* ds_full = sp_free + 1;
+  uint64_t* ds_empty = ds_full + 1;
+  uint64_t* acc_done = ds_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -460,6 +463,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(qd_full, 1);
+    mbar_init(q_tm, kComputeThreads);
     for (int s = 0; s < NK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -470,20 +474,17 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(sp_free, kComputeThreads);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&ds_full[b], kComputeThreads);
-      mbar_init(&ds_empty[b], 1);
-    }
+    mbar_init(ds_full, kComputeThreads);
+    mbar_init(ds_empty, 1);
     mbar_init(acc_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (BETA < T::BM) {
-    for (int t = 0; t < 2; ++t)
-      for (int c = 0; c < T::NCH; ++c) {
-        uint4* z = reinterpret_cast<uint4*>(sQ + t * T::A_BYTES + c * T::A_CHUNK + BETA * 128);
-        for (int i = threadIdx.x; i < (T::BM - BETA) * 128 / 16; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
-      }
+    for (int c = 0; c < T::NCH; ++c) {
+      uint4* z = reinterpret_cast<uint4*>(sdO + c * T::A_CHUNK + BETA * 128);
+      for (int i = threadIdx.x; i < (T::BM - BETA) * 128 / 16; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+    }
     fence_proxy_async_smem();
   }
   if (warp == 1) {
@@ -500,7 +501,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     for (int i = threadIdx.x; i < BETA * D / 8; i += blockDim.x)
       reinterpret_cast<uint4*>(dQ + qrow0 * D)[i] = make_uint4(0, 0, 0, 0);
   } else if (warp == 0 || warp == kQVWarp) {
-    // TMA producers, one per warp: warp 0 loads Q_g, dO_g and the K ring,
+    // TMA producers, one per warp: warp 0 loads dO_g and the K ring,
     // warp 10 the V ring
     if (lane == 0) {
       const bool is_k = warp == 0;
@@ -511,13 +512,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
       uint64_t* empty = is_k ? k_empty : v_empty;
       tma_prefetch_desc(map);
       if (is_k) {
-        tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmdO);
-        mbar_arrive_expect_tx(qd_full, 2 * T::TX_BYTES);
-        for (int c = 0; c < T::NCH; ++c) {
-          tma_load_2d(sQ + c * T::A_CHUNK, &tmQ, qd_full, c * 64, (int)qrow0);
-          tma_load_2d(sdO + c * T::A_CHUNK, &tmdO, qd_full, c * 64, (int)qrow0);
-        }
+        mbar_arrive_expect_tx(qd_full, T::TX_BYTES);
+        for (int c = 0; c < T::NCH; ++c) tma_load_2d(sdO + c * T::A_CHUNK, &tmdO, qd_full, c * 64, (int)qrow0);
       }
       int issued = 0;
       int jn = fwd_col[start];
@@ -546,7 +543,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
       // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
       constexpr uint32_t ID_S = idesc_bf16_f32(T::BM, BETA, false, false);
       constexpr uint32_t ID_Q = idesc_bf16_f32(T::BM, D, false, true);
-      const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t ddO0 = sdesc_sw128(smem_u32(sdO), 16, 1024);
       const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16, 1024);
@@ -560,7 +556,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ao = (kk >> 2) * T::A_CHUNK + (kk & 3) * 32;
           const uint32_t bo = (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32;
-          mma_ss_w(tmem + T::S_COL, desc_off(dQ0, ao), desc_off(kb, bo), ID_S, kk > 0 ? 1u : 0u);
+          mma_ts_w(tmem + T::S_COL, tmem + T::Q_COL + kk * 8, desc_off(kb, bo), ID_S, kk > 0 ? 1u : 0u);
         }
         if (!mbar_wait_warp(&v_full[sv], (uint32_t)(n / NV) & 1u, abort_flag, ctl, kid | W_VFULL)) return false;
         tc_fence_after();
@@ -575,7 +571,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
         mma_commit_w(&v_empty[sv]);   // V_j is only needed by dP
         return true;
       };
-      bool ok = mbar_wait_warp(qd_full, 0, abort_flag, ctl, kid | W_KV);
+      bool ok = mbar_wait_warp(qd_full, 0, abort_flag, ctl, kid | W_KV) &&
+                mbar_wait_warp(q_tm, 0, abort_flag, ctl, kid | W_KV);
       if (ok) ok = issue_sdp(0);
       for (int n = 0; ok && n < cnt; ++n) {
         DSV_TRACE_POINT(g_trace_q, n, 0);
@@ -586,18 +583,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
           if (!issue_sdp(n + 1)) break;
         }
         DSV_TRACE_POINT(g_trace_q, n, 1);
-        if (!mbar_wait_warp(&ds_full[n & 1], (uint32_t)(n >> 1) & 1u, abort_flag, ctl, kid | W_DSFULL)) break;
+        if (!mbar_wait_warp(ds_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_DSFULL)) break;
         DSV_TRACE_POINT(g_trace_q, n, 2);
         tc_fence_after();
         const int s = n % NK;
         const uint64_t kmn = desc_off(dKmn0, (uint32_t)s * T::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BETA / 16; ++kk) {
-          mma_ts_w(tmem + T::DQ_COL, tmem + T::DS_COL + (uint32_t)(n & 1) * T::DS_STRIDE + kk * 8,
-                 desc_off(kmn, kk * 16 * 128), ID_Q, (n > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_w(tmem + T::DQ_COL, tmem + T::DS_COL + kk * 8, desc_off(kmn, kk * 16 * 128), ID_Q,
+                   (n > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit_w(&k_empty[s]);
-        mma_commit_w(&ds_empty[n & 1]);
+        mma_commit_w(ds_empty);
         DSV_TRACE_POINT(g_trace_q, n, 3);
       }
       mma_commit_w(acc_done);
@@ -612,6 +609,25 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const float scale_log2 = scale * kLog2e;
     const float lse2 = (r < BETA) ? L2w[qrow0 + r] : 0.f;
     const float dd = (r < BETA) ? Dw[qrow0 + r] : 0.f;
+    {
+      // row r of Q_g into TMEM (this warp's half of its D/2 columns), as the A
+      // operand of every S product; rows past BETA are zero
+      constexpr int QW = D / 4;                   // columns per warp
+      const uint4* src = reinterpret_cast<const uint4*>(Qg + (qrow0 + r) * D + hf * (D / 2));
+      uint32_t q[QW];
+#pragma unroll
+      for (int i = 0; i < QW / 4; ++i) {
+        const uint4 v = r < BETA ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+        q[4 * i] = v.x;
+        q[4 * i + 1] = v.y;
+        q[4 * i + 2] = v.z;
+        q[4 * i + 3] = v.w;
+      }
+      tmem_st_w<QW>(tmem + lane_off + T::Q_COL + hf * QW, q);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(q_tm);
+    }
     bool ok = true;
     for (int n = 0; n < cnt; ++n) {
       if (!mbar_wait_warp(s_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_S)) {
@@ -638,18 +654,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
         dw[i] = pack_bf16x2(p0 * (__uint_as_float(xp[2 * i]) - dd), p1 * (__uint_as_float(xp[2 * i + 1]) - dd));
       }
       if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 6);
-      if (!mbar_wait_warp(&ds_empty[n & 1], ((uint32_t)(n >> 1) & 1u) ^ 1u, abort_flag, ctl, kid | W_DSEMPTY)) {
+      // the single dS buffer is free once dQ of the previous block is done
+      if (!mbar_wait_warp(ds_empty, ((uint32_t)n & 1u) ^ 1u, abort_flag, ctl, kid | W_DSEMPTY)) {
         ok = false;
         break;
       }
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < HALF / 32; ++c)
-        tmem_st16(tmem + lane_off + T::DS_COL + (uint32_t)(n & 1) * T::DS_STRIDE + hf * (HALF / 2) + c * 16,
-                  dw + c * 16);
+        tmem_st16(tmem + lane_off + T::DS_COL + hf * (HALF / 2) + c * 16, dw + c * 16);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&ds_full[n & 1]);
+      mbar_arrive(ds_full);
       if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 7);
     }
     if (ok) ok = mbar_wait_warp(acc_done, 0, abort_flag, ctl, kid | W_ACC);
@@ -681,7 +697,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 }
 
 template <int BETA, int D>
-cudaError_t launch_bwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+cudaError_t launch_bwd_t(const void* Q, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                          const CUtensorMap& tmdO, const void* O, const void* dO, const float* lse, const dsv_shape& s,
                          const int32_t* fwd_ptr, const int32_t* fwd_col, const int32_t* bwd_ptr,
                          const int32_t* bwd_col, float scale, void* dQ, void* dK, void* dV, void* ws, const Ctl& ctl,
@@ -708,7 +724,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
   if ((e = cudaFuncSetAttribute(qk, cudaFuncAttributeMaxDynamicSharedMemorySize, QTraits<BETA, D>::SMEM)) !=
       cudaSuccess)
     return e;
-  qk<<<(unsigned)groups, kQThreads, QTraits<BETA, D>::SMEM, st>>>(tmQ, tmK, tmV, tmdO, L2w, Dw, fwd_ptr, fwd_col,
+  qk<<<(unsigned)groups, kQThreads, QTraits<BETA, D>::SMEM, st>>>(static_cast<const __nv_bfloat16*>(Q), tmK, tmV, tmdO, L2w, Dw, fwd_ptr, fwd_col,
                                                                  s.N, G, scale, static_cast<__nv_bfloat16*>(dQ), ctl);
   return cudaGetLastError();
 }
@@ -719,13 +735,13 @@ size_t attn_bwd_ws_bytes(const dsv_shape& s) {
   return 2 * align256((size_t)s.B * s.H * s.N * sizeof(float));  // D and lse*log2(e)
 }
 
-cudaError_t launch_attn_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+cudaError_t launch_attn_bwd(const void* Q, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             const CUtensorMap& tmdO, const void* O, const void* dO, const float* lse,
                             const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col,
                             const int32_t* bwd_ptr, const int32_t* bwd_col, float scale, void* dQ, void* dK,
                             void* dV, void* ws, const Ctl& ctl, cudaStream_t st) {
 #define DSV_BWD(BE, DD)                                                                                        \
-  return launch_bwd_t<BE, DD>(tmQ, tmK, tmV, tmdO, O, dO, lse, s, fwd_ptr, fwd_col, bwd_ptr, bwd_col, scale, dQ, \
+  return launch_bwd_t<BE, DD>(Q, tmQ, tmK, tmV, tmdO, O, dO, lse, s, fwd_ptr, fwd_col, bwd_ptr, bwd_col, scale, dQ, \
                               dK, dV, ws, ctl, st)
   if (s.block == 128 && s.d == 128) DSV_BWD(128, 128);
   if (s.block == 128 && s.d == 64) DSV_BWD(128, 64);

@@ -7,7 +7,7 @@
 // One CTA per query group (b, h, g): the group's `block` query rows form the
 // M = 128 rows of every MMA (for block = 64 the upper 64 rows are zero
 // padding).  For each key block j in the group's list:
-//   S = Q K_j^T            tcgen05.mma, A = Q (smem), B = K_j (smem), D in TMEM
+//   S = Q K_j^T            tcgen05.mma, A = Q (TMEM), B = K_j (smem), D in TMEM
 //   P = exp2(S*c - m)      softmax warpgroup, P written back to TMEM as bf16
 //   O += P V_j             tcgen05.mma, A = P (TMEM), B = V_j (smem, MN-major)
 // with an online (running-max) softmax; O is only rescaled when the running
@@ -20,8 +20,13 @@
 //   warps 2..5  softmax / epilogue; warp w owns TMEM lanes 32*(w%4)..+31,
 //               i.e. one query row per thread.
 //   warp 6      TMA producer of the V_j ring (one lane).
-// TMEM columns: S/P buffer 0 at [0,128), buffer 1 at [128,256), O at [256,256+d).
-// S is double-buffered so the MMA of block n+1 overlaps the softmax of block n.
+// TMEM columns: S/P buffer 0 at [0,128), buffer 1 at [128,256), O at
+// [256,256+d), Q (bf16 pairs) at [256+d, 256+d+d/2).  S is double-buffered so
+// the MMA of block n+1 overlaps the softmax of block n.  Q is the A operand of
+// every S product, so it is read into TMEM once by the softmax warps: with
+// both operands in shared memory an M=128 MMA reads 128 B/clock, the whole
+// shared-memory bandwidth, and every barrier operation and TMA write of the
+// CTA then waits behind it.
 #include <math.h>
 
 #include "dsv_launch.h"
@@ -39,17 +44,16 @@ template <int BETA, int D>
 struct FwdTraits {
   static constexpr int BM = 128;                 // MMA M (query rows incl. padding)
   static constexpr int NCH = D / 64;             // 64-column (128-byte) chunks along d
-  static constexpr int Q_CHUNK = BM * 128;       // bytes of one Q chunk
   static constexpr int KV_CHUNK = BETA * 128;    // bytes of one K or V chunk
-  static constexpr int Q_BYTES = NCH * Q_CHUNK;
   static constexpr int KV_BYTES = NCH * KV_CHUNK;
-  static constexpr int NST = (Q_BYTES + 6 * KV_BYTES + 2048 <= 227 * 1024) ? 3 : 2;
+  static constexpr int NST = (6 * KV_BYTES + 2048 <= 227 * 1024) ? 3 : 2;
   static constexpr int NBAR = 1 + 4 * NST + 2 + 2 + 2 + 1;
-  static constexpr int SMEM_USED = 1024 + Q_BYTES + 2 * NST * KV_BYTES + NBAR * 8 + 16;
+  static constexpr int SMEM_USED = 1024 + 2 * NST * KV_BYTES + NBAR * 8 + 16;
   // at least 120 KB so that one CTA owns an SM (and its 512 TMEM columns)
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static constexpr uint32_t S_COL = 128;         // column stride of the two S/P buffers
   static constexpr uint32_t O_COL = 256;
+  static constexpr uint32_t Q_COL = 256 + D;     // Q as bf16 pairs: D/2 columns
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TX_BYTES = BETA * D * 2;   // one K or V tile (and the Q tile)
 };
@@ -61,7 +65,7 @@ enum : unsigned int { W_Q = 1, W_KEMPTY, W_K, W_P, W_V, W_S, W_O, W_OFINAL, W_DR
 
 template <int BETA, int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    attn_fwd_kernel(const __nv_bfloat16* __restrict__ Qg, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ fwd_ptr,
                     const int32_t* __restrict__ fwd_col, int N, int G, int nb, float scale_log2,
                     __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, Ctl ctl) {
@@ -69,8 +73,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   constexpr int NST = T::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = align_up_ptr<uint8_t>(smem_raw, 1024);
-  uint8_t* sQ = sbase;
-  uint8_t* sK = sQ + T::Q_BYTES;
+  uint8_t* sK = sbase;
   uint8_t* sV = sK + NST * T::KV_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NST * T::KV_BYTES);
   uint64_t* q_full = bars;
@@ -95,7 +98,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const unsigned int kid = (unsigned int)KID_FWD << 8;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_full, 128);                        // Q in TMEM: one arrival per softmax thread
     for (int s = 0; s < NST; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
@@ -110,14 +113,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(o_final, 1);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (BETA < T::BM) {
-    // rows BETA..127 of every Q chunk are never loaded: make them zero
-    for (int c = 0; c < T::NCH; ++c) {
-      uint4* z = reinterpret_cast<uint4*>(sQ + c * T::Q_CHUNK + BETA * 128);
-      for (int i = threadIdx.x; i < (T::BM - BETA) * 128 / 16; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, T::TMEM_COLS);
@@ -136,7 +131,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int i = threadIdx.x; i < BETA; i += blockDim.x) LSE[bh * N + (long long)g * BETA + i] = -INFINITY;
   } else if (warp == 0 || warp == kVWarp) {
-    // ---------------- TMA producers: warp 0 loads Q and the K ring, warp 6 the V ring ----------------
+    // ---------------- TMA producers: warp 0 loads the K ring, warp 6 the V ring ----------------
     // K is consumed by S = Q K^T one block before V is consumed by O += P V, and each
     // slot is released as soon as its own product is done, so K runs further ahead.
     // One producer per warp: lanes of one warp spinning on different barriers
@@ -148,12 +143,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       uint64_t* full = is_k ? k_full : v_full;
       uint64_t* empty = is_k ? k_empty : v_empty;
       tma_prefetch_desc(map);
-      if (is_k) {
-        tma_prefetch_desc(&tmQ);
-        const int qrow = (int)(bh * N + (long long)g * BETA);
-        mbar_arrive_expect_tx(q_full, T::TX_BYTES);
-        for (int c = 0; c < T::NCH; ++c) tma_load_2d(sQ + c * T::Q_CHUNK, &tmQ, q_full, c * 64, qrow);
-      }
       int issued = 0;
       int jn = fwd_col[start];
       for (int n = 0; n < cnt; ++n) {
@@ -173,7 +162,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         issued = n + 1;
       }
       // every copy this thread started must land before the CTA exits
-      if (is_k) mbar_wait(q_full, 0, nullptr, ctl, kid | W_DRAIN);
       for (int n = (issued > NST ? issued - NST : 0); n < issued; ++n)
         mbar_wait(&full[n % NST], (uint32_t)(n / NST) & 1u, nullptr, ctl, kid | W_DRAIN);
     }
@@ -183,7 +171,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t IDS = idesc_bf16_f32(T::BM, BETA, false, false);
       constexpr uint32_t IDO = idesc_bf16_f32(T::BM, D, false, true);
       // base descriptors; every MMA adds a compile-time offset
-      const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(sV), T::KV_CHUNK, 1024);
       bool ok = mbar_wait_warp(q_full, 0, abort_flag, ctl, kid | W_Q);
@@ -197,8 +184,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint64_t kb = desc_off(dK0, (uint32_t)s * T::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          mma_ss_w(d_tmem, desc_off(dQ0, (kk >> 2) * T::Q_CHUNK + (kk & 3) * 32),
-                 desc_off(kb, (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32), IDS, kk > 0 ? 1u : 0u);
+          mma_ts_w(d_tmem, tmem + T::Q_COL + kk * 8, desc_off(kb, (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32), IDS,
+                   kk > 0 ? 1u : 0u);
         }
         mma_commit_w(&s_full[n & 1]);
         mma_commit_w(&k_empty[s]);
@@ -234,6 +221,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int r = sp * 32 + lane;
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     float m = -INFINITY, l = 0.f;
+    {
+      // this thread's query row of Q into TMEM, as the A operand of every S
+      // product (rows past the group's BETA rows are zero)
+      const uint4* src = reinterpret_cast<const uint4*>(Qg + (bh * N + (long long)g * BETA + r) * D);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t q[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = r < BETA ? __ldg(src + c * 8 + i) : make_uint4(0, 0, 0, 0);
+          q[4 * i] = v.x;
+          q[4 * i + 1] = v.y;
+          q[4 * i + 2] = v.z;
+          q[4 * i + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_off + T::Q_COL + c * 32, q);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(q_full);
+    }
     bool ok = true;
     for (int n = 0; n < cnt; ++n) {
       if (!mbar_wait_warp(&s_full[n & 1], (uint32_t)(n >> 1) & 1u, abort_flag, ctl, kid | W_S)) {
@@ -332,7 +340,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 }
 
 template <int BETA, int D>
-cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const dsv_shape& s,
+cudaError_t launch_fwd_t(const void* Q, const CUtensorMap& tmK, const CUtensorMap& tmV, const dsv_shape& s,
                          const int32_t* fwd_ptr, const int32_t* fwd_col, float scale, void* O, float* lse,
                          const Ctl& ctl, cudaStream_t st) {
   using T = FwdTraits<BETA, D>;
@@ -342,23 +350,23 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
   const int G = s.N / s.block;
   const long long rows = (long long)s.B * s.H * G;
   const float scale_log2 = scale * 1.4426950408889634f;
-  kern<<<(unsigned)rows, kFwdThreads, T::SMEM, st>>>(tmQ, tmK, tmV, fwd_ptr, fwd_col, s.N, G, G, scale_log2,
+  kern<<<(unsigned)rows, kFwdThreads, T::SMEM, st>>>(static_cast<const __nv_bfloat16*>(Q), tmK, tmV, fwd_ptr, fwd_col, s.N, G, G, scale_log2,
                                              static_cast<__nv_bfloat16*>(O), lse, ctl);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+cudaError_t launch_attn_fwd(const void* Q, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col, float scale,
                             void* O, float* lse, const Ctl& ctl, cudaStream_t st) {
   if (s.block == 128 && s.d == 128)
-    return launch_fwd_t<128, 128>(tmQ, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
+    return launch_fwd_t<128, 128>(Q, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
   if (s.block == 128 && s.d == 64)
-    return launch_fwd_t<128, 64>(tmQ, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
+    return launch_fwd_t<128, 64>(Q, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
   if (s.block == 64 && s.d == 128)
-    return launch_fwd_t<64, 128>(tmQ, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
-  return launch_fwd_t<64, 64>(tmQ, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
+    return launch_fwd_t<64, 128>(Q, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
+  return launch_fwd_t<64, 64>(Q, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
 }
 
 }  // namespace dsv

@@ -210,11 +210,10 @@ dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const void* V, dsv_
   Ctl ctl;
   if (current_ctl(&ctl) != cudaSuccess) return DSV_ERR_CUDA;
   const long long rows = (long long)s.B * s.H * s.N;
-  CUtensorMap tq, tk, tv;
-  if (make_map(&tq, Q, rows, s.d, s.block) != cudaSuccess || make_map(&tk, K, rows, s.d, s.block) != cudaSuccess ||
-      make_map(&tv, V, rows, s.d, s.block) != cudaSuccess)
+  CUtensorMap tk, tv;
+  if (make_map(&tk, K, rows, s.d, s.block) != cudaSuccess || make_map(&tv, V, rows, s.d, s.block) != cudaSuccess)
     return DSV_ERR_CUDA;
-  return from_cuda(launch_attn_fwd(tq, tk, tv, s, fwd_ptr, fwd_col, resolve_scale(s, softmax_scale), O, lse, ctl,
+  return from_cuda(launch_attn_fwd(Q, tk, tv, s, fwd_ptr, fwd_col, resolve_scale(s, softmax_scale), O, lse, ctl,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -244,7 +243,7 @@ dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, cons
   if (make_map(&tq, Q, rows, s.d, s.block) != cudaSuccess || make_map(&tk, K, rows, s.d, s.block) != cudaSuccess ||
       make_map(&tv, V, rows, s.d, s.block) != cudaSuccess || make_map(&tdo, dO, rows, s.d, s.block) != cudaSuccess)
     return DSV_ERR_CUDA;
-  return from_cuda(launch_attn_bwd(tq, tk, tv, tdo, O, dO, lse, s, fwd_ptr, fwd_col, bwd_ptr, bwd_col,
+  return from_cuda(launch_attn_bwd(Q, tq, tk, tv, tdo, O, dO, lse, s, fwd_ptr, fwd_col, bwd_ptr, bwd_col,
                                    resolve_scale(s, softmax_scale), dQ, dK, dV, workspace, ctl,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
