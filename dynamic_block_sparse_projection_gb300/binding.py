@@ -16,7 +16,7 @@ import torch
 
 _LIB_PATH = Path(__file__).resolve().parent / "_build" / "libdsv.so"
 
-DSV_OK, DSV_ERR_INVALID_ARG, DSV_ERR_UNSUPPORTED, DSV_ERR_CUDA, DSV_ERR_BAD_INDEX, DSV_ERR_TIMEOUT = range(6)
+DSV_OK, DSV_ERR_INVALID_ARG, DSV_ERR_UNSUPPORTED, DSV_ERR_CUDA, DSV_ERR_BAD_INDEX, DSV_ERR_TIMEOUT, DSV_ERR_INTERNAL = range(7)
 
 # Every symbol the header declares; checked at load time.
 EXPORTS = (
@@ -271,3 +271,4 @@ def clear_device_error(stream=None, device=None) -> None:
 
 def set_wait_limit_ns(limit_ns: int) -> None:
     _check(lib.dsv_set_wait_limit_ns(int(limit_ns)), "dsv_set_wait_limit_ns")
+

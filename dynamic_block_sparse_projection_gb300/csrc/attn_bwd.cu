@@ -175,10 +175,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  // Every CTA owns its SM's whole TMEM (512 columns), so the allocation starts
+  // at lane 0, column 0: with that constant every TMEM address is known at
+  // compile time and the MMA warp spends no instructions moving them into
+  // uniform registers.  A different address is reported and nothing is run.
+  const uint32_t tmem_base = *tmem_slot;
+  constexpr uint32_t tmem = 0;
   const long long krow0 = bh * N + (long long)j * BETA;
 
-  if (cnt <= 0) {
+  if (tmem_base != tmem) {
+    if (threadIdx.x == 0) set_error(ctl, DSV_ERR_INTERNAL, (unsigned int)(row & 0x7fffffff));
+  } else if (cnt <= 0) {
     if (cnt < 0 && threadIdx.x == 0) set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
     for (int i = threadIdx.x; i < BETA * D / 8; i += blockDim.x) {
       reinterpret_cast<uint4*>(dK + krow0 * D)[i] = make_uint4(0, 0, 0, 0);
@@ -390,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, T::TMEM_COLS);
+  if (warp == 1) tmem_dealloc(tmem_base, T::TMEM_COLS);
 }
 
 // ---------------------------------------------------------------------------
@@ -494,9 +501,16 @@ __global__ void __launch_bounds__(kQThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  // Every CTA owns its SM's whole TMEM (512 columns), so the allocation starts
+  // at lane 0, column 0: with that constant every TMEM address is known at
+  // compile time and the MMA warp spends no instructions moving them into
+  // uniform registers.  A different address is reported and nothing is run.
+  const uint32_t tmem_base = *tmem_slot;
+  constexpr uint32_t tmem = 0;
 
-  if (cnt <= 0) {
+  if (tmem_base != tmem) {
+    if (threadIdx.x == 0) set_error(ctl, DSV_ERR_INTERNAL, (unsigned int)(row & 0x7fffffff));
+  } else if (cnt <= 0) {
     if (cnt < 0 && threadIdx.x == 0) set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
     for (int i = threadIdx.x; i < BETA * D / 8; i += blockDim.x)
       reinterpret_cast<uint4*>(dQ + qrow0 * D)[i] = make_uint4(0, 0, 0, 0);
@@ -693,7 +707,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, T::TMEM_COLS);
+  if (warp == 1) tmem_dealloc(tmem_base, T::TMEM_COLS);
 }
 
 template <int BETA, int D>

@@ -7,7 +7,7 @@
 // One CTA per query group (b, h, g): the group's `block` query rows form the
 // M = 128 rows of every MMA (for block = 64 the upper 64 rows are zero
 // padding).  For each key block j in the group's list:
-//   S = Q K_j^T            tcgen05.mma, A = Q (TMEM), B = K_j (smem), D in TMEM
+//   S = Q K_j^T            tcgen05.mma, A = Q (smem), B = K_j (smem), D in TMEM
 //   P = exp2(S*c - m)      softmax warpgroup, P written back to TMEM as bf16
 //   O += P V_j             tcgen05.mma, A = P (TMEM), B = V_j (smem, MN-major)
 // with an online (running-max) softmax; O is only rescaled when the running
@@ -20,13 +20,16 @@
 //   warps 2..5  softmax / epilogue; warp w owns TMEM lanes 32*(w%4)..+31,
 //               i.e. one query row per thread.
 //   warp 6      TMA producer of the V_j ring (one lane).
-// TMEM columns: S/P buffer 0 at [0,128), buffer 1 at [128,256), O at
-// [256,256+d), Q (bf16 pairs) at [256+d, 256+d+d/2).  S is double-buffered so
-// the MMA of block n+1 overlaps the softmax of block n.  Q is the A operand of
-// every S product, so it is read into TMEM once by the softmax warps: with
-// both operands in shared memory an M=128 MMA reads 128 B/clock, the whole
-// shared-memory bandwidth, and every barrier operation and TMA write of the
-// CTA then waits behind it.
+// TMEM columns: three S/P buffers at [0,128), [128,256), [256,384) and O at
+// [384,384+d).  With three buffers the MMA warp queues S of block n+2 before
+// it waits for P of block n, so the tensor core always has the next S
+// products queued while the softmax runs, and the softmax of block n+1 can
+// start as soon as that of block n is done.
+//
+// Ring slots are released without extra barriers: K slot n%3 is free once
+// S(n) is done (s_full), V slot n%3 once O += P(n) V_n is done (o_done); the
+// producer of tile n+3 waits for exactly that phase, which cannot be
+// overtaken because S(n+3) / PV(n+3) need the very tile it is about to load.
 #include <math.h>
 
 #include "dsv_launch.h"
@@ -44,16 +47,18 @@ template <int BETA, int D>
 struct FwdTraits {
   static constexpr int BM = 128;                 // MMA M (query rows incl. padding)
   static constexpr int NCH = D / 64;             // 64-column (128-byte) chunks along d
+  static constexpr int Q_CHUNK = BM * 128;       // bytes of one Q chunk
   static constexpr int KV_CHUNK = BETA * 128;    // bytes of one K or V chunk
+  static constexpr int Q_BYTES = NCH * Q_CHUNK;
   static constexpr int KV_BYTES = NCH * KV_CHUNK;
-  static constexpr int NST = (6 * KV_BYTES + 2048 <= 227 * 1024) ? 3 : 2;
-  static constexpr int NBAR = 1 + 4 * NST + 2 + 2 + 2 + 1;
-  static constexpr int SMEM_USED = 1024 + 2 * NST * KV_BYTES + NBAR * 8 + 16;
+  static constexpr int NST = 3;                  // K and V ring slots = S/P buffers
+  static constexpr int NBAR = 1 + 2 * NST + 3 * NST + 1;
+  static constexpr int SMEM_USED = 1024 + Q_BYTES + 2 * NST * KV_BYTES + NBAR * 8 + 16;
+  static_assert(SMEM_USED <= 227 * 1024, "forward tiles exceed shared memory");
   // at least 120 KB so that one CTA owns an SM (and its 512 TMEM columns)
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
-  static constexpr uint32_t S_COL = 128;         // column stride of the two S/P buffers
-  static constexpr uint32_t O_COL = 256;
-  static constexpr uint32_t Q_COL = 256 + D;     // Q as bf16 pairs: D/2 columns
+  static constexpr uint32_t S_COL = 128;         // column stride of the S/P buffers
+  static constexpr uint32_t O_COL = 384;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TX_BYTES = BETA * D * 2;   // one K or V tile (and the Q tile)
 };
@@ -65,7 +70,7 @@ enum : unsigned int { W_Q = 1, W_KEMPTY, W_K, W_P, W_V, W_S, W_O, W_OFINAL, W_DR
 
 template <int BETA, int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
-    attn_fwd_kernel(const __nv_bfloat16* __restrict__ Qg, const __grid_constant__ CUtensorMap tmK,
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ fwd_ptr,
                     const int32_t* __restrict__ fwd_col, int N, int G, int nb, float scale_log2,
                     __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, Ctl ctl) {
@@ -73,18 +78,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   constexpr int NST = T::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = align_up_ptr<uint8_t>(smem_raw, 1024);
-  uint8_t* sK = sbase;
+  uint8_t* sQ = sbase;
+  uint8_t* sK = sQ + T::Q_BYTES;
   uint8_t* sV = sK + NST * T::KV_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NST * T::KV_BYTES);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
   uint64_t* v_full = k_full + NST;
-  uint64_t* k_empty = v_full + NST;                // K slot free: its S product is done
-  uint64_t* v_empty = k_empty + NST;               // V slot free: its PV product is done
-  uint64_t* s_full = v_empty + NST;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;   // [2]: PV of block n arrives on o_done[n & 1]
-  uint64_t* o_final = o_done + 2;
+  uint64_t* s_full = v_full + NST;    // [3] S(n) in buffer n%3; also frees K slot n%3
+  uint64_t* p_full = s_full + NST;    // [3] P(n) written over S(n)
+  uint64_t* o_done = p_full + NST;    // [3] O += P(n) V_n done; also frees V slot n%3
+  uint64_t* o_final = o_done + NST;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_final + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -98,21 +102,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const unsigned int kid = (unsigned int)KID_FWD << 8;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 128);                        // Q in TMEM: one arrival per softmax thread
+    mbar_init(q_full, 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], 128);
-      mbar_init(&o_done[b], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 128);
+      mbar_init(&o_done[s], 1);
     }
     mbar_init(o_final, 1);
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  if (BETA < T::BM) {
+    // rows BETA..127 of every Q chunk are never loaded: make them zero
+    for (int c = 0; c < T::NCH; ++c) {
+      uint4* z = reinterpret_cast<uint4*>(sQ + c * T::Q_CHUNK + BETA * 128);
+      for (int i = threadIdx.x; i < (T::BM - BETA) * 128 / 16; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, T::TMEM_COLS);
@@ -121,9 +129,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  // Every CTA owns its SM's whole TMEM (512 columns), so the allocation starts
+  // at lane 0, column 0: with that constant every TMEM address is known at
+  // compile time and the MMA warp spends no instructions moving them into
+  // uniform registers.  A different address is reported and nothing is run.
+  const uint32_t tmem_base = *tmem_slot;
+  constexpr uint32_t tmem = 0;
 
-  if (cnt <= 0) {
+  if (tmem_base != tmem) {
+    if (threadIdx.x == 0) set_error(ctl, DSV_ERR_INTERNAL, (unsigned int)(row & 0x7fffffff));
+  } else if (cnt <= 0) {
     // empty (or malformed) list: O = 0, lse = -inf
     if (cnt < 0 && threadIdx.x == 0) set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
     for (int i = threadIdx.x; i < BETA * D / 8; i += blockDim.x) {
@@ -131,9 +146,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int i = threadIdx.x; i < BETA; i += blockDim.x) LSE[bh * N + (long long)g * BETA + i] = -INFINITY;
   } else if (warp == 0 || warp == kVWarp) {
-    // ---------------- TMA producers: warp 0 loads the K ring, warp 6 the V ring ----------------
-    // K is consumed by S = Q K^T one block before V is consumed by O += P V, and each
-    // slot is released as soon as its own product is done, so K runs further ahead.
+    // ---------------- TMA producers: warp 0 loads Q and the K ring, warp 6 the V ring ----------------
     // One producer per warp: lanes of one warp spinning on different barriers
     // would serialise each other.
     if (lane == 0) {
@@ -141,16 +154,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const CUtensorMap* map = is_k ? &tmK : &tmV;
       uint8_t* ring = is_k ? sK : sV;
       uint64_t* full = is_k ? k_full : v_full;
-      uint64_t* empty = is_k ? k_empty : v_empty;
+      uint64_t* freed = is_k ? s_full : o_done;   // phase n of slot n%3: its last reader is done
       tma_prefetch_desc(map);
+      if (is_k) {
+        tma_prefetch_desc(&tmQ);
+        const int qrow = (int)(bh * N + (long long)g * BETA);
+        mbar_arrive_expect_tx(q_full, T::TX_BYTES);
+        for (int c = 0; c < T::NCH; ++c) tma_load_2d(sQ + c * T::Q_CHUNK, &tmQ, q_full, c * 64, qrow);
+      }
       int issued = 0;
       int jn = fwd_col[start];
       for (int n = 0; n < cnt; ++n) {
         const int s = n % NST;
-        const uint32_t ph = (uint32_t)(n / NST) & 1u;
         int j = jn;
         if (n + 1 < cnt) jn = fwd_col[start + n + 1];
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, ctl, kid | W_KEMPTY)) break;
+        if (n >= NST && !mbar_wait(&freed[s], (uint32_t)((n - NST) / NST) & 1u, abort_flag, ctl, kid | W_KEMPTY))
+          break;
         if ((unsigned)j >= (unsigned)nb) {
           if (is_k) set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
           j = 0;
@@ -162,100 +181,83 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         issued = n + 1;
       }
       // every copy this thread started must land before the CTA exits
+      if (is_k) mbar_wait(q_full, 0, nullptr, ctl, kid | W_DRAIN);
       for (int n = (issued > NST ? issued - NST : 0); n < issued; ++n)
         mbar_wait(&full[n % NST], (uint32_t)(n / NST) & 1u, nullptr, ctl, kid | W_DRAIN);
     }
   } else if (warp == 1) {
-    {
-      // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
-      constexpr uint32_t IDS = idesc_bf16_f32(T::BM, BETA, false, false);
-      constexpr uint32_t IDO = idesc_bf16_f32(T::BM, D, false, true);
-      // base descriptors; every MMA adds a compile-time offset
-      const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t dV0 = sdesc_sw128(smem_u32(sV), T::KV_CHUNK, 1024);
-      bool ok = mbar_wait_warp(q_full, 0, abort_flag, ctl, kid | W_Q);
-      auto issue_S = [&](int n) -> bool {
-        const int s = n % NST;
-        DSV_TRACE_POINT(g_trace_fwd, n, 0);
-        if (!mbar_wait_warp(&k_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_K)) return false;
-        DSV_TRACE_POINT(g_trace_fwd, n, 1);
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(n & 1) * T::S_COL;
-        const uint64_t kb = desc_off(dK0, (uint32_t)s * T::KV_BYTES);
+    // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+    constexpr uint32_t IDS = idesc_bf16_f32(T::BM, BETA, false, false);
+    constexpr uint32_t IDO = idesc_bf16_f32(T::BM, D, false, true);
+    // base descriptors; every MMA adds a compile-time offset
+    const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(smem_u32(sV), T::KV_CHUNK, 1024);
+    // S(n) = Q K_n^T into buffer n%3
+    auto issue_S = [&](int n) -> bool {
+      const int s = n % NST;
+      DSV_TRACE_POINT(g_trace_fwd, n, 0);
+      if (!mbar_wait_warp(&k_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_K)) return false;
+      DSV_TRACE_POINT(g_trace_fwd, n, 1);
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + (uint32_t)s * T::S_COL;
+      const uint64_t kb = desc_off(dK0, (uint32_t)s * T::KV_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          mma_ts_w(d_tmem, tmem + T::Q_COL + kk * 8, desc_off(kb, (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32), IDS,
-                   kk > 0 ? 1u : 0u);
-        }
-        mma_commit_w(&s_full[n & 1]);
-        mma_commit_w(&k_empty[s]);
-        DSV_TRACE_POINT(g_trace_fwd, n, 2);
-        return true;
-      };
-      if (ok) ok = issue_S(0);
-      for (int n = 0; ok && n < cnt; ++n) {
-        if (n + 1 < cnt && !issue_S(n + 1)) break;
-        if (!mbar_wait_warp(&p_full[n & 1], (uint32_t)(n >> 1) & 1u, abort_flag, ctl, kid | W_P)) break;
-        DSV_TRACE_POINT(g_trace_fwd, n, 3);
-        const int s = n % NST;
-        if (!mbar_wait_warp(&v_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_V)) break;
-        DSV_TRACE_POINT(g_trace_fwd, n, 4);
-        tc_fence_after();
-        const uint32_t p_tmem = tmem + (uint32_t)(n & 1) * T::S_COL;
-        const uint64_t vb = desc_off(dV0, (uint32_t)s * T::KV_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < BETA / 16; ++kk) {
-          mma_ts_w(tmem + T::O_COL, p_tmem + kk * 8, desc_off(vb, kk * 16 * 128), IDO, (n > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit_w(&v_empty[s]);
-        mma_commit_w(&o_done[n & 1]);
-        DSV_TRACE_POINT(g_trace_fwd, n, 5);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        mma_ss_w(d_tmem, desc_off(dQ0, (kk >> 2) * T::Q_CHUNK + (kk & 3) * 32),
+                 desc_off(kb, (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32), IDS, kk > 0 ? 1u : 0u);
       }
-      mma_commit_w(o_final);
-      // TMEM is freed after the closing CTA-wide sync only once every MMA is done
-      mbar_wait_warp(o_final, 0, nullptr, ctl, kid | W_DRAIN);
+      mma_commit_w(&s_full[s]);
+      DSV_TRACE_POINT(g_trace_fwd, n, 2);
+      return true;
+    };
+    bool ok = mbar_wait_warp(q_full, 0, abort_flag, ctl, kid | W_Q);
+    if (ok) ok = issue_S(0);
+    if (ok && cnt > 1) ok = issue_S(1);
+    for (int n = 0; ok && n < cnt; ++n) {
+      // S(n+2) reuses the buffer of P(n-1), whose PV product is already queued
+      if (n + 2 < cnt && !issue_S(n + 2)) break;
+      const int s = n % NST;
+      const uint32_t ph = (uint32_t)(n / NST) & 1u;
+      if (!mbar_wait_warp(&p_full[s], ph, abort_flag, ctl, kid | W_P)) break;
+      DSV_TRACE_POINT(g_trace_fwd, n, 3);
+      if (!mbar_wait_warp(&v_full[s], ph, abort_flag, ctl, kid | W_V)) break;
+      DSV_TRACE_POINT(g_trace_fwd, n, 4);
+      tc_fence_after();
+      const uint32_t p_tmem = tmem + (uint32_t)s * T::S_COL;
+      const uint64_t vb = desc_off(dV0, (uint32_t)s * T::KV_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < BETA / 16; ++kk) {
+        mma_ts_w(tmem + T::O_COL, p_tmem + kk * 8, desc_off(vb, kk * 16 * 128), IDO, (n > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit_w(&o_done[s]);
+      DSV_TRACE_POINT(g_trace_fwd, n, 5);
     }
+    mma_commit_w(o_final);
+    // TMEM is freed after the closing CTA-wide sync only once every MMA is done
+    mbar_wait_warp(o_final, 0, nullptr, ctl, kid | W_DRAIN);
   } else if (warp < kVWarp) {
     // ---------------- softmax warpgroup (warps 2..5) ----------------
     const int sp = warp & 3;
     const int r = sp * 32 + lane;
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     float m = -INFINITY, l = 0.f;
-    {
-      // this thread's query row of Q into TMEM, as the A operand of every S
-      // product (rows past the group's BETA rows are zero)
-      const uint4* src = reinterpret_cast<const uint4*>(Qg + (bh * N + (long long)g * BETA + r) * D);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t q[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = r < BETA ? __ldg(src + c * 8 + i) : make_uint4(0, 0, 0, 0);
-          q[4 * i] = v.x;
-          q[4 * i + 1] = v.y;
-          q[4 * i + 2] = v.z;
-          q[4 * i + 3] = v.w;
-        }
-        tmem_st32(tmem + lane_off + T::Q_COL + c * 32, q);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(q_full);
-    }
     bool ok = true;
     for (int n = 0; n < cnt; ++n) {
-      if (!mbar_wait_warp(&s_full[n & 1], (uint32_t)(n >> 1) & 1u, abort_flag, ctl, kid | W_S)) {
+      const int s = n % NST;
+      if (!mbar_wait_warp(&s_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_S)) {
         ok = false;
         break;
       }
       if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 8);
       tc_fence_after();
-      const uint32_t sb = tmem + lane_off + (uint32_t)(n & 1) * T::S_COL;
+      const uint32_t sb = tmem + lane_off + (uint32_t)s * T::S_COL;
       uint32_t xr[BETA];
 #pragma unroll
       for (int c = 0; c < BETA / 32; ++c) tmem_ld32(sb + c * 32, xr + c * 32);
       tmem_ld_wait();
       if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 9);
+      if (warp == 5 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 6);
       // row max as 8 independent partial maxima (short dependency chains)
       float mx8[8];
 #pragma unroll
@@ -271,7 +273,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         m = m_new;
       } else if (__any_sync(0xffffffffu, m_new > m + 8.0f)) {
         // rescale this warp's O rows once the previous PV product has landed
-        if (!mbar_wait_warp(&o_done[(n - 1) & 1], (uint32_t)((n - 1) >> 1) & 1u, abort_flag, ctl, kid | W_O)) {
+        const int sp1 = (n - 1) % NST;
+        if (!mbar_wait_warp(&o_done[sp1], (uint32_t)((n - 1) / NST) & 1u, abort_flag, ctl, kid | W_O)) {
           ok = false;
           break;
         }
@@ -295,19 +298,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       uint32_t pk[BETA / 2];
 #pragma unroll
       for (int j = 0; j < BETA / 2; ++j) {
-        const float p0 = ex2(fmaf(__uint_as_float(xr[2 * j]), scale_log2, neg_m));
-        const float p1 = ex2(fmaf(__uint_as_float(xr[2 * j + 1]), scale_log2, neg_m));
+        const float x0 = fmaf(__uint_as_float(xr[2 * j]), scale_log2, neg_m);
+        const float x1 = fmaf(__uint_as_float(xr[2 * j + 1]), scale_log2, neg_m);
+        const float p0 = ex2(x0);
+        const float p1 = ex2(x1);
         rs8[j & 7] += p0 + p1;
         pk[j] = pack_bf16x2(p0, p1);
       }
       l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 10);
+      if (warp == 5 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 7);
 #pragma unroll
       for (int c = 0; c < BETA / 32; ++c) tmem_st16(sb + c * 16, pk + c * 16);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[n & 1]);
+      mbar_arrive(&p_full[s]);
       if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 11);
+      if (warp > 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 9 + warp);
     }
     if (ok) ok = mbar_wait_warp(o_final, 0, abort_flag, ctl, kid | W_OFINAL);
     if (ok) {
@@ -336,11 +343,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, T::TMEM_COLS);
+  if (warp == 1) tmem_dealloc(tmem_base, T::TMEM_COLS);
 }
 
 template <int BETA, int D>
-cudaError_t launch_fwd_t(const void* Q, const CUtensorMap& tmK, const CUtensorMap& tmV, const dsv_shape& s,
+cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const dsv_shape& s,
                          const int32_t* fwd_ptr, const int32_t* fwd_col, float scale, void* O, float* lse,
                          const Ctl& ctl, cudaStream_t st) {
   using T = FwdTraits<BETA, D>;
@@ -350,23 +357,23 @@ cudaError_t launch_fwd_t(const void* Q, const CUtensorMap& tmK, const CUtensorMa
   const int G = s.N / s.block;
   const long long rows = (long long)s.B * s.H * G;
   const float scale_log2 = scale * 1.4426950408889634f;
-  kern<<<(unsigned)rows, kFwdThreads, T::SMEM, st>>>(static_cast<const __nv_bfloat16*>(Q), tmK, tmV, fwd_ptr, fwd_col, s.N, G, G, scale_log2,
-                                             static_cast<__nv_bfloat16*>(O), lse, ctl);
+  kern<<<(unsigned)rows, kFwdThreads, T::SMEM, st>>>(tmQ, tmK, tmV, fwd_ptr, fwd_col, s.N, G, G, scale_log2,
+                                                     static_cast<__nv_bfloat16*>(O), lse, ctl);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attn_fwd(const void* Q, const CUtensorMap& tmK, const CUtensorMap& tmV,
+cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col, float scale,
                             void* O, float* lse, const Ctl& ctl, cudaStream_t st) {
   if (s.block == 128 && s.d == 128)
-    return launch_fwd_t<128, 128>(Q, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
+    return launch_fwd_t<128, 128>(tmQ, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
   if (s.block == 128 && s.d == 64)
-    return launch_fwd_t<128, 64>(Q, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
+    return launch_fwd_t<128, 64>(tmQ, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
   if (s.block == 64 && s.d == 128)
-    return launch_fwd_t<64, 128>(Q, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
-  return launch_fwd_t<64, 64>(Q, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
+    return launch_fwd_t<64, 128>(tmQ, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
+  return launch_fwd_t<64, 64>(tmQ, tmK, tmV, s, fwd_ptr, fwd_col, scale, O, lse, ctl, st);
 }
 
 }  // namespace dsv

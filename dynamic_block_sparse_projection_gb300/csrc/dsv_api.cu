@@ -106,6 +106,7 @@ extern "C" {
 
 int32_t dsv_version(void) { return 10000; }
 
+
 const char* dsv_status_string(dsv_status st) {
   switch (st) {
     case DSV_OK: return "ok";
@@ -114,6 +115,7 @@ const char* dsv_status_string(dsv_status st) {
     case DSV_ERR_CUDA: return "CUDA error";
     case DSV_ERR_BAD_INDEX: return "out-of-range block index in a CSR list";
     case DSV_ERR_TIMEOUT: return "a kernel wait ran past its time limit";
+    case DSV_ERR_INTERNAL: return "a kernel consistency check failed";
   }
   return "unknown status";
 }
@@ -210,10 +212,11 @@ dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const void* V, dsv_
   Ctl ctl;
   if (current_ctl(&ctl) != cudaSuccess) return DSV_ERR_CUDA;
   const long long rows = (long long)s.B * s.H * s.N;
-  CUtensorMap tk, tv;
-  if (make_map(&tk, K, rows, s.d, s.block) != cudaSuccess || make_map(&tv, V, rows, s.d, s.block) != cudaSuccess)
+  CUtensorMap tq, tk, tv;
+  if (make_map(&tq, Q, rows, s.d, s.block) != cudaSuccess || make_map(&tk, K, rows, s.d, s.block) != cudaSuccess ||
+      make_map(&tv, V, rows, s.d, s.block) != cudaSuccess)
     return DSV_ERR_CUDA;
-  return from_cuda(launch_attn_fwd(Q, tk, tv, s, fwd_ptr, fwd_col, resolve_scale(s, softmax_scale), O, lse, ctl,
+  return from_cuda(launch_attn_fwd(tq, tk, tv, s, fwd_ptr, fwd_col, resolve_scale(s, softmax_scale), O, lse, ctl,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -30,7 +30,7 @@ cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk
 size_t topk_ws_bytes(const dsv_shape& s);
 
 // Attention forward.  Tensor maps cover [B*H*N, d] bf16 with a 64-column box.
-cudaError_t launch_attn_fwd(const void* Q, const CUtensorMap& tmK, const CUtensorMap& tmV,
+cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col, float scale,
                             void* O, float* lse, const Ctl& ctl, cudaStream_t st);
 

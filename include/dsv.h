@@ -52,7 +52,8 @@ typedef enum {
   DSV_ERR_UNSUPPORTED = 2,  /* a size this build has no kernel for */
   DSV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
   DSV_ERR_BAD_INDEX = 4,    /* a kernel met an out-of-range CSR entry */
-  DSV_ERR_TIMEOUT = 5       /* a kernel wait ran past its time limit */
+  DSV_ERR_TIMEOUT = 5,      /* a kernel wait ran past its time limit */
+  DSV_ERR_INTERNAL = 6      /* a kernel's own consistency check failed */
 } dsv_status;
 
 /* Problem shape.  Supported: d in {64, 128}; block in {64, 128};
@@ -184,6 +185,7 @@ dsv_status dsv_set_wait_limit_ns(uint64_t limit_ns);
 
 /* Library version as major*10000 + minor*100 + patch. */
 int32_t dsv_version(void);
+
 
 #ifdef __cplusplus
 }

@@ -20,7 +20,7 @@ def lib():
 def _declared():
     text = (ROOT / "include" / "dsv.h").read_text()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dsv_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(dsv_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(lib):
@@ -37,6 +37,7 @@ def test_status_strings_and_version(lib):
     assert "argument" in lib.status_string(1)
     assert lib.lib.dsv_version() >= 10000
     assert lib.status_string(99) == "unknown status"
+    assert "consistency" in lib.status_string(lib.DSV_ERR_INTERNAL)
 
 
 def _shape(lib, B=1, H=2, N=512, d=128, block=128, r=16):
@@ -103,3 +104,4 @@ def test_host_validation_attention(lib):
         lib.DSV_ERR_INVALID_ARG
     assert L.dsv_sparse_attn_bwd(*p, s, FAKE, FAKE, FAKE, FAKE, 0.0, FAKE, FAKE, FAKE, FAKE + 64, ws, None) == \
         lib.DSV_ERR_INVALID_ARG
+

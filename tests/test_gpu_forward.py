@@ -171,3 +171,4 @@ def test_empty_problem(dsv):
     fp, fc, bp, bc = dsv.topk_blocks(S, [1, 1], 128, 0, 128)
     torch.cuda.synchronize()
     assert fp.cpu().tolist() == [0] and bp.cpu().tolist() == [0]
+
