@@ -8,11 +8,12 @@
 // it; that transpose is built deterministically without atomics.
 //
 // Kernels:
-//   topk_rows      one warp per row.  Scores become order-preserving uint32
-//                  keys in shared memory; an MSB-first radix select (4 x 8
-//                  bits) finds the k-th largest key T and how many keys equal
-//                  to T to take; one pass in index order then emits the list
-//                  (ballot + prefix) and the row's bitmask word by word.
+//   topk_select    one CTA per row (32 ... 512 threads, 16 keys per thread
+//                  in registers).  Scores become order-preserving uint32
+//                  keys; an MSB-first radix select below the row's common
+//                  prefix finds the k-th largest key T and how many keys equal
+//                  to T to take; ballots per 32-index chunk then give the
+//                  row's bitmask and the ascending list.
 //   topk_colcount  per (b, h, 32-column slab): 32x32 bit transposes of the
 //                  mask give each column's population.
 //   topk_scan      per (b, h): exclusive scan of the column counts -> bwd_ptr.
@@ -26,8 +27,6 @@ namespace dsv {
 
 namespace {
 
-constexpr int kRowWarps = 8;
-constexpr size_t kTopkSmemBudget = 200 * 1024;  // rows kernel: keys + histogram per warp
 
 // Order-preserving map float -> uint32 with -0.0 == +0.0 and NaN below -inf.
 __device__ __forceinline__ uint32_t score_key(float f) {
@@ -48,93 +47,254 @@ struct TopkArgs {
   HeadK hk;
 };
 
-__global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const __grid_constant__ TopkArgs a) {
-  extern __shared__ uint32_t sm[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + warp;
-  if (row >= a.rows) return;
+// One CTA of RT threads per row; the row's scores live in registers as keys
+// (KPT per thread, element i in thread i % RT, slot i / RT).
+//   1. AND / OR of all keys: the leading bits where they agree are a common
+//      prefix, so the radix select starts at the first bit that differs.
+//   2. MSB-first radix select over the remaining bits, 11 bits per pass
+//      (shared-memory histogram of 2048 bins; at most 3 passes): the k-th
+//      largest key T and how many keys equal to T are taken (need_eq).
+//   3. Per 32-element chunk (consecutive indices: chunk c = slot j of warp w),
+//      ballots of key > T and key == T; the equal keys are taken lowest index
+//      first, which gives the row's selection mask word by word.
+//   4. The set bits are written out in ascending order (prefix over chunks).
+// Per element this is a few instructions per pass and no contended atomics
+// on the leading bits, which for float scores are nearly all equal.
+constexpr int kKPT = 16;                 // keys per thread
+
+// Digit width of the radix passes: 11 bits (2048 bins) for long rows, 8 bits
+// for rows of at most 1024 keys, where clearing and scanning a large
+// histogram would cost more than the keys themselves.
+template <int RT>
+struct SelCfg {
+  static constexpr int DIGIT = RT >= 128 ? 11 : 8;
+  static constexpr int BINS = 1 << DIGIT;
+};
+
+template <int RT>
+__device__ __forceinline__ void cta_find_bin(const uint32_t* hist, uint32_t kk, uint32_t* s_tot, uint32_t* s_res) {
+  // the bin holding the kk-th largest key (counted from the top bin down) and its rank inside the bin
+  constexpr int kBins = SelCfg<RT>::BINS;
+  constexpr int BPT = kBins / RT;
+  constexpr int NW = RT / 32;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  uint32_t tot = 0;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) tot += hist[t * BPT + i];
+  // suffix sum over threads above t: warp-level, then across warps
+  uint32_t suf = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += v;
+  }
+  if (NW > 1) {
+    if (lane == 0) s_tot[w] = suf;  // total of warp w
+    __syncthreads();
+    uint32_t above_w = 0;
+    for (int v = w + 1; v < NW; ++v) above_w += s_tot[v];
+    suf += above_w;
+  }
+  uint32_t above = suf - tot;      // keys in bins above this thread's range
+  if (above < kk && above + tot >= kk) {
+    for (int i = BPT - 1; i >= 0; --i) {
+      const uint32_t c = hist[t * BPT + i];
+      if (above + c >= kk) {
+        s_res[0] = (uint32_t)(t * BPT + i);
+        s_res[1] = kk - above;
+        break;
+      }
+      above += c;
+    }
+  }
+  __syncthreads();
+}
+
+template <int RT>
+__global__ void __launch_bounds__(RT) topk_select_kernel(const __grid_constant__ TopkArgs a) {
+  constexpr int kBins = SelCfg<RT>::BINS;
+  constexpr int kDigit = SelCfg<RT>::DIGIT;
+  constexpr int NW = RT / 32;
+  constexpr int MAXC = RT * kKPT / 32;   // 32-element chunks of the row
+  __shared__ uint32_t hist[kBins];
+  __shared__ uint32_t s_tot[NW > 1 ? NW : 1];
+  __shared__ uint32_t s_red[2 * NW];
+  __shared__ uint32_t s_res[2];
+  __shared__ uint32_t eqw[MAXC];
+  __shared__ uint32_t selw[MAXC];
+  __shared__ int32_t offw[MAXC];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const long long row = blockIdx.x;
   const int nb = a.nb;
-  const int nbp = (nb + 31) & ~31;
-  uint32_t* keys = sm + warp * (nbp + 256);
-  uint32_t* hist = keys + nbp;
   const long long bh = row / a.G;
   const int g = (int)(row - bh * a.G);
   const int h = (int)(bh % a.H);
   const int b = (int)(bh / a.H);
-  const int k = a.hk.k[h];
+  const uint32_t k = (uint32_t)a.hk.k[h];
 
   const float* src = a.scores + row * (long long)nb;
-#pragma unroll 8
-  for (int i = lane; i < nbp; i += 32) keys[i] = (i < nb) ? score_key(__ldcs(src + i)) : 0u;
-  __syncwarp();
-
-  // MSB-first radix select of the k-th largest key.
-  uint32_t prefix = 0u, pmask = 0u;
-  int kk = k;  // rank of the wanted key among the keys that match `prefix`
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
+  uint32_t key[kKPT];
+  uint32_t vand = 0xffffffffu, vor = 0u;
 #pragma unroll
-    for (int i = lane; i < 256; i += 32) hist[i] = 0u;
-    __syncwarp();
-    for (int i = lane; i < nb; i += 32) {
-      const uint32_t key = keys[i];
-      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+  for (int j = 0; j < kKPT; ++j) {
+    const int i = j * RT + t;
+    key[j] = (i < nb) ? score_key(__ldcs(src + i)) : 0u;
+    if (i < nb) {
+      vand &= key[j];
+      vor |= key[j];
     }
-    __syncwarp();
-    int c[8];
-    int tot = 0;
+  }
+  // CTA-wide AND / OR
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      c[e] = (int)hist[8 * lane + e];
-      tot += c[e];
-    }
-    int suf = tot;  // sum of tot over lanes >= lane
+  for (int o = 16; o > 0; o >>= 1) {
+    vand &= __shfl_xor_sync(0xffffffffu, vand, o);
+    vor |= __shfl_xor_sync(0xffffffffu, vor, o);
+  }
+  if (lane == 0) {
+    s_red[w] = vand;
+    s_red[NW + w] = vor;
+  }
+  __syncthreads();
+  vand = 0xffffffffu;
+  vor = 0u;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_down_sync(0xffffffffu, suf, o);
-      if (lane + o < 32) suf += v;
-    }
-    int cum = suf - tot;  // keys in bins above this lane's 8 bins
-    int found = -1, newkk = 0;
+  for (int v = 0; v < NW; ++v) {
+    vand &= s_red[v];
+    vor |= s_red[NW + v];
+  }
+  const uint32_t diff = vand ^ vor;
+  int remaining = diff ? 32 - __clz(diff) : 0;          // bits below the common prefix
+  uint32_t hi_mask = remaining >= 32 ? 0u : ~((1u << remaining) - 1u);
+  uint32_t prefix = vand & hi_mask;
+  uint32_t kk = k;                                       // rank of the wanted key among those matching prefix
+  while (remaining > 0) {
+    const int nbits = remaining < kDigit ? remaining : kDigit;
+    const int sh = remaining - nbits;
+    const uint32_t dmask = (1u << nbits) - 1u;
+    for (int i = t; i < kBins; i += RT) hist[i] = 0u;
+    __syncthreads();
 #pragma unroll
-    for (int e = 7; e >= 0; --e) {
-      if (found < 0 && cum < kk && cum + c[e] >= kk) {
-        found = 8 * lane + e;
-        newkk = kk - cum;
+    for (int j = 0; j < kKPT; ++j) {
+      const int i = j * RT + t;
+      const bool in = i < nb && (key[j] & hi_mask) == prefix;
+      if constexpr (kDigit == 8) {
+        // few bins: lanes with the same digit add once, since same-address
+        // shared atomics serialise (measured faster for short rows only)
+        const uint32_t d = in ? (key[j] >> sh) & dmask : 0xffffffffu;
+        const uint32_t same = __match_any_sync(0xffffffffu, d);
+        if (in && lane == __ffs(same) - 1) atomicAdd(&hist[d], (uint32_t)__popc(same));
+      } else {
+        if (in) atomicAdd(&hist[(key[j] >> sh) & dmask], 1u);
       }
-      cum += c[e];
     }
-    const unsigned bal = __ballot_sync(0xffffffffu, found >= 0);
-    const int src_lane = __ffs(bal) - 1;
-    const int digit = __shfl_sync(0xffffffffu, found, src_lane);
-    kk = __shfl_sync(0xffffffffu, newkk, src_lane);
-    prefix |= (uint32_t)digit << shift;
-    pmask |= 255u << shift;
-    __syncwarp();
+    __syncthreads();
+    cta_find_bin<RT>(hist, kk, s_tot, s_res);
+    prefix |= s_res[0] << sh;
+    kk = s_res[1];
+    hi_mask |= dmask << sh;
+    remaining = sh;
+    __syncthreads();   // s_res / hist are reused
   }
   const uint32_t T = prefix;
-  const int need_eq = kk;  // how many keys equal to T are taken, lowest index first
+  const uint32_t need_eq = kk;   // keys equal to T that are taken, lowest index first
 
-  // Emit in index order; the selection ballot of each 32-element chunk is the mask word.
+  // selection words: chunk c = j * NW + w covers indices [32c, 32c + 32)
+  const int words = (nb + 31) >> 5;
+  uint32_t gtw[kKPT];
+#pragma unroll
+  for (int j = 0; j < kKPT; ++j) {
+    const int i = j * RT + t;
+    const bool valid = i < nb;
+    gtw[j] = __ballot_sync(0xffffffffu, valid && key[j] > T);
+    const uint32_t e = __ballot_sync(0xffffffffu, valid && key[j] == T);
+    if (lane == 0 && j * NW + w < MAXC) eqw[j * NW + w] = e;
+  }
+  __syncthreads();
+  // equal keys before each chunk (exclusive prefix over chunk order), by warp 0
+  if (w == 0) {
+    constexpr int CPL = (MAXC + 31) / 32;   // chunks per lane
+    uint32_t c[CPL];
+    uint32_t tot = 0;
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+      const int ci = lane * CPL + q;
+      c[q] = (ci < words) ? (uint32_t)__popc(eqw[ci]) : 0u;
+      tot += c[q];
+    }
+    uint32_t inc = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    uint32_t run = inc - tot;
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+      const int ci = lane * CPL + q;
+      if (ci < MAXC) offw[ci] = (int32_t)run;   // equal keys in chunks before ci
+      run += c[q];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kKPT; ++j) {
+    const int ci = j * NW + w;
+    if (ci < words) {
+      const uint32_t e = eqw[ci];
+      const uint32_t before = (uint32_t)offw[ci];
+      uint32_t take = 0u;
+      if (e != 0u && before < need_eq) {
+        const uint32_t room = need_eq - before;            // equal keys still to take, lowest first
+        if ((uint32_t)__popc(e) <= room) {
+          take = e;
+        } else {
+          uint32_t x = e;
+          for (uint32_t q = 0; q < room; ++q) {
+            take |= x & (~x + 1u);
+            x &= x - 1u;
+          }
+        }
+      }
+      if (lane == 0) selw[ci] = gtw[j] | take;
+    }
+  }
+  __syncthreads();
+  // output offsets per chunk (exclusive prefix of the selection counts), by warp 0
+  if (w == 0) {
+    constexpr int CPL = (MAXC + 31) / 32;
+    uint32_t c[CPL];
+    uint32_t tot = 0;
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+      const int ci = lane * CPL + q;
+      c[q] = (ci < words) ? (uint32_t)__popc(selw[ci]) : 0u;
+      tot += c[q];
+    }
+    uint32_t inc = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    uint32_t run = inc - tot;
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+      const int ci = lane * CPL + q;
+      if (ci < MAXC) offw[ci] = (int32_t)run;
+      run += c[q];
+    }
+  }
+  __syncthreads();
   const long long base = (long long)b * a.G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * a.G + (long long)g * k;
   int32_t* dst = a.fwd_col + base;
   uint32_t* mrow = a.mask + row * (long long)a.words;
   const unsigned lt = (1u << lane) - 1u;
-  int n_eq = 0, n_sel = 0;
-  for (int c0 = 0; c0 < nbp; c0 += 32) {
-    const int i = c0 + lane;
-    const bool valid = i < nb;
-    const uint32_t key = keys[i];
-    const bool eq = valid && key == T;
-    const unsigned beq = __ballot_sync(0xffffffffu, eq);
-    const bool sel = valid && (key > T || (eq && (n_eq + __popc(beq & lt)) < need_eq));
-    const unsigned bsel = __ballot_sync(0xffffffffu, sel);
-    if (sel) dst[n_sel + __popc(bsel & lt)] = i;
-    if (lane == 0) mrow[c0 >> 5] = bsel;
-    n_eq += __popc(beq);
-    n_sel += __popc(bsel);
+  for (int ci = w; ci < words; ci += NW) {
+    const uint32_t sw = selw[ci];
+    if ((sw >> lane) & 1u) dst[offw[ci] + __popc(sw & lt)] = ci * 32 + lane;
+    if (lane == 0) mrow[ci] = sw;
   }
-  if (lane == 0) {
+  if (t == 0) {
     a.fwd_ptr[row] = (int32_t)base;
     if (row == a.rows - 1) a.fwd_ptr[a.rows] = a.nnz;
   }
@@ -263,13 +423,14 @@ cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk
   a.rows = bhs * G;
   a.nnz = (int)nnz;
   a.hk = hk;
-  const int nbp = (G + 31) & ~31;
-  const size_t per_warp = (size_t)(nbp + 256) * sizeof(uint32_t);
-  const int warps = (int)std::max<size_t>(1, std::min<size_t>(kRowWarps, kTopkSmemBudget / per_warp));
-  const size_t smem = (size_t)warps * per_warp;
-  cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  topk_rows_kernel<<<(unsigned)((a.rows + warps - 1) / warps), warps * 32, smem, st>>>(a);
+  // threads per row: the smallest of 32 ... 512 holding the row in kKPT keys per thread
+  cudaError_t e;
+  const unsigned grid = (unsigned)a.rows;
+  if (G <= 32 * kKPT) topk_select_kernel<32><<<grid, 32, 0, st>>>(a);
+  else if (G <= 64 * kKPT) topk_select_kernel<64><<<grid, 64, 0, st>>>(a);
+  else if (G <= 128 * kKPT) topk_select_kernel<128><<<grid, 128, 0, st>>>(a);
+  else if (G <= 256 * kKPT) topk_select_kernel<256><<<grid, 256, 0, st>>>(a);
+  else topk_select_kernel<512><<<grid, 512, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   dim3 g2((unsigned)((words + 7) / 8), (unsigned)bhs);
   topk_colcount_kernel<<<g2, 256, 0, st>>>(mask, G, G, words, counts);
