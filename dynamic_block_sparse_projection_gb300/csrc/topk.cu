@@ -110,6 +110,51 @@ __device__ __forceinline__ void cta_find_bin(const uint32_t* hist, uint32_t kk, 
   __syncthreads();
 }
 
+constexpr int kCandMax = 256;            // keys tied for the threshold bucket, ranked exactly
+
+// CTA-wide exclusive prefix of popc(words[ci]) over chunks ci < nw, into off[]
+// (warp 0; MAXC chunks at most).
+template <int MAXC>
+__device__ __forceinline__ void chunk_prefix(const uint32_t* words, int nw, int32_t* off, int lane) {
+  constexpr int CPL = (MAXC + 31) / 32;   // chunks per lane
+  uint32_t c[CPL];
+  uint32_t tot = 0;
+#pragma unroll
+  for (int q = 0; q < CPL; ++q) {
+    const int ci = lane * CPL + q;
+    c[q] = (ci < nw) ? (uint32_t)__popc(words[ci]) : 0u;
+    tot += c[q];
+  }
+  uint32_t inc = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  uint32_t run = inc - tot;
+#pragma unroll
+  for (int q = 0; q < CPL; ++q) {
+    const int ci = lane * CPL + q;
+    if (ci < MAXC) off[ci] = (int32_t)run;
+    run += c[q];
+  }
+}
+
+// One row per CTA of RT threads, kKPT scores per thread in registers
+// (element i in thread i % RT, slot i / RT; 32-element chunk c = slot j of
+// warp w covers indices [32c, 32c + 32)).
+//
+// Fast path (finite row with max > min): the scores are binned by value into
+// BINS equal-width buckets between the row minimum and maximum (a monotone
+// map, so a higher bucket holds only larger scores).  One histogram gives the
+// bucket b* holding the k-th largest score; every score in a higher bucket is
+// kept, and the few scores tied in b* (at most kCandMax) are ranked exactly
+// by (key desc, index asc).  Value binning spreads the scores over the
+// buckets, so the shared-memory atomics rarely collide; radix digits of float
+// bits would pile into the few bins of the common exponents.
+// Fallback (non-finite scores, all equal, or a crowded b*): MSB-first radix
+// select on the order-preserving keys below their common prefix, then equal
+// keys taken lowest index first.
 template <int RT>
 __global__ void __launch_bounds__(RT) topk_select_kernel(const __grid_constant__ TopkArgs a) {
   constexpr int kBins = SelCfg<RT>::BINS;
@@ -118,14 +163,18 @@ __global__ void __launch_bounds__(RT) topk_select_kernel(const __grid_constant__
   constexpr int MAXC = RT * kKPT / 32;   // 32-element chunks of the row
   __shared__ uint32_t hist[kBins];
   __shared__ uint32_t s_tot[NW > 1 ? NW : 1];
-  __shared__ uint32_t s_red[2 * NW];
+  __shared__ uint32_t s_red[3 * NW];
   __shared__ uint32_t s_res[2];
+  __shared__ uint32_t s_cnt;
+  __shared__ uint32_t candk[kCandMax];
+  __shared__ int32_t candi[kCandMax];
   __shared__ uint32_t eqw[MAXC];
   __shared__ uint32_t selw[MAXC];
   __shared__ int32_t offw[MAXC];
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const long long row = blockIdx.x;
   const int nb = a.nb;
+  const int words = (nb + 31) >> 5;
   const long long bh = row / a.G;
   const int g = (int)(row - bh * a.G);
   const int h = (int)(bh % a.H);
@@ -133,157 +182,189 @@ __global__ void __launch_bounds__(RT) topk_select_kernel(const __grid_constant__
   const uint32_t k = (uint32_t)a.hk.k[h];
 
   const float* src = a.scores + row * (long long)nb;
-  uint32_t key[kKPT];
-  uint32_t vand = 0xffffffffu, vor = 0u;
+  float f[kKPT];
+  float lo = INFINITY, hi = -INFINITY;
+  bool bad = false;
 #pragma unroll
   for (int j = 0; j < kKPT; ++j) {
     const int i = j * RT + t;
-    key[j] = (i < nb) ? score_key(__ldcs(src + i)) : 0u;
+    f[j] = (i < nb) ? __ldcs(src + i) : 0.f;
     if (i < nb) {
-      vand &= key[j];
-      vor |= key[j];
+      bad |= !isfinite(f[j]);
+      lo = fminf(lo, f[j]);
+      hi = fmaxf(hi, f[j]);
     }
   }
-  // CTA-wide AND / OR
+  for (int i = t; i < MAXC; i += RT) selw[i] = 0u;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    vand &= __shfl_xor_sync(0xffffffffu, vand, o);
-    vor |= __shfl_xor_sync(0xffffffffu, vor, o);
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
   }
+  const uint32_t bad_w = __any_sync(0xffffffffu, bad) ? 1u : 0u;
   if (lane == 0) {
-    s_red[w] = vand;
-    s_red[NW + w] = vor;
+    s_red[w] = __float_as_uint(lo);
+    s_red[NW + w] = __float_as_uint(hi);
+    s_red[2 * NW + w] = bad_w;
   }
   __syncthreads();
-  vand = 0xffffffffu;
-  vor = 0u;
+  bool any_bad = false;
 #pragma unroll
   for (int v = 0; v < NW; ++v) {
-    vand &= s_red[v];
-    vor |= s_red[NW + v];
+    lo = fminf(lo, __uint_as_float(s_red[v]));
+    hi = fmaxf(hi, __uint_as_float(s_red[NW + v]));
+    any_bad |= s_red[2 * NW + v] != 0u;
   }
-  const uint32_t diff = vand ^ vor;
-  int remaining = diff ? 32 - __clz(diff) : 0;          // bits below the common prefix
-  uint32_t hi_mask = remaining >= 32 ? 0u : ~((1u << remaining) - 1u);
-  uint32_t prefix = vand & hi_mask;
-  uint32_t kk = k;                                       // rank of the wanted key among those matching prefix
-  while (remaining > 0) {
-    const int nbits = remaining < kDigit ? remaining : kDigit;
-    const int sh = remaining - nbits;
-    const uint32_t dmask = (1u << nbits) - 1u;
+  const float scale = (float)(kBins - 1) / (hi - lo);
+  bool fast = !any_bad && hi > lo && scale < 1e30f;   // uniform over the CTA
+
+  if (fast) {
+    uint32_t bk[kKPT];
     for (int i = t; i < kBins; i += RT) hist[i] = 0u;
+    if (t == 0) s_cnt = 0u;
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < kKPT; ++j) {
       const int i = j * RT + t;
-      const bool in = i < nb && (key[j] & hi_mask) == prefix;
-      if constexpr (kDigit == 8) {
-        // few bins: lanes with the same digit add once, since same-address
-        // shared atomics serialise (measured faster for short rows only)
+      bk[j] = min((uint32_t)(kBins - 1), (uint32_t)((f[j] - lo) * scale));
+      if (i < nb) atomicAdd(&hist[bk[j]], 1u);
+    }
+    __syncthreads();
+    cta_find_bin<RT>(hist, k, s_tot, s_res);
+    const uint32_t bstar = s_res[0];
+    const uint32_t kk = s_res[1];                         // how many of bucket b* are kept
+    const uint32_t C = hist[bstar];
+    if (C <= (uint32_t)kCandMax) {
+#pragma unroll
+      for (int j = 0; j < kKPT; ++j) {
+        const int i = j * RT + t;
+        if (i < nb && bk[j] == bstar) {
+          const uint32_t pos = atomicAdd(&s_cnt, 1u);
+          candk[pos] = score_key(f[j]);
+          candi[pos] = i;
+        }
+      }
+      __syncthreads();
+      for (uint32_t c = t; c < C; c += RT) {
+        const uint32_t kc = candk[c];
+        const int ic = candi[c];
+        uint32_t rank = 0;
+        for (uint32_t c2 = 0; c2 < C; ++c2) {
+          const uint32_t k2 = candk[c2];
+          rank += (k2 > kc || (k2 == kc && candi[c2] < ic)) ? 1u : 0u;
+        }
+        if (rank < kk) atomicOr(&selw[ic >> 5], 1u << (ic & 31));
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < kKPT; ++j) {
+        const int i = j * RT + t;
+        const uint32_t gt = __ballot_sync(0xffffffffu, i < nb && bk[j] > bstar);
+        if (lane == 0 && j * NW + w < words) selw[j * NW + w] |= gt;
+      }
+    } else {
+      fast = false;                                       // crowded bucket: exact radix select
+    }
+    __syncthreads();
+  }
+
+  if (!fast) {
+    uint32_t key[kKPT];
+    uint32_t vand = 0xffffffffu, vor = 0u;
+#pragma unroll
+    for (int j = 0; j < kKPT; ++j) {
+      const int i = j * RT + t;
+      key[j] = (i < nb) ? score_key(f[j]) : 0u;
+      if (i < nb) {
+        vand &= key[j];
+        vor |= key[j];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      vand &= __shfl_xor_sync(0xffffffffu, vand, o);
+      vor |= __shfl_xor_sync(0xffffffffu, vor, o);
+    }
+    if (lane == 0) {
+      s_red[w] = vand;
+      s_red[NW + w] = vor;
+    }
+    __syncthreads();
+    vand = 0xffffffffu;
+    vor = 0u;
+#pragma unroll
+    for (int v = 0; v < NW; ++v) {
+      vand &= s_red[v];
+      vor |= s_red[NW + v];
+    }
+    const uint32_t diff = vand ^ vor;
+    int remaining = diff ? 32 - __clz(diff) : 0;          // bits below the common prefix
+    uint32_t hi_mask = remaining >= 32 ? 0u : ~((1u << remaining) - 1u);
+    uint32_t prefix = vand & hi_mask;
+    uint32_t kk = k;                                       // rank of the wanted key among those matching prefix
+    while (remaining > 0) {
+      const int nbits = remaining < kDigit ? remaining : kDigit;
+      const int sh = remaining - nbits;
+      const uint32_t dmask = (1u << nbits) - 1u;
+      for (int i = t; i < kBins; i += RT) hist[i] = 0u;
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < kKPT; ++j) {
+        const int i = j * RT + t;
+        const bool in = i < nb && (key[j] & hi_mask) == prefix;
         const uint32_t d = in ? (key[j] >> sh) & dmask : 0xffffffffu;
         const uint32_t same = __match_any_sync(0xffffffffu, d);
         if (in && lane == __ffs(same) - 1) atomicAdd(&hist[d], (uint32_t)__popc(same));
-      } else {
-        if (in) atomicAdd(&hist[(key[j] >> sh) & dmask], 1u);
+      }
+      __syncthreads();
+      cta_find_bin<RT>(hist, kk, s_tot, s_res);
+      prefix |= s_res[0] << sh;
+      kk = s_res[1];
+      hi_mask |= dmask << sh;
+      remaining = sh;
+      __syncthreads();   // s_res / hist are reused
+    }
+    const uint32_t T = prefix;
+    const uint32_t need_eq = kk;   // keys equal to T that are taken, lowest index first
+    uint32_t gtw[kKPT];
+#pragma unroll
+    for (int j = 0; j < kKPT; ++j) {
+      const int i = j * RT + t;
+      const bool valid = i < nb;
+      gtw[j] = __ballot_sync(0xffffffffu, valid && key[j] > T);
+      const uint32_t e = __ballot_sync(0xffffffffu, valid && key[j] == T);
+      if (lane == 0) eqw[j * NW + w] = e;
+    }
+    __syncthreads();
+    if (w == 0) chunk_prefix<MAXC>(eqw, words, offw, lane);   // equal keys before each chunk
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kKPT; ++j) {
+      const int ci = j * NW + w;
+      if (ci < words) {
+        const uint32_t e = eqw[ci];
+        const uint32_t before = (uint32_t)offw[ci];
+        uint32_t take = 0u;
+        if (e != 0u && before < need_eq) {
+          const uint32_t room = need_eq - before;
+          if ((uint32_t)__popc(e) <= room) {
+            take = e;
+          } else {
+            uint32_t x = e;
+            for (uint32_t q = 0; q < room; ++q) {
+              take |= x & (~x + 1u);
+              x &= x - 1u;
+            }
+          }
+        }
+        if (lane == 0) selw[ci] = gtw[j] | take;
       }
     }
     __syncthreads();
-    cta_find_bin<RT>(hist, kk, s_tot, s_res);
-    prefix |= s_res[0] << sh;
-    kk = s_res[1];
-    hi_mask |= dmask << sh;
-    remaining = sh;
-    __syncthreads();   // s_res / hist are reused
   }
-  const uint32_t T = prefix;
-  const uint32_t need_eq = kk;   // keys equal to T that are taken, lowest index first
 
-  // selection words: chunk c = j * NW + w covers indices [32c, 32c + 32)
-  const int words = (nb + 31) >> 5;
-  uint32_t gtw[kKPT];
-#pragma unroll
-  for (int j = 0; j < kKPT; ++j) {
-    const int i = j * RT + t;
-    const bool valid = i < nb;
-    gtw[j] = __ballot_sync(0xffffffffu, valid && key[j] > T);
-    const uint32_t e = __ballot_sync(0xffffffffu, valid && key[j] == T);
-    if (lane == 0 && j * NW + w < MAXC) eqw[j * NW + w] = e;
-  }
-  __syncthreads();
-  // equal keys before each chunk (exclusive prefix over chunk order), by warp 0
-  if (w == 0) {
-    constexpr int CPL = (MAXC + 31) / 32;   // chunks per lane
-    uint32_t c[CPL];
-    uint32_t tot = 0;
-#pragma unroll
-    for (int q = 0; q < CPL; ++q) {
-      const int ci = lane * CPL + q;
-      c[q] = (ci < words) ? (uint32_t)__popc(eqw[ci]) : 0u;
-      tot += c[q];
-    }
-    uint32_t inc = tot;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += v;
-    }
-    uint32_t run = inc - tot;
-#pragma unroll
-    for (int q = 0; q < CPL; ++q) {
-      const int ci = lane * CPL + q;
-      if (ci < MAXC) offw[ci] = (int32_t)run;   // equal keys in chunks before ci
-      run += c[q];
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int j = 0; j < kKPT; ++j) {
-    const int ci = j * NW + w;
-    if (ci < words) {
-      const uint32_t e = eqw[ci];
-      const uint32_t before = (uint32_t)offw[ci];
-      uint32_t take = 0u;
-      if (e != 0u && before < need_eq) {
-        const uint32_t room = need_eq - before;            // equal keys still to take, lowest first
-        if ((uint32_t)__popc(e) <= room) {
-          take = e;
-        } else {
-          uint32_t x = e;
-          for (uint32_t q = 0; q < room; ++q) {
-            take |= x & (~x + 1u);
-            x &= x - 1u;
-          }
-        }
-      }
-      if (lane == 0) selw[ci] = gtw[j] | take;
-    }
-  }
-  __syncthreads();
-  // output offsets per chunk (exclusive prefix of the selection counts), by warp 0
-  if (w == 0) {
-    constexpr int CPL = (MAXC + 31) / 32;
-    uint32_t c[CPL];
-    uint32_t tot = 0;
-#pragma unroll
-    for (int q = 0; q < CPL; ++q) {
-      const int ci = lane * CPL + q;
-      c[q] = (ci < words) ? (uint32_t)__popc(selw[ci]) : 0u;
-      tot += c[q];
-    }
-    uint32_t inc = tot;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += v;
-    }
-    uint32_t run = inc - tot;
-#pragma unroll
-    for (int q = 0; q < CPL; ++q) {
-      const int ci = lane * CPL + q;
-      if (ci < MAXC) offw[ci] = (int32_t)run;
-      run += c[q];
-    }
-  }
+  // output: ascending list (offsets per chunk) and the row's mask words
+  if (w == 0) chunk_prefix<MAXC>(selw, words, offw, lane);
   __syncthreads();
   const long long base = (long long)b * a.G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * a.G + (long long)g * k;
   int32_t* dst = a.fwd_col + base;
