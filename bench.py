@@ -3,7 +3,8 @@
 
 One step = one pass of the whole hot path over one batch of synthetic video
 latents: dsv_predict_scores -> dsv_topk_blocks -> dsv_sparse_attn_fwd ->
-dsv_sparse_attn_bwd.  The metric is the effective TFLOP/s of the sparse
+the backward (timed as its three public stages dsv_attn_bwd_preprocess,
+dsv_attn_bwd_dkdv, dsv_attn_bwd_dq, bitwise equal to dsv_sparse_attn_bwd).  The metric is the effective TFLOP/s of the sparse
 attention forward + backward (computed blocks only: 4*block^2*d FLOPs per
 selected (group, block) pair forward, 10*block^2*d backward) over the whole
 step time, with the inputs resident in HBM.
@@ -48,6 +49,10 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--traffic-from", metavar="CSV",
+                   help="write profiles/traffic.json from an ncu --csv log of dram__bytes_read.sum and "
+                        "dram__bytes_write.sum for this bench's kernels, then exit (no GPU needed)")
+    p.add_argument("--traffic-command", default="", help="the ncu command line recorded with --traffic-from")
     return p.parse_args(argv)
 
 
@@ -167,7 +172,9 @@ class HotPath:
         self.ws_b = torch.empty(max(1, dsv.attn_bwd_workspace_bytes(B, H, N, d, w.block)), dtype=u8, device=dev)
 
     def run(self, ev=None):
-        """ev: optional list of 5 CUDA events recorded around the four calls."""
+        """The four public calls.  With ev (a list of 7 CUDA events) the
+        backward runs as its three public stages with an event between each,
+        so that every kernel of the step is timed on its own stream."""
         d, x, w = self.dsv, self.x, self.w
         if ev:
             ev[0].record()
@@ -180,10 +187,15 @@ class HotPath:
         d.sparse_attn_fwd(x.Q, x.K, x.V, fp, fc, w.block, out=self.O, lse=self.lse)
         if ev:
             ev[3].record()
-        d.sparse_attn_bwd(x.Q, x.K, x.V, self.O, x.dO, self.lse, fp, fc, bp, bc, w.block, outs=self.grads,
-                          workspace=self.ws_b)
-        if ev:
+            d.attn_bwd_preprocess(self.O, x.dO, self.lse, w.block, workspace=self.ws_b)
             ev[4].record()
+            d.attn_bwd_dkdv(x.Q, x.K, x.V, x.dO, bp, bc, w.block, outs=self.grads[1:], workspace=self.ws_b)
+            ev[5].record()
+            d.attn_bwd_dq(x.Q, x.K, x.V, x.dO, fp, fc, w.block, out=self.grads[0], workspace=self.ws_b)
+            ev[6].record()
+        else:
+            d.sparse_attn_bwd(x.Q, x.K, x.V, self.O, x.dO, self.lse, fp, fc, bp, bc, w.block, outs=self.grads,
+                              workspace=self.ws_b)
 
     def attention_only(self):
         d, x, w = self.dsv, self.x, self.w
@@ -193,7 +205,8 @@ class HotPath:
                           workspace=self.ws_b)
 
 
-KERNELS_PER_STEP = {"predict": 2, "topk": 4, "fwd": 1, "bwd": 3}
+KERNELS_PER_STEP = {"predict": 2, "topk": 4, "fwd": 1, "bwd_pre": 1, "bwd_kv": 1, "bwd_q": 1}
+STAGES = ("predict", "topk", "fwd", "bwd_pre", "bwd_kv", "bwd_q")
 
 
 def profile_traffic(kernel: str, source_files):
@@ -242,7 +255,7 @@ def run_ours(args):
         raise RuntimeError(f"device error {dsv.status_string(st)} ({info})")
 
     # timed region: K steps, L2 flushed (untimed) before each step
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -254,18 +267,19 @@ def run_ours(args):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    parts = {"predict": 0.0, "topk": 0.0, "fwd": 0.0, "bwd": 0.0}
+    parts = {k: 0.0 for k in STAGES}
     step_ms = []
     for e in evs:
-        t = [e[k].elapsed_time(e[k + 1]) for k in range(4)]
+        t = [e[k].elapsed_time(e[k + 1]) for k in range(len(STAGES))]
         for name, v in zip(parts, t):
             parts[name] += v
-        step_ms.append(sum(t))
+        step_ms.append(e[0].elapsed_time(e[-1]))
     total_ms = sum(step_ms)
     total_ms_max = reduce_replicas(total_ms, "max")
     flops_all = reduce_replicas(step_flops * args.steps, "sum")
     value = flops_all / (total_ms_max * 1e-3) / 1e12
     per_call = {k: v / args.steps for k, v in parts.items()}
+    per_call["bwd"] = per_call["bwd_pre"] + per_call["bwd_kv"] + per_call["bwd_q"]
     attn_ms = per_call["fwd"] + per_call["bwd"]
     peaks, peak_src = load_peaks()
 
@@ -274,8 +288,8 @@ def run_ours(args):
     if not args.no_dense:
         dense = time_dense(dsv, x, w, hp, flush)
 
-    # roofline of the dominant call
-    dom = max(per_call, key=per_call.get)
+    # roofline of the dominant kernel (the predictor and the top-k are whole calls of 2 and 4 launches)
+    dom = max(STAGES, key=lambda k: per_call[k])
     roofline = roofline_entry(dom, per_call, w, hp, peaks, peak_src)
 
     e2e = None if args.no_e2e else time_e2e(dsv, x, w, hp, args, flops_per_step=step_flops)
@@ -309,30 +323,44 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+# tcgen05 GEMMs of (block x block x d) each kernel runs per (group, block) pair
+MMAS_PER_PAIR = {"fwd": 2, "bwd_kv": 4, "bwd_q": 3}
+KERNEL_OF = {"fwd": "attn_fwd_kernel", "bwd_kv": "attn_bwd_kv_kernel", "bwd_q": "attn_bwd_q_kernel",
+             "bwd_pre": "bwd_rowdot_kernel"}
+KERNEL_SRC = {"fwd": "dynamic_block_sparse_projection_gb300/csrc/attn_fwd.cu",
+              "bwd_kv": "dynamic_block_sparse_projection_gb300/csrc/attn_bwd.cu",
+              "bwd_q": "dynamic_block_sparse_projection_gb300/csrc/attn_bwd.cu",
+              "bwd_pre": "dynamic_block_sparse_projection_gb300/csrc/attn_bwd.cu",
+              "predict": "dynamic_block_sparse_projection_gb300/csrc/predict.cu",
+              "topk": "dynamic_block_sparse_projection_gb300/csrc/topk.cu"}
+
+
 def roofline_entry(dom, per_call, w, hp, peaks, peak_src):
-    fwd_f, bwd_f = pair_flops(w.block, w.d)
     B, H, N, d, G = w.B, w.H, w.N, w.d, w.nb
-    if dom in ("fwd", "bwd"):
-        flops = (fwd_f if dom == "fwd" else bwd_f) * hp.nnz
+    srcs = [KERNEL_SRC[dom], "dynamic_block_sparse_projection_gb300/csrc/dsv_device.cuh"]
+    if dom in MMAS_PER_PAIR:
+        flops = MMAS_PER_PAIR[dom] * 2 * w.block * w.block * d * hp.nnz
         achieved = flops / (per_call[dom] * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
-        srcs = ["dynamic_block_sparse_projection_gb300/csrc/attn_fwd.cu" if dom == "fwd"
-                else "dynamic_block_sparse_projection_gb300/csrc/attn_bwd.cu"]
-        return {"kernel": f"dsv_sparse_attn_{dom}", "bound": "tensor", "achieved": round(achieved, 3),
-                "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "peak_source": f"{peak_src} bf16 burst",
-                "traffic": profile_traffic(f"attn_{dom}", srcs)}
-    if dom == "predict":
+        return {"kernel": KERNEL_OF[dom], "bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "algorithmic": f"{MMAS_PER_PAIR[dom]} x 2*block^2*d FLOP per (group, block) pair x {hp.nnz} pairs",
+                "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
+                "traffic": profile_traffic(KERNEL_OF[dom], srcs)}
+    if dom == "bwd_pre":
+        nbytes = 2 * B * H * N * d * 2 + B * H * N * 4 * 3
+        kname = KERNEL_OF[dom]
+    elif dom == "predict":
         nbytes = 2 * B * H * N * d * 2 + B * H * G * G * 4
-        src = ["dynamic_block_sparse_projection_gb300/csrc/predict.cu"]
+        kname = "dsv_predict_scores"
     else:
         nbytes = B * H * G * G * 4 + 2 * hp.nnz * 4 + 2 * (B * H * G + 1) * 4
-        src = ["dynamic_block_sparse_projection_gb300/csrc/topk.cu"]
+        kname = "dsv_topk_blocks"
     achieved = nbytes / (per_call[dom] * 1e-3) / 1e9
     peak = peaks["hbm_gbs"]
-    return {"kernel": f"dsv_{dom}", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+    return {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} copy",
-            "traffic": profile_traffic(dom, src)}
+            "traffic": profile_traffic(kname, srcs)}
 
 
 def time_dense(dsv, x, w, hp, flush, iters=2):
@@ -489,8 +517,45 @@ def run_reference(args):
     }), flush=True)
 
 
+def write_traffic(csv_path, command, workload):
+    """profiles/traffic.json: mean DRAM bytes (read + write) per launch of each
+    attention kernel in an ncu CSV, with the sha256 of the sources it was
+    built from (bench.py reports null once they change)."""
+    import csv
+    rows = list(csv.reader(open(csv_path)))
+    hi = next(i for i, r in enumerate(rows) if "Kernel Name" in r and "Metric Name" in r)
+    h = rows[hi]
+    ki, mi, vi, ui, idi = (h.index(c) for c in ("Kernel Name", "Metric Name", "Metric Value", "Metric Unit", "ID"))
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+    per_launch = {}
+    for r in rows[hi + 1:]:
+        if len(r) <= max(ki, mi, vi, ui) or r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        name = next((k for k in KERNEL_OF.values() if k in r[ki]), None)
+        if name is None:
+            continue
+        v = float(r[vi].replace(",", "")) * scale.get(r[ui], 1.0)
+        key = (name, r[idi])
+        per_launch[key] = per_launch.get(key, 0.0) + v
+    out = {}
+    for stage, name in KERNEL_OF.items():
+        vals = [v for (n, _), v in per_launch.items() if n == name]
+        if not vals:
+            continue
+        hsh = hashlib.sha256()
+        for src in (KERNEL_SRC[stage], "dynamic_block_sparse_projection_gb300/csrc/dsv_device.cuh"):
+            hsh.update((ROOT / src).read_bytes())
+        out[name] = {"dram_bytes_per_launch": round(sum(vals) / len(vals)), "launches": len(vals),
+                     "workload": workload, "source_sha256": hsh.hexdigest(), "command": command}
+    (ROOT / "profiles" / "traffic.json").write_text(json.dumps(out, indent=1) + "\n")
+    print(json.dumps(out, indent=1))
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.traffic_from:
+        write_traffic(args.traffic_from, args.traffic_command, args.workload)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

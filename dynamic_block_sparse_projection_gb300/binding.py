@@ -27,6 +27,7 @@ EXPORTS = (
     "dsv_status_string", "dsv_get_device_error", "dsv_clear_device_error",
     "dsv_set_wait_limit_ns", "dsv_version",
     "dsv_topk_blocks_noalloc",
+    "dsv_attn_bwd_preprocess", "dsv_attn_bwd_dkdv", "dsv_attn_bwd_dq",
 )
 
 
@@ -74,6 +75,12 @@ def _load() -> ctypes.CDLL:
     lib.dsv_set_wait_limit_ns.restype = ctypes.c_int
     lib.dsv_topk_blocks_noalloc.argtypes = [vp, Shape, ctypes.POINTER(i32), vp, vp, vp, vp, vp]
     lib.dsv_topk_blocks_noalloc.restype = ctypes.c_int
+    lib.dsv_attn_bwd_preprocess.argtypes = [vp, vp, vp, Shape, vp, sz, vp]
+    lib.dsv_attn_bwd_preprocess.restype = ctypes.c_int
+    lib.dsv_attn_bwd_dkdv.argtypes = [vp, vp, vp, vp, Shape, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp]
+    lib.dsv_attn_bwd_dkdv.restype = ctypes.c_int
+    lib.dsv_attn_bwd_dq.argtypes = [vp, vp, vp, vp, Shape, vp, vp, ctypes.c_float, vp, vp, sz, vp]
+    lib.dsv_attn_bwd_dq.restype = ctypes.c_int
     lib.dsv_version.argtypes = []
     lib.dsv_version.restype = i32
     return lib
@@ -250,6 +257,50 @@ def sparse_attn_bwd(Q, K, V, O, dO, lse, fwd_ptr, fwd_col, bwd_ptr, bwd_col, blo
                                    float(softmax_scale), *[_ptr(t) for t in outs], _ptr(ws), nbytes,
                                    _stream(dev, stream)), "dsv_sparse_attn_bwd")
     return outs
+
+
+def attn_bwd_preprocess(O, dO, lse, block: int, *, workspace, stream=None) -> None:
+    """D and lse * log2(e) into `workspace`; see dsv_attn_bwd_preprocess."""
+    _need(O, "O", torch.bfloat16)
+    dev = O.device
+    _need(dO, "dO", torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    B, H, N, d = O.shape
+    s = Shape(B, H, N, d, block, 8)
+    _check(lib.dsv_attn_bwd_preprocess(_ptr(O), _ptr(dO), _ptr(lse), s, _ptr(workspace), workspace.numel(),
+                                       _stream(dev, stream)), "dsv_attn_bwd_preprocess")
+
+
+def attn_bwd_dkdv(Q, K, V, dO, bwd_ptr, bwd_col, block: int, softmax_scale: float = 0.0, *, outs, workspace,
+                  stream=None) -> None:
+    """dK, dV into outs = (dK, dV) after attn_bwd_preprocess; see dsv_attn_bwd_dkdv."""
+    _need(Q, "Q", torch.bfloat16)
+    dev = Q.device
+    for name, t in (("K", K), ("V", V), ("dO", dO), ("dK", outs[0]), ("dV", outs[1])):
+        _need(t, name, torch.bfloat16, dev)
+    for name, t in (("bwd_ptr", bwd_ptr), ("bwd_col", bwd_col)):
+        _need(t, name, torch.int32, dev)
+    B, H, N, d = Q.shape
+    s = Shape(B, H, N, d, block, 8)
+    _check(lib.dsv_attn_bwd_dkdv(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), s, _ptr(bwd_ptr), _ptr(bwd_col),
+                                 float(softmax_scale), _ptr(outs[0]), _ptr(outs[1]), _ptr(workspace),
+                                 workspace.numel(), _stream(dev, stream)), "dsv_attn_bwd_dkdv")
+
+
+def attn_bwd_dq(Q, K, V, dO, fwd_ptr, fwd_col, block: int, softmax_scale: float = 0.0, *, out, workspace,
+                stream=None) -> None:
+    """dQ into `out` after attn_bwd_preprocess; see dsv_attn_bwd_dq."""
+    _need(Q, "Q", torch.bfloat16)
+    dev = Q.device
+    for name, t in (("K", K), ("V", V), ("dO", dO), ("dQ", out)):
+        _need(t, name, torch.bfloat16, dev)
+    for name, t in (("fwd_ptr", fwd_ptr), ("fwd_col", fwd_col)):
+        _need(t, name, torch.int32, dev)
+    B, H, N, d = Q.shape
+    s = Shape(B, H, N, d, block, 8)
+    _check(lib.dsv_attn_bwd_dq(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), s, _ptr(fwd_ptr), _ptr(fwd_col),
+                               float(softmax_scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                               _stream(dev, stream)), "dsv_attn_bwd_dq")
 
 
 # ---------------------------------------------------------------------------

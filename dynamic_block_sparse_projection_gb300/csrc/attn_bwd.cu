@@ -711,36 +711,45 @@ __global__ void __launch_bounds__(kQThreads, 1)
 }
 
 template <int BETA, int D>
-cudaError_t launch_bwd_t(const void* Q, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                         const CUtensorMap& tmdO, const void* O, const void* dO, const float* lse, const dsv_shape& s,
-                         const int32_t* fwd_ptr, const int32_t* fwd_col, const int32_t* bwd_ptr,
-                         const int32_t* bwd_col, float scale, void* dQ, void* dK, void* dV, void* ws, const Ctl& ctl,
-                         cudaStream_t st) {
+cudaError_t launch_kv_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                        const CUtensorMap& tmdO, const dsv_shape& s, const int32_t* bwd_ptr, const int32_t* bwd_col,
+                        float scale, void* dK, void* dV, const float* Dw, const float* L2w, const Ctl& ctl,
+                        cudaStream_t st) {
   const int G = s.N / s.block;
-  const long long rows = (long long)s.B * s.H * s.N;
   const long long groups = (long long)s.B * s.H * G;
-  float* Dw = static_cast<float*>(ws);
-  float* L2w = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)rows * sizeof(float)));
-  constexpr int RPC = 256 / (D / 8);
-  bwd_rowdot_kernel<D><<<(unsigned)((rows + RPC - 1) / RPC), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse, Dw, L2w, rows);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   auto kv = attn_bwd_kv_kernel<BETA, D>;
+  cudaError_t e;
   if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KVTraits<BETA, D>::SMEM)) !=
       cudaSuccess)
     return e;
   kv<<<(unsigned)groups, kThreads, KVTraits<BETA, D>::SMEM, st>>>(tmQ, tmK, tmV, tmdO, L2w, Dw, bwd_ptr, bwd_col,
                                                                    s.N, G, scale, static_cast<__nv_bfloat16*>(dK),
                                                                    static_cast<__nv_bfloat16*>(dV), ctl);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int BETA, int D>
+cudaError_t launch_q_t(const void* Q, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                       const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col, float scale, void* dQ,
+                       const float* Dw, const float* L2w, const Ctl& ctl, cudaStream_t st) {
+  const int G = s.N / s.block;
+  const long long groups = (long long)s.B * s.H * G;
   auto qk = attn_bwd_q_kernel<BETA, D>;
+  cudaError_t e;
   if ((e = cudaFuncSetAttribute(qk, cudaFuncAttributeMaxDynamicSharedMemorySize, QTraits<BETA, D>::SMEM)) !=
       cudaSuccess)
     return e;
-  qk<<<(unsigned)groups, kQThreads, QTraits<BETA, D>::SMEM, st>>>(static_cast<const __nv_bfloat16*>(Q), tmK, tmV, tmdO, L2w, Dw, fwd_ptr, fwd_col,
-                                                                 s.N, G, scale, static_cast<__nv_bfloat16*>(dQ), ctl);
+  qk<<<(unsigned)groups, kQThreads, QTraits<BETA, D>::SMEM, st>>>(static_cast<const __nv_bfloat16*>(Q), tmK, tmV,
+                                                                  tmdO, L2w, Dw, fwd_ptr, fwd_col, s.N, G, scale,
+                                                                  static_cast<__nv_bfloat16*>(dQ), ctl);
   return cudaGetLastError();
+}
+
+// workspace: D_i, then lse_i * log2(e), each B*H*N floats (256-byte aligned)
+const float* ws_D(const void* ws) { return static_cast<const float*>(ws); }
+const float* ws_L2(const void* ws, const dsv_shape& s) {
+  return reinterpret_cast<const float*>(static_cast<const char*>(ws) +
+                                        align256((size_t)s.B * s.H * s.N * sizeof(float)));
 }
 
 }  // namespace
@@ -749,19 +758,58 @@ size_t attn_bwd_ws_bytes(const dsv_shape& s) {
   return 2 * align256((size_t)s.B * s.H * s.N * sizeof(float));  // D and lse*log2(e)
 }
 
+cudaError_t launch_attn_bwd_pre(const void* O, const void* dO, const float* lse, const dsv_shape& s, void* ws,
+                                cudaStream_t st) {
+  const long long rows = (long long)s.B * s.H * s.N;
+  float* Dw = static_cast<float*>(ws);
+  float* L2w = const_cast<float*>(ws_L2(ws, s));
+  const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(O);
+  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(dO);
+  if (s.d == 128) {
+    constexpr int RPC = 256 / (128 / 8);
+    bwd_rowdot_kernel<128><<<(unsigned)((rows + RPC - 1) / RPC), 256, 0, st>>>(o, g, lse, Dw, L2w, rows);
+  } else {
+    constexpr int RPC = 256 / (64 / 8);
+    bwd_rowdot_kernel<64><<<(unsigned)((rows + RPC - 1) / RPC), 256, 0, st>>>(o, g, lse, Dw, L2w, rows);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_kv(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                               const CUtensorMap& tmdO, const dsv_shape& s, const int32_t* bwd_ptr,
+                               const int32_t* bwd_col, float scale, void* dK, void* dV, const void* ws,
+                               const Ctl& ctl, cudaStream_t st) {
+#define DSV_KV(BE, DD) \
+  return launch_kv_t<BE, DD>(tmQ, tmK, tmV, tmdO, s, bwd_ptr, bwd_col, scale, dK, dV, ws_D(ws), ws_L2(ws, s), ctl, st)
+  if (s.block == 128 && s.d == 128) DSV_KV(128, 128);
+  if (s.block == 128 && s.d == 64) DSV_KV(128, 64);
+  if (s.block == 64 && s.d == 128) DSV_KV(64, 128);
+  DSV_KV(64, 64);
+#undef DSV_KV
+}
+
+cudaError_t launch_attn_bwd_q(const void* Q, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                              const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col, float scale,
+                              void* dQ, const void* ws, const Ctl& ctl, cudaStream_t st) {
+#define DSV_Q(BE, DD) \
+  return launch_q_t<BE, DD>(Q, tmK, tmV, tmdO, s, fwd_ptr, fwd_col, scale, dQ, ws_D(ws), ws_L2(ws, s), ctl, st)
+  if (s.block == 128 && s.d == 128) DSV_Q(128, 128);
+  if (s.block == 128 && s.d == 64) DSV_Q(128, 64);
+  if (s.block == 64 && s.d == 128) DSV_Q(64, 128);
+  DSV_Q(64, 64);
+#undef DSV_Q
+}
+
 cudaError_t launch_attn_bwd(const void* Q, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             const CUtensorMap& tmdO, const void* O, const void* dO, const float* lse,
                             const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col,
                             const int32_t* bwd_ptr, const int32_t* bwd_col, float scale, void* dQ, void* dK,
                             void* dV, void* ws, const Ctl& ctl, cudaStream_t st) {
-#define DSV_BWD(BE, DD)                                                                                        \
-  return launch_bwd_t<BE, DD>(Q, tmQ, tmK, tmV, tmdO, O, dO, lse, s, fwd_ptr, fwd_col, bwd_ptr, bwd_col, scale, dQ, \
-                              dK, dV, ws, ctl, st)
-  if (s.block == 128 && s.d == 128) DSV_BWD(128, 128);
-  if (s.block == 128 && s.d == 64) DSV_BWD(128, 64);
-  if (s.block == 64 && s.d == 128) DSV_BWD(64, 128);
-  DSV_BWD(64, 64);
-#undef DSV_BWD
+  cudaError_t e = launch_attn_bwd_pre(O, dO, lse, s, ws, st);
+  if (e != cudaSuccess) return e;
+  if ((e = launch_attn_bwd_kv(tmQ, tmK, tmV, tmdO, s, bwd_ptr, bwd_col, scale, dK, dV, ws, ctl, st)) != cudaSuccess)
+    return e;
+  return launch_attn_bwd_q(Q, tmK, tmV, tmdO, s, fwd_ptr, fwd_col, scale, dQ, ws, ctl, st);
 }
 
 }  // namespace dsv

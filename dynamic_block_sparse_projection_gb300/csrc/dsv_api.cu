@@ -251,4 +251,56 @@ dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, cons
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+dsv_status dsv_attn_bwd_preprocess(const void* O, const void* dO, const float* lse, dsv_shape s, void* workspace,
+                                   size_t workspace_bytes, dsv_stream_t stream) {
+  dsv_status v = check_shape(s, false);
+  if (v != DSV_OK) return v;
+  if (empty(s)) return DSV_OK;
+  if (!O || !dO || !lse || !workspace) return DSV_ERR_INVALID_ARG;
+  if (!al16(O) || !al16(dO) || !al16(lse) || !al256(workspace)) return DSV_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_bwd_ws_bytes(s)) return DSV_ERR_INVALID_ARG;
+  return from_cuda(launch_attn_bwd_pre(O, dO, lse, s, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dsv_status dsv_attn_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO, dsv_shape s,
+                             const int32_t* bwd_ptr, const int32_t* bwd_col, float softmax_scale, void* dK, void* dV,
+                             const void* workspace, size_t workspace_bytes, dsv_stream_t stream) {
+  dsv_status v = check_shape(s, false);
+  if (v != DSV_OK) return v;
+  if (empty(s)) return DSV_OK;
+  if (!Q || !K || !V || !dO || !bwd_ptr || !bwd_col || !dK || !dV || !workspace) return DSV_ERR_INVALID_ARG;
+  if (!al16(Q) || !al16(K) || !al16(V) || !al16(dO) || !al16(dK) || !al16(dV) || !al256(workspace))
+    return DSV_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_bwd_ws_bytes(s)) return DSV_ERR_INVALID_ARG;
+  Ctl ctl;
+  if (current_ctl(&ctl) != cudaSuccess) return DSV_ERR_CUDA;
+  const long long rows = (long long)s.B * s.H * s.N;
+  CUtensorMap tq, tk, tv, tdo;
+  if (make_map(&tq, Q, rows, s.d, s.block) != cudaSuccess || make_map(&tk, K, rows, s.d, s.block) != cudaSuccess ||
+      make_map(&tv, V, rows, s.d, s.block) != cudaSuccess || make_map(&tdo, dO, rows, s.d, s.block) != cudaSuccess)
+    return DSV_ERR_CUDA;
+  return from_cuda(launch_attn_bwd_kv(tq, tk, tv, tdo, s, bwd_ptr, bwd_col, resolve_scale(s, softmax_scale), dK, dV,
+                                      workspace, ctl, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dsv_status dsv_attn_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, dsv_shape s,
+                           const int32_t* fwd_ptr, const int32_t* fwd_col, float softmax_scale, void* dQ,
+                           const void* workspace, size_t workspace_bytes, dsv_stream_t stream) {
+  dsv_status v = check_shape(s, false);
+  if (v != DSV_OK) return v;
+  if (empty(s)) return DSV_OK;
+  if (!Q || !K || !V || !dO || !fwd_ptr || !fwd_col || !dQ || !workspace) return DSV_ERR_INVALID_ARG;
+  if (!al16(Q) || !al16(K) || !al16(V) || !al16(dO) || !al16(dQ) || !al256(workspace)) return DSV_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_bwd_ws_bytes(s)) return DSV_ERR_INVALID_ARG;
+  Ctl ctl;
+  if (current_ctl(&ctl) != cudaSuccess) return DSV_ERR_CUDA;
+  const long long rows = (long long)s.B * s.H * s.N;
+  CUtensorMap tk, tv, tdo;
+  if (make_map(&tk, K, rows, s.d, s.block) != cudaSuccess || make_map(&tv, V, rows, s.d, s.block) != cudaSuccess ||
+      make_map(&tdo, dO, rows, s.d, s.block) != cudaSuccess)
+    return DSV_ERR_CUDA;
+  return from_cuda(launch_attn_bwd_q(Q, tk, tv, tdo, s, fwd_ptr, fwd_col, resolve_scale(s, softmax_scale), dQ,
+                                     workspace, ctl, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

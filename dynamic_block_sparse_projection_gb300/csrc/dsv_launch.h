@@ -40,6 +40,16 @@ cudaError_t launch_attn_bwd(const void* Q, const CUtensorMap& tmQ, const CUtenso
                             const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col,
                             const int32_t* bwd_ptr, const int32_t* bwd_col, float scale, void* dQ, void* dK,
                             void* dV, void* ws, const Ctl& ctl, cudaStream_t st);
+// The stages of launch_attn_bwd (preprocess; dK/dV; dQ).
+cudaError_t launch_attn_bwd_pre(const void* O, const void* dO, const float* lse, const dsv_shape& s, void* ws,
+                                cudaStream_t st);
+cudaError_t launch_attn_bwd_kv(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                               const CUtensorMap& tmdO, const dsv_shape& s, const int32_t* bwd_ptr,
+                               const int32_t* bwd_col, float scale, void* dK, void* dV, const void* ws,
+                               const Ctl& ctl, cudaStream_t st);
+cudaError_t launch_attn_bwd_q(const void* Q, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                              const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col, float scale,
+                              void* dQ, const void* ws, const Ctl& ctl, cudaStream_t st);
 size_t attn_bwd_ws_bytes(const dsv_shape& s);
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

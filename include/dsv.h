@@ -165,6 +165,26 @@ dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, cons
                                void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
                                dsv_stream_t stream);
 
+/* The three stages dsv_sparse_attn_bwd runs, one kernel each, for callers
+ * that schedule or time them separately; in this order on one stream (or
+ * with the ordering made explicit) they give results bitwise equal to the
+ * single call, and dsv_attn_bwd_dkdv / dsv_attn_bwd_dq may run in either
+ * order once the preprocess is done.  Arguments mean what they mean above.
+ *   dsv_attn_bwd_preprocess  D_i and lse_i * log2(e) into the workspace.
+ *   dsv_attn_bwd_dkdv        dK, dV (one CTA per key block, transposed lists).
+ *   dsv_attn_bwd_dq          dQ (one CTA per query group, forward lists).
+ * Errors as for dsv_sparse_attn_bwd; a stage does not check that the
+ * preprocess ran. */
+dsv_status dsv_attn_bwd_preprocess(const void* O, const void* dO, const float* lse, dsv_shape s,
+                                   void* workspace, size_t workspace_bytes, dsv_stream_t stream);
+dsv_status dsv_attn_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO, dsv_shape s,
+                             const int32_t* bwd_ptr, const int32_t* bwd_col, float softmax_scale,
+                             void* dK, void* dV, const void* workspace, size_t workspace_bytes,
+                             dsv_stream_t stream);
+dsv_status dsv_attn_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, dsv_shape s,
+                           const int32_t* fwd_ptr, const int32_t* fwd_col, float softmax_scale,
+                           void* dQ, const void* workspace, size_t workspace_bytes, dsv_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Status and device-side error reporting.
  * ------------------------------------------------------------------------ */

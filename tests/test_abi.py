@@ -105,3 +105,23 @@ def test_host_validation_attention(lib):
     assert L.dsv_sparse_attn_bwd(*p, s, FAKE, FAKE, FAKE, FAKE, 0.0, FAKE, FAKE, FAKE, FAKE + 64, ws, None) == \
         lib.DSV_ERR_INVALID_ARG
 
+
+def test_host_validation_backward_stages(lib):
+    L = lib.lib
+    s = _shape(lib)
+    ws = L.dsv_attn_bwd_workspace_bytes(s)
+    assert L.dsv_attn_bwd_preprocess(FAKE, FAKE, FAKE, s, FAKE, ws - 1, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_attn_bwd_preprocess(FAKE, None, FAKE, s, FAKE, ws, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_attn_bwd_preprocess(FAKE, FAKE, FAKE, s, FAKE + 64, ws, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_attn_bwd_preprocess(FAKE, FAKE, FAKE, _shape(lib, d=96), FAKE, ws, None) == lib.DSV_ERR_UNSUPPORTED
+    p4 = (FAKE,) * 4
+    assert L.dsv_attn_bwd_dkdv(*p4, s, FAKE, None, 0.0, FAKE, FAKE, FAKE, ws, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_attn_bwd_dkdv(*p4, s, FAKE, FAKE, 0.0, FAKE + 2, FAKE, FAKE, ws, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_attn_bwd_dkdv(*p4, s, FAKE, FAKE, 0.0, FAKE, FAKE, FAKE, ws - 1, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_attn_bwd_dq(*p4, s, None, FAKE, 0.0, FAKE, FAKE, ws, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_attn_bwd_dq(*p4, s, FAKE, FAKE, 0.0, FAKE, FAKE + 64, ws, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_attn_bwd_dq(*p4, _shape(lib, N=500), FAKE, FAKE, 0.0, FAKE, FAKE, ws, None) == \
+        lib.DSV_ERR_INVALID_ARG
+    empty = _shape(lib, B=0)
+    assert L.dsv_attn_bwd_dq(*p4, empty, None, None, 0.0, None, None, 0, None) == 0
+

@@ -116,3 +116,25 @@ def test_backward_empty_group_list(dsv):
         sl = slice(j * 64, (j + 1) * 64)
         assert rel_l2(to64(dK)[0, 0, sl], rk) <= GRAD_REL_L2
         assert rel_l2(to64(dV)[0, 0, sl], rv) <= GRAD_REL_L2
+
+
+def test_backward_stages_equal_single_call(dsv):
+    """preprocess, dK/dV and dQ run as separate calls (dQ first) give the
+    single call's gradients bit for bit."""
+    w = SMALL["stress_small"]
+    x = wl.make_inputs(w, device="cuda")
+    S_ref = oracle.predict_scores(to64(x.Q), to64(x.K), to64(x.Wq), to64(x.Wk), w.block)
+    lists = oracle_lists(S_ref, x.k_per_head, w.nb)
+    O, lse, dQ, dK, dV = _gpu_fwd_bwd(dsv, x.Q, x.K, x.V, x.dO, lists, w.block)
+    fp, fc, bp, bc = csr_to_device(lists, x.Q.device)
+    B, H, N, d = x.Q.shape
+    nbytes = dsv.attn_bwd_workspace_bytes(B, H, N, d, w.block)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    sQ, sK, sV = (torch.full_like(x.Q, 7.0) for _ in range(3))
+    dsv.attn_bwd_preprocess(O, x.dO, lse, w.block, workspace=ws)
+    dsv.attn_bwd_dq(x.Q, x.K, x.V, x.dO, fp, fc, w.block, out=sQ, workspace=ws)
+    dsv.attn_bwd_dkdv(x.Q, x.K, x.V, x.dO, bp, bc, w.block, outs=(sK, sV), workspace=ws)
+    torch.cuda.synchronize()
+    assert dsv.device_error()[0] == 0
+    assert torch.equal(sQ, dQ) and torch.equal(sK, dK) and torch.equal(sV, dV)
+
