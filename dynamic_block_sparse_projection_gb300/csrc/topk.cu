@@ -15,7 +15,8 @@
 //                  to T to take; ballots per 32-index chunk then give the
 //                  row's bitmask and the ascending list.
 //   topk_colcount  per (b, h, 32-column slab): 32x32 bit transposes of the
-//                  mask give each column's population.
+//                  mask (stored word column by word column, rows contiguous)
+//                  give each column's population.
 //   topk_scan      per (b, h): exclusive scan of the column counts -> bwd_ptr.
 //   topk_fill      same walk as colcount; each lane appends the set rows of
 //                  its column in ascending g.
@@ -184,17 +185,18 @@ __global__ void __launch_bounds__(RT) topk_select_kernel(const __grid_constant__
   const float* src = a.scores + row * (long long)nb;
   float f[kKPT];
   float lo = INFINITY, hi = -INFINITY;
-  bool bad = false;
+  float sum = 0.f;      // non-finite iff a score is NaN or infinite (or, harmlessly, the sum overflows)
 #pragma unroll
   for (int j = 0; j < kKPT; ++j) {
     const int i = j * RT + t;
     f[j] = (i < nb) ? __ldcs(src + i) : 0.f;
     if (i < nb) {
-      bad |= !isfinite(f[j]);
+      sum += f[j];
       lo = fminf(lo, f[j]);
       hi = fmaxf(hi, f[j]);
     }
   }
+  const bool bad = !isfinite(sum);
   for (int i = t; i < MAXC; i += RT) selw[i] = 0u;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -363,17 +365,22 @@ __global__ void __launch_bounds__(RT) topk_select_kernel(const __grid_constant__
     __syncthreads();
   }
 
-  // output: ascending list (offsets per chunk) and the row's mask words
+  // output: ascending list (offsets per chunk) and the row's mask words; one
+  // thread per chunk writes that chunk's few selected indices
   if (w == 0) chunk_prefix<MAXC>(selw, words, offw, lane);
   __syncthreads();
   const long long base = (long long)b * a.G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * a.G + (long long)g * k;
   int32_t* dst = a.fwd_col + base;
-  uint32_t* mrow = a.mask + row * (long long)a.words;
-  const unsigned lt = (1u << lane) - 1u;
-  for (int ci = w; ci < words; ci += NW) {
-    const uint32_t sw = selw[ci];
-    if ((sw >> lane) & 1u) dst[offw[ci] + __popc(sw & lt)] = ci * 32 + lane;
-    if (lane == 0) mrow[ci] = sw;
+  // mask word (b, h, ci, g): word columns contiguous over g for the transpose kernels
+  uint32_t* mcol = a.mask + bh * (long long)a.words * a.G + g;
+  for (int ci = t; ci < words; ci += RT) {
+    uint32_t sw = selw[ci];
+    mcol[(long long)ci * a.G] = sw;
+    int o = offw[ci];
+    while (sw) {
+      dst[o++] = ci * 32 + (__ffs(sw) - 1);
+      sw &= sw - 1u;
+    }
   }
   if (t == 0) {
     a.fwd_ptr[row] = (int32_t)base;
@@ -395,37 +402,49 @@ __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
   return x;
 }
 
-// grid: (ceil(words / 8), B*H); warp w handles mask word column blockIdx.x*8 + w.
+// The G rows of a (b, h) slice are cut into segments of kSeg rows so that the
+// column walks below run in parallel: counts[bh][seg][col] is the number of
+// rows of segment seg that selected column col.
+constexpr int kSeg = 512;
+
+// grid: (ceil(words / 8), nseg, B*H); warp w handles mask word column blockIdx.x*8 + w.
 __global__ void __launch_bounds__(256) topk_colcount_kernel(const uint32_t* __restrict__ mask, int G, int nb,
                                                             int words, int32_t* __restrict__ counts) {
   const int wc = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (wc >= words) return;
   const int lane = threadIdx.x & 31;
-  const long long bh = blockIdx.y;
-  const uint32_t* M = mask + bh * (long long)G * words;
+  const int seg = blockIdx.y, nseg = gridDim.y;
+  const long long bh = blockIdx.z;
+  const uint32_t* M = mask + (bh * words + wc) * (long long)G;   // this word column, rows contiguous
+  const int g1 = min(G, (seg + 1) * kSeg);
   int cnt = 0;
-  for (int g0 = 0; g0 < G; g0 += 32) {
+#pragma unroll 4
+  for (int g0 = seg * kSeg; g0 < g1; g0 += 32) {
     const int g = g0 + lane;
-    const uint32_t x = (g < G) ? M[(long long)g * words + wc] : 0u;
+    const uint32_t x = (g < g1) ? M[g] : 0u;
     cnt += __popc(warp_transpose32(x, lane));
   }
   const int col = wc * 32 + lane;
-  if (col < nb) counts[bh * nb + col] = cnt;
+  if (col < nb) counts[(bh * nseg + seg) * nb + col] = cnt;
 }
 
-// One CTA (1024 threads) per (b, h): bwd_ptr = slice base + exclusive scan of counts.
-__global__ void __launch_bounds__(1024) topk_scan_kernel(const int32_t* __restrict__ counts,
+// One CTA (1024 threads) per (b, h): bwd_ptr = slice base + exclusive scan of
+// the column totals; counts[bh][seg][col] becomes the output position of the
+// first entry of segment seg in column col.
+__global__ void __launch_bounds__(1024) topk_scan_kernel(int32_t* __restrict__ counts, int nseg,
                                                          const __grid_constant__ TopkArgs a,
                                                          int32_t* __restrict__ bwd_ptr, long long nslices) {
   __shared__ int warp_tot[32];
   const long long bh = blockIdx.x;
   const int h = (int)(bh % a.H), b = (int)(bh / a.H);
   const int nb = a.nb;
+  int32_t* C = counts + bh * (long long)nseg * nb;
   const int per = (nb + 1023) / 1024;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int j0 = t * per;
   int loc = 0;
-  for (int j = j0; j < min(nb, j0 + per); ++j) loc += counts[bh * nb + j];
+  for (int j = j0; j < min(nb, j0 + per); ++j)
+    for (int sg = 0; sg < nseg; ++sg) loc += C[sg * nb + j];
   int inc = loc;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -448,31 +467,66 @@ __global__ void __launch_bounds__(1024) topk_scan_kernel(const int32_t* __restri
   int run = (int)base + (w > 0 ? warp_tot[w - 1] : 0) + inc - loc;
   for (int j = j0; j < min(nb, j0 + per); ++j) {
     bwd_ptr[bh * nb + j] = run;
-    run += counts[bh * nb + j];
+    for (int sg = 0; sg < nseg; ++sg) {
+      const int c = C[sg * nb + j];
+      C[sg * nb + j] = run;
+      run += c;
+    }
   }
   if (bh == nslices - 1 && t == 0) bwd_ptr[nslices * nb] = a.nnz;
 }
 
-__global__ void __launch_bounds__(256) topk_fill_kernel(const uint32_t* __restrict__ mask, int G, int nb, int words,
-                                                        const int32_t* __restrict__ bwd_ptr,
-                                                        int32_t* __restrict__ bwd_col) {
-  const int wc = blockIdx.x * 8 + (threadIdx.x >> 5);
+// Each warp walks the G rows of 32 mask columns (one word column), 32 rows at a
+// time; after a 32x32 bit transpose lane l holds column l's bits.  The rows
+// found are staged per column in shared memory and written out 33..64 at a
+// time by the whole warp (coalesced), not one 4-byte store per lane.
+constexpr int kFillWarps = 4;
+constexpr int kFillCap = 64;             // staged entries per column
+// grid: (ceil(words / kFillWarps), nseg, B*H); pos = counts after topk_scan.
+__global__ void __launch_bounds__(kFillWarps * 32) topk_fill_kernel(const uint32_t* __restrict__ mask, int G, int nb,
+                                                                    int words, const int32_t* __restrict__ pos,
+                                                                    int32_t* __restrict__ bwd_col) {
+  __shared__ int32_t stage[kFillWarps][32][kFillCap + 1];   // +1: lanes at the same depth hit different banks
+  const int warp = threadIdx.x >> 5;
+  const int wc = blockIdx.x * kFillWarps + warp;
   if (wc >= words) return;
   const int lane = threadIdx.x & 31;
-  const long long bh = blockIdx.y;
-  const uint32_t* M = mask + bh * (long long)G * words;
+  const int seg = blockIdx.y, nseg = gridDim.y;
+  const long long bh = blockIdx.z;
+  const uint32_t* M = mask + (bh * words + wc) * (long long)G;   // this word column, rows contiguous
   const int col = wc * 32 + lane;
-  int cur = (col < nb) ? bwd_ptr[bh * nb + col] : 0;
-  for (int g0 = 0; g0 < G; g0 += 32) {
-    const int g = g0 + lane;
-    const uint32_t x = (g < G) ? M[(long long)g * words + wc] : 0u;
+  int32_t (*buf)[kFillCap + 1] = stage[warp];
+  int cur = (col < nb) ? pos[(bh * nseg + seg) * nb + col] : 0;   // next output position of this lane's column
+  int cnt = 0;                                          // staged entries of this lane's column
+  auto flush = [&](unsigned who) {
+    while (who) {
+      const int l = __ffs(who) - 1;
+      who &= who - 1u;
+      const int n = __shfl_sync(0xffffffffu, cnt, l);
+      const int base = __shfl_sync(0xffffffffu, cur, l);
+      for (int i = lane; i < n; i += 32) bwd_col[base + i] = buf[l][i];
+      if (lane == l) {
+        cur += cnt;
+        cnt = 0;
+      }
+    }
+    __syncwarp();
+  };
+  const int gs = seg * kSeg, g1 = min(G, gs + kSeg);
+  uint32_t xn = (gs + lane < g1) ? M[gs + lane] : 0u;
+  for (int g0 = gs; g0 < g1; g0 += 32) {
+    const uint32_t x = xn;
+    if (g0 + 32 < g1) xn = (g0 + 32 + lane < g1) ? M[g0 + 32 + lane] : 0u;   // next chunk in flight
     uint32_t t = warp_transpose32(x, lane);
+    flush(__ballot_sync(0xffffffffu, cnt + __popc(t) > kFillCap));
     while (t) {
       const int bit = __ffs(t) - 1;
-      bwd_col[cur++] = g0 + bit;
+      buf[lane][cnt++] = g0 + bit;
       t &= t - 1u;
     }
+    __syncwarp();
   }
+  flush(__ballot_sync(0xffffffffu, cnt > 0));
 }
 
 }  // namespace
@@ -481,7 +535,8 @@ size_t topk_ws_bytes(const dsv_shape& s) {
   const size_t G = (size_t)(s.N / s.block);
   const size_t words = (G + 31) / 32;
   const size_t bhs = (size_t)s.B * s.H;
-  return align256(bhs * G * words * sizeof(uint32_t)) + align256(bhs * G * sizeof(int32_t));
+  const size_t nseg = (G + kSeg - 1) / kSeg;
+  return align256(bhs * G * words * sizeof(uint32_t)) + align256(bhs * nseg * G * sizeof(int32_t));
 }
 
 cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk, int64_t nnz, int32_t* fwd_ptr,
@@ -513,12 +568,14 @@ cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk
   else if (G <= 256 * kKPT) topk_select_kernel<256><<<grid, 256, 0, st>>>(a);
   else topk_select_kernel<512><<<grid, 512, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  dim3 g2((unsigned)((words + 7) / 8), (unsigned)bhs);
+  const int nseg = (G + kSeg - 1) / kSeg;
+  dim3 g2((unsigned)((words + 7) / 8), (unsigned)nseg, (unsigned)bhs);
   topk_colcount_kernel<<<g2, 256, 0, st>>>(mask, G, G, words, counts);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  topk_scan_kernel<<<(unsigned)bhs, 1024, 0, st>>>(counts, a, bwd_ptr, bhs);
+  topk_scan_kernel<<<(unsigned)bhs, 1024, 0, st>>>(counts, nseg, a, bwd_ptr, bhs);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  topk_fill_kernel<<<g2, 256, 0, st>>>(mask, G, G, words, bwd_ptr, bwd_col);
+  dim3 g3((unsigned)((words + kFillWarps - 1) / kFillWarps), (unsigned)nseg, (unsigned)bhs);
+  topk_fill_kernel<<<g3, kFillWarps * 32, 0, st>>>(mask, G, G, words, counts, bwd_col);
   return cudaGetLastError();
 }
 
