@@ -61,7 +61,6 @@ struct TopkArgs {
 //   4. The set bits are written out in ascending order (prefix over chunks).
 // Per element this is a few instructions per pass and no contended atomics
 // on the leading bits, which for float scores are nearly all equal.
-constexpr int kKPT = 16;                 // keys per thread
 
 // Digit width of the radix passes: 11 bits (2048 bins) for long rows, 8 bits
 // for rows of at most 1024 keys, where clearing and scanning a large
@@ -156,8 +155,8 @@ __device__ __forceinline__ void chunk_prefix(const uint32_t* words, int nw, int3
 // Fallback (non-finite scores, all equal, or a crowded b*): MSB-first radix
 // select on the order-preserving keys below their common prefix, then equal
 // keys taken lowest index first.
-template <int RT>
-__global__ void __launch_bounds__(RT) topk_select_kernel(const __grid_constant__ TopkArgs a) {
+template <int RT, int kKPT>
+__global__ void __launch_bounds__(RT, (RT == 128 || RT == 256) ? 1024 / RT : 1) topk_select_kernel(const __grid_constant__ TopkArgs a) {
   constexpr int kBins = SelCfg<RT>::BINS;
   constexpr int kDigit = SelCfg<RT>::DIGIT;
   constexpr int NW = RT / 32;
@@ -271,15 +270,15 @@ __global__ void __launch_bounds__(RT) topk_select_kernel(const __grid_constant__
   }
 
   if (!fast) {
-    uint32_t key[kKPT];
+    // the keys are recomputed from the scores where needed (rare path, fewer registers)
     uint32_t vand = 0xffffffffu, vor = 0u;
 #pragma unroll
     for (int j = 0; j < kKPT; ++j) {
       const int i = j * RT + t;
-      key[j] = (i < nb) ? score_key(f[j]) : 0u;
       if (i < nb) {
-        vand &= key[j];
-        vor |= key[j];
+        const uint32_t kj = score_key(f[j]);
+        vand &= kj;
+        vor |= kj;
       }
     }
 #pragma unroll
@@ -313,8 +312,9 @@ __global__ void __launch_bounds__(RT) topk_select_kernel(const __grid_constant__
 #pragma unroll
       for (int j = 0; j < kKPT; ++j) {
         const int i = j * RT + t;
-        const bool in = i < nb && (key[j] & hi_mask) == prefix;
-        const uint32_t d = in ? (key[j] >> sh) & dmask : 0xffffffffu;
+        const uint32_t kj = score_key(f[j]);
+        const bool in = i < nb && (kj & hi_mask) == prefix;
+        const uint32_t d = in ? (kj >> sh) & dmask : 0xffffffffu;
         const uint32_t same = __match_any_sync(0xffffffffu, d);
         if (in && lane == __ffs(same) - 1) atomicAdd(&hist[d], (uint32_t)__popc(same));
       }
@@ -333,8 +333,9 @@ __global__ void __launch_bounds__(RT) topk_select_kernel(const __grid_constant__
     for (int j = 0; j < kKPT; ++j) {
       const int i = j * RT + t;
       const bool valid = i < nb;
-      gtw[j] = __ballot_sync(0xffffffffu, valid && key[j] > T);
-      const uint32_t e = __ballot_sync(0xffffffffu, valid && key[j] == T);
+      const uint32_t kj = score_key(f[j]);
+      gtw[j] = __ballot_sync(0xffffffffu, valid && kj > T);
+      const uint32_t e = __ballot_sync(0xffffffffu, valid && kj == T);
       if (lane == 0) eqw[j * NW + w] = e;
     }
     __syncthreads();
@@ -559,14 +560,16 @@ cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk
   a.rows = bhs * G;
   a.nnz = (int)nnz;
   a.hk = hk;
-  // threads per row: the smallest of 32 ... 512 holding the row in kKPT keys per thread
+  // threads per row: the smallest of 32 ... 512 holding the row in 16 keys per
+  // thread (32 keys per thread measured slower on 4050-block rows: half the
+  // threads per SM for the load latency)
   cudaError_t e;
   const unsigned grid = (unsigned)a.rows;
-  if (G <= 32 * kKPT) topk_select_kernel<32><<<grid, 32, 0, st>>>(a);
-  else if (G <= 64 * kKPT) topk_select_kernel<64><<<grid, 64, 0, st>>>(a);
-  else if (G <= 128 * kKPT) topk_select_kernel<128><<<grid, 128, 0, st>>>(a);
-  else if (G <= 256 * kKPT) topk_select_kernel<256><<<grid, 256, 0, st>>>(a);
-  else topk_select_kernel<512><<<grid, 512, 0, st>>>(a);
+  if (G <= 32 * 16) topk_select_kernel<32, 16><<<grid, 32, 0, st>>>(a);
+  else if (G <= 64 * 16) topk_select_kernel<64, 16><<<grid, 64, 0, st>>>(a);
+  else if (G <= 128 * 16) topk_select_kernel<128, 16><<<grid, 128, 0, st>>>(a);
+  else if (G <= 256 * 16) topk_select_kernel<256, 16><<<grid, 256, 0, st>>>(a);
+  else topk_select_kernel<512, 16><<<grid, 512, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int nseg = (G + kSeg - 1) / kSeg;
   dim3 g2((unsigned)((words + 7) / 8), (unsigned)nseg, (unsigned)bhs);
