@@ -26,7 +26,7 @@ from parity_util import (GRAD_REL_L2, LSE_MAX_ABS, O_MAX_ABS, O_REL_L2, SCORE_RE
 
 pytestmark = pytest.mark.gpu
 
-FULL = ["latent123k_global", "stress61k", "long518k"]
+FULL = ["latent16k", "latent123k_global", "stress61k", "long518k"]
 MAX_GROUPS = 48
 
 
