@@ -258,14 +258,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tmem_ld_wait();
       if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 9);
       if (warp == 5 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 6);
-      // row max as 8 independent partial maxima (short dependency chains)
+      // row max as 8 independent partial maxima (short dependency chains),
+      // two new values per three-input max
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(xr[i]);
 #pragma unroll
-      for (int j = 8; j < BETA; j += 8)
+      for (int j = 8; j < BETA; j += 16)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], __uint_as_float(xr[j + i]));
+        for (int i = 0; i < 8; ++i)
+          mx8[i] = j + 8 < BETA ? max3f(mx8[i], __uint_as_float(xr[j + i]), __uint_as_float(xr[j + 8 + i]))
+                                : fmaxf(mx8[i], __uint_as_float(xr[j + i]));
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m, mx * scale_log2);
@@ -293,19 +296,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         tmem_st_wait();
       }
-      const float neg_m = -m;
-      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // P = exp2(S c - m): exponent and row sum on packed fp32 pairs
+      const uint64_t c2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m, -m);
+      uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[BETA / 2];
 #pragma unroll
       for (int j = 0; j < BETA / 2; ++j) {
-        const float x0 = fmaf(__uint_as_float(xr[2 * j]), scale_log2, neg_m);
-        const float x1 = fmaf(__uint_as_float(xr[2 * j + 1]), scale_log2, neg_m);
+        float x0, x1;
+        f2_unpack(fma2(f2_pack(__uint_as_float(xr[2 * j]), __uint_as_float(xr[2 * j + 1])), c2, nm2), x0, x1);
         const float p0 = ex2(x0);
         const float p1 = ex2(x1);
-        rs8[j & 7] += p0 + p1;
+        rs2[j & 3] = add2(rs2[j & 3], f2_pack(p0, p1));
         pk[j] = pack_bf16x2(p0, p1);
       }
-      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      {
+        float a0, a1;
+        f2_unpack(add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3])), a0, a1);
+        l += a0 + a1;
+      }
       if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 10);
       if (warp == 5 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 7);
 #pragma unroll
