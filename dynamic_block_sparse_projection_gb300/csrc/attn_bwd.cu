@@ -46,7 +46,7 @@ constexpr int kQThreads = 352;         // q kernel: 3 control warps + 8 compute 
 constexpr int kComputeThreads = 256;
 
 // ---------------------------------------------------------------------------
-// Pre-pass: D_i = sum_c dO_ic O_ic and lse_i * log2(e) for the main kernels.
+// Pre-pass: D_i = sum_c dO_ic O_ic and -lse_i * log2(e) for the main kernels.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ O,
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __nv_bfloat16* __
   for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (row < rows && c == 0) {
     Dw[row] = acc;
-    L2w[row] = lse[row] * kLog2e;
+    L2w[row] = -lse[row] * kLog2e;
   }
 }
 
@@ -93,7 +93,7 @@ struct KVTraits {
   static constexpr int B_CHUNK = BETA * 128;       // Q_g / dO_g tiles
   static constexpr int B_BYTES = NCH * B_CHUNK;
   static constexpr int NST = 2;
-  static constexpr int VEC_BYTES = BETA * 4;       // lse2_g or D_g
+  static constexpr int VEC_BYTES = BETA * 4;       // -lse2_g or D_g
   static constexpr int STAGE_BYTES = (2 * B_BYTES + 2 * VEC_BYTES + 1023) / 1024 * 1024;  // keeps tiles 1024-aligned
   static constexpr int NBAR = 1 + 2 * NST + 5;
   static constexpr int SMEM_USED = 1024 + 2 * A_BYTES + NST * STAGE_BYTES + NBAR * 8 + 16;
@@ -341,20 +341,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         if (warp == 2 && lane == 0 && h == 0) DSV_TRACE_POINT(g_trace_kv, n, 5);
         uint32_t pw[W / 2], dw[W / 2];
+        const uint64_t c2 = f2_pack(scale_log2, scale_log2);
 #pragma unroll
         for (int q = 0; q < W / 4; ++q) {
-          const float4 L = l4[q], Dd = d4[q];
-          const float Lv[4] = {L.x, L.y, L.z, L.w}, Dv[4] = {Dd.x, Dd.y, Dd.z, Dd.w};
-          float p[4], ds[4];
+          const float4 L = l4[q], Dd = d4[q];   // -lse*log2(e) and D of four queries
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            p[e] = ex2(fmaf(__uint_as_float(xs[4 * q + e]), scale_log2, -Lv[e]));
-            ds[e] = p[e] * (__uint_as_float(xp[4 * q + e]) - Dv[e]);
+          for (int e = 0; e < 2; ++e) {
+            // exponent, dP - D and dS on packed fp32 pairs
+            const int i0 = 4 * q + 2 * e;
+            float x0, x1, d0, d1;
+            f2_unpack(fma2(f2_pack(__uint_as_float(xs[i0]), __uint_as_float(xs[i0 + 1])), c2,
+                           e ? f2_pack(L.z, L.w) : f2_pack(L.x, L.y)), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            const uint64_t t = sub2(f2_pack(__uint_as_float(xp[i0]), __uint_as_float(xp[i0 + 1])),
+                                    e ? f2_pack(Dd.z, Dd.w) : f2_pack(Dd.x, Dd.y));
+            f2_unpack(mul2(f2_pack(p0, p1), t), d0, d1);
+            pw[2 * q + e] = pack_bf16x2(p0, p1);
+            dw[2 * q + e] = pack_bf16x2(d0, d1);
           }
-          pw[2 * q] = pack_bf16x2(p[0], p[1]);
-          pw[2 * q + 1] = pack_bf16x2(p[2], p[3]);
-          dw[2 * q] = pack_bf16x2(ds[0], ds[1]);
-          dw[2 * q + 1] = pack_bf16x2(ds[2], ds[3]);
         }
         if (warp == 2 && lane == 0 && h == 0) DSV_TRACE_POINT(g_trace_kv, n, 6);
         // each warp overwrites only the TMEM lanes and columns it has just read
@@ -621,7 +625,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int r = sp * 32 + lane;
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     const float scale_log2 = scale * kLog2e;
-    const float lse2 = (r < BETA) ? L2w[qrow0 + r] : 0.f;
+    const float nlse2 = (r < BETA) ? L2w[qrow0 + r] : 0.f;   // -lse*log2(e)
     const float dd = (r < BETA) ? Dw[qrow0 + r] : 0.f;
     {
       // row r of Q_g into TMEM (this warp's half of its D/2 columns), as the A
@@ -660,12 +664,17 @@ __global__ void __launch_bounds__(kQThreads, 1)
       if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 5);
       tc_fence_before();
       mbar_arrive(sp_free);
+      // exponent, dP - D and dS on packed fp32 pairs
       uint32_t dw[HALF / 2];
+      const uint64_t c2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(nlse2, nlse2), dd2 = f2_pack(dd, dd);
 #pragma unroll
       for (int i = 0; i < HALF / 2; ++i) {
-        const float p0 = ex2(fmaf(__uint_as_float(xs[2 * i]), scale_log2, -lse2));
-        const float p1 = ex2(fmaf(__uint_as_float(xs[2 * i + 1]), scale_log2, -lse2));
-        dw[i] = pack_bf16x2(p0 * (__uint_as_float(xp[2 * i]) - dd), p1 * (__uint_as_float(xp[2 * i + 1]) - dd));
+        float x0, x1, d0, d1;
+        f2_unpack(fma2(f2_pack(__uint_as_float(xs[2 * i]), __uint_as_float(xs[2 * i + 1])), c2, nl2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        const uint64_t t = sub2(f2_pack(__uint_as_float(xp[2 * i]), __uint_as_float(xp[2 * i + 1])), dd2);
+        f2_unpack(mul2(f2_pack(p0, p1), t), d0, d1);
+        dw[i] = pack_bf16x2(d0, d1);
       }
       if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 6);
       // the single dS buffer is free once dQ of the previous block is done
@@ -745,7 +754,7 @@ cudaError_t launch_q_t(const void* Q, const CUtensorMap& tmK, const CUtensorMap&
   return cudaGetLastError();
 }
 
-// workspace: D_i, then lse_i * log2(e), each B*H*N floats (256-byte aligned)
+// workspace: D_i, then -lse_i * log2(e), each B*H*N floats (256-byte aligned)
 const float* ws_D(const void* ws) { return static_cast<const float*>(ws); }
 const float* ws_L2(const void* ws, const dsv_shape& s) {
   return reinterpret_cast<const float*>(static_cast<const char*>(ws) +
@@ -755,7 +764,7 @@ const float* ws_L2(const void* ws, const dsv_shape& s) {
 }  // namespace
 
 size_t attn_bwd_ws_bytes(const dsv_shape& s) {
-  return 2 * align256((size_t)s.B * s.H * s.N * sizeof(float));  // D and lse*log2(e)
+  return 2 * align256((size_t)s.B * s.H * s.N * sizeof(float));  // D and -lse*log2(e)
 }
 
 cudaError_t launch_attn_bwd_pre(const void* O, const void* dO, const float* lse, const dsv_shape& s, void* ws,

@@ -170,7 +170,7 @@ dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, cons
  * with the ordering made explicit) they give results bitwise equal to the
  * single call, and dsv_attn_bwd_dkdv / dsv_attn_bwd_dq may run in either
  * order once the preprocess is done.  Arguments mean what they mean above.
- *   dsv_attn_bwd_preprocess  D_i and lse_i * log2(e) into the workspace.
+ *   dsv_attn_bwd_preprocess  D_i and -lse_i * log2(e) into the workspace.
  *   dsv_attn_bwd_dkdv        dK, dV (one CTA per key block, transposed lists).
  *   dsv_attn_bwd_dq          dQ (one CTA per query group, forward lists).
  * Errors as for dsv_sparse_attn_bwd; a stage does not check that the
