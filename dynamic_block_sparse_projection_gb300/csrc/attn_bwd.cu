@@ -662,6 +662,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       }
       tmem_ld_wait();
       if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 5);
+      if (warp > 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 6 + warp);
       tc_fence_before();
       mbar_arrive(sp_free);
       // exponent, dP - D and dS on packed fp32 pairs

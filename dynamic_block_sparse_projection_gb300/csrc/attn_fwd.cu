@@ -216,12 +216,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (ok && cnt > 1) ok = issue_S(1);
     for (int n = 0; ok && n < cnt; ++n) {
       // S(n+2) reuses the buffer of P(n-1), whose PV product is already queued
-      if (n + 2 < cnt && !issue_S(n + 2)) break;
       const int s = n % NST;
       const uint32_t ph = (uint32_t)(n / NST) & 1u;
+      const uint32_t v_tested = mbar_test(&v_full[s], ph);   // V_n normally landed long ago
+      if (n + 2 < cnt && !issue_S(n + 2)) break;
       if (!mbar_wait_warp(&p_full[s], ph, abort_flag, ctl, kid | W_P)) break;
       DSV_TRACE_POINT(g_trace_fwd, n, 3);
-      if (!mbar_wait_warp(&v_full[s], ph, abort_flag, ctl, kid | W_V)) break;
+      if (!mbar_wait_warp_tested(&v_full[s], ph, v_tested, abort_flag, ctl, kid | W_V)) break;
       DSV_TRACE_POINT(g_trace_fwd, n, 4);
       tc_fence_after();
       const uint32_t p_tmem = tmem + (uint32_t)s * T::S_COL;
@@ -243,9 +244,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    uint32_t s_tested = 0u;   // S(n) already known complete (tested during block n-1)
     for (int n = 0; n < cnt; ++n) {
       const int s = n % NST;
-      if (!mbar_wait_warp(&s_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_S)) {
+      if (!mbar_wait_warp_tested(&s_full[s], (uint32_t)(n / NST) & 1u, s_tested, abort_flag, ctl, kid | W_S)) {
         ok = false;
         break;
       }
@@ -255,6 +257,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       uint32_t xr[BETA];
 #pragma unroll
       for (int c = 0; c < BETA / 32; ++c) tmem_ld32(sb + c * 32, xr + c * 32);
+      s_tested = (n + 1 < cnt) ? mbar_test(&s_full[(n + 1) % NST], (uint32_t)((n + 1) / NST) & 1u) : 0u;
       tmem_ld_wait();
       if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 9);
       if (warp == 5 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 6);

@@ -112,6 +112,27 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// A wait costs a shared-memory round trip (~90 clocks measured) even when the
+// phase is long complete.  Where the next wait is known early, its test is
+// issued early (mbar_test, non-blocking) and consumed at the wait
+// (mbar_wait_warp_tested), so the round trip overlaps other work.
+__device__ __forceinline__ uint32_t mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok;
+}
+__device__ __forceinline__ bool mbar_wait_warp_tested(uint64_t* bar, uint32_t parity, uint32_t tested,
+                                                      volatile int* abort, const Ctl& ctl, unsigned int where) {
+  if (__all_sync(0xffffffffu, tested != 0u)) return true;
+  return mbar_wait_warp(bar, parity, abort, ctl, where);
+}
+
 // ---------------------------------------------------------------------------
 // TMA (tiled tensor copies global -> shared, completion on an mbarrier)
 // ---------------------------------------------------------------------------
