@@ -287,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int n = 0; ok && n < cnt; ++n) {
         DSV_TRACE_POINT(g_trace_kv, n, 0);
+        const uint32_t tg = n + 1 < cnt ? mbar_test(&g_full[(n + 1) % NST], (uint32_t)((n + 1) / NST) & 1u) : 0u;
         issue_sdp(n, 1);
         DSV_TRACE_POINT(g_trace_kv, n, 1);
         if (!mbar_wait_warp(&p_full[0], (uint32_t)n & 1u, abort_flag, ctl, kid | W_P)) break;
@@ -295,7 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_grad(n, 0);
         if (n + 1 < cnt) {
           const int s1 = (n + 1) % NST;
-          if (!mbar_wait_warp(&g_full[s1], (uint32_t)((n + 1) / NST) & 1u, abort_flag, ctl, kid | W_GFULL)) break;
+          if (!mbar_wait_warp_tested(&g_full[s1], (uint32_t)((n + 1) / NST) & 1u, tg, abort_flag, ctl, kid | W_GFULL))
+            break;
           tc_fence_after();
           issue_sdp(n + 1, 0);
         }
@@ -316,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     const float scale_log2 = scale * kLog2e;
     bool ok = true;
+    uint32_t s_tested = 0u;
     for (int n = 0; ok && n < cnt; ++n) {
       const int s = n % NST;
       if (!mbar_wait_warp(&g_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_GFULL)) {
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
-        if (!mbar_wait_warp(&s_full[h], (uint32_t)n & 1u, abort_flag, ctl, kid | W_S)) {
+        if (!mbar_wait_warp_tested(&s_full[h], (uint32_t)n & 1u, s_tested, abort_flag, ctl, kid | W_S)) {
           ok = false;
           break;
         }
@@ -335,6 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t xs[W], xp[W];
         tmem_ld_w<W>(cs, xs);
         tmem_ld_w<W>(cp, xp);
+        // the next half: (n, 1) after (n, 0), (n + 1, 0) after (n, 1)
+        s_tested = (h == 0 || n + 1 < cnt) ? mbar_test(&s_full[h ^ 1], (uint32_t)(n + h) & 1u) : 0u;
         const int q0 = h * HALF + hf * W;            // first query of this warp's columns
         const float4* l4 = reinterpret_cast<const float4*>(sStage + s * T::STAGE_BYTES + 2 * T::B_BYTES) + q0 / 4;
         const float4* d4 = l4 + BETA / 4;
@@ -565,9 +570,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t dKmn0 = sdesc_sw128(smem_u32(sK), T::KV_CHUNK, 1024);
-      auto issue_sdp = [&](int n) -> bool {
+      // tk / tv: early tests of K_n / V_n (see mbar_test); td: of dS of block n-1
+      auto issue_sdp = [&](int n, uint32_t tk, uint32_t tv, uint32_t* td) -> bool {
         const int sk = n % NK, sv = n % NV;
-        if (!mbar_wait_warp(&k_full[sk], (uint32_t)(n / NK) & 1u, abort_flag, ctl, kid | W_KFULL)) return false;
+        if (!mbar_wait_warp_tested(&k_full[sk], (uint32_t)(n / NK) & 1u, tk, abort_flag, ctl, kid | W_KFULL))
+          return false;
         tc_fence_after();
         const uint64_t kb = desc_off(dK0, (uint32_t)sk * T::KV_BYTES);
 #pragma unroll
@@ -576,7 +583,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
           const uint32_t bo = (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32;
           mma_ts_w(tmem + T::S_COL, tmem + T::Q_COL + kk * 8, desc_off(kb, bo), ID_S, kk > 0 ? 1u : 0u);
         }
-        if (!mbar_wait_warp(&v_full[sv], (uint32_t)(n / NV) & 1u, abort_flag, ctl, kid | W_VFULL)) return false;
+        if (td != nullptr) *td = mbar_test(ds_full, (uint32_t)(n - 1) & 1u);
+        if (!mbar_wait_warp_tested(&v_full[sv], (uint32_t)(n / NV) & 1u, tv, abort_flag, ctl, kid | W_VFULL))
+          return false;
         tc_fence_after();
         const uint64_t vb = desc_off(dV0, (uint32_t)sv * T::KV_BYTES);
 #pragma unroll
@@ -591,17 +600,20 @@ __global__ void __launch_bounds__(kQThreads, 1)
       };
       bool ok = mbar_wait_warp(qd_full, 0, abort_flag, ctl, kid | W_KV) &&
                 mbar_wait_warp(q_tm, 0, abort_flag, ctl, kid | W_KV);
-      if (ok) ok = issue_sdp(0);
+      if (ok) ok = issue_sdp(0, 0u, 0u, nullptr);
       for (int n = 0; ok && n < cnt; ++n) {
         DSV_TRACE_POINT(g_trace_q, n, 0);
+        uint32_t td = 0u;
         if (n + 1 < cnt) {
+          const uint32_t tk = mbar_test(&k_full[(n + 1) % NK], (uint32_t)((n + 1) / NK) & 1u);
+          const uint32_t tv = mbar_test(&v_full[(n + 1) % NV], (uint32_t)((n + 1) / NV) & 1u);
           // S and dP are single-buffered: overwrite them once the compute warps hold block n
           if (!mbar_wait_warp(sp_free, (uint32_t)n & 1u, abort_flag, ctl, kid | W_SPFREE)) break;
           tc_fence_after();
-          if (!issue_sdp(n + 1)) break;
+          if (!issue_sdp(n + 1, tk, tv, &td)) break;
         }
         DSV_TRACE_POINT(g_trace_q, n, 1);
-        if (!mbar_wait_warp(ds_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_DSFULL)) break;
+        if (!mbar_wait_warp_tested(ds_full, (uint32_t)n & 1u, td, abort_flag, ctl, kid | W_DSFULL)) break;
         DSV_TRACE_POINT(g_trace_q, n, 2);
         tc_fence_after();
         const int s = n % NK;
@@ -647,8 +659,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
       mbar_arrive(q_tm);
     }
     bool ok = true;
+    uint32_t s_tested = 0u;
     for (int n = 0; n < cnt; ++n) {
-      if (!mbar_wait_warp(s_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_S)) {
+      if (!mbar_wait_warp_tested(s_full, (uint32_t)n & 1u, s_tested, abort_flag, ctl, kid | W_S)) {
         ok = false;
         break;
       }
@@ -665,6 +678,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       if (warp > 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 6 + warp);
       tc_fence_before();
       mbar_arrive(sp_free);
+      const uint32_t e_tested = mbar_test(ds_empty, ((uint32_t)n & 1u) ^ 1u);
       // exponent, dP - D and dS on packed fp32 pairs
       uint32_t dw[HALF / 2];
       const uint64_t c2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(nlse2, nlse2), dd2 = f2_pack(dd, dd);
@@ -679,7 +693,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
       }
       if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 6);
       // the single dS buffer is free once dQ of the previous block is done
-      if (!mbar_wait_warp(ds_empty, ((uint32_t)n & 1u) ^ 1u, abort_flag, ctl, kid | W_DSEMPTY)) {
+      if (n + 1 < cnt) s_tested = mbar_test(s_full, (uint32_t)(n + 1) & 1u);
+      if (!mbar_wait_warp_tested(ds_empty, ((uint32_t)n & 1u) ^ 1u, e_tested, abort_flag, ctl, kid | W_DSEMPTY)) {
         ok = false;
         break;
       }
