@@ -205,7 +205,7 @@ class HotPath:
                           workspace=self.ws_b)
 
 
-KERNELS_PER_STEP = {"predict": 2, "topk": 4, "fwd": 1, "bwd_pre": 1, "bwd_kv": 1, "bwd_q": 1}
+KERNELS_PER_STEP = {"predict": 2, "topk": 4, "fwd": 1, "bwd_pre": 1, "bwd_kv": 2, "bwd_q": 1}
 STAGES = ("predict", "topk", "fwd", "bwd_pre", "bwd_kv", "bwd_q")
 
 

@@ -115,8 +115,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const float* __restrict__ L2w, const float* __restrict__ Dw,
-                       const int32_t* __restrict__ bwd_ptr, const int32_t* __restrict__ bwd_col, int N, int G,
-                       float scale, __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, Ctl ctl) {
+                       const int32_t* __restrict__ bwd_ptr, const int32_t* __restrict__ bwd_col,
+                       const int32_t* __restrict__ order, int N, int G, float scale,
+                       __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, Ctl ctl) {
   using T = KVTraits<BETA, D>;
   constexpr int NST = T::NST;
   constexpr int HALF = T::HALF;
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   DSV_TRACE_INIT;
-  const long long row = blockIdx.x;               // (b*H + h)*nb + j
+  const long long row = order[blockIdx.x];        // (b*H + h)*nb + j, longest transposed lists first
   const int nb = G;
   const long long bh = row / nb;
   const int j = (int)(row - bh * nb);
@@ -735,20 +736,85 @@ __global__ void __launch_bounds__(kQThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, T::TMEM_COLS);
 }
 
+// Key blocks in order of decreasing transposed-list length within chunks of
+// consecutive (b, h) slices (counting sort by length, one CTA per chunk).
+// Chunks keep their order and hold as many heads as leave their Q and dO in
+// a part of L2, so the blocks running together share them; within a chunk
+// the long blocks start first and the grid's last wave holds short ones.
+// Ties in any order: a block's result does not depend on when it runs.
+constexpr int kOrderThreads = 256;
+constexpr int kMaxOrderLen = kMaxBlocksPerRow;   // a list holds at most G groups
+__global__ void __launch_bounds__(kOrderThreads) kv_order_kernel(const int32_t* __restrict__ bwd_ptr,
+                                                                 long long rows, int chunk, int maxlen,
+                                                                 int32_t* __restrict__ order) {
+  __shared__ int32_t cnt[kMaxOrderLen + 1];
+  __shared__ int32_t wtot[kOrderThreads / 32];
+  const long long base = (long long)blockIdx.x * chunk;
+  const int nb = (int)(rows - base < chunk ? rows - base : chunk);   // rows of this chunk
+  const int32_t* P = bwd_ptr + base;
+  for (int i = threadIdx.x; i <= maxlen; i += kOrderThreads) cnt[i] = 0;
+  __syncthreads();
+  for (int r = threadIdx.x; r < nb; r += kOrderThreads) atomicAdd(&cnt[min(maxlen, max(0, P[r + 1] - P[r]))], 1);
+  __syncthreads();
+  // exclusive scan from the longest length down: start[len] = blocks with a longer list
+  const int per = (maxlen + 1 + kOrderThreads - 1) / kOrderThreads;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int b0 = t * per;            // this thread's lengths, counted from the top: maxlen - b0 ...
+  int loc = 0;
+  for (int q = b0; q < min(maxlen + 1, b0 + per); ++q) loc += cnt[maxlen - q];
+  int inc = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) wtot[w] = inc;
+  __syncthreads();
+  if (w == 0) {
+    int x = lane < kOrderThreads / 32 ? wtot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += v;
+    }
+    if (lane < kOrderThreads / 32) wtot[lane] = x;
+  }
+  __syncthreads();
+  int run = (w > 0 ? wtot[w - 1] : 0) + inc - loc;
+  for (int q = b0; q < min(maxlen + 1, b0 + per); ++q) {
+    const int c = cnt[maxlen - q];
+    cnt[maxlen - q] = run;
+    run += c;
+  }
+  __syncthreads();
+  for (int r = threadIdx.x; r < nb; r += kOrderThreads)
+    order[base + atomicAdd(&cnt[min(maxlen, max(0, P[r + 1] - P[r]))], 1)] = (int32_t)(base + r);
+}
+
 template <int BETA, int D>
 cudaError_t launch_kv_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                         const CUtensorMap& tmdO, const dsv_shape& s, const int32_t* bwd_ptr, const int32_t* bwd_col,
-                        float scale, void* dK, void* dV, const float* Dw, const float* L2w, const Ctl& ctl,
-                        cudaStream_t st) {
+                        float scale, void* dK, void* dV, const float* Dw, const float* L2w, int32_t* order,
+                        const Ctl& ctl, cudaStream_t st) {
   const int G = s.N / s.block;
   const long long groups = (long long)s.B * s.H * G;
+  // heads per chunk: their Q and dO within ~48 MB of L2
+  const long long head_bytes = 2LL * s.N * s.d * 2;
+  const long long heads = (long long)s.B * s.H;
+  long long hpc = (48LL << 20) / (head_bytes > 0 ? head_bytes : 1);
+  hpc = hpc < 1 ? 1 : (hpc > heads ? heads : hpc);
+  const long long chunk = hpc * G;
+  kv_order_kernel<<<(unsigned)((groups + chunk - 1) / chunk), kOrderThreads, 0, st>>>(
+      bwd_ptr, groups, (int)chunk, G < kMaxOrderLen ? G : kMaxOrderLen, order);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   auto kv = attn_bwd_kv_kernel<BETA, D>;
-  cudaError_t e;
   if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KVTraits<BETA, D>::SMEM)) !=
       cudaSuccess)
     return e;
   kv<<<(unsigned)groups, kThreads, KVTraits<BETA, D>::SMEM, st>>>(tmQ, tmK, tmV, tmdO, L2w, Dw, bwd_ptr, bwd_col,
-                                                                   s.N, G, scale, static_cast<__nv_bfloat16*>(dK),
+                                                                   order, s.N, G, scale,
+                                                                   static_cast<__nv_bfloat16*>(dK),
                                                                    static_cast<__nv_bfloat16*>(dV), ctl);
   return cudaGetLastError();
 }
@@ -770,17 +836,23 @@ cudaError_t launch_q_t(const void* Q, const CUtensorMap& tmK, const CUtensorMap&
   return cudaGetLastError();
 }
 
-// workspace: D_i, then -lse_i * log2(e), each B*H*N floats (256-byte aligned)
+// workspace: D_i, then -lse_i * log2(e), each B*H*N floats, then the dK/dV
+// kernel's block order (B*H*nb ints), each part 256-byte aligned
 const float* ws_D(const void* ws) { return static_cast<const float*>(ws); }
 const float* ws_L2(const void* ws, const dsv_shape& s) {
   return reinterpret_cast<const float*>(static_cast<const char*>(ws) +
                                         align256((size_t)s.B * s.H * s.N * sizeof(float)));
 }
+int32_t* ws_order(const void* ws, const dsv_shape& s) {
+  return reinterpret_cast<int32_t*>(const_cast<char*>(static_cast<const char*>(ws)) +
+                                    2 * align256((size_t)s.B * s.H * s.N * sizeof(float)));
+}
 
 }  // namespace
 
 size_t attn_bwd_ws_bytes(const dsv_shape& s) {
-  return 2 * align256((size_t)s.B * s.H * s.N * sizeof(float));  // D and -lse*log2(e)
+  return 2 * align256((size_t)s.B * s.H * s.N * sizeof(float)) +   // D and -lse*log2(e)
+         align256((size_t)s.B * s.H * (s.N / s.block) * sizeof(int32_t));   // dK/dV block order
 }
 
 cudaError_t launch_attn_bwd_pre(const void* O, const void* dO, const float* lse, const dsv_shape& s, void* ws,
@@ -802,10 +874,11 @@ cudaError_t launch_attn_bwd_pre(const void* O, const void* dO, const float* lse,
 
 cudaError_t launch_attn_bwd_kv(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const CUtensorMap& tmdO, const dsv_shape& s, const int32_t* bwd_ptr,
-                               const int32_t* bwd_col, float scale, void* dK, void* dV, const void* ws,
+                               const int32_t* bwd_col, float scale, void* dK, void* dV, void* ws,
                                const Ctl& ctl, cudaStream_t st) {
 #define DSV_KV(BE, DD) \
-  return launch_kv_t<BE, DD>(tmQ, tmK, tmV, tmdO, s, bwd_ptr, bwd_col, scale, dK, dV, ws_D(ws), ws_L2(ws, s), ctl, st)
+  return launch_kv_t<BE, DD>(tmQ, tmK, tmV, tmdO, s, bwd_ptr, bwd_col, scale, dK, dV, ws_D(ws), ws_L2(ws, s), \
+                             ws_order(ws, s), ctl, st)
   if (s.block == 128 && s.d == 128) DSV_KV(128, 128);
   if (s.block == 128 && s.d == 64) DSV_KV(128, 64);
   if (s.block == 64 && s.d == 128) DSV_KV(64, 128);

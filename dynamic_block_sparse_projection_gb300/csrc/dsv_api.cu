@@ -264,7 +264,7 @@ dsv_status dsv_attn_bwd_preprocess(const void* O, const void* dO, const float* l
 
 dsv_status dsv_attn_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO, dsv_shape s,
                              const int32_t* bwd_ptr, const int32_t* bwd_col, float softmax_scale, void* dK, void* dV,
-                             const void* workspace, size_t workspace_bytes, dsv_stream_t stream) {
+                             void* workspace, size_t workspace_bytes, dsv_stream_t stream) {
   dsv_status v = check_shape(s, false);
   if (v != DSV_OK) return v;
   if (empty(s)) return DSV_OK;

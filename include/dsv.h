@@ -155,7 +155,8 @@ dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const void* V, dsv_
  *
  * Q, K, V, O, dO bf16 [B,H,N,d]; lse fp32 [B,H,N] from the forward.
  * dQ, dK, dV bf16 [B,H,N,d]; overwritten.
- * workspace >= dsv_attn_bwd_workspace_bytes(s) bytes, 256-byte aligned (holds D).
+ * workspace >= dsv_attn_bwd_workspace_bytes(s) bytes, 256-byte aligned: D_i,
+ * -lse_i*log2(e) and the dK/dV kernel's block order.
  * ------------------------------------------------------------------------ */
 size_t dsv_attn_bwd_workspace_bytes(dsv_shape s);
 dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, const void* O,
@@ -171,7 +172,9 @@ dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, cons
  * single call, and dsv_attn_bwd_dkdv / dsv_attn_bwd_dq may run in either
  * order once the preprocess is done.  Arguments mean what they mean above.
  *   dsv_attn_bwd_preprocess  D_i and -lse_i * log2(e) into the workspace.
- *   dsv_attn_bwd_dkdv        dK, dV (one CTA per key block, transposed lists).
+ *   dsv_attn_bwd_dkdv        dK, dV (one CTA per key block, transposed lists, the
+ *                            blocks with the longest lists first; the order is
+ *                            kept in the workspace's last part).
  *   dsv_attn_bwd_dq          dQ (one CTA per query group, forward lists).
  * Errors as for dsv_sparse_attn_bwd; a stage does not check that the
  * preprocess ran. */
@@ -179,7 +182,7 @@ dsv_status dsv_attn_bwd_preprocess(const void* O, const void* dO, const float* l
                                    void* workspace, size_t workspace_bytes, dsv_stream_t stream);
 dsv_status dsv_attn_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO, dsv_shape s,
                              const int32_t* bwd_ptr, const int32_t* bwd_col, float softmax_scale,
-                             void* dK, void* dV, const void* workspace, size_t workspace_bytes,
+                             void* dK, void* dV, void* workspace, size_t workspace_bytes,
                              dsv_stream_t stream);
 dsv_status dsv_attn_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, dsv_shape s,
                            const int32_t* fwd_ptr, const int32_t* fwd_col, float softmax_scale,
