@@ -4,13 +4,16 @@ The whole hot path runs at the benchmark's sizes and launch configuration;
 the fp64 oracle then checks what it can evaluate one item at a time:
 
   scores    rows S[b,h,g,:] of sampled groups against the oracle's per-row form
-  lists     sampled forward rows bit-exact against the oracle's top-k fed the
-            GPU's own fp32 scores of that row; for sampled heads the whole
-            transposed CSR equal to the oracle's transpose of the GPU lists
-  forward   O and lse of sampled groups against the per-group oracle
-  backward  dQ of sampled groups and dK/dV of sampled key blocks (the most
-            selected block of the head, a random one and the least selected)
-            against the per-group / per-block oracle forms, on the GPU lists
+  lists     every forward row bit-exact against the oracle's top-k fed the
+            GPU's own fp32 scores (long518k: 64 rows per sampled head); for
+            sampled heads the whole transposed CSR equal to the oracle's
+            transpose of the GPU lists
+  forward   O and lse of 16 sampled groups in each of 4 sampled heads against
+            the per-group oracle
+  backward  dQ of the same groups and dK/dV of up to 8 sampled key blocks per
+            head (the least selected, the most selected with at most
+            MAX_GROUPS groups, random ones) against the per-group / per-block
+            oracle forms, on the GPU lists
 
 The oracle sees one (b, h) slice at a time, as fp32 copies of the bf16 inputs
 (exact), with the CSR rows of that slice re-based to (0, 0).
@@ -64,12 +67,25 @@ def test_full_size_sampled_parity(dsv, name):
     fpn, fcn = fp.cpu().numpy().astype(np.int64), fc.cpu().numpy().astype(np.int64)
     bpn, bcn = bp.cpu().numpy().astype(np.int64), bc.cpu().numpy().astype(np.int64)
     rng = np.random.default_rng(97 + w.seed)
-    heads = sorted({(0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))})
+    heads = {(0, 0), (w.B - 1, w.H - 1)}
+    while len(heads) < min(4, w.B * w.H):
+        heads.add((int(rng.integers(w.B)), int(rng.integers(w.H))))
+    heads = sorted(heads)
+    checked = {"O": [], "dQ": [], "dK": [], "dV": []}
+
+    # lists bit-exact on every row of the smaller workloads (a sample of rows at long518k)
+    if w.B * w.H * G * G <= 64 << 20:
+        Sn = S.cpu().numpy()
+        for b in range(w.B):
+            for h in range(w.H):
+                hp_, hc_ = _head_csr(fpn, fcn, b * w.H + h, G)
+                ref = oracle.topk_lists(Sn[b:b + 1, h:h + 1], [x.k_per_head[h]])
+                assert np.array_equal(hp_, ref[0]) and np.array_equal(hc_, ref[1]), f"lists {name} head {(b, h)}"
     for (b, h) in heads:
         bh = b * w.H + h
         Qh, Kh, Vh, dOh = (_f32(t[b, h]) for t in (x.Q, x.K, x.V, x.dO))
         Wq, Wk = x.Wq[h:h + 1].double().cpu().numpy(), x.Wk[h:h + 1].double().cpu().numpy()
-        groups = sorted({0, G - 1, int(rng.integers(G))})
+        groups = sorted({0, G - 1} | {int(v) for v in rng.integers(G, size=14)})
         hp, hc = _head_csr(fpn, fcn, bh, G)
 
         # scores: sampled rows
@@ -80,7 +96,7 @@ def test_full_size_sampled_parity(dsv, name):
         # forward lists: the oracle's top-k on the GPU's scores of the same rows
         k = int(x.k_per_head[h])
         rows_gpu = S[b, h].double().cpu().numpy()
-        for g in list(groups) + [int(v) for v in rng.integers(G, size=16)]:
+        for g in list(groups) + [int(v) for v in rng.integers(G, size=64)]:
             assert np.array_equal(hc[hp[g]:hp[g + 1]], oracle.topk_row(rows_gpu[g], k)), (name, b, h, g)
 
         # transposed CSR of the head: the oracle's transpose of the GPU lists
@@ -93,15 +109,15 @@ def test_full_size_sampled_parity(dsv, name):
                                                                      rows=[(0, 0, g) for g in groups])):
             sl = slice(g * w.block, (g + 1) * w.block)
             o = O[b, h, sl].double().cpu().numpy()
-            assert rel_l2(o, o_ref) <= O_REL_L2
+            checked["O"].append((o, o_ref))
             assert max_abs_beyond_rounding(o, o_ref) <= O_MAX_ABS
             assert np.max(np.abs(lse[b, h, sl].double().cpu().numpy() - l_ref)) <= LSE_MAX_ABS
 
-        # backward: dQ of sampled groups
+        # backward: dQ of sampled groups (rel-L2 over all checked elements, below)
         for g, dq_ref in zip(groups, oracle.attn_bwd_dq_rows(Qh, Kh, Vh, dOh, hp, hc, w.block,
                                                               [(0, 0, g) for g in groups])):
             sl = slice(g * w.block, (g + 1) * w.block)
-            assert rel_l2(dQ[b, h, sl].double().cpu().numpy(), dq_ref) <= GRAD_REL_L2, f"dQ {name} {(b, h, g)}"
+            checked["dQ"].append((dQ[b, h, sl].double().cpu().numpy(), dq_ref))
 
         # backward: dK, dV of sampled key blocks.  The per-block oracle redoes
         # the whole softmax of every group in the block's list, so only blocks
@@ -112,7 +128,7 @@ def test_full_size_sampled_parity(dsv, name):
         cheap = np.nonzero((lens > 0) & (lens <= MAX_GROUPS))[0]
         blocks = {int(np.argmin(lens))}
         if cheap.size:
-            blocks |= {int(cheap[np.argmax(lens[cheap])]), int(rng.choice(cheap))}
+            blocks |= {int(cheap[np.argmax(lens[cheap])])} | {int(v) for v in rng.choice(cheap, size=6)}
         blocks = sorted(blocks)
         for j, (dk_ref, dv_ref) in zip(blocks, oracle.attn_bwd_kv_blocks(Qh, Kh, Vh, dOh, hp, hc, gp, gc, w.block,
                                                                           [(0, 0, j) for j in blocks])):
@@ -122,8 +138,8 @@ def test_full_size_sampled_parity(dsv, name):
             if lens[j] == 0:
                 assert np.all(dk == 0) and np.all(dv == 0)
             else:
-                assert rel_l2(dk, dk_ref) <= GRAD_REL_L2, f"dK {name} {(b, h, j)}"
-                assert rel_l2(dv, dv_ref) <= GRAD_REL_L2, f"dV {name} {(b, h, j)}"
+                checked["dK"].append((dk, dk_ref))
+                checked["dV"].append((dv, dv_ref))
 
         # gradient sums over every key of the head: each query's softmax row sums
         # to one, so sum_keys dV = sum_queries dO and sum_keys dK = 0 (every
@@ -131,3 +147,13 @@ def test_full_size_sampled_parity(dsv, name):
         dKs = dK[b, h].double().sum(dim=0)
         assert torch.all(dKs.abs() <= 2e-2 * dK[b, h].double().abs().sum(dim=0) + 1e-3)
         assert rel_l2(dV[b, h].double().sum(dim=0).cpu().numpy(), x.dO[b, h].double().sum(dim=0).cpu().numpy()) <= 1e-2
+
+    # rel-L2 over all checked elements of the workload (the gate's definition)
+    for nm, bar in (("O", O_REL_L2), ("dQ", GRAD_REL_L2), ("dK", GRAD_REL_L2), ("dV", GRAD_REL_L2)):
+        got = np.concatenate([a.ravel() for a, _ in checked[nm]])
+        ref = np.concatenate([r.ravel() for _, r in checked[nm]])
+        e = rel_l2(got, ref)
+        worst = max(rel_l2(a, r) for a, r in checked[nm])
+        print(f"{name} {nm}: rel-L2 {e:.4f} over {len(checked[nm])} tiles (worst tile {worst:.4f})")
+        assert e <= bar, f"{nm} {name}: rel-L2 {e:.4f} over {len(checked[nm])} tiles"
+
