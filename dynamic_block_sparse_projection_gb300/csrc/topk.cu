@@ -145,8 +145,8 @@ __device__ __forceinline__ void chunk_prefix(const uint32_t* words, int nw, int3
 // warp w covers indices [32c, 32c + 32)).
 //
 // Fast path (finite row with max > min): the scores are binned by value into
-// BINS equal-width buckets between the row minimum and maximum (a monotone
-// map, so a higher bucket holds only larger scores).  One histogram gives the
+// BINS equal-width buckets between the row minimum and maximum (rounded, a
+// monotone map, so a higher bucket holds only larger scores).  One histogram gives the
 // bucket b* holding the k-th largest score; every score in a higher bucket is
 // kept, and the few scores tied in b* (at most kCandMax) are ranked exactly
 // by (key desc, index asc).  Value binning spreads the scores over the
@@ -224,10 +224,15 @@ __global__ void __launch_bounds__(RT, (RT == 128 || RT == 256) ? 1024 / RT : 1) 
     for (int i = t; i < kBins; i += RT) hist[i] = 0u;
     if (t == 0) s_cnt = 0u;
     __syncthreads();
+    // bucket = round((f - lo) * scale): adding 1.5 * 2^23 leaves the rounded
+    // value in the low mantissa bits (one FMA instead of a float-to-int
+    // conversion); the map stays monotone in f, clamped to [0, kBins - 1]
+    const float c0 = 12582912.0f - lo * scale;
 #pragma unroll
     for (int j = 0; j < kKPT; ++j) {
       const int i = j * RT + t;
-      bk[j] = min((uint32_t)(kBins - 1), (uint32_t)((f[j] - lo) * scale));
+      const int q = __float_as_int(fmaf(f[j], scale, c0)) - 0x4B400000;
+      bk[j] = (uint32_t)min(kBins - 1, max(0, q));
       if (i < nb) atomicAdd(&hist[bk[j]], 1u);
     }
     __syncthreads();
