@@ -8,12 +8,13 @@
 // it; that transpose is built deterministically without atomics.
 //
 // Kernels:
-//   topk_select    one CTA per row (32 ... 512 threads, 16 keys per thread
-//                  in registers).  Scores become order-preserving uint32
-//                  keys; an MSB-first radix select below the row's common
-//                  prefix finds the k-th largest key T and how many keys equal
-//                  to T to take; ballots per 32-index chunk then give the
-//                  row's bitmask and the ascending list.
+//   topk_select    one CTA per row (32 ... 512 threads, 16 consecutive
+//                  scores per thread in registers).  Scores are binned by
+//                  value between the row's min and max; the bucket holding
+//                  the k-th largest is ranked exactly on order-preserving
+//                  uint32 keys (ties to the lower index), with an MSB-first
+//                  radix select as the fallback.  Each thread writes its kept
+//                  indices (ascending) and the row's bitmask words.
 //   topk_colcount  per (b, h, 32-column slab): 32x32 bit transposes of the
 //                  mask (stored word column by word column, rows contiguous)
 //                  give each column's population.
@@ -48,39 +49,62 @@ struct TopkArgs {
   HeadK hk;
 };
 
-// One CTA of RT threads per row; the row's scores live in registers as keys
-// (KPT per thread, element i in thread i % RT, slot i / RT).
-//   1. AND / OR of all keys: the leading bits where they agree are a common
-//      prefix, so the radix select starts at the first bit that differs.
-//   2. MSB-first radix select over the remaining bits, 11 bits per pass
-//      (shared-memory histogram of 2048 bins; at most 3 passes): the k-th
-//      largest key T and how many keys equal to T are taken (need_eq).
-//   3. Per 32-element chunk (consecutive indices: chunk c = slot j of warp w),
-//      ballots of key > T and key == T; the equal keys are taken lowest index
-//      first, which gives the row's selection mask word by word.
-//   4. The set bits are written out in ascending order (prefix over chunks).
-// Per element this is a few instructions per pass and no contended atomics
-// on the leading bits, which for float scores are nearly all equal.
+// One CTA of RT threads per row.  Thread t holds kE consecutive scores
+// (slots [kE*t - off, kE*t - off + kE), off = the row start's offset from a
+// 16-byte boundary, so whole threads load with 16-byte vectors).
+//
+// Fast path (finite row with max > min): the scores are binned by value into
+// BINS equal-width buckets between the row minimum and maximum (one FMA,
+// rounded by the 1.5 * 2^23 trick, clamped: a monotone map, so a higher
+// bucket holds only larger scores).  One shared-memory histogram gives the
+// bucket b* holding the k-th largest score; every score in a higher bucket is
+// kept, and the few scores of b* (at most kCandMax) are ranked exactly by
+// (key desc, index asc) unless all of them are kept.  Each thread then writes
+// its own kept indices (ascending) at its prefix position and 32-bit mask
+// words are put together from the threads' 16-bit slot masks.  Value binning
+// spreads the scores over the buckets, so the shared-memory atomics rarely
+// collide; radix digits of float bits would pile into the few bins of the
+// common exponents.  Slots outside the row hold NaN: ignored by min / max,
+// binned into bucket 0 and taken out of its count.  Real NaNs also land in
+// bucket 0 and rank below every number there.
+// Fallback (infinite scores, all equal, or a crowded b*): the row is re-read
+// with element i in thread i % RT, and an MSB-first radix select on the
+// order-preserving keys (11-bit digits, 2048-bin histogram; 8-bit for rows of
+// at most 1024 keys) below their common prefix gives the k-th largest key T and
+// how many keys equal to T to take (lowest index first); ballots per 32-index
+// chunk give the mask words.
 
-// Digit width of the radix passes: 11 bits (2048 bins) for long rows, 8 bits
-// for rows of at most 1024 keys, where clearing and scanning a large
-// histogram would cost more than the keys themselves.
+// Digit width of the radix passes and bucket count of the value binning: 11
+// bits (2048 bins) for long rows, 8 bits for rows of at most 1024 keys, where
+// clearing and scanning a large histogram would cost more than the keys.
 template <int RT>
 struct SelCfg {
   static constexpr int DIGIT = RT >= 128 ? 11 : 8;
   static constexpr int BINS = 1 << DIGIT;
 };
 
+constexpr int kE = 16;                   // scores per thread
+
 template <int RT>
 __device__ __forceinline__ void cta_find_bin(const uint32_t* hist, uint32_t kk, uint32_t* s_tot, uint32_t* s_res) {
   // the bin holding the kk-th largest key (counted from the top bin down) and its rank inside the bin
   constexpr int kBins = SelCfg<RT>::BINS;
   constexpr int BPT = kBins / RT;
+  static_assert(BPT % 4 == 0, "bins per thread in 16-byte loads");
   constexpr int NW = RT / 32;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  uint32_t c[BPT];
+#pragma unroll
+  for (int q = 0; q < BPT / 4; ++q) {
+    const uint4 u = reinterpret_cast<const uint4*>(hist)[t * (BPT / 4) + q];
+    c[4 * q] = u.x;
+    c[4 * q + 1] = u.y;
+    c[4 * q + 2] = u.z;
+    c[4 * q + 3] = u.w;
+  }
   uint32_t tot = 0;
 #pragma unroll
-  for (int i = 0; i < BPT; ++i) tot += hist[t * BPT + i];
+  for (int i = 0; i < BPT; ++i) tot += c[i];
   // suffix sum over threads above t: warp-level, then across warps
   uint32_t suf = tot;
 #pragma unroll
@@ -91,20 +115,19 @@ __device__ __forceinline__ void cta_find_bin(const uint32_t* hist, uint32_t kk, 
   if (NW > 1) {
     if (lane == 0) s_tot[w] = suf;  // total of warp w
     __syncthreads();
-    uint32_t above_w = 0;
-    for (int v = w + 1; v < NW; ++v) above_w += s_tot[v];
-    suf += above_w;
+#pragma unroll
+    for (int v = 1; v < NW; ++v)
+      if (v > w) suf += s_tot[v];
   }
   uint32_t above = suf - tot;      // keys in bins above this thread's range
   if (above < kk && above + tot >= kk) {
+#pragma unroll
     for (int i = BPT - 1; i >= 0; --i) {
-      const uint32_t c = hist[t * BPT + i];
-      if (above + c >= kk) {
+      if (above < kk && above + c[i] >= kk) {
         s_res[0] = (uint32_t)(t * BPT + i);
         s_res[1] = kk - above;
-        break;
       }
-      above += c;
+      above += c[i];
     }
   }
   __syncthreads();
@@ -140,35 +163,26 @@ __device__ __forceinline__ void chunk_prefix(const uint32_t* words, int nw, int3
   }
 }
 
-// One row per CTA of RT threads, kKPT scores per thread in registers
-// (element i in thread i % RT, slot i / RT; 32-element chunk c = slot j of
-// warp w covers indices [32c, 32c + 32)).
-//
-// Fast path (finite row with max > min): the scores are binned by value into
-// BINS equal-width buckets between the row minimum and maximum (rounded, a
-// monotone map, so a higher bucket holds only larger scores).  One histogram gives the
-// bucket b* holding the k-th largest score; every score in a higher bucket is
-// kept, and the few scores tied in b* (at most kCandMax) are ranked exactly
-// by (key desc, index asc).  Value binning spreads the scores over the
-// buckets, so the shared-memory atomics rarely collide; radix digits of float
-// bits would pile into the few bins of the common exponents.
-// Fallback (non-finite scores, all equal, or a crowded b*): MSB-first radix
-// select on the order-preserving keys below their common prefix, then equal
-// keys taken lowest index first.
-template <int RT, int kKPT>
-__global__ void __launch_bounds__(RT, (RT == 128 || RT == 256) ? 1024 / RT : 1) topk_select_kernel(const __grid_constant__ TopkArgs a) {
+// CTAs per SM the register budget is sized for (64 registers a thread at 128
+// and 256 threads; more where fewer registers would spill)
+constexpr int select_min_blocks(int rt) { return (rt == 128 || rt == 256) ? 1024 / rt : 1; }
+
+template <int RT>
+__global__ void __launch_bounds__(RT, select_min_blocks(RT)) topk_select_kernel(const __grid_constant__ TopkArgs a) {
+  constexpr int E = kE;
   constexpr int kBins = SelCfg<RT>::BINS;
   constexpr int kDigit = SelCfg<RT>::DIGIT;
   constexpr int NW = RT / 32;
-  constexpr int MAXC = RT * kKPT / 32;   // 32-element chunks of the row
-  __shared__ uint32_t hist[kBins];
-  __shared__ uint32_t s_tot[NW > 1 ? NW : 1];
-  __shared__ uint32_t s_red[3 * NW];
+  constexpr int MAXC = RT * E / 32;      // 32-element chunks of the row
+  __shared__ __align__(16) uint32_t hist[kBins];
+  __shared__ uint32_t s_tot[NW];
+  __shared__ uint32_t s_red[2 * NW];
   __shared__ uint32_t s_res[2];
   __shared__ uint32_t s_cnt;
   __shared__ uint32_t candk[kCandMax];
   __shared__ int32_t candi[kCandMax];
-  __shared__ uint32_t eqw[MAXC];
+  __shared__ uint32_t gms[RT + 2];       // fast path: kept slots of thread t (bit e = slot e); two zero slots after
+  __shared__ uint32_t eqw[MAXC];         // fallback: per-chunk words
   __shared__ uint32_t selw[MAXC];
   __shared__ int32_t offw[MAXC];
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -180,105 +194,171 @@ __global__ void __launch_bounds__(RT, (RT == 128 || RT == 256) ? 1024 / RT : 1) 
   const int h = (int)(bh % a.H);
   const int b = (int)(bh / a.H);
   const uint32_t k = (uint32_t)a.hk.k[h];
+  const long long base = (long long)b * a.G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * a.G + (long long)g * k;
+  int32_t* dst = a.fwd_col + base;
+  // mask word (b, h, ci, g): word columns contiguous over g for the transpose kernels
+  uint32_t* mcol = a.mask + bh * (long long)a.words * a.G + g;
 
   const float* src = a.scores + row * (long long)nb;
-  float f[kKPT];
-  float lo = INFINITY, hi = -INFINITY;
-  float sum = 0.f;      // non-finite iff a score is NaN or infinite (or, harmlessly, the sum overflows)
+  int off = (int)((reinterpret_cast<uintptr_t>(src) >> 2) & 3u);
+  const bool vec = off + nb <= RT * E;   // else (rows of nearly RT * E keys) scalar loads from slot 0 = index 0
+  if (!vec) off = 0;
+  const int i0 = E * t - off;
+  float x[E];
+  float lo, hi;
+  uint32_t vmask;                        // slots inside the row
+  if (vec && i0 >= 0 && i0 + E <= nb) {
+    const float4* p = reinterpret_cast<const float4*>(src + i0);
 #pragma unroll
-  for (int j = 0; j < kKPT; ++j) {
-    const int i = j * RT + t;
-    f[j] = (i < nb) ? __ldcs(src + i) : 0.f;
-    if (i < nb) {
-      sum += f[j];
-      lo = fminf(lo, f[j]);
-      hi = fmaxf(hi, f[j]);
+    for (int q = 0; q < E / 4; ++q) {
+      const float4 v = __ldcs(p + q);
+      x[4 * q] = v.x;
+      x[4 * q + 1] = v.y;
+      x[4 * q + 2] = v.z;
+      x[4 * q + 3] = v.w;
+    }
+    lo = fminf(x[0], x[E - 1]);
+    hi = fmaxf(x[0], x[E - 1]);
+#pragma unroll
+    for (int e = 1; e + 1 < E - 1; e += 2) {
+      lo = min3f(lo, x[e], x[e + 1]);
+      hi = max3f(hi, x[e], x[e + 1]);
+    }
+    vmask = (1u << E) - 1u;
+  } else {
+    lo = INFINITY;
+    hi = -INFINITY;
+    vmask = 0u;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = i0 + e;
+      const bool in = i >= 0 && i < nb;
+      x[e] = in ? __ldcs(src + i) : __int_as_float(0x7fffffff);
+      if (in) {
+        lo = fminf(lo, x[e]);
+        hi = fmaxf(hi, x[e]);
+        vmask |= 1u << e;
+      }
     }
   }
-  const bool bad = !isfinite(sum);
-  for (int i = t; i < MAXC; i += RT) selw[i] = 0u;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
     hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
   }
-  const uint32_t bad_w = __any_sync(0xffffffffu, bad) ? 1u : 0u;
   if (lane == 0) {
     s_red[w] = __float_as_uint(lo);
     s_red[NW + w] = __float_as_uint(hi);
-    s_red[2 * NW + w] = bad_w;
   }
+  for (int i = 4 * t; i < kBins; i += 4 * RT) *reinterpret_cast<uint4*>(&hist[i]) = make_uint4(0u, 0u, 0u, 0u);
+  if (t == 0) s_cnt = 0u;
+  if (t < 2) gms[RT + t] = 0u;
   __syncthreads();
-  bool any_bad = false;
 #pragma unroll
   for (int v = 0; v < NW; ++v) {
     lo = fminf(lo, __uint_as_float(s_red[v]));
     hi = fmaxf(hi, __uint_as_float(s_red[NW + v]));
-    any_bad |= s_red[2 * NW + v] != 0u;
   }
-  const float scale = (float)(kBins - 1) / (hi - lo);
-  bool fast = !any_bad && hi > lo && scale < 1e30f;   // uniform over the CTA
+  // any monotone bucket map will do, so a fast division: 0 (no fast path) when
+  // hi - lo overflows or exceeds 2^126, huge when it is tiny
+  const float scale = __fdividef((float)(kBins - 1), hi - lo);
+  bool fast = hi > lo && scale > 0.f && scale < 1e30f;   // finite min < max (uniform over the CTA)
 
   if (fast) {
-    uint32_t bk[kKPT];
-    for (int i = t; i < kBins; i += RT) hist[i] = 0u;
-    if (t == 0) s_cnt = 0u;
-    __syncthreads();
     // bucket = round((f - lo) * scale): adding 1.5 * 2^23 leaves the rounded
-    // value in the low mantissa bits (one FMA instead of a float-to-int
-    // conversion); the map stays monotone in f, clamped to [0, kBins - 1]
-    const float c0 = 12582912.0f - lo * scale;
+    // value in the low mantissa bits; NaN clamps to bucket 0
+    const float B0 = 12582912.0f, B1 = B0 + (float)(kBins - 1);
+    const float c0 = B0 - lo * scale;
 #pragma unroll
-    for (int j = 0; j < kKPT; ++j) {
-      const int i = j * RT + t;
-      const int q = __float_as_int(fmaf(f[j], scale, c0)) - 0x4B400000;
-      bk[j] = (uint32_t)min(kBins - 1, max(0, q));
-      if (i < nb) atomicAdd(&hist[bk[j]], 1u);
+    for (int e = 0; e < E; ++e) {
+      x[e] = fminf(fmaxf(fmaf(x[e], scale, c0), B0), B1);
+      atomicAdd(&hist[__float_as_uint(x[e]) - 0x4B400000u], 1u);
     }
+    if (t == 0) atomicAdd(&hist[0], (uint32_t)nb - (uint32_t)(RT * E));   // the NaN slots outside the row
     __syncthreads();
     cta_find_bin<RT>(hist, k, s_tot, s_res);
     const uint32_t bstar = s_res[0];
     const uint32_t kk = s_res[1];                         // how many of bucket b* are kept
     const uint32_t C = hist[bstar];
     if (C <= (uint32_t)kCandMax) {
+      const float xs = __uint_as_float(0x4B400000u + bstar);
+      uint32_t gm = 0u;
+      bool anyeq = false;
 #pragma unroll
-      for (int j = 0; j < kKPT; ++j) {
-        const int i = j * RT + t;
-        if (i < nb && bk[j] == bstar) {
+      for (int e = 0; e < E; ++e) {
+        gm |= (x[e] > xs) ? 1u << e : 0u;
+        anyeq |= x[e] == xs;
+      }
+      uint32_t eqm = 0u;
+      if (anyeq) {                                        // few threads
+#pragma unroll
+        for (int e = 0; e < E; ++e) eqm |= (x[e] == xs) ? 1u << e : 0u;
+        eqm &= vmask;
+      }
+      if (C == kk) gm |= eqm;                             // the whole bucket is kept
+      gms[t] = gm;
+      if (C != kk) {                                      // uniform
+        while (eqm) {
+          const int i = i0 + __ffs(eqm) - 1;
+          eqm &= eqm - 1u;
           const uint32_t pos = atomicAdd(&s_cnt, 1u);
-          candk[pos] = score_key(f[j]);
+          candk[pos] = score_key(__ldg(src + i));
           candi[pos] = i;
         }
-      }
-      __syncthreads();
-      for (uint32_t c = t; c < C; c += RT) {
-        const uint32_t kc = candk[c];
-        const int ic = candi[c];
-        uint32_t rank = 0;
-        for (uint32_t c2 = 0; c2 < C; ++c2) {
-          const uint32_t k2 = candk[c2];
-          rank += (k2 > kc || (k2 == kc && candi[c2] < ic)) ? 1u : 0u;
+        __syncthreads();
+        for (uint32_t c = t; c < C; c += RT) {
+          const uint32_t kc = candk[c];
+          const int ic = candi[c];
+          uint32_t rank = 0;
+          for (uint32_t c2 = 0; c2 < C; ++c2) {
+            const uint32_t k2 = candk[c2];
+            rank += (k2 > kc || (k2 == kc && candi[c2] < ic)) ? 1u : 0u;
+          }
+          if (rank < kk) atomicOr(&gms[(ic + off) / E], 1u << ((ic + off) % E));
         }
-        if (rank < kk) atomicOr(&selw[ic >> 5], 1u << (ic & 31));
       }
       __syncthreads();
+      gm = gms[t];
+      // list positions: exclusive prefix of the kept counts over threads
+      const uint32_t cnt = (uint32_t)__popc(gm);
+      uint32_t inc = cnt;
 #pragma unroll
-      for (int j = 0; j < kKPT; ++j) {
-        const int i = j * RT + t;
-        const uint32_t gt = __ballot_sync(0xffffffffu, i < nb && bk[j] > bstar);
-        if (lane == 0 && j * NW + w < words) selw[j * NW + w] |= gt;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
+      }
+      if (lane == 31) s_tot[w] = inc;
+      __syncthreads();
+      uint32_t before = inc - cnt;
+#pragma unroll
+      for (int v = 0; v < NW - 1; ++v)
+        if (v < w) before += s_tot[v];
+      int32_t* d = dst + before;
+      while (gm) {
+        *d++ = i0 + __ffs(gm) - 1;
+        gm &= gm - 1u;
+      }
+      // mask word m covers indices [32m, 32m + 32): slots 2m .. 2m + 2 shifted by off
+      for (int m = t; m < words; m += RT) {
+        const uint64_t v = (uint64_t)gms[2 * m] | ((uint64_t)gms[2 * m + 1] << 16) | ((uint64_t)gms[2 * m + 2] << 32);
+        mcol[(long long)m * a.G] = (uint32_t)(v >> off);
       }
     } else {
       fast = false;                                       // crowded bucket: exact radix select
     }
-    __syncthreads();
   }
 
   if (!fast) {
-    // the keys are recomputed from the scores where needed (rare path, fewer registers)
+    // the row again, element i in thread i % RT (rare path)
+    float f[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const int i = j * RT + t;
+      f[j] = (i < nb) ? __ldg(src + i) : 0.f;
+    }
     uint32_t vand = 0xffffffffu, vor = 0u;
 #pragma unroll
-    for (int j = 0; j < kKPT; ++j) {
+    for (int j = 0; j < E; ++j) {
       const int i = j * RT + t;
       if (i < nb) {
         const uint32_t kj = score_key(f[j]);
@@ -315,7 +395,7 @@ __global__ void __launch_bounds__(RT, (RT == 128 || RT == 256) ? 1024 / RT : 1) 
       for (int i = t; i < kBins; i += RT) hist[i] = 0u;
       __syncthreads();
 #pragma unroll
-      for (int j = 0; j < kKPT; ++j) {
+      for (int j = 0; j < E; ++j) {
         const int i = j * RT + t;
         const uint32_t kj = score_key(f[j]);
         const bool in = i < nb && (kj & hi_mask) == prefix;
@@ -333,9 +413,9 @@ __global__ void __launch_bounds__(RT, (RT == 128 || RT == 256) ? 1024 / RT : 1) 
     }
     const uint32_t T = prefix;
     const uint32_t need_eq = kk;   // keys equal to T that are taken, lowest index first
-    uint32_t gtw[kKPT];
+    uint32_t gtw[E];
 #pragma unroll
-    for (int j = 0; j < kKPT; ++j) {
+    for (int j = 0; j < E; ++j) {
       const int i = j * RT + t;
       const bool valid = i < nb;
       const uint32_t kj = score_key(f[j]);
@@ -347,7 +427,7 @@ __global__ void __launch_bounds__(RT, (RT == 128 || RT == 256) ? 1024 / RT : 1) 
     if (w == 0) chunk_prefix<MAXC>(eqw, words, offw, lane);   // equal keys before each chunk
     __syncthreads();
 #pragma unroll
-    for (int j = 0; j < kKPT; ++j) {
+    for (int j = 0; j < E; ++j) {
       const int ci = j * NW + w;
       if (ci < words) {
         const uint32_t e = eqw[ci];
@@ -358,10 +438,10 @@ __global__ void __launch_bounds__(RT, (RT == 128 || RT == 256) ? 1024 / RT : 1) 
           if ((uint32_t)__popc(e) <= room) {
             take = e;
           } else {
-            uint32_t x = e;
+            uint32_t x2 = e;
             for (uint32_t q = 0; q < room; ++q) {
-              take |= x & (~x + 1u);
-              x &= x - 1u;
+              take |= x2 & (~x2 + 1u);
+              x2 &= x2 - 1u;
             }
           }
         }
@@ -369,25 +449,20 @@ __global__ void __launch_bounds__(RT, (RT == 128 || RT == 256) ? 1024 / RT : 1) 
       }
     }
     __syncthreads();
-  }
-
-  // output: ascending list (offsets per chunk) and the row's mask words; one
-  // thread per chunk writes that chunk's few selected indices
-  if (w == 0) chunk_prefix<MAXC>(selw, words, offw, lane);
-  __syncthreads();
-  const long long base = (long long)b * a.G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * a.G + (long long)g * k;
-  int32_t* dst = a.fwd_col + base;
-  // mask word (b, h, ci, g): word columns contiguous over g for the transpose kernels
-  uint32_t* mcol = a.mask + bh * (long long)a.words * a.G + g;
-  for (int ci = t; ci < words; ci += RT) {
-    uint32_t sw = selw[ci];
-    mcol[(long long)ci * a.G] = sw;
-    int o = offw[ci];
-    while (sw) {
-      dst[o++] = ci * 32 + (__ffs(sw) - 1);
-      sw &= sw - 1u;
+    // ascending list (offsets per chunk) and the row's mask words
+    if (w == 0) chunk_prefix<MAXC>(selw, words, offw, lane);
+    __syncthreads();
+    for (int ci = t; ci < words; ci += RT) {
+      uint32_t sw = selw[ci];
+      mcol[(long long)ci * a.G] = sw;
+      int o = offw[ci];
+      while (sw) {
+        dst[o++] = ci * 32 + (__ffs(sw) - 1);
+        sw &= sw - 1u;
+      }
     }
   }
+
   if (t == 0) {
     a.fwd_ptr[row] = (int32_t)base;
     if (row == a.rows - 1) a.fwd_ptr[a.rows] = a.nnz;
@@ -570,11 +645,11 @@ cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk
   // threads per SM for the load latency)
   cudaError_t e;
   const unsigned grid = (unsigned)a.rows;
-  if (G <= 32 * 16) topk_select_kernel<32, 16><<<grid, 32, 0, st>>>(a);
-  else if (G <= 64 * 16) topk_select_kernel<64, 16><<<grid, 64, 0, st>>>(a);
-  else if (G <= 128 * 16) topk_select_kernel<128, 16><<<grid, 128, 0, st>>>(a);
-  else if (G <= 256 * 16) topk_select_kernel<256, 16><<<grid, 256, 0, st>>>(a);
-  else topk_select_kernel<512, 16><<<grid, 512, 0, st>>>(a);
+  if (G <= 32 * kE) topk_select_kernel<32><<<grid, 32, 0, st>>>(a);
+  else if (G <= 64 * kE) topk_select_kernel<64><<<grid, 64, 0, st>>>(a);
+  else if (G <= 128 * kE) topk_select_kernel<128><<<grid, 128, 0, st>>>(a);
+  else if (G <= 256 * kE) topk_select_kernel<256><<<grid, 256, 0, st>>>(a);
+  else topk_select_kernel<512><<<grid, 512, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int nseg = (G + kSeg - 1) / kSeg;
   dim3 g2((unsigned)((words + 7) / 8), (unsigned)nseg, (unsigned)bhs);
