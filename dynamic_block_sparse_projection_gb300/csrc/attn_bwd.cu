@@ -14,8 +14,14 @@
 //                S^T = K_j Q_g^T, dP^T = V_j dO_g^T       (tcgen05, smem x smem)
 //                P^T, dS^T -> TMEM (bf16) by the compute warps
 //                dV += P^T dO_g, dK += dS^T Q_g           (tcgen05, TMEM x smem)
-//   q kernel   one CTA per group (b, h, g), looping over its forward list:
+//   q kernel   persistent CTAs (one per SM) working through the groups
+//              (b, h, g), each looping over its forward list:
 //                S = Q_g K_j^T, dP = dO_g V_j^T; dS -> TMEM; dQ += dS K_j
+//              The rings and barrier phases run on across groups, so the
+//              next group's tiles load while the current one finishes.  The
+//              kv kernel keeps one CTA per block: its list lengths vary
+//              widely, and the hardware's dynamic block scheduling balances
+//              them better than a static persistent split.
 // The price of no atomics is recomputing S and dP in both kernels (7 MMAs
 // per pair instead of 5).
 //
@@ -411,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// dQ: one CTA per query group
+// dQ: persistent CTAs over the query groups
 // ---------------------------------------------------------------------------
 template <int BETA, int D>
 struct QTraits {
@@ -425,7 +431,7 @@ struct QTraits {
   // each slot released as soon as its last product is done.
   static constexpr int NK = 3;
   static constexpr int NV = (A_BYTES + 6 * KV_BYTES + 2048 <= 227 * 1024) ? 3 : 2;
-  static constexpr int NBAR = 2 + 2 * NK + 2 * NV + 2 + 2 + 1;
+  static constexpr int NBAR = 2 + 2 * NK + 2 * NV + 2 + 2 + 2;
   static constexpr int SMEM_USED = 1024 + A_BYTES + (NK + NV) * KV_BYTES + NBAR * 8 + 16;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   // TMEM: S and dP (fp32), dQ (fp32), dS (bf16 pairs, BETA/2 columns), and Q_g
@@ -442,8 +448,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     attn_bwd_q_kernel(const __nv_bfloat16* __restrict__ Qg, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                       const float* __restrict__ L2w, const float* __restrict__ Dw,
-                      const int32_t* __restrict__ fwd_ptr, const int32_t* __restrict__ fwd_col, int N, int G,
-                      float scale, __nv_bfloat16* __restrict__ dQ, Ctl ctl) {
+                      const int32_t* __restrict__ fwd_ptr, const int32_t* __restrict__ fwd_col, long long items,
+                      int N, int G, float scale, __nv_bfloat16* __restrict__ dQ, Ctl ctl) {
   using T = QTraits<BETA, D>;
   constexpr int NK = T::NK, NV = T::NV;
   constexpr int HALF = T::HALF;
@@ -463,20 +469,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
   uint64_t* sp_free = s_full + 1;                 // compute threads have read S, dP
   uint64_t* ds_full = sp_free + 1;
   uint64_t* ds_empty = ds_full + 1;
-  uint64_t* acc_done = ds_empty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  uint64_t* acc_done = ds_empty + 1;              // dQ of the current group is complete
+  uint64_t* mma_drain = acc_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   DSV_TRACE_INIT;
-  const long long row = blockIdx.x;               // (b*H + h)*G + g
-  const long long bh = row / G;
-  const int g = (int)(row - bh * G);
   const int nb = G;
-  const int start = fwd_ptr[row];
-  const int cnt = fwd_ptr[row + 1] - start;
   const unsigned int kid = (unsigned int)KID_BWD_Q << 8;
-  const long long qrow0 = bh * N + (long long)g * BETA;
 
   if (threadIdx.x == 0) {
     mbar_init(qd_full, 1);
@@ -494,6 +495,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     mbar_init(ds_full, kComputeThreads);
     mbar_init(ds_empty, 1);
     mbar_init(acc_done, 1);
+    mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -518,12 +520,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   constexpr uint32_t tmem = 0;
 
+  // The CTA works through groups blockIdx.x, blockIdx.x + gridDim.x, ...
+  // Every role counts the pairs of the groups before the current one (gq: the
+  // global pair index of ring slots and barrier phases) and the non-empty
+  // groups (ne: the phase of qd_full, q_tm and acc_done), so the next group's
+  // dO, K and V tiles load while the compute warps finish the current group.
   if (tmem_base != tmem) {
-    if (threadIdx.x == 0) set_error(ctl, DSV_ERR_INTERNAL, (unsigned int)(row & 0x7fffffff));
-  } else if (cnt <= 0) {
-    if (cnt < 0 && threadIdx.x == 0) set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
-    for (int i = threadIdx.x; i < BETA * D / 8; i += blockDim.x)
-      reinterpret_cast<uint4*>(dQ + qrow0 * D)[i] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) set_error(ctl, DSV_ERR_INTERNAL, blockIdx.x);
   } else if (warp == 0 || warp == kQVWarp) {
     // TMA producers, one per warp: warp 0 loads dO_g and the K ring,
     // warp 10 the V ring
@@ -535,32 +538,54 @@ __global__ void __launch_bounds__(kQThreads, 1)
       uint64_t* full = is_k ? k_full : v_full;
       uint64_t* empty = is_k ? k_empty : v_empty;
       tma_prefetch_desc(map);
-      if (is_k) {
-        tma_prefetch_desc(&tmdO);
-        mbar_arrive_expect_tx(qd_full, T::TX_BYTES);
-        for (int c = 0; c < T::NCH; ++c) tma_load_2d(sdO + c * T::A_CHUNK, &tmdO, qd_full, c * 64, (int)qrow0);
-      }
-      int issued = 0;
-      int jn = fwd_col[start];
-      for (int n = 0; n < cnt; ++n) {
-        const int s = n % nst;
-        const uint32_t ph = (uint32_t)(n / nst) & 1u;
-        int j = jn;
-        if (n + 1 < cnt) jn = fwd_col[start + n + 1];
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, ctl, kid | W_KVEMPTY)) break;
-        if ((unsigned)j >= (unsigned)nb) {
-          if (is_k) set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
-          j = 0;
+      if (is_k) tma_prefetch_desc(&tmdO);
+      uint32_t gq = 0;                            // tiles issued so far
+      int qd_issued = 0;
+      bool ok = true;
+      ItemCursor cur(fwd_ptr, nullptr, items, false);
+      long long row;
+      int start, cnt;
+      while (ok && cur.next(row, start, cnt)) {
+        if (cnt <= 0) continue;
+        const long long bh = row / G;
+        const int g = (int)(row - bh * G);
+        if (is_k) {
+          // dO_g is the A operand of every dP product: the previous group's
+          // products must be done.  acc_done (one phase per group) is at most
+          // one phase behind here; the per-pair s_full could be two behind,
+          // and its parity would then alias.
+          if (qd_issued > 0 && !mbar_wait(acc_done, (uint32_t)(qd_issued - 1) & 1u, abort_flag, ctl, kid | W_KVEMPTY))
+            break;
+          mbar_arrive_expect_tx(qd_full, T::TX_BYTES);
+          for (int c = 0; c < T::NCH; ++c)
+            tma_load_2d(sdO + c * T::A_CHUNK, &tmdO, qd_full, c * 64, (int)(bh * N + (long long)g * BETA));
+          ++qd_issued;
         }
-        const int krow = (int)(bh * N + (long long)j * BETA);
-        mbar_arrive_expect_tx(&full[s], T::TX_BYTES);
-        for (int c = 0; c < T::NCH; ++c)
-          tma_load_2d(ring + s * T::KV_BYTES + c * T::KV_CHUNK, map, &full[s], c * 64, krow);
-        issued = n + 1;
+        int jn = fwd_col[start];
+        for (int n = 0; n < cnt; ++n) {
+          const int s = (int)(gq % (uint32_t)nst);
+          const uint32_t ph = (gq / (uint32_t)nst) & 1u;
+          int j = jn;
+          if (n + 1 < cnt) jn = fwd_col[start + n + 1];
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, ctl, kid | W_KVEMPTY)) {
+            ok = false;
+            break;
+          }
+          if ((unsigned)j >= (unsigned)nb) {
+            if (is_k) set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
+            j = 0;
+          }
+          const int krow = (int)(bh * N + (long long)j * BETA);
+          mbar_arrive_expect_tx(&full[s], T::TX_BYTES);
+          for (int c = 0; c < T::NCH; ++c)
+            tma_load_2d(ring + s * T::KV_BYTES + c * T::KV_CHUNK, map, &full[s], c * 64, krow);
+          ++gq;
+        }
       }
-      if (is_k) mbar_wait(qd_full, 0, nullptr, ctl, kid | W_DRAIN);
-      for (int n = (issued > nst ? issued - nst : 0); n < issued; ++n)
-        mbar_wait(&full[n % nst], (uint32_t)(n / nst) & 1u, nullptr, ctl, kid | W_DRAIN);
+      // every copy this thread started must land before the CTA exits
+      if (is_k && qd_issued > 0) mbar_wait(qd_full, (uint32_t)(qd_issued - 1) & 1u, nullptr, ctl, kid | W_DRAIN);
+      for (uint32_t n = (gq > (uint32_t)nst ? gq - (uint32_t)nst : 0u); n < gq; ++n)
+        mbar_wait(&full[n % (uint32_t)nst], (n / (uint32_t)nst) & 1u, nullptr, ctl, kid | W_DRAIN);
     }
   } else if (warp == 1) {
     {
@@ -572,21 +597,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t dKmn0 = sdesc_sw128(smem_u32(sK), T::KV_CHUNK, 1024);
       // tk / tv: early tests of K_n / V_n (see mbar_test); td: of dS of block n-1
-      auto issue_sdp = [&](int n, uint32_t tk, uint32_t tv, uint32_t* td) -> bool {
-        const int sk = n % NK, sv = n % NV;
-        if (!mbar_wait_warp_tested(&k_full[sk], (uint32_t)(n / NK) & 1u, tk, abort_flag, ctl, kid | W_KFULL))
-          return false;
+      auto issue_sdp = [&](uint32_t gn, uint32_t tk, uint32_t tv, uint32_t* td) -> bool {
+        const int sk = (int)(gn % NK), sv = (int)(gn % NV);
+        if (!mbar_wait_warp_tested(&k_full[sk], (gn / NK) & 1u, tk, abort_flag, ctl, kid | W_KFULL)) return false;
         tc_fence_after();
         const uint64_t kb = desc_off(dK0, (uint32_t)sk * T::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ao = (kk >> 2) * T::A_CHUNK + (kk & 3) * 32;
           const uint32_t bo = (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32;
           mma_ts_w(tmem + T::S_COL, tmem + T::Q_COL + kk * 8, desc_off(kb, bo), ID_S, kk > 0 ? 1u : 0u);
         }
-        if (td != nullptr) *td = mbar_test(ds_full, (uint32_t)(n - 1) & 1u);
-        if (!mbar_wait_warp_tested(&v_full[sv], (uint32_t)(n / NV) & 1u, tv, abort_flag, ctl, kid | W_VFULL))
-          return false;
+        if (td != nullptr) *td = mbar_test(ds_full, (gn - 1) & 1u);
+        if (!mbar_wait_warp_tested(&v_full[sv], (gn / NV) & 1u, tv, abort_flag, ctl, kid | W_VFULL)) return false;
         tc_fence_after();
         const uint64_t vb = desc_off(dV0, (uint32_t)sv * T::KV_BYTES);
 #pragma unroll
@@ -599,37 +621,65 @@ __global__ void __launch_bounds__(kQThreads, 1)
         mma_commit_w(&v_empty[sv]);   // V_j is only needed by dP
         return true;
       };
-      bool ok = mbar_wait_warp(qd_full, 0, abort_flag, ctl, kid | W_KV) &&
-                mbar_wait_warp(q_tm, 0, abort_flag, ctl, kid | W_KV);
-      if (ok) ok = issue_sdp(0, 0u, 0u, nullptr);
-      for (int n = 0; ok && n < cnt; ++n) {
-        DSV_TRACE_POINT(g_trace_q, n, 0);
-        uint32_t td = 0u;
-        if (n + 1 < cnt) {
-          const uint32_t tk = mbar_test(&k_full[(n + 1) % NK], (uint32_t)((n + 1) / NK) & 1u);
-          const uint32_t tv = mbar_test(&v_full[(n + 1) % NV], (uint32_t)((n + 1) / NV) & 1u);
-          // S and dP are single-buffered: overwrite them once the compute warps hold block n
-          if (!mbar_wait_warp(sp_free, (uint32_t)n & 1u, abort_flag, ctl, kid | W_SPFREE)) break;
+      uint32_t gq = 0;
+      int ne = 0;
+      bool ok = true;
+      ItemCursor cur(fwd_ptr, nullptr, items, false);
+      long long row;
+      int start, cnt;
+      while (ok && cur.next(row, start, cnt)) {
+        if (cnt <= 0) continue;
+        // q_tm of a group also means the compute warps have read the previous
+        // group's last S and dP, so both may be overwritten
+        ok = mbar_wait_warp(qd_full, (uint32_t)ne & 1u, abort_flag, ctl, kid | W_KV) &&
+             mbar_wait_warp(q_tm, (uint32_t)ne & 1u, abort_flag, ctl, kid | W_KV);
+        if (ok) ok = issue_sdp(gq, 0u, 0u, nullptr);
+        for (int n = 0; ok && n < cnt; ++n) {
+          const uint32_t gn = gq + (uint32_t)n;
+          DSV_TRACE_POINT(g_trace_q, n, 0);
+          uint32_t td = 0u;
+          if (n + 1 < cnt) {
+            const uint32_t tk = mbar_test(&k_full[(gn + 1) % NK], ((gn + 1) / NK) & 1u);
+            const uint32_t tv = mbar_test(&v_full[(gn + 1) % NV], ((gn + 1) / NV) & 1u);
+            // S and dP are single-buffered: overwrite them once the compute warps hold block n
+            if (!mbar_wait_warp(sp_free, gn & 1u, abort_flag, ctl, kid | W_SPFREE)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (!issue_sdp(gn + 1, tk, tv, &td)) {
+              ok = false;
+              break;
+            }
+          }
+          DSV_TRACE_POINT(g_trace_q, n, 1);
+          // ds_full of a group's first pair also means the compute warps have
+          // read the previous group's dQ
+          if (!mbar_wait_warp_tested(ds_full, gn & 1u, td, abort_flag, ctl, kid | W_DSFULL)) {
+            ok = false;
+            break;
+          }
+          DSV_TRACE_POINT(g_trace_q, n, 2);
           tc_fence_after();
-          if (!issue_sdp(n + 1, tk, tv, &td)) break;
-        }
-        DSV_TRACE_POINT(g_trace_q, n, 1);
-        if (!mbar_wait_warp_tested(ds_full, (uint32_t)n & 1u, td, abort_flag, ctl, kid | W_DSFULL)) break;
-        DSV_TRACE_POINT(g_trace_q, n, 2);
-        tc_fence_after();
-        const int s = n % NK;
-        const uint64_t kmn = desc_off(dKmn0, (uint32_t)s * T::KV_BYTES);
+          const int s = (int)(gn % NK);
+          const uint64_t kmn = desc_off(dKmn0, (uint32_t)s * T::KV_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BETA / 16; ++kk) {
-          mma_ts_w(tmem + T::DQ_COL, tmem + T::DS_COL + kk * 8, desc_off(kmn, kk * 16 * 128), ID_Q,
-                   (n > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BETA / 16; ++kk) {
+            mma_ts_w(tmem + T::DQ_COL, tmem + T::DS_COL + kk * 8, desc_off(kmn, kk * 16 * 128), ID_Q,
+                     (n > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit_w(&k_empty[s]);
+          mma_commit_w(ds_empty);
+          DSV_TRACE_POINT(g_trace_q, n, 3);
         }
-        mma_commit_w(&k_empty[s]);
-        mma_commit_w(ds_empty);
-        DSV_TRACE_POINT(g_trace_q, n, 3);
+        if (!ok) break;
+        mma_commit_w(acc_done);
+        gq += (uint32_t)cnt;
+        ++ne;
       }
-      mma_commit_w(acc_done);
-      mbar_wait_warp(acc_done, 0, nullptr, ctl, kid | W_DRAIN);
+      // TMEM is freed after the closing CTA-wide sync only once every MMA is done
+      mma_commit_w(mma_drain);
+      mbar_wait_warp(mma_drain, 0, nullptr, ctl, kid | W_DRAIN);
     }
   } else if (warp < kQVWarp) {
     // ------------- compute warps: query row r, key half hf -------------
@@ -638,80 +688,101 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int r = sp * 32 + lane;
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     const float scale_log2 = scale * kLog2e;
-    const float nlse2 = (r < BETA) ? L2w[qrow0 + r] : 0.f;   // -lse*log2(e)
-    const float dd = (r < BETA) ? Dw[qrow0 + r] : 0.f;
-    {
-      // row r of Q_g into TMEM (this warp's half of its D/2 columns), as the A
-      // operand of every S product; rows past BETA are zero
-      constexpr int QW = D / 4;                   // columns per warp
-      const uint4* src = reinterpret_cast<const uint4*>(Qg + (qrow0 + r) * D + hf * (D / 2));
-      uint32_t q[QW];
-#pragma unroll
-      for (int i = 0; i < QW / 4; ++i) {
-        const uint4 v = r < BETA ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
-        q[4 * i] = v.x;
-        q[4 * i + 1] = v.y;
-        q[4 * i + 2] = v.z;
-        q[4 * i + 3] = v.w;
-      }
-      tmem_st_w<QW>(tmem + lane_off + T::Q_COL + hf * QW, q);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(q_tm);
-    }
     bool ok = true;
-    uint32_t s_tested = 0u;
-    for (int n = 0; n < cnt; ++n) {
-      if (!mbar_wait_warp_tested(s_full, (uint32_t)n & 1u, s_tested, abort_flag, ctl, kid | W_S)) {
-        ok = false;
-        break;
-      }
-      if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 4);
-      tc_fence_after();
-      uint32_t xs[HALF], xp[HALF];
-#pragma unroll
-      for (int c = 0; c < HALF / 32; ++c) {
-        tmem_ld32(tmem + lane_off + T::S_COL + hf * HALF + c * 32, xs + c * 32);
-        tmem_ld32(tmem + lane_off + T::DP_COL + hf * HALF + c * 32, xp + c * 32);
-      }
-      tmem_ld_wait();
-      if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 5);
-      if (warp > 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 6 + warp);
-      tc_fence_before();
-      mbar_arrive(sp_free);
-      const uint32_t e_tested = mbar_test(ds_empty, ((uint32_t)n & 1u) ^ 1u);
-      // exponent, dP - D and dS on packed fp32 pairs
-      uint32_t dw[HALF / 2];
-      const uint64_t c2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(nlse2, nlse2), dd2 = f2_pack(dd, dd);
-#pragma unroll
-      for (int i = 0; i < HALF / 2; ++i) {
-        float x0, x1, d0, d1;
-        f2_unpack(fma2(f2_pack(__uint_as_float(xs[2 * i]), __uint_as_float(xs[2 * i + 1])), c2, nl2), x0, x1);
-        const float p0 = ex2(x0), p1 = ex2(x1);
-        const uint64_t t = sub2(f2_pack(__uint_as_float(xp[2 * i]), __uint_as_float(xp[2 * i + 1])), dd2);
-        f2_unpack(mul2(f2_pack(p0, p1), t), d0, d1);
-        dw[i] = pack_bf16x2(d0, d1);
-      }
-      if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 6);
-      // the single dS buffer is free once dQ of the previous block is done
-      if (n + 1 < cnt) s_tested = mbar_test(s_full, (uint32_t)(n + 1) & 1u);
-      if (!mbar_wait_warp_tested(ds_empty, ((uint32_t)n & 1u) ^ 1u, e_tested, abort_flag, ctl, kid | W_DSEMPTY)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < HALF / 32; ++c)
-        tmem_st16(tmem + lane_off + T::DS_COL + hf * (HALF / 2) + c * 16, dw + c * 16);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(ds_full);
-      if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 7);
-    }
-    if (ok) ok = mbar_wait_warp(acc_done, 0, abort_flag, ctl, kid | W_ACC);
-    if (ok) {
-      tc_fence_after();
+    uint32_t gq = 0;
+    int ne = 0;
+    ItemCursor cur(fwd_ptr, nullptr, items, false);
+    long long row;
+    int start, cnt;
+    while (ok && cur.next(row, start, cnt)) {
+      const long long bh = row / G;
+      const int g = (int)(row - bh * G);
+      const long long qrow0 = bh * N + (long long)g * BETA;
       const long long orow = qrow0 + r;
+      if (cnt <= 0) {
+        // empty (or malformed) list: dQ = 0
+        if (cnt < 0 && r == 0 && hf == 0) set_error(ctl, DSV_ERR_BAD_INDEX, (unsigned int)(row & 0x7fffffff));
+        if (r < BETA) {
+          uint4* dst = reinterpret_cast<uint4*>(dQ + orow * D + hf * (D / 2));
+#pragma unroll
+          for (int q = 0; q < D / 16; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      const float nlse2 = (r < BETA) ? L2w[orow] : 0.f;   // -lse*log2(e)
+      const float dd = (r < BETA) ? Dw[orow] : 0.f;
+      {
+        // row r of Q_g into TMEM (this warp's half of its D/2 columns), as the A
+        // operand of every S product; rows past BETA are zero.  The previous
+        // group's S products are all done: this thread has waited for its last.
+        constexpr int QW = D / 4;                   // columns per warp
+        const uint4* src = reinterpret_cast<const uint4*>(Qg + orow * D + hf * (D / 2));
+        uint32_t q[QW];
+#pragma unroll
+        for (int i = 0; i < QW / 4; ++i) {
+          const uint4 v = r < BETA ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+          q[4 * i] = v.x;
+          q[4 * i + 1] = v.y;
+          q[4 * i + 2] = v.z;
+          q[4 * i + 3] = v.w;
+        }
+        tmem_st_w<QW>(tmem + lane_off + T::Q_COL + hf * QW, q);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(q_tm);
+      }
+      uint32_t s_tested = 0u;
+      for (int n = 0; n < cnt; ++n) {
+        const uint32_t gn = gq + (uint32_t)n;
+        if (!mbar_wait_warp_tested(s_full, gn & 1u, s_tested, abort_flag, ctl, kid | W_S)) {
+          ok = false;
+          break;
+        }
+        if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 4);
+        tc_fence_after();
+        uint32_t xs[HALF], xp[HALF];
+#pragma unroll
+        for (int c = 0; c < HALF / 32; ++c) {
+          tmem_ld32(tmem + lane_off + T::S_COL + hf * HALF + c * 32, xs + c * 32);
+          tmem_ld32(tmem + lane_off + T::DP_COL + hf * HALF + c * 32, xp + c * 32);
+        }
+        tmem_ld_wait();
+        if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 5);
+        if (warp > 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 6 + warp);
+        tc_fence_before();
+        mbar_arrive(sp_free);
+        const uint32_t e_tested = mbar_test(ds_empty, (gn & 1u) ^ 1u);
+        // exponent, dP - D and dS on packed fp32 pairs
+        uint32_t dw[HALF / 2];
+        const uint64_t c2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(nlse2, nlse2), dd2 = f2_pack(dd, dd);
+#pragma unroll
+        for (int i = 0; i < HALF / 2; ++i) {
+          float x0, x1, d0, d1;
+          f2_unpack(fma2(f2_pack(__uint_as_float(xs[2 * i]), __uint_as_float(xs[2 * i + 1])), c2, nl2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          const uint64_t t = sub2(f2_pack(__uint_as_float(xp[2 * i]), __uint_as_float(xp[2 * i + 1])), dd2);
+          f2_unpack(mul2(f2_pack(p0, p1), t), d0, d1);
+          dw[i] = pack_bf16x2(d0, d1);
+        }
+        if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 6);
+        // the single dS buffer is free once dQ of the previous block is done
+        if (n + 1 < cnt) s_tested = mbar_test(s_full, (gn + 1) & 1u);
+        if (!mbar_wait_warp_tested(ds_empty, (gn & 1u) ^ 1u, e_tested, abort_flag, ctl, kid | W_DSEMPTY)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < HALF / 32; ++c)
+          tmem_st16(tmem + lane_off + T::DS_COL + hf * (HALF / 2) + c * 16, dw + c * 16);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+        if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 7);
+      }
+      if (ok) ok = mbar_wait_warp(acc_done, (uint32_t)ne & 1u, abort_flag, ctl, kid | W_ACC);
+      if (!ok) break;
+      tc_fence_after();
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t o[32];
@@ -727,6 +798,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
           for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
         }
       }
+      gq += (uint32_t)cnt;
+      ++ne;
     }
   }
 
@@ -830,9 +903,14 @@ cudaError_t launch_q_t(const void* Q, const CUtensorMap& tmK, const CUtensorMap&
   if ((e = cudaFuncSetAttribute(qk, cudaFuncAttributeMaxDynamicSharedMemorySize, QTraits<BETA, D>::SMEM)) !=
       cudaSuccess)
     return e;
-  qk<<<(unsigned)groups, kQThreads, QTraits<BETA, D>::SMEM, st>>>(static_cast<const __nv_bfloat16*>(Q), tmK, tmV,
-                                                                  tmdO, L2w, Dw, fwd_ptr, fwd_col, s.N, G, scale,
-                                                                  static_cast<__nv_bfloat16*>(dQ), ctl);
+  // persistent: one CTA per SM (the CTA holds the SM's whole TMEM)
+  int dev = 0, nsm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(groups < nsm ? groups : nsm);
+  qk<<<grid, kQThreads, QTraits<BETA, D>::SMEM, st>>>(static_cast<const __nv_bfloat16*>(Q), tmK, tmV, tmdO, L2w, Dw,
+                                                      fwd_ptr, fwd_col, groups, s.N, G, scale,
+                                                      static_cast<__nv_bfloat16*>(dQ), ctl);
   return cudaGetLastError();
 }
 

@@ -70,31 +70,6 @@ struct FwdTraits {
   static constexpr uint32_t TX_BYTES = BETA * D * 2;   // one K or V tile (and the Q tile)
 };
 
-// The list bounds of the rows a persistent CTA visits (row, row + gridDim.x,
-// ...), read one row ahead so that the load is off the critical path:
-// next(row) returns the current row's count (its start is `start` before the
-// call) and fetches the following row's bounds.
-struct RowCursor {
-  const int32_t* ptr;
-  long long rows;
-  int start, end;
-  __device__ RowCursor(const int32_t* p, long long r) : ptr(p), rows(r), start(0), end(0) {
-    if ((long long)blockIdx.x < rows) {
-      start = ptr[blockIdx.x];
-      end = ptr[blockIdx.x + 1];
-    }
-  }
-  __device__ int next(long long row) {
-    const int cnt = end - start;
-    const long long nrow = row + gridDim.x;
-    if (nrow < rows) {
-      start = ptr[nrow];
-      end = ptr[nrow + 1];
-    }
-    return cnt;
-  }
-};
-
 constexpr int kVWarp = 6;                // V producer warp
 constexpr int kFwdThreads = 224;         // 7 warps
 
@@ -189,9 +164,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       uint32_t gq = 0;                            // tiles issued so far
       int q_issued = 0;
       bool ok = true;
-      RowCursor cur(fwd_ptr, rows);
-      for (long long row = blockIdx.x; ok && row < rows; row += gridDim.x) {
-        const int start = cur.start, cnt = cur.next(row);
+      ItemCursor cur(fwd_ptr, nullptr, rows, false);
+      long long row;
+      int start, cnt;
+      while (ok && cur.next(row, start, cnt)) {
         if (cnt <= 0) continue;
         const long long bh = row / G;
         const int g = (int)(row - bh * G);
@@ -260,9 +236,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     uint32_t gq = 0;
     int ne = 0;
     bool ok = true;
-    RowCursor cur(fwd_ptr, rows);
-    for (long long row = blockIdx.x; ok && row < rows; row += gridDim.x) {
-      const int cnt = cur.next(row);
+    ItemCursor cur(fwd_ptr, nullptr, rows, false);
+    long long row;
+    int start, cnt;
+    while (ok && cur.next(row, start, cnt)) {
       if (cnt <= 0) continue;
       ok = mbar_wait_warp(q_full, (uint32_t)ne & 1u, abort_flag, ctl, kid | W_Q);
       if (ok) ok = issue_S(gq, 0);
@@ -314,9 +291,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     uint32_t gq = 0;
     int ne = 0;
     bool ok = true;
-    RowCursor cur(fwd_ptr, rows);
-    for (long long row = blockIdx.x; ok && row < rows; row += gridDim.x) {
-      const int cnt = cur.next(row);
+    ItemCursor cur(fwd_ptr, nullptr, rows, false);
+    long long row;
+    int start, cnt;
+    while (ok && cur.next(row, start, cnt)) {
       const long long bh = row / G;
       const int g = (int)(row - bh * G);
       const long long orow = bh * N + (long long)g * BETA + r;

@@ -375,6 +375,43 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+// The work items of a persistent CTA: rounds r = 0, 1, ... take item
+// r * gridDim.x + blockIdx.x (with `snake`, odd rounds run the CTAs in reverse,
+// so that a list sorted by decreasing cost spreads evenly).  Item idx is CSR
+// row order[idx] (or idx itself); the row and its list bounds are read one
+// item ahead, so the loads are off the critical path.
+struct ItemCursor {
+  const int32_t* ptr;
+  const int32_t* order;
+  long long items, r, row;
+  int start, end;
+  bool snake, valid;
+  __device__ ItemCursor(const int32_t* p, const int32_t* ord, long long n, bool sn)
+      : ptr(p), order(ord), items(n), r(0), row(0), start(0), end(0), snake(sn), valid(false) {
+    load();
+  }
+  __device__ void load() {
+    const long long pos = (snake && (r & 1)) ? (long long)(gridDim.x - 1 - blockIdx.x) : (long long)blockIdx.x;
+    const long long idx = r * gridDim.x + pos;
+    valid = idx < items;
+    if (valid) {
+      row = order != nullptr ? (long long)order[idx] : idx;
+      start = ptr[row];
+      end = ptr[row + 1];
+    }
+  }
+  // the current item (false when there is none left); then fetch the next one
+  __device__ bool next(long long& rw, int& st, int& cnt) {
+    if (!valid) return false;
+    rw = row;
+    st = start;
+    cnt = end - start;
+    ++r;
+    load();
+    return true;
+  }
+};
+
 // min of three (one instruction)
 __device__ __forceinline__ float min3f(float a, float b, float c) {
   float d;
