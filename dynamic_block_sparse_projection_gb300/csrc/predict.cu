@@ -114,8 +114,10 @@ __global__ void __launch_bounds__(kPoolThreads) pool_project_kernel(const __nv_b
 
 // Scores of one (b, h): a 128 x 128 tile of S per CTA, r-deep fp32 FMAs.
 // Thread (tr, tc) owns rows 8*tr .. 8*tr+7 and columns 4*tc .. 4*tc+3 and
-// 64 + 4*tc .. 64 + 4*tc+3: per rank step 4 vector shared loads feed 64 FMAs.
-// VW = 4, 2 or 1: the widest store the row length allows.
+// 64 + 4*tc .. 64 + 4*tc+3: per rank step 4 vector shared loads feed 64 FMAs,
+// issued as 32 packed two-lane FMAs (each lane rounds like fmaf, so the sums
+// are those of the scalar loop).  VW = 4, 2 or 1: the widest store the row
+// length allows.
 constexpr int kST = 128;
 
 template <int R, int VW>
@@ -129,15 +131,16 @@ __global__ void __launch_bounds__(256) score_kernel(const float* __restrict__ qp
   const int j0 = blockIdx.x * kST;
   const float4* qsrc = reinterpret_cast<const float4*>(qp + (bh * G + g0) * (long long)R);
   const float4* ksrc = reinterpret_cast<const float4*>(kp + (bh * nb + j0) * (long long)R);
-  // transpose the pooled vectors into [rank][row] tiles
+  // transpose the pooled vectors into [rank][row] tiles: a warp takes 32
+  // consecutive rows of one 4-rank slice, so its shared stores hit 32 banks
   for (int i = threadIdx.x; i < kST * R / 4; i += 256) {
-    const int row = i / (R / 4), k4 = (i - row * (R / 4)) * 4;
-    const float4 a = (g0 + row < G) ? __ldg(qsrc + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int row = i % kST, k4 = (i / kST) * 4;
+    const float4 a = (g0 + row < G) ? __ldg(qsrc + row * (R / 4) + k4 / 4) : make_float4(0.f, 0.f, 0.f, 0.f);
     qs[(k4 + 0) * kST + row] = a.x;
     qs[(k4 + 1) * kST + row] = a.y;
     qs[(k4 + 2) * kST + row] = a.z;
     qs[(k4 + 3) * kST + row] = a.w;
-    const float4 b = (j0 + row < nb) ? __ldg(ksrc + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 b = (j0 + row < nb) ? __ldg(ksrc + row * (R / 4) + k4 / 4) : make_float4(0.f, 0.f, 0.f, 0.f);
     ks[(k4 + 0) * kST + row] = b.x;
     ks[(k4 + 1) * kST + row] = b.y;
     ks[(k4 + 2) * kST + row] = b.z;
@@ -146,11 +149,11 @@ __global__ void __launch_bounds__(256) score_kernel(const float* __restrict__ qp
   __syncthreads();
   const int tc = threadIdx.x & 15;
   const int tr = threadIdx.x >> 4;
-  float acc[8][8];
+  uint64_t acc[8][4];                          // column pairs (2m, 2m + 1) of row i
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int m = 0; m < 8; ++m) acc[i][m] = 0.f;
+    for (int m = 0; m < 4; ++m) acc[i][m] = 0ull;
 #pragma unroll
   for (int kk = 0; kk < R; ++kk) {
     const float4 a0 = *reinterpret_cast<const float4*>(qs + kk * kST + tr * 8);
@@ -158,11 +161,13 @@ __global__ void __launch_bounds__(256) score_kernel(const float* __restrict__ qp
     const float4 b0 = *reinterpret_cast<const float4*>(ks + kk * kST + 4 * tc);
     const float4 b1 = *reinterpret_cast<const float4*>(ks + kk * kST + 64 + 4 * tc);
     const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const uint64_t b2[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y), f2_pack(b1.z, b1.w)};
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 8; ++i) {
+      const uint64_t a2 = f2_pack(a[i], a[i]);
 #pragma unroll
-      for (int m = 0; m < 8; ++m) acc[i][m] = fmaf(a[i], b[m], acc[i][m]);
+      for (int m = 0; m < 4; ++m) acc[i][m] = fma2(a2, b2[m], acc[i][m]);
+    }
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -172,7 +177,9 @@ __global__ void __launch_bounds__(256) score_kernel(const float* __restrict__ qp
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int j = j0 + 64 * hh + 4 * tc;
-      const float* v = &acc[i][4 * hh];
+      float v[4];
+      f2_unpack(acc[i][2 * hh], v[0], v[1]);
+      f2_unpack(acc[i][2 * hh + 1], v[2], v[3]);
       if (j + 3 < nb) {
         if (VW == 4) {
           __stcs(reinterpret_cast<float4*>(dst + j), make_float4(v[0], v[1], v[2], v[3]));
