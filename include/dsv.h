@@ -175,7 +175,8 @@ dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, cons
  *   dsv_attn_bwd_dkdv        dK, dV (one CTA per key block, transposed lists, the
  *                            blocks with the longest lists first; the order is
  *                            kept in the workspace's last part).
- *   dsv_attn_bwd_dq          dQ (one CTA per query group, forward lists).
+ *   dsv_attn_bwd_dq          dQ (persistent CTAs over the query groups, forward
+ *                            lists).
  * Errors as for dsv_sparse_attn_bwd; a stage does not check that the
  * preprocess ran. */
 dsv_status dsv_attn_bwd_preprocess(const void* O, const void* dO, const float* lse, dsv_shape s,
