@@ -47,6 +47,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="latent16k")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cube", default="", metavar="CT,CY,CX",
+                   help="regroup tokens into ct x cy x cx cubes of the latent grid inside the step")
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--traffic-from", metavar="CSV",
@@ -148,13 +150,24 @@ class ClockSampler:
 # our CUDA path
 # ---------------------------------------------------------------------------
 
-class HotPath:
-    """Preallocated buffers of one step; run() enqueues the four C-ABI calls."""
+class _Tensors:
+    pass
 
-    def __init__(self, dsv, x, w, k_per_head):
+
+class HotPath:
+    """Preallocated buffers of one step; run() enqueues the four C-ABI calls.
+
+    With cube = (ct, cy, cx) the step also regroups the tokens into 3D cubes
+    of the latent grid (dsv_cube_permute on Q, K, V, dO before the path, and
+    its inverse on O, dQ, dK, dV after it), so that query groups and key
+    blocks are cubes; O and the gradients then come out in raster order."""
+
+    def __init__(self, dsv, x, w, k_per_head, cube=None):
         import torch
         self.dsv, self.x, self.w = dsv, x, w
         self.k = list(k_per_head)
+        self.cube = tuple(cube) if cube else None
+        self.grid = (w.T, w.Hl, w.Wl)
         dev = x.Q.device
         B, H, N, d, G = w.B, w.H, w.N, w.d, w.nb
         self.nnz = dsv.nnz_of(B, G, self.k)
@@ -170,32 +183,63 @@ class HotPath:
         self.ws_p = torch.empty(max(1, dsv.predict_workspace_bytes(B, H, N, d, w.block, w.r)), dtype=u8, device=dev)
         self.ws_t = torch.empty(max(1, dsv.topk_workspace_bytes(B, H, N, d, w.block)), dtype=u8, device=dev)
         self.ws_b = torch.empty(max(1, dsv.attn_bwd_workspace_bytes(B, H, N, d, w.block)), dtype=u8, device=dev)
+        if self.cube:
+            # the path's inputs in cube order, and O / gradients back in raster order
+            self.xc = _Tensors()
+            self.xc.Q, self.xc.K, self.xc.V, self.xc.dO = (torch.empty_like(t) for t in (x.Q, x.K, x.V, x.dO))
+            self.xc.Wq, self.xc.Wk = x.Wq, x.Wk
+            self.out_raster = tuple(torch.empty_like(x.Q) for _ in range(4))   # O, dQ, dK, dV
+
+    @property
+    def stages(self):
+        return (("cube_in",) if self.cube else ()) + STAGES + (("cube_out",) if self.cube else ())
 
     def run(self, ev=None):
-        """The four public calls.  With ev (a list of 7 CUDA events) the
-        backward runs as its three public stages with an event between each,
-        so that every kernel of the step is timed on its own stream."""
-        d, x, w = self.dsv, self.x, self.w
-        if ev:
-            ev[0].record()
+        """The four public calls (six with cube order).  With ev (one CUDA
+        event per stage boundary) the backward runs as its three public
+        stages with an event between each, so that every kernel of the step
+        is timed on its own stream."""
+        d, w = self.dsv, self.w
+        marks = iter(ev or ())
+
+        def mark():
+            if ev:
+                next(marks).record()
+
+        mark()
+        x = self.x
+        if self.cube:
+            for src, dst in zip((x.Q, x.K, x.V, x.dO), (self.xc.Q, self.xc.K, self.xc.V, self.xc.dO)):
+                d.cube_permute(src, self.grid, self.cube, out=dst)
+            mark()
+            x = self.xc
         d.predict_scores(x.Q, x.K, x.Wq, x.Wk, w.block, out=self.S, workspace=self.ws_p)
-        if ev:
-            ev[1].record()
+        mark()
         fp, fc, bp, bc = d.topk_blocks(self.S, self.k, w.block, w.N, w.d, outs=self.lists, workspace=self.ws_t)
-        if ev:
-            ev[2].record()
+        mark()
         d.sparse_attn_fwd(x.Q, x.K, x.V, fp, fc, w.block, out=self.O, lse=self.lse)
+        mark()
         if ev:
-            ev[3].record()
             d.attn_bwd_preprocess(self.O, x.dO, self.lse, w.block, workspace=self.ws_b)
-            ev[4].record()
+            mark()
             d.attn_bwd_dkdv(x.Q, x.K, x.V, x.dO, bp, bc, w.block, outs=self.grads[1:], workspace=self.ws_b)
-            ev[5].record()
+            mark()
             d.attn_bwd_dq(x.Q, x.K, x.V, x.dO, fp, fc, w.block, out=self.grads[0], workspace=self.ws_b)
-            ev[6].record()
+            mark()
         else:
             d.sparse_attn_bwd(x.Q, x.K, x.V, self.O, x.dO, self.lse, fp, fc, bp, bc, w.block, outs=self.grads,
                               workspace=self.ws_b)
+        if self.cube:
+            for src, dst in zip((self.O, *self.grads), self.out_raster):
+                d.cube_permute(src, self.grid, self.cube, inverse=True, out=dst)
+            mark()
+
+    def results(self):
+        """O, LSE and the gradients as the step hands them out (raster order;
+        LSE stays in the path's token order)."""
+        if self.cube:
+            return (self.out_raster[0], self.lse, *self.out_raster[1:])
+        return (self.O, self.lse, *self.grads)
 
     def attention_only(self):
         d, x, w = self.dsv, self.x, self.w
@@ -205,7 +249,8 @@ class HotPath:
                           workspace=self.ws_b)
 
 
-KERNELS_PER_STEP = {"predict": 2, "topk": 4, "fwd": 1, "bwd_pre": 1, "bwd_kv": 2, "bwd_q": 1}
+KERNELS_PER_STEP = {"predict": 2, "topk": 4, "fwd": 1, "bwd_pre": 1, "bwd_kv": 2, "bwd_q": 1, "cube_in": 4,
+                    "cube_out": 4}
 STAGES = ("predict", "topk", "fwd", "bwd_pre", "bwd_kv", "bwd_q")
 
 
@@ -242,7 +287,8 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     w = wl.WORKLOADS[args.workload]
     x = wl.make_inputs(w, device=dev)
-    hp = HotPath(dsv, x, w, x.k_per_head)
+    cube = tuple(int(v) for v in args.cube.split(",")) if args.cube else None
+    hp = HotPath(dsv, x, w, x.k_per_head, cube=cube)
     fwd_f, bwd_f = pair_flops(w.block, w.d)
     step_flops = (fwd_f + bwd_f) * hp.nnz
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -255,7 +301,8 @@ def run_ours(args):
         raise RuntimeError(f"device error {dsv.status_string(st)} ({info})")
 
     # timed region: K steps, L2 flushed (untimed) before each step
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(args.steps)]
+    stages = hp.stages
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -267,10 +314,10 @@ def run_ours(args):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    parts = {k: 0.0 for k in STAGES}
+    parts = {k: 0.0 for k in stages}
     step_ms = []
     for e in evs:
-        t = [e[k].elapsed_time(e[k + 1]) for k in range(len(STAGES))]
+        t = [e[k].elapsed_time(e[k + 1]) for k in range(len(stages))]
         for name, v in zip(parts, t):
             parts[name] += v
         step_ms.append(e[0].elapsed_time(e[-1]))
@@ -300,6 +347,8 @@ def run_ours(args):
         "config": {"workload": w.name, "description": w.description, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                    "block": w.block, "r": w.r, "k_per_head": sorted(set(x.k_per_head)), "pairs": hp.nnz,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   **({"cube": list(cube), "token_order": "3D cubes (dsv_cube_permute in and out, timed)"}
+                      if cube else {}),
                    "l2": "flushed before every step (256 MiB write, outside the step events); "
                          "inputs are also larger than L2"},
         "pct_of_bf16_peak": round(100.0 * value / peaks["bf16_tflops"], 2),
@@ -310,13 +359,13 @@ def run_ours(args):
         "breakdown_ms": {k: round(v, 4) for k, v in per_call.items()},
         "speedup_vs_dense": dense,
         "roofline": roofline,
-        "gpu_launches": sum(KERNELS_PER_STEP.values()) * args.steps,
+        "gpu_launches": sum(KERNELS_PER_STEP[k] for k in stages) * args.steps,
         "clocks": clk.summary(),
         "e2e": e2e,
         "peaks_source": peak_src,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, x)
+        out["cpu_baseline"] = cpu_baseline(w, x, cube=cube)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -427,8 +476,8 @@ def time_e2e(dsv, x, w, hp, args, flops_per_step):
         dev_in = [torch.empty_like(t) for t in (x.Q, x.K, x.V, x.dO, x.Wq, x.Wk)]
         xd = X()
         xd.Q, xd.K, xd.V, xd.dO, xd.Wq, xd.Wk = dev_in
-        hp2 = HotPath(dsv, xd, w, hp.k)
-        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (hp2.O, hp2.lse, *hp2.grads)]
+        hp2 = HotPath(dsv, xd, w, hp.k, cube=hp.cube)
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in hp2.results()]
         sets.append((dev_in, hp2, host_out))
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in sets[0][2])
@@ -453,7 +502,7 @@ def time_e2e(dsv, x, w, hp, args, flops_per_step):
             cmp_done[i % 2].record(s_cmp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(cmp_done[i % 2])
-            for h_, d_ in zip(host_out, (hp2.O, hp2.lse, *hp2.grads)):
+            for h_, d_ in zip(host_out, hp2.results()):
                 h_.copy_(d_, non_blocking=True)
             out_done[i % 2].record(s_out)
 
@@ -476,30 +525,38 @@ def time_e2e(dsv, x, w, hp, args, flops_per_step):
 # the oracle on the host cores (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_head_step(w, x, b, h):
-    """The fp64 oracle's whole hot path for one (b, h): returns its pair count."""
+def oracle_head_step(w, x, b, h, cube=None):
+    """The fp64 oracle's whole hot path for one (b, h) (with cube, on the
+    tokens in cube order, and O and the gradients put back): returns its pair
+    count."""
     import numpy as np
     import torch
 
     import oracle
     f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
     Q, K, V, dO = (f64(t[b:b + 1, h:h + 1]) for t in (x.Q, x.K, x.V, x.dO))
+    perm = oracle.cube_order(w.T, w.Hl, w.Wl, *cube) if cube else None
+    if cube:
+        Q, K, V, dO = (oracle.permute_tokens(t, perm) for t in (Q, K, V, dO))
     Wq, Wk = f64(x.Wq[h:h + 1]), f64(x.Wk[h:h + 1])
     S = oracle.predict_scores(Q, K, Wq, Wk, w.block)
     k = [x.k_per_head[h]]
     fp, fc = oracle.topk_lists(S, k)
     oracle.transpose_lists(fp, fc, 1, 1, w.nb, w.nb)
-    oracle.attn_fwd_groups(Q, K, V, fp, fc, w.block)
-    oracle.attn_bwd_groups(Q, K, V, dO, fp, fc, w.block)
+    O, _ = oracle.attn_fwd_groups(Q, K, V, fp, fc, w.block)
+    grads = oracle.attn_bwd_groups(Q, K, V, dO, fp, fc, w.block)
+    if cube:
+        for t in (O, *grads):
+            oracle.permute_tokens(t, perm, inverse=True)
     return int(fc.shape[0])
 
 
-def cpu_baseline(w, x, min_s=10.0, max_s=30.0):
+def cpu_baseline(w, x, min_s=10.0, max_s=30.0, cube=None):
     fwd_f, bwd_f = pair_flops(w.block, w.d)
     t0 = time.perf_counter()
     pairs, heads = 0, 0
     for h in range(w.H):
-        pairs += oracle_head_step(w, x, 0, h)
+        pairs += oracle_head_step(w, x, 0, h, cube)
         heads += 1
         el = time.perf_counter() - t0
         if el >= min_s or el * (heads + 1) / heads > max_s:
@@ -518,16 +575,17 @@ def run_reference(args):
     import torch
     from dynamic_block_sparse_projection_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload]
+    cube = tuple(int(v) for v in args.cube.split(",")) if args.cube else None
     heads = sorted(set(range(w.H)))
     x = wl.make_inputs(w, device="cpu")
     fwd_f, bwd_f = pair_flops(w.block, w.d)
     slices = [(b, h) for b in range(w.B) for h in heads]
     for i in range(max(3, args.warmup)):
-        oracle_head_step(w, x, *slices[i % len(slices)])
+        oracle_head_step(w, x, *slices[i % len(slices)], cube)
     t0 = time.perf_counter()
     pairs = 0
     for i in range(args.steps):
-        pairs += oracle_head_step(w, x, *slices[i % len(slices)])
+        pairs += oracle_head_step(w, x, *slices[i % len(slices)], cube)
     el = time.perf_counter() - t0
     value = (fwd_f + bwd_f) * pairs / el / 1e12
     sample = (f"each step one (batch, head) slice of {w.name} (1 of {len(slices)}): predictor, top-k, transpose, "
@@ -536,7 +594,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(1e3 * el / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "description": w.description},
+        "config": {"workload": w.name, "description": w.description, **({"cube": list(cube)} if cube else {})},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

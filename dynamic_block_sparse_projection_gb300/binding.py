@@ -28,6 +28,7 @@ EXPORTS = (
     "dsv_set_wait_limit_ns", "dsv_version",
     "dsv_topk_blocks_noalloc",
     "dsv_attn_bwd_preprocess", "dsv_attn_bwd_dkdv", "dsv_attn_bwd_dq",
+    "dsv_cube_permute",
 )
 
 
@@ -81,6 +82,8 @@ def _load() -> ctypes.CDLL:
     lib.dsv_attn_bwd_dkdv.restype = ctypes.c_int
     lib.dsv_attn_bwd_dq.argtypes = [vp, vp, vp, vp, Shape, vp, vp, ctypes.c_float, vp, vp, sz, vp]
     lib.dsv_attn_bwd_dq.restype = ctypes.c_int
+    lib.dsv_cube_permute.argtypes = [vp, vp, Shape, i32, i32, i32, i32, i32, i32, i32, vp]
+    lib.dsv_cube_permute.restype = ctypes.c_int
     lib.dsv_version.argtypes = []
     lib.dsv_version.restype = i32
     return lib
@@ -257,6 +260,25 @@ def sparse_attn_bwd(Q, K, V, O, dO, lse, fwd_ptr, fwd_col, bwd_ptr, bwd_col, blo
                                    float(softmax_scale), *[_ptr(t) for t in outs], _ptr(ws), nbytes,
                                    _stream(dev, stream)), "dsv_sparse_attn_bwd")
     return outs
+
+
+def cube_permute(x, grid, cube, *, inverse: bool = False, out=None, stream=None) -> torch.Tensor:
+    """x bf16 [B,H,N,d] between raster and cube token order; see dsv_cube_permute.
+
+    grid = (T, Hl, Wl) with N = T*Hl*Wl; cube = (ct, cy, cx), whose volume is
+    the group / block size of the hot path."""
+    _need(x, "x", torch.bfloat16)
+    dev = x.device
+    B, H, N, d = x.shape
+    T, Hl, Wl = (int(v) for v in grid)
+    ct, cy, cx = (int(v) for v in cube)
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", torch.bfloat16, dev)
+    s = Shape(B, H, N, d, ct * cy * cx, 8)
+    _check(lib.dsv_cube_permute(_ptr(x), _ptr(out), s, T, Hl, Wl, ct, cy, cx, 1 if inverse else 0,
+                                _stream(dev, stream)), "dsv_cube_permute")
+    return out
 
 
 def attn_bwd_preprocess(O, dO, lse, block: int, *, workspace, stream=None) -> None:

@@ -251,6 +251,24 @@ dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, cons
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+dsv_status dsv_cube_permute(const void* src, void* dst, dsv_shape s, int T, int Hl, int Wl, int ct, int cy, int cx,
+                            int inverse, dsv_stream_t stream) {
+  dsv_status v = check_shape(s, false);
+  if (v != DSV_OK) return v;
+  if (T <= 0 || Hl <= 0 || Wl <= 0 || ct <= 0 || cy <= 0 || cx <= 0) return DSV_ERR_INVALID_ARG;
+  if ((long long)T * Hl * Wl != s.N || ct * cy * cx != s.block) return DSV_ERR_INVALID_ARG;
+  if (T % ct != 0 || Hl % cy != 0 || Wl % cx != 0) return DSV_ERR_INVALID_ARG;
+  if (inverse != 0 && inverse != 1) return DSV_ERR_INVALID_ARG;
+  if (empty(s)) return DSV_OK;
+  if (!src || !dst || !al16(src) || !al16(dst)) return DSV_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)s.B * s.H * s.N * s.d * 2;
+  const char* a = static_cast<const char*>(src);
+  const char* b = static_cast<const char*>(dst);
+  if (a < b + bytes && b < a + bytes) return DSV_ERR_INVALID_ARG;   // overlapping buffers
+  return from_cuda(launch_cube_permute(src, dst, s, T, Hl, Wl, ct, cy, cx, inverse,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
 dsv_status dsv_attn_bwd_preprocess(const void* O, const void* dO, const float* lse, dsv_shape s, void* workspace,
                                    size_t workspace_bytes, dsv_stream_t stream) {
   dsv_status v = check_shape(s, false);

@@ -41,6 +41,9 @@ cudaError_t launch_attn_bwd(const void* Q, const CUtensorMap& tmQ, const CUtenso
                             const int32_t* bwd_ptr, const int32_t* bwd_col, float scale, void* dQ, void* dK,
                             void* dV, void* ws, const Ctl& ctl, cudaStream_t st);
 // The stages of launch_attn_bwd (preprocess; dK/dV; dQ).
+// 3D cube query grouping: token rows moved between raster and cube order.
+cudaError_t launch_cube_permute(const void* src, void* dst, const dsv_shape& s, int T, int Hl, int Wl, int ct, int cy,
+                                int cx, int inverse, cudaStream_t st);
 cudaError_t launch_attn_bwd_pre(const void* O, const void* dO, const float* lse, const dsv_shape& s, void* ws,
                                 cudaStream_t st);
 cudaError_t launch_attn_bwd_kv(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,

@@ -190,6 +190,29 @@ dsv_status dsv_attn_bwd_dq(const void* Q, const void* K, const void* V, const vo
                            void* dQ, const void* workspace, size_t workspace_bytes, dsv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * dsv_cube_permute — 3D cube query grouping as a token permutation
+ * ([nl] 2B and [hi] 2B query grouping: adjacent tokens in 3D space share
+ * critical KV, so queries are grouped in small cubes, e.g. 2x2x2)
+ *
+ * The hot path groups s.block consecutive tokens.  This call reorders the
+ * tokens of every (b, h) so that each run of s.block consecutive tokens is
+ * one ct x cy x cx cube of the T x Hl x Wl latent grid: the caller applies
+ * it to Q, K, V, dO before the path and its inverse to O, dQ, dK, dV after.
+ * Raster order n = (t*Hl + y)*Wl + x; cube order walks the cube grid
+ * (T/ct, Hl/cy, Wl/cx) in raster order and the tokens inside a cube in
+ * raster order (lt, ly, lx); perm(n_cube) = n_raster.
+ *   inverse = 0:  dst[b,h,n] = src[b,h,perm(n)]   (raster -> cube order)
+ *   inverse = 1:  dst[b,h,perm(n)] = src[b,h,n]   (cube -> raster order)
+ *
+ * src, dst  bf16 [B,H,N,d] device, 16-byte aligned, not overlapping; dst is
+ *           overwritten.  s.r is ignored.
+ * Requires s.N == T*Hl*Wl, s.block == ct*cy*cx and T % ct == Hl % cy ==
+ * Wl % cx == 0 (DSV_ERR_INVALID_ARG otherwise).
+ * ------------------------------------------------------------------------ */
+dsv_status dsv_cube_permute(const void* src, void* dst, dsv_shape s, int T, int Hl, int Wl, int ct, int cy,
+                            int cx, int inverse, dsv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Status and device-side error reporting.
  * ------------------------------------------------------------------------ */
 const char* dsv_status_string(dsv_status status);

@@ -359,3 +359,45 @@ def attn_bwd_kv_blocks(Q, K, V, dO, fwd_ptr, fwd_col, bwd_ptr, bwd_col, block: i
             dv += dvv[pos * block:(pos + 1) * block]
         out.append((dk, dv))
     return out
+
+
+# --------------------------------------------------------------------------
+# 3D cube query grouping ([nl] 2B, [hi] 2B: adjacent tokens in 3D space share
+# their critical KV; queries are grouped in small cubes, e.g. 2x2x2)
+# --------------------------------------------------------------------------
+
+def cube_order(T: int, Hl: int, Wl: int, ct: int, cy: int, cx: int) -> np.ndarray:
+    """perm[n_cube] = n_raster for the T x Hl x Wl latent grid cut into
+    ct x cy x cx cubes.
+
+    Raster order is n = (t*Hl + y)*Wl + x.  Cube order walks the cube grid
+    (T/ct, Hl/cy, Wl/cx) in raster order and, inside each cube, its tokens in
+    raster order (lt, ly, lx), so every run of ct*cy*cx consecutive positions
+    is one cube: a query group / key block of the hot path becomes a cube.
+    Written as the nested walk it is (small grids only).
+    """
+    if T % ct or Hl % cy or Wl % cx:
+        raise ValueError("the cube must tile the grid")
+    perm = []
+    for bt in range(T // ct):
+        for by in range(Hl // cy):
+            for bx in range(Wl // cx):
+                for lt in range(ct):
+                    for ly in range(cy):
+                        for lx in range(cx):
+                            t, y, x = bt * ct + lt, by * cy + ly, bx * cx + lx
+                            perm.append((t * Hl + y) * Wl + x)
+    return np.asarray(perm, dtype=np.int64)
+
+
+def permute_tokens(X, perm, inverse: bool = False) -> np.ndarray:
+    """Token rows of X [B, H, N, d] into cube order (out[:, :, n] =
+    X[:, :, perm[n]]) or, with inverse, back (out[:, :, perm[n]] = X[:, :, n]).
+    Pure data movement: the dtype is kept."""
+    X = np.asarray(X)
+    perm = np.asarray(perm)
+    if not inverse:
+        return X[:, :, perm]
+    out = np.empty_like(X)
+    out[:, :, perm] = X
+    return out

@@ -125,3 +125,20 @@ def test_host_validation_backward_stages(lib):
     empty = _shape(lib, B=0)
     assert L.dsv_attn_bwd_dq(*p4, empty, None, None, 0.0, None, None, 0, None) == 0
 
+
+
+def test_host_validation_cube_permute(lib):
+    L = lib.lib
+    s = _shape(lib, N=512, block=128)            # grid 2 x 16 x 16, cube 2 x 8 x 8
+    grid, cube = (2, 16, 16), (2, 8, 8)
+    far = FAKE + (64 << 20)                      # a second buffer that does not overlap the first
+    assert L.dsv_cube_permute(FAKE, far, s, 2, 16, 16, 1, 8, 8, 0, None) == lib.DSV_ERR_INVALID_ARG   # volume != block
+    assert L.dsv_cube_permute(FAKE, far, s, 2, 16, 17, *cube, 0, None) == lib.DSV_ERR_INVALID_ARG     # T*Hl*Wl != N
+    assert L.dsv_cube_permute(FAKE, far, _shape(lib, N=384), 2, 12, 16, *cube, 0, None) == \
+        lib.DSV_ERR_INVALID_ARG                                                                         # 12 % 8 != 0
+    assert L.dsv_cube_permute(FAKE, far, s, *grid, *cube, 2, None) == lib.DSV_ERR_INVALID_ARG          # inverse flag
+    assert L.dsv_cube_permute(FAKE, FAKE + 256, s, *grid, *cube, 0, None) == lib.DSV_ERR_INVALID_ARG   # overlap
+    assert L.dsv_cube_permute(None, far, s, *grid, *cube, 0, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_cube_permute(FAKE + 8, far, s, *grid, *cube, 0, None) == lib.DSV_ERR_INVALID_ARG      # alignment
+    assert L.dsv_cube_permute(FAKE, far, _shape(lib, d=96), *grid, *cube, 0, None) == lib.DSV_ERR_UNSUPPORTED
+    assert L.dsv_cube_permute(None, None, _shape(lib, B=0), *grid, *cube, 0, None) == lib.DSV_OK
