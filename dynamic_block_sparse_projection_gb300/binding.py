@@ -9,6 +9,7 @@ module raises.
 from __future__ import annotations
 
 import ctypes
+import math
 from pathlib import Path
 from typing import Optional, Sequence, Tuple
 
@@ -28,7 +29,7 @@ EXPORTS = (
     "dsv_set_wait_limit_ns", "dsv_version",
     "dsv_topk_blocks_noalloc",
     "dsv_attn_bwd_preprocess", "dsv_attn_bwd_dkdv", "dsv_attn_bwd_dq",
-    "dsv_cube_permute",
+    "dsv_cube_permute", "dsv_topk_mass_workspace_bytes", "dsv_topk_mass_blocks",
 )
 
 
@@ -82,6 +83,11 @@ def _load() -> ctypes.CDLL:
     lib.dsv_attn_bwd_dkdv.restype = ctypes.c_int
     lib.dsv_attn_bwd_dq.argtypes = [vp, vp, vp, vp, Shape, vp, vp, ctypes.c_float, vp, vp, sz, vp]
     lib.dsv_attn_bwd_dq.restype = ctypes.c_int
+    lib.dsv_topk_mass_workspace_bytes.argtypes = [Shape]
+    lib.dsv_topk_mass_workspace_bytes.restype = sz
+    lib.dsv_topk_mass_blocks.argtypes = [vp, Shape, ctypes.c_float, ctypes.c_float, i32, i32, vp, vp, vp, vp, sz, vp,
+                                         sz, vp]
+    lib.dsv_topk_mass_blocks.restype = ctypes.c_int
     lib.dsv_cube_permute.argtypes = [vp, vp, Shape, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.dsv_cube_permute.restype = ctypes.c_int
     lib.dsv_version.argtypes = []
@@ -193,6 +199,40 @@ def topk_blocks(scores, k_per_head: Sequence[int], block: int, N: int, d: int = 
     _check(lib.dsv_topk_blocks(_ptr(scores), s, karr, *[_ptr(t) for t in outs], _ptr(ws), nbytes,
                                _stream(dev, stream)), "dsv_topk_blocks")
     fp, fc, bp, bc = outs
+    return fp, fc[:nnz], bp, bc[:nnz]
+
+
+def topk_mass_workspace_bytes(B: int, H: int, N: int, d: int, block: int) -> int:
+    return lib.dsv_topk_mass_workspace_bytes(Shape(B, H, N, d, block, 8))
+
+
+def topk_mass_blocks(scores, tau: float, block: int, N: int, d: int = 128, *, temperature: float = 0.0,
+                     kmin: int = 1, kmax: int = 0, outs=None, workspace=None, stream=None):
+    """(fwd_ptr, fwd_col, bwd_ptr, bwd_col) int32 CSR lists of the
+    mass-threshold selection; see dsv_topk_mass_blocks.  temperature <= 0
+    selects 1/sqrt(d), kmax <= 0 selects nb.  The column arrays are returned
+    cut to nnz = fwd_ptr[-1], which this reads back from the device."""
+    _need(scores, "scores", torch.float32)
+    dev = scores.device
+    B, H, G, nb = scores.shape
+    s = Shape(B, H, N, d, block, 8)
+    temperature = float(temperature) if temperature > 0 else 1.0 / math.sqrt(d)
+    kmax = int(kmax) if kmax > 0 else nb
+    cap = B * H * G * kmax
+    if outs is None:
+        outs = (torch.empty(B * H * G + 1, dtype=torch.int32, device=dev),
+                torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+                torch.empty(B * H * nb + 1, dtype=torch.int32, device=dev),
+                torch.empty(max(cap, 1), dtype=torch.int32, device=dev))
+    for name, t in zip(("fwd_ptr", "fwd_col", "bwd_ptr", "bwd_col"), outs):
+        _need(t, name, torch.int32, dev)
+    cap = min(outs[1].numel(), outs[3].numel())
+    nbytes = lib.dsv_topk_mass_workspace_bytes(s)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(lib.dsv_topk_mass_blocks(_ptr(scores), s, float(tau), temperature, int(kmin), kmax, *[_ptr(t) for t in outs],
+                                    cap, _ptr(ws), nbytes, _stream(dev, stream)), "dsv_topk_mass_blocks")
+    fp, fc, bp, bc = outs
+    nnz = int(fp[-1].item()) if B * H * G > 0 else 0
     return fp, fc[:nnz], bp, bc[:nnz]
 
 

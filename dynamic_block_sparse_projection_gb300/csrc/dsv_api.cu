@@ -201,6 +201,38 @@ dsv_status dsv_topk_blocks(const float* scores, dsv_shape s, const int32_t* k_pe
   return from_cuda(launch_topk(scores, s, hk, nnz, fwd_ptr, fwd_col, bwd_ptr, bwd_col, workspace, st));
 }
 
+size_t dsv_topk_mass_workspace_bytes(dsv_shape s) {
+  if (check_shape(s, false) != DSV_OK || empty(s)) return 0;
+  return topk_mass_ws_bytes(s);
+}
+
+dsv_status dsv_topk_mass_blocks(const float* scores, dsv_shape s, float tau, float temperature, int32_t kmin,
+                                int32_t kmax, int32_t* fwd_ptr, int32_t* fwd_col, int32_t* bwd_ptr, int32_t* bwd_col,
+                                size_t col_capacity, void* workspace, size_t workspace_bytes, dsv_stream_t stream) {
+  dsv_status v = check_shape(s, false);
+  if (v != DSV_OK) return v;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!fwd_ptr || !bwd_ptr) return DSV_ERR_INVALID_ARG;
+  if (!(tau > 0.f && tau <= 1.f) || !(temperature > 0.f) || !isfinite(temperature)) return DSV_ERR_INVALID_ARG;
+  if (empty(s)) {
+    cudaError_t e = cudaMemsetAsync(fwd_ptr, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(bwd_ptr, 0, sizeof(int32_t), st);
+    return from_cuda(e);
+  }
+  const int nb = s.N / s.block;
+  if (nb > kMaxBlocksPerRow) return DSV_ERR_UNSUPPORTED;
+  if (kmin < 1 || kmin > kmax || kmax > nb) return DSV_ERR_INVALID_ARG;
+  if (!scores || !fwd_col || !bwd_col || !workspace) return DSV_ERR_INVALID_ARG;
+  if (!al16(scores) || !al16(fwd_ptr) || !al16(fwd_col) || !al16(bwd_ptr) || !al16(bwd_col) || !al256(workspace))
+    return DSV_ERR_INVALID_ARG;
+  if (workspace_bytes < topk_mass_ws_bytes(s)) return DSV_ERR_INVALID_ARG;
+  const long long cap = (long long)s.B * s.H * nb * kmax;   // every row at most kmax entries
+  if (cap > INT32_MAX) return DSV_ERR_UNSUPPORTED;
+  if ((long long)col_capacity < cap) return DSV_ERR_INVALID_ARG;
+  return from_cuda(
+      launch_topk_mass(scores, s, tau, temperature, kmin, kmax, fwd_ptr, fwd_col, bwd_ptr, bwd_col, workspace, st));
+}
+
 dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const void* V, dsv_shape s, const int32_t* fwd_ptr,
                                const int32_t* fwd_col, float softmax_scale, void* O, float* lse,
                                dsv_stream_t stream) {

@@ -28,6 +28,12 @@ size_t predict_ws_bytes(const dsv_shape& s);
 cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk, int64_t nnz, int32_t* fwd_ptr,
                         int32_t* fwd_col, int32_t* bwd_ptr, int32_t* bwd_col, void* ws, cudaStream_t st);
 size_t topk_ws_bytes(const dsv_shape& s);
+// Mass-threshold selection: per row the smallest top set carrying >= tau of
+// the predicted softmax mass (temperature * scores), clamped to [kmin, kmax].
+cudaError_t launch_topk_mass(const float* scores, const dsv_shape& s, float tau, float temperature, int kmin,
+                             int kmax, int32_t* fwd_ptr, int32_t* fwd_col, int32_t* bwd_ptr, int32_t* bwd_col,
+                             void* ws, cudaStream_t st);
+size_t topk_mass_ws_bytes(const dsv_shape& s);
 
 // Attention forward.  Tensor maps cover [B*H*N, d] bf16 with a 64-column box.
 cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,

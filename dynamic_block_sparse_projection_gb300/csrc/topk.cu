@@ -47,6 +47,11 @@ struct TopkArgs {
   long long rows;   // B*H*G
   int nnz;
   HeadK hk;
+  // per-row list sizes (mass-threshold selection): k and the list start of
+  // row r are row_k[r] and row_ptr[r] (fwd_ptr, already written), the head's
+  // first entry row_ptr[bh * G] and the total row_ptr[rows]; null: k per head
+  const int32_t* row_k;
+  const int32_t* row_ptr;
 };
 
 // One CTA of RT threads per row.  Thread t holds kE consecutive scores
@@ -193,8 +198,9 @@ __global__ void __launch_bounds__(RT, select_min_blocks(RT)) topk_select_kernel(
   const int g = (int)(row - bh * a.G);
   const int h = (int)(bh % a.H);
   const int b = (int)(bh / a.H);
-  const uint32_t k = (uint32_t)a.hk.k[h];
-  const long long base = (long long)b * a.G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * a.G + (long long)g * k;
+  const uint32_t k = a.row_k ? (uint32_t)a.row_k[row] : (uint32_t)a.hk.k[h];
+  const long long base = a.row_k ? (long long)a.row_ptr[row]
+                                 : (long long)b * a.G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * a.G + (long long)g * k;
   int32_t* dst = a.fwd_col + base;
   // mask word (b, h, ci, g): word columns contiguous over g for the transpose kernels
   uint32_t* mcol = a.mask + bh * (long long)a.words * a.G + g;
@@ -464,8 +470,10 @@ __global__ void __launch_bounds__(RT, select_min_blocks(RT)) topk_select_kernel(
   }
 
   if (t == 0) {
-    a.fwd_ptr[row] = (int32_t)base;
-    if (row == a.rows - 1) a.fwd_ptr[a.rows] = a.nnz;
+    if (!a.row_k) {
+      a.fwd_ptr[row] = (int32_t)base;
+      if (row == a.rows - 1) a.fwd_ptr[a.rows] = a.nnz;
+    }
   }
 }
 
@@ -544,7 +552,8 @@ __global__ void __launch_bounds__(1024) topk_scan_kernel(int32_t* __restrict__ c
     warp_tot[lane] = x;  // inclusive over warps
   }
   __syncthreads();
-  const long long base = (long long)b * a.G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * a.G;
+  const long long base = a.row_k ? (long long)a.row_ptr[bh * a.G]
+                                 : (long long)b * a.G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * a.G;
   int run = (int)base + (w > 0 ? warp_tot[w - 1] : 0) + inc - loc;
   for (int j = j0; j < min(nb, j0 + per); ++j) {
     bwd_ptr[bh * nb + j] = run;
@@ -554,7 +563,7 @@ __global__ void __launch_bounds__(1024) topk_scan_kernel(int32_t* __restrict__ c
       run += c;
     }
   }
-  if (bh == nslices - 1 && t == 0) bwd_ptr[nslices * nb] = a.nnz;
+  if (bh == nslices - 1 && t == 0) bwd_ptr[nslices * nb] = a.row_k ? a.row_ptr[a.rows] : a.nnz;
 }
 
 // Each warp walks the G rows of 32 mask columns (one word column), 32 rows at a
@@ -610,6 +619,331 @@ __global__ void __launch_bounds__(kFillWarps * 32) topk_fill_kernel(const uint32
   flush(__ballot_sync(0xffffffffu, cnt > 0));
 }
 
+// ---------------------------------------------------------------------------
+// Mass-threshold selection: the list size m of each row.
+//
+// DSV pages [nl] 2A and [hi] 2A: the critical KV pairs are those that carry
+// about 90 % of the attention score.  The predicted mass of block j in row r
+// is p_j = softmax(temperature * S_r)_j; with the blocks in rank order
+// (larger score first, equal scores by lower index) m is the smallest count
+// whose leading blocks carry mass >= tau, clamped to [kmin, kmax]; the row
+// then keeps its top m blocks (topk_select with per-row k).
+//
+// One CTA per row, 16 consecutive scores per thread as in topk_select.  The
+// masses are fixed-point integers, P_j = round(2^40 exp2((s_j - max) c)), so
+// every sum is exact and independent of the order of the atomics; the target
+// is ceil(tau * sum P).  A histogram of counts and masses over value buckets
+// finds the bucket where the leading mass reaches the target; if it holds at
+// most kCandMax scores they are ranked exactly, else the search goes on
+// inside that bucket with 11-bit radix digits of the order-preserving keys
+// below their common prefix, until the remaining scores are all equal (then
+// m follows by division).  A row holding a non-finite score gets m = kmax.
+// ---------------------------------------------------------------------------
+struct MassArgs {
+  const float* scores;
+  int32_t* m_out;
+  int nb;
+  long long rows;
+  float coef;                            // temperature * log2(e)
+  double tau;
+  int kmin, kmax;
+};
+
+constexpr float kMassOne = 1099511627776.0f;   // 2^40: fixed-point unit of a mass
+
+// 128 registers a thread: the 16 keys, masses (64-bit) and buckets stay in registers
+constexpr int mass_min_blocks(int rt) { return rt >= 128 ? 512 / rt : 1; }
+
+template <int RT>
+__global__ void __launch_bounds__(RT, mass_min_blocks(RT)) topk_mass_count_kernel(const __grid_constant__ MassArgs a) {
+  using u64 = unsigned long long;
+  constexpr int E = kE;
+  constexpr int kBins = SelCfg<RT>::BINS;
+  constexpr int kDigit = SelCfg<RT>::DIGIT;
+  constexpr int NW = RT / 32;
+  constexpr int BPT = kBins / RT;
+  __shared__ uint32_t hcnt[kBins];
+  __shared__ u64 hmass[kBins];
+  __shared__ u64 s_u[NW];
+  __shared__ uint32_t s_w[2 * NW];
+  __shared__ uint32_t s_bin, s_cnt;
+  __shared__ u64 s_above, s_above_cnt;
+  __shared__ uint32_t candk[kCandMax];
+  __shared__ int32_t candi[kCandMax];
+  __shared__ u64 candp[kCandMax];
+  __shared__ u64 sortedp[kCandMax];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const long long row = blockIdx.x;
+  const int nb = a.nb;
+  const float* src = a.scores + row * (long long)nb;
+  const int i0 = E * t;
+  float x[E];
+  uint32_t inplay = 0u;                  // slots in the search
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = i0 + e;
+    x[e] = i < nb ? __ldg(src + i) : 0.f;
+    if (i < nb) inplay |= 1u << e;
+  }
+  // CTA-wide helpers (every thread calls them)
+  auto cta_max = [&](float v) -> float {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if (lane == 0) s_w[w] = __float_as_uint(v);
+    __syncthreads();
+    float r = __uint_as_float(s_w[0]);
+    for (int q = 1; q < NW; ++q) r = fmaxf(r, __uint_as_float(s_w[q]));
+    return r;
+  };
+  auto cta_sum64 = [&](u64 v) -> u64 {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if (lane == 0) s_u[w] = v;
+    __syncthreads();
+    u64 r = 0;
+    for (int q = 0; q < NW; ++q) r += s_u[q];
+    return r;
+  };
+  auto cta_and_or = [&](uint32_t& va, uint32_t& vo) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      va &= __shfl_xor_sync(0xffffffffu, va, o);
+      vo |= __shfl_xor_sync(0xffffffffu, vo, o);
+    }
+    __syncthreads();
+    if (lane == 0) {
+      s_w[w] = va;
+      s_w[NW + w] = vo;
+    }
+    __syncthreads();
+    va = 0xffffffffu;
+    vo = 0u;
+    for (int q = 0; q < NW; ++q) {
+      va &= s_w[q];
+      vo |= s_w[NW + q];
+    }
+  };
+
+  // a non-finite score: m = kmax
+  bool bad = false;
+#pragma unroll
+  for (int e = 0; e < E; ++e) bad |= ((inplay >> e) & 1u) && !isfinite(x[e]);
+  if (__syncthreads_or(bad)) {
+    if (t == 0) a.m_out[row] = a.kmax;
+    return;
+  }
+  float mx = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if ((inplay >> e) & 1u) mx = fmaxf(mx, x[e]);
+  const float hi = cta_max(mx);
+  u64 P[E];
+  u64 zs = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    P[e] = ((inplay >> e) & 1u) ? (u64)__float2ull_rn(exp2f((x[e] - hi) * a.coef) * kMassOne) : 0ull;
+    zs += P[e];
+  }
+  const u64 Z = cta_sum64(zs);
+  u64 target = (u64)ceil(a.tau * (double)Z);
+  if (target > Z) target = Z;
+  if (target == 0) target = 1;
+  u64 mass_above = 0, cnt_above = 0;     // of the scores ranked above those still in play
+  long long m = -1;
+  uint32_t keys[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) keys[e] = score_key(x[e]);
+  for (int level = 0; level < 5 && m < 0; ++level) {
+    // bucket of every score in play: value buckets first, then radix digits
+    uint32_t va = 0xffffffffu, vo = 0u;
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if ((inplay >> e) & 1u) {
+        va &= keys[e];
+        vo |= keys[e];
+      }
+    cta_and_or(va, vo);
+    const uint32_t diff = va ^ vo;
+    if (diff == 0u) {
+      // all scores in play are equal (equal masses): take as many as needed
+      u64 pe = 0;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if ((inplay >> e) & 1u) pe = P[e];
+      for (int o = 16; o > 0; o >>= 1) pe = max(pe, __shfl_xor_sync(0xffffffffu, pe, o));
+      __syncthreads();
+      if (lane == 0) s_u[w] = pe;
+      __syncthreads();
+      for (int q = 0; q < NW; ++q) pe = max(pe, s_u[q]);
+      const u64 need = target - mass_above;
+      m = (long long)cnt_above + (long long)((need + pe - 1) / (pe > 0 ? pe : 1));
+      break;
+    }
+    const int remaining = 32 - __clz(diff);
+    const int nbits = remaining < kDigit ? remaining : kDigit;
+    const int sh = remaining - nbits;
+    float scale = 0.f, c0 = 0.f, lo = 0.f, hv = 0.f;
+    bool by_value = false;
+    if (level == 0) {
+      float mn = INFINITY;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if ((inplay >> e) & 1u) mn = fminf(mn, x[e]);
+      lo = -cta_max(-mn);
+      hv = hi;
+      scale = __fdividef((float)(kBins - 1), hv - lo);
+      by_value = hv > lo && scale > 0.f && scale < 1e30f;
+      c0 = 12582912.0f - lo * scale;
+    }
+    uint32_t bk[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if (by_value) {
+        bk[e] = __float_as_uint(fminf(fmaxf(fmaf(x[e], scale, c0), 12582912.0f), 12582912.0f + (float)(kBins - 1))) -
+                0x4B400000u;
+      } else {
+        bk[e] = (keys[e] >> sh) & ((1u << nbits) - 1u);
+      }
+    }
+    for (int i = t; i < kBins; i += RT) {
+      hcnt[i] = 0u;
+      hmass[i] = 0ull;
+    }
+    if (t == 0) s_cnt = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if ((inplay >> e) & 1u) {
+        atomicAdd(&hcnt[bk[e]], 1u);
+        atomicAdd(&hmass[bk[e]], P[e]);
+      }
+    __syncthreads();
+    // the bucket where the leading mass reaches the target: suffix sums from the top bucket down
+    u64 tm = 0;
+    uint32_t tc = 0;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      tm += hmass[t * BPT + i];
+      tc += hcnt[t * BPT + i];
+    }
+    u64 sm = tm;
+    uint32_t sc = tc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const u64 vm = __shfl_down_sync(0xffffffffu, sm, o);
+      const uint32_t vc = __shfl_down_sync(0xffffffffu, sc, o);
+      if (lane + o < 32) {
+        sm += vm;
+        sc += vc;
+      }
+    }
+    if (lane == 0) {
+      s_u[w] = sm;
+      s_w[w] = sc;
+    }
+    __syncthreads();
+    for (int q = w + 1; q < NW; ++q) {
+      sm += s_u[q];
+      sc += s_w[q];
+    }
+    u64 above = mass_above + (sm - tm);          // mass of the buckets above this thread's range
+    uint32_t above_c = sc - tc;
+    if (above < target && above + tm >= target) {
+      for (int i = BPT - 1; i >= 0; --i) {
+        const u64 c = hmass[t * BPT + i];
+        if (above + c >= target) {
+          s_bin = (uint32_t)(t * BPT + i);
+          s_above = above;
+          s_above_cnt = cnt_above + above_c;
+          break;
+        }
+        above += c;
+        above_c += hcnt[t * BPT + i];
+      }
+    }
+    __syncthreads();
+    const uint32_t bstar = s_bin;
+    mass_above = s_above;
+    cnt_above = s_above_cnt;
+    const uint32_t C = hcnt[bstar];
+    // only the scores of bucket b* stay in play
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (bk[e] != bstar) inplay &= ~(1u << e);
+    if (C <= (uint32_t)kCandMax) {
+      // rank the bucket exactly by (key desc, index asc) and walk its masses in that order
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if ((inplay >> e) & 1u) {
+          const uint32_t pos = atomicAdd(&s_cnt, 1u);
+          candk[pos] = keys[e];
+          candi[pos] = i0 + e;
+          candp[pos] = P[e];
+        }
+      __syncthreads();
+      for (uint32_t c = t; c < C; c += RT) {
+        const uint32_t kc = candk[c];
+        const int ic = candi[c];
+        uint32_t rank = 0;
+        for (uint32_t c2 = 0; c2 < C; ++c2) {
+          const uint32_t k2 = candk[c2];
+          rank += (k2 > kc || (k2 == kc && candi[c2] < ic)) ? 1u : 0u;
+        }
+        sortedp[rank] = candp[c];
+      }
+      __syncthreads();
+      if (t == 0) {
+        u64 run = mass_above;
+        uint32_t r = 0;
+        while (r + 1 < C && run + sortedp[r] < target) run += sortedp[r++];
+        s_w[0] = r + 1;                          // how many of the bucket are needed
+      }
+      __syncthreads();
+      m = (long long)cnt_above + (long long)s_w[0];
+    }
+    __syncthreads();                             // s_* and the histograms are reused
+  }
+  if (m < 0) m = a.kmax;                         // not reached: the digits run out first
+  if (t == 0) a.m_out[row] = (int32_t)(m < a.kmin ? a.kmin : (m > a.kmax ? a.kmax : m));
+}
+
+// fwd_ptr[r] = sum of m over rows before r, fwd_ptr[rows] = the total (one CTA)
+__global__ void __launch_bounds__(1024) topk_row_scan_kernel(const int32_t* __restrict__ m, long long rows,
+                                                             int32_t* __restrict__ fwd_ptr) {
+  __shared__ long long warp_tot[32];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const long long per = (rows + 1023) / 1024;
+  const long long j0 = t * per, j1 = j0 + per < rows ? j0 + per : rows;
+  long long loc = 0;
+  for (long long j = j0; j < j1; ++j) loc += m[j];
+  long long inc = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) warp_tot[w] = inc;
+  __syncthreads();
+  if (w == 0) {
+    long long v = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    warp_tot[lane] = v;
+  }
+  __syncthreads();
+  long long run = (w > 0 ? warp_tot[w - 1] : 0) + inc - loc;
+  for (long long j = j0; j < j1; ++j) {
+    fwd_ptr[j] = (int32_t)run;
+    run += m[j];
+  }
+  if (t == 1023) fwd_ptr[rows] = (int32_t)warp_tot[31];
+}
+
 }  // namespace
 
 size_t topk_ws_bytes(const dsv_shape& s) {
@@ -620,26 +954,12 @@ size_t topk_ws_bytes(const dsv_shape& s) {
   return align256(bhs * G * words * sizeof(uint32_t)) + align256(bhs * nseg * G * sizeof(int32_t));
 }
 
-cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk, int64_t nnz, int32_t* fwd_ptr,
-                        int32_t* fwd_col, int32_t* bwd_ptr, int32_t* bwd_col, void* ws, cudaStream_t st) {
-  const int G = s.N / s.block;
-  const int words = (G + 31) / 32;
-  const long long bhs = (long long)s.B * s.H;
-  uint32_t* mask = static_cast<uint32_t*>(ws);
-  int32_t* counts =
-      reinterpret_cast<int32_t*>(static_cast<char*>(ws) + align256((size_t)bhs * G * words * sizeof(uint32_t)));
-  TopkArgs a;
-  a.scores = scores;
-  a.fwd_ptr = fwd_ptr;
-  a.fwd_col = fwd_col;
-  a.mask = mask;
-  a.H = s.H;
-  a.G = G;
-  a.nb = G;
-  a.words = words;
-  a.rows = bhs * G;
-  a.nnz = (int)nnz;
-  a.hk = hk;
+namespace {
+
+// the select kernel and the transposed lists, for fixed (a.row_k == null) or per-row k
+cudaError_t run_topk(const TopkArgs& a, int32_t* bwd_ptr, int32_t* bwd_col, int32_t* counts, cudaStream_t st) {
+  const int G = a.G, words = a.words;
+  const long long bhs = a.rows / G;
   // threads per row: the smallest of 32 ... 512 holding the row in 16 keys per
   // thread (32 keys per thread measured slower on 4050-block rows: half the
   // threads per SM for the load latency)
@@ -653,13 +973,80 @@ cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int nseg = (G + kSeg - 1) / kSeg;
   dim3 g2((unsigned)((words + 7) / 8), (unsigned)nseg, (unsigned)bhs);
-  topk_colcount_kernel<<<g2, 256, 0, st>>>(mask, G, G, words, counts);
+  topk_colcount_kernel<<<g2, 256, 0, st>>>(a.mask, G, G, words, counts);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   topk_scan_kernel<<<(unsigned)bhs, 1024, 0, st>>>(counts, nseg, a, bwd_ptr, bhs);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   dim3 g3((unsigned)((words + kFillWarps - 1) / kFillWarps), (unsigned)nseg, (unsigned)bhs);
-  topk_fill_kernel<<<g3, kFillWarps * 32, 0, st>>>(mask, G, G, words, counts, bwd_col);
+  topk_fill_kernel<<<g3, kFillWarps * 32, 0, st>>>(a.mask, G, G, words, counts, bwd_col);
   return cudaGetLastError();
+}
+
+TopkArgs topk_args(const float* scores, const dsv_shape& s, int32_t* fwd_ptr, int32_t* fwd_col, void* ws) {
+  const int G = s.N / s.block;
+  TopkArgs a{};
+  a.scores = scores;
+  a.fwd_ptr = fwd_ptr;
+  a.fwd_col = fwd_col;
+  a.mask = static_cast<uint32_t*>(ws);
+  a.H = s.H;
+  a.G = G;
+  a.nb = G;
+  a.words = (G + 31) / 32;
+  a.rows = (long long)s.B * s.H * G;
+  a.row_k = nullptr;
+  a.row_ptr = nullptr;
+  return a;
+}
+
+int32_t* topk_counts(void* ws, const dsv_shape& s) {
+  const size_t G = (size_t)(s.N / s.block);
+  return reinterpret_cast<int32_t*>(static_cast<char*>(ws) +
+                                    align256((size_t)s.B * s.H * G * ((G + 31) / 32) * sizeof(uint32_t)));
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk, int64_t nnz, int32_t* fwd_ptr,
+                        int32_t* fwd_col, int32_t* bwd_ptr, int32_t* bwd_col, void* ws, cudaStream_t st) {
+  TopkArgs a = topk_args(scores, s, fwd_ptr, fwd_col, ws);
+  a.nnz = (int)nnz;
+  a.hk = hk;
+  return run_topk(a, bwd_ptr, bwd_col, topk_counts(ws, s), st);
+}
+
+size_t topk_mass_ws_bytes(const dsv_shape& s) {
+  return topk_ws_bytes(s) + align256((size_t)s.B * s.H * (size_t)(s.N / s.block) * sizeof(int32_t));
+}
+
+cudaError_t launch_topk_mass(const float* scores, const dsv_shape& s, float tau, float temperature, int kmin,
+                             int kmax, int32_t* fwd_ptr, int32_t* fwd_col, int32_t* bwd_ptr, int32_t* bwd_col,
+                             void* ws, cudaStream_t st) {
+  TopkArgs a = topk_args(scores, s, fwd_ptr, fwd_col, ws);
+  int32_t* m = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + topk_ws_bytes(s));
+  MassArgs ma;
+  ma.scores = scores;
+  ma.m_out = m;
+  ma.nb = a.nb;
+  ma.rows = a.rows;
+  ma.coef = temperature * 1.4426950408889634f;
+  ma.tau = (double)tau;
+  ma.kmin = kmin;
+  ma.kmax = kmax;
+  const unsigned grid = (unsigned)a.rows;
+  const int G = a.G;
+  if (G <= 32 * kE) topk_mass_count_kernel<32><<<grid, 32, 0, st>>>(ma);
+  else if (G <= 64 * kE) topk_mass_count_kernel<64><<<grid, 64, 0, st>>>(ma);
+  else if (G <= 128 * kE) topk_mass_count_kernel<128><<<grid, 128, 0, st>>>(ma);
+  else if (G <= 256 * kE) topk_mass_count_kernel<256><<<grid, 256, 0, st>>>(ma);
+  else topk_mass_count_kernel<512><<<grid, 512, 0, st>>>(ma);
+  cudaError_t e;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  topk_row_scan_kernel<<<1, 1024, 0, st>>>(m, a.rows, fwd_ptr);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  a.row_k = m;
+  a.row_ptr = fwd_ptr;
+  return run_topk(a, bwd_ptr, bwd_col, topk_counts(ws, s), st);
 }
 
 }  // namespace dsv

@@ -105,6 +105,35 @@ dsv_status dsv_topk_blocks(const float* scores, dsv_shape s, const int32_t* k_pe
                            void* workspace, size_t workspace_bytes, dsv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * dsv_topk_mass_blocks — mass-threshold selection of the critical key blocks
+ * ([nl] 2A and [hi] 2A: the critical KV pairs carry about 90 % of the
+ * attention score)
+ *
+ * For every row (b,h,g): p_j = softmax(temperature * scores[b,h,g,:])_j is
+ * the predicted attention mass of block j; with the blocks in rank order
+ * (larger score first, equal scores to the lower j) m is the smallest count
+ * whose leading blocks carry mass >= tau, clamped to [kmin, kmax], and the row
+ * keeps its top m blocks, listed in ascending j.  A row holding a non-finite
+ * score gets m = kmax.  The masses are summed in fixed point (2^-40 units,
+ * exact and independent of order, fp32 exponentials), so m can differ from an
+ * exact-arithmetic count only where the leading mass passes tau within about
+ * 1e-6.
+ *
+ * Arguments and outputs as dsv_topk_blocks, except that the rows have
+ * variable lengths: nnz = fwd_ptr[B*H*G] = bwd_ptr[B*H*nb] (device).
+ * fwd_col, bwd_col   int32 arrays of col_capacity >= B*H*G*kmax entries.
+ * tau                in (0, 1]; temperature > 0, finite; 1 <= kmin <= kmax <= nb.
+ * workspace          >= dsv_topk_mass_workspace_bytes(s) bytes, 256-byte aligned
+ *                    (that of dsv_topk_blocks plus the row sizes).
+ * DSV_ERR_UNSUPPORTED if B*H*G*kmax >= 2^31 (or as dsv_topk_blocks).
+ * ------------------------------------------------------------------------ */
+size_t dsv_topk_mass_workspace_bytes(dsv_shape s);
+dsv_status dsv_topk_mass_blocks(const float* scores, dsv_shape s, float tau, float temperature,
+                                int32_t kmin, int32_t kmax, int32_t* fwd_ptr, int32_t* fwd_col,
+                                int32_t* bwd_ptr, int32_t* bwd_col, size_t col_capacity,
+                                void* workspace, size_t workspace_bytes, dsv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * dsv_topk_blocks_noalloc — dsv_topk_blocks for callers that cannot allocate
  * (the DSV pages have no counterpart: this is a deployment convenience)
  *

@@ -401,3 +401,41 @@ def permute_tokens(X, perm, inverse: bool = False) -> np.ndarray:
     out = np.empty_like(X)
     out[:, :, perm] = X
     return out
+
+
+# --------------------------------------------------------------------------
+# Mass-threshold selection ([nl] 2A and [hi] 2A: the critical KV pairs are
+# those that carry about 90 % of the attention score)
+# --------------------------------------------------------------------------
+
+def mass_count_row(scores_row, tau: float, temperature: float, kmin: int, kmax: int) -> int:
+    """m of one row: the predicted attention mass of block j is
+    p_j = softmax(temperature * s)_j over the row; with the blocks in rank
+    order (larger score first, equal scores by lower index), m is the
+    smallest count whose leading blocks carry p-mass >= tau, clamped to
+    [kmin, kmax].  A row holding a non-finite score gets m = kmax."""
+    s = _f64(scores_row)
+    if not np.all(np.isfinite(s)):
+        return int(kmax)
+    z = temperature * s
+    p = np.exp(z - z.max())
+    p = p / p.sum()
+    cum = np.cumsum(p[_rank_order(s[None, :])[0]])
+    m = min(int(np.searchsorted(cum, tau, side="left")) + 1, s.shape[0])
+    return int(min(max(m, kmin), kmax))
+
+
+def mass_lists(S, tau: float, temperature: float, kmin: int, kmax: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Forward CSR over all rows (b, h, g) of the mass-threshold selection:
+    row (b, h, g) keeps the top mass_count_row(...) blocks, ascending."""
+    S = _f64(S)
+    B, H, G, nb = S.shape
+    ptr = [0]
+    cols = []
+    for b in range(B):
+        for h in range(H):
+            for g in range(G):
+                m = mass_count_row(S[b, h, g], tau, temperature, kmin, kmax)
+                cols.append(topk_row(S[b, h, g], m))
+                ptr.append(ptr[-1] + m)
+    return np.asarray(ptr, dtype=np.int64), (np.concatenate(cols).astype(np.int64) if cols else np.zeros(0, np.int64))

@@ -142,3 +142,22 @@ def test_host_validation_cube_permute(lib):
     assert L.dsv_cube_permute(FAKE + 8, far, s, *grid, *cube, 0, None) == lib.DSV_ERR_INVALID_ARG      # alignment
     assert L.dsv_cube_permute(FAKE, far, _shape(lib, d=96), *grid, *cube, 0, None) == lib.DSV_ERR_UNSUPPORTED
     assert L.dsv_cube_permute(None, None, _shape(lib, B=0), *grid, *cube, 0, None) == lib.DSV_OK
+
+
+def test_host_validation_topk_mass(lib):
+    L = lib.lib
+    s = _shape(lib)                               # nb = 4
+    ws = L.dsv_topk_mass_workspace_bytes(s)
+    assert ws > L.dsv_topk_workspace_bytes(s)
+    cap = 1 * 2 * 4 * 4
+    ok = (FAKE, FAKE, FAKE, FAKE)
+
+    def call(tau=0.9, temp=0.1, kmin=1, kmax=4, capacity=cap, wsb=ws, shape=s):
+        return L.dsv_topk_mass_blocks(FAKE, shape, tau, temp, kmin, kmax, *ok, capacity, FAKE, wsb, None)
+    for bad in (dict(tau=0.0), dict(tau=1.5), dict(tau=float("nan")), dict(temp=0.0), dict(temp=float("inf")),
+                dict(kmin=0), dict(kmin=3, kmax=2), dict(kmax=5), dict(capacity=cap - 1), dict(wsb=ws - 1)):
+        assert call(**bad) == lib.DSV_ERR_INVALID_ARG, bad
+    assert call(shape=_shape(lib, d=96)) == lib.DSV_ERR_UNSUPPORTED
+    big = _shape(lib, N=128 * 8193, H=1)
+    assert L.dsv_topk_mass_blocks(FAKE, big, 0.9, 0.1, 1, 4, *ok, 1 << 40, FAKE, 1 << 40, None) == \
+        lib.DSV_ERR_UNSUPPORTED
