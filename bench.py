@@ -47,6 +47,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="latent16k")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--mass", type=float, default=0.0, metavar="TAU",
+                   help="select per group the smallest top set carrying >= TAU of the predicted mass (instead of top-k)")
     p.add_argument("--cube", default="", metavar="CT,CY,CX",
                    help="regroup tokens into ct x cy x cx cubes of the latent grid inside the step")
     p.add_argument("--no-dense", action="store_true")
@@ -162,15 +164,17 @@ class HotPath:
     its inverse on O, dQ, dK, dV after it), so that query groups and key
     blocks are cubes; O and the gradients then come out in raster order."""
 
-    def __init__(self, dsv, x, w, k_per_head, cube=None):
+    def __init__(self, dsv, x, w, k_per_head, cube=None, mass=None):
         import torch
         self.dsv, self.x, self.w = dsv, x, w
         self.k = list(k_per_head)
         self.cube = tuple(cube) if cube else None
+        self.mass = mass                 # tau of the mass-threshold selection, or None for top-k
         self.grid = (w.T, w.Hl, w.Wl)
         dev = x.Q.device
         B, H, N, d, G = w.B, w.H, w.N, w.d, w.nb
-        self.nnz = dsv.nnz_of(B, G, self.k)
+        # the mass selection's list sizes are known only on the device: room for every block
+        self.nnz = B * H * G * G if mass else dsv.nnz_of(B, G, self.k)
         self.S = torch.empty(B, H, G, G, dtype=torch.float32, device=dev)
         self.lists = (torch.empty(B * H * G + 1, dtype=torch.int32, device=dev),
                       torch.empty(self.nnz, dtype=torch.int32, device=dev),
@@ -181,7 +185,8 @@ class HotPath:
         self.grads = (torch.empty_like(x.Q), torch.empty_like(x.K), torch.empty_like(x.V))
         u8 = torch.uint8
         self.ws_p = torch.empty(max(1, dsv.predict_workspace_bytes(B, H, N, d, w.block, w.r)), dtype=u8, device=dev)
-        self.ws_t = torch.empty(max(1, dsv.topk_workspace_bytes(B, H, N, d, w.block)), dtype=u8, device=dev)
+        self.ws_t = torch.empty(max(1, (dsv.topk_mass_workspace_bytes if mass else dsv.topk_workspace_bytes)(
+            B, H, N, d, w.block)), dtype=u8, device=dev)
         self.ws_b = torch.empty(max(1, dsv.attn_bwd_workspace_bytes(B, H, N, d, w.block)), dtype=u8, device=dev)
         if self.cube:
             # the path's inputs in cube order, and O / gradients back in raster order
@@ -215,7 +220,11 @@ class HotPath:
             x = self.xc
         d.predict_scores(x.Q, x.K, x.Wq, x.Wk, w.block, out=self.S, workspace=self.ws_p)
         mark()
-        fp, fc, bp, bc = d.topk_blocks(self.S, self.k, w.block, w.N, w.d, outs=self.lists, workspace=self.ws_t)
+        if self.mass:
+            fp, fc, bp, bc = d.topk_mass_blocks(self.S, self.mass, w.block, w.N, w.d, outs=self.lists,
+                                                workspace=self.ws_t, trim=False)
+        else:
+            fp, fc, bp, bc = d.topk_blocks(self.S, self.k, w.block, w.N, w.d, outs=self.lists, workspace=self.ws_t)
         mark()
         d.sparse_attn_fwd(x.Q, x.K, x.V, fp, fc, w.block, out=self.O, lse=self.lse)
         mark()
@@ -288,14 +297,16 @@ def run_ours(args):
     w = wl.WORKLOADS[args.workload]
     x = wl.make_inputs(w, device=dev)
     cube = tuple(int(v) for v in args.cube.split(",")) if args.cube else None
-    hp = HotPath(dsv, x, w, x.k_per_head, cube=cube)
+    hp = HotPath(dsv, x, w, x.k_per_head, cube=cube, mass=args.mass or None)
     fwd_f, bwd_f = pair_flops(w.block, w.d)
-    step_flops = (fwd_f + bwd_f) * hp.nnz
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     for _ in range(max(3, args.warmup)):
         hp.run()
     torch.cuda.synchronize()
+    if hp.mass:
+        hp.nnz = int(hp.lists[0][-1].item())      # the pairs the selection kept (the same every step)
+    step_flops = (fwd_f + bwd_f) * hp.nnz
     st, info = dsv.device_error()
     if st != 0:
         raise RuntimeError(f"device error {dsv.status_string(st)} ({info})")
@@ -345,10 +356,13 @@ def run_ours(args):
         "warmup": max(3, args.warmup), "ms_per_step": round(total_ms_max / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "description": w.description, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "block": w.block, "r": w.r, "k_per_head": sorted(set(x.k_per_head)), "pairs": hp.nnz,
+                   "block": w.block, "r": w.r,
+                   "k_per_head": None if args.mass else sorted(set(x.k_per_head)), "pairs": hp.nnz,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                    **({"cube": list(cube), "token_order": "3D cubes (dsv_cube_permute in and out, timed)"}
                       if cube else {}),
+                   **({"selection": f"mass threshold tau={args.mass}, temperature 1/sqrt(d), k in [1, nb]"}
+                      if args.mass else {}),
                    "l2": "flushed before every step (256 MiB write, outside the step events); "
                          "inputs are also larger than L2"},
         "pct_of_bf16_peak": round(100.0 * value / peaks["bf16_tflops"], 2),
@@ -359,13 +373,13 @@ def run_ours(args):
         "breakdown_ms": {k: round(v, 4) for k, v in per_call.items()},
         "speedup_vs_dense": dense,
         "roofline": roofline,
-        "gpu_launches": sum(KERNELS_PER_STEP[k] for k in stages) * args.steps,
+        "gpu_launches": (sum(KERNELS_PER_STEP[k] for k in stages) + (2 if args.mass else 0)) * args.steps,
         "clocks": clk.summary(),
         "e2e": e2e,
         "peaks_source": peak_src,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, x, cube=cube)
+        out["cpu_baseline"] = cpu_baseline(w, x, cube=cube, mass=args.mass or None)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -476,7 +490,7 @@ def time_e2e(dsv, x, w, hp, args, flops_per_step):
         dev_in = [torch.empty_like(t) for t in (x.Q, x.K, x.V, x.dO, x.Wq, x.Wk)]
         xd = X()
         xd.Q, xd.K, xd.V, xd.dO, xd.Wq, xd.Wk = dev_in
-        hp2 = HotPath(dsv, xd, w, hp.k, cube=hp.cube)
+        hp2 = HotPath(dsv, xd, w, hp.k, cube=hp.cube, mass=hp.mass)
         host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in hp2.results()]
         sets.append((dev_in, hp2, host_out))
     h2d = sum(t.numel() * t.element_size() for t in host_in)
@@ -525,7 +539,7 @@ def time_e2e(dsv, x, w, hp, args, flops_per_step):
 # the oracle on the host cores (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_head_step(w, x, b, h, cube=None):
+def oracle_head_step(w, x, b, h, cube=None, mass=None):
     """The fp64 oracle's whole hot path for one (b, h) (with cube, on the
     tokens in cube order, and O and the gradients put back): returns its pair
     count."""
@@ -540,8 +554,10 @@ def oracle_head_step(w, x, b, h, cube=None):
         Q, K, V, dO = (oracle.permute_tokens(t, perm) for t in (Q, K, V, dO))
     Wq, Wk = f64(x.Wq[h:h + 1]), f64(x.Wk[h:h + 1])
     S = oracle.predict_scores(Q, K, Wq, Wk, w.block)
-    k = [x.k_per_head[h]]
-    fp, fc = oracle.topk_lists(S, k)
+    if mass:
+        fp, fc = oracle.mass_lists(S, mass, 1.0 / math.sqrt(w.d), 1, w.nb)
+    else:
+        fp, fc = oracle.topk_lists(S, [x.k_per_head[h]])
     oracle.transpose_lists(fp, fc, 1, 1, w.nb, w.nb)
     O, _ = oracle.attn_fwd_groups(Q, K, V, fp, fc, w.block)
     grads = oracle.attn_bwd_groups(Q, K, V, dO, fp, fc, w.block)
@@ -551,12 +567,12 @@ def oracle_head_step(w, x, b, h, cube=None):
     return int(fc.shape[0])
 
 
-def cpu_baseline(w, x, min_s=10.0, max_s=30.0, cube=None):
+def cpu_baseline(w, x, min_s=10.0, max_s=30.0, cube=None, mass=None):
     fwd_f, bwd_f = pair_flops(w.block, w.d)
     t0 = time.perf_counter()
     pairs, heads = 0, 0
     for h in range(w.H):
-        pairs += oracle_head_step(w, x, 0, h, cube)
+        pairs += oracle_head_step(w, x, 0, h, cube, mass)
         heads += 1
         el = time.perf_counter() - t0
         if el >= min_s or el * (heads + 1) / heads > max_s:
@@ -581,11 +597,11 @@ def run_reference(args):
     fwd_f, bwd_f = pair_flops(w.block, w.d)
     slices = [(b, h) for b in range(w.B) for h in heads]
     for i in range(max(3, args.warmup)):
-        oracle_head_step(w, x, *slices[i % len(slices)], cube)
+        oracle_head_step(w, x, *slices[i % len(slices)], cube, args.mass or None)
     t0 = time.perf_counter()
     pairs = 0
     for i in range(args.steps):
-        pairs += oracle_head_step(w, x, *slices[i % len(slices)], cube)
+        pairs += oracle_head_step(w, x, *slices[i % len(slices)], cube, args.mass or None)
     el = time.perf_counter() - t0
     value = (fwd_f + bwd_f) * pairs / el / 1e12
     sample = (f"each step one (batch, head) slice of {w.name} (1 of {len(slices)}): predictor, top-k, transpose, "
@@ -594,7 +610,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(1e3 * el / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "description": w.description, **({"cube": list(cube)} if cube else {})},
+        "config": {"workload": w.name, "description": w.description, **({"cube": list(cube)} if cube else {}),
+                   **({"selection": f"mass threshold tau={args.mass}, temperature 1/sqrt(d), k in [1, nb]"}
+                      if args.mass else {})},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

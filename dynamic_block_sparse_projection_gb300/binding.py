@@ -207,11 +207,12 @@ def topk_mass_workspace_bytes(B: int, H: int, N: int, d: int, block: int) -> int
 
 
 def topk_mass_blocks(scores, tau: float, block: int, N: int, d: int = 128, *, temperature: float = 0.0,
-                     kmin: int = 1, kmax: int = 0, outs=None, workspace=None, stream=None):
+                     kmin: int = 1, kmax: int = 0, outs=None, workspace=None, stream=None, trim: bool = True):
     """(fwd_ptr, fwd_col, bwd_ptr, bwd_col) int32 CSR lists of the
     mass-threshold selection; see dsv_topk_mass_blocks.  temperature <= 0
-    selects 1/sqrt(d), kmax <= 0 selects nb.  The column arrays are returned
-    cut to nnz = fwd_ptr[-1], which this reads back from the device."""
+    selects 1/sqrt(d), kmax <= 0 selects nb.  With trim the column arrays are
+    returned cut to nnz = fwd_ptr[-1], which this reads back from the device
+    (a synchronisation); without it they are returned whole."""
     _need(scores, "scores", torch.float32)
     dev = scores.device
     B, H, G, nb = scores.shape
@@ -232,6 +233,8 @@ def topk_mass_blocks(scores, tau: float, block: int, N: int, d: int = 128, *, te
     _check(lib.dsv_topk_mass_blocks(_ptr(scores), s, float(tau), temperature, int(kmin), kmax, *[_ptr(t) for t in outs],
                                     cap, _ptr(ws), nbytes, _stream(dev, stream)), "dsv_topk_mass_blocks")
     fp, fc, bp, bc = outs
+    if not trim:
+        return fp, fc, bp, bc
     nnz = int(fp[-1].item()) if B * H * G > 0 else 0
     return fp, fc[:nnz], bp, bc[:nnz]
 
