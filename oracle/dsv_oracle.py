@@ -26,6 +26,13 @@ What the pages fix, and the reading taken where they are silent:
     bidirectional (no causal mask), no forced blocks.
   * Backward: the pages train with it ([nl] 2A stage 2); the gradient is the
     ordinary softmax-attention gradient restricted to the same mask.
+  * Mass-threshold selection ([nl] 2A, [hi] 2A: the critical KV carry about
+    90 % of the attention score).  Reading: block masses are the softmax of
+    temperature * S over the row; the smallest top set reaching tau is kept,
+    clamped to [kmin, kmax]; a row with a non-finite score keeps kmax.
+  * 3D cube grouping ([nl] 2B, [hi] 2B: queries grouped in small cubes).
+    Reading: a token permutation making every run of `block` tokens one
+    ct x cy x cx cube (cube grid and cube interior both in raster order).
 
 Every function works in float64 on numpy arrays.  Shapes:
   Q, K, V, dO : [B, H, N, d];  Wq, Wk : [H, d, r];  S : [B, H, G, nb]
