@@ -49,7 +49,7 @@ typedef struct CUstream_st* dsv_stream_t;
 typedef enum {
   DSV_OK = 0,
   DSV_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, k out of range */
-  DSV_ERR_UNSUPPORTED = 2,  /* a size this build has no kernel for */
+  DSV_ERR_UNSUPPORTED = 2,  /* a size the library has no kernel for */
   DSV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
   DSV_ERR_BAD_INDEX = 4,    /* a kernel met an out-of-range CSR entry */
   DSV_ERR_TIMEOUT = 5,      /* a kernel wait ran past its time limit */
