@@ -423,21 +423,21 @@ template <int BETA, int D>
 struct QTraits {
   static constexpr int BM = 128;
   static constexpr int NCH = D / 64;
-  static constexpr int A_CHUNK = BM * 128;         // dO_g as the A operand of dP (padded rows)
+  static constexpr int A_CHUNK = BM * 128;         // Q_g and dO_g as the A operands of S and dP (padded rows)
   static constexpr int A_BYTES = NCH * A_CHUNK;
   static constexpr int KV_CHUNK = BETA * 128;
   static constexpr int KV_BYTES = NCH * KV_CHUNK;
   // K_j is read by S (early) and by dQ (late); V_j only by dP: separate rings,
   // each slot released as soon as its last product is done.
   static constexpr int NK = 3;
-  static constexpr int NV = (A_BYTES + 6 * KV_BYTES + 2048 <= 227 * 1024) ? 3 : 2;
+  static constexpr int NV = (2 * A_BYTES + 6 * KV_BYTES + 2048 <= 227 * 1024) ? 3 : 2;
   static constexpr int NBAR = 2 + 2 * NK + 2 * NV + 2 + 2 + 3;
-  static constexpr int SMEM_USED = 1024 + A_BYTES + (NK + NV) * KV_BYTES + NBAR * 8 + 16;
+  static constexpr int SMEM_USED = 1024 + 2 * A_BYTES + (NK + NV) * KV_BYTES + NBAR * 8 + 16;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
-  // TMEM: S and dP (fp32), dQ (fp32), dS (bf16 pairs, BETA/2 columns), and Q_g
-  // (bf16 pairs, D/2 columns) as the A operand of S, read in once per CTA: an
-  // M=128 MMA with both operands in shared memory takes all of its bandwidth.
-  static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256, DS_COL = 256 + D, Q_COL = 256 + D + 64;
+  // TMEM: S and dP (fp32), dQ (fp32), dS (bf16 pairs, BETA/2 columns).  S and
+  // dP take both operands from shared memory (an M=128, N=128 product reads 8 KB
+  // in its 64 clocks, the port's 128 B/clock); dQ takes dS from TMEM.
+  static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256, DS_COL = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TX_BYTES = BETA * D * 2;
   static constexpr int HALF = BETA / 2;
@@ -445,7 +445,7 @@ struct QTraits {
 
 template <int BETA, int D>
 __global__ void __launch_bounds__(kQThreads, 1)
-    attn_bwd_q_kernel(const __nv_bfloat16* __restrict__ Qg, const __grid_constant__ CUtensorMap tmK,
+    attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                       const float* __restrict__ L2w, const float* __restrict__ Dw,
                       const int32_t* __restrict__ fwd_ptr, const int32_t* __restrict__ fwd_col, long long items,
@@ -456,11 +456,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = align_up_ptr<uint8_t>(smem_raw, 1024);
   uint8_t* sdO = sbase;
-  uint8_t* sK = sdO + T::A_BYTES;
+  uint8_t* sQ = sdO + T::A_BYTES;
+  uint8_t* sK = sQ + T::A_BYTES;
   uint8_t* sV = sK + NK * T::KV_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NV * T::KV_BYTES);
-  uint64_t* qd_full = bars;                       // dO_g landed in smem
-  uint64_t* q_tm = bars + 1;                      // Q_g written to TMEM by the compute threads
+  uint64_t* qd_full = bars;                       // Q_g and dO_g landed in smem
+  uint64_t* q_spare = bars + 1;                   // (unused)
   uint64_t* k_full = bars + 2;
   uint64_t* k_empty = k_full + NK;
   uint64_t* v_full = k_empty + NK;
@@ -482,7 +483,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(qd_full, 1);
-    mbar_init(q_tm, kComputeThreads);
+    mbar_init(q_spare, 1);
     for (int s = 0; s < NK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -503,8 +504,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
   }
   if (BETA < T::BM) {
     for (int c = 0; c < T::NCH; ++c) {
-      uint4* z = reinterpret_cast<uint4*>(sdO + c * T::A_CHUNK + BETA * 128);
-      for (int i = threadIdx.x; i < (T::BM - BETA) * 128 / 16; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+      for (int t = 0; t < 2; ++t) {
+        uint4* z = reinterpret_cast<uint4*>(sdO + t * T::A_BYTES + c * T::A_CHUNK + BETA * 128);
+        for (int i = threadIdx.x; i < (T::BM - BETA) * 128 / 16; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+      }
     }
     fence_proxy_async_smem();
   }
@@ -525,7 +528,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   // The CTA works through groups blockIdx.x, blockIdx.x + gridDim.x, ...
   // Every role counts the pairs of the groups before the current one (gq: the
   // global pair index of ring slots and barrier phases) and the non-empty
-  // groups (ne: the phase of qd_full, q_tm and acc_done), so the next group's
+  // groups (ne: the phase of qd_full, qd_free and acc_done), so the next group's
   // dO, K and V tiles load while the compute warps finish the current group.
   if (tmem_base != tmem) {
     if (threadIdx.x == 0) set_error(ctl, DSV_ERR_INTERNAL, blockIdx.x);
@@ -540,7 +543,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
       uint64_t* full = is_k ? k_full : v_full;
       uint64_t* empty = is_k ? k_empty : v_empty;
       tma_prefetch_desc(map);
-      if (is_k) tma_prefetch_desc(&tmdO);
+      if (is_k) {
+        tma_prefetch_desc(&tmdO);
+        tma_prefetch_desc(&tmQ);
+      }
       uint32_t gq = 0;                            // tiles issued so far
       int qd_issued = 0;
       bool ok = true;
@@ -552,15 +558,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
         const long long bh = row / G;
         const int g = (int)(row - bh * G);
         if (is_k) {
-          // dO_g is the A operand of every dP product: the previous group's
-          // last one must be done.  qd_free (one phase per group) is at most
-          // one phase behind here; the per-pair s_full could be two behind,
-          // and its parity would then alias.
+          // Q_g and dO_g are the A operands of every S and dP product: the
+          // previous group's last ones must be done.  qd_free (one phase per
+          // group) is at most one phase behind here; the per-pair s_full could
+          // be two behind, and its parity would then alias.
           if (qd_issued > 0 && !mbar_wait(qd_free, (uint32_t)(qd_issued - 1) & 1u, abort_flag, ctl, kid | W_KVEMPTY))
             break;
-          mbar_arrive_expect_tx(qd_full, T::TX_BYTES);
-          for (int c = 0; c < T::NCH; ++c)
-            tma_load_2d(sdO + c * T::A_CHUNK, &tmdO, qd_full, c * 64, (int)(bh * N + (long long)g * BETA));
+          mbar_arrive_expect_tx(qd_full, 2 * T::TX_BYTES);
+          const int qrow = (int)(bh * N + (long long)g * BETA);
+          for (int c = 0; c < T::NCH; ++c) {
+            tma_load_2d(sdO + c * T::A_CHUNK, &tmdO, qd_full, c * 64, qrow);
+            tma_load_2d(sQ + c * T::A_CHUNK, &tmQ, qd_full, c * 64, qrow);
+          }
           ++qd_issued;
         }
         int jn = fwd_col[start];
@@ -595,6 +604,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       constexpr uint32_t ID_S = idesc_bf16_f32(T::BM, BETA, false, false);
       constexpr uint32_t ID_Q = idesc_bf16_f32(T::BM, D, false, true);
       const uint64_t ddO0 = sdesc_sw128(smem_u32(sdO), 16, 1024);
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t dKmn0 = sdesc_sw128(smem_u32(sK), T::KV_CHUNK, 1024);
@@ -607,7 +617,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t bo = (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32;
-          mma_ts_w(tmem + T::S_COL, tmem + T::Q_COL + kk * 8, desc_off(kb, bo), ID_S, kk > 0 ? 1u : 0u);
+          const uint32_t ao = (kk >> 2) * T::A_CHUNK + (kk & 3) * 32;
+          mma_ss_w(tmem + T::S_COL, desc_off(dQ0, ao), desc_off(kb, bo), ID_S, kk > 0 ? 1u : 0u);
         }
         if (td != nullptr) *td = mbar_test(ds_full, (gn - 1) & 1u);
         if (!mbar_wait_warp_tested(&v_full[sv], (gn / NV) & 1u, tv, abort_flag, ctl, kid | W_VFULL)) return false;
@@ -631,10 +642,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
       int start, cnt;
       while (ok && cur.next(row, start, cnt)) {
         if (cnt <= 0) continue;
-        // q_tm of a group also means the compute warps have read the previous
-        // group's last S and dP, so both may be overwritten
+        // S and dP are single-buffered: the previous group's last ones must
+        // have been read by the compute warps (sp_free of its last pair)
         ok = mbar_wait_warp(qd_full, (uint32_t)ne & 1u, abort_flag, ctl, kid | W_KV) &&
-             mbar_wait_warp(q_tm, (uint32_t)ne & 1u, abort_flag, ctl, kid | W_KV);
+             (gq == 0 || mbar_wait_warp(sp_free, (gq - 1) & 1u, abort_flag, ctl, kid | W_SPFREE));
         if (ok) ok = issue_sdp(gq, 0u, 0u, nullptr);
         if (ok && cnt == 1) mma_commit_w(qd_free);    // the group's last read of dO_g
         for (int n = 0; ok && n < cnt; ++n) {
@@ -715,26 +726,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       }
       const float nlse2 = (r < BETA) ? L2w[orow] : 0.f;   // -lse*log2(e)
       const float dd = (r < BETA) ? Dw[orow] : 0.f;
-      {
-        // row r of Q_g into TMEM (this warp's half of its D/2 columns), as the A
-        // operand of every S product; rows past BETA are zero.  The previous
-        // group's S products are all done: this thread has waited for its last.
-        constexpr int QW = D / 4;                   // columns per warp
-        const uint4* src = reinterpret_cast<const uint4*>(Qg + orow * D + hf * (D / 2));
-        uint32_t q[QW];
-#pragma unroll
-        for (int i = 0; i < QW / 4; ++i) {
-          const uint4 v = r < BETA ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
-          q[4 * i] = v.x;
-          q[4 * i + 1] = v.y;
-          q[4 * i + 2] = v.z;
-          q[4 * i + 3] = v.w;
-        }
-        tmem_st_w<QW>(tmem + lane_off + T::Q_COL + hf * QW, q);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(q_tm);
-      }
+
       uint32_t s_tested = 0u;
       for (int n = 0; n < cnt; ++n) {
         const uint32_t gn = gq + (uint32_t)n;
@@ -897,7 +889,7 @@ cudaError_t launch_kv_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CU
 }
 
 template <int BETA, int D>
-cudaError_t launch_q_t(const void* Q, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmdO,
+cudaError_t launch_q_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmdO,
                        const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col, float scale, void* dQ,
                        const float* Dw, const float* L2w, const Ctl& ctl, cudaStream_t st) {
   const int G = s.N / s.block;
@@ -912,9 +904,8 @@ cudaError_t launch_q_t(const void* Q, const CUtensorMap& tmK, const CUtensorMap&
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const unsigned grid = (unsigned)(groups < nsm ? groups : nsm);
-  qk<<<grid, kQThreads, QTraits<BETA, D>::SMEM, st>>>(static_cast<const __nv_bfloat16*>(Q), tmK, tmV, tmdO, L2w, Dw,
-                                                      fwd_ptr, fwd_col, groups, s.N, G, scale,
-                                                      static_cast<__nv_bfloat16*>(dQ), ctl);
+  qk<<<grid, kQThreads, QTraits<BETA, D>::SMEM, st>>>(tmQ, tmK, tmV, tmdO, L2w, Dw, fwd_ptr, fwd_col, groups, s.N,
+                                                      G, scale, static_cast<__nv_bfloat16*>(dQ), ctl);
   return cudaGetLastError();
 }
 
@@ -968,11 +959,11 @@ cudaError_t launch_attn_bwd_kv(const CUtensorMap& tmQ, const CUtensorMap& tmK, c
 #undef DSV_KV
 }
 
-cudaError_t launch_attn_bwd_q(const void* Q, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmdO,
+cudaError_t launch_attn_bwd_q(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmdO,
                               const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col, float scale,
                               void* dQ, const void* ws, const Ctl& ctl, cudaStream_t st) {
 #define DSV_Q(BE, DD) \
-  return launch_q_t<BE, DD>(Q, tmK, tmV, tmdO, s, fwd_ptr, fwd_col, scale, dQ, ws_D(ws), ws_L2(ws, s), ctl, st)
+  return launch_q_t<BE, DD>(tmQ, tmK, tmV, tmdO, s, fwd_ptr, fwd_col, scale, dQ, ws_D(ws), ws_L2(ws, s), ctl, st)
   if (s.block == 128 && s.d == 128) DSV_Q(128, 128);
   if (s.block == 128 && s.d == 64) DSV_Q(128, 64);
   if (s.block == 64 && s.d == 128) DSV_Q(64, 128);
@@ -989,7 +980,8 @@ cudaError_t launch_attn_bwd(const void* Q, const CUtensorMap& tmQ, const CUtenso
   if (e != cudaSuccess) return e;
   if ((e = launch_attn_bwd_kv(tmQ, tmK, tmV, tmdO, s, bwd_ptr, bwd_col, scale, dK, dV, ws, ctl, st)) != cudaSuccess)
     return e;
-  return launch_attn_bwd_q(Q, tmK, tmV, tmdO, s, fwd_ptr, fwd_col, scale, dQ, ws, ctl, st);
+  (void)Q;
+  return launch_attn_bwd_q(tmQ, tmK, tmV, tmdO, s, fwd_ptr, fwd_col, scale, dQ, ws, ctl, st);
 }
 
 }  // namespace dsv

@@ -345,11 +345,11 @@ dsv_status dsv_attn_bwd_dq(const void* Q, const void* K, const void* V, const vo
   Ctl ctl;
   if (current_ctl(&ctl) != cudaSuccess) return DSV_ERR_CUDA;
   const long long rows = (long long)s.B * s.H * s.N;
-  CUtensorMap tk, tv, tdo;
-  if (make_map(&tk, K, rows, s.d, s.block) != cudaSuccess || make_map(&tv, V, rows, s.d, s.block) != cudaSuccess ||
-      make_map(&tdo, dO, rows, s.d, s.block) != cudaSuccess)
+  CUtensorMap tq, tk, tv, tdo;
+  if (make_map(&tq, Q, rows, s.d, s.block) != cudaSuccess || make_map(&tk, K, rows, s.d, s.block) != cudaSuccess ||
+      make_map(&tv, V, rows, s.d, s.block) != cudaSuccess || make_map(&tdo, dO, rows, s.d, s.block) != cudaSuccess)
     return DSV_ERR_CUDA;
-  return from_cuda(launch_attn_bwd_q(Q, tk, tv, tdo, s, fwd_ptr, fwd_col, resolve_scale(s, softmax_scale), dQ,
+  return from_cuda(launch_attn_bwd_q(tq, tk, tv, tdo, s, fwd_ptr, fwd_col, resolve_scale(s, softmax_scale), dQ,
                                      workspace, ctl, reinterpret_cast<cudaStream_t>(stream)));
 }
 

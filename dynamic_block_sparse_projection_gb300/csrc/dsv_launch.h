@@ -56,7 +56,7 @@ cudaError_t launch_attn_bwd_kv(const CUtensorMap& tmQ, const CUtensorMap& tmK, c
                                const CUtensorMap& tmdO, const dsv_shape& s, const int32_t* bwd_ptr,
                                const int32_t* bwd_col, float scale, void* dK, void* dV, void* ws,
                                const Ctl& ctl, cudaStream_t st);
-cudaError_t launch_attn_bwd_q(const void* Q, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmdO,
+cudaError_t launch_attn_bwd_q(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmdO,
                               const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col, float scale,
                               void* dQ, const void* ws, const Ctl& ctl, cudaStream_t st);
 size_t attn_bwd_ws_bytes(const dsv_shape& s);
