@@ -90,3 +90,64 @@ def test_mutant_backward_slips_are_caught(monkeypatch):
     got = oracle.attn_bwd_groups(Q, K, V, dO, ptr, col, blk)
     for a, r in zip(got, ref):
         assert np.max(np.abs(a - r)) <= 1e-11
+
+
+def _golden_perm(name):
+    from pathlib import Path
+    lines = [l for l in (Path(__file__).resolve().parent / "golden" / name).read_text().splitlines()
+             if l.strip() and not l.startswith("#")]
+    return np.array([int(v) for v in lines[0].split()])
+
+
+def test_mutant_cube_order_slips_are_caught():
+    """Plausible slips in the cube token order: the loops inside a cube
+    swapped (x before y), the cube extents swapped, the frame stride of the
+    raster index wrong; each fails a hand-worked order or the tiling check."""
+    def walk(T, Hl, Wl, ct, cy, cx, inner, stride_t):
+        perm = []
+        for bt in range(T // ct):
+            for by in range(Hl // cy):
+                for bx in range(Wl // cx):
+                    for lt in range(ct):
+                        for a in range(cx if inner == "xy" else cy):
+                            for b in range(cy if inner == "xy" else cx):
+                                ly, lx = (b, a) if inner == "xy" else (a, b)
+                                t, y, x = bt * ct + lt, by * cy + ly, bx * cx + lx
+                                perm.append(t * stride_t + y * Wl + x)
+        return np.array(perm)
+    g1 = _golden_perm("cube_order_1x4x4_cube_1x2x2.txt")
+    g2 = _golden_perm("cube_order_2x2x4_cube_2x1x2.txt")
+    assert np.array_equal(walk(1, 4, 4, 1, 2, 2, "yx", 16), g1)          # the faithful walk passes
+    assert not np.array_equal(walk(1, 4, 4, 1, 2, 2, "xy", 16), g1)      # x and y swapped inside a cube
+    assert not np.array_equal(walk(2, 2, 4, 2, 1, 2, "yx", 4), g2)       # frame stride Wl instead of Hl*Wl
+    swapped = walk(2, 2, 4, 2, 2, 1, "yx", 8)                             # cy and cx swapped
+    assert not np.array_equal(swapped, oracle.cube_order(2, 2, 4, 2, 1, 2))
+
+
+def test_mutant_mass_count_slips_are_caught():
+    """Slips in the mass-threshold count: the mass taken without the
+    temperature, the count one too small (strict >), and the order by
+    ascending score; each disagrees with brute force or a closed form."""
+    s = np.full(8, 1.7)
+    assert oracle.mass_count_row(s, 0.75, 0.8, 1, 8) == 6                # ceil(0.75 * 8) for equal scores
+
+    def mutant_strict(row, tau, temp):                                   # first count with mass > tau
+        p = np.exp(temp * (row - row.max()))
+        p /= p.sum()
+        cum = np.cumsum(np.sort(p)[::-1])
+        return int(np.searchsorted(cum, tau, side="right")) + 1
+    assert mutant_strict(s, 0.75, 0.8) != 6
+
+    row = np.array([0.3, 2.0, -1.0, 1.5, 0.9])
+
+    def mutant_no_temp(row, tau):
+        p = np.exp(row - row.max())
+        p /= p.sum()
+        return int(np.searchsorted(np.cumsum(np.sort(p)[::-1]), tau)) + 1
+    assert mutant_no_temp(row, 0.9) != oracle.mass_count_row(row, 0.9, 1e3, 1, 5)   # sharp softmax: m = 1
+
+    def mutant_ascending(row, tau, temp):
+        p = np.exp(temp * (row - row.max()))
+        p /= p.sum()
+        return int(np.searchsorted(np.cumsum(np.sort(p)), tau)) + 1
+    assert mutant_ascending(row, 0.5, 2.0) != oracle.mass_count_row(row, 0.5, 2.0, 1, 5)
