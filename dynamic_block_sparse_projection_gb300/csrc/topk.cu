@@ -811,7 +811,12 @@ __global__ void __launch_bounds__(RT, mass_min_blocks(RT)) topk_mass_count_kerne
       hcnt[i] = 0u;
       hmass[i] = 0ull;
     }
-    if (t == 0) s_cnt = 0u;
+    if (t == 0) {
+      s_cnt = 0u;
+      s_bin = 0u;               // always overwritten below (the target lies in play); never read uninitialised
+      s_above = mass_above;
+      s_above_cnt = cnt_above;
+    }
     __syncthreads();
 #pragma unroll
     for (int e = 0; e < E; ++e)
