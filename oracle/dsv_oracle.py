@@ -111,6 +111,43 @@ def predict_scores_pool_first(Q, K, Wq, Wk, block: int) -> np.ndarray:
     return S
 
 
+def predict_scores_max(Q, K, Wq, Wk, block: int) -> np.ndarray:
+    """Max-pooled block scores: S[b,h,g,j] = the largest low-rank logit
+    Q_lr[i] . K_lr[l] over the query tokens i of group g and the key tokens l
+    of block j (no scale).
+
+    The pages do not say how a block is scored; this is the alternative to the
+    mean reading (predict_scores), which is the mean of the same tile.  The
+    whole [N, N] low-rank logit matrix of one (b, h) is formed, then each
+    block x block tile is reduced by its maximum.
+    """
+    Q, K, Wq, Wk = _f64(Q), _f64(K), _f64(Wq), _f64(Wk)
+    B, H, N, d = Q.shape
+    G = N // block
+    S = np.empty((B, H, G, G), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            L = (Q[b, h] @ Wq[h]) @ (K[b, h] @ Wk[h]).T      # [N, N] low-rank logits
+            S[b, h] = L.reshape(G, block, G, block).max(axis=(1, 3))
+    return S
+
+
+def predict_scores_max_rows(Q, K, Wq, Wk, block: int, rows: Sequence[Tuple[int, int, int]]) -> np.ndarray:
+    """Rows S[b,h,g,:] of predict_scores_max for the listed (b, h, g)."""
+    Wq, Wk = _f64(Wq), _f64(Wk)
+    B, H, N, d = Q.shape
+    G = N // block
+    out = np.empty((len(rows), G), dtype=np.float64)
+    k_cache = {}
+    for n, (b, h, g) in enumerate(rows):
+        if (b, h) not in k_cache:
+            k_cache[(b, h)] = _f64(K[b, h]) @ Wk[h]                # [N, r]
+        q_lr = _f64(Q[b, h, g * block:(g + 1) * block]) @ Wq[h]   # [block, r]
+        L = q_lr @ k_cache[(b, h)].T                              # [block, N]
+        out[n] = L.reshape(block, G, block).max(axis=(0, 2))
+    return out
+
+
 # --------------------------------------------------------------------------
 # Top-k selection and the transposed lists ([nl] 2B, [hi] 2B)
 # --------------------------------------------------------------------------
