@@ -30,6 +30,7 @@ EXPORTS = (
     "dsv_topk_blocks_noalloc",
     "dsv_attn_bwd_preprocess", "dsv_attn_bwd_dkdv", "dsv_attn_bwd_dq",
     "dsv_cube_permute", "dsv_topk_mass_workspace_bytes", "dsv_topk_mass_blocks",
+    "dsv_predict_max_workspace_bytes", "dsv_predict_scores_max",
 )
 
 
@@ -56,6 +57,10 @@ def _load() -> ctypes.CDLL:
     lib.dsv_predict_workspace_bytes.restype = sz
     lib.dsv_predict_scores.argtypes = [vp, vp, vp, vp, Shape, vp, vp, sz, vp]
     lib.dsv_predict_scores.restype = ctypes.c_int
+    lib.dsv_predict_max_workspace_bytes.argtypes = [Shape]
+    lib.dsv_predict_max_workspace_bytes.restype = sz
+    lib.dsv_predict_scores_max.argtypes = [vp, vp, vp, vp, Shape, vp, vp, sz, vp]
+    lib.dsv_predict_scores_max.restype = ctypes.c_int
     lib.dsv_topk_workspace_bytes.argtypes = [Shape]
     lib.dsv_topk_workspace_bytes.restype = sz
     lib.dsv_topk_blocks.argtypes = [vp, Shape, ctypes.POINTER(i32), vp, vp, vp, vp, vp, sz, vp]
@@ -175,6 +180,30 @@ def predict_scores(Q, K, Wq, Wk, block: int, *, out=None, workspace=None, stream
     ws = _workspace(nbytes, dev, workspace)
     _check(lib.dsv_predict_scores(_ptr(Q), _ptr(K), _ptr(Wq), _ptr(Wk), s, _ptr(out), _ptr(ws), nbytes,
                                   _stream(dev, stream)), "dsv_predict_scores")
+    return out
+
+
+def predict_max_workspace_bytes(B: int, H: int, N: int, d: int, block: int, r: int) -> int:
+    return int(lib.dsv_predict_max_workspace_bytes(Shape(B, H, N, d, block, r)))
+
+
+def predict_scores_max(Q, K, Wq, Wk, block: int, *, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """scores[b,h,g,j] = max low-rank logit of tile (g, j) (fp32 [B,H,G,nb]); see dsv_predict_scores_max."""
+    _need(Q, "Q", torch.bfloat16)
+    dev = Q.device
+    _need(K, "K", torch.bfloat16, dev)
+    _need(Wq, "Wq", torch.float32, dev)
+    _need(Wk, "Wk", torch.float32, dev)
+    B, H, N, d = Q.shape
+    s = Shape(B, H, N, d, block, Wq.shape[-1])
+    G = N // block if block else 0
+    if out is None:
+        out = torch.empty(B, H, G, G, dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, dev)
+    nbytes = lib.dsv_predict_max_workspace_bytes(s)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(lib.dsv_predict_scores_max(_ptr(Q), _ptr(K), _ptr(Wq), _ptr(Wk), s, _ptr(out), _ptr(ws), nbytes,
+                                      _stream(dev, stream)), "dsv_predict_scores_max")
     return out
 
 

@@ -23,6 +23,10 @@ struct HeadK {
 cudaError_t launch_predict(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s,
                            float* scores, void* ws, cudaStream_t st);
 size_t predict_ws_bytes(const dsv_shape& s);
+// Max-pooled predictor: per-token rank-r projections into `ws`, then the tile-maximum kernel.
+cudaError_t launch_predict_max(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s,
+                               float* scores, void* ws, cudaStream_t st);
+size_t predict_max_ws_bytes(const dsv_shape& s);
 
 // Top-k, transposed lists.
 cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk, int64_t nnz, int32_t* fwd_ptr,
@@ -47,9 +51,6 @@ cudaError_t launch_attn_bwd(const void* Q, const CUtensorMap& tmQ, const CUtenso
                             const int32_t* bwd_ptr, const int32_t* bwd_col, float scale, void* dQ, void* dK,
                             void* dV, void* ws, const Ctl& ctl, cudaStream_t st);
 // The stages of launch_attn_bwd (preprocess; dK/dV; dQ).
-// 3D cube query grouping: token rows moved between raster and cube order.
-cudaError_t launch_cube_permute(const void* src, void* dst, const dsv_shape& s, int T, int Hl, int Wl, int ct, int cy,
-                                int cx, int inverse, cudaStream_t st);
 cudaError_t launch_attn_bwd_pre(const void* O, const void* dO, const float* lse, const dsv_shape& s, void* ws,
                                 cudaStream_t st);
 cudaError_t launch_attn_bwd_kv(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
@@ -60,6 +61,10 @@ cudaError_t launch_attn_bwd_q(const CUtensorMap& tmQ, const CUtensorMap& tmK, co
                               const dsv_shape& s, const int32_t* fwd_ptr, const int32_t* fwd_col, float scale,
                               void* dQ, const void* ws, const Ctl& ctl, cudaStream_t st);
 size_t attn_bwd_ws_bytes(const dsv_shape& s);
+
+// 3D cube query grouping: token rows moved between raster and cube order.
+cudaError_t launch_cube_permute(const void* src, void* dst, const dsv_shape& s, int T, int Hl, int Wl, int ct, int cy,
+                                int cx, int inverse, cudaStream_t st);
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 

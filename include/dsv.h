@@ -83,6 +83,30 @@ dsv_status dsv_predict_scores(const void* Q, const void* K, const float* Wq, con
                               dsv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * dsv_predict_scores_max — max-pooled block scores of the same predictor
+ * ([nl] 2A low-rank logits approximating Q K^T; 2B one proxy per group).
+ * The pages do not fix how a (group, key block) tile of low-rank logits
+ * becomes one score; dsv_predict_scores takes the tile mean, this call the
+ * tile maximum:
+ *
+ *   scores[b,h,g,j] = max over tokens i of group g and l of key block j of
+ *                     (Q[b,h,i] W^Q[h]) . (K[b,h,l] W^K[h])     (fp32, no scale)
+ *
+ * Every token is projected and every tile formed (block^2 * r FMAs per
+ * (g, j), fp32 on the CUDA cores).  A NaN logit is dropped by the maximum.
+ * Arguments and layout as dsv_predict_scores, except:
+ * workspace >= dsv_predict_max_workspace_bytes(s) bytes, 256-byte aligned
+ *           (holds the rank-r projection of every token of Q and K:
+ *           2 * B*H*N*r fp32).
+ * DSV_ERR_UNSUPPORTED also when G * ceil(G / 16) >= 2^31.
+ * The scores feed dsv_topk_blocks or dsv_topk_mass_blocks unchanged.
+ * ------------------------------------------------------------------------ */
+size_t dsv_predict_max_workspace_bytes(dsv_shape s);
+dsv_status dsv_predict_scores_max(const void* Q, const void* K, const float* Wq, const float* Wk,
+                                  dsv_shape s, float* scores, void* workspace, size_t workspace_bytes,
+                                  dsv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * dsv_topk_blocks — per-group top-k critical key blocks and their transpose
  * ([nl] 2B fused estimation & selection; [hi] 2B top-k selection)
  *
