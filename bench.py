@@ -38,6 +38,8 @@ METRIC = "sparse attn fwd+bwd effective TFLOP/s"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+# fp32 FMA peak of the CUDA cores (152 SMs x 128 lanes x 2 FLOP at the 2.07 GHz maximum SM clock)
+FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def parse_args(argv=None):
@@ -50,6 +52,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--mass", type=float, default=0.0, metavar="TAU",
                    help="select per group the smallest top set carrying >= TAU of the predicted mass (instead of top-k)")
+    p.add_argument("--scores", choices=["mean", "max"], default="mean",
+                   help="block score of the predictor: mean (dsv_predict_scores) or maximum "
+                        "(dsv_predict_scores_max) of each group x key-block tile of low-rank logits")
     p.add_argument("--cube", default="", metavar="CT,CY,CX",
                    help="regroup tokens into ct x cy x cx cubes of the latent grid inside the step")
     p.add_argument("--no-dense", action="store_true")
@@ -165,12 +170,13 @@ class HotPath:
     its inverse on O, dQ, dK, dV after it), so that query groups and key
     blocks are cubes; O and the gradients then come out in raster order."""
 
-    def __init__(self, dsv, x, w, k_per_head, cube=None, mass=None):
+    def __init__(self, dsv, x, w, k_per_head, cube=None, mass=None, scores="mean"):
         import torch
         self.dsv, self.x, self.w = dsv, x, w
         self.k = list(k_per_head)
         self.cube = tuple(cube) if cube else None
         self.mass = mass                 # tau of the mass-threshold selection, or None for top-k
+        self.scores = scores             # "mean" or "max" block scores
         self.grid = (w.T, w.Hl, w.Wl)
         dev = x.Q.device
         B, H, N, d, G = w.B, w.H, w.N, w.d, w.nb
@@ -185,7 +191,8 @@ class HotPath:
         self.lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
         self.grads = (torch.empty_like(x.Q), torch.empty_like(x.K), torch.empty_like(x.V))
         u8 = torch.uint8
-        self.ws_p = torch.empty(max(1, dsv.predict_workspace_bytes(B, H, N, d, w.block, w.r)), dtype=u8, device=dev)
+        ws_bytes = dsv.predict_max_workspace_bytes if scores == "max" else dsv.predict_workspace_bytes
+        self.ws_p = torch.empty(max(1, ws_bytes(B, H, N, d, w.block, w.r)), dtype=u8, device=dev)
         self.ws_t = torch.empty(max(1, (dsv.topk_mass_workspace_bytes if mass else dsv.topk_workspace_bytes)(
             B, H, N, d, w.block)), dtype=u8, device=dev)
         self.ws_b = torch.empty(max(1, dsv.attn_bwd_workspace_bytes(B, H, N, d, w.block)), dtype=u8, device=dev)
@@ -219,7 +226,8 @@ class HotPath:
                 d.cube_permute(src, self.grid, self.cube, out=dst)
             mark()
             x = self.xc
-        d.predict_scores(x.Q, x.K, x.Wq, x.Wk, w.block, out=self.S, workspace=self.ws_p)
+        predict = d.predict_scores_max if self.scores == "max" else d.predict_scores
+        predict(x.Q, x.K, x.Wq, x.Wk, w.block, out=self.S, workspace=self.ws_p)
         mark()
         if self.mass:
             fp, fc, bp, bc = d.topk_mass_blocks(self.S, self.mass, w.block, w.N, w.d, outs=self.lists,
@@ -298,7 +306,7 @@ def run_ours(args):
     w = wl.WORKLOADS[args.workload]
     x = wl.make_inputs(w, device=dev)
     cube = tuple(int(v) for v in args.cube.split(",")) if args.cube else None
-    hp = HotPath(dsv, x, w, x.k_per_head, cube=cube, mass=args.mass or None)
+    hp = HotPath(dsv, x, w, x.k_per_head, cube=cube, mass=args.mass or None, scores=args.scores)
     fwd_f, bwd_f = pair_flops(w.block, w.d)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -364,6 +372,8 @@ def run_ours(args):
                       if cube else {}),
                    **({"selection": f"mass threshold tau={args.mass}, temperature 1/sqrt(d), k in [1, nb]"}
                       if args.mass else {}),
+                   **({"block_scores": "tile maximum of the low-rank logits (dsv_predict_scores_max)"}
+                      if args.scores == "max" else {}),
                    "l2": "flushed before every step (256 MiB write, outside the step events); "
                          "inputs are also larger than L2"},
         "pct_of_bf16_peak": round(100.0 * value / peaks["bf16_tflops"], 2),
@@ -380,7 +390,7 @@ def run_ours(args):
         "peaks_source": peak_src,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, x, cube=cube, mass=args.mass or None)
+        out["cpu_baseline"] = cpu_baseline(w, x, cube=cube, mass=args.mass or None, scores=args.scores)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -411,6 +421,15 @@ def roofline_entry(dom, per_call, w, hp, peaks, peak_src):
                 "algorithmic": f"{MMAS_PER_PAIR[dom]} x 2*block^2*d FLOP per (group, block) pair x {hp.nnz} pairs",
                 "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
                 "traffic": profile_traffic(KERNEL_OF[dom], srcs)}
+    if dom == "predict" and hp.scores == "max":
+        # every logit of every tile: 2 * r FLOP per (query token, key token) pair, fp32 FMA on the CUDA cores
+        flops = 2.0 * B * H * N * N * w.r
+        achieved = flops / (per_call[dom] * 1e-3) / 1e12
+        peak = FP32_FMA_TFLOPS
+        return {"kernel": "dsv_predict_scores_max", "bound": "alu", "achieved": round(achieved, 3), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "algorithmic": f"2*r FLOP per (query, key) token pair x {B * H * N * N} pairs",
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz", "traffic": None}
     if dom == "bwd_pre":
         nbytes = 2 * B * H * N * d * 2 + B * H * N * 4 * 3
         kname = KERNEL_OF[dom]
@@ -491,7 +510,7 @@ def time_e2e(dsv, x, w, hp, args, flops_per_step):
         dev_in = [torch.empty_like(t) for t in (x.Q, x.K, x.V, x.dO, x.Wq, x.Wk)]
         xd = X()
         xd.Q, xd.K, xd.V, xd.dO, xd.Wq, xd.Wk = dev_in
-        hp2 = HotPath(dsv, xd, w, hp.k, cube=hp.cube, mass=hp.mass)
+        hp2 = HotPath(dsv, xd, w, hp.k, cube=hp.cube, mass=hp.mass, scores=hp.scores)
         host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in hp2.results()]
         sets.append((dev_in, hp2, host_out))
     h2d = sum(t.numel() * t.element_size() for t in host_in)
@@ -540,7 +559,7 @@ def time_e2e(dsv, x, w, hp, args, flops_per_step):
 # the oracle on the host cores (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_head_step(w, x, b, h, cube=None, mass=None):
+def oracle_head_step(w, x, b, h, cube=None, mass=None, scores="mean"):
     """The fp64 oracle's whole hot path for one (b, h) (with cube, on the
     tokens in cube order, and O and the gradients put back): returns its pair
     count."""
@@ -554,7 +573,7 @@ def oracle_head_step(w, x, b, h, cube=None, mass=None):
     if cube:
         Q, K, V, dO = (oracle.permute_tokens(t, perm) for t in (Q, K, V, dO))
     Wq, Wk = f64(x.Wq[h:h + 1]), f64(x.Wk[h:h + 1])
-    S = oracle.predict_scores(Q, K, Wq, Wk, w.block)
+    S = (oracle.predict_scores_max if scores == "max" else oracle.predict_scores)(Q, K, Wq, Wk, w.block)
     if mass:
         fp, fc = oracle.mass_lists(S, mass, 1.0 / math.sqrt(w.d), 1, w.nb)
     else:
@@ -568,12 +587,12 @@ def oracle_head_step(w, x, b, h, cube=None, mass=None):
     return int(fc.shape[0])
 
 
-def cpu_baseline(w, x, min_s=10.0, max_s=30.0, cube=None, mass=None):
+def cpu_baseline(w, x, min_s=10.0, max_s=30.0, cube=None, mass=None, scores="mean"):
     fwd_f, bwd_f = pair_flops(w.block, w.d)
     t0 = time.perf_counter()
     pairs, heads = 0, 0
     for h in range(w.H):
-        pairs += oracle_head_step(w, x, 0, h, cube, mass)
+        pairs += oracle_head_step(w, x, 0, h, cube, mass, scores)
         heads += 1
         el = time.perf_counter() - t0
         if el >= min_s or el * (heads + 1) / heads > max_s:
@@ -598,11 +617,11 @@ def run_reference(args):
     fwd_f, bwd_f = pair_flops(w.block, w.d)
     slices = [(b, h) for b in range(w.B) for h in heads]
     for i in range(max(3, args.warmup)):
-        oracle_head_step(w, x, *slices[i % len(slices)], cube, args.mass or None)
+        oracle_head_step(w, x, *slices[i % len(slices)], cube, args.mass or None, args.scores)
     t0 = time.perf_counter()
     pairs = 0
     for i in range(args.steps):
-        pairs += oracle_head_step(w, x, *slices[i % len(slices)], cube, args.mass or None)
+        pairs += oracle_head_step(w, x, *slices[i % len(slices)], cube, args.mass or None, args.scores)
     el = time.perf_counter() - t0
     value = (fwd_f + bwd_f) * pairs / el / 1e12
     sample = (f"each step one (batch, head) slice of {w.name} (1 of {len(slices)}): predictor, top-k, transpose, "
@@ -613,7 +632,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "description": w.description, **({"cube": list(cube)} if cube else {}),
                    **({"selection": f"mass threshold tau={args.mass}, temperature 1/sqrt(d), k in [1, nb]"}
-                      if args.mass else {})},
+                      if args.mass else {}),
+                   **({"block_scores": "tile maximum of the low-rank logits"} if args.scores == "max" else {})},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
