@@ -30,6 +30,10 @@ What the pages fix, and the reading taken where they are silent:
     90 % of the attention score).  Reading: block masses are the softmax of
     temperature * S over the row; the smallest top set reaching tau is kept,
     clamped to [kmin, kmax]; a row with a non-finite score keeps kmax.
+  * Max-pooled block scores ([nl] 2A, 2B: the pages do not say how a tile of
+    low-rank logits becomes one score).  Reading, as the alternative to the
+    mean: the largest logit (Q_i W^Q) . (K_l W^K) over the group's query
+    tokens i and the block's key tokens l, no scale.
   * 3D cube grouping ([nl] 2B, [hi] 2B: queries grouped in small cubes).
     Reading: a token permutation making every run of `block` tokens one
     ct x cy x cx cube (cube grid and cube interior both in raster order).
