@@ -134,6 +134,40 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, device: Optional[torch
         raise ValueError(f"{name} must be contiguous")
 
 
+def _dims(t, name: str, n: int) -> Tuple[int, ...]:
+    """The shape of t, which must be an n-dimensional tensor."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dim() != n:
+        raise ValueError(f"{name} must have {n} dimensions, got shape {tuple(t.shape)}")
+    return tuple(int(v) for v in t.shape)
+
+
+def _shape(t, name: str, shape) -> None:
+    """t must have exactly this shape (the library reads and writes whole tensors)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    want = tuple(int(v) for v in shape)
+    if tuple(t.shape) != want:
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {want}")
+
+
+def _room(t, name: str, n: int) -> None:
+    """t must hold at least n elements (a CSR array may be longer than its contents)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.numel() < n:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs at least {n}")
+
+
+def _groups(N: int, block: int) -> int:
+    return N // block if block > 0 else 0
+
+
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
 def nnz_of(B: int, G: int, k_per_head: Sequence[int]) -> int:
     return B * G * int(sum(int(k) for k in k_per_head))
 
@@ -164,22 +198,32 @@ def attn_bwd_workspace_bytes(B: int, H: int, N: int, d: int, block: int) -> int:
 
 def predict_scores(Q, K, Wq, Wk, block: int, *, out=None, workspace=None, stream=None) -> torch.Tensor:
     """scores[b,h,g,j] = qbar_g . kbar_j (fp32 [B,H,G,nb]); see dsv_predict_scores."""
+    return _predict(lib.dsv_predict_scores, lib.dsv_predict_workspace_bytes, "dsv_predict_scores",
+                    Q, K, Wq, Wk, block, out, workspace, stream)
+
+
+def _predict(fn, ws_fn, what, Q, K, Wq, Wk, block, out, workspace, stream):
+    B, H, N, d = _dims(Q, "Q", 4)
+    _shape(K, "K", (B, H, N, d))
+    r = _dims(Wq, "Wq", 3)[2]
+    _shape(Wq, "Wq", (H, d, r))
+    _shape(Wk, "Wk", (H, d, r))
+    G = _groups(N, block)
+    if out is not None:
+        _shape(out, "out", (B, H, G, G))
     _need(Q, "Q", torch.bfloat16)
     dev = Q.device
     _need(K, "K", torch.bfloat16, dev)
     _need(Wq, "Wq", torch.float32, dev)
     _need(Wk, "Wk", torch.float32, dev)
-    B, H, N, d = Q.shape
-    r = Wq.shape[-1]
     s = Shape(B, H, N, d, block, r)
-    G = N // block if block else 0
     if out is None:
         out = torch.empty(B, H, G, G, dtype=torch.float32, device=dev)
     _need(out, "out", torch.float32, dev)
-    nbytes = lib.dsv_predict_workspace_bytes(s)
+    nbytes = ws_fn(s)
     ws = _workspace(nbytes, dev, workspace)
-    _check(lib.dsv_predict_scores(_ptr(Q), _ptr(K), _ptr(Wq), _ptr(Wk), s, _ptr(out), _ptr(ws), nbytes,
-                                  _stream(dev, stream)), "dsv_predict_scores")
+    with torch.cuda.device(dev):
+        _check(fn(_ptr(Q), _ptr(K), _ptr(Wq), _ptr(Wk), s, _ptr(out), _ptr(ws), nbytes, _stream(dev, stream)), what)
     return out
 
 
@@ -189,32 +233,20 @@ def predict_max_workspace_bytes(B: int, H: int, N: int, d: int, block: int, r: i
 
 def predict_scores_max(Q, K, Wq, Wk, block: int, *, out=None, workspace=None, stream=None) -> torch.Tensor:
     """scores[b,h,g,j] = max low-rank logit of tile (g, j) (fp32 [B,H,G,nb]); see dsv_predict_scores_max."""
-    _need(Q, "Q", torch.bfloat16)
-    dev = Q.device
-    _need(K, "K", torch.bfloat16, dev)
-    _need(Wq, "Wq", torch.float32, dev)
-    _need(Wk, "Wk", torch.float32, dev)
-    B, H, N, d = Q.shape
-    s = Shape(B, H, N, d, block, Wq.shape[-1])
-    G = N // block if block else 0
-    if out is None:
-        out = torch.empty(B, H, G, G, dtype=torch.float32, device=dev)
-    _need(out, "out", torch.float32, dev)
-    nbytes = lib.dsv_predict_max_workspace_bytes(s)
-    ws = _workspace(nbytes, dev, workspace)
-    _check(lib.dsv_predict_scores_max(_ptr(Q), _ptr(K), _ptr(Wq), _ptr(Wk), s, _ptr(out), _ptr(ws), nbytes,
-                                      _stream(dev, stream)), "dsv_predict_scores_max")
-    return out
+    return _predict(lib.dsv_predict_scores_max, lib.dsv_predict_max_workspace_bytes, "dsv_predict_scores_max",
+                    Q, K, Wq, Wk, block, out, workspace, stream)
 
 
 def topk_blocks(scores, k_per_head: Sequence[int], block: int, N: int, d: int = 128, *, outs=None,
                 workspace=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor]:
     """(fwd_ptr, fwd_col, bwd_ptr, bwd_col) int32 CSR lists; see dsv_topk_blocks."""
+    B, H, G, nb = _score_dims(scores, block, N, k_per_head)
+    nnz = nnz_of(B, G, k_per_head)
+    if outs is not None:
+        _csr_room(outs, B * H * G + 1, nnz, B * H * nb + 1, nnz)
     _need(scores, "scores", torch.float32)
     dev = scores.device
-    B, H, G, nb = scores.shape
     s = Shape(B, H, N, d, block, 8)
-    nnz = nnz_of(B, G, k_per_head)
     if outs is None:
         outs = (torch.empty(B * H * G + 1, dtype=torch.int32, device=dev),
                 torch.empty(max(nnz, 1), dtype=torch.int32, device=dev),
@@ -225,10 +257,29 @@ def topk_blocks(scores, k_per_head: Sequence[int], block: int, N: int, d: int = 
     karr = (ctypes.c_int32 * max(H, 1))(*[int(k) for k in k_per_head])
     nbytes = lib.dsv_topk_workspace_bytes(s)
     ws = _workspace(nbytes, dev, workspace)
-    _check(lib.dsv_topk_blocks(_ptr(scores), s, karr, *[_ptr(t) for t in outs], _ptr(ws), nbytes,
-                               _stream(dev, stream)), "dsv_topk_blocks")
+    with torch.cuda.device(dev):
+        _check(lib.dsv_topk_blocks(_ptr(scores), s, karr, *[_ptr(t) for t in outs], _ptr(ws), nbytes,
+                                   _stream(dev, stream)), "dsv_topk_blocks")
     fp, fc, bp, bc = outs
     return fp, fc[:nnz], bp, bc[:nnz]
+
+
+def _score_dims(scores, block: int, N: int, k_per_head=None) -> Tuple[int, int, int, int]:
+    """[B, H, G, nb] of a score matrix, which must be square with G = N / block."""
+    B, H, G, nb = _dims(scores, "scores", 4)
+    if G != nb or G != _groups(N, block):
+        raise ValueError(f"scores has shape {(B, H, G, nb)}, expected [B, H, N/block, N/block] "
+                         f"with N = {N}, block = {block}")
+    if k_per_head is not None and len(k_per_head) != H:
+        raise ValueError(f"k_per_head has {len(k_per_head)} entries, expected one per head ({H})")
+    return B, H, G, nb
+
+
+def _csr_room(outs, n_fptr: int, n_fcol: int, n_bptr: int, n_bcol: int) -> None:
+    if len(outs) != 4:
+        raise ValueError("outs must be (fwd_ptr, fwd_col, bwd_ptr, bwd_col)")
+    for name, t, n in zip(("fwd_ptr", "fwd_col", "bwd_ptr", "bwd_col"), outs, (n_fptr, n_fcol, n_bptr, n_bcol)):
+        _room(t, name, n)
 
 
 def topk_mass_workspace_bytes(B: int, H: int, N: int, d: int, block: int) -> int:
@@ -242,9 +293,11 @@ def topk_mass_blocks(scores, tau: float, block: int, N: int, d: int = 128, *, te
     selects 1/sqrt(d), kmax <= 0 selects nb.  With trim the column arrays are
     returned cut to nnz = fwd_ptr[-1], which this reads back from the device
     (a synchronisation); without it they are returned whole."""
+    B, H, G, nb = _score_dims(scores, block, N)
+    if outs is not None:
+        _csr_room(outs, B * H * G + 1, 0, B * H * nb + 1, 0)     # the columns' capacity goes to the library
     _need(scores, "scores", torch.float32)
     dev = scores.device
-    B, H, G, nb = scores.shape
     s = Shape(B, H, N, d, block, 8)
     temperature = float(temperature) if temperature > 0 else 1.0 / math.sqrt(d)
     kmax = int(kmax) if kmax > 0 else nb
@@ -259,8 +312,10 @@ def topk_mass_blocks(scores, tau: float, block: int, N: int, d: int = 128, *, te
     cap = min(outs[1].numel(), outs[3].numel())
     nbytes = lib.dsv_topk_mass_workspace_bytes(s)
     ws = _workspace(nbytes, dev, workspace)
-    _check(lib.dsv_topk_mass_blocks(_ptr(scores), s, float(tau), temperature, int(kmin), kmax, *[_ptr(t) for t in outs],
-                                    cap, _ptr(ws), nbytes, _stream(dev, stream)), "dsv_topk_mass_blocks")
+    with torch.cuda.device(dev):
+        _check(lib.dsv_topk_mass_blocks(_ptr(scores), s, float(tau), temperature, int(kmin), kmax,
+                                        *[_ptr(t) for t in outs], cap, _ptr(ws), nbytes, _stream(dev, stream)),
+               "dsv_topk_mass_blocks")
     fp, fc, bp, bc = outs
     if not trim:
         return fp, fc, bp, bc
@@ -276,19 +331,28 @@ def topk_blocks_noalloc(scores, k_per_head: Sequence[int], block: int, N: int, d
     device scratch replaces the workspace.  Calls share that scratch, so do
     not let two of them overlap on the GPU.
     """
+    B, H, G, nb = _score_dims(scores, block, N, k_per_head)
+    nnz = nnz_of(B, G, k_per_head)
+    _csr_room(outs, B * H * G + 1, nnz, B * H * nb + 1, nnz)
     _need(scores, "scores", torch.float32)
     dev = scores.device
-    B, H, G, nb = scores.shape
     for name, t in zip(("fwd_ptr", "fwd_col", "bwd_ptr", "bwd_col"), outs):
         _need(t, name, torch.int32, dev)
     karr = (ctypes.c_int32 * max(H, 1))(*[int(k) for k in k_per_head])
-    _check(lib.dsv_topk_blocks_noalloc(_ptr(scores), Shape(B, H, N, d, block, 8), karr, *[_ptr(t) for t in outs],
-                                       _stream(dev, stream)), "dsv_topk_blocks_noalloc")
+    with torch.cuda.device(dev):
+        _check(lib.dsv_topk_blocks_noalloc(_ptr(scores), Shape(B, H, N, d, block, 8), karr,
+                                           *[_ptr(t) for t in outs], _stream(dev, stream)), "dsv_topk_blocks_noalloc")
 
 
 def sparse_attn_fwd(Q, K, V, fwd_ptr, fwd_col, block: int, softmax_scale: float = 0.0, *, out=None, lse=None,
                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """(O bf16 [B,H,N,d], lse fp32 [B,H,N]); see dsv_sparse_attn_fwd."""
+    B, H, N, d = _dims(Q, "Q", 4)
+    for name, t in (("K", K), ("V", V)) + ((("out", out),) if out is not None else ()):
+        _shape(t, name, (B, H, N, d))
+    if lse is not None:
+        _shape(lse, "lse", (B, H, N))
+    _room(fwd_ptr, "fwd_ptr", B * H * _groups(N, block) + 1)
     _need(Q, "Q", torch.bfloat16)
     dev = Q.device
     for name, t in (("K", K), ("V", V)):
@@ -303,15 +367,28 @@ def sparse_attn_fwd(Q, K, V, fwd_ptr, fwd_col, block: int, softmax_scale: float 
         lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
     _need(out, "out", torch.bfloat16, dev)
     _need(lse, "lse", torch.float32, dev)
-    _check(lib.dsv_sparse_attn_fwd(_ptr(Q), _ptr(K), _ptr(V), s, _ptr(fwd_ptr), _ptr(fwd_col),
-                                   float(softmax_scale), _ptr(out), _ptr(lse), _stream(dev, stream)),
-           "dsv_sparse_attn_fwd")
+    with torch.cuda.device(dev):
+        _check(lib.dsv_sparse_attn_fwd(_ptr(Q), _ptr(K), _ptr(V), s, _ptr(fwd_ptr), _ptr(fwd_col),
+                                       float(softmax_scale), _ptr(out), _ptr(lse), _stream(dev, stream)),
+               "dsv_sparse_attn_fwd")
     return out, lse
 
 
 def sparse_attn_bwd(Q, K, V, O, dO, lse, fwd_ptr, fwd_col, bwd_ptr, bwd_col, block: int,
                     softmax_scale: float = 0.0, *, outs=None, workspace=None, stream=None):
     """(dQ, dK, dV) bf16 [B,H,N,d]; see dsv_sparse_attn_bwd."""
+    B, H, N, d = _dims(Q, "Q", 4)
+    for name, t in (("K", K), ("V", V), ("O", O), ("dO", dO)):
+        _shape(t, name, (B, H, N, d))
+    if outs is not None:
+        if len(outs) != 3:
+            raise ValueError("outs must be (dQ, dK, dV)")
+        for name, t in zip(("dQ", "dK", "dV"), outs):
+            _shape(t, name, (B, H, N, d))
+    _shape(lse, "lse", (B, H, N))
+    rows = B * H * _groups(N, block) + 1
+    _room(fwd_ptr, "fwd_ptr", rows)
+    _room(bwd_ptr, "bwd_ptr", rows)
     _need(Q, "Q", torch.bfloat16)
     dev = Q.device
     for name, t in (("K", K), ("V", V), ("O", O), ("dO", dO)):
@@ -327,10 +404,11 @@ def sparse_attn_bwd(Q, K, V, O, dO, lse, fwd_ptr, fwd_col, bwd_ptr, bwd_col, blo
         _need(t, name, torch.bfloat16, dev)
     nbytes = lib.dsv_attn_bwd_workspace_bytes(s)
     ws = _workspace(nbytes, dev, workspace)
-    _check(lib.dsv_sparse_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse), s,
-                                   _ptr(fwd_ptr), _ptr(fwd_col), _ptr(bwd_ptr), _ptr(bwd_col),
-                                   float(softmax_scale), *[_ptr(t) for t in outs], _ptr(ws), nbytes,
-                                   _stream(dev, stream)), "dsv_sparse_attn_bwd")
+    with torch.cuda.device(dev):
+        _check(lib.dsv_sparse_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse), s,
+                                       _ptr(fwd_ptr), _ptr(fwd_col), _ptr(bwd_ptr), _ptr(bwd_col),
+                                       float(softmax_scale), *[_ptr(t) for t in outs], _ptr(ws), nbytes,
+                                       _stream(dev, stream)), "dsv_sparse_attn_bwd")
     return outs
 
 
@@ -339,6 +417,9 @@ def cube_permute(x, grid, cube, *, inverse: bool = False, out=None, stream=None)
 
     grid = (T, Hl, Wl) with N = T*Hl*Wl; cube = (ct, cy, cx), whose volume is
     the group / block size of the hot path."""
+    _dims(x, "x", 4)
+    if out is not None:
+        _shape(out, "out", x.shape)
     _need(x, "x", torch.bfloat16)
     dev = x.device
     B, H, N, d = x.shape
@@ -348,26 +429,37 @@ def cube_permute(x, grid, cube, *, inverse: bool = False, out=None, stream=None)
         out = torch.empty_like(x)
     _need(out, "out", torch.bfloat16, dev)
     s = Shape(B, H, N, d, ct * cy * cx, 8)
-    _check(lib.dsv_cube_permute(_ptr(x), _ptr(out), s, T, Hl, Wl, ct, cy, cx, 1 if inverse else 0,
-                                _stream(dev, stream)), "dsv_cube_permute")
+    with torch.cuda.device(dev):
+        _check(lib.dsv_cube_permute(_ptr(x), _ptr(out), s, T, Hl, Wl, ct, cy, cx, 1 if inverse else 0,
+                                    _stream(dev, stream)), "dsv_cube_permute")
     return out
 
 
 def attn_bwd_preprocess(O, dO, lse, block: int, *, workspace, stream=None) -> None:
     """D and lse * log2(e) into `workspace`; see dsv_attn_bwd_preprocess."""
+    B, H, N, d = _dims(O, "O", 4)
+    _shape(dO, "dO", (B, H, N, d))
+    _shape(lse, "lse", (B, H, N))
     _need(O, "O", torch.bfloat16)
     dev = O.device
     _need(dO, "dO", torch.bfloat16, dev)
     _need(lse, "lse", torch.float32, dev)
-    B, H, N, d = O.shape
+    _need(workspace, "workspace", workspace.dtype, dev)
     s = Shape(B, H, N, d, block, 8)
-    _check(lib.dsv_attn_bwd_preprocess(_ptr(O), _ptr(dO), _ptr(lse), s, _ptr(workspace), workspace.numel(),
-                                       _stream(dev, stream)), "dsv_attn_bwd_preprocess")
+    with torch.cuda.device(dev):
+        _check(lib.dsv_attn_bwd_preprocess(_ptr(O), _ptr(dO), _ptr(lse), s, _ptr(workspace), _nbytes(workspace),
+                                           _stream(dev, stream)), "dsv_attn_bwd_preprocess")
 
 
 def attn_bwd_dkdv(Q, K, V, dO, bwd_ptr, bwd_col, block: int, softmax_scale: float = 0.0, *, outs, workspace,
                   stream=None) -> None:
     """dK, dV into outs = (dK, dV) after attn_bwd_preprocess; see dsv_attn_bwd_dkdv."""
+    B, H, N, d = _dims(Q, "Q", 4)
+    if len(outs) != 2:
+        raise ValueError("outs must be (dK, dV)")
+    for name, t in (("K", K), ("V", V), ("dO", dO), ("dK", outs[0]), ("dV", outs[1])):
+        _shape(t, name, (B, H, N, d))
+    _room(bwd_ptr, "bwd_ptr", B * H * _groups(N, block) + 1)
     _need(Q, "Q", torch.bfloat16)
     dev = Q.device
     for name, t in (("K", K), ("V", V), ("dO", dO), ("dK", outs[0]), ("dV", outs[1])):
@@ -376,14 +468,20 @@ def attn_bwd_dkdv(Q, K, V, dO, bwd_ptr, bwd_col, block: int, softmax_scale: floa
         _need(t, name, torch.int32, dev)
     B, H, N, d = Q.shape
     s = Shape(B, H, N, d, block, 8)
-    _check(lib.dsv_attn_bwd_dkdv(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), s, _ptr(bwd_ptr), _ptr(bwd_col),
-                                 float(softmax_scale), _ptr(outs[0]), _ptr(outs[1]), _ptr(workspace),
-                                 workspace.numel(), _stream(dev, stream)), "dsv_attn_bwd_dkdv")
+    _need(workspace, "workspace", workspace.dtype, dev)
+    with torch.cuda.device(dev):
+        _check(lib.dsv_attn_bwd_dkdv(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), s, _ptr(bwd_ptr), _ptr(bwd_col),
+                                     float(softmax_scale), _ptr(outs[0]), _ptr(outs[1]), _ptr(workspace),
+                                     _nbytes(workspace), _stream(dev, stream)), "dsv_attn_bwd_dkdv")
 
 
 def attn_bwd_dq(Q, K, V, dO, fwd_ptr, fwd_col, block: int, softmax_scale: float = 0.0, *, out, workspace,
                 stream=None) -> None:
     """dQ into `out` after attn_bwd_preprocess; see dsv_attn_bwd_dq."""
+    B, H, N, d = _dims(Q, "Q", 4)
+    for name, t in (("K", K), ("V", V), ("dO", dO), ("dQ", out)):
+        _shape(t, name, (B, H, N, d))
+    _room(fwd_ptr, "fwd_ptr", B * H * _groups(N, block) + 1)
     _need(Q, "Q", torch.bfloat16)
     dev = Q.device
     for name, t in (("K", K), ("V", V), ("dO", dO), ("dQ", out)):
@@ -392,9 +490,11 @@ def attn_bwd_dq(Q, K, V, dO, fwd_ptr, fwd_col, block: int, softmax_scale: float 
         _need(t, name, torch.int32, dev)
     B, H, N, d = Q.shape
     s = Shape(B, H, N, d, block, 8)
-    _check(lib.dsv_attn_bwd_dq(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), s, _ptr(fwd_ptr), _ptr(fwd_col),
-                               float(softmax_scale), _ptr(out), _ptr(workspace), workspace.numel(),
-                               _stream(dev, stream)), "dsv_attn_bwd_dq")
+    _need(workspace, "workspace", workspace.dtype, dev)
+    with torch.cuda.device(dev):
+        _check(lib.dsv_attn_bwd_dq(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), s, _ptr(fwd_ptr), _ptr(fwd_col),
+                                   float(softmax_scale), _ptr(out), _ptr(workspace), _nbytes(workspace),
+                                   _stream(dev, stream)), "dsv_attn_bwd_dq")
 
 
 # ---------------------------------------------------------------------------

@@ -181,3 +181,56 @@ def test_host_validation_predict_max(lib):
     big = _shape(lib, B=1, H=1, N=64 * 200000, d=64, block=64, r=8)
     assert L.dsv_predict_scores_max(*ok, big, FAKE, FAKE, 1 << 40, None) == lib.DSV_ERR_UNSUPPORTED
     assert L.dsv_predict_scores_max(None, None, None, None, _shape(lib, N=0), None, None, 0, None) == lib.DSV_OK
+
+
+def test_binding_rejects_mismatched_shapes_on_the_host(lib):
+    """The binding checks every tensor's shape (and each CSR array's room)
+    before the device check and before any call into the library."""
+    import torch
+    bf = torch.bfloat16
+    Q = torch.zeros(1, 2, 256, 64, dtype=bf)             # G = nb = 4 at block 64
+    W = torch.zeros(2, 64, 16)
+    S = torch.zeros(1, 2, 4, 4)
+    i32 = lambda n: torch.zeros(n, dtype=torch.int32)   # noqa: E731
+    with pytest.raises(ValueError, match="K has shape"):
+        lib.predict_scores(Q, torch.zeros(1, 2, 128, 64, dtype=bf), W, W, 64)
+    with pytest.raises(ValueError, match="Wk has shape"):
+        lib.predict_scores(Q, Q, W, torch.zeros(2, 64, 8), 64)
+    with pytest.raises(ValueError, match="Wq must have 3 dimensions"):
+        lib.predict_scores_max(Q, Q, W[0], W, 64)
+    with pytest.raises(ValueError, match="out has shape"):
+        lib.predict_scores_max(Q, Q, W, W, 64, out=torch.zeros(1, 2, 4, 3))
+    with pytest.raises(ValueError, match="scores has shape"):
+        lib.topk_blocks(S, [1, 1], 64, 512)
+    with pytest.raises(ValueError, match="k_per_head has 1 entries"):
+        lib.topk_blocks(S, [1], 64, 256)
+    with pytest.raises(ValueError, match="fwd_col holds 15"):
+        lib.topk_blocks(S, [2, 2], 64, 256, outs=(i32(9), i32(15), i32(9), i32(16)))
+    with pytest.raises(ValueError, match="bwd_ptr holds 8"):
+        lib.topk_blocks_noalloc(S, [2, 2], 64, 256, outs=(i32(9), i32(16), i32(8), i32(16)))
+    with pytest.raises(ValueError, match="fwd_ptr holds 8"):
+        lib.topk_mass_blocks(S, 0.9, 64, 256, outs=(i32(8), i32(32), i32(9), i32(32)))
+    with pytest.raises(ValueError, match="V has shape"):
+        lib.sparse_attn_fwd(Q, Q, Q[:, :1], i32(9), i32(8), 64)
+    with pytest.raises(ValueError, match="fwd_ptr holds 8"):
+        lib.sparse_attn_fwd(Q, Q, Q, i32(8), i32(8), 64)
+    with pytest.raises(ValueError, match="lse has shape"):
+        lib.sparse_attn_fwd(Q, Q, Q, i32(9), i32(8), 64, lse=torch.zeros(1, 2, 255))
+    with pytest.raises(ValueError, match="lse has shape"):
+        lib.sparse_attn_bwd(Q, Q, Q, Q, Q, torch.zeros(1, 2, 255), i32(9), i32(8), i32(9), i32(8), 64)
+    with pytest.raises(ValueError, match="dV has shape"):
+        lib.sparse_attn_bwd(Q, Q, Q, Q, Q, torch.zeros(1, 2, 256), i32(9), i32(8), i32(9), i32(8), 64,
+                            outs=(Q, Q, Q[..., :32]))
+    with pytest.raises(ValueError, match="bwd_ptr holds 4"):
+        lib.attn_bwd_dkdv(Q, Q, Q, Q, i32(4), i32(8), 64, outs=(Q, Q), workspace=i32(64))
+    with pytest.raises(ValueError, match="dQ has shape"):
+        lib.attn_bwd_dq(Q, Q, Q, Q, i32(9), i32(8), 64, out=Q[0], workspace=i32(64))
+    with pytest.raises(ValueError, match="dO has shape"):
+        lib.attn_bwd_preprocess(Q, Q[:, :, :128], torch.zeros(1, 2, 256), 64, workspace=i32(64))
+    with pytest.raises(ValueError, match="out has shape"):
+        lib.cube_permute(Q, (4, 8, 8), (1, 8, 8), out=Q[:, :1])
+    # consistent shapes reach the device check, still before the library
+    with pytest.raises(ValueError, match="CUDA device"):
+        lib.predict_scores(Q, Q, W, W, 64)
+    with pytest.raises(ValueError, match="CUDA device"):
+        lib.sparse_attn_bwd(Q, Q, Q, Q, Q, torch.zeros(1, 2, 256), i32(9), i32(8), i32(9), i32(8), 64)
