@@ -48,7 +48,11 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="latent16k")
+    p.add_argument("--workload", default="long518k",
+                   help="synthetic workload (default: long518k, the largest one-GPU configuration)")
+    p.add_argument("--heads", type=int, default=0, metavar="N",
+                   help="keep only the first N heads of the workload (a reduced case of the same per-head "
+                        "structure, for profiler captures); 0 = all")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--mass", type=float, default=0.0, metavar="TAU",
                    help="select per group the smallest top set carrying >= TAU of the predicted mass (instead of top-k)")
@@ -272,22 +276,30 @@ KERNELS_PER_STEP = {"predict": 2, "topk": 4, "fwd": 1, "bwd_pre": 1, "bwd_kv": 2
 STAGES = ("predict", "topk", "fwd", "bwd_pre", "bwd_kv", "bwd_q")
 
 
-def profile_traffic(kernel: str, source_files):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel's
-    sources still hash to what was profiled; else None."""
+def profile_traffic(kernel: str, source_files, w, pairs):
+    """DRAM bytes per launch of `kernel` on this workload, from a committed
+    ncu summary (profiles/traffic.json): None unless the entry was captured on
+    the same workload and the kernel's sources still hash to what was
+    profiled.  An entry captured on a head subset of the workload (same
+    per-head structure) is scaled to this launch by its pairs; the second
+    value says how the figure was obtained."""
     f = ROOT / "profiles" / "traffic.json"
     if not f.exists():
-        return None
-    data = json.loads(f.read_text())
-    ent = data.get(kernel)
-    if not ent:
-        return None
+        return None, None
+    ent = json.loads(f.read_text()).get(kernel)
+    if not ent or ent.get("workload") != w.name:
+        return None, None
     h = hashlib.sha256()
     for s in source_files:
         h.update((ROOT / s).read_bytes())
     if ent.get("source_sha256") != h.hexdigest():
-        return None
-    return ent.get("dram_bytes_per_launch")
+        return None, None
+    got = float(ent["dram_bytes_per_launch"])
+    cap_pairs = ent.get("pairs")
+    if cap_pairs and pairs and cap_pairs != pairs:
+        return round(got * pairs / cap_pairs), (f"ncu DRAM read+write of a {ent.get('heads')}-head capture of "
+                                                f"{w.name} ({cap_pairs} pairs), scaled by pairs to {pairs}")
+    return round(got), f"ncu DRAM read+write per launch on {w.name}"
 
 
 def run_ours(args):
@@ -304,6 +316,8 @@ def run_ours(args):
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
     w = wl.WORKLOADS[args.workload]
+    if args.heads and args.heads < w.H:
+        w = wl.scaled(w, name=w.name, H=args.heads)
     x = wl.make_inputs(w, device=dev)
     cube = tuple(int(v) for v in args.cube.split(",")) if args.cube else None
     hp = HotPath(dsv, x, w, x.k_per_head, cube=cube, mass=args.mass or None, scores=args.scores)
@@ -353,11 +367,13 @@ def run_ours(args):
     # dense run of the same kernels (k = nb) for the speedup
     dense = None
     if not args.no_dense:
-        dense = time_dense(dsv, x, w, hp, flush)
+        dense = time_dense(dsv, x, w, hp, flush, attn_ms=attn_ms,
+                           pre_ms=per_call["predict"] + per_call["topk"])
 
     # roofline of the dominant kernel (the predictor and the top-k are whole calls of 2 and 4 launches)
     dom = max(STAGES, key=lambda k: per_call[k])
     roofline = roofline_entry(dom, per_call, w, hp, peaks, peak_src)
+    bwd_eff = step_flops * bwd_f / (fwd_f + bwd_f) / (per_call["bwd"] * 1e-3) / 1e12
 
     e2e = None if args.no_e2e else time_e2e(dsv, x, w, hp, args, flops_per_step=step_flops)
     out = {
@@ -368,6 +384,7 @@ def run_ours(args):
                    "block": w.block, "r": w.r,
                    "k_per_head": None if args.mass else sorted(set(x.k_per_head)), "pairs": hp.nnz,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   **({"heads_kept": w.H, "reduced": "first heads only (profiler case)"} if args.heads else {}),
                    **({"cube": list(cube), "token_order": "3D cubes (dsv_cube_permute in and out, timed)"}
                       if cube else {}),
                    **({"selection": f"mass threshold tau={args.mass}, temperature 1/sqrt(d), k in [1, nb]"}
@@ -382,6 +399,10 @@ def run_ours(args):
                            "pct_of_bf16_peak": round(100.0 * step_flops / (attn_ms * 1e-3) / 1e12
                                                      / peaks["bf16_tflops"], 2)},
         "breakdown_ms": {k: round(v, 4) for k, v in per_call.items()},
+        "backward_effective": {"tflops": round(bwd_eff, 3), "frac": round(bwd_eff / peaks["bf16_tflops"], 4),
+                               "algorithmic": "10*block^2*d FLOP per pair (5 GEMMs) over the three backward "
+                                              "stages' time; the kernels execute 7 (S and dP twice, no atomics)"},
+        "predictor_topk": hbm_fractions(w, hp, per_call, peaks),
         "speedup_vs_dense": dense,
         "roofline": roofline,
         "gpu_launches": (sum(KERNELS_PER_STEP[k] for k in stages) + (2 if args.mass else 0)) * args.steps,
@@ -412,6 +433,7 @@ KERNEL_SRC = {"fwd": "dynamic_block_sparse_projection_gb300/csrc/attn_fwd.cu",
 def roofline_entry(dom, per_call, w, hp, peaks, peak_src):
     B, H, N, d, G = w.B, w.H, w.N, w.d, w.nb
     srcs = [KERNEL_SRC[dom], "dynamic_block_sparse_projection_gb300/csrc/dsv_device.cuh"]
+    traffic, tnote = profile_traffic(KERNEL_OF.get(dom, dom), srcs, w, hp.nnz)
     if dom in MMAS_PER_PAIR:
         flops = MMAS_PER_PAIR[dom] * 2 * w.block * w.block * d * hp.nnz
         achieved = flops / (per_call[dom] * 1e-3) / 1e12
@@ -420,7 +442,7 @@ def roofline_entry(dom, per_call, w, hp, peaks, peak_src):
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                 "algorithmic": f"{MMAS_PER_PAIR[dom]} x 2*block^2*d FLOP per (group, block) pair x {hp.nnz} pairs",
                 "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
-                "traffic": profile_traffic(KERNEL_OF[dom], srcs)}
+                "traffic": traffic, "traffic_source": tnote}
     if dom == "predict" and hp.scores == "max":
         # every logit of every tile: 2 * r FLOP per (query token, key token) pair, fp32 FMA on the CUDA cores
         flops = 2.0 * B * H * N * N * w.r
@@ -443,38 +465,50 @@ def roofline_entry(dom, per_call, w, hp, peaks, peak_src):
     peak = peaks["hbm_gbs"]
     return {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} copy",
-            "traffic": profile_traffic(kname, srcs)}
+            "traffic": profile_traffic(kname, srcs, w, hp.nnz)[0]}
 
 
-def time_dense(dsv, x, w, hp, flush, iters=2):
-    """The same attention kernels with every block selected (k = nb)."""
+DENSE_MAX_PAIRS = 1 << 25    # a dense run with more pairs is timed on 2 heads and scaled (heads are independent)
+
+
+def time_dense(dsv, x, w, hp, flush, attn_ms, pre_ms, iters=2):
+    """The same attention kernels with every block selected (k = nb).  Heads
+    are independent, so a large workload's dense run is timed on its first 2
+    heads and scaled by H / 2 (long518k: ~0.5 PFLOP per head, ~10 s for all
+    24)."""
     import torch
     B, H, G = w.B, w.H, w.nb
+    heads = H if B * H * G * G <= DENSE_MAX_PAIRS else min(2, H)
     dev = x.Q.device
-    rows = B * H * G
+    Q, K, V, dO = ((t if heads == H else t[:, :heads].contiguous()) for t in (x.Q, x.K, x.V, x.dO))
+    rows = B * heads * G
     fp = torch.arange(0, rows * G + 1, G, dtype=torch.int32, device=dev)
     fc = torch.arange(G, dtype=torch.int32, device=dev).repeat(rows)
     dense_pairs = rows * G
     fwd_f, bwd_f = pair_flops(w.block, w.d)
-    O = torch.empty_like(x.Q)
-    lse = torch.empty_like(hp.lse)
-    grads = tuple(torch.empty_like(t) for t in (x.Q, x.K, x.V))
-    # with every block selected the transposed lists have the same form
-    dsv.sparse_attn_fwd(x.Q, x.K, x.V, fp, fc, w.block, out=O, lse=lse)
-    dsv.sparse_attn_bwd(x.Q, x.K, x.V, O, x.dO, lse, fp, fc, fp, fc, w.block, outs=grads, workspace=hp.ws_b)
+    O = torch.empty_like(Q)
+    lse = torch.empty(B, heads, w.N, dtype=torch.float32, device=dev)
+    grads = tuple(torch.empty_like(t) for t in (Q, K, V))
+
+    def run():
+        # with every block selected the transposed lists have the same form as the forward ones
+        dsv.sparse_attn_fwd(Q, K, V, fp, fc, w.block, out=O, lse=lse)
+        dsv.sparse_attn_bwd(Q, K, V, O, dO, lse, fp, fc, fp, fc, w.block, outs=grads, workspace=hp.ws_b)
+
+    run()
     torch.cuda.synchronize()
     ts = []
     for _ in range(iters):
         flush.fill_(1)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        dsv.sparse_attn_fwd(x.Q, x.K, x.V, fp, fc, w.block, out=O, lse=lse)
-        dsv.sparse_attn_bwd(x.Q, x.K, x.V, O, x.dO, lse, fp, fc, fp, fc, w.block, outs=grads, workspace=hp.ws_b)
+        run()
         b.record()
         torch.cuda.synchronize()
         ts.append(a.elapsed_time(b))
-    t_dense = min(ts)
-    # sparse attention only, same measurement
+    t_meas = min(ts)
+    t_dense = t_meas * H / heads
+    # sparse attention only, same measurement (the fused backward call)
     ts = []
     for _ in range(iters):
         flush.fill_(2)
@@ -485,10 +519,32 @@ def time_dense(dsv, x, w, hp, flush, iters=2):
         torch.cuda.synchronize()
         ts.append(a.elapsed_time(b))
     t_sparse = min(ts)
-    dense_tflops = (fwd_f + bwd_f) * dense_pairs / (t_dense * 1e-3) / 1e12
+    dense_tflops = (fwd_f + bwd_f) * dense_pairs / (t_meas * 1e-3) / 1e12
     return {"dense_attn_ms": round(t_dense, 3), "sparse_attn_ms": round(t_sparse, 3),
-            "speedup": round(t_dense / t_sparse, 3), "dense_tflops": round(dense_tflops, 3),
-            "dense_pairs": dense_pairs}
+            "speedup": round(t_dense / t_sparse, 3),
+            "speedup_with_predictor_topk": round(t_dense / (t_sparse + pre_ms), 3),
+            "step_attention_ms": round(attn_ms, 3),
+            "dense_tflops": round(dense_tflops, 3), "dense_pairs": dense_pairs * H // heads,
+            "dense_heads_timed": heads,
+            "method": ("all heads" if heads == H else
+                       f"timed on {heads} of {H} heads ({dense_pairs} pairs) and scaled by {H}/{heads}: heads are "
+                       f"independent") + "; same kernels with k = nb, L2 flushed, best of %d" % iters}
+
+
+def hbm_fractions(w, hp, per_call, peaks):
+    """Algorithmic bytes and HBM fraction of the predictor and of the top-k."""
+    B, H, N, d, G = w.B, w.H, w.N, w.d, w.nb
+    pred = 2 * B * H * N * d * 2 + 4 * B * H * G * G
+    topk = 4 * B * H * G * G + 8 * hp.nnz + 4 * (B * H * G + 1) + 4 * (B * H * G + 1)
+    out = {}
+    for nm, nbytes, ms in (("predict", pred, per_call["predict"]), ("topk", topk, per_call["topk"]),
+                           ("predict+topk", pred + topk, per_call["predict"] + per_call["topk"])):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[nm] = {"bytes": nbytes, "ms": round(ms, 4), "gbs": round(gbs, 1),
+                   "frac": round(gbs / peaks["hbm_gbs"], 4), "frac_of_8tbs": round(gbs / 8000.0, 4)}
+    out["bytes_rule"] = ("predict: read Q and K + write S; top-k: read S + write both column arrays and "
+                         "both row-pointer arrays")
+    return out
 
 
 def time_e2e(dsv, x, w, hp, args, flops_per_step):
@@ -500,7 +556,8 @@ def time_e2e(dsv, x, w, hp, args, flops_per_step):
     region runs from the first host-to-device copy to the last device-to-host
     copy."""
     import torch
-    host_in = [t.cpu().pin_memory() for t in (x.Q, x.K, x.V, x.dO, x.Wq, x.Wk)]
+    host_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in (x.Q, x.K, x.V, x.dO, x.Wq, x.Wk)]
+    host_out = None     # one set of pinned result buffers: the device-to-host copies run in order on one stream
 
     class X:
         pass
@@ -511,7 +568,8 @@ def time_e2e(dsv, x, w, hp, args, flops_per_step):
         xd = X()
         xd.Q, xd.K, xd.V, xd.dO, xd.Wq, xd.Wk = dev_in
         hp2 = HotPath(dsv, xd, w, hp.k, cube=hp.cube, mass=hp.mass, scores=hp.scores)
-        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in hp2.results()]
+        if host_out is None:
+            host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in hp2.results()]
         sets.append((dev_in, hp2, host_out))
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in sets[0][2])
@@ -550,8 +608,12 @@ def time_e2e(dsv, x, w, hp, args, flops_per_step):
     b.record(s_out)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / args.steps
+    del sets, host_in, host_out
+    torch.cuda.empty_cache()
+    if hasattr(torch._C, "_host_emptyCache"):
+        torch._C._host_emptyCache()          # hand the pinned buffers back before the oracle leg
     return {"value": round(flops_per_step / (ms * 1e-3) / 1e12, 3), "unit": UNIT, "ms_per_step": round(ms, 4),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "pinned_host_bytes": h2d + d2h,
             "overlap": "host-to-device and device-to-host copies on their own streams overlap neighbouring steps' compute (2 buffer sets)"}
 
 
@@ -559,49 +621,215 @@ def time_e2e(dsv, x, w, hp, args, flops_per_step):
 # the oracle on the host cores (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_head_step(w, x, b, h, cube=None, mass=None, scores="mean"):
-    """The fp64 oracle's whole hot path for one (b, h) (with cube, on the
-    tokens in cube order, and O and the gradients put back): returns its pair
-    count."""
+ORACLE_HEADS, ORACLE_GROUPS_PER_HEAD = 4, 16       # 64 seeded query groups in 4 seeded (batch, head) slices
+BLAS_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
+
+
+def oracle_sample(w):
+    """The seeded sample the oracle legs time: ORACLE_HEADS (batch, head)
+    slices and ORACLE_GROUPS_PER_HEAD query groups in each, as
+    [((b, h), [g, ...]), ...]."""
+    from dynamic_block_sparse_projection_gb300 import workloads as wl
+    bhs = wl.sample_indices(w.B * w.H, ORACLE_HEADS, w.seed)
+    out = []
+    for i, bh in enumerate(bhs):
+        groups = wl.sample_indices(w.nb, ORACLE_GROUPS_PER_HEAD, w.seed, gid=100 + i)
+        out.append(((bh // w.H, bh % w.H), groups))
+    return out
+
+
+class _Bf16Head:
+    """A [1, 1, N, d] stand-in for one (batch, head) slice of a bf16 tensor
+    kept as raw 16-bit patterns (a memory-mapped file): indexing widens just
+    the rows it selects to fp32, exactly.  Lets the oracle functions index a
+    518k-token head without every worker holding it in floating point."""
+
+    def __init__(self, bits):
+        self.bits = bits
+        self.shape = (1, 1) + tuple(bits.shape)
+
+    def __getitem__(self, idx):
+        import numpy as np
+        rest = idx[2:] if isinstance(idx, tuple) else ()
+        sel = self.bits[rest] if rest else self.bits
+        return (np.asarray(sel).astype(np.uint32) << 16).view(np.float32)
+
+    def full(self):
+        return self[(0, 0)][None, None]
+
+
+def _oracle_worker(conn, path, meta):
+    """One host core: loads its (batch, head) slice from `path` once (input
+    staging, untimed), then on each request runs the fp64 oracle's whole hot
+    path for one of its query groups -- predictor row, top-k (or the mass
+    count), attention forward and the group's backward (dQ and the group's
+    dK/dV contributions, every pair of its list) -- and answers the pairs and
+    the seconds it took."""
     import numpy as np
-    import torch
 
     import oracle
-    f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
-    Q, K, V, dO = (f64(t[b:b + 1, h:h + 1]) for t in (x.Q, x.K, x.V, x.dO))
-    perm = oracle.cube_order(w.T, w.Hl, w.Wl, *cube) if cube else None
-    if cube:
-        Q, K, V, dO = (oracle.permute_tokens(t, perm) for t in (Q, K, V, dO))
-    Wq, Wk = f64(x.Wq[h:h + 1]), f64(x.Wk[h:h + 1])
-    S = (oracle.predict_scores_max if scores == "max" else oracle.predict_scores)(Q, K, Wq, Wk, w.block)
-    if mass:
-        fp, fc = oracle.mass_lists(S, mass, 1.0 / math.sqrt(w.d), 1, w.nb)
-    else:
-        fp, fc = oracle.topk_lists(S, [x.k_per_head[h]])
-    oracle.transpose_lists(fp, fc, 1, 1, w.nb, w.nb)
-    O, _ = oracle.attn_fwd_groups(Q, K, V, fp, fc, w.block)
-    grads = oracle.attn_bwd_groups(Q, K, V, dO, fp, fc, w.block)
-    if cube:
-        for t in (O, *grads):
-            oracle.permute_tokens(t, perm, inverse=True)
-    return int(fc.shape[0])
+    X = {nm: _Bf16Head(np.load(os.path.join(path, nm + ".npy"), mmap_mode="r")) for nm in ("Q", "K", "V", "dO")}
+    Wq = np.load(os.path.join(path, "Wq.npy"))[None]
+    Wk = np.load(os.path.join(path, "Wk.npy"))[None]
+    block, d, k, nb = meta["block"], meta["d"], meta["k"], meta["nb"]
+    if meta["cube"]:
+        perm = oracle.cube_order(*meta["grid"], *meta["cube"])
+        X = {nm: oracle.permute_tokens(t.full(), perm) for nm, t in X.items()}
+    Q, K, V, dO = X["Q"], X["K"], X["V"], X["dO"]
+    conn.send("ready")
+    while True:
+        g = conn.recv()
+        if g is None:
+            break
+        t0 = time.perf_counter()
+        rows = [(0, 0, g)]
+        pred = oracle.predict_scores_max_rows if meta["scores"] == "max" else oracle.predict_scores_rows
+        s = pred(Q, K, Wq, Wk, block, rows)[0]
+        m = (oracle.mass_count_row(s, meta["mass"], 1.0 / math.sqrt(d), 1, nb) if meta["mass"] else k)
+        cols = oracle.topk_row(s, m)
+        ptr = np.zeros(nb + 1, dtype=np.int64)
+        ptr[g + 1:] = len(cols)
+        oracle.attn_fwd_groups(Q, K, V, ptr, cols, block, rows=rows)
+        oracle.attn_bwd_dq_rows(Q, K, V, dO, ptr, cols, block, rows)
+        conn.send((len(cols), time.perf_counter() - t0))
+    conn.close()
+
+
+class OraclePool:
+    """The fp64 oracle on the host cores: one spawned process per core, each
+    owning a few of the seeded query groups of one sampled (batch, head)
+    slice (ORACLE_GROUPS_PER_HEAD per head, split over the cores).  A round
+    asks every process for one of its groups; a round's wall time is the
+    slowest process.  BLAS runs single-threaded in each process, so the
+    cores used are the processes."""
+
+    def __init__(self, w, x_heads, cube=None, mass=None, scores="mean", cores=None):
+        import multiprocessing as mp
+
+        import numpy as np
+        self.w = w
+        sample = oracle_sample(w)
+        cores = cores or os.cpu_count() or 1
+        per_head = max(1, cores // len(sample))
+        self.tmp = tempfile.mkdtemp(prefix="dsv_oracle_", dir=_scratch_dir(w, len(sample)))
+        self.slots = []                                  # (process, conn, [groups])
+        ctx = mp.get_context("spawn")
+        saved = {v: os.environ.get(v) for v in BLAS_THREAD_VARS}
+        os.environ.update({v: "1" for v in BLAS_THREAD_VARS})
+        try:
+            for i, ((b, h), groups) in enumerate(sample):
+                path = os.path.join(self.tmp, f"bh{i}")
+                os.mkdir(path)
+                for nm in ("Q", "K", "V", "dO"):
+                    t = getattr(x_heads, nm)[b, x_heads.head_index[h]]
+                    np.save(os.path.join(path, nm + ".npy"), t.cpu().view(__import__("torch").int16).numpy())
+                hi = x_heads.head_index[h]
+                np.save(os.path.join(path, "Wq.npy"), x_heads.Wq[hi].double().cpu().numpy())
+                np.save(os.path.join(path, "Wk.npy"), x_heads.Wk[hi].double().cpu().numpy())
+                meta = {"block": w.block, "d": w.d, "k": int(x_heads.k_per_head[hi]), "nb": w.nb, "cube": cube,
+                        "grid": (w.T, w.Hl, w.Wl), "mass": mass, "scores": scores}
+                for part in range(min(per_head, len(groups))):
+                    mine = groups[part::per_head]
+                    a, bconn = ctx.Pipe()
+                    p = ctx.Process(target=_oracle_worker, args=(bconn, path, meta), daemon=True)
+                    p.start()
+                    self.slots.append((p, a, mine))
+        finally:
+            for v, old in saved.items():
+                if old is None:
+                    os.environ.pop(v, None)
+                else:
+                    os.environ[v] = old
+        for _, a, _ in self.slots:
+            if a.recv() != "ready":
+                raise RuntimeError("oracle worker failed to start")
+        self.groups = sum(len(s[2]) for s in self.slots)
+        self.max_groups = max(len(s[2]) for s in self.slots)     # rounds until every group has run once
+        self.rounds = 0
+
+    @property
+    def cores(self):
+        return len(self.slots)
+
+    def round(self):
+        """Every process runs one of its groups (in turn); returns (pairs, wall seconds)."""
+        t0 = time.perf_counter()
+        for _, a, mine in self.slots:
+            a.send(mine[self.rounds % len(mine)])
+        pairs = sum(a.recv()[0] for _, a, _ in self.slots)
+        self.rounds += 1
+        return pairs, time.perf_counter() - t0
+
+    def close(self):
+        import shutil
+        for p, a, _ in self.slots:
+            try:
+                a.send(None)
+            except OSError:
+                pass
+        for p, _, _ in self.slots:
+            p.join(timeout=30)
+            if p.is_alive():
+                p.terminate()
+        shutil.rmtree(self.tmp, ignore_errors=True)
+
+    def describe(self):
+        sample = oracle_sample(self.w)
+        return (f"{self.groups} seeded query groups of {self.w.name} ({len(sample[0][1])} in each of "
+                f"{len(sample)} seeded (batch, head) slices {[bh for bh, _ in sample]}); per group the fp64 numpy "
+                f"oracle's predictor row, top-k, attention forward and the group's backward (dQ and its dK/dV "
+                f"contributions) over every pair of its list; {self.cores} processes, one per host core, BLAS "
+                f"single-threaded")
+
+
+def _scratch_dir(w, heads):
+    """A directory with room for the sampled slices' raw bf16 tensors."""
+    import shutil
+    need = 2 * heads * 4 * w.N * w.d * 2
+    for cand in ("/dev/shm", tempfile.gettempdir()):
+        try:
+            if os.path.isdir(cand) and shutil.disk_usage(cand).free > need:
+                return cand
+        except OSError:
+            continue
+    return tempfile.gettempdir()
+
+
+def oracle_inputs(w, device):
+    """The workload's tensors for the sampled (batch, head) slices only (drawn
+    on `device` from the same seeded generators, so they are the values the
+    GPU arm sees), with head_index mapping a head to its position."""
+    from dynamic_block_sparse_projection_gb300 import workloads as wl
+    heads = sorted({h for (_, h), _ in oracle_sample(w)})
+    x = wl.make_inputs(w, device=device, heads=heads)
+    x.head_index = {h: i for i, h in enumerate(heads)}
+    return x
 
 
 def cpu_baseline(w, x, min_s=10.0, max_s=30.0, cube=None, mass=None, scores="mean"):
-    fwd_f, bwd_f = pair_flops(w.block, w.d)
-    t0 = time.perf_counter()
-    pairs, heads = 0, 0
-    for h in range(w.H):
-        pairs += oracle_head_step(w, x, 0, h, cube, mass, scores)
-        heads += 1
-        el = time.perf_counter() - t0
-        if el >= min_s or el * (heads + 1) / heads > max_s:
-            break
-    el = time.perf_counter() - t0
-    return {"value": round((fwd_f + bwd_f) * pairs / el / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(),
-            "kind": "oracle", "seconds": round(el, 2),
-            "sample": f"{heads} of {w.B * w.H} (batch, head) slices of {w.name}: predictor, top-k, transpose, "
-                      f"attention fwd+bwd in fp64 numpy ({pairs} pairs)"}
+    """The oracle on the host cores over the seeded sample, in the metric's
+    unit: effective FLOPs of the pairs it processed over its wall time.
+    Rounds repeat (cycling through the sample) until min_s has passed."""
+    xs = _Tensors()
+    for nm in ("Q", "K", "V", "dO", "Wq", "Wk", "k_per_head"):
+        setattr(xs, nm, getattr(x, nm))
+    xs.head_index = {h: h for h in range(w.H)}
+    pool = OraclePool(w, xs, cube=cube, mass=mass, scores=scores)
+    try:
+        fwd_f, bwd_f = pair_flops(w.block, w.d)
+        pairs, el = 0, 0.0
+        while True:
+            p, t = pool.round()
+            pairs, el = pairs + p, el + t
+            per = el / pool.rounds
+            if (el >= min_s and pool.rounds >= pool.max_groups) or el + per > max_s:
+                break
+        return {"value": round((fwd_f + bwd_f) * pairs / el / 1e12, 6), "unit": UNIT, "cores": pool.cores,
+                "host_cpus": os.cpu_count(), "kind": "oracle", "seconds": round(el, 2), "pairs": pairs,
+                "rounds": pool.rounds,
+                "sample": f"sampled: {pool.describe()}; {pool.rounds} rounds of one group per process"}
+    finally:
+        pool.close()
 
 
 def run_reference(args):
@@ -612,39 +840,54 @@ def run_reference(args):
     from dynamic_block_sparse_projection_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload]
     cube = tuple(int(v) for v in args.cube.split(",")) if args.cube else None
-    heads = sorted(set(range(w.H)))
-    x = wl.make_inputs(w, device="cpu")
-    fwd_f, bwd_f = pair_flops(w.block, w.d)
-    slices = [(b, h) for b in range(w.B) for h in heads]
-    for i in range(max(3, args.warmup)):
-        oracle_head_step(w, x, *slices[i % len(slices)], cube, args.mass or None, args.scores)
-    t0 = time.perf_counter()
-    pairs = 0
-    for i in range(args.steps):
-        pairs += oracle_head_step(w, x, *slices[i % len(slices)], cube, args.mass or None, args.scores)
-    el = time.perf_counter() - t0
+    # the inputs come from the seeded generators on the GPU when there is one (the values the GPU arm sees)
+    x = oracle_inputs(w, "cuda" if torch.cuda.is_available() else "cpu")
+    pool = OraclePool(w, x, cube=cube, mass=args.mass or None, scores=args.scores)
+    try:
+        fwd_f, bwd_f = pair_flops(w.block, w.d)
+        for _ in range(max(3, args.warmup)):
+            pool.round()
+        pairs, el = 0, 0.0
+        for _ in range(args.steps):
+            p, t = pool.round()
+            pairs, el = pairs + p, el + t
+        sample = f"sampled: each step one group per process; {pool.describe()}"
+        cores = pool.cores
+    finally:
+        pool.close()
     value = (fwd_f + bwd_f) * pairs / el / 1e12
-    sample = (f"each step one (batch, head) slice of {w.name} (1 of {len(slices)}): predictor, top-k, transpose, "
-              f"attention fwd+bwd in fp64 numpy on the host cores")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(1e3 * el / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "description": w.description, **({"cube": list(cube)} if cube else {}),
+        "config": {"workload": w.name, "description": w.description, "pairs": pairs,
+                   **({"cube": list(cube)} if cube else {}),
                    **({"selection": f"mass threshold tau={args.mass}, temperature 1/sqrt(d), k in [1, nb]"}
                       if args.mass else {}),
                    **({"block_scores": "tile maximum of the low-rank logits"} if args.scores == "max" else {})},
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "host_cpus": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
 
-def write_traffic(csv_path, command, workload):
-    """profiles/traffic.json: mean DRAM bytes (read + write) per launch of each
-    attention kernel in an ncu CSV, with the sha256 of the sources it was
-    built from (bench.py reports null once they change)."""
+TRAFFIC_KERNELS = {name: KERNEL_SRC[stage] for stage, name in KERNEL_OF.items()}
+
+
+def write_traffic(csv_path, command, workload, heads):
+    """Merge into profiles/traffic.json the mean DRAM bytes (read + write) per
+    launch of each attention kernel found in an ncu CSV, with the workload and
+    head count it was captured on, the pairs one launch processed, and the
+    sha256 of the sources it was built from (bench.py reports null once they
+    change, or on another workload)."""
     import csv
+
+    from dynamic_block_sparse_projection_gb300 import workloads as wl
+    w = wl.WORKLOADS[workload]
+    if heads and heads < w.H:
+        w = wl.scaled(w, name=w.name, H=heads)
+    ks = wl.head_params(w)[0]
+    pairs = w.B * w.nb * sum(ks)
     rows = list(csv.reader(open(csv_path)))
     hi = next(i for i, r in enumerate(rows) if "Kernel Name" in r and "Metric Name" in r)
     h = rows[hi]
@@ -654,30 +897,32 @@ def write_traffic(csv_path, command, workload):
     for r in rows[hi + 1:]:
         if len(r) <= max(ki, mi, vi, ui) or r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
             continue
-        name = next((k for k in KERNEL_OF.values() if k in r[ki]), None)
+        name = next((k for k in TRAFFIC_KERNELS if k in r[ki]), None)
         if name is None:
             continue
         v = float(r[vi].replace(",", "")) * scale.get(r[ui], 1.0)
         key = (name, r[idi])
         per_launch[key] = per_launch.get(key, 0.0) + v
-    out = {}
-    for stage, name in KERNEL_OF.items():
+    f = ROOT / "profiles" / "traffic.json"
+    out = json.loads(f.read_text()) if f.exists() else {}
+    for name, src in TRAFFIC_KERNELS.items():
         vals = [v for (n, _), v in per_launch.items() if n == name]
         if not vals:
             continue
         hsh = hashlib.sha256()
-        for src in (KERNEL_SRC[stage], "dynamic_block_sparse_projection_gb300/csrc/dsv_device.cuh"):
-            hsh.update((ROOT / src).read_bytes())
+        for s in (src, "dynamic_block_sparse_projection_gb300/csrc/dsv_device.cuh"):
+            hsh.update((ROOT / s).read_bytes())
         out[name] = {"dram_bytes_per_launch": round(sum(vals) / len(vals)), "launches": len(vals),
-                     "workload": workload, "source_sha256": hsh.hexdigest(), "command": command}
-    (ROOT / "profiles" / "traffic.json").write_text(json.dumps(out, indent=1) + "\n")
+                     "workload": workload, "heads": w.H, "pairs": pairs, "source_sha256": hsh.hexdigest(),
+                     "command": command}
+    f.write_text(json.dumps(out, indent=1) + "\n")
     print(json.dumps(out, indent=1))
 
 
 def main(argv=None):
     args = parse_args(argv)
     if args.traffic_from:
-        write_traffic(args.traffic_from, args.traffic_command, args.workload)
+        write_traffic(args.traffic_from, args.traffic_command, args.workload, args.heads)
         return
     if args.impl == "reference":
         run_reference(args)

@@ -31,7 +31,9 @@ EXPORTS = (
     "dsv_attn_bwd_preprocess", "dsv_attn_bwd_dkdv", "dsv_attn_bwd_dq",
     "dsv_cube_permute", "dsv_topk_mass_workspace_bytes", "dsv_topk_mass_blocks",
     "dsv_predict_max_workspace_bytes", "dsv_predict_scores_max",
+    "dsv_selftest_wait_timeout",
 )
+SELFTEST_WAIT_ID = 0xD5F0
 
 
 class Shape(ctypes.Structure):
@@ -95,6 +97,8 @@ def _load() -> ctypes.CDLL:
     lib.dsv_topk_mass_blocks.restype = ctypes.c_int
     lib.dsv_cube_permute.argtypes = [vp, vp, Shape, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.dsv_cube_permute.restype = ctypes.c_int
+    lib.dsv_selftest_wait_timeout.argtypes = [vp]
+    lib.dsv_selftest_wait_timeout.restype = ctypes.c_int
     lib.dsv_version.argtypes = []
     lib.dsv_version.restype = i32
     return lib
@@ -517,3 +521,11 @@ def clear_device_error(stream=None, device=None) -> None:
 def set_wait_limit_ns(limit_ns: int) -> None:
     _check(lib.dsv_set_wait_limit_ns(int(limit_ns)), "dsv_set_wait_limit_ns")
 
+
+
+def selftest_wait_timeout(stream=None, device=None) -> None:
+    """Enqueue the library's failure-detection self-test: a kernel whose only
+    wait can never be satisfied runs out of its time limit (set_wait_limit_ns)
+    and records DSV_ERR_TIMEOUT; read it with device_error()."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _check(lib.dsv_selftest_wait_timeout(_stream(dev, stream)), "dsv_selftest_wait_timeout")

@@ -97,6 +97,18 @@ float resolve_scale(const dsv_shape& s, float scale) {
   return (scale > 0.f && isfinite(scale)) ? scale : 1.0f / sqrtf((float)s.d);
 }
 
+// One thread waits on a barrier that nothing arrives at: phase 0 of a freshly
+// initialised barrier never completes, so the bounded wait runs out, records
+// DSV_ERR_TIMEOUT and returns.  Nothing else is in flight in this CTA.
+__global__ void selftest_wait_kernel(Ctl ctl) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  mbar_wait(&bar, 0, &abort_flag, ctl, DSV_SELFTEST_WAIT_ID);
+}
+
 }  // namespace
 }  // namespace dsv
 
@@ -136,6 +148,13 @@ dsv_status dsv_get_device_error(dsv_stream_t stream, uint32_t* info) {
   if (cudaMemcpy(&h, ctl.err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return DSV_ERR_CUDA;
   if (info) *info = h.info;
   return static_cast<dsv_status>(h.code);
+}
+
+dsv_status dsv_selftest_wait_timeout(dsv_stream_t stream) {
+  Ctl ctl;
+  if (current_ctl(&ctl) != cudaSuccess) return DSV_ERR_CUDA;
+  selftest_wait_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(ctl);
+  return from_cuda(cudaGetLastError());
 }
 
 dsv_status dsv_clear_device_error(dsv_stream_t stream) {

@@ -80,16 +80,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Lower bound of the time limit of a drain wait.  A drain wait (abort ==
+// nullptr) waits for copies or MMAs this CTA has already issued, which finish
+// without any other warp's help; a CTA must not exit, or free its TMEM, while
+// they are in flight, so a short caller limit (dsv_set_wait_limit_ns) does not
+// shorten these waits below this bound.
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
+
 // Wait for the phase with parity `parity` of `bar` to complete.  Gives up
 // (returns false) when `*abort` becomes non-zero or the per-device time
 // limit passes; in the latter case it records DSV_ERR_TIMEOUT with `where`
 // and raises `*abort` so that every other waiter in the CTA gives up too.
-// abort == nullptr: only the time limit applies (used for draining).
+// abort == nullptr: a drain wait; only the time limit applies, and it is at
+// least kDrainLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, const Ctl& ctl,
                                           unsigned int where) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  const uint64_t limit = ctl.wait_limit_ns;
+  const uint64_t limit =
+      (abort == nullptr && ctl.wait_limit_ns < kDrainLimitNs) ? kDrainLimitNs : ctl.wait_limit_ns;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0u) {

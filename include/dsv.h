@@ -280,8 +280,23 @@ dsv_status dsv_clear_device_error(dsv_stream_t stream);
 
 /* Time limit, in nanoseconds, of every wait inside the kernels on the
  * current device (default 1e9).  A wait past it records DSV_ERR_TIMEOUT and
- * the kernel returns without finishing.  0 restores the default. */
+ * the kernel returns without finishing.  0 restores the default.  The waits
+ * with which a kernel drains the copies and tensor-core products it has
+ * already issued (before it exits, or frees its tensor memory) keep a limit
+ * of at least 2 s whatever is set here: that work finishes on its own. */
 dsv_status dsv_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Failure-detection self-test (the pages have no counterpart; it checks the
+ * library's own error reporting).  Enqueues on `stream` one single-thread
+ * kernel that waits, through the same bounded barrier wait the attention
+ * kernels use, on a shared-memory barrier nothing ever arrives at.  The wait
+ * gives up after the limit set by dsv_set_wait_limit_ns, records
+ * DSV_ERR_TIMEOUT with info DSV_SELFTEST_WAIT_ID in the device error word
+ * (unless an earlier error is already recorded) and the kernel returns: no
+ * fault, and the context stays usable.  Returns DSV_ERR_CUDA if the launch
+ * fails; read the outcome with dsv_get_device_error(). */
+#define DSV_SELFTEST_WAIT_ID 0xD5F0u
+dsv_status dsv_selftest_wait_timeout(dsv_stream_t stream);
 
 /* Library version as major*10000 + minor*100 + patch. */
 int32_t dsv_version(void);

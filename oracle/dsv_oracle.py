@@ -409,6 +409,41 @@ def attn_bwd_kv_blocks(Q, K, V, dO, fwd_ptr, fwd_col, bwd_ptr, bwd_col, block: i
     return out
 
 
+def attn_bwd_kv_blocks_given_stats(Q, K, V, dO, lse, D, bwd_ptr, bwd_col, block: int, blocks,
+                                   scale: Optional[float] = None):
+    """dK, dV of the listed key blocks (b, h, j), given each query row's
+    softmax statistics: its log-sum-exp LSE_i over its whole list and
+    D_i = sum_j P_ij dP_ij.
+
+    With those two numbers the gradient of a key block needs only the tile of
+    each group g in its transposed list: P = exp(scale * Q_g K_j^T - LSE_g),
+    dP = dO_g V_j^T, dS = P * (dP - D_g), dV_j = sum_g P^T dO_g,
+    dK_j = scale * sum_g dS^T Q_g -- the same closed form as attn_bwd_masked,
+    restricted to the columns of block j.  It lets a block chosen by thousands
+    of groups be checked without redoing each group's whole softmax; lse and
+    D are [B, H, N] arrays (only the rows of the listed groups are read).
+    """
+    B, H, N, d = Q.shape
+    nb = N // block
+    tau = _scale(d, scale)
+    out = []
+    for (b, h, j) in blocks:
+        ks = slice(j * block, (j + 1) * block)
+        kj, vj = _f64(K[b, h, ks]), _f64(V[b, h, ks])
+        dk = np.zeros((block, d))
+        dv = np.zeros((block, d))
+        r = (b * H + h) * nb + j
+        for g in bwd_col[bwd_ptr[r]:bwd_ptr[r + 1]]:
+            qs = slice(int(g) * block, (int(g) + 1) * block)
+            q, do = _f64(Q[b, h, qs]), _f64(dO[b, h, qs])
+            P = np.exp(tau * (q @ kj.T) - _f64(lse[b, h, qs])[:, None])
+            dS = P * (do @ vj.T - _f64(D[b, h, qs])[:, None])
+            dv += P.T @ do
+            dk += tau * (dS.T @ q)
+        out.append((dk, dv))
+    return out
+
+
 # --------------------------------------------------------------------------
 # 3D cube query grouping ([nl] 2B, [hi] 2B: adjacent tokens in 3D space share
 # their critical KV; queries are grouped in small cubes, e.g. 2x2x2)

@@ -14,6 +14,16 @@ the fp64 oracle then checks what it can evaluate one item at a time:
             head (the least selected, the most selected with at most
             MAX_GROUPS groups, random ones) against the per-group / per-block
             oracle forms, on the GPU lists
+  long lists  in the first sampled head, dK/dV of the key blocks with long
+            transposed lists: against the per-block oracle (which redoes the
+            whole softmax of every group in the list) a block of about the
+            mean list length, the longest list within FULL_BUDGET group-blocks
+            and, on latent123k_global, the head's least-chosen amplified global
+            block; against the oracle's block form fed each row's LSE and
+            D = rowsum(dO * O) from the GPU forward (those are checked against
+            the oracle on the sampled groups) the most-selected block (3865
+            groups at long518k), the most-selected global block and a
+            90th-percentile block
 
 The oracle sees one (b, h) slice at a time, as fp32 copies of the bf16 inputs
 (exact), with the CSR rows of that slice re-based to (0, 0).
@@ -31,6 +41,7 @@ pytestmark = pytest.mark.gpu
 
 FULL = ["latent16k", "latent123k_global", "stress61k", "long518k"]
 MAX_GROUPS = 48
+FULL_BUDGET = 45000       # groups x their list lengths the per-block oracle may redo for one block
 
 
 @pytest.fixture(scope="module")
@@ -147,6 +158,47 @@ def test_full_size_sampled_parity(dsv, name):
         dKs = dK[b, h].double().sum(dim=0)
         assert torch.all(dKs.abs() <= 2e-2 * dK[b, h].double().abs().sum(dim=0) + 1e-3)
         assert rel_l2(dV[b, h].double().sum(dim=0).cpu().numpy(), x.dO[b, h].double().sum(dim=0).cpu().numpy()) <= 1e-2
+
+    # long transposed lists, first sampled head
+    b, h = heads[0]
+    bh = b * w.H + h
+    hp, hc = _head_csr(fpn, fcn, bh, G)
+    gp, gc = _head_csr(bpn, bcn, bh, G)
+    lens = np.diff(gp)
+    row_len = np.diff(hp)
+    cost = np.array([int(row_len[gc[gp[j]:gp[j + 1]]].sum()) for j in range(G)])   # group-blocks redone per block
+    full_blocks = {"mean-length": int(np.argmin(np.abs(lens - lens.mean()) + 1e9 * (cost > FULL_BUDGET)))}
+    within = np.nonzero(cost <= FULL_BUDGET)[0]
+    full_blocks["longest within budget"] = int(within[np.argmax(lens[within])])
+    stat_blocks = {"most-selected": int(np.argmax(lens)),
+                   "90th percentile": int(np.argmin(np.abs(lens - np.percentile(lens, 90))))}
+    if x.global_blocks and x.global_blocks[h]:
+        gl = sorted(x.global_blocks[h], key=lambda j: lens[j])
+        if cost[gl[0]] <= FULL_BUDGET:
+            full_blocks["global, least chosen"] = gl[0]
+        stat_blocks["global, most chosen"] = gl[-1]
+    Qh, Kh, Vh, dOh = (_f32(t[b, h]) for t in (x.Q, x.K, x.V, x.dO))
+    lse_h = lse[b, h].double().cpu().numpy()[None, None]
+    D_h = (O[b, h].double() * x.dO[b, h].double()).sum(dim=-1).cpu().numpy()[None, None]
+    for form, chosen in (("per-block oracle", full_blocks), ("block form given GPU LSE and D", stat_blocks)):
+        js = list(chosen.values())
+        if form == "per-block oracle":
+            refs = oracle.attn_bwd_kv_blocks(Qh, Kh, Vh, dOh, hp, hc, gp, gc, w.block, [(0, 0, j) for j in js])
+        else:
+            refs = oracle.attn_bwd_kv_blocks_given_stats(Qh, Kh, Vh, dOh, lse_h, D_h, gp, gc, w.block,
+                                                         [(0, 0, j) for j in js])
+        for (what, j), (dk_ref, dv_ref) in zip(chosen.items(), refs):
+            sl = slice(j * w.block, (j + 1) * w.block)
+            ek = rel_l2(dK[b, h, sl].double().cpu().numpy(), dk_ref)
+            ev = rel_l2(dV[b, h, sl].double().cpu().numpy(), dv_ref)
+            print(f"{name} head {(b, h)} block {j} ({what}, {int(lens[j])} groups, {form}): "
+                  f"dK rel-L2 {ek:.4f}, dV rel-L2 {ev:.4f}")
+            assert ek <= GRAD_REL_L2 and ev <= GRAD_REL_L2, (name, what, j, ek, ev)
+
+    # O max-abs: raw, and beyond the half-ulp rounding of the bf16 output
+    raw = max(float(np.max(np.abs(a - r))) for a, r in checked["O"])
+    beyond = max(max_abs_beyond_rounding(a, r) for a, r in checked["O"])
+    print(f"{name} O max-abs: raw {raw:.4f}, beyond bf16 rounding {beyond:.4f}")
 
     # rel-L2 over all checked elements of the workload (the gate's definition)
     for nm, bar in (("O", O_REL_L2), ("dQ", GRAD_REL_L2), ("dK", GRAD_REL_L2), ("dV", GRAD_REL_L2)):

@@ -314,3 +314,42 @@ def test_bwd_invariants_and_group_forms(rng):
     rows = [(0, 1, 3), (1, 0, 0)]
     for (b, h, g), dq in zip(rows, oracle.attn_bwd_dq_rows(Q, K, V, dO, ptr, col, blk, rows)):
         assert np.allclose(dq, dQ[b, h, g * blk:(g + 1) * blk], atol=1e-12)
+
+
+def test_bwd_kv_blocks_given_stats_equals_closed_form(rng):
+    """The block form fed each row's LSE and D gives the closed-form dK/dV
+    of attn_bwd_masked (itself pinned to torch autograd and finite
+    differences); LSE and D are taken from their definitions over the
+    masked rows, not from the GPU."""
+    B, H, N, d, blk = 2, 2, 96, 8, 8
+    G = N // blk
+    Q, K, V = _rand_qkv(rng, B, H, N, d, scale=2.0)
+    dO = rng.standard_normal((B, H, N, d))
+    ptr, col = _random_lists(rng, B, H, G, G, [3, 7])
+    mask = oracle.block_mask(ptr, col, B, H, G, G)
+    O, lse = oracle.attn_fwd_masked(Q, K, V, mask, blk)
+    _, dK, dV = oracle.attn_bwd_masked(Q, K, V, dO, mask, blk)
+    # D_i = sum_j P_ij dP_ij over the masked row, written out from P and dP
+    tau = 1.0 / math.sqrt(d)
+    D = np.empty((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            tok = np.repeat(np.repeat(mask[b, h], blk, axis=0), blk, axis=1)
+            P = np.where(tok, np.exp(tau * Q[b, h] @ K[b, h].T - lse[b, h][:, None]), 0.0)
+            D[b, h] = (P * (dO[b, h] @ V[b, h].T)).sum(axis=1)
+    assert np.allclose(D, (dO * O).sum(axis=3), atol=1e-12)     # the rowsum(dO * O) identity
+    bptr, bcol = oracle.transpose_lists(ptr, col, B, H, G, G)
+    blocks = [(b, h, j) for b in range(B) for h in range(H) for j in range(G)]
+    got = oracle.attn_bwd_kv_blocks_given_stats(Q, K, V, dO, lse, D, bptr, bcol, blk, blocks)
+    for (b, h, j), (dk, dv) in zip(blocks, got):
+        sl = slice(j * blk, (j + 1) * blk)
+        assert np.max(np.abs(dk - dK[b, h, sl])) <= 1e-12 * max(1.0, np.abs(dK).max())
+        assert np.max(np.abs(dv - dV[b, h, sl])) <= 1e-12 * max(1.0, np.abs(dV).max())
+    # each statistic matters: a shifted LSE or a dropped D moves the result
+    bad_l = oracle.attn_bwd_kv_blocks_given_stats(Q, K, V, dO, lse + 0.1, D, bptr, bcol, blk, blocks[:4])
+    bad_d = oracle.attn_bwd_kv_blocks_given_stats(Q, K, V, dO, lse, 0 * D, bptr, bcol, blk, blocks[:4])
+    for (b, h, j), (dk, dv), (dk2, _) in zip(blocks[:4], bad_l, bad_d):
+        sl = slice(j * blk, (j + 1) * blk)
+        if np.abs(dV[b, h, sl]).max() > 0:
+            assert np.max(np.abs(dv - dV[b, h, sl])) > 1e-3
+            assert np.max(np.abs(dk2 - dK[b, h, sl])) > 1e-3

@@ -57,6 +57,12 @@ def test_noalloc_matches_allocating_topk_twice(dsv, name):
         assert dsv.device_error()[0] == 0
         for got, want in zip(outs, ref):
             assert torch.equal(got, want)
+    # the Python wrapper (its room and dtype checks, then the same entry point)
+    outs = tuple(torch.full_like(t, -1) for t in ref)
+    dsv.topk_blocks_noalloc(S, x.k_per_head, w.block, w.N, w.d, outs=outs)
+    torch.cuda.synchronize()
+    for got, want in zip(outs, ref):
+        assert torch.equal(got, want)
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch(dsv):
