@@ -61,6 +61,9 @@ def parse_args(argv=None):
                         "(dsv_predict_scores_max) of each group x key-block tile of low-rank logits")
     p.add_argument("--cube", default="", metavar="CT,CY,CX",
                    help="regroup tokens into ct x cy x cx cubes of the latent grid inside the step")
+    p.add_argument("--predict", choices=["fused", "two-call"], default="fused",
+                   help="fused: dsv_predict_topk_blocks (scores stay on chip); two-call: dsv_predict_scores "
+                        "then dsv_topk_blocks (the score matrix goes through HBM)")
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--traffic-from", metavar="CSV",
@@ -174,9 +177,11 @@ class HotPath:
     its inverse on O, dQ, dK, dV after it), so that query groups and key
     blocks are cubes; O and the gradients then come out in raster order."""
 
-    def __init__(self, dsv, x, w, k_per_head, cube=None, mass=None, scores="mean"):
+    def __init__(self, dsv, x, w, k_per_head, cube=None, mass=None, scores="mean", fused=False):
         import torch
         self.dsv, self.x, self.w = dsv, x, w
+        # the fused predictor + top-k serves the mean block scores with a fixed k per head
+        self.fused = bool(fused) and not mass and scores == "mean"
         self.k = list(k_per_head)
         self.cube = tuple(cube) if cube else None
         self.mass = mass                 # tau of the mass-threshold selection, or None for top-k
@@ -186,7 +191,7 @@ class HotPath:
         B, H, N, d, G = w.B, w.H, w.N, w.d, w.nb
         # the mass selection's list sizes are known only on the device: room for every block
         self.nnz = B * H * G * G if mass else dsv.nnz_of(B, G, self.k)
-        self.S = torch.empty(B, H, G, G, dtype=torch.float32, device=dev)
+        self.S = None if self.fused else torch.empty(B, H, G, G, dtype=torch.float32, device=dev)
         self.lists = (torch.empty(B * H * G + 1, dtype=torch.int32, device=dev),
                       torch.empty(self.nnz, dtype=torch.int32, device=dev),
                       torch.empty(B * H * G + 1, dtype=torch.int32, device=dev),
@@ -195,10 +200,15 @@ class HotPath:
         self.lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
         self.grads = (torch.empty_like(x.Q), torch.empty_like(x.K), torch.empty_like(x.V))
         u8 = torch.uint8
-        ws_bytes = dsv.predict_max_workspace_bytes if scores == "max" else dsv.predict_workspace_bytes
-        self.ws_p = torch.empty(max(1, ws_bytes(B, H, N, d, w.block, w.r)), dtype=u8, device=dev)
-        self.ws_t = torch.empty(max(1, (dsv.topk_mass_workspace_bytes if mass else dsv.topk_workspace_bytes)(
-            B, H, N, d, w.block)), dtype=u8, device=dev)
+        if self.fused:
+            self.ws_p = torch.empty(max(1, dsv.predict_topk_workspace_bytes(B, H, N, d, w.block, w.r)), dtype=u8,
+                                    device=dev)
+            self.ws_t = None
+        else:
+            ws_bytes = dsv.predict_max_workspace_bytes if scores == "max" else dsv.predict_workspace_bytes
+            self.ws_p = torch.empty(max(1, ws_bytes(B, H, N, d, w.block, w.r)), dtype=u8, device=dev)
+            self.ws_t = torch.empty(max(1, (dsv.topk_mass_workspace_bytes if mass else dsv.topk_workspace_bytes)(
+                B, H, N, d, w.block)), dtype=u8, device=dev)
         self.ws_b = torch.empty(max(1, dsv.attn_bwd_workspace_bytes(B, H, N, d, w.block)), dtype=u8, device=dev)
         if self.cube:
             # the path's inputs in cube order, and O / gradients back in raster order
@@ -209,7 +219,8 @@ class HotPath:
 
     @property
     def stages(self):
-        return (("cube_in",) if self.cube else ()) + STAGES + (("cube_out",) if self.cube else ())
+        core = FUSED_STAGES if self.fused else STAGES
+        return (("cube_in",) if self.cube else ()) + core + (("cube_out",) if self.cube else ())
 
     def run(self, ev=None):
         """The four public calls (six with cube order).  With ev (one CUDA
@@ -230,10 +241,16 @@ class HotPath:
                 d.cube_permute(src, self.grid, self.cube, out=dst)
             mark()
             x = self.xc
-        predict = d.predict_scores_max if self.scores == "max" else d.predict_scores
-        predict(x.Q, x.K, x.Wq, x.Wk, w.block, out=self.S, workspace=self.ws_p)
-        mark()
-        if self.mass:
+        if self.fused:
+            fp, fc, bp, bc = d.predict_topk_blocks(x.Q, x.K, x.Wq, x.Wk, self.k, w.block, outs=self.lists,
+                                                   workspace=self.ws_p)
+        else:
+            predict = d.predict_scores_max if self.scores == "max" else d.predict_scores
+            predict(x.Q, x.K, x.Wq, x.Wk, w.block, out=self.S, workspace=self.ws_p)
+            mark()
+        if self.fused:
+            pass
+        elif self.mass:
             fp, fc, bp, bc = d.topk_mass_blocks(self.S, self.mass, w.block, w.N, w.d, outs=self.lists,
                                                 workspace=self.ws_t, trim=False)
         else:
@@ -271,9 +288,10 @@ class HotPath:
                           workspace=self.ws_b)
 
 
-KERNELS_PER_STEP = {"predict": 2, "topk": 4, "fwd": 1, "bwd_pre": 1, "bwd_kv": 2, "bwd_q": 1, "cube_in": 4,
-                    "cube_out": 4}
+KERNELS_PER_STEP = {"predict": 2, "topk": 4, "predict_topk": 6, "fwd": 1, "bwd_pre": 1, "bwd_kv": 2, "bwd_q": 1,
+                    "cube_in": 4, "cube_out": 4}
 STAGES = ("predict", "topk", "fwd", "bwd_pre", "bwd_kv", "bwd_q")
+FUSED_STAGES = ("predict_topk", "fwd", "bwd_pre", "bwd_kv", "bwd_q")
 
 
 def profile_traffic(kernel: str, source_files, w, pairs):
@@ -320,7 +338,8 @@ def run_ours(args):
         w = wl.scaled(w, name=w.name, H=args.heads)
     x = wl.make_inputs(w, device=dev)
     cube = tuple(int(v) for v in args.cube.split(",")) if args.cube else None
-    hp = HotPath(dsv, x, w, x.k_per_head, cube=cube, mass=args.mass or None, scores=args.scores)
+    hp = HotPath(dsv, x, w, x.k_per_head, cube=cube, mass=args.mass or None, scores=args.scores,
+                 fused=args.predict == "fused")
     fwd_f, bwd_f = pair_flops(w.block, w.d)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -367,11 +386,10 @@ def run_ours(args):
     # dense run of the same kernels (k = nb) for the speedup
     dense = None
     if not args.no_dense:
-        dense = time_dense(dsv, x, w, hp, flush, attn_ms=attn_ms,
-                           pre_ms=per_call["predict"] + per_call["topk"])
+        dense = time_dense(dsv, x, w, hp, flush, attn_ms=attn_ms, pre_ms=pre_ms(per_call))
 
-    # roofline of the dominant kernel (the predictor and the top-k are whole calls of 2 and 4 launches)
-    dom = max(STAGES, key=lambda k: per_call[k])
+    # roofline of the dominant kernel (the predictor and the top-k are whole calls of several launches)
+    dom = max(hp.stages, key=lambda k: per_call[k])
     roofline = roofline_entry(dom, per_call, w, hp, peaks, peak_src)
     bwd_eff = step_flops * bwd_f / (fwd_f + bwd_f) / (per_call["bwd"] * 1e-3) / 1e12
 
@@ -384,6 +402,8 @@ def run_ours(args):
                    "block": w.block, "r": w.r,
                    "k_per_head": None if args.mass else sorted(set(x.k_per_head)), "pairs": hp.nnz,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "predictor_topk": ("fused (dsv_predict_topk_blocks: scores on chip)" if hp.fused else
+                                      "two calls (dsv_predict_scores, dsv_topk_blocks)"),
                    **({"heads_kept": w.H, "reduced": "first heads only (profiler case)"} if args.heads else {}),
                    **({"cube": list(cube), "token_order": "3D cubes (dsv_cube_permute in and out, timed)"}
                       if cube else {}),
@@ -427,7 +447,8 @@ KERNEL_SRC = {"fwd": "dynamic_block_sparse_projection_gb300/csrc/attn_fwd.cu",
               "bwd_q": "dynamic_block_sparse_projection_gb300/csrc/attn_bwd.cu",
               "bwd_pre": "dynamic_block_sparse_projection_gb300/csrc/attn_bwd.cu",
               "predict": "dynamic_block_sparse_projection_gb300/csrc/predict.cu",
-              "topk": "dynamic_block_sparse_projection_gb300/csrc/topk.cu"}
+              "topk": "dynamic_block_sparse_projection_gb300/csrc/topk.cu",
+              "predict_topk": "dynamic_block_sparse_projection_gb300/csrc/predict_topk.cu"}
 
 
 def roofline_entry(dom, per_call, w, hp, peaks, peak_src):
@@ -458,6 +479,9 @@ def roofline_entry(dom, per_call, w, hp, peaks, peak_src):
     elif dom == "predict":
         nbytes = 2 * B * H * N * d * 2 + B * H * G * G * 4
         kname = "dsv_predict_scores"
+    elif dom == "predict_topk":
+        nbytes = 2 * B * H * N * d * 2 + 8 * hp.nnz + 8 * (B * H * G + 1)
+        kname = "dsv_predict_topk_blocks"
     else:
         nbytes = B * H * G * G * 4 + 2 * hp.nnz * 4 + 2 * (B * H * G + 1) * 4
         kname = "dsv_topk_blocks"
@@ -531,11 +555,26 @@ def time_dense(dsv, x, w, hp, flush, attn_ms, pre_ms, iters=2):
                        f"independent") + "; same kernels with k = nb, L2 flushed, best of %d" % iters}
 
 
+def pre_ms(per_call):
+    """Time of the predictor and the top-k (one fused call or two calls)."""
+    return per_call["predict_topk"] if "predict_topk" in per_call else per_call["predict"] + per_call["topk"]
+
+
 def hbm_fractions(w, hp, per_call, peaks):
-    """Algorithmic bytes and HBM fraction of the predictor and of the top-k."""
+    """Algorithmic bytes and HBM fraction of the predictor and of the top-k.
+    The fused call's bytes are the Q and K reads and the list writes (its
+    score matrix never reaches HBM); the two-call path also writes and reads
+    the score matrix."""
     B, H, N, d, G = w.B, w.H, w.N, w.d, w.nb
+    lists = 8 * hp.nnz + 4 * (B * H * G + 1) + 4 * (B * H * G + 1)
+    if hp.fused:
+        fused = 2 * B * H * N * d * 2 + lists
+        gbs = fused / (per_call["predict_topk"] * 1e-3) / 1e9
+        return {"predict+topk": {"bytes": fused, "ms": round(per_call["predict_topk"], 4), "gbs": round(gbs, 1),
+                                 "frac": round(gbs / peaks["hbm_gbs"], 4), "frac_of_8tbs": round(gbs / 8000.0, 4)},
+                "bytes_rule": "fused call: read Q and K + write both column arrays and both row-pointer arrays"}
     pred = 2 * B * H * N * d * 2 + 4 * B * H * G * G
-    topk = 4 * B * H * G * G + 8 * hp.nnz + 4 * (B * H * G + 1) + 4 * (B * H * G + 1)
+    topk = 4 * B * H * G * G + lists
     out = {}
     for nm, nbytes, ms in (("predict", pred, per_call["predict"]), ("topk", topk, per_call["topk"]),
                            ("predict+topk", pred + topk, per_call["predict"] + per_call["topk"])):
@@ -567,7 +606,7 @@ def time_e2e(dsv, x, w, hp, args, flops_per_step):
         dev_in = [torch.empty_like(t) for t in (x.Q, x.K, x.V, x.dO, x.Wq, x.Wk)]
         xd = X()
         xd.Q, xd.K, xd.V, xd.dO, xd.Wq, xd.Wk = dev_in
-        hp2 = HotPath(dsv, xd, w, hp.k, cube=hp.cube, mass=hp.mass, scores=hp.scores)
+        hp2 = HotPath(dsv, xd, w, hp.k, cube=hp.cube, mass=hp.mass, scores=hp.scores, fused=hp.fused)
         if host_out is None:
             host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in hp2.results()]
         sets.append((dev_in, hp2, host_out))

@@ -32,6 +32,7 @@ EXPORTS = (
     "dsv_cube_permute", "dsv_topk_mass_workspace_bytes", "dsv_topk_mass_blocks",
     "dsv_predict_max_workspace_bytes", "dsv_predict_scores_max",
     "dsv_selftest_wait_timeout",
+    "dsv_predict_topk_workspace_bytes", "dsv_predict_topk_blocks",
 )
 SELFTEST_WAIT_ID = 0xD5F0
 
@@ -97,6 +98,11 @@ def _load() -> ctypes.CDLL:
     lib.dsv_topk_mass_blocks.restype = ctypes.c_int
     lib.dsv_cube_permute.argtypes = [vp, vp, Shape, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.dsv_cube_permute.restype = ctypes.c_int
+    lib.dsv_predict_topk_workspace_bytes.argtypes = [Shape]
+    lib.dsv_predict_topk_workspace_bytes.restype = sz
+    lib.dsv_predict_topk_blocks.argtypes = [vp, vp, vp, vp, Shape, ctypes.POINTER(i32), vp, vp, vp, vp, vp, vp, sz,
+                                            vp]
+    lib.dsv_predict_topk_blocks.restype = ctypes.c_int
     lib.dsv_selftest_wait_timeout.argtypes = [vp]
     lib.dsv_selftest_wait_timeout.restype = ctypes.c_int
     lib.dsv_version.argtypes = []
@@ -264,6 +270,55 @@ def topk_blocks(scores, k_per_head: Sequence[int], block: int, N: int, d: int = 
     with torch.cuda.device(dev):
         _check(lib.dsv_topk_blocks(_ptr(scores), s, karr, *[_ptr(t) for t in outs], _ptr(ws), nbytes,
                                    _stream(dev, stream)), "dsv_topk_blocks")
+    fp, fc, bp, bc = outs
+    return fp, fc[:nnz], bp, bc[:nnz]
+
+
+def predict_topk_workspace_bytes(B: int, H: int, N: int, d: int, block: int, r: int) -> int:
+    return int(lib.dsv_predict_topk_workspace_bytes(Shape(B, H, N, d, block, r)))
+
+
+def predict_topk_blocks(Q, K, Wq, Wk, k_per_head: Sequence[int], block: int, *, outs=None, scores=None,
+                        workspace=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(fwd_ptr, fwd_col, bwd_ptr, bwd_col) int32 CSR lists of the fused
+    predictor + top-k (the score matrix stays on chip); see
+    dsv_predict_topk_blocks.  `scores`, if given (fp32 [B, H, G, G]),
+    receives the scores the selection used."""
+    B, H, N, d = _dims(Q, "Q", 4)
+    _shape(K, "K", (B, H, N, d))
+    r = _dims(Wq, "Wq", 3)[2]
+    _shape(Wq, "Wq", (H, d, r))
+    _shape(Wk, "Wk", (H, d, r))
+    if len(k_per_head) != H:
+        raise ValueError(f"k_per_head has {len(k_per_head)} entries, expected one per head ({H})")
+    G = _groups(N, block)
+    nnz = nnz_of(B, G, k_per_head)
+    if outs is not None:
+        _csr_room(outs, B * H * G + 1, nnz, B * H * G + 1, nnz)
+    if scores is not None:
+        _shape(scores, "scores", (B, H, G, G))
+    _need(Q, "Q", torch.bfloat16)
+    dev = Q.device
+    _need(K, "K", torch.bfloat16, dev)
+    _need(Wq, "Wq", torch.float32, dev)
+    _need(Wk, "Wk", torch.float32, dev)
+    if scores is not None:
+        _need(scores, "scores", torch.float32, dev)
+    if outs is None:
+        outs = (torch.empty(B * H * G + 1, dtype=torch.int32, device=dev),
+                torch.empty(max(nnz, 1), dtype=torch.int32, device=dev),
+                torch.empty(B * H * G + 1, dtype=torch.int32, device=dev),
+                torch.empty(max(nnz, 1), dtype=torch.int32, device=dev))
+    for name, t in zip(("fwd_ptr", "fwd_col", "bwd_ptr", "bwd_col"), outs):
+        _need(t, name, torch.int32, dev)
+    s = Shape(B, H, N, d, block, r)
+    karr = (ctypes.c_int32 * max(H, 1))(*[int(k) for k in k_per_head])
+    nbytes = lib.dsv_predict_topk_workspace_bytes(s)
+    ws = _workspace(nbytes, dev, workspace)
+    with torch.cuda.device(dev):
+        _check(lib.dsv_predict_topk_blocks(_ptr(Q), _ptr(K), _ptr(Wq), _ptr(Wk), s, karr, *[_ptr(t) for t in outs],
+                                           _ptr(scores), _ptr(ws), nbytes, _stream(dev, stream)),
+               "dsv_predict_topk_blocks")
     fp, fc, bp, bc = outs
     return fp, fc[:nnz], bp, bc[:nnz]
 

@@ -20,7 +20,7 @@ INCLUDE = ROOT / "include"
 OUT = PKG / "_build"
 LIB = OUT / "libdsv.so"
 SOURCES = ["dsv_api.cu", "predict.cu", "topk.cu", "attn_fwd.cu", "attn_bwd.cu", "topk_noalloc.cu", "cube.cu",
-           "predict_max.cu"]
+           "predict_max.cu", "predict_topk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -75,6 +75,22 @@ cudaError_t make_map(CUtensorMap* map, const void* base, long long rows, int d, 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 2D map over a [rows, 32] fp32 array, box = [32 columns, box_rows], 128-byte swizzle
+// (the tf32 operand tiles of the fused predictor + top-k).
+cudaError_t make_map_f32x32(CUtensorMap* map, const void* base, long long rows, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  cudaError_t e = get_encode(&enc);
+  if (e != cudaSuccess) return e;
+  cuuint64_t dims[2] = {32u, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {32u * 4u};
+  cuuint32_t box[2] = {32u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool al256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 
@@ -237,6 +253,71 @@ dsv_status dsv_topk_blocks(const float* scores, dsv_shape s, const int32_t* k_pe
   const long long nnz = (long long)s.B * nb * hk.kpre[s.H];
   if (nnz > INT32_MAX) return DSV_ERR_UNSUPPORTED;
   return from_cuda(launch_topk(scores, s, hk, nnz, fwd_ptr, fwd_col, bwd_ptr, bwd_col, workspace, st));
+}
+
+size_t dsv_predict_topk_workspace_bytes(dsv_shape s) {
+  if (check_shape(s, true) != DSV_OK || empty(s) || s.r > 32) return 0;
+  return predict_ws_bytes(s) + split_tf32_bytes(s) + topk_ws_bytes(s);
+}
+
+dsv_status dsv_predict_topk_blocks(const void* Q, const void* K, const float* Wq, const float* Wk, dsv_shape s,
+                                   const int32_t* k_per_head, int32_t* fwd_ptr, int32_t* fwd_col, int32_t* bwd_ptr,
+                                   int32_t* bwd_col, float* scores, void* workspace, size_t workspace_bytes,
+                                   dsv_stream_t stream) {
+  dsv_status v = check_shape(s, true);
+  if (v != DSV_OK) return v;
+  if (s.r > 32) return DSV_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!fwd_ptr || !bwd_ptr) return DSV_ERR_INVALID_ARG;
+  if (empty(s)) {
+    cudaError_t e = cudaMemsetAsync(fwd_ptr, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(bwd_ptr, 0, sizeof(int32_t), st);
+    return from_cuda(e);
+  }
+  const int nb = s.N / s.block;
+  if (nb > kMaxBlocksPerRow) return DSV_ERR_UNSUPPORTED;
+  if (!Q || !K || !Wq || !Wk || !k_per_head || !fwd_col || !bwd_col || !workspace) return DSV_ERR_INVALID_ARG;
+  if (!al16(Q) || !al16(K) || !al16(Wq) || !al16(Wk) || !al16(fwd_ptr) || !al16(fwd_col) || !al16(bwd_ptr) ||
+      !al16(bwd_col) || !al256(workspace) || (scores && !al16(scores)))
+    return DSV_ERR_INVALID_ARG;
+  if (workspace_bytes < predict_ws_bytes(s) + split_tf32_bytes(s) + topk_ws_bytes(s)) return DSV_ERR_INVALID_ARG;
+  HeadK hk;
+  hk.kpre[0] = 0;
+  for (int h = 0; h < s.H; ++h) {
+    const int k = k_per_head[h];
+    if (k < 1 || k > nb) return DSV_ERR_INVALID_ARG;
+    hk.k[h] = k;
+    hk.kpre[h + 1] = hk.kpre[h] + k;
+  }
+  for (int h = s.H; h < kMaxHeads; ++h) {
+    hk.k[h] = 0;
+    hk.kpre[h + 1] = hk.kpre[h];
+  }
+  const long long nnz = (long long)s.B * nb * hk.kpre[s.H];
+  if (nnz > INT32_MAX) return DSV_ERR_UNSUPPORTED;
+  Ctl ctl;
+  if (current_ctl(&ctl) != cudaSuccess) return DSV_ERR_CUDA;
+  // workspace: pooled vectors | tf32 parts | top-k bitmask and transpose counts
+  char* w = static_cast<char*>(workspace);
+  const size_t rows = (size_t)s.B * s.H * nb;
+  float* qp = reinterpret_cast<float*>(w);
+  float* kp = reinterpret_cast<float*>(w + align256(rows * (size_t)s.r * sizeof(float)));
+  float* split = reinterpret_cast<float*>(w + predict_ws_bytes(s));
+  void* tws = w + predict_ws_bytes(s) + split_tf32_bytes(s);
+  const size_t part = align256(rows * 32 * sizeof(float));
+  PredictTopkMaps maps;
+  const char* sp = reinterpret_cast<const char*>(split);
+  if (make_map_f32x32(&maps.qh, sp, (long long)rows, 128) != cudaSuccess ||
+      make_map_f32x32(&maps.ql, sp + part, (long long)rows, 128) != cudaSuccess ||
+      make_map_f32x32(&maps.kh, sp + 2 * part, (long long)rows, 128) != cudaSuccess ||
+      make_map_f32x32(&maps.kl, sp + 3 * part, (long long)rows, 128) != cudaSuccess)
+    return DSV_ERR_CUDA;
+  cudaError_t e = launch_pool_project(Q, K, Wq, Wk, s, qp, kp, st);
+  if (e == cudaSuccess) e = launch_split_tf32(qp, kp, s, split, st);
+  if (e == cudaSuccess)
+    e = launch_score_select(maps, s, hk, nnz, fwd_ptr, fwd_col, static_cast<uint32_t*>(tws), scores, ctl, st);
+  if (e == cudaSuccess) e = launch_topk_transpose(s, hk, nnz, bwd_ptr, bwd_col, tws, st);
+  return from_cuda(e);
 }
 
 size_t dsv_topk_mass_workspace_bytes(dsv_shape s) {

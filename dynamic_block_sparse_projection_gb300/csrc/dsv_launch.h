@@ -32,6 +32,28 @@ size_t predict_max_ws_bytes(const dsv_shape& s);
 cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk, int64_t nnz, int32_t* fwd_ptr,
                         int32_t* fwd_col, int32_t* bwd_ptr, int32_t* bwd_col, void* ws, cudaStream_t st);
 size_t topk_ws_bytes(const dsv_shape& s);
+// The transposed lists only, from a selection bitmask already in `ws` (the
+// layout launch_topk's select kernel writes: word (b, h, w, g) at
+// ((b*H + h) * words + w) * G + g).
+cudaError_t launch_topk_transpose(const dsv_shape& s, const HeadK& hk, int64_t nnz, int32_t* bwd_ptr,
+                                  int32_t* bwd_col, void* ws, cudaStream_t st);
+// Pooled rank-r projections only (qp, kp: [B*H*G, r] fp32), the first kernel of launch_predict.
+cudaError_t launch_pool_project(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s,
+                                float* qp, float* kp, cudaStream_t st);
+// Fused predictor + top-k: tf32 operand splits of the pooled vectors, then one
+// kernel that scores every (group, key block) pair on the tensor cores and
+// selects each group's top k without writing the score matrix (unless
+// `scores` is given); the forward lists and the selection bitmask (in the
+// top-k workspace layout) come out of it.  `split` holds 4 arrays of
+// [B*H*G, 32] fp32 (q hi, q lo, k hi, k lo), each 256-byte aligned.
+struct PredictTopkMaps {
+  CUtensorMap qh, ql, kh, kl;
+};
+cudaError_t launch_split_tf32(const float* qp, const float* kp, const dsv_shape& s, float* split, cudaStream_t st);
+cudaError_t launch_score_select(const PredictTopkMaps& maps, const dsv_shape& s, const HeadK& hk, int64_t nnz,
+                                int32_t* fwd_ptr, int32_t* fwd_col, uint32_t* mask, float* scores, const Ctl& ctl,
+                                cudaStream_t st);
+size_t split_tf32_bytes(const dsv_shape& s);
 // Mass-threshold selection: per row the smallest top set carrying >= tau of
 // the predicted softmax mass (temperature * scores), clamped to [kmin, kmax].
 cudaError_t launch_topk_mass(const float* scores, const dsv_shape& s, float tau, float temperature, int kmin,

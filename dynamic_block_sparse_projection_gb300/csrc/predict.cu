@@ -15,6 +15,8 @@
 // pooled vectors with r-deep fp32 FMA register tiles (8 x 8 per thread).
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "dsv_launch.h"
 
 namespace dsv {
@@ -232,6 +234,23 @@ cudaError_t launch_predict_r(const void* Q, const void* K, const float* Wq, cons
 }
 
 }  // namespace
+
+cudaError_t launch_pool_project(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s,
+                                float* qp, float* kp, cudaStream_t st) {
+  auto pool = [&](auto rtag) -> cudaError_t {
+    constexpr int R = decltype(rtag)::value;
+    if (s.d == 128 && s.block == 128) return launch_pool<128, 128, R>(Q, K, Wq, Wk, s, qp, kp, st);
+    if (s.d == 128 && s.block == 64) return launch_pool<128, 64, R>(Q, K, Wq, Wk, s, qp, kp, st);
+    if (s.d == 64 && s.block == 128) return launch_pool<64, 128, R>(Q, K, Wq, Wk, s, qp, kp, st);
+    return launch_pool<64, 64, R>(Q, K, Wq, Wk, s, qp, kp, st);
+  };
+  switch (s.r) {
+    case 8: return pool(std::integral_constant<int, 8>{});
+    case 16: return pool(std::integral_constant<int, 16>{});
+    case 24: return pool(std::integral_constant<int, 24>{});
+    default: return pool(std::integral_constant<int, 32>{});
+  }
+}
 
 size_t predict_ws_bytes(const dsv_shape& s) {
   const size_t rows = (size_t)s.B * s.H * (size_t)(s.N / s.block);

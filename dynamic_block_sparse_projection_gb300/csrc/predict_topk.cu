@@ -1,0 +1,588 @@
+// predict_topk.cu — the block-score predictor fused with the per-group top-k.
+//
+// DSV page [nl], "Technische samenvatting" 2B: the critical KV of a query
+// group are estimated and selected in one custom kernel, so the memory of the
+// estimate stays proportional to the selection instead of the full group x
+// block score matrix ([hi] 2B says the same).  Here the pooled rank-r vectors
+// (qbar_g, kbar_j, as in predict.cu) go through:
+//
+//   split_tf32_kernel   every pooled vector x becomes x_hi = tf32(x) and
+//                       x_lo = tf32(x - x_hi), zero-padded to 32 rank columns.
+//   score_select_kernel one CTA per (b, h) and 128 consecutive groups.  The
+//                       score tile S[g, j] = qbar_g . kbar_j of 128 groups x
+//                       128 key blocks is q_hi k_hi + q_hi k_lo + q_lo k_hi:
+//                       three tcgen05 kind::tf32 products accumulated in fp32
+//                       in tensor memory (the dropped q_lo k_lo term and the
+//                       tf32 rounding of the parts leave ~2^-21 of each
+//                       product).  The tiles are recomputed in every pass
+//                       (the tensor pipe is otherwise idle), so the scores
+//                       never leave the SM.  Thread r of the four selection
+//                       warps owns group row r (its tensor-memory lane) and
+//                       selects that row's top k alone, with no CTA-wide
+//                       reductions:
+//     pass 0  mean and variance of the row;
+//     pass 1  a 128-bin histogram of the row over mean + (z_k -+ 1) sd, z_k
+//             the normal quantile of 1 - k/nb (bins clamp at both ends, so the
+//             range only decides how many scores share a bin, never which are
+//             kept); the bin b* holding the k-th largest score follows;
+//     pass 2  the selection bitmask: scores in bins above b* are kept, the
+//             few in b* (at most kCand) are collected and ranked exactly by
+//             (score desc, index asc) unless all of them are kept.
+//   A row whose bin b* holds more than kCand scores and is only partly kept
+//   (for example a row of equal scores) is finished by an exact radix select
+//   on order-preserving 32-bit keys (five digit passes and an emit pass, run
+//   by the CTA only when one of its rows needs it).  Each thread then writes
+//   its row's ascending list; the bitmask, in the layout of the two-call
+//   top-k's workspace, feeds the same transpose kernels.
+#include <cuda_runtime.h>
+
+#include "dsv_launch.h"
+
+namespace dsv {
+
+namespace {
+
+constexpr int kRP = 32;                 // rank columns of the split operands (r <= 32, zero padded)
+constexpr int kRows = 128;              // groups per CTA: tensor-memory lanes, MMA M
+constexpr int kChunk = 128;             // key blocks per score tile: MMA N
+constexpr int kNBuf = 4;                // score tiles in tensor memory (4 x 128 columns)
+constexpr int kNSlot = 2;               // shared-memory slots of k_hi / k_lo tiles
+constexpr int kBins = 128;              // value bins of a row (pass 1)
+constexpr int kCand = 32;               // scores of the threshold bin ranked exactly per row
+constexpr float kZHalf = 1.0f;          // half-width of the binned range, in standard deviations
+constexpr int kSelWarp0 = 2;            // warps 2..5 select, one row per thread
+constexpr int kThreads = 192;
+constexpr int kTileBytes = kRows * kRP * 4;   // one 128 x 32 fp32 operand tile (16 KB)
+constexpr int kNumMain = 3;             // passes 0..2
+constexpr int kNumRadix = 5;            // digit passes of the exact fallback (7, 7, 7, 7, 4 bits)
+// digit dp of a 32-bit key: bits [shift, shift + width): 7, 7, 7, 7, 4 bits from the top
+__host__ __device__ constexpr int radix_bits(int dp) { return dp < 4 ? 7 : 4; }
+__host__ __device__ constexpr int radix_shift(int dp) { return dp < 4 ? 25 - 7 * dp : 0; }
+
+enum : unsigned int { W_QF = 1, W_KF, W_KFREE, W_SF, W_TFREE, W_DRAIN };
+constexpr unsigned int KID_SEL = 4;
+
+struct SelArgs {
+  CUtensorMap qh, ql, kh, kl;          // [B*H*G, 32] fp32, box 32 x 128, 128-byte swizzle
+  int H, G, words, tiles;              // tiles = ceil(G / 128) per (b, h)
+  long long rows;                      // B*H*G
+  int nnz;
+  int32_t* fwd_ptr;
+  int32_t* fwd_col;
+  uint32_t* mask;                      // [B*H][words][G]
+  float* scores;                       // optional [B*H*G, G]: the scores the selection used
+  HeadK hk;
+  Ctl ctl;
+};
+
+// Order-preserving map of a score to uint32: larger score, larger key; -0.0
+// and +0.0 map to the same key; NaN maps below every number.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  if (f != f) return 0u;
+  uint32_t b = __float_as_uint(f);
+  if ((b << 1) == 0u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+// Instruction descriptor of kind::tf32 with fp32 accumulation, both operands
+// K-major: D format F32 (bits 4-5 = 1), A and B format TF32 (bits 7-9 and
+// 10-12 = 2), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem], tf32 operands; the whole warp calls it and
+// one elected lane issues.
+__device__ __forceinline__ void mma_tf32_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tf32 hi / lo parts of the pooled vectors
+// ---------------------------------------------------------------------------
+// grid-stride over 2 * rows * 32 outputs; part 0 = queries, part 1 = keys.
+__global__ void __launch_bounds__(256) split_tf32_kernel(const float* __restrict__ qp, const float* __restrict__ kp,
+                                                         int r, long long rows, float* __restrict__ qh,
+                                                         float* __restrict__ ql, float* __restrict__ kh,
+                                                         float* __restrict__ kl) {
+  const long long n = rows * kRP;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n; i += (long long)gridDim.x * blockDim.x) {
+    const bool keys = i >= n;
+    const long long e = keys ? i - n : i;
+    const long long row = e / kRP;
+    const int c = (int)(e - row * kRP);
+    const float x = c < r ? (keys ? kp : qp)[row * r + c] : 0.f;
+    const float hi = tf32_rna(x);
+    const float lo = tf32_rna(x - hi);
+    (keys ? kh : qh)[e] = hi;
+    (keys ? kl : ql)[e] = lo;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Score tiles on the tensor cores, selection one row per thread
+// ---------------------------------------------------------------------------
+struct RowState {
+  // pass 0
+  float shift, sum, sq;
+  // bin map (pass 1 / 2): bin(s) = low bits of clamp(fma(s, sc, c0), B0, B0 + 127)
+  float sc, c0;
+  uint32_t keep_above;   // float bits: keep bins whose bits exceed this
+  uint32_t collect;      // float bits of the bin whose scores are ranked (none: 0xffffffff)
+  uint32_t kk;           // scores of that bin that are kept
+  int ncand;
+  bool fail;
+  // exact fallback
+  uint32_t prefix, hmask, rk;
+};
+
+constexpr float kB0 = 12582912.0f;      // 1.5 * 2^23: adding it leaves round(x) in the low mantissa bits
+constexpr float kB1 = kB0 + (float)(kBins - 1);
+
+__device__ __forceinline__ uint32_t bin_bits(float s, float sc, float c0) {
+  return __float_as_uint(fminf(fmaxf(fmaf(s, sc, c0), kB0), kB1));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_constant__ SelArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sbase = align_up_ptr<uint8_t>(smem_raw, 1024);
+  uint8_t* sQh = sbase;
+  uint8_t* sQl = sQh + kTileBytes;
+  uint8_t* sKh = sQl + kTileBytes;                       // [kNSlot] tiles
+  uint8_t* sKl = sKh + kNSlot * kTileBytes;              // [kNSlot] tiles
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sKl + kNSlot * kTileBytes);   // [kBins][kRows]
+  uint2* cand = reinterpret_cast<uint2*>(hist + kBins * kRows);             // [kCand][kRows]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(cand + kCand * kRows);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = q_full + 1;
+  uint64_t* k_free = k_full + kNSlot;
+  uint64_t* s_full = k_free + kNSlot;
+  uint64_t* t_free = s_full + kNBuf;
+  uint64_t* mma_drain = t_free + kNBuf;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_fail = const_cast<int*>(abort_flag + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Ctl& ctl = a.ctl;
+  const unsigned int kid = KID_SEL << 8;
+  const int G = a.G, nb = a.G, words = a.words;
+  const long long bh = blockIdx.x / a.tiles;
+  const int g0 = (int)(blockIdx.x - bh * a.tiles) * kRows;
+  const int h = (int)(bh % a.H), b = (int)(bh / a.H);
+  const int k = a.hk.k[h];
+  const int nc = (nb + kChunk - 1) / kChunk;             // score tiles per pass
+  const int main_passes = k >= nb ? 0 : kNumMain;        // k = nb: every block, nothing to score
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kNSlot; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_free[s], 1);
+    }
+    for (int s = 0; s < kNBuf; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&t_free[s], 4 * 32);
+    }
+    mbar_init(mma_drain, 1);
+    *abort_flag = 0;
+    *s_fail = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kNBuf * kChunk);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const bool tmem_ok = tmem_base == 0u;
+  if (!tmem_ok && threadIdx.x == 0) set_error(ctl, DSV_ERR_INTERNAL, blockIdx.x);
+
+  // ---- per-row selection state (selection warps) ----
+  const int quarter = warp & 3;
+  const int r = quarter * 32 + lane;                     // row of this thread in the tile
+  const int g = g0 + r;
+  const bool row_ok = warp >= kSelWarp0 && g < G;
+  const long long grow = bh * G + g;                     // global row
+  RowState st{};
+  st.collect = 0xffffffffu;
+
+  uint32_t gc = 0;                                       // score tiles so far (all passes)
+  int issued_q = 0;
+  uint32_t issued_k = 0;
+  bool ok = tmem_ok;
+
+  // One run of `npass` passes over the row's score tiles; `pass0` numbers
+  // them.  Every role walks the same tiles, so barrier phases follow gc.
+  auto run_passes = [&](int pass0, int npass) {
+    if (!ok || npass == 0) return;
+    const uint32_t total = (uint32_t)(npass * nc);
+    if (warp == 0) {
+      // ---------------- TMA producer ----------------
+      if (lane == 0) {
+        if (issued_q == 0) {
+          tma_prefetch_desc(&a.kh);
+          tma_prefetch_desc(&a.kl);
+          mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+          tma_load_2d(sQh, &a.qh, q_full, 0, (int)(bh * G + g0));
+          tma_load_2d(sQl, &a.ql, q_full, 0, (int)(bh * G + g0));
+          issued_q = 1;
+        }
+        for (uint32_t t = 0; t < total; ++t) {
+          const uint32_t n = gc + t;
+          const int slot = (int)(n % kNSlot);
+          const int c = (int)(t % (uint32_t)nc);
+          if (n >= kNSlot && !mbar_wait(&k_free[slot], ((n - kNSlot) / kNSlot) & 1u, abort_flag, ctl, kid | W_KFREE)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&k_full[slot], 2 * kTileBytes);
+          const int y = (int)(bh * G + (long long)c * kChunk);
+          tma_load_2d(sKh + slot * kTileBytes, &a.kh, &k_full[slot], 0, y);
+          tma_load_2d(sKl + slot * kTileBytes, &a.kl, &k_full[slot], 0, y);
+          issued_k = n + 1;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    } else if (warp == 1) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t ID = idesc_tf32_f32(kRows, kChunk);
+      if (!mbar_wait_warp(q_full, 0, abort_flag, ctl, kid | W_QF)) {
+        ok = false;
+        return;
+      }
+      const uint64_t dQh = sdesc_sw128(smem_u32(sQh), 16, 1024);
+      const uint64_t dQl = sdesc_sw128(smem_u32(sQl), 16, 1024);
+      const uint64_t dKh = sdesc_sw128(smem_u32(sKh), 16, 1024);
+      const uint64_t dKl = sdesc_sw128(smem_u32(sKl), 16, 1024);
+      for (uint32_t t = 0; t < total; ++t) {
+        const uint32_t n = gc + t;
+        const int slot = (int)(n % kNSlot);
+        const int buf = (int)(n % kNBuf);
+        if (!mbar_wait_warp(&k_full[slot], (n / kNSlot) & 1u, abort_flag, ctl, kid | W_KF)) {
+          ok = false;
+          break;
+        }
+        if (n >= kNBuf && !mbar_wait_warp(&t_free[buf], ((n - kNBuf) / kNBuf) & 1u, abort_flag, ctl, kid | W_TFREE)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = (uint32_t)buf * kChunk;
+        const uint32_t koff = (uint32_t)slot * kTileBytes;
+#pragma unroll
+        for (int p = 0; p < 3; ++p) {
+          const uint64_t da = p == 2 ? dQl : dQh;               // q_hi k_hi, q_hi k_lo, q_lo k_hi
+          const uint64_t db = desc_off(p == 1 ? dKl : dKh, koff);
+#pragma unroll
+          for (int kk = 0; kk < kRP / 8; ++kk)
+            mma_tf32_w(d, desc_off(da, kk * 32), desc_off(db, kk * 32), ID, (p > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit_w(&s_full[buf]);
+        mma_commit_w(&k_free[slot]);
+      }
+    } else {
+      // ---------------- selection: one row per thread ----------------
+      const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+      for (uint32_t t = 0; t < total; ++t) {
+        const uint32_t n = gc + t;
+        const int buf = (int)(n % kNBuf);
+        const int pass = pass0 + (int)(t / (uint32_t)nc);
+        const int c = (int)(t % (uint32_t)nc);
+        if (c == 0) {
+          // start of a pass: per-row set-up
+          if (pass == 1 || pass >= kNumMain) {
+            if (row_ok && !(pass >= kNumMain && !st.fail) && pass < kNumMain + kNumRadix) {
+              for (int i = 0; i < kBins; ++i) hist[i * kRows + r] = 0u;
+            }
+          }
+        }
+        if (!mbar_wait_warp(&s_full[buf], (n / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int jc = c * kChunk;
+        const int nv = min(kChunk, nb - jc);               // valid columns of this tile (uniform)
+        const bool work = row_ok && (pass < kNumMain || st.fail);
+#pragma unroll 1
+        for (int q = 0; q < kChunk / 32; ++q) {
+          uint32_t x[32];
+          tmem_ld32(tmem_base + lane_off + (uint32_t)buf * kChunk + (uint32_t)q * 32, x);
+          tmem_ld_wait();
+          if (q == kChunk / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&t_free[buf]);
+          }
+          const int j0 = jc + q * 32;
+          const int nvg = nv - q * 32;                   // valid columns of this group of 32 (may be <= 0)
+          if (!work || nvg <= 0) continue;
+          const int wi = j0 >> 5;                        // bitmask word of these 32 columns
+          if (pass == 0) {
+            if (j0 == 0) st.shift = __uint_as_float(x[0]);
+            float s0 = 0.f, s1 = 0.f, q0 = 0.f, q1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float d0 = e < nvg ? __uint_as_float(x[e]) - st.shift : 0.f;
+              const float d1 = e + 1 < nvg ? __uint_as_float(x[e + 1]) - st.shift : 0.f;
+              s0 += d0;
+              s1 += d1;
+              q0 = fmaf(d0, d0, q0);
+              q1 = fmaf(d1, d1, q1);
+            }
+            st.sum += s0 + s1;
+            st.sq += q0 + q1;
+            if (a.scores != nullptr) {
+              float* dst = a.scores + grow * (long long)nb + j0;
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (e < nvg) dst[e] = __uint_as_float(x[e]);
+            }
+          } else if (pass == 1) {
+            uint32_t* hrow = hist + r;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              if (e < nvg) {
+                const uint32_t bb = bin_bits(__uint_as_float(x[e]), st.sc, st.c0);
+                atomicAdd(hrow + (bb & (kBins - 1)) * kRows, 1u);
+              }
+            }
+          } else if (pass == 2 || pass == kNumMain + kNumRadix) {
+            // emit the bitmask word of these 32 columns
+            uint32_t word = 0u;
+            if (pass == 2) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                if (e < nvg) {
+                  const uint32_t bb = bin_bits(__uint_as_float(x[e]), st.sc, st.c0);
+                  word |= (bb > st.keep_above ? 1u : 0u) << e;
+                  if (bb == st.collect) {
+                    if (st.ncand < kCand) cand[st.ncand * kRows + r] = make_uint2(order_key(__uint_as_float(x[e])), (uint32_t)(j0 + e));
+                    ++st.ncand;
+                  }
+                }
+              }
+            } else {
+              // exact fallback: keys above T, then keys equal to T lowest index first
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                if (e < nvg) {
+                  const uint32_t u = order_key(__uint_as_float(x[e]));
+                  const bool eq = u == st.prefix;
+                  word |= ((u > st.prefix) || (eq && st.rk > 0u) ? 1u : 0u) << e;
+                  if (eq && st.rk > 0u) --st.rk;
+                }
+              }
+            }
+            a.mask[(bh * words + wi) * (long long)G + g] = word;
+          } else {
+            // exact fallback, digit pass: histogram of this digit among keys matching the prefix
+            const int dp = pass - kNumMain;
+            const int sh = radix_shift(dp);
+            const uint32_t dmask = (1u << radix_bits(dp)) - 1u;
+            uint32_t* hrow = hist + r;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              if (e < nvg) {
+                const uint32_t u = order_key(__uint_as_float(x[e]));
+                if ((u & st.hmask) == st.prefix) atomicAdd(hrow + ((u >> sh) & dmask) * kRows, 1u);
+              }
+            }
+          }
+        }
+        if (c == nc - 1 && row_ok) {
+          // end of a pass
+          if (pass == 0) {
+            const float inv_n = 1.0f / (float)nb;
+            const float m1 = st.sum * inv_n;
+            const float var = fmaxf(st.sq * inv_n - m1 * m1, 0.f);
+            const float sd = sqrtf(var);
+            const float mean = st.shift + m1;
+            const float zk = normcdfinvf(1.0f - (float)k / (float)nb);
+            const float lo = mean + (zk - kZHalf) * sd;
+            float sc = (float)(kBins - 1) / (2.0f * kZHalf * sd);
+            float c0 = kB0 - lo * sc;
+            if (!(sc > 0.f && sc < 1e30f && isfinite(c0) && isfinite(zk))) {
+              sc = 0.f;                                  // one bin: the exact fallback will decide
+              c0 = kB0;
+            }
+            st.sc = sc;
+            st.c0 = c0;
+          } else if (pass == 1) {
+            uint32_t above = 0u, bstar = 0u, cnt = 0u;
+            for (int i = kBins - 1; i >= 0; --i) {
+              const uint32_t ci = hist[i * kRows + r];
+              if (above + ci >= (uint32_t)k) {
+                bstar = (uint32_t)i;
+                cnt = ci;
+                break;
+              }
+              above += ci;
+            }
+            st.kk = (uint32_t)k - above;
+            const uint32_t bsbits = __float_as_uint(kB0) + bstar;
+            if (cnt == st.kk) {
+              st.keep_above = bsbits - 1u;               // the whole bin is kept
+              st.collect = 0xffffffffu;
+            } else {
+              st.keep_above = bsbits;
+              st.collect = bsbits;
+              st.fail = cnt > (uint32_t)kCand;
+            }
+            st.ncand = 0;
+          } else if (pass == 2) {
+            if (st.collect != 0xffffffffu && !st.fail) {
+              // rank the threshold bin's scores exactly and add the kept ones to the bitmask
+              const int nc2 = st.ncand;
+              for (int i = 0; i < nc2; ++i) {
+                const uint2 ci = cand[i * kRows + r];
+                uint32_t rank = 0u;
+                for (int j = 0; j < nc2; ++j) {
+                  const uint2 cj = cand[j * kRows + r];
+                  rank += (cj.x > ci.x || (cj.x == ci.x && cj.y < ci.y)) ? 1u : 0u;
+                }
+                if (rank < st.kk) {
+                  uint32_t* wp = a.mask + (bh * words + (ci.y >> 5)) * (long long)G + g;
+                  *wp |= 1u << (ci.y & 31u);
+                }
+              }
+            }
+            if (st.fail) {
+              st.prefix = 0u;
+              st.hmask = 0u;
+              st.rk = (uint32_t)k;
+            }
+          } else if (pass < kNumMain + kNumRadix && st.fail) {
+            const int dp = pass - kNumMain;
+            const int sh = radix_shift(dp);
+            const int nbin = 1 << radix_bits(dp);
+            uint32_t above = 0u;
+            for (int i = nbin - 1; i >= 0; --i) {
+              const uint32_t ci = hist[i * kRows + r];
+              if (above + ci >= st.rk) {
+                st.prefix |= (uint32_t)i << sh;
+                st.rk -= above;
+                break;
+              }
+              above += ci;
+            }
+            st.hmask |= (uint32_t)(nbin - 1) << sh;
+            // after the last digit: prefix = T, the k-th largest key; rk = keys equal to T to take
+          }
+        }
+      }
+    }
+    gc += total;
+  };
+
+  run_passes(0, main_passes);
+
+  // rows that need the exact fallback: the CTA runs its passes if any does
+  if (row_ok && st.fail) atomicOr(s_fail, 1);
+  __syncthreads();
+  if (ok && *s_fail && !*abort_flag) run_passes(kNumMain, kNumRadix + 1);
+
+  // every copy and product this CTA issued must be done before it exits
+  if (warp == 0 && lane == 0) {
+    if (issued_q) mbar_wait(q_full, 0, nullptr, ctl, kid | W_DRAIN);
+    for (uint32_t n = (issued_k > kNSlot ? issued_k - kNSlot : 0u); n < issued_k; ++n)
+      mbar_wait(&k_full[n % kNSlot], (n / kNSlot) & 1u, nullptr, ctl, kid | W_DRAIN);
+  } else if (warp == 1 && tmem_ok) {
+    mma_commit_w(mma_drain);
+    mbar_wait_warp(mma_drain, 0, nullptr, ctl, kid | W_DRAIN);
+  }
+
+  // the row's ascending list from its bitmask words (written by this thread)
+  if (row_ok && ok && !*abort_flag) {
+    const long long base = (long long)b * G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * G + (long long)g * k;
+    int32_t* dst = a.fwd_col + base;
+    if (k >= nb) {
+      for (int wi = 0; wi < words; ++wi) {
+        const int rem = nb - wi * 32;
+        a.mask[(bh * words + wi) * (long long)G + g] = rem >= 32 ? 0xffffffffu : ((1u << rem) - 1u);
+      }
+      for (int j = 0; j < nb; ++j) dst[j] = j;
+    } else {
+      int pos = 0;
+      for (int wi = 0; wi < words; ++wi) {
+        uint32_t m = a.mask[(bh * words + wi) * (long long)G + g];
+        while (m) {
+          if (pos < k) dst[pos] = wi * 32 + __ffs(m) - 1;
+          ++pos;
+          m &= m - 1u;
+        }
+      }
+      if (pos != k) set_error(ctl, DSV_ERR_INTERNAL, (unsigned int)(grow & 0x7fffffff));
+    }
+    a.fwd_ptr[grow] = (int32_t)base;
+    if (grow == a.rows - 1) a.fwd_ptr[a.rows] = a.nnz;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1 && tmem_ok) tmem_dealloc(tmem_base, kNBuf * kChunk);
+}
+
+constexpr int kSelSmem = 1024 + 2 * kTileBytes + 2 * kNSlot * kTileBytes + kBins * kRows * 4 + kCand * kRows * 8 +
+                         (1 + 2 * kNSlot + 2 * kNBuf + 1) * 8 + 16;
+static_assert(kSelSmem <= 227 * 1024, "score/select tiles exceed shared memory");
+
+}  // namespace
+
+size_t split_tf32_bytes(const dsv_shape& s) {
+  return 4 * align256((size_t)s.B * s.H * (size_t)(s.N / s.block) * kRP * sizeof(float));
+}
+
+cudaError_t launch_split_tf32(const float* qp, const float* kp, const dsv_shape& s, float* split, cudaStream_t st) {
+  const long long rows = (long long)s.B * s.H * (s.N / s.block);
+  const size_t part = align256((size_t)rows * kRP * sizeof(float)) / sizeof(float);
+  const long long n = 2 * rows * kRP;
+  const unsigned grid = (unsigned)std::min<long long>((n + 255) / 256, 152LL * 16);
+  split_tf32_kernel<<<grid, 256, 0, st>>>(qp, kp, s.r, rows, split, split + part, split + 2 * part, split + 3 * part);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_score_select(const PredictTopkMaps& maps, const dsv_shape& s, const HeadK& hk, int64_t nnz,
+                                int32_t* fwd_ptr, int32_t* fwd_col, uint32_t* mask, float* scores, const Ctl& ctl,
+                                cudaStream_t st) {
+  SelArgs a;
+  a.qh = maps.qh;
+  a.ql = maps.ql;
+  a.kh = maps.kh;
+  a.kl = maps.kl;
+  a.H = s.H;
+  a.G = s.N / s.block;
+  a.words = (a.G + 31) / 32;
+  a.tiles = (a.G + kRows - 1) / kRows;
+  a.rows = (long long)s.B * s.H * a.G;
+  a.nnz = (int)nnz;
+  a.fwd_ptr = fwd_ptr;
+  a.fwd_col = fwd_col;
+  a.mask = mask;
+  a.scores = scores;
+  a.hk = hk;
+  a.ctl = ctl;
+  cudaError_t e = cudaFuncSetAttribute(score_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)s.B * s.H * a.tiles;
+  score_select_kernel<<<(unsigned)grid, kThreads, kSelSmem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dsv

@@ -961,6 +961,9 @@ size_t topk_ws_bytes(const dsv_shape& s) {
 
 namespace {
 
+cudaError_t run_topk_transpose(const TopkArgs& a, int32_t* bwd_ptr, int32_t* bwd_col, int32_t* counts,
+                               cudaStream_t st);
+
 // the select kernel and the transposed lists, for fixed (a.row_k == null) or per-row k
 cudaError_t run_topk(const TopkArgs& a, int32_t* bwd_ptr, int32_t* bwd_col, int32_t* counts, cudaStream_t st) {
   const int G = a.G, words = a.words;
@@ -976,6 +979,16 @@ cudaError_t run_topk(const TopkArgs& a, int32_t* bwd_ptr, int32_t* bwd_col, int3
   else if (G <= 256 * kE) topk_select_kernel<256><<<grid, 256, 0, st>>>(a);
   else topk_select_kernel<512><<<grid, 512, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return run_topk_transpose(a, bwd_ptr, bwd_col, counts, st);
+}
+
+// The transposed lists from the selection bitmask a.mask: per-segment column
+// counts, their scan into bwd_ptr and output positions, then the fill.
+cudaError_t run_topk_transpose(const TopkArgs& a, int32_t* bwd_ptr, int32_t* bwd_col, int32_t* counts,
+                               cudaStream_t st) {
+  const int G = a.G, words = a.words;
+  const long long bhs = a.rows / G;
+  cudaError_t e;
   const int nseg = (G + kSeg - 1) / kSeg;
   dim3 g2((unsigned)((words + 7) / 8), (unsigned)nseg, (unsigned)bhs);
   topk_colcount_kernel<<<g2, 256, 0, st>>>(a.mask, G, G, words, counts);
@@ -1018,6 +1031,14 @@ cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk
   a.nnz = (int)nnz;
   a.hk = hk;
   return run_topk(a, bwd_ptr, bwd_col, topk_counts(ws, s), st);
+}
+
+cudaError_t launch_topk_transpose(const dsv_shape& s, const HeadK& hk, int64_t nnz, int32_t* bwd_ptr,
+                                  int32_t* bwd_col, void* ws, cudaStream_t st) {
+  TopkArgs a = topk_args(nullptr, s, nullptr, nullptr, ws);
+  a.nnz = (int)nnz;
+  a.hk = hk;
+  return run_topk_transpose(a, bwd_ptr, bwd_col, topk_counts(ws, s), st);
 }
 
 size_t topk_mass_ws_bytes(const dsv_shape& s) {

@@ -266,6 +266,35 @@ dsv_status dsv_cube_permute(const void* src, void* dst, dsv_shape s, int T, int 
                             int cx, int inverse, dsv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * dsv_predict_topk_blocks — the predictor fused with the top-k
+ * ([nl] 2B: the critical KV of a query group are estimated and selected in
+ * one kernel, so the group x block score matrix is never stored; [hi] 2B)
+ *
+ * Same result as dsv_predict_scores followed by dsv_topk_blocks, with the
+ * score matrix kept on chip: the lists hold, for every row (b, h, g), the
+ * k_h blocks with the largest score qbar_g . kbar_j (ties to the lower block
+ * index), ascending, and the transposed lists as dsv_topk_blocks writes them.
+ * The scores are computed on the tensor cores from tf32 hi / lo parts of the
+ * pooled fp32 vectors (three products, ~2^-21 relative to each product), so
+ * they agree with dsv_predict_scores' fp32 sums to about 1e-6 of the row's
+ * scale, not bit for bit; near-ties may therefore select differently from the
+ * two-call path.  The selection is exact for the scores this call computed.
+ *
+ * Q, K, Wq, Wk  as dsv_predict_scores.  Requires r <= 32 (else
+ *               DSV_ERR_UNSUPPORTED) and N / block <= 8192.
+ * k_per_head, fwd_ptr, fwd_col, bwd_ptr, bwd_col  as dsv_topk_blocks.
+ * scores        optional (NULL: not written).  If given, fp32 [B,H,G,nb],
+ *               16-byte aligned: the scores the selection used (a check
+ *               output; writing it costs the score matrix's HBM traffic).
+ * workspace     >= dsv_predict_topk_workspace_bytes(s) bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------ */
+size_t dsv_predict_topk_workspace_bytes(dsv_shape s);
+dsv_status dsv_predict_topk_blocks(const void* Q, const void* K, const float* Wq, const float* Wk, dsv_shape s,
+                                   const int32_t* k_per_head, int32_t* fwd_ptr, int32_t* fwd_col, int32_t* bwd_ptr,
+                                   int32_t* bwd_col, float* scores, void* workspace, size_t workspace_bytes,
+                                   dsv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Status and device-side error reporting.
  * ------------------------------------------------------------------------ */
 const char* dsv_status_string(dsv_status status);

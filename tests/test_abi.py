@@ -234,3 +234,27 @@ def test_binding_rejects_mismatched_shapes_on_the_host(lib):
         lib.predict_scores(Q, Q, W, W, 64)
     with pytest.raises(ValueError, match="CUDA device"):
         lib.sparse_attn_bwd(Q, Q, Q, Q, Q, torch.zeros(1, 2, 256), i32(9), i32(8), i32(9), i32(8), 64)
+
+
+def test_host_validation_predict_topk(lib):
+    L = lib.lib
+    s = _shape(lib)
+    ws = L.dsv_predict_topk_workspace_bytes(s)
+    assert ws >= L.dsv_predict_workspace_bytes(s) + L.dsv_topk_workspace_bytes(s)
+    assert L.dsv_predict_topk_workspace_bytes(_shape(lib, r=40)) == 0
+    k = (ctypes.c_int32 * 2)(2, 3)
+    w4 = (FAKE,) * 4
+    outs = (FAKE,) * 4
+    assert L.dsv_predict_topk_blocks(*w4, _shape(lib, r=40), k, *outs, None, FAKE, ws, None) == lib.DSV_ERR_UNSUPPORTED
+    assert L.dsv_predict_topk_blocks(*w4, _shape(lib, d=96), k, *outs, None, FAKE, ws, None) == lib.DSV_ERR_UNSUPPORTED
+    assert L.dsv_predict_topk_blocks(*w4, s, (ctypes.c_int32 * 2)(0, 3), *outs, None, FAKE, ws, None) == \
+        lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_predict_topk_blocks(*w4, s, (ctypes.c_int32 * 2)(2, 5), *outs, None, FAKE, ws, None) == \
+        lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_predict_topk_blocks(*w4, s, k, *outs, None, FAKE, ws - 1, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_predict_topk_blocks(*w4, s, k, *outs, FAKE + 4, FAKE, ws, None) == lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_predict_topk_blocks(None, FAKE, FAKE, FAKE, s, k, *outs, None, FAKE, ws, None) == \
+        lib.DSV_ERR_INVALID_ARG
+    assert L.dsv_predict_topk_blocks(*w4, s, k, *outs, None, FAKE + 16, ws, None) == lib.DSV_ERR_INVALID_ARG
+    big = _shape(lib, N=128 * 8193, H=1)
+    assert L.dsv_predict_topk_blocks(*w4, big, k, *outs, None, FAKE, 1 << 40, None) == lib.DSV_ERR_UNSUPPORTED
