@@ -805,29 +805,48 @@ __global__ void __launch_bounds__(kQThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, T::TMEM_COLS);
 }
 
-// Key blocks in order of decreasing transposed-list length within chunks of
-// consecutive (b, h) slices (counting sort by length, one CTA per chunk).
-// Chunks keep their order and hold as many heads as leave their Q and dO in
-// a part of L2, so the blocks running together share them; within a chunk
-// the long blocks start first and the grid's last wave holds short ones.
-// Ties in any order: a block's result does not depend on when it runs.
+// The order in which the dK/dV kernel takes its key blocks, per chunk of
+// consecutive (b, h) slices (one CTA per chunk; chunks keep their order and
+// hold as many heads as leave their Q and dO in a part of L2).  Inside a
+// chunk the few blocks whose transposed list is far longer than the chunk's
+// mean (more than kLongFactor times it: the blocks nearly every group picks)
+// go first, longest first, so that none of them starts in the grid's last
+// wave; every other block follows in its natural order.  Blocks that run
+// together are then neighbours in the latent, chosen by largely the same
+// query groups, so the Q and dO tiles they load are shared in L2: on a
+// 518k-token head (266 MB of Q and dO) ordering all blocks by list length
+// instead spread the CTAs running together over the whole head and re-read
+// its Q and dO from HBM ~44 times per launch.  Ties among long blocks in any
+// order: a block's result does not depend on when it runs.
 constexpr int kOrderThreads = 256;
 constexpr int kMaxOrderLen = kMaxBlocksPerRow;   // a list holds at most G groups
+constexpr int kLongFactor = 4;
 __global__ void __launch_bounds__(kOrderThreads) kv_order_kernel(const int32_t* __restrict__ bwd_ptr,
                                                                  long long rows, int chunk, int maxlen,
                                                                  int32_t* __restrict__ order) {
   __shared__ int32_t cnt[kMaxOrderLen + 1];
   __shared__ int32_t wtot[kOrderThreads / 32];
+  __shared__ int32_t s_nlong;
   const long long base = (long long)blockIdx.x * chunk;
   const int nb = (int)(rows - base < chunk ? rows - base : chunk);   // rows of this chunk
   const int32_t* P = bwd_ptr + base;
-  for (int i = threadIdx.x; i <= maxlen; i += kOrderThreads) cnt[i] = 0;
-  __syncthreads();
-  for (int r = threadIdx.x; r < nb; r += kOrderThreads) atomicAdd(&cnt[min(maxlen, max(0, P[r + 1] - P[r]))], 1);
-  __syncthreads();
-  // exclusive scan from the longest length down: start[len] = blocks with a longer list
-  const int per = (maxlen + 1 + kOrderThreads - 1) / kOrderThreads;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  // long: more than kLongFactor times the chunk's mean list length (and at least 64 groups)
+  const long long total = (long long)P[nb] - P[0];
+  const int thr = (int)max(64LL, kLongFactor * ((total + nb - 1) / nb));
+  for (int i = t; i <= maxlen; i += kOrderThreads) cnt[i] = 0;
+  if (t == 0) s_nlong = 0;
+  __syncthreads();
+  for (int r = t; r < nb; r += kOrderThreads) {
+    const int len = min(maxlen, max(0, P[r + 1] - P[r]));
+    if (len > thr) {
+      atomicAdd(&cnt[len], 1);
+      atomicAdd(&s_nlong, 1);
+    }
+  }
+  __syncthreads();
+  // long blocks: exclusive scan of their counts from the longest length down
+  const int per = (maxlen + 1 + kOrderThreads - 1) / kOrderThreads;
   const int b0 = t * per;            // this thread's lengths, counted from the top: maxlen - b0 ...
   int loc = 0;
   for (int q = b0; q < min(maxlen + 1, b0 + per); ++q) loc += cnt[maxlen - q];
@@ -856,8 +875,38 @@ __global__ void __launch_bounds__(kOrderThreads) kv_order_kernel(const int32_t* 
     run += c;
   }
   __syncthreads();
-  for (int r = threadIdx.x; r < nb; r += kOrderThreads)
-    order[base + atomicAdd(&cnt[min(maxlen, max(0, P[r + 1] - P[r]))], 1)] = (int32_t)(base + r);
+  for (int r = t; r < nb; r += kOrderThreads) {
+    const int len = min(maxlen, max(0, P[r + 1] - P[r]));
+    if (len > thr) order[base + atomicAdd(&cnt[len], 1)] = (int32_t)(base + r);
+  }
+  // the other blocks in natural order after them: exclusive scan of "short" over consecutive runs of rows
+  const int nlong = s_nlong;
+  const int span = (nb + kOrderThreads - 1) / kOrderThreads;
+  const int r0 = t * span, r1 = min(nb, r0 + span);
+  int mine = 0;
+  for (int r = r0; r < r1; ++r) mine += (min(maxlen, max(0, P[r + 1] - P[r])) > thr) ? 0 : 1;
+  __syncthreads();                   // wtot is reused
+  int sinc = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, sinc, o);
+    if (lane >= o) sinc += v;
+  }
+  if (lane == 31) wtot[w] = sinc;
+  __syncthreads();
+  if (w == 0) {
+    int x = lane < kOrderThreads / 32 ? wtot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += v;
+    }
+    if (lane < kOrderThreads / 32) wtot[lane] = x;
+  }
+  __syncthreads();
+  int pos = nlong + (w > 0 ? wtot[w - 1] : 0) + sinc - mine;
+  for (int r = r0; r < r1; ++r)
+    if (min(maxlen, max(0, P[r + 1] - P[r])) <= thr) order[base + pos++] = (int32_t)(base + r);
 }
 
 template <int BETA, int D>

@@ -87,9 +87,9 @@ def test_fused_equal_scores_take_the_exact_fallback(dsv):
     w = SMALL["global_small"]
     x = wl.make_inputs(w, device="cuda", with_dO=False)
     x.K[:, 0] = x.K[:, 0, :1].clone()
-    Kb = x.K[:, 1].reshape(w.B, w.nb, w.block, w.d)
-    Kb[:, 1::2] = Kb[:, 0:-1:2][:, : Kb[:, 1::2].shape[1]]
-    x.K[:, 1] = Kb.reshape(w.B, w.N, w.d)
+    Kb = x.K[:, 1].reshape(w.B, w.nb, w.block, w.d)            # a view of head 1
+    assert Kb.data_ptr() == x.K[:, 1].data_ptr()
+    Kb[:, 1::2] = Kb[:, 0:-1:2][:, : Kb[:, 1::2].shape[1]].clone()
     S, lists = _fused(dsv, x, w)
     S64 = to64(S)
     assert np.all(S64[:, 0] == S64[:, 0, :, :1])               # constant rows
