@@ -275,7 +275,7 @@ dsv_status dsv_predict_topk_blocks(const void* Q, const void* K, const float* Wq
     return from_cuda(e);
   }
   const int nb = s.N / s.block;
-  if (nb > kMaxBlocksPerRow) return DSV_ERR_UNSUPPORTED;
+  if (nb > kPredictTopkMaxBlocks) return DSV_ERR_UNSUPPORTED;
   if (!Q || !K || !Wq || !Wk || !k_per_head || !fwd_col || !bwd_col || !workspace) return DSV_ERR_INVALID_ARG;
   if (!al16(Q) || !al16(K) || !al16(Wq) || !al16(Wk) || !al16(fwd_ptr) || !al16(fwd_col) || !al16(bwd_ptr) ||
       !al16(bwd_col) || !al256(workspace) || (scores && !al16(scores)))

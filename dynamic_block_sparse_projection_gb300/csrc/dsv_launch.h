@@ -12,6 +12,7 @@ namespace dsv {
 
 constexpr int kMaxHeads = 1024;
 constexpr int kMaxBlocksPerRow = 8192;
+constexpr int kPredictTopkMaxBlocks = 4096;   // key blocks per row of the fused predictor + top-k
 
 // Per-head top-k sizes and their prefix sums (kernel parameter by value).
 struct HeadK {

@@ -36,6 +36,8 @@
 //   top-k's workspace, feeds the same transpose kernels.
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "dsv_launch.h"
 
 namespace dsv {
@@ -49,6 +51,8 @@ constexpr int kNBuf = 4;                // score tiles in tensor memory (4 x 128
 constexpr int kNSlot = 2;               // shared-memory slots of k_hi / k_lo tiles
 constexpr int kBins = 128;              // value bins of a row (pass 1)
 constexpr int kCand = 32;               // scores of the threshold bin ranked exactly per row
+constexpr int kHS = kRows + 1;          // row stride of the per-row columns in shared memory (bank spread)
+static_assert(kBins * 32 >= kPredictTopkMaxBlocks, "a row's bitmask words must fit its shared-memory column");
 constexpr float kZHalf = 1.0f;          // half-width of the binned range, in standard deviations
 constexpr int kSelWarp0 = 2;            // warps 2..5 select, one row per thread
 constexpr int kThreads = 192;
@@ -163,8 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   uint8_t* sQl = sQh + kTileBytes;
   uint8_t* sKh = sQl + kTileBytes;                       // [kNSlot] tiles
   uint8_t* sKl = sKh + kNSlot * kTileBytes;              // [kNSlot] tiles
-  uint32_t* hist = reinterpret_cast<uint32_t*>(sKl + kNSlot * kTileBytes);   // [kBins][kRows]
-  uint2* cand = reinterpret_cast<uint2*>(hist + kBins * kRows);             // [kCand][kRows]
+  // [kBins][kHS]: per row (column r) its histogram, then its bitmask words
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sKl + kNSlot * kTileBytes);
+  uint2* cand = reinterpret_cast<uint2*>(hist + kBins * kHS);               // [kCand][kRows]
   uint64_t* bars = reinterpret_cast<uint64_t*>(cand + kCand * kRows);
   uint64_t* q_full = bars;
   uint64_t* k_full = q_full + 1;
@@ -299,18 +304,15 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
     } else {
       // ---------------- selection: one row per thread ----------------
       const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+      uint32_t* hcol = hist + r;                          // this row's column: histogram, then bitmask words
       for (uint32_t t = 0; t < total; ++t) {
         const uint32_t n = gc + t;
         const int buf = (int)(n % kNBuf);
         const int pass = pass0 + (int)(t / (uint32_t)nc);
         const int c = (int)(t % (uint32_t)nc);
-        if (c == 0) {
-          // start of a pass: per-row set-up
-          if (pass == 1 || pass >= kNumMain) {
-            if (row_ok && !(pass >= kNumMain && !st.fail) && pass < kNumMain + kNumRadix) {
-              for (int i = 0; i < kBins; ++i) hist[i * kRows + r] = 0u;
-            }
-          }
+        const bool work = row_ok && (pass < kNumMain || st.fail);
+        if (c == 0 && work && (pass == 1 || (pass >= kNumMain && pass < kNumMain + kNumRadix))) {
+          for (int i = 0; i < kBins; ++i) hcol[i * kHS] = 0u;   // a histogram pass starts
         }
         if (!mbar_wait_warp(&s_full[buf], (n / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
           ok = false;
@@ -319,27 +321,19 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
         tc_fence_after();
         const int jc = c * kChunk;
         const int nv = min(kChunk, nb - jc);               // valid columns of this tile (uniform)
-        const bool work = row_ok && (pass < kNumMain || st.fail);
-#pragma unroll 1
-        for (int q = 0; q < kChunk / 32; ++q) {
-          uint32_t x[32];
-          tmem_ld32(tmem_base + lane_off + (uint32_t)buf * kChunk + (uint32_t)q * 32, x);
-          tmem_ld_wait();
-          if (q == kChunk / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive(&t_free[buf]);
-          }
+        // one group of 32 scores (columns j0 .. j0 + 31, the first nvg of them valid)
+        auto proc = [&](const uint32_t (&x)[32], int q, auto full_tag) {
+          constexpr bool FULL = decltype(full_tag)::value;
           const int j0 = jc + q * 32;
-          const int nvg = nv - q * 32;                   // valid columns of this group of 32 (may be <= 0)
-          if (!work || nvg <= 0) continue;
-          const int wi = j0 >> 5;                        // bitmask word of these 32 columns
+          const int nvg = nv - q * 32;
+          const int wi = j0 >> 5;                         // bitmask word of these 32 columns
           if (pass == 0) {
             if (j0 == 0) st.shift = __uint_as_float(x[0]);
             float s0 = 0.f, s1 = 0.f, q0 = 0.f, q1 = 0.f;
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
-              const float d0 = e < nvg ? __uint_as_float(x[e]) - st.shift : 0.f;
-              const float d1 = e + 1 < nvg ? __uint_as_float(x[e + 1]) - st.shift : 0.f;
+              const float d0 = (FULL || e < nvg) ? __uint_as_float(x[e]) - st.shift : 0.f;
+              const float d1 = (FULL || e + 1 < nvg) ? __uint_as_float(x[e + 1]) - st.shift : 0.f;
               s0 += d0;
               s1 += d1;
               q0 = fmaf(d0, d0, q0);
@@ -351,59 +345,75 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
               float* dst = a.scores + grow * (long long)nb + j0;
 #pragma unroll
               for (int e = 0; e < 32; ++e)
-                if (e < nvg) dst[e] = __uint_as_float(x[e]);
+                if (FULL || e < nvg) dst[e] = __uint_as_float(x[e]);
             }
           } else if (pass == 1) {
-            uint32_t* hrow = hist + r;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              if (e < nvg) {
+              if (FULL || e < nvg) {
                 const uint32_t bb = bin_bits(__uint_as_float(x[e]), st.sc, st.c0);
-                atomicAdd(hrow + (bb & (kBins - 1)) * kRows, 1u);
+                atomicAdd(hcol + (bb & (kBins - 1)) * kHS, 1u);
               }
             }
-          } else if (pass == 2 || pass == kNumMain + kNumRadix) {
-            // emit the bitmask word of these 32 columns
+          } else if (pass == 2) {
             uint32_t word = 0u;
-            if (pass == 2) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                if (e < nvg) {
-                  const uint32_t bb = bin_bits(__uint_as_float(x[e]), st.sc, st.c0);
-                  word |= (bb > st.keep_above ? 1u : 0u) << e;
-                  if (bb == st.collect) {
-                    if (st.ncand < kCand) cand[st.ncand * kRows + r] = make_uint2(order_key(__uint_as_float(x[e])), (uint32_t)(j0 + e));
-                    ++st.ncand;
-                  }
-                }
-              }
-            } else {
-              // exact fallback: keys above T, then keys equal to T lowest index first
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                if (e < nvg) {
-                  const uint32_t u = order_key(__uint_as_float(x[e]));
-                  const bool eq = u == st.prefix;
-                  word |= ((u > st.prefix) || (eq && st.rk > 0u) ? 1u : 0u) << e;
-                  if (eq && st.rk > 0u) --st.rk;
+            for (int e = 0; e < 32; ++e) {
+              if (FULL || e < nvg) {
+                const uint32_t bb = bin_bits(__uint_as_float(x[e]), st.sc, st.c0);
+                word |= (bb > st.keep_above ? 1u : 0u) << e;
+                if (bb == st.collect) {
+                  if (st.ncand < kCand)
+                    cand[st.ncand * kRows + r] = make_uint2(order_key(__uint_as_float(x[e])), (uint32_t)(j0 + e));
+                  ++st.ncand;
                 }
               }
             }
-            a.mask[(bh * words + wi) * (long long)G + g] = word;
+            hcol[wi * kHS] = word;
+          } else if (pass == kNumMain + kNumRadix) {
+            // exact fallback, emit: keys above T, then keys equal to T lowest index first
+            uint32_t word = 0u;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              if (FULL || e < nvg) {
+                const uint32_t u = order_key(__uint_as_float(x[e]));
+                const bool eq = u == st.prefix;
+                word |= ((u > st.prefix) || (eq && st.rk > 0u) ? 1u : 0u) << e;
+                if (eq && st.rk > 0u) --st.rk;
+              }
+            }
+            hcol[wi * kHS] = word;
           } else {
             // exact fallback, digit pass: histogram of this digit among keys matching the prefix
             const int dp = pass - kNumMain;
             const int sh = radix_shift(dp);
             const uint32_t dmask = (1u << radix_bits(dp)) - 1u;
-            uint32_t* hrow = hist + r;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              if (e < nvg) {
+              if (FULL || e < nvg) {
                 const uint32_t u = order_key(__uint_as_float(x[e]));
-                if ((u & st.hmask) == st.prefix) atomicAdd(hrow + ((u >> sh) & dmask) * kRows, 1u);
+                if ((u & st.hmask) == st.prefix) atomicAdd(hcol + ((u >> sh) & dmask) * kHS, 1u);
               }
             }
           }
+        };
+#pragma unroll 1
+        for (int q2 = 0; q2 < kChunk / 64; ++q2) {
+          uint32_t x0[32], x1[32];
+          const uint32_t ta = tmem_base + lane_off + (uint32_t)buf * kChunk + (uint32_t)q2 * 64;
+          tmem_ld32(ta, x0);
+          tmem_ld32(ta + 32, x1);
+          tmem_ld_wait();
+          if (q2 == kChunk / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(&t_free[buf]);
+          }
+          if (!work) continue;
+          const int qa = 2 * q2, qb = 2 * q2 + 1;
+          if (nv - qa * 32 >= 32) proc(x0, qa, std::true_type{});
+          else if (nv - qa * 32 > 0) proc(x0, qa, std::false_type{});
+          if (nv - qb * 32 >= 32) proc(x1, qb, std::true_type{});
+          else if (nv - qb * 32 > 0) proc(x1, qb, std::false_type{});
         }
         if (c == nc - 1 && row_ok) {
           // end of a pass
@@ -426,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
           } else if (pass == 1) {
             uint32_t above = 0u, bstar = 0u, cnt = 0u;
             for (int i = kBins - 1; i >= 0; --i) {
-              const uint32_t ci = hist[i * kRows + r];
+              const uint32_t ci = hcol[i * kHS];
               if (above + ci >= (uint32_t)k) {
                 bstar = (uint32_t)i;
                 cnt = ci;
@@ -456,10 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
                   const uint2 cj = cand[j * kRows + r];
                   rank += (cj.x > ci.x || (cj.x == ci.x && cj.y < ci.y)) ? 1u : 0u;
                 }
-                if (rank < st.kk) {
-                  uint32_t* wp = a.mask + (bh * words + (ci.y >> 5)) * (long long)G + g;
-                  *wp |= 1u << (ci.y & 31u);
-                }
+                if (rank < st.kk) hcol[(ci.y >> 5) * kHS] |= 1u << (ci.y & 31u);
               }
             }
             if (st.fail) {
@@ -473,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             const int nbin = 1 << radix_bits(dp);
             uint32_t above = 0u;
             for (int i = nbin - 1; i >= 0; --i) {
-              const uint32_t ci = hist[i * kRows + r];
+              const uint32_t ci = hcol[i * kHS];
               if (above + ci >= st.rk) {
                 st.prefix |= (uint32_t)i << sh;
                 st.rk -= above;
@@ -507,30 +514,49 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
     mbar_wait_warp(mma_drain, 0, nullptr, ctl, kid | W_DRAIN);
   }
 
-  // the row's ascending list from its bitmask words (written by this thread)
-  if (row_ok && ok && !*abort_flag) {
-    const long long base = (long long)b * G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * G + (long long)g * k;
-    int32_t* dst = a.fwd_col + base;
-    if (k >= nb) {
+  // outputs: this row's bitmask words (coalesced over the warp's consecutive
+  // rows), then the ascending lists, written cooperatively row by row
+  const bool out_ok = ok && !*abort_flag;
+  if (warp >= kSelWarp0 && out_ok) {
+    uint32_t* hcol = hist + r;
+    if (row_ok && k >= nb) {
       for (int wi = 0; wi < words; ++wi) {
         const int rem = nb - wi * 32;
-        a.mask[(bh * words + wi) * (long long)G + g] = rem >= 32 ? 0xffffffffu : ((1u << rem) - 1u);
+        hcol[wi * kHS] = rem >= 32 ? 0xffffffffu : ((1u << rem) - 1u);
       }
-      for (int j = 0; j < nb; ++j) dst[j] = j;
-    } else {
-      int pos = 0;
-      for (int wi = 0; wi < words; ++wi) {
-        uint32_t m = a.mask[(bh * words + wi) * (long long)G + g];
+    }
+    if (row_ok)
+      for (int wi = 0; wi < words; ++wi) a.mask[(bh * words + wi) * (long long)G + g] = hcol[wi * kHS];
+    __syncwarp();
+    const long long hbase = (long long)b * G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * G;
+    for (int rr = 0; rr < 32; ++rr) {
+      const int r2 = quarter * 32 + rr;
+      const int g2 = g0 + r2;
+      if (g2 >= G) break;
+      int32_t* dst = a.fwd_col + hbase + (long long)g2 * k;
+      int run = 0;
+      for (int i = 0; i * 32 < words; ++i) {
+        const int wi = i * 32 + lane;
+        uint32_t m = wi < words ? hist[wi * kHS + r2] : 0u;
+        const int cnt = __popc(m);
+        int inc = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += v;
+        }
+        int pos = run + inc - cnt;
         while (m) {
           if (pos < k) dst[pos] = wi * 32 + __ffs(m) - 1;
           ++pos;
           m &= m - 1u;
         }
+        run += __shfl_sync(0xffffffffu, inc, 31);
       }
-      if (pos != k) set_error(ctl, DSV_ERR_INTERNAL, (unsigned int)(grow & 0x7fffffff));
+      if (run != k && lane == 0) set_error(ctl, DSV_ERR_INTERNAL, (unsigned int)((bh * G + g2) & 0x7fffffff));
+      if (lane == 0) a.fwd_ptr[bh * G + g2] = (int32_t)(hbase + (long long)g2 * k);
     }
-    a.fwd_ptr[grow] = (int32_t)base;
-    if (grow == a.rows - 1) a.fwd_ptr[a.rows] = a.nnz;
+    if (row_ok && grow == a.rows - 1) a.fwd_ptr[a.rows] = a.nnz;
   }
 
   tc_fence_before();
@@ -539,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   if (warp == 1 && tmem_ok) tmem_dealloc(tmem_base, kNBuf * kChunk);
 }
 
-constexpr int kSelSmem = 1024 + 2 * kTileBytes + 2 * kNSlot * kTileBytes + kBins * kRows * 4 + kCand * kRows * 8 +
+constexpr int kSelSmem = 1024 + 2 * kTileBytes + 2 * kNSlot * kTileBytes + kBins * kHS * 4 + kCand * kRows * 8 +
                          (1 + 2 * kNSlot + 2 * kNBuf + 1) * 8 + 16;
 static_assert(kSelSmem <= 227 * 1024, "score/select tiles exceed shared memory");
 

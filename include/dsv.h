@@ -280,8 +280,8 @@ dsv_status dsv_cube_permute(const void* src, void* dst, dsv_shape s, int T, int 
  * scale, not bit for bit; near-ties may therefore select differently from the
  * two-call path.  The selection is exact for the scores this call computed.
  *
- * Q, K, Wq, Wk  as dsv_predict_scores.  Requires r <= 32 (else
- *               DSV_ERR_UNSUPPORTED) and N / block <= 8192.
+ * Q, K, Wq, Wk  as dsv_predict_scores.  Requires r <= 32 and
+ *               N / block <= 4096 (else DSV_ERR_UNSUPPORTED).
  * k_per_head, fwd_ptr, fwd_col, bwd_ptr, bwd_col  as dsv_topk_blocks.
  * scores        optional (NULL: not written).  If given, fp32 [B,H,G,nb],
  *               16-byte aligned: the scores the selection used (a check

@@ -256,5 +256,5 @@ def test_host_validation_predict_topk(lib):
     assert L.dsv_predict_topk_blocks(None, FAKE, FAKE, FAKE, s, k, *outs, None, FAKE, ws, None) == \
         lib.DSV_ERR_INVALID_ARG
     assert L.dsv_predict_topk_blocks(*w4, s, k, *outs, None, FAKE + 16, ws, None) == lib.DSV_ERR_INVALID_ARG
-    big = _shape(lib, N=128 * 8193, H=1)
+    big = _shape(lib, N=128 * 4097, H=1)
     assert L.dsv_predict_topk_blocks(*w4, big, k, *outs, None, FAKE, 1 << 40, None) == lib.DSV_ERR_UNSUPPORTED
