@@ -51,17 +51,20 @@ constexpr int kNBuf = 4;                // score tiles in tensor memory (4 x 128
 constexpr int kNSlot = 2;               // shared-memory slots of k_hi / k_lo tiles
 constexpr int kBins = 128;              // value bins of a row (pass 1)
 constexpr int kCand = 32;               // scores of the threshold bin ranked exactly per row
-constexpr int kHS = kRows + 1;          // row stride of the per-row columns in shared memory (bank spread)
 static_assert(kBins * 32 >= kPredictTopkMaxBlocks, "a row's bitmask words must fit its shared-memory column");
 constexpr float kZHalf = 1.0f;          // half-width of the binned range, in standard deviations
-constexpr int kSelWarp0 = 2;            // warps 2..5 select, one row per thread
-constexpr int kThreads = 192;
+constexpr int kColGroups = 4;           // threads per row: each takes 32 of a tile's 128 columns
+constexpr int kSelWarp0 = 2;            // warps 2 .. 17 select
+constexpr int kSelWarps = 4 * kColGroups;
+constexpr int kThreads = 32 * (kSelWarp0 + kSelWarps);
+constexpr int kMomStride = 4;           // the moment pass reads every kMomStride-th tile of a row
 constexpr int kTileBytes = kRows * kRP * 4;   // one 128 x 32 fp32 operand tile (16 KB)
 constexpr int kNumMain = 3;             // passes 0..2
-constexpr int kNumRadix = 5;            // digit passes of the exact fallback (7, 7, 7, 7, 4 bits)
-// digit dp of a 32-bit key: bits [shift, shift + width): 7, 7, 7, 7, 4 bits from the top
-__host__ __device__ constexpr int radix_bits(int dp) { return dp < 4 ? 7 : 4; }
-__host__ __device__ constexpr int radix_shift(int dp) { return dp < 4 ? 25 - 7 * dp : 0; }
+constexpr int kNumRadix = 6;            // digit passes of the exact fallback (6, 6, 6, 6, 6, 2 bits)
+constexpr int kRadixBins = 64;
+// digit dp of a 32-bit key: bits [shift, shift + width) counted from the top
+__host__ __device__ constexpr int radix_bits(int dp) { return dp < 5 ? 6 : 2; }
+__host__ __device__ constexpr int radix_shift(int dp) { return dp < 5 ? 26 - 6 * dp : 0; }
 
 enum : unsigned int { W_QF = 1, W_KF, W_KFREE, W_SF, W_TFREE, W_DRAIN };
 constexpr unsigned int KID_SEL = 4;
@@ -139,25 +142,29 @@ __global__ void __launch_bounds__(256) split_tf32_kernel(const float* __restrict
 // ---------------------------------------------------------------------------
 // Score tiles on the tensor cores, selection one row per thread
 // ---------------------------------------------------------------------------
-struct RowState {
-  // pass 0
-  float shift, sum, sq;
-  // bin map (pass 1 / 2): bin(s) = low bits of clamp(fma(s, sc, c0), B0, B0 + 127)
-  float sc, c0;
-  uint32_t keep_above;   // float bits: keep bins whose bits exceed this
-  uint32_t collect;      // float bits of the bin whose scores are ranked (none: 0xffffffff)
-  uint32_t kk;           // scores of that bin that are kept
-  int ncand;
-  bool fail;
-  // exact fallback
-  uint32_t prefix, hmask, rk;
-};
-
 constexpr float kB0 = 12582912.0f;      // 1.5 * 2^23: adding it leaves round(x) in the low mantissa bits
 constexpr float kB1 = kB0 + (float)(kBins - 1);
 
 __device__ __forceinline__ uint32_t bin_bits(float s, float sc, float c0) {
   return __float_as_uint(fminf(fmaxf(fmaf(s, sc, c0), kB0), kB1));
+}
+
+// Per-row state shared by the four threads of a row (shared memory).
+struct RowShared {
+  float mom_n[kColGroups], mom_mean[kColGroups], mom_m2[kColGroups];   // pass-0 partial moments
+  uint32_t keep_above;   // bin bits: keep scores whose bin bits exceed this
+  uint32_t collect;      // bin bits of the bin whose scores are ranked exactly (none: 0xffffffff)
+  uint32_t kk;           // how many of that bin are kept
+  int ccount;            // scores collected from that bin so far
+  int fail;              // the row needs the exact fallback
+};
+
+// bitmask word wi of row r in the shared column region (XOR spread: a warp's
+// rows, or a row's 32 consecutive words, fall in 32 different banks)
+__device__ __forceinline__ int word_at(int wi, int r) { return wi * kRows + (r ^ (wi & 31)); }
+
+__device__ __forceinline__ void sel_barrier() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kSelWarps * 32) : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_constant__ SelArgs a) {
@@ -167,10 +174,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   uint8_t* sQl = sQh + kTileBytes;
   uint8_t* sKh = sQl + kTileBytes;                       // [kNSlot] tiles
   uint8_t* sKl = sKh + kNSlot * kTileBytes;              // [kNSlot] tiles
-  // [kBins][kHS]: per row (column r) its histogram, then its bitmask words
+  // [kBins][kRows]: per row (column r) its histogram (bin * kRows + r), later its bitmask words (word_at)
   uint32_t* hist = reinterpret_cast<uint32_t*>(sKl + kNSlot * kTileBytes);
-  uint2* cand = reinterpret_cast<uint2*>(hist + kBins * kHS);               // [kCand][kRows]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(cand + kCand * kRows);
+  uint2* cand = reinterpret_cast<uint2*>(hist + kBins * kRows);             // [kCand][kRows]
+  RowShared* rs = reinterpret_cast<RowShared*>(cand + kCand * kRows);      // [kRows]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rs + kRows);
   uint64_t* q_full = bars;
   uint64_t* k_full = q_full + 1;
   uint64_t* k_free = k_full + kNSlot;
@@ -189,8 +197,18 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   const int g0 = (int)(blockIdx.x - bh * a.tiles) * kRows;
   const int h = (int)(bh % a.H), b = (int)(bh / a.H);
   const int k = a.hk.k[h];
-  const int nc = (nb + kChunk - 1) / kChunk;             // score tiles per pass
-  const int main_passes = k >= nb ? 0 : kNumMain;        // k = nb: every block, nothing to score
+  const int nc = (nb + kChunk - 1) / kChunk;             // score tiles of a row
+  const int nc0 = (nc + kMomStride - 1) / kMomStride;    // tiles of the moment pass (every kMomStride-th)
+  const bool select_all = k >= nb;                       // k = nb: every block, nothing to score
+
+  // selection threads: row r (tensor-memory lane) and column group cg of each 128-column tile
+  const bool sel = warp >= kSelWarp0;
+  const int quarter = warp & 3;
+  const int cg = sel ? (warp - kSelWarp0) >> 2 : 0;
+  const int r = quarter * 32 + lane;
+  const int g = g0 + r;
+  const bool row_ok = sel && g < G;
+  const long long grow = bh * G + g;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -200,12 +218,19 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
     }
     for (int s = 0; s < kNBuf; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&t_free[s], 4 * 32);
+      mbar_init(&t_free[s], kSelWarps * 32);
     }
     mbar_init(mma_drain, 1);
     *abort_flag = 0;
     *s_fail = 0;
     fence_mbar_init();
+  }
+  if (sel) {
+    for (int i = cg * (kBins / kColGroups); i < (cg + 1) * (kBins / kColGroups); ++i) hist[i * kRows + r] = 0u;
+    if (cg == 0) {
+      rs[r].ccount = 0;
+      rs[r].fail = 0;
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kNBuf * kChunk);
@@ -218,25 +243,24 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   const bool tmem_ok = tmem_base == 0u;
   if (!tmem_ok && threadIdx.x == 0) set_error(ctl, DSV_ERR_INTERNAL, blockIdx.x);
 
-  // ---- per-row selection state (selection warps) ----
-  const int quarter = warp & 3;
-  const int r = quarter * 32 + lane;                     // row of this thread in the tile
-  const int g = g0 + r;
-  const bool row_ok = warp >= kSelWarp0 && g < G;
-  const long long grow = bh * G + g;                     // global row
-  RowState st{};
-  st.collect = 0xffffffffu;
+  // per-thread row state
+  float sc = 0.f, c0 = kB0;                              // bin map
+  uint32_t keep_above = 0u, collect = 0xffffffffu;
+  bool fail = false;
+  uint32_t prefix = 0u, hmask = 0u, rk = 0u;             // exact fallback (column group 0)
 
   uint32_t gc = 0;                                       // score tiles so far (all passes)
   int issued_q = 0;
   uint32_t issued_k = 0;
   bool ok = tmem_ok;
 
-  // One run of `npass` passes over the row's score tiles; `pass0` numbers
-  // them.  Every role walks the same tiles, so barrier phases follow gc.
+  auto ntiles = [&](int pass) { return pass == 0 ? nc0 : nc; };
+  auto tile_of = [&](int pass, int t) { return pass == 0 ? t * kMomStride : t; };
+
+  // One run of passes pass0 .. pass0 + npass - 1 over the score tiles; every
+  // role walks the same tiles, so barrier phases follow gc.
   auto run_passes = [&](int pass0, int npass) {
     if (!ok || npass == 0) return;
-    const uint32_t total = (uint32_t)(npass * nc);
     if (warp == 0) {
       // ---------------- TMA producer ----------------
       if (lane == 0) {
@@ -248,19 +272,21 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
           tma_load_2d(sQl, &a.ql, q_full, 0, (int)(bh * G + g0));
           issued_q = 1;
         }
-        for (uint32_t t = 0; t < total; ++t) {
-          const uint32_t n = gc + t;
-          const int slot = (int)(n % kNSlot);
-          const int c = (int)(t % (uint32_t)nc);
-          if (n >= kNSlot && !mbar_wait(&k_free[slot], ((n - kNSlot) / kNSlot) & 1u, abort_flag, ctl, kid | W_KFREE)) {
-            ok = false;
-            break;
+        uint32_t n = gc;
+        for (int pass = pass0; ok && pass < pass0 + npass; ++pass) {
+          for (int t = 0; t < ntiles(pass); ++t, ++n) {
+            const int slot = (int)(n % kNSlot);
+            if (n >= kNSlot &&
+                !mbar_wait(&k_free[slot], ((n - kNSlot) / kNSlot) & 1u, abort_flag, ctl, kid | W_KFREE)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&k_full[slot], 2 * kTileBytes);
+            const int y = (int)(bh * G + (long long)tile_of(pass, t) * kChunk);
+            tma_load_2d(sKh + slot * kTileBytes, &a.kh, &k_full[slot], 0, y);
+            tma_load_2d(sKl + slot * kTileBytes, &a.kl, &k_full[slot], 0, y);
+            issued_k = n + 1;
           }
-          mbar_arrive_expect_tx(&k_full[slot], 2 * kTileBytes);
-          const int y = (int)(bh * G + (long long)c * kChunk);
-          tma_load_2d(sKh + slot * kTileBytes, &a.kh, &k_full[slot], 0, y);
-          tma_load_2d(sKl + slot * kTileBytes, &a.kl, &k_full[slot], 0, y);
-          issued_k = n + 1;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -269,174 +295,216 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       constexpr uint32_t ID = idesc_tf32_f32(kRows, kChunk);
       if (!mbar_wait_warp(q_full, 0, abort_flag, ctl, kid | W_QF)) {
         ok = false;
-        return;
-      }
-      const uint64_t dQh = sdesc_sw128(smem_u32(sQh), 16, 1024);
-      const uint64_t dQl = sdesc_sw128(smem_u32(sQl), 16, 1024);
-      const uint64_t dKh = sdesc_sw128(smem_u32(sKh), 16, 1024);
-      const uint64_t dKl = sdesc_sw128(smem_u32(sKl), 16, 1024);
-      for (uint32_t t = 0; t < total; ++t) {
-        const uint32_t n = gc + t;
-        const int slot = (int)(n % kNSlot);
-        const int buf = (int)(n % kNBuf);
-        if (!mbar_wait_warp(&k_full[slot], (n / kNSlot) & 1u, abort_flag, ctl, kid | W_KF)) {
-          ok = false;
-          break;
-        }
-        if (n >= kNBuf && !mbar_wait_warp(&t_free[buf], ((n - kNBuf) / kNBuf) & 1u, abort_flag, ctl, kid | W_TFREE)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d = (uint32_t)buf * kChunk;
-        const uint32_t koff = (uint32_t)slot * kTileBytes;
+      } else {
+        const uint64_t dQh = sdesc_sw128(smem_u32(sQh), 16, 1024);
+        const uint64_t dQl = sdesc_sw128(smem_u32(sQl), 16, 1024);
+        const uint64_t dKh = sdesc_sw128(smem_u32(sKh), 16, 1024);
+        const uint64_t dKl = sdesc_sw128(smem_u32(sKl), 16, 1024);
+        uint32_t n = gc;
+        for (int pass = pass0; ok && pass < pass0 + npass; ++pass) {
+          for (int t = 0; t < ntiles(pass); ++t, ++n) {
+            const int slot = (int)(n % kNSlot);
+            const int buf = (int)(n % kNBuf);
+            if (!mbar_wait_warp(&k_full[slot], (n / kNSlot) & 1u, abort_flag, ctl, kid | W_KF)) {
+              ok = false;
+              break;
+            }
+            if (n >= kNBuf &&
+                !mbar_wait_warp(&t_free[buf], ((n - kNBuf) / kNBuf) & 1u, abort_flag, ctl, kid | W_TFREE)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d = (uint32_t)buf * kChunk;
+            const uint32_t koff = (uint32_t)slot * kTileBytes;
 #pragma unroll
-        for (int p = 0; p < 3; ++p) {
-          const uint64_t da = p == 2 ? dQl : dQh;               // q_hi k_hi, q_hi k_lo, q_lo k_hi
-          const uint64_t db = desc_off(p == 1 ? dKl : dKh, koff);
+            for (int p = 0; p < 3; ++p) {
+              const uint64_t da = p == 2 ? dQl : dQh;               // q_hi k_hi, q_hi k_lo, q_lo k_hi
+              const uint64_t db = desc_off(p == 1 ? dKl : dKh, koff);
 #pragma unroll
-          for (int kk = 0; kk < kRP / 8; ++kk)
-            mma_tf32_w(d, desc_off(da, kk * 32), desc_off(db, kk * 32), ID, (p > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < kRP / 8; ++kk)
+                mma_tf32_w(d, desc_off(da, kk * 32), desc_off(db, kk * 32), ID, (p > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit_w(&s_full[buf]);
+            mma_commit_w(&k_free[slot]);
+          }
         }
-        mma_commit_w(&s_full[buf]);
-        mma_commit_w(&k_free[slot]);
       }
     } else {
-      // ---------------- selection: one row per thread ----------------
+      // ---------------- selection: row r, columns cg*32 .. cg*32 + 31 of every tile ----------------
       const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-      uint32_t* hcol = hist + r;                          // this row's column: histogram, then bitmask words
-      for (uint32_t t = 0; t < total; ++t) {
-        const uint32_t n = gc + t;
-        const int buf = (int)(n % kNBuf);
-        const int pass = pass0 + (int)(t / (uint32_t)nc);
-        const int c = (int)(t % (uint32_t)nc);
-        const bool work = row_ok && (pass < kNumMain || st.fail);
-        if (c == 0 && work && (pass == 1 || (pass >= kNumMain && pass < kNumMain + kNumRadix))) {
-          for (int i = 0; i < kBins; ++i) hcol[i * kHS] = 0u;   // a histogram pass starts
-        }
-        if (!mbar_wait_warp(&s_full[buf], (n / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const int jc = c * kChunk;
-        const int nv = min(kChunk, nb - jc);               // valid columns of this tile (uniform)
-        // one group of 32 scores (columns j0 .. j0 + 31, the first nvg of them valid)
-        auto proc = [&](const uint32_t (&x)[32], int q, auto full_tag) {
-          constexpr bool FULL = decltype(full_tag)::value;
-          const int j0 = jc + q * 32;
-          const int nvg = nv - q * 32;
-          const int wi = j0 >> 5;                         // bitmask word of these 32 columns
-          if (pass == 0) {
-            if (j0 == 0) st.shift = __uint_as_float(x[0]);
-            float s0 = 0.f, s1 = 0.f, q0 = 0.f, q1 = 0.f;
+      uint32_t* hcol = hist + r;
+      uint32_t n = gc;
+      float shift = 0.f, s1 = 0.f, s2 = 0.f, cnt_n = 0.f;  // pass-0 partial moments of this thread's columns
+      bool have_shift = false;
+      for (int pass = pass0; pass < pass0 + npass; ++pass) {
+        const bool fb = pass >= kNumMain;                  // exact fallback pass: column group 0 does the row
+        const bool work = row_ok && (!fb || (fail && cg == 0));
+        // the fallback's digit histograms live in the candidate region, [bin][row]: the
+        // histogram region now holds bitmask words, spread over other rows' columns
+        uint32_t* fcol = reinterpret_cast<uint32_t*>(cand) + r;
+        if (fb && work && pass < kNumMain + kNumRadix)
+          for (int i = 0; i < kRadixBins; ++i) fcol[i * kRows] = 0u;   // this digit's histogram
+        for (int t = 0; t < ntiles(pass); ++t, ++n) {
+          const int buf = (int)(n % kNBuf);
+          const int c = tile_of(pass, t);
+          // after an abort the warp keeps walking the passes without waiting or
+          // working, so that it still reaches every named barrier below
+          if (!ok) continue;
+          if (!mbar_wait_warp(&s_full[buf], (n / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
+            ok = false;
+            continue;
+          }
+          tc_fence_after();
+          const int nv = min(kChunk, nb - c * kChunk);   // valid columns of this tile (uniform)
+          // the 32 scores of column group q of this tile (columns j0 .. j0 + 31, the first nvg valid)
+          auto proc = [&](const uint32_t (&x)[32], int q, auto full_tag) {
+            constexpr bool FULL = decltype(full_tag)::value;
+            const int j0 = c * kChunk + q * 32;
+            const int nvg = nv - q * 32;
+            const int wi = j0 >> 5;                       // bitmask word of these 32 columns
+            if (pass == 0) {
+              if (!have_shift) {
+                shift = __uint_as_float(x[0]);
+                have_shift = true;
+              }
+              float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float d0 = (FULL || e < nvg) ? __uint_as_float(x[e]) - st.shift : 0.f;
-              const float d1 = (FULL || e + 1 < nvg) ? __uint_as_float(x[e + 1]) - st.shift : 0.f;
-              s0 += d0;
-              s1 += d1;
-              q0 = fmaf(d0, d0, q0);
-              q1 = fmaf(d1, d1, q1);
-            }
-            st.sum += s0 + s1;
-            st.sq += q0 + q1;
-            if (a.scores != nullptr) {
-              float* dst = a.scores + grow * (long long)nb + j0;
+              for (int e = 0; e < 32; e += 2) {
+                const float d0 = (FULL || e < nvg) ? __uint_as_float(x[e]) - shift : 0.f;
+                const float d1 = (FULL || e + 1 < nvg) ? __uint_as_float(x[e + 1]) - shift : 0.f;
+                a0 += d0;
+                a1 += d1;
+                b0 = fmaf(d0, d0, b0);
+                b1 = fmaf(d1, d1, b1);
+              }
+              s1 += a0 + a1;
+              s2 += b0 + b1;
+              cnt_n += (float)(FULL ? 32 : nvg);
+            } else if (pass == 1) {
 #pragma unroll
               for (int e = 0; e < 32; ++e)
-                if (FULL || e < nvg) dst[e] = __uint_as_float(x[e]);
-            }
-          } else if (pass == 1) {
+                if (FULL || e < nvg) atomicAdd(hcol + (bin_bits(__uint_as_float(x[e]), sc, c0) & (kBins - 1)) * kRows, 1u);
+              if (a.scores != nullptr) {
+                // check output: the scores this selection uses
+                float* dst = a.scores + grow * (long long)nb + j0;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              if (FULL || e < nvg) {
-                const uint32_t bb = bin_bits(__uint_as_float(x[e]), st.sc, st.c0);
-                atomicAdd(hcol + (bb & (kBins - 1)) * kHS, 1u);
+                for (int e = 0; e < 32; ++e)
+                  if (FULL || e < nvg) dst[e] = __uint_as_float(x[e]);
               }
-            }
-          } else if (pass == 2) {
-            uint32_t word = 0u;
+            } else if (pass == 2) {
+              uint32_t word = 0u, eq = 0u;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              if (FULL || e < nvg) {
-                const uint32_t bb = bin_bits(__uint_as_float(x[e]), st.sc, st.c0);
-                word |= (bb > st.keep_above ? 1u : 0u) << e;
-                if (bb == st.collect) {
-                  if (st.ncand < kCand)
-                    cand[st.ncand * kRows + r] = make_uint2(order_key(__uint_as_float(x[e])), (uint32_t)(j0 + e));
-                  ++st.ncand;
+              for (int e = 0; e < 32; ++e) {
+                if (FULL || e < nvg) {
+                  const uint32_t bb = bin_bits(__uint_as_float(x[e]), sc, c0);
+                  word |= (bb > keep_above ? 1u : 0u) << e;
+                  eq |= (bb == collect ? 1u : 0u) << e;
+                }
+              }
+              hist[word_at(wi, r)] = word;
+              if (eq) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                  if ((eq >> e) & 1u) {
+                    const int pos = atomicAdd(&rs[r].ccount, 1);
+                    if (pos < kCand) cand[pos * kRows + r] = make_uint2(order_key(__uint_as_float(x[e])), (uint32_t)(j0 + e));
+                  }
+                }
+              }
+            } else if (pass == kNumMain + kNumRadix) {
+              // exact fallback, emit: keys above T, then keys equal to T lowest index first
+              uint32_t word = 0u;
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                if (FULL || e < nvg) {
+                  const uint32_t u = order_key(__uint_as_float(x[e]));
+                  const bool eqk = u == prefix;
+                  word |= ((u > prefix) || (eqk && rk > 0u) ? 1u : 0u) << e;
+                  if (eqk && rk > 0u) --rk;
+                }
+              }
+              hist[word_at(wi, r)] = word;
+            } else {
+              // exact fallback, digit pass: histogram of this digit among keys matching the prefix
+              const int dp = pass - kNumMain;
+              const int sh = radix_shift(dp);
+              const uint32_t dmask = (1u << radix_bits(dp)) - 1u;
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                if (FULL || e < nvg) {
+                  const uint32_t u = order_key(__uint_as_float(x[e]));
+                  if ((u & hmask) == prefix) atomicAdd(fcol + ((u >> sh) & dmask) * kRows, 1u);
                 }
               }
             }
-            hcol[wi * kHS] = word;
-          } else if (pass == kNumMain + kNumRadix) {
-            // exact fallback, emit: keys above T, then keys equal to T lowest index first
-            uint32_t word = 0u;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              if (FULL || e < nvg) {
-                const uint32_t u = order_key(__uint_as_float(x[e]));
-                const bool eq = u == st.prefix;
-                word |= ((u > st.prefix) || (eq && st.rk > 0u) ? 1u : 0u) << e;
-                if (eq && st.rk > 0u) --st.rk;
-              }
-            }
-            hcol[wi * kHS] = word;
-          } else {
-            // exact fallback, digit pass: histogram of this digit among keys matching the prefix
-            const int dp = pass - kNumMain;
-            const int sh = radix_shift(dp);
-            const uint32_t dmask = (1u << radix_bits(dp)) - 1u;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              if (FULL || e < nvg) {
-                const uint32_t u = order_key(__uint_as_float(x[e]));
-                if ((u & st.hmask) == st.prefix) atomicAdd(hcol + ((u >> sh) & dmask) * kHS, 1u);
-              }
-            }
-          }
-        };
-#pragma unroll 1
-        for (int q2 = 0; q2 < kChunk / 64; ++q2) {
-          uint32_t x0[32], x1[32];
-          const uint32_t ta = tmem_base + lane_off + (uint32_t)buf * kChunk + (uint32_t)q2 * 64;
-          tmem_ld32(ta, x0);
-          tmem_ld32(ta + 32, x1);
-          tmem_ld_wait();
-          if (q2 == kChunk / 64 - 1) {
+          };
+          auto run_group = [&](const uint32_t (&x)[32], int q) {
+            if (nv - q * 32 >= 32) proc(x, q, std::true_type{});
+            else if (nv - q * 32 > 0) proc(x, q, std::false_type{});
+          };
+          const uint32_t tb = tmem_base + lane_off + (uint32_t)buf * kChunk;
+          if (!fb) {
+            uint32_t x[32];
+            tmem_ld32(tb + (uint32_t)cg * 32, x);
+            tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&t_free[buf]);
+            if (work) run_group(x, cg);
+          } else if (cg == 0) {
+            // the fallback row's four column groups, in order, by one thread
+#pragma unroll 1
+            for (int q = 0; q < kColGroups; ++q) {
+              uint32_t x[32];
+              tmem_ld32(tb + (uint32_t)q * 32, x);
+              tmem_ld_wait();
+              if (q == kColGroups - 1) {
+                tc_fence_before();
+                mbar_arrive(&t_free[buf]);
+              }
+              if (work) run_group(x, q);
+            }
+          } else {
+            mbar_arrive(&t_free[buf]);
           }
-          if (!work) continue;
-          const int qa = 2 * q2, qb = 2 * q2 + 1;
-          if (nv - qa * 32 >= 32) proc(x0, qa, std::true_type{});
-          else if (nv - qa * 32 > 0) proc(x0, qa, std::false_type{});
-          if (nv - qb * 32 >= 32) proc(x1, qb, std::true_type{});
-          else if (nv - qb * 32 > 0) proc(x1, qb, std::false_type{});
         }
-        if (c == nc - 1 && row_ok) {
-          // end of a pass
-          if (pass == 0) {
-            const float inv_n = 1.0f / (float)nb;
-            const float m1 = st.sum * inv_n;
-            const float var = fmaxf(st.sq * inv_n - m1 * m1, 0.f);
-            const float sd = sqrtf(var);
-            const float mean = st.shift + m1;
+        // ---- end of a pass ----
+        if (pass == 0) {
+          if (row_ok) {
+            rs[r].mom_n[cg] = cnt_n;
+            rs[r].mom_mean[cg] = cnt_n > 0.f ? shift + s1 / cnt_n : 0.f;
+            rs[r].mom_m2[cg] = cnt_n > 0.f ? fmaxf(s2 - s1 * s1 / cnt_n, 0.f) : 0.f;
+          }
+          sel_barrier();
+          if (row_ok) {
+            // the row's mean and variance from the four parts (same order in all four threads)
+            float nn = 0.f, mean = 0.f;
+            for (int q = 0; q < kColGroups; ++q) {
+              nn += rs[r].mom_n[q];
+              mean += rs[r].mom_n[q] * rs[r].mom_mean[q];
+            }
+            mean = nn > 0.f ? mean / nn : 0.f;
+            float m2 = 0.f;
+            for (int q = 0; q < kColGroups; ++q) {
+              const float dm = rs[r].mom_mean[q] - mean;
+              m2 += rs[r].mom_m2[q] + rs[r].mom_n[q] * dm * dm;
+            }
+            const float sd = nn > 0.f ? sqrtf(m2 / nn) : 0.f;
             const float zk = normcdfinvf(1.0f - (float)k / (float)nb);
             const float lo = mean + (zk - kZHalf) * sd;
-            float sc = (float)(kBins - 1) / (2.0f * kZHalf * sd);
-            float c0 = kB0 - lo * sc;
+            sc = (float)(kBins - 1) / (2.0f * kZHalf * sd);
+            c0 = kB0 - lo * sc;
             if (!(sc > 0.f && sc < 1e30f && isfinite(c0) && isfinite(zk))) {
-              sc = 0.f;                                  // one bin: the exact fallback will decide
+              sc = 0.f;                                  // one bin: the exact fallback decides
               c0 = kB0;
             }
-            st.sc = sc;
-            st.c0 = c0;
-          } else if (pass == 1) {
+          }
+        } else if (pass == 1) {
+          sel_barrier();                                 // every thread's histogram adds are in
+          if (row_ok && cg == 0) {
             uint32_t above = 0u, bstar = 0u, cnt = 0u;
             for (int i = kBins - 1; i >= 0; --i) {
-              const uint32_t ci = hcol[i * kHS];
+              const uint32_t ci = hcol[i * kRows];
               if (above + ci >= (uint32_t)k) {
                 bstar = (uint32_t)i;
                 cnt = ci;
@@ -444,63 +512,73 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
               }
               above += ci;
             }
-            st.kk = (uint32_t)k - above;
+            const uint32_t kk = (uint32_t)k - above;
             const uint32_t bsbits = __float_as_uint(kB0) + bstar;
-            if (cnt == st.kk) {
-              st.keep_above = bsbits - 1u;               // the whole bin is kept
-              st.collect = 0xffffffffu;
+            rs[r].kk = kk;
+            if (cnt == kk) {
+              rs[r].keep_above = bsbits - 1u;            // the whole bin is kept
+              rs[r].collect = 0xffffffffu;
             } else {
-              st.keep_above = bsbits;
-              st.collect = bsbits;
-              st.fail = cnt > (uint32_t)kCand;
+              rs[r].keep_above = bsbits;
+              rs[r].collect = bsbits;
+              rs[r].fail = cnt > (uint32_t)kCand ? 1 : 0;
             }
-            st.ncand = 0;
-          } else if (pass == 2) {
-            if (st.collect != 0xffffffffu && !st.fail) {
+          }
+          sel_barrier();                                 // decisions out; the histogram region becomes words
+          if (row_ok) {
+            keep_above = rs[r].keep_above;
+            collect = rs[r].collect;
+            fail = rs[r].fail != 0;
+          }
+        } else if (pass == 2) {
+          sel_barrier();                                 // every word and candidate of the row is in
+          if (row_ok && cg == 0) {
+            if (collect != 0xffffffffu && !fail) {
               // rank the threshold bin's scores exactly and add the kept ones to the bitmask
-              const int nc2 = st.ncand;
-              for (int i = 0; i < nc2; ++i) {
+              const int n2 = min(rs[r].ccount, kCand);
+              const uint32_t kk = rs[r].kk;
+              for (int i = 0; i < n2; ++i) {
                 const uint2 ci = cand[i * kRows + r];
                 uint32_t rank = 0u;
-                for (int j = 0; j < nc2; ++j) {
+                for (int j = 0; j < n2; ++j) {
                   const uint2 cj = cand[j * kRows + r];
                   rank += (cj.x > ci.x || (cj.x == ci.x && cj.y < ci.y)) ? 1u : 0u;
                 }
-                if (rank < st.kk) hcol[(ci.y >> 5) * kHS] |= 1u << (ci.y & 31u);
+                if (rank < kk) hist[word_at((int)(ci.y >> 5), r)] |= 1u << (ci.y & 31u);
               }
             }
-            if (st.fail) {
-              st.prefix = 0u;
-              st.hmask = 0u;
-              st.rk = (uint32_t)k;
+            if (fail) {
+              prefix = 0u;
+              hmask = 0u;
+              rk = (uint32_t)k;
             }
-          } else if (pass < kNumMain + kNumRadix && st.fail) {
-            const int dp = pass - kNumMain;
-            const int sh = radix_shift(dp);
-            const int nbin = 1 << radix_bits(dp);
-            uint32_t above = 0u;
-            for (int i = nbin - 1; i >= 0; --i) {
-              const uint32_t ci = hcol[i * kHS];
-              if (above + ci >= st.rk) {
-                st.prefix |= (uint32_t)i << sh;
-                st.rk -= above;
-                break;
-              }
-              above += ci;
-            }
-            st.hmask |= (uint32_t)(nbin - 1) << sh;
-            // after the last digit: prefix = T, the k-th largest key; rk = keys equal to T to take
           }
+        } else if (work && pass < kNumMain + kNumRadix) {
+          const int dp = pass - kNumMain;
+          const int sh = radix_shift(dp);
+          const int nbin = 1 << radix_bits(dp);
+          uint32_t above = 0u;
+          for (int i = nbin - 1; i >= 0; --i) {
+            const uint32_t ci = fcol[i * kRows];
+            if (above + ci >= rk) {
+              prefix |= (uint32_t)i << sh;
+              rk -= above;
+              break;
+            }
+            above += ci;
+          }
+          hmask |= (uint32_t)(nbin - 1) << sh;
+          // after the last digit: prefix = T, the k-th largest key; rk = keys equal to T to take
         }
       }
     }
-    gc += total;
+    for (int pass = pass0; pass < pass0 + npass; ++pass) gc += (uint32_t)ntiles(pass);
   };
 
-  run_passes(0, main_passes);
+  if (!select_all) run_passes(0, kNumMain);
 
   // rows that need the exact fallback: the CTA runs its passes if any does
-  if (row_ok && st.fail) atomicOr(s_fail, 1);
+  if (row_ok && cg == 0 && fail) atomicOr(s_fail, 1);
   __syncthreads();
   if (ok && *s_fail && !*abort_flag) run_passes(kNumMain, kNumRadix + 1);
 
@@ -514,30 +592,30 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
     mbar_wait_warp(mma_drain, 0, nullptr, ctl, kid | W_DRAIN);
   }
 
-  // outputs: this row's bitmask words (coalesced over the warp's consecutive
-  // rows), then the ascending lists, written cooperatively row by row
+  // outputs: the bitmask words (coalesced over consecutive rows), then the
+  // ascending lists, written cooperatively row by row
   const bool out_ok = ok && !*abort_flag;
-  if (warp >= kSelWarp0 && out_ok) {
-    uint32_t* hcol = hist + r;
-    if (row_ok && k >= nb) {
-      for (int wi = 0; wi < words; ++wi) {
+  if (sel && out_ok) {
+    if (row_ok && select_all) {
+      for (int wi = cg; wi < words; wi += kColGroups) {
         const int rem = nb - wi * 32;
-        hcol[wi * kHS] = rem >= 32 ? 0xffffffffu : ((1u << rem) - 1u);
+        hist[word_at(wi, r)] = rem >= 32 ? 0xffffffffu : ((1u << rem) - 1u);
       }
     }
+    sel_barrier();                                       // every word of every row is final
     if (row_ok)
-      for (int wi = 0; wi < words; ++wi) a.mask[(bh * words + wi) * (long long)G + g] = hcol[wi * kHS];
-    __syncwarp();
+      for (int wi = cg; wi < words; wi += kColGroups) a.mask[(bh * words + wi) * (long long)G + g] = hist[word_at(wi, r)];
     const long long hbase = (long long)b * G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * G;
-    for (int rr = 0; rr < 32; ++rr) {
-      const int r2 = quarter * 32 + rr;
+    const int cw = warp - kSelWarp0;
+    for (int rr = 0; rr < kRows / kSelWarps; ++rr) {
+      const int r2 = cw * (kRows / kSelWarps) + rr;
       const int g2 = g0 + r2;
       if (g2 >= G) break;
       int32_t* dst = a.fwd_col + hbase + (long long)g2 * k;
       int run = 0;
       for (int i = 0; i * 32 < words; ++i) {
         const int wi = i * 32 + lane;
-        uint32_t m = wi < words ? hist[wi * kHS + r2] : 0u;
+        uint32_t m = wi < words ? hist[word_at(wi, r2)] : 0u;
         const int cnt = __popc(m);
         int inc = cnt;
 #pragma unroll
@@ -553,10 +631,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
         }
         run += __shfl_sync(0xffffffffu, inc, 31);
       }
-      if (run != k && lane == 0) set_error(ctl, DSV_ERR_INTERNAL, (unsigned int)((bh * G + g2) & 0x7fffffff));
-      if (lane == 0) a.fwd_ptr[bh * G + g2] = (int32_t)(hbase + (long long)g2 * k);
+      if (lane == 0) {
+        if (run != k) set_error(ctl, DSV_ERR_INTERNAL, (unsigned int)((bh * G + g2) & 0x7fffffff));
+        a.fwd_ptr[bh * G + g2] = (int32_t)(hbase + (long long)g2 * k);
+        if (bh * G + g2 == a.rows - 1) a.fwd_ptr[a.rows] = a.nnz;
+      }
     }
-    if (row_ok && grow == a.rows - 1) a.fwd_ptr[a.rows] = a.nnz;
   }
 
   tc_fence_before();
@@ -565,9 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   if (warp == 1 && tmem_ok) tmem_dealloc(tmem_base, kNBuf * kChunk);
 }
 
-constexpr int kSelSmem = 1024 + 2 * kTileBytes + 2 * kNSlot * kTileBytes + kBins * kHS * 4 + kCand * kRows * 8 +
-                         (1 + 2 * kNSlot + 2 * kNBuf + 1) * 8 + 16;
+constexpr int kSelSmem = 1024 + 2 * kTileBytes + 2 * kNSlot * kTileBytes + kBins * kRows * 4 + kCand * kRows * 8 +
+                         kRows * (int)sizeof(RowShared) + (1 + 2 * kNSlot + 2 * kNBuf + 1) * 8 + 16;
 static_assert(kSelSmem <= 227 * 1024, "score/select tiles exceed shared memory");
+static_assert(kRadixBins * 4 <= kCand * 8, "the fallback's digit histograms must fit the candidate region");
 
 }  // namespace
 
