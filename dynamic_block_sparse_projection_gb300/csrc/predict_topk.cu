@@ -163,13 +163,22 @@ struct RowShared {
 // rows, or a row's 32 consecutive words, fall in 32 different banks)
 __device__ __forceinline__ int word_at(int wi, int r) { return wi * kRows + (r ^ (wi & 31)); }
 
+// Fire-and-forget add to a shared-memory counter (32-bit shared address).
+__device__ __forceinline__ void red_shared_add(uint32_t saddr, uint32_t v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+static_assert(kRows * 4 == 512, "histogram rows are 512 bytes apart (bin << 9)");
+
 __device__ __forceinline__ void sel_barrier() {
   asm volatile("bar.sync 1, %0;" ::"r"(kSelWarps * 32) : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_constant__ SelArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sbase = align_up_ptr<uint8_t>(smem_raw, 1024);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment by pointer arithmetic on the shared array itself, so
+  // that the compiler keeps every access below in the shared address space
+  // (a round trip through an integer would turn them into generic accesses)
+  uint8_t* sbase = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQh = sbase;
   uint8_t* sQl = sQh + kTileBytes;
   uint8_t* sKh = sQl + kTileBytes;                       // [kNSlot] tiles
@@ -334,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       // ---------------- selection: row r, columns cg*32 .. cg*32 + 31 of every tile ----------------
       const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
       uint32_t* hcol = hist + r;
+      const uint32_t hcol_s = smem_u32(hcol);            // shared address of this row's histogram column
       uint32_t n = gc;
       float shift = 0.f, s1 = 0.f, s2 = 0.f, cnt_n = 0.f;  // pass-0 partial moments of this thread's columns
       bool have_shift = false;
@@ -343,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
         // the fallback's digit histograms live in the candidate region, [bin][row]: the
         // histogram region now holds bitmask words, spread over other rows' columns
         uint32_t* fcol = reinterpret_cast<uint32_t*>(cand) + r;
+        const uint32_t fcol_s = smem_u32(fcol);
         if (fb && work && pass < kNumMain + kNumRadix)
           for (int i = 0; i < kRadixBins; ++i) fcol[i * kRows] = 0u;   // this digit's histogram
         for (int t = 0; t < ntiles(pass); ++t, ++n) {
@@ -384,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             } else if (pass == 1) {
 #pragma unroll
               for (int e = 0; e < 32; ++e)
-                if (FULL || e < nvg) atomicAdd(hcol + (bin_bits(__uint_as_float(x[e]), sc, c0) & (kBins - 1)) * kRows, 1u);
+                if (FULL || e < nvg)
+                  red_shared_add(hcol_s + ((bin_bits(__uint_as_float(x[e]), sc, c0) & (kBins - 1)) << 9), 1u);
               if (a.scores != nullptr) {
                 // check output: the scores this selection uses
                 float* dst = a.scores + grow * (long long)nb + j0;
@@ -434,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
               for (int e = 0; e < 32; ++e) {
                 if (FULL || e < nvg) {
                   const uint32_t u = order_key(__uint_as_float(x[e]));
-                  if ((u & hmask) == prefix) atomicAdd(fcol + ((u >> sh) & dmask) * kRows, 1u);
+                  if ((u & hmask) == prefix) red_shared_add(fcol_s + (((u >> sh) & dmask) << 9), 1u);
                 }
               }
             }
