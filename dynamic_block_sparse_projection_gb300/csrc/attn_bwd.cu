@@ -128,8 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NST = T::NST;
   constexpr int HALF = T::HALF;
   constexpr int W = T::W;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sbase = align_up_ptr<uint8_t>(smem_raw, 1024);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sbase = smem_align1024(smem_raw);
   uint8_t* sK = sbase;
   uint8_t* sV = sK + T::A_BYTES;
   uint8_t* sStage = sV + T::A_BYTES;              // NST x [Q_g | dO_g | lse2 | D]
@@ -453,8 +453,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
   using T = QTraits<BETA, D>;
   constexpr int NK = T::NK, NV = T::NV;
   constexpr int HALF = T::HALF;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sbase = align_up_ptr<uint8_t>(smem_raw, 1024);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sbase = smem_align1024(smem_raw);
   uint8_t* sdO = sbase;
   uint8_t* sQ = sdO + T::A_BYTES;
   uint8_t* sK = sQ + T::A_BYTES;

@@ -83,8 +83,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, Ctl ctl) {
   using T = FwdTraits<BETA, D>;
   constexpr int NST = T::NST;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sbase = align_up_ptr<uint8_t>(smem_raw, 1024);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sbase = smem_align1024(smem_raw);
   uint8_t* sQ = sbase;
   uint8_t* sK = sQ + T::Q_BYTES;
   uint8_t* sV = sK + NST * T::KV_BYTES;

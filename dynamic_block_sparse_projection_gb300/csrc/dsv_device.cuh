@@ -432,6 +432,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// The 1024-byte aligned start inside a dynamic shared-memory array, found by
+// pointer arithmetic on the array itself, so that the compiler keeps accesses
+// through it in the shared address space (ld/st/atom.shared); aligning through
+// an integer round trip turns them into generic accesses.
+__device__ __forceinline__ uint8_t* smem_align1024(uint8_t* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
 template <typename T>
 __device__ __forceinline__ T* align_up_ptr(void* p, uintptr_t a) {
   uintptr_t v = reinterpret_cast<uintptr_t>(p);

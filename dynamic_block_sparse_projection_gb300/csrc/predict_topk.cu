@@ -175,10 +175,7 @@ __device__ __forceinline__ void sel_barrier() {
 
 __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_constant__ SelArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // 1024-byte alignment by pointer arithmetic on the shared array itself, so
-  // that the compiler keeps every access below in the shared address space
-  // (a round trip through an integer would turn them into generic accesses)
-  uint8_t* sbase = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sbase = smem_align1024(smem_raw);             // accesses below stay in the shared space
   uint8_t* sQh = sbase;
   uint8_t* sQl = sQh + kTileBytes;
   uint8_t* sKh = sQl + kTileBytes;                       // [kNSlot] tiles
