@@ -57,7 +57,6 @@ constexpr int kColGroups = 4;           // threads per row: each takes 32 of a t
 constexpr int kSelWarp0 = 2;            // warps 2 .. 17 select
 constexpr int kSelWarps = 4 * kColGroups;
 constexpr int kThreads = 32 * (kSelWarp0 + kSelWarps);
-constexpr int kMomStride = 4;           // the moment pass reads every kMomStride-th tile of a row
 constexpr int kTileBytes = kRows * kRP * 4;   // one 128 x 32 fp32 operand tile (16 KB)
 constexpr int kNumMain = 3;             // passes 0..2
 constexpr int kNumRadix = 6;            // digit passes of the exact fallback (6, 6, 6, 6, 6, 2 bits)
@@ -149,11 +148,32 @@ __device__ __forceinline__ uint32_t bin_bits(float s, float sc, float c0) {
   return __float_as_uint(fminf(fmaxf(fmaf(s, sc, c0), kB0), kB1));
 }
 
+// inverse of order_key for the keys of numbers (not NaN)
+__device__ __forceinline__ float key_float(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
+// The largest value (+inf included) whose bin is at most `bin`.  bin_bits is
+// non-decreasing in its argument, so {s : bin(s) > bin} = {s : s > result}:
+// a pass can compare scores with this value instead of recomputing bins.
+// Binary search over the ordered keys of -inf .. +inf.
+__device__ float bin_upper(float sc, float c0, uint32_t bin) {
+  const uint32_t target = __float_as_uint(kB0) + bin;
+  uint32_t lo = 0x007fffffu, hi = 0xff800000u;          // keys of -inf and +inf
+  if (bin_bits(key_float(hi), sc, c0) <= target) return __uint_as_float(0x7f800000u);
+  while (hi - lo > 1u) {                                // bin(key_float(lo)) <= target < bin(key_float(hi))
+    const uint32_t mid = lo + ((hi - lo) >> 1);
+    if (bin_bits(key_float(mid), sc, c0) <= target) lo = mid;
+    else hi = mid;
+  }
+  return key_float(lo);
+}
+
 // Per-row state shared by the four threads of a row (shared memory).
 struct RowShared {
   float mom_n[kColGroups], mom_mean[kColGroups], mom_m2[kColGroups];   // pass-0 partial moments
-  uint32_t keep_above;   // bin bits: keep scores whose bin bits exceed this
-  uint32_t collect;      // bin bits of the bin whose scores are ranked exactly (none: 0xffffffff)
+  float keep_v;          // pass 2 keeps the scores above this value
+  float coll_v;          // and collects the scores in (coll_v, keep_v] for exact ranking
   uint32_t kk;           // how many of that bin are kept
   int ccount;            // scores collected from that bin so far
   int fail;              // the row needs the exact fallback
@@ -173,7 +193,7 @@ __device__ __forceinline__ void sel_barrier() {
   asm volatile("bar.sync 1, %0;" ::"r"(kSelWarps * 32) : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_constant__ SelArgs a) {
+__global__ void __maxnreg__(112) score_select_kernel(const __grid_constant__ SelArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sbase = smem_align1024(smem_raw);             // accesses below stay in the shared space
   uint8_t* sQh = sbase;
@@ -204,7 +224,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   const int h = (int)(bh % a.H), b = (int)(bh / a.H);
   const int k = a.hk.k[h];
   const int nc = (nb + kChunk - 1) / kChunk;             // score tiles of a row
-  const int nc0 = (nc + kMomStride - 1) / kMomStride;    // tiles of the moment pass (every kMomStride-th)
   const bool select_all = k >= nb;                       // k = nb: every block, nothing to score
 
   // selection threads: row r (tensor-memory lane) and column group cg of each 128-column tile
@@ -251,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
 
   // per-thread row state
   float sc = 0.f, c0 = kB0;                              // bin map
-  uint32_t keep_above = 0u, collect = 0xffffffffu;
+  float keep_v = 0.f, coll_v = __uint_as_float(0x7f800000u);
   bool fail = false;
   uint32_t prefix = 0u, hmask = 0u, rk = 0u;             // exact fallback (column group 0)
 
@@ -260,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   uint32_t issued_k = 0;
   bool ok = tmem_ok;
 
-  auto ntiles = [&](int pass) { return pass == 0 ? nc0 : nc; };
-  auto tile_of = [&](int pass, int t) { return pass == 0 ? t * kMomStride : t; };
+  auto ntiles = [&](int pass) { return nc; };
+  auto tile_of = [&](int pass, int t) { return t; };
 
   // One run of passes pass0 .. pass0 + npass - 1 over the score tiles; every
   // role walks the same tiles, so barrier phases follow gc.
@@ -353,20 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
         const uint32_t fcol_s = smem_u32(fcol);
         if (fb && work && pass < kNumMain + kNumRadix)
           for (int i = 0; i < kRadixBins; ++i) fcol[i * kRows] = 0u;   // this digit's histogram
-        for (int t = 0; t < ntiles(pass); ++t, ++n) {
-          const int buf = (int)(n % kNBuf);
-          const int c = tile_of(pass, t);
-          // after an abort the warp keeps walking the passes without waiting or
-          // working, so that it still reaches every named barrier below
-          if (!ok) continue;
-          if (!mbar_wait_warp(&s_full[buf], (n / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
-            ok = false;
-            continue;
-          }
-          tc_fence_after();
-          const int nv = min(kChunk, nb - c * kChunk);   // valid columns of this tile (uniform)
-          // the 32 scores of column group q of this tile (columns j0 .. j0 + 31, the first nvg valid)
-          auto proc = [&](const uint32_t (&x)[32], int q, auto full_tag) {
+        const int nt = ntiles(pass);
+        // the 32 scores of column group q of tile c (columns j0 .. j0 + 31, the first nvg valid)
+          auto proc = [&](const uint32_t (&x)[32], int c, int nv, int q, auto full_tag) {
             constexpr bool FULL = decltype(full_tag)::value;
             const int j0 = c * kChunk + q * 32;
             const int nvg = nv - q * 32;
@@ -406,9 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
 #pragma unroll
               for (int e = 0; e < 32; ++e) {
                 if (FULL || e < nvg) {
-                  const uint32_t bb = bin_bits(__uint_as_float(x[e]), sc, c0);
-                  word |= (bb > keep_above ? 1u : 0u) << e;
-                  eq |= (bb == collect ? 1u : 0u) << e;
+                  const float s = __uint_as_float(x[e]);
+                  const bool kp = s > keep_v;
+                  word |= (kp ? 1u : 0u) << e;
+                  eq |= (!kp && s > coll_v ? 1u : 0u) << e;
                 }
               }
               hist[word_at(wi, r)] = word;
@@ -448,33 +457,73 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
               }
             }
           };
-          auto run_group = [&](const uint32_t (&x)[32], int q) {
-            if (nv - q * 32 >= 32) proc(x, q, std::true_type{});
-            else if (nv - q * 32 > 0) proc(x, q, std::false_type{});
+          auto run_group = [&](const uint32_t (&x)[32], int c, int q) {
+            const int nv = min(kChunk, nb - c * kChunk);   // valid columns of tile c (uniform)
+            if (nv - q * 32 >= 32) proc(x, c, nv, q, std::true_type{});
+            else if (nv - q * 32 > 0) proc(x, c, nv, q, std::false_type{});
           };
-          const uint32_t tb = tmem_base + lane_off + (uint32_t)buf * kChunk;
-          if (!fb) {
-            uint32_t x[32];
-            tmem_ld32(tb + (uint32_t)cg * 32, x);
+        auto tile_addr = [&](uint32_t nn) { return tmem_base + lane_off + (uint32_t)(nn % kNBuf) * kChunk; };
+        if (!fb) {
+          // every thread its own 32 columns; the tensor-memory load of tile t + 1 is
+          // in flight while tile t is processed.  After an abort the warp still
+          // walks the pass (no waits, no work) so that it reaches the barriers below.
+          uint32_t xa[32], xb[32];
+          if (ok && nt > 0) {
+            if (mbar_wait_warp(&s_full[n % kNBuf], (n / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
+              tc_fence_after();
+              tmem_ld32(tile_addr(n) + (uint32_t)cg * 32, xa);
+            } else {
+              ok = false;
+            }
+          }
+          auto step = [&](uint32_t (&cur)[32], uint32_t (&nxt)[32], int t) {
+            const uint32_t nn = n + (uint32_t)t;
+            if (!ok) return;
             tmem_ld_wait();
             tc_fence_before();
-            mbar_arrive(&t_free[buf]);
-            if (work) run_group(x, cg);
-          } else if (cg == 0) {
-            // the fallback row's four column groups, in order, by one thread
-#pragma unroll 1
-            for (int q = 0; q < kColGroups; ++q) {
-              uint32_t x[32];
-              tmem_ld32(tb + (uint32_t)q * 32, x);
-              tmem_ld_wait();
-              if (q == kColGroups - 1) {
-                tc_fence_before();
-                mbar_arrive(&t_free[buf]);
+            mbar_arrive(&t_free[nn % kNBuf]);
+            if (t + 1 < nt) {
+              if (mbar_wait_warp(&s_full[(nn + 1) % kNBuf], ((nn + 1) / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
+                tc_fence_after();
+                tmem_ld32(tile_addr(nn + 1) + (uint32_t)cg * 32, nxt);
+              } else {
+                ok = false;
+                return;
               }
-              if (work) run_group(x, q);
             }
-          } else {
-            mbar_arrive(&t_free[buf]);
+            if (work) run_group(cur, tile_of(pass, t), cg);
+          };
+#pragma unroll 1
+          for (int t = 0; t < nt; t += 2) {
+            step(xa, xb, t);
+            if (t + 1 < nt) step(xb, xa, t + 1);
+          }
+          n += (uint32_t)nt;
+        } else {
+          for (int t = 0; t < nt; ++t, ++n) {
+            if (!ok) continue;
+            const int buf = (int)(n % kNBuf);
+            if (!mbar_wait_warp(&s_full[buf], (n / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
+              ok = false;
+              continue;
+            }
+            tc_fence_after();
+            if (cg == 0) {
+              // the fallback row's four column groups, in order, by one thread
+#pragma unroll 1
+              for (int q = 0; q < kColGroups; ++q) {
+                uint32_t x[32];
+                tmem_ld32(tile_addr(n) + (uint32_t)q * 32, x);
+                tmem_ld_wait();
+                if (q == kColGroups - 1) {
+                  tc_fence_before();
+                  mbar_arrive(&t_free[buf]);
+                }
+                if (work) run_group(x, t, q);
+              }
+            } else {
+              mbar_arrive(&t_free[buf]);
+            }
           }
         }
         // ---- end of a pass ----
@@ -522,27 +571,28 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
               above += ci;
             }
             const uint32_t kk = (uint32_t)k - above;
-            const uint32_t bsbits = __float_as_uint(kB0) + bstar;
             rs[r].kk = kk;
+            // value bounds of bin b*: (below, top]
+            const float below = bstar > 0u ? bin_upper(sc, c0, bstar - 1u) : __uint_as_float(0xff800000u);
             if (cnt == kk) {
-              rs[r].keep_above = bsbits - 1u;            // the whole bin is kept
-              rs[r].collect = 0xffffffffu;
+              rs[r].keep_v = below;                      // the whole bin is kept
+              rs[r].coll_v = __uint_as_float(0x7f800000u);
             } else {
-              rs[r].keep_above = bsbits;
-              rs[r].collect = bsbits;
+              rs[r].keep_v = bin_upper(sc, c0, bstar);
+              rs[r].coll_v = below;
               rs[r].fail = cnt > (uint32_t)kCand ? 1 : 0;
             }
           }
           sel_barrier();                                 // decisions out; the histogram region becomes words
           if (row_ok) {
-            keep_above = rs[r].keep_above;
-            collect = rs[r].collect;
+            keep_v = rs[r].keep_v;
+            coll_v = rs[r].coll_v;
             fail = rs[r].fail != 0;
           }
         } else if (pass == 2) {
           sel_barrier();                                 // every word and candidate of the row is in
           if (row_ok && cg == 0) {
-            if (collect != 0xffffffffu && !fail) {
+            if (coll_v < __uint_as_float(0x7f800000u) && !fail) {
               // rank the threshold bin's scores exactly and add the kept ones to the bitmask
               const int n2 = min(rs[r].ccount, kCand);
               const uint32_t kk = rs[r].kk;
