@@ -61,6 +61,7 @@ constexpr int kTileBytes = kRows * kRP * 4;   // one 128 x 32 fp32 operand tile 
 constexpr int kNumMain = 3;             // passes 0..2
 constexpr int kNumRadix = 6;            // digit passes of the exact fallback (6, 6, 6, 6, 6, 2 bits)
 constexpr int kRadixBins = 64;
+constexpr int kFallbackDigit = -1;      // compile-time tag of the fallback's digit passes
 // digit dp of a 32-bit key: bits [shift, shift + width) counted from the top
 __host__ __device__ constexpr int radix_bits(int dp) { return dp < 5 ? 6 : 2; }
 __host__ __device__ constexpr int radix_shift(int dp) { return dp < 5 ? 26 - 6 * dp : 0; }
@@ -193,7 +194,7 @@ __device__ __forceinline__ void sel_barrier() {
   asm volatile("bar.sync 1, %0;" ::"r"(kSelWarps * 32) : "memory");
 }
 
-__global__ void __maxnreg__(112) score_select_kernel(const __grid_constant__ SelArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_constant__ SelArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sbase = smem_align1024(smem_raw);             // accesses below stay in the shared space
   uint8_t* sQh = sbase;
@@ -374,12 +375,14 @@ __global__ void __maxnreg__(112) score_select_kernel(const __grid_constant__ Sel
           for (int i = 0; i < kRadixBins; ++i) fcol[i * kRows] = 0u;   // this digit's histogram
         const int nt = ntiles(pass);
         // the 32 scores of column group q of tile c (columns j0 .. j0 + 31, the first nvg valid)
-          auto proc = [&](const uint32_t (&x)[32], int c, int nv, int q, auto full_tag) {
+          // P: the pass, known at compile time (kFallbackDigit: one of the fallback's digit passes)
+          auto proc = [&](const uint32_t (&x)[32], int c, int nv, int q, auto full_tag, auto pass_tag) {
             constexpr bool FULL = decltype(full_tag)::value;
+            constexpr int P = decltype(pass_tag)::value;
             const int j0 = c * kChunk + q * 32;
             const int nvg = nv - q * 32;
             const int wi = j0 >> 5;                       // bitmask word of these 32 columns
-            if (pass == 0) {
+            if constexpr (P == 0) {
               if (!have_shift) {
                 shift = __uint_as_float(x[0]);
                 have_shift = true;
@@ -397,7 +400,7 @@ __global__ void __maxnreg__(112) score_select_kernel(const __grid_constant__ Sel
               s1 += a0 + a1;
               s2 += b0 + b1;
               cnt_n += (float)(FULL ? 32 : nvg);
-            } else if (pass == 1) {
+            } else if constexpr (P == 1) {
 #pragma unroll
               for (int e = 0; e < 32; ++e)
                 if (FULL || e < nvg)
@@ -409,7 +412,7 @@ __global__ void __maxnreg__(112) score_select_kernel(const __grid_constant__ Sel
                 for (int e = 0; e < 32; ++e)
                   if (FULL || e < nvg) dst[e] = __uint_as_float(x[e]);
               }
-            } else if (pass == 2) {
+            } else if constexpr (P == 2) {
               uint32_t word = 0u, eq = 0u;
 #pragma unroll
               for (int e = 0; e < 32; ++e) {
@@ -430,7 +433,7 @@ __global__ void __maxnreg__(112) score_select_kernel(const __grid_constant__ Sel
                   }
                 }
               }
-            } else if (pass == kNumMain + kNumRadix) {
+            } else if constexpr (P == kNumMain + kNumRadix) {
               // exact fallback, emit: keys above T, then keys equal to T lowest index first
               uint32_t word = 0u;
 #pragma unroll
@@ -457,48 +460,36 @@ __global__ void __maxnreg__(112) score_select_kernel(const __grid_constant__ Sel
               }
             }
           };
-          auto run_group = [&](const uint32_t (&x)[32], int c, int q) {
+          auto run_group = [&](const uint32_t (&x)[32], int c, int q, auto pass_tag) {
             const int nv = min(kChunk, nb - c * kChunk);   // valid columns of tile c (uniform)
-            if (nv - q * 32 >= 32) proc(x, c, nv, q, std::true_type{});
-            else if (nv - q * 32 > 0) proc(x, c, nv, q, std::false_type{});
+            if (nv - q * 32 >= 32) proc(x, c, nv, q, std::true_type{}, pass_tag);
+            else if (nv - q * 32 > 0) proc(x, c, nv, q, std::false_type{}, pass_tag);
           };
         auto tile_addr = [&](uint32_t nn) { return tmem_base + lane_off + (uint32_t)(nn % kNBuf) * kChunk; };
-        if (!fb) {
-          // every thread its own 32 columns; the tensor-memory load of tile t + 1 is
-          // in flight while tile t is processed.  After an abort the warp still
-          // walks the pass (no waits, no work) so that it reaches the barriers below.
-          uint32_t xa[32], xb[32];
-          if (ok && nt > 0) {
-            if (mbar_wait_warp(&s_full[n % kNBuf], (n / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
-              tc_fence_after();
-              tmem_ld32(tile_addr(n) + (uint32_t)cg * 32, xa);
-            } else {
+        auto main_tiles = [&](auto pass_tag) {
+          // every thread its own 32 columns of each tile.  After an abort the warp
+          // still walks the pass (no waits, no work) so that it reaches the barriers below.
+#pragma unroll 1
+          for (int t = 0; t < nt; ++t, ++n) {
+            if (!ok) continue;
+            const int buf = (int)(n % kNBuf);
+            if (!mbar_wait_warp(&s_full[buf], (n / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
               ok = false;
+              continue;
             }
-          }
-          auto step = [&](uint32_t (&cur)[32], uint32_t (&nxt)[32], int t) {
-            const uint32_t nn = n + (uint32_t)t;
-            if (!ok) return;
+            tc_fence_after();
+            uint32_t x[32];
+            tmem_ld32(tile_addr(n) + (uint32_t)cg * 32, x);
             tmem_ld_wait();
             tc_fence_before();
-            mbar_arrive(&t_free[nn % kNBuf]);
-            if (t + 1 < nt) {
-              if (mbar_wait_warp(&s_full[(nn + 1) % kNBuf], ((nn + 1) / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
-                tc_fence_after();
-                tmem_ld32(tile_addr(nn + 1) + (uint32_t)cg * 32, nxt);
-              } else {
-                ok = false;
-                return;
-              }
-            }
-            if (work) run_group(cur, tile_of(pass, t), cg);
-          };
-#pragma unroll 1
-          for (int t = 0; t < nt; t += 2) {
-            step(xa, xb, t);
-            if (t + 1 < nt) step(xb, xa, t + 1);
+            mbar_arrive(&t_free[buf]);
+            if (work) run_group(x, tile_of(pass, t), cg, pass_tag);
           }
-          n += (uint32_t)nt;
+        };
+        if (!fb) {
+          if (pass == 0) main_tiles(std::integral_constant<int, 0>{});
+          else if (pass == 1) main_tiles(std::integral_constant<int, 1>{});
+          else main_tiles(std::integral_constant<int, 2>{});
         } else {
           for (int t = 0; t < nt; ++t, ++n) {
             if (!ok) continue;
@@ -519,7 +510,10 @@ __global__ void __maxnreg__(112) score_select_kernel(const __grid_constant__ Sel
                   tc_fence_before();
                   mbar_arrive(&t_free[buf]);
                 }
-                if (work) run_group(x, t, q);
+                if (work) {
+                  if (pass == kNumMain + kNumRadix) run_group(x, t, q, std::integral_constant<int, kNumMain + kNumRadix>{});
+                  else run_group(x, t, q, std::integral_constant<int, kFallbackDigit>{});
+                }
               }
             } else {
               mbar_arrive(&t_free[buf]);
