@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
     }
     for (int s = 0; s < kNBuf; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&t_free[s], kSelWarps * 32);
+      mbar_init(&t_free[s], 4 * 32);                   // the four warps of the group that reads the tile
     }
     mbar_init(mma_drain, 1);
     *abort_flag = 0;
@@ -467,24 +467,34 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
           };
         auto tile_addr = [&](uint32_t nn) { return tmem_base + lane_off + (uint32_t)(nn % kNBuf) * kChunk; };
         auto main_tiles = [&](auto pass_tag) {
-          // every thread its own 32 columns of each tile.  After an abort the warp
-          // still walks the pass (no waits, no work) so that it reaches the barriers below.
+          // tile t belongs to column group t % kColGroups: its four warps read all
+          // 128 columns, so the warps sharing a scheduler (same lane quarter,
+          // different groups) work on different tiles and hide each other's
+          // latencies.  After an abort the warp still walks the pass (no waits, no
+          // work) so that it reaches the barriers below.
 #pragma unroll 1
-          for (int t = 0; t < nt; ++t, ++n) {
+          for (int t = cg; t < nt; t += kColGroups) {
+            const uint32_t nn = n + (uint32_t)t;
             if (!ok) continue;
-            const int buf = (int)(n % kNBuf);
-            if (!mbar_wait_warp(&s_full[buf], (n / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
+            const int buf = (int)(nn % kNBuf);
+            if (!mbar_wait_warp(&s_full[buf], (nn / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
               ok = false;
               continue;
             }
             tc_fence_after();
-            uint32_t x[32];
-            tmem_ld32(tile_addr(n) + (uint32_t)cg * 32, x);
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&t_free[buf]);
-            if (work) run_group(x, tile_of(pass, t), cg, pass_tag);
+#pragma unroll 1
+            for (int q = 0; q < kColGroups; ++q) {
+              uint32_t x[32];
+              tmem_ld32(tile_addr(nn) + (uint32_t)q * 32, x);
+              tmem_ld_wait();
+              if (q == kColGroups - 1) {
+                tc_fence_before();
+                mbar_arrive(&t_free[buf]);
+              }
+              if (work) run_group(x, tile_of(pass, t), q, pass_tag);
+            }
           }
+          n += (uint32_t)nt;
         };
         if (!fb) {
           if (pass == 0) main_tiles(std::integral_constant<int, 0>{});
@@ -492,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
           else main_tiles(std::integral_constant<int, 2>{});
         } else {
           for (int t = 0; t < nt; ++t, ++n) {
-            if (!ok) continue;
+            if (!ok || cg != 0) continue;              // column group 0 reads every tile of a fallback pass
             const int buf = (int)(n % kNBuf);
             if (!mbar_wait_warp(&s_full[buf], (n / kNBuf) & 1u, abort_flag, ctl, kid | W_SF)) {
               ok = false;
@@ -515,8 +525,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
                   else run_group(x, t, q, std::integral_constant<int, kFallbackDigit>{});
                 }
               }
-            } else {
-              mbar_arrive(&t_free[buf]);
             }
           }
         }
