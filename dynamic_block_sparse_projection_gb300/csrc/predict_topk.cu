@@ -143,10 +143,26 @@ __global__ void __launch_bounds__(256) split_tf32_kernel(const float* __restrict
 // Score tiles on the tensor cores, selection one row per thread
 // ---------------------------------------------------------------------------
 constexpr float kB0 = 12582912.0f;      // 1.5 * 2^23: adding it leaves round(x) in the low mantissa bits
-constexpr float kB1 = kB0 + (float)(kBins - 1);
 
+// fma with the result clamped to [0, 1] (one instruction)
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+  float d;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// all ones where a > b, else zero (one instruction)
+__device__ __forceinline__ uint32_t gt_mask(float a, float b) {
+  uint32_t d;
+  asm("set.gt.u32.f32 %0, %1, %2;" : "=r"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// The bin map of a row: z = clamp(s * sc + c0, 0, 1) (scores below the binned
+// range give 0, above it 1), bin = round(127 z), returned as the float bits
+// B0 + bin (adding 1.5 * 2^23 leaves the rounded value in the low mantissa
+// bits).  Two fma, both non-decreasing in s, so the map is monotone.
 __device__ __forceinline__ uint32_t bin_bits(float s, float sc, float c0) {
-  return __float_as_uint(fminf(fmaxf(fmaf(s, sc, c0), kB0), kB1));
+  return __float_as_uint(fmaf(fma_sat(s, sc, c0), (float)(kBins - 1), kB0));
 }
 
 // inverse of order_key for the keys of numbers (not NaN)
@@ -270,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   if (!tmem_ok && threadIdx.x == 0) set_error(ctl, DSV_ERR_INTERNAL, blockIdx.x);
 
   // per-thread row state
-  float sc = 0.f, c0 = kB0;                              // bin map
+  float sc = 0.f, c0 = 0.f;                              // bin map
   float keep_v = 0.f, coll_v = __uint_as_float(0x7f800000u);
   bool fail = false;
   uint32_t prefix = 0u, hmask = 0u, rk = 0u;             // exact fallback (column group 0)
@@ -361,6 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
       uint32_t* hcol = hist + r;
       const uint32_t hcol_s = smem_u32(hcol);            // shared address of this row's histogram column
+      // address of bin b from the bin bits B0 + b: ((B0 + b) << 9) = (B0 << 9) + 512 b (mod 2^32)
+      const uint32_t hbase = hcol_s - (__float_as_uint(kB0) << 9);
       uint32_t n = gc;
       float shift = 0.f, s1 = 0.f, s2 = 0.f, cnt_n = 0.f;  // pass-0 partial moments of this thread's columns
       bool have_shift = false;
@@ -387,16 +405,20 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
                 shift = __uint_as_float(x[0]);
                 have_shift = true;
               }
-              float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+              // sums of d = s - shift and d^2 on packed fp32 pairs
+              uint64_t acc = f2_pack(0.f, 0.f), acq = f2_pack(0.f, 0.f);
+              const uint64_t nsh = f2_pack(-shift, -shift);
 #pragma unroll
               for (int e = 0; e < 32; e += 2) {
-                const float d0 = (FULL || e < nvg) ? __uint_as_float(x[e]) - shift : 0.f;
-                const float d1 = (FULL || e + 1 < nvg) ? __uint_as_float(x[e + 1]) - shift : 0.f;
-                a0 += d0;
-                a1 += d1;
-                b0 = fmaf(d0, d0, b0);
-                b1 = fmaf(d1, d1, b1);
+                const float x0 = (FULL || e < nvg) ? __uint_as_float(x[e]) : shift;
+                const float x1 = (FULL || e + 1 < nvg) ? __uint_as_float(x[e + 1]) : shift;
+                const uint64_t d = add2(f2_pack(x0, x1), nsh);
+                acc = add2(acc, d);
+                acq = fma2(d, d, acq);
               }
+              float a0, a1, b0, b1;
+              f2_unpack(acc, a0, a1);
+              f2_unpack(acq, b0, b1);
               s1 += a0 + a1;
               s2 += b0 + b1;
               cnt_n += (float)(FULL ? 32 : nvg);
@@ -404,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
 #pragma unroll
               for (int e = 0; e < 32; ++e)
                 if (FULL || e < nvg)
-                  red_shared_add(hcol_s + ((bin_bits(__uint_as_float(x[e]), sc, c0) & (kBins - 1)) << 9), 1u);
+                  red_shared_add(hbase + (bin_bits(__uint_as_float(x[e]), sc, c0) << 9), 1u);
               if (a.scores != nullptr) {
                 // check output: the scores this selection uses
                 float* dst = a.scores + grow * (long long)nb + j0;
@@ -413,16 +435,18 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
                   if (FULL || e < nvg) dst[e] = __uint_as_float(x[e]);
               }
             } else if constexpr (P == 2) {
-              uint32_t word = 0u, eq = 0u;
+              // word: scores above keep_v; above: scores above coll_v (a superset);
+              // the threshold bin's scores are the difference
+              uint32_t word = 0u, above = 0u;
 #pragma unroll
               for (int e = 0; e < 32; ++e) {
                 if (FULL || e < nvg) {
                   const float s = __uint_as_float(x[e]);
-                  const bool kp = s > keep_v;
-                  word |= (kp ? 1u : 0u) << e;
-                  eq |= (!kp && s > coll_v ? 1u : 0u) << e;
+                  word |= gt_mask(s, keep_v) & (1u << e);
+                  above |= gt_mask(s, coll_v) & (1u << e);
                 }
               }
+              const uint32_t eq = above & ~word;
               hist[word_at(wi, r)] = word;
               if (eq) {
 #pragma unroll
@@ -552,11 +576,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             const float sd = nn > 0.f ? sqrtf(m2 / nn) : 0.f;
             const float zk = normcdfinvf(1.0f - (float)k / (float)nb);
             const float lo = mean + (zk - kZHalf) * sd;
-            sc = (float)(kBins - 1) / (2.0f * kZHalf * sd);
-            c0 = kB0 - lo * sc;
+            sc = 1.0f / (2.0f * kZHalf * sd);
+            c0 = -lo * sc;
             if (!(sc > 0.f && sc < 1e30f && isfinite(c0) && isfinite(zk))) {
               sc = 0.f;                                  // one bin: the exact fallback decides
-              c0 = kB0;
+              c0 = 0.f;
             }
           }
         } else if (pass == 1) {
