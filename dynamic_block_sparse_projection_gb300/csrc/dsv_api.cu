@@ -315,7 +315,7 @@ dsv_status dsv_predict_topk_blocks(const void* Q, const void* K, const float* Wq
   cudaError_t e = launch_pool_project(Q, K, Wq, Wk, s, qp, kp, st);
   if (e == cudaSuccess) e = launch_split_tf32(qp, kp, s, split, st);
   if (e == cudaSuccess)
-    e = launch_score_select(maps, s, hk, nnz, fwd_ptr, fwd_col, static_cast<uint32_t*>(tws), scores, ctl, st);
+    e = launch_score_select(maps, s, hk, nnz, fwd_ptr, fwd_col, static_cast<uint32_t*>(tws), scores, split, ctl, st);
   if (e == cudaSuccess) e = launch_topk_transpose(s, hk, nnz, bwd_ptr, bwd_col, tws, st);
   return from_cuda(e);
 }

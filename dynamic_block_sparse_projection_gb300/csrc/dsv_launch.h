@@ -46,14 +46,15 @@ cudaError_t launch_pool_project(const void* Q, const void* K, const float* Wq, c
 // selects each group's top k without writing the score matrix (unless
 // `scores` is given); the forward lists and the selection bitmask (in the
 // top-k workspace layout) come out of it.  `split` holds 4 arrays of
-// [B*H*G, 32] fp32 (q hi, q lo, k hi, k lo), each 256-byte aligned.
+// [B*H*G, 32] fp32 (q hi, q lo, k hi, k lo), then the per-head key statistics
+// (partial sums, then mean and covariance), each part 256-byte aligned.
 struct PredictTopkMaps {
   CUtensorMap qh, ql, kh, kl;
 };
 cudaError_t launch_split_tf32(const float* qp, const float* kp, const dsv_shape& s, float* split, cudaStream_t st);
 cudaError_t launch_score_select(const PredictTopkMaps& maps, const dsv_shape& s, const HeadK& hk, int64_t nnz,
-                                int32_t* fwd_ptr, int32_t* fwd_col, uint32_t* mask, float* scores, const Ctl& ctl,
-                                cudaStream_t st);
+                                int32_t* fwd_ptr, int32_t* fwd_col, uint32_t* mask, float* scores, const float* split,
+                                const Ctl& ctl, cudaStream_t st);
 size_t split_tf32_bytes(const dsv_shape& s);
 // Mass-threshold selection: per row the smallest top set carrying >= tau of
 // the predicted softmax mass (temperature * scores), clamped to [kmin, kmax].

@@ -8,6 +8,7 @@
 //
 //   split_tf32_kernel   every pooled vector x becomes x_hi = tf32(x) and
 //                       x_lo = tf32(x - x_hi), zero-padded to 32 rank columns.
+//   kstats_*_kernel     per head, the mean and covariance of the pooled keys.
 //   score_select_kernel one CTA per (b, h) and 128 consecutive groups.  The
 //                       score tile S[g, j] = qbar_g . kbar_j of 128 groups x
 //                       128 key blocks is q_hi k_hi + q_hi k_lo + q_lo k_hi:
@@ -20,7 +21,8 @@
 //                       warps owns group row r (its tensor-memory lane) and
 //                       selects that row's top k alone, with no CTA-wide
 //                       reductions:
-//     pass 0  mean and variance of the row;
+//     pass 0  mean and variance of the row, in closed form from the query's
+//             pooled vector and the head's key mean and covariance (no tiles);
 //     pass 1  a 128-bin histogram of the row over mean + (z_k -+ 1) sd, z_k
 //             the normal quantile of 1 - k/nb (bins clamp at both ends, so the
 //             range only decides how many scores share a bin, never which are
@@ -58,7 +60,9 @@ constexpr int kSelWarp0 = 2;            // warps 2 .. 17 select
 constexpr int kSelWarps = 4 * kColGroups;
 constexpr int kThreads = 32 * (kSelWarp0 + kSelWarps);
 constexpr int kTileBytes = kRows * kRP * 4;   // one 128 x 32 fp32 operand tile (16 KB)
-constexpr int kNumMain = 3;             // passes 0..2
+constexpr int kNumMain = 3;             // passes 0..2 (pass 0: the row moments, in closed form, no tiles)
+constexpr int kKStatSplits = 16;
+constexpr int kKStat = kRP + kRP * kRP;   // per head: mu[32], then C[32][32]
 constexpr int kNumRadix = 6;            // digit passes of the exact fallback (6, 6, 6, 6, 6, 2 bits)
 constexpr int kRadixBins = 64;
 constexpr int kFallbackDigit = -1;      // compile-time tag of the fallback's digit passes
@@ -78,6 +82,7 @@ struct SelArgs {
   int32_t* fwd_col;
   uint32_t* mask;                      // [B*H][words][G]
   float* scores;                       // optional [B*H*G, G]: the scores the selection used
+  const float* kstats;                 // [B*H][kKStat]: mu and C of the pooled keys of each head
   HeadK hk;
   Ctl ctl;
 };
@@ -140,6 +145,67 @@ __global__ void __launch_bounds__(256) split_tf32_kernel(const float* __restrict
 }
 
 // ---------------------------------------------------------------------------
+// Per-head statistics of the pooled keys: the mean and covariance of a row of
+// scores are closed forms of them, S[g, .] = qbar_g . kbar_.:
+//   mean_j S[g, j] = qbar_g . mu,   var_j S[g, j] = qbar_g^T C qbar_g,
+// with mu the mean and C the covariance of the kbar_j over the row's nb key
+// blocks.  Sums are taken about the head's first key block (shifted data) in
+// fixed order: kKStatSplits partial sums per head, then one reduction.
+// ---------------------------------------------------------------------------
+
+// grid: (B*H, kKStatSplits), 1024 threads: thread (i, j) = (t / 32, t % 32)
+__global__ void __launch_bounds__(1024) kstats_partial_kernel(const float* __restrict__ kp, int r, int G,
+                                                              float* __restrict__ part) {
+  __shared__ float tile[128][kRP + 1];
+  __shared__ float k0[kRP];
+  const long long bh = blockIdx.x;
+  const int t = threadIdx.x, i = t >> 5, j = t & 31;
+  const float* K = kp + bh * G * (long long)r;
+  const int per = (G + kKStatSplits - 1) / kKStatSplits;
+  const int g_begin = blockIdx.y * per, g_end = min(G, g_begin + per);
+  if (t < kRP) k0[t] = t < r ? K[t] : 0.f;
+  float acc = 0.f, si = 0.f;
+  for (int g0 = g_begin; g0 < g_end; g0 += 128) {
+    __syncthreads();
+    for (int e = t; e < 128 * kRP; e += 1024) {
+      const int row = e / kRP, c = e % kRP;
+      tile[row][c] = (g0 + row < g_end && c < r) ? K[(long long)(g0 + row) * r + c] - k0[c] : 0.f;
+    }
+    __syncthreads();
+    const int nrow = min(128, g_end - g0);
+    for (int row = 0; row < nrow; ++row) {
+      const float a = tile[row][i];
+      acc = fmaf(a, tile[row][j], acc);
+      si += a;
+    }
+  }
+  float* P = part + (bh * kKStatSplits + blockIdx.y) * (long long)kKStat;
+  if (j == 0) P[i] = si;
+  P[kRP + i * kRP + j] = acc;
+}
+
+// grid: B*H, 1024 threads: mu and C of each head from its partial sums
+__global__ void __launch_bounds__(1024) kstats_reduce_kernel(const float* __restrict__ kp, int r, int G,
+                                                             const float* __restrict__ part, float* __restrict__ stats) {
+  __shared__ float s[kRP];
+  const long long bh = blockIdx.x;
+  const int t = threadIdx.x, i = t >> 5, j = t & 31;
+  const float* P = part + bh * kKStatSplits * (long long)kKStat;
+  float acc = 0.f, si = 0.f;
+  for (int q = 0; q < kKStatSplits; ++q) {
+    acc += P[q * kKStat + kRP + i * kRP + j];
+    if (j == 0) si += P[q * kKStat + i];
+  }
+  if (j == 0) s[i] = si;
+  __syncthreads();
+  const float inv = 1.0f / (float)G;
+  const float mi = s[i] * inv, mj = s[j] * inv;
+  float* S = stats + bh * (long long)kKStat;
+  S[kRP + i * kRP + j] = acc * inv - mi * mj;
+  if (j == 0) S[i] = (i < r ? kp[bh * G * (long long)r + i] : 0.f) + mi;
+}
+
+// ---------------------------------------------------------------------------
 // Score tiles on the tensor cores, selection one row per thread
 // ---------------------------------------------------------------------------
 constexpr float kB0 = 12582912.0f;      // 1.5 * 2^23: adding it leaves round(x) in the low mantissa bits
@@ -188,7 +254,7 @@ __device__ float bin_upper(float sc, float c0, uint32_t bin) {
 
 // Per-row state shared by the four threads of a row (shared memory).
 struct RowShared {
-  float mom_n[kColGroups], mom_mean[kColGroups], mom_m2[kColGroups];   // pass-0 partial moments
+  float mom_mean[kColGroups], mom_m2[kColGroups];   // pass 0: the four threads' parts of the mean and variance
   float keep_v;          // pass 2 keeps the scores above this value
   float coll_v;          // and collects the scores in (coll_v, keep_v] for exact ranking
   uint32_t kk;           // how many of that bin are kept
@@ -221,7 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   uint32_t* hist = reinterpret_cast<uint32_t*>(sKl + kNSlot * kTileBytes);
   uint2* cand = reinterpret_cast<uint2*>(hist + kBins * kRows);             // [kCand][kRows]
   RowShared* rs = reinterpret_cast<RowShared*>(cand + kCand * kRows);      // [kRows]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rs + kRows);
+  float* kst = reinterpret_cast<float*>(rs + kRows);                       // [kKStat]: mu, C of this head
+  uint64_t* bars = reinterpret_cast<uint64_t*>(kst + kKStat);
   uint64_t* q_full = bars;
   uint64_t* k_full = q_full + 1;
   uint64_t* k_free = k_full + kNSlot;
@@ -268,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
     fence_mbar_init();
   }
   if (sel) {
+    for (int i = threadIdx.x - kSelWarp0 * 32; i < kKStat; i += kSelWarps * 32) kst[i] = a.kstats[bh * kKStat + i];
     for (int i = cg * (kBins / kColGroups); i < (cg + 1) * (kBins / kColGroups); ++i) hist[i * kRows + r] = 0u;
     if (cg == 0) {
       rs[r].ccount = 0;
@@ -296,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   uint32_t issued_k = 0;
   bool ok = tmem_ok;
 
-  auto ntiles = [&](int pass) { return nc; };
+  auto ntiles = [&](int pass) { return pass == 0 ? 0 : nc; };     // pass 0: closed-form moments
   auto tile_of = [&](int pass, int t) { return t; };
 
   // One run of passes pass0 .. pass0 + npass - 1 over the score tiles; every
@@ -380,8 +448,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       // address of bin b from the bin bits B0 + b: ((B0 + b) << 9) = (B0 << 9) + 512 b (mod 2^32)
       const uint32_t hbase = hcol_s - (__float_as_uint(kB0) << 9);
       uint32_t n = gc;
-      float shift = 0.f, s1 = 0.f, s2 = 0.f, cnt_n = 0.f;  // pass-0 partial moments of this thread's columns
-      bool have_shift = false;
       for (int pass = pass0; pass < pass0 + npass; ++pass) {
         const bool fb = pass >= kNumMain;                  // exact fallback pass: column group 0 does the row
         const bool work = row_ok && (!fb || (fail && cg == 0));
@@ -400,29 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             const int j0 = c * kChunk + q * 32;
             const int nvg = nv - q * 32;
             const int wi = j0 >> 5;                       // bitmask word of these 32 columns
-            if constexpr (P == 0) {
-              if (!have_shift) {
-                shift = __uint_as_float(x[0]);
-                have_shift = true;
-              }
-              // sums of d = s - shift and d^2 on packed fp32 pairs
-              uint64_t acc = f2_pack(0.f, 0.f), acq = f2_pack(0.f, 0.f);
-              const uint64_t nsh = f2_pack(-shift, -shift);
-#pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                const float x0 = (FULL || e < nvg) ? __uint_as_float(x[e]) : shift;
-                const float x1 = (FULL || e + 1 < nvg) ? __uint_as_float(x[e + 1]) : shift;
-                const uint64_t d = add2(f2_pack(x0, x1), nsh);
-                acc = add2(acc, d);
-                acq = fma2(d, d, acq);
-              }
-              float a0, a1, b0, b1;
-              f2_unpack(acc, a0, a1);
-              f2_unpack(acq, b0, b1);
-              s1 += a0 + a1;
-              s2 += b0 + b1;
-              cnt_n += (float)(FULL ? 32 : nvg);
-            } else if constexpr (P == 1) {
+            if constexpr (P == 1) {
 #pragma unroll
               for (int e = 0; e < 32; ++e)
                 if (FULL || e < nvg)
@@ -521,9 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
           n += (uint32_t)nt;
         };
         if (!fb) {
-          if (pass == 0) main_tiles(std::integral_constant<int, 0>{});
-          else if (pass == 1) main_tiles(std::integral_constant<int, 1>{});
-          else main_tiles(std::integral_constant<int, 2>{});
+          if (pass == 1) main_tiles(std::integral_constant<int, 1>{});
+          else if (pass == 2) main_tiles(std::integral_constant<int, 2>{});
         } else {
           for (int t = 0; t < nt; ++t, ++n) {
             if (!ok || cg != 0) continue;              // column group 0 reads every tile of a fallback pass
@@ -554,26 +597,40 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
         }
         // ---- end of a pass ----
         if (pass == 0) {
-          if (row_ok) {
-            rs[r].mom_n[cg] = cnt_n;
-            rs[r].mom_mean[cg] = cnt_n > 0.f ? shift + s1 / cnt_n : 0.f;
-            rs[r].mom_m2[cg] = cnt_n > 0.f ? fmaxf(s2 - s1 * s1 / cnt_n, 0.f) : 0.f;
+          // the row's mean and variance in closed form: qbar . mu and qbar^T C qbar, the
+          // four threads of a row each taking 8 of the 32 terms of the outer sum
+          if (ok && !mbar_wait_warp(q_full, 0, abort_flag, ctl, kid | W_QF)) ok = false;
+          if (row_ok && ok) {
+            // element (r, c) of the 128-byte-swizzled tiles: 16-byte chunk c/4 of row r sits at chunk (c/4) ^ (r % 8)
+            auto qval = [&](int c) {
+              const int off = r * 128 + ((((c >> 2) ^ (r & 7))) << 4) + ((c & 3) << 2);
+              return *reinterpret_cast<const float*>(sQh + off) + *reinterpret_cast<const float*>(sQl + off);
+            };
+            float q[kRP];
+#pragma unroll
+            for (int c = 0; c < kRP; ++c) q[c] = qval(c);
+            float pm = 0.f, pv = 0.f;
+#pragma unroll 1
+            for (int ii = 0; ii < kRP / kColGroups; ++ii) {
+              const int i = cg * (kRP / kColGroups) + ii;
+              float ci = 0.f;
+#pragma unroll
+              for (int jj = 0; jj < kRP; ++jj) ci = fmaf(kst[kRP + i * kRP + jj], q[jj], ci);
+              const float qi = qval(i);
+              pm = fmaf(qi, kst[i], pm);
+              pv = fmaf(qi, ci, pv);
+            }
+            rs[r].mom_mean[cg] = pm;
+            rs[r].mom_m2[cg] = pv;
           }
           sel_barrier();
-          if (row_ok) {
-            // the row's mean and variance from the four parts (same order in all four threads)
-            float nn = 0.f, mean = 0.f;
-            for (int q = 0; q < kColGroups; ++q) {
-              nn += rs[r].mom_n[q];
-              mean += rs[r].mom_n[q] * rs[r].mom_mean[q];
+          if (row_ok && ok) {
+            float mean = 0.f, var = 0.f;
+            for (int qg = 0; qg < kColGroups; ++qg) {
+              mean += rs[r].mom_mean[qg];
+              var += rs[r].mom_m2[qg];
             }
-            mean = nn > 0.f ? mean / nn : 0.f;
-            float m2 = 0.f;
-            for (int q = 0; q < kColGroups; ++q) {
-              const float dm = rs[r].mom_mean[q] - mean;
-              m2 += rs[r].mom_m2[q] + rs[r].mom_n[q] * dm * dm;
-            }
-            const float sd = nn > 0.f ? sqrtf(m2 / nn) : 0.f;
+            const float sd = sqrtf(fmaxf(var, 0.f));
             const float zk = normcdfinvf(1.0f - (float)k / (float)nb);
             const float lo = mean + (zk - kZHalf) * sd;
             sc = 1.0f / (2.0f * kZHalf * sd);
@@ -731,14 +788,17 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
 }
 
 constexpr int kSelSmem = 1024 + 2 * kTileBytes + 2 * kNSlot * kTileBytes + kBins * kRows * 4 + kCand * kRows * 8 +
-                         kRows * (int)sizeof(RowShared) + (1 + 2 * kNSlot + 2 * kNBuf + 1) * 8 + 16;
+                         kRows * (int)sizeof(RowShared) + kKStat * 4 + (1 + 2 * kNSlot + 2 * kNBuf + 1) * 8 + 16;
+static_assert((kRows * (int)sizeof(RowShared) + kKStat * 4) % 8 == 0, "barriers must stay 8-byte aligned");
 static_assert(kSelSmem <= 227 * 1024, "score/select tiles exceed shared memory");
 static_assert(kRadixBins * 4 <= kCand * 8, "the fallback's digit histograms must fit the candidate region");
 
 }  // namespace
 
 size_t split_tf32_bytes(const dsv_shape& s) {
-  return 4 * align256((size_t)s.B * s.H * (size_t)(s.N / s.block) * kRP * sizeof(float));
+  const size_t bhs = (size_t)s.B * s.H;
+  return 4 * align256(bhs * (size_t)(s.N / s.block) * kRP * sizeof(float)) +
+         align256(bhs * kKStatSplits * kKStat * sizeof(float)) + align256(bhs * kKStat * sizeof(float));
 }
 
 cudaError_t launch_split_tf32(const float* qp, const float* kp, const dsv_shape& s, float* split, cudaStream_t st) {
@@ -747,12 +807,21 @@ cudaError_t launch_split_tf32(const float* qp, const float* kp, const dsv_shape&
   const long long n = 2 * rows * kRP;
   const unsigned grid = (unsigned)std::min<long long>((n + 255) / 256, 152LL * 16);
   split_tf32_kernel<<<grid, 256, 0, st>>>(qp, kp, s.r, rows, split, split + part, split + 2 * part, split + 3 * part);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // per-head key statistics after the four parts: partial sums, then mu and C
+  const unsigned bhs = (unsigned)(s.B * s.H);
+  float* kpart = split + 4 * part;
+  float* kstats = kpart + align256((size_t)bhs * kKStatSplits * kKStat * sizeof(float)) / sizeof(float);
+  kstats_partial_kernel<<<dim3(bhs, kKStatSplits), 1024, 0, st>>>(kp, s.r, s.N / s.block, kpart);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  kstats_reduce_kernel<<<bhs, 1024, 0, st>>>(kp, s.r, s.N / s.block, kpart, kstats);
   return cudaGetLastError();
 }
 
 cudaError_t launch_score_select(const PredictTopkMaps& maps, const dsv_shape& s, const HeadK& hk, int64_t nnz,
-                                int32_t* fwd_ptr, int32_t* fwd_col, uint32_t* mask, float* scores, const Ctl& ctl,
-                                cudaStream_t st) {
+                                int32_t* fwd_ptr, int32_t* fwd_col, uint32_t* mask, float* scores, const float* split,
+                                const Ctl& ctl, cudaStream_t st) {
   SelArgs a;
   a.qh = maps.qh;
   a.ql = maps.ql;
@@ -768,6 +837,11 @@ cudaError_t launch_score_select(const PredictTopkMaps& maps, const dsv_shape& s,
   a.fwd_col = fwd_col;
   a.mask = mask;
   a.scores = scores;
+  {
+    const size_t bhs = (size_t)s.B * s.H;
+    const size_t part = align256(bhs * (size_t)a.G * kRP * sizeof(float)) / sizeof(float);
+    a.kstats = split + 4 * part + align256(bhs * kKStatSplits * kKStat * sizeof(float)) / sizeof(float);
+  }
   a.hk = hk;
   a.ctl = ctl;
   cudaError_t e = cudaFuncSetAttribute(score_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem);
