@@ -64,6 +64,12 @@ def parse_args(argv=None):
     p.add_argument("--predict", choices=["fused", "two-call"], default="fused",
                    help="fused: dsv_predict_topk_blocks (scores stay on chip); two-call: dsv_predict_scores "
                         "then dsv_topk_blocks (the score matrix goes through HBM)")
+    p.add_argument("--dispatch", action="store_true",
+                   help="route each head sparse or dense by the OP dispatcher and the measured profile "
+                        "profiles/dispatch_<workload>.json")
+    p.add_argument("--dispatch-profile", action="store_true",
+                   help="measure the sparse/dense time ratio against the kept fraction on the workload's first "
+                        "2 heads, write profiles/dispatch_<workload>.json and exit")
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--traffic-from", metavar="CSV",
@@ -338,7 +344,13 @@ def run_ours(args):
         w = wl.scaled(w, name=w.name, H=args.heads)
     x = wl.make_inputs(w, device=dev)
     cube = tuple(int(v) for v in args.cube.split(",")) if args.cube else None
-    hp = HotPath(dsv, x, w, x.k_per_head, cube=cube, mass=args.mass or None, scores=args.scores,
+    ks, dispatch = list(x.k_per_head), None
+    if args.dispatch:
+        prof = json.loads((ROOT / "profiles" / f"dispatch_{w.name}.json").read_text())
+        ks, dense = dsv.dispatch_heads(ks, w.nb, prof["rho"], prof["ratio"])
+        dispatch = {"profile": f"profiles/dispatch_{w.name}.json", "threshold_rho": prof.get("threshold_rho"),
+                    "dense_heads": [h for h, d in enumerate(dense) if d]}
+    hp = HotPath(dsv, x, w, ks, cube=cube, mass=args.mass or None, scores=args.scores,
                  fused=args.predict == "fused")
     fwd_f, bwd_f = pair_flops(w.block, w.d)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -405,6 +417,7 @@ def run_ours(args):
                    "predictor_topk": ("fused (dsv_predict_topk_blocks: scores on chip)" if hp.fused else
                                       "two calls (dsv_predict_scores, dsv_topk_blocks)"),
                    **({"heads_kept": w.H, "reduced": "first heads only (profiler case)"} if args.heads else {}),
+                   **({"dispatch": dispatch} if dispatch else {}),
                    **({"cube": list(cube), "token_order": "3D cubes (dsv_cube_permute in and out, timed)"}
                       if cube else {}),
                    **({"selection": f"mass threshold tau={args.mass}, temperature 1/sqrt(d), k in [1, nb]"}
@@ -958,8 +971,76 @@ def write_traffic(csv_path, command, workload, heads):
     print(json.dumps(out, indent=1))
 
 
+DISPATCH_RHO = (0.05, 0.1, 0.2, 0.35, 0.5, 0.65, 0.8, 0.9, 0.95, 1.0)
+
+
+def dispatch_profile(args):
+    """The OP dispatcher's profile: on the workload's first 2 heads, the time
+    of the sparse path (fused predictor + top-k, attention forward and
+    backward) at kept fractions rho over the dense path (the same attention
+    kernels with every block, no predictor), best of 2 after a warm-up, L2
+    flushed before each run.  Written to profiles/dispatch_<workload>.json."""
+    import torch
+    from dynamic_block_sparse_projection_gb300 import binding as dsv
+    from dynamic_block_sparse_projection_gb300 import workloads as wl
+    torch.cuda.set_device(0)
+    w0 = wl.WORKLOADS[args.workload]
+    w = wl.scaled(w0, name=w0.name, H=min(w0.H, args.heads or 2))
+    x = wl.make_inputs(w, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def timed(fn, reps=2):
+        fn()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            flush.fill_(3)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        return best
+
+    dense_hp = HotPath(dsv, x, w, [w.nb] * w.H, fused=True)
+    dense_hp.run()                                     # the all-block lists (select-all path)
+    torch.cuda.synchronize()
+    t_dense = timed(dense_hp.attention_only)
+    with ClockSampler(0) as clk:
+        t_sparse = []
+        for rho in DISPATCH_RHO:
+            k = max(1, min(w.nb, math.ceil(rho * w.nb)))
+            hp = HotPath(dsv, x, w, [k] * w.H, fused=True)
+            t_sparse.append(timed(hp.run))
+            del hp
+    ratio = [t / t_dense for t in t_sparse]
+    thr = None
+    for i, r in enumerate(ratio):
+        if r >= 1.0:
+            if i == 0:
+                thr = DISPATCH_RHO[0]
+            else:
+                r0, r1, x0, x1 = ratio[i - 1], r, DISPATCH_RHO[i - 1], DISPATCH_RHO[i]
+                thr = x0 + (1.0 - r0) * (x1 - x0) / (r1 - r0)
+            break
+    out = {"workload": w.name, "heads_timed": w.H, "rho": list(DISPATCH_RHO), "ratio": [round(v, 4) for v in ratio],
+           "t_sparse_ms": [round(v, 3) for v in t_sparse], "t_dense_ms": round(t_dense, 3),
+           "threshold_rho": None if thr is None else round(thr, 4),
+           "rule": "dense when t_sparse(rho) / t_dense >= 1 at the head's kept fraction (linear between points)",
+           "sparse_path": "dsv_predict_topk_blocks + dsv_sparse_attn_fwd + the three backward stages",
+           "dense_path": "dsv_sparse_attn_fwd + dsv_sparse_attn_bwd with every block (k = nb), no predictor",
+           "clocks": clk.summary(),
+           "command": "python bench.py --dispatch-profile --workload " + w.name}
+    (ROOT / "profiles" / f"dispatch_{w.name}.json").write_text(json.dumps(out, indent=1) + "\n")
+    print(json.dumps(out), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.dispatch_profile:
+        dispatch_profile(args)
+        return
     if args.traffic_from:
         write_traffic(args.traffic_from, args.traffic_command, args.workload, args.heads)
         return

@@ -33,6 +33,7 @@ EXPORTS = (
     "dsv_predict_max_workspace_bytes", "dsv_predict_scores_max",
     "dsv_selftest_wait_timeout",
     "dsv_predict_topk_workspace_bytes", "dsv_predict_topk_blocks",
+    "dsv_dispatch_heads",
 )
 SELFTEST_WAIT_ID = 0xD5F0
 
@@ -103,6 +104,10 @@ def _load() -> ctypes.CDLL:
     lib.dsv_predict_topk_blocks.argtypes = [vp, vp, vp, vp, Shape, ctypes.POINTER(i32), vp, vp, vp, vp, vp, vp, sz,
                                             vp]
     lib.dsv_predict_topk_blocks.restype = ctypes.c_int
+    f32p = ctypes.POINTER(ctypes.c_float)
+    lib.dsv_dispatch_heads.argtypes = [ctypes.POINTER(i32), i32, i32, f32p, f32p, i32, ctypes.POINTER(i32),
+                                       ctypes.POINTER(i32)]
+    lib.dsv_dispatch_heads.restype = ctypes.c_int
     lib.dsv_selftest_wait_timeout.argtypes = [vp]
     lib.dsv_selftest_wait_timeout.restype = ctypes.c_int
     lib.dsv_version.argtypes = []
@@ -584,3 +589,19 @@ def selftest_wait_timeout(stream=None, device=None) -> None:
     and records DSV_ERR_TIMEOUT; read it with device_error()."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     _check(lib.dsv_selftest_wait_timeout(_stream(dev, stream)), "dsv_selftest_wait_timeout")
+
+
+def dispatch_heads(k_per_head: Sequence[int], nb: int, rho: Sequence[float], ratio: Sequence[float]):
+    """The OP dispatcher (host-only): per head, dense (k = nb) when the profile's
+    sparse/dense time ratio at the head's kept fraction is >= 1, else sparse.
+    Returns (k_out, dense) as lists; see dsv_dispatch_heads."""
+    H, n = len(k_per_head), len(rho)
+    if len(ratio) != n:
+        raise ValueError("rho and ratio must have the same length")
+    karr = (ctypes.c_int32 * max(H, 1))(*[int(k) for k in k_per_head])
+    rarr = (ctypes.c_float * max(n, 1))(*[float(v) for v in rho])
+    qarr = (ctypes.c_float * max(n, 1))(*[float(v) for v in ratio])
+    kout = (ctypes.c_int32 * max(H, 1))()
+    dout = (ctypes.c_int32 * max(H, 1))()
+    _check(lib.dsv_dispatch_heads(karr, H, int(nb), rarr, qarr, n, kout, dout), "dsv_dispatch_heads")
+    return [int(kout[h]) for h in range(H)], [bool(dout[h]) for h in range(H)]

@@ -320,6 +320,35 @@ dsv_status dsv_predict_topk_blocks(const void* Q, const void* K, const float* Wq
   return from_cuda(e);
 }
 
+dsv_status dsv_dispatch_heads(const int32_t* k_per_head, int32_t H, int32_t nb, const float* rho,
+                              const float* ratio, int32_t n, int32_t* k_out, int32_t* dense_out) {
+  if (!k_per_head || !rho || !ratio || !k_out || !dense_out || H < 1 || nb < 1 || n < 1) return DSV_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n; ++i) {
+    if (!(rho[i] > 0.f && rho[i] <= 1.f) || !(ratio[i] > 0.f) || !isfinite(ratio[i])) return DSV_ERR_INVALID_ARG;
+    if (i > 0 && !(rho[i] > rho[i - 1])) return DSV_ERR_INVALID_ARG;
+  }
+  for (int32_t h = 0; h < H; ++h)
+    if (k_per_head[h] < 1 || k_per_head[h] > nb) return DSV_ERR_INVALID_ARG;
+  for (int32_t h = 0; h < H; ++h) {
+    const double x = (double)k_per_head[h] / (double)nb;
+    double y;
+    if (x <= rho[0]) {
+      y = ratio[0];
+    } else if (x >= rho[n - 1]) {
+      y = ratio[n - 1];
+    } else {
+      int32_t i = 1;
+      while (rho[i] < x) ++i;                     // rho[i-1] < x <= rho[i]
+      const double t = (x - rho[i - 1]) / ((double)rho[i] - rho[i - 1]);
+      y = ratio[i - 1] + t * ((double)ratio[i] - ratio[i - 1]);
+    }
+    const int dense = y >= 1.0 ? 1 : 0;
+    dense_out[h] = dense;
+    k_out[h] = dense ? nb : k_per_head[h];
+  }
+  return DSV_OK;
+}
+
 size_t dsv_topk_mass_workspace_bytes(dsv_shape s) {
   if (check_shape(s, false) != DSV_OK || empty(s)) return 0;
   return topk_mass_ws_bytes(s);

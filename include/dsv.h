@@ -295,6 +295,30 @@ dsv_status dsv_predict_topk_blocks(const void* Q, const void* K, const float* Wq
                                    dsv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * dsv_dispatch_heads — the OP dispatcher ([nl] 2A, [hi] 2A: each block goes
+ * sparse or dense by a sparsity threshold found by offline profiling)
+ *
+ * Host-only; touches no device memory.  For every head h, with kept fraction
+ * rho_h = k_per_head[h] / nb, the measured profile gives the time of the
+ * sparse path (predictor, top-k and sparse attention with k_h blocks per
+ * group) relative to the dense path (the same attention kernels with every
+ * block: k = nb, no predictor): ratio(rho), piecewise linear between the
+ * profile points and constant beyond its ends.  The head goes dense when
+ * ratio(rho_h) >= 1: k_out[h] = nb and dense_out[h] = 1; otherwise
+ * k_out[h] = k_per_head[h] and dense_out[h] = 0.
+ *
+ * k_per_head  host [H], each in [1, nb].
+ * rho, ratio  host [n], n >= 1: rho strictly increasing in (0, 1], ratio
+ *             finite and > 0 (a profile such as bench.py --dispatch-profile
+ *             writes).
+ * k_out, dense_out  host [H], written.
+ * Returns DSV_ERR_INVALID_ARG (nothing written) on a null pointer, H < 1,
+ * nb < 1, a k outside [1, nb] or a malformed profile.
+ * ------------------------------------------------------------------------ */
+dsv_status dsv_dispatch_heads(const int32_t* k_per_head, int32_t H, int32_t nb, const float* rho,
+                              const float* ratio, int32_t n, int32_t* k_out, int32_t* dense_out);
+
+/* ------------------------------------------------------------------------
  * Status and device-side error reporting.
  * ------------------------------------------------------------------------ */
 const char* dsv_status_string(dsv_status status);
