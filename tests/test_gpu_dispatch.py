@@ -26,13 +26,11 @@ def test_dense_routed_head_matches_dense_attention(dsv):
     w = SMALL["stress_small"]                      # 3 heads, per-head keep ratios
     x = wl.make_inputs(w, device="cuda")
     nb = w.nb
-    ks = list(x.k_per_head)
-    # a profile whose crossover sits between the heads' kept fractions: the
-    # head with the largest fraction goes dense, the others stay sparse
-    rhos = sorted(k / nb for k in ks)
-    cut = (rhos[-1] + rhos[-2]) / 2 if rhos[-1] > rhos[-2] else rhos[-1]
-    k_out, dense = dsv.dispatch_heads(ks, nb, [cut * 0.5, cut, 1.0], [0.5, 1.0, 1.2])
-    assert any(dense) and not all(dense)
+    # kept fractions 2/15, 12/15, 4/15 and a profile crossing 1 at rho = 0.5:
+    # head 1 goes dense, heads 0 and 2 stay sparse
+    ks = [2, 12, 4]
+    k_out, dense = dsv.dispatch_heads(ks, nb, [0.1, 0.5, 1.0], [0.4, 1.0, 1.1])
+    assert dense == [False, True, False] and k_out == [2, nb, 4]
     fp, fc, bp, bc = dsv.predict_topk_blocks(x.Q, x.K, x.Wq, x.Wk, k_out, w.block)
     O, lse = dsv.sparse_attn_fwd(x.Q, x.K, x.V, fp, fc, w.block)
     dQ, dK, dV = dsv.sparse_attn_bwd(x.Q, x.K, x.V, O, x.dO, lse, fp, fc, bp, bc, w.block)
