@@ -294,7 +294,7 @@ class HotPath:
                           workspace=self.ws_b)
 
 
-KERNELS_PER_STEP = {"predict": 2, "topk": 4, "predict_topk": 6, "fwd": 1, "bwd_pre": 1, "bwd_kv": 2, "bwd_q": 1,
+KERNELS_PER_STEP = {"predict": 2, "topk": 4, "predict_topk": 8, "fwd": 1, "bwd_pre": 1, "bwd_kv": 2, "bwd_q": 1,
                     "cube_in": 4, "cube_out": 4}
 STAGES = ("predict", "topk", "fwd", "bwd_pre", "bwd_kv", "bwd_q")
 FUSED_STAGES = ("predict_topk", "fwd", "bwd_pre", "bwd_kv", "bwd_q")
@@ -394,6 +394,12 @@ def run_ours(args):
     per_call["bwd"] = per_call["bwd_pre"] + per_call["bwd_kv"] + per_call["bwd_q"]
     attn_ms = per_call["fwd"] + per_call["bwd"]
     peaks, peak_src = load_peaks()
+    # the bf16 denominator: the burst figure for a short timed region, the sustained one
+    # (a seconds-long loop under the power cap) once the timed steps run for a second or more
+    sustained = total_ms_max >= 1000.0
+    bf16_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    bf16_kind = (f"{peak_src} bf16 sustained (cuBLAS, seconds-long loop; the timed region is "
+                 f"{total_ms_max / 1e3:.1f} s)" if sustained else f"{peak_src} bf16 burst (cuBLAS)")
 
     # dense run of the same kernels (k = nb) for the speedup
     dense = None
@@ -402,7 +408,7 @@ def run_ours(args):
 
     # roofline of the dominant kernel (the predictor and the top-k are whole calls of several launches)
     dom = max(hp.stages, key=lambda k: per_call[k])
-    roofline = roofline_entry(dom, per_call, w, hp, peaks, peak_src)
+    roofline = roofline_entry(dom, per_call, w, hp, peaks, peak_src, bf16_peak, bf16_kind)
     bwd_eff = step_flops * bwd_f / (fwd_f + bwd_f) / (per_call["bwd"] * 1e-3) / 1e12
 
     e2e = None if args.no_e2e else time_e2e(dsv, x, w, hp, args, flops_per_step=step_flops)
@@ -426,13 +432,15 @@ def run_ours(args):
                       if args.scores == "max" else {}),
                    "l2": "flushed before every step (256 MiB write, outside the step events); "
                          "inputs are also larger than L2"},
-        "pct_of_bf16_peak": round(100.0 * value / peaks["bf16_tflops"], 2),
+        "pct_of_bf16_peak": round(100.0 * value / bf16_peak, 2),
+        "bf16_peak": {"tflops": bf16_peak, "kind": bf16_kind,
+                      "pct_of_burst": round(100.0 * value / peaks["bf16_tflops"], 2)},
         "attention_only": {"ms": round(attn_ms, 4),
                            "tflops": round(step_flops / (attn_ms * 1e-3) / 1e12, 3),
                            "pct_of_bf16_peak": round(100.0 * step_flops / (attn_ms * 1e-3) / 1e12
-                                                     / peaks["bf16_tflops"], 2)},
+                                                     / bf16_peak, 2)},
         "breakdown_ms": {k: round(v, 4) for k, v in per_call.items()},
-        "backward_effective": {"tflops": round(bwd_eff, 3), "frac": round(bwd_eff / peaks["bf16_tflops"], 4),
+        "backward_effective": {"tflops": round(bwd_eff, 3), "frac": round(bwd_eff / bf16_peak, 4),
                                "algorithmic": "10*block^2*d FLOP per pair (5 GEMMs) over the three backward "
                                               "stages' time; the kernels execute 7 (S and dP twice, no atomics)"},
         "predictor_topk": hbm_fractions(w, hp, per_call, peaks),
@@ -464,18 +472,19 @@ KERNEL_SRC = {"fwd": "dynamic_block_sparse_projection_gb300/csrc/attn_fwd.cu",
               "predict_topk": "dynamic_block_sparse_projection_gb300/csrc/predict_topk.cu"}
 
 
-def roofline_entry(dom, per_call, w, hp, peaks, peak_src):
+def roofline_entry(dom, per_call, w, hp, peaks, peak_src, bf16_peak=None, bf16_kind=None):
     B, H, N, d, G = w.B, w.H, w.N, w.d, w.nb
     srcs = [KERNEL_SRC[dom], "dynamic_block_sparse_projection_gb300/csrc/dsv_device.cuh"]
     traffic, tnote = profile_traffic(KERNEL_OF.get(dom, dom), srcs, w, hp.nnz)
     if dom in MMAS_PER_PAIR:
         flops = MMAS_PER_PAIR[dom] * 2 * w.block * w.block * d * hp.nnz
         achieved = flops / (per_call[dom] * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
+        peak = bf16_peak or peaks["bf16_tflops"]
         return {"kernel": KERNEL_OF[dom], "bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                 "algorithmic": f"{MMAS_PER_PAIR[dom]} x 2*block^2*d FLOP per (group, block) pair x {hp.nnz} pairs",
-                "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
+                "peak_source": bf16_kind or f"{peak_src} bf16 burst (cuBLAS)",
+                "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
                 "traffic": traffic, "traffic_source": tnote}
     if dom == "predict" and hp.scores == "max":
         # every logit of every tile: 2 * r FLOP per (query token, key token) pair, fp32 FMA on the CUDA cores
