@@ -14,6 +14,9 @@
 //                S^T = K_j Q_g^T, dP^T = V_j dO_g^T       (tcgen05, smem x smem)
 //                P^T, dS^T -> TMEM (bf16) by the compute warps
 //                dV += P^T dO_g, dK += dS^T Q_g           (tcgen05, TMEM x smem)
+//              with the products of consecutive pairs interleaved so that
+//              the tensor core runs one while the compute warps convert the
+//              other's output.
 //   q kernel   persistent CTAs (one per SM) working through the groups
 //              (b, h, g), each looping over its forward list:
 //                S = Q_g K_j^T, dP = dO_g V_j^T; dS -> TMEM; dQ += dS K_j
@@ -104,16 +107,17 @@ struct KVTraits {
   static constexpr int NBAR = 1 + 2 * NST + 5;
   static constexpr int SMEM_USED = 1024 + 2 * A_BYTES + NST * STAGE_BYTES + NBAR * 8 + 16;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
-  // Each pair (j, g) is processed as two halves of the query group, so the
-  // compute warps work on one half while the tensor core runs the other:
-  // half h owns columns [h*BETA, h*BETA + HALF) for S^T_h and the next HALF
-  // for dP^T_h; P^T_h / dS^T_h (bf16) are written back over them.
-  static constexpr int HALF = BETA / 2;            // queries per half
-  static constexpr int W = HALF / 2;               // columns of a half per compute warp
-  static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
+  // TMEM: S^T (fp32, BETA columns) at 0, dP^T at 128, dV at 256, dK at 256+D.
+  // S^T and dP^T are whole-group products (N = BETA): an M=128, N=128
+  // smem x smem product reads 8 KB in its 64 clocks, the shared-memory port's
+  // rate, where a half-group (N = 64) product would need 6 KB in 32.  The
+  // compute warps write P^T and dS^T (bf16 pairs) over the columns they read:
+  // warp half hf owns queries [hf*W, hf*W + W) and packs them into its first
+  // W/2 columns.
+  static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
-  __host__ __device__ static constexpr uint32_t st_col(int h) { return (uint32_t)(h * BETA); }
-  __host__ __device__ static constexpr uint32_t dpt_col(int h) { return (uint32_t)(h * BETA + HALF); }
+  static constexpr int W = BETA / 2;               // columns per compute warp
+  __host__ __device__ static constexpr uint32_t packed_col(int q) { return (uint32_t)((q / W) * W + (q % W) / 2); }
 };
 
 template <int BETA, int D>
@@ -126,7 +130,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                        __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, Ctl ctl) {
   using T = KVTraits<BETA, D>;
   constexpr int NST = T::NST;
-  constexpr int HALF = T::HALF;
   constexpr int W = T::W;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sbase = smem_align1024(smem_raw);
@@ -137,14 +140,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bars;
   uint64_t* g_full = bars + 1;
   uint64_t* g_empty = g_full + NST;
-  uint64_t* s_full = g_empty + NST;               // [2] S^T_h, dP^T_h in TMEM
-  uint64_t* p_full = s_full + 2;                  // [2] P^T_h, dS^T_h in TMEM
-  uint64_t* acc_done = p_full + 2;
+  uint64_t* s_full = g_empty + NST;               // S^T in TMEM
+  uint64_t* dp_full = s_full + 1;                 // dP^T in TMEM
+  uint64_t* p_full = dp_full + 1;                 // P^T written back (bf16)
+  uint64_t* ds_full = p_full + 1;                 // dS^T written back (bf16)
+  uint64_t* acc_done = ds_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  DSV_TRACE_INIT;
   const long long row = order[blockIdx.x];        // (b*H + h)*nb + j, longest transposed lists first
   const int nb = G;
   const long long bh = row / nb;
@@ -159,10 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&g_full[s], 1);
       mbar_init(&g_empty[s], 1);
     }
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(&s_full[h], 1);
-      mbar_init(&p_full[h], kComputeThreads);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, kComputeThreads);
+    mbar_init(ds_full, kComputeThreads);
     mbar_init(acc_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -240,50 +244,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     {
       // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
-      // Order per pair n: S/dP(n, 1), dV/dK(n, 0), S/dP(n+1, 0), dV/dK(n, 1).
-      // Each S/dP half is issued once the compute warps have released that
-      // TMEM buffer (p_full of the previous use, awaited before its dV/dK).
-      constexpr uint32_t ID_S = idesc_bf16_f32(T::BM, HALF, false, false);  // S^T_h, dP^T_h: N = HALF queries
+      // Order: S^T(0), dP^T(0), then per pair n
+      //   dV(n) [P^T(n) written], S^T(n+1), dK(n) [dS^T(n) written], dP^T(n+1).
+      // The tensor core runs S^T(n+1) while the compute warps turn dP^T(n)
+      // into dS^T(n), and dK(n), dP^T(n+1) while they turn S^T(n+1) into
+      // P^T(n+1).  A product that overwrites a TMEM buffer is issued after
+      // the products that read it, and the tensor core runs them in order.
+      constexpr uint32_t ID_S = idesc_bf16_f32(T::BM, BETA, false, false);  // S^T, dP^T: N = BETA queries
       constexpr uint32_t ID_G = idesc_bf16_f32(T::BM, D, false, true);      // dV, dK: B MN-major
       const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t dS0 = sdesc_sw128(smem_u32(sStage), 16, 1024);           // K-major view of a stage
       const uint64_t dSmn0 = sdesc_sw128(smem_u32(sStage), T::B_CHUNK, 1024);  // MN-major view
-      auto issue_sdp = [&](int n, int h) {
-        const int s = n % NST;
-        const uint64_t qg = desc_off(dS0, (uint32_t)(s * T::STAGE_BYTES + h * HALF * 128));
-        const uint64_t dog = desc_off(qg, T::B_BYTES);
+      // S^T = K_j Q_g^T (t = 0) or dP^T = V_j dO_g^T (t = 1)
+      auto issue_sdp = [&](int n, int t) {
+        const uint64_t a0 = t ? dV0 : dK0;
+        const uint64_t b0 = desc_off(dS0, (uint32_t)((n % NST) * T::STAGE_BYTES + t * T::B_BYTES));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ao = (kk >> 2) * T::A_CHUNK + (kk & 3) * 32;
           const uint32_t bo = (kk >> 2) * T::B_CHUNK + (kk & 3) * 32;
-          mma_ss_w(tmem + T::st_col(h), desc_off(dK0, ao), desc_off(qg, bo), ID_S, kk > 0 ? 1u : 0u);
+          mma_ss_w(tmem + (t ? T::DP_COL : T::S_COL), desc_off(a0, ao), desc_off(b0, bo), ID_S, kk > 0 ? 1u : 0u);
         }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ao = (kk >> 2) * T::A_CHUNK + (kk & 3) * 32;
-          const uint32_t bo = (kk >> 2) * T::B_CHUNK + (kk & 3) * 32;
-          mma_ss_w(tmem + T::dpt_col(h), desc_off(dV0, ao), desc_off(dog, bo), ID_S, kk > 0 ? 1u : 0u);
-        }
-        mma_commit_w(&s_full[h]);
+        mma_commit_w(t ? dp_full : s_full);
       };
-      // dV += P^T_h dO_g[half h], dK += dS^T_h Q_g[half h].  Compute warp hf
-      // of a half packed its W queries into the first W/2 of its own W columns.
-      auto issue_grad = [&](int n, int h) {
-        const int s = n % NST;
-        const uint64_t qmn = desc_off(dSmn0, (uint32_t)(s * T::STAGE_BYTES + h * HALF * 128));
-        const uint64_t domn = desc_off(qmn, T::B_BYTES);
+      // dV += P^T dO_g (t = 0) or dK += dS^T Q_g (t = 1)
+      auto issue_grad = [&](int n, int t) {
+        const uint64_t b0 = desc_off(dSmn0, (uint32_t)((n % NST) * T::STAGE_BYTES + (t ? 0 : T::B_BYTES)));
 #pragma unroll
-        for (int kk = 0; kk < HALF / 16; ++kk) {
-          const uint32_t acc = (n > 0 || h > 0 || kk > 0) ? 1u : 0u;
-          const uint32_t pc = (uint32_t)(((kk * 16) / W) * W + ((kk * 16) % W) / 2);
-          mma_ts_w(tmem + T::DV_COL, tmem + T::st_col(h) + pc, desc_off(domn, kk * 16 * 128), ID_G, acc);
-        }
-#pragma unroll
-        for (int kk = 0; kk < HALF / 16; ++kk) {
-          const uint32_t acc = (n > 0 || h > 0 || kk > 0) ? 1u : 0u;
-          const uint32_t pc = (uint32_t)(((kk * 16) / W) * W + ((kk * 16) % W) / 2);
-          mma_ts_w(tmem + T::DK_COL, tmem + T::dpt_col(h) + pc, desc_off(qmn, kk * 16 * 128), ID_G, acc);
+        for (int kk = 0; kk < BETA / 16; ++kk) {
+          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
+          mma_ts_w(tmem + (t ? T::DK_COL : T::DV_COL), tmem + (t ? T::DP_COL : T::S_COL) + T::packed_col(kk * 16),
+                   desc_off(b0, kk * 16 * 128), ID_G, acc);
         }
       };
       bool ok = mbar_wait_warp(kv_full, 0, abort_flag, ctl, kid | W_KV) &&
@@ -291,95 +283,104 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         issue_sdp(0, 0);
+        issue_sdp(0, 1);
       }
       for (int n = 0; ok && n < cnt; ++n) {
-        DSV_TRACE_POINT(g_trace_kv, n, 0);
-        const uint32_t tg = n + 1 < cnt ? mbar_test(&g_full[(n + 1) % NST], (uint32_t)((n + 1) / NST) & 1u) : 0u;
-        issue_sdp(n, 1);
-        DSV_TRACE_POINT(g_trace_kv, n, 1);
-        if (!mbar_wait_warp(&p_full[0], (uint32_t)n & 1u, abort_flag, ctl, kid | W_P)) break;
-        DSV_TRACE_POINT(g_trace_kv, n, 2);
+        const bool more = n + 1 < cnt;
+        const uint32_t tg = more ? mbar_test(&g_full[(n + 1) % NST], (uint32_t)((n + 1) / NST) & 1u) : 0u;
+        if (!mbar_wait_warp(p_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_P)) break;
         tc_fence_after();
         issue_grad(n, 0);
-        if (n + 1 < cnt) {
-          const int s1 = (n + 1) % NST;
-          if (!mbar_wait_warp_tested(&g_full[s1], (uint32_t)((n + 1) / NST) & 1u, tg, abort_flag, ctl, kid | W_GFULL))
+        if (more) {
+          if (!mbar_wait_warp_tested(&g_full[(n + 1) % NST], (uint32_t)((n + 1) / NST) & 1u, tg, abort_flag, ctl,
+                                     kid | W_GFULL))
             break;
           tc_fence_after();
           issue_sdp(n + 1, 0);
         }
-        if (!mbar_wait_warp(&p_full[1], (uint32_t)n & 1u, abort_flag, ctl, kid | W_P)) break;
+        if (!mbar_wait_warp(ds_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_DSFULL)) break;
         tc_fence_after();
         issue_grad(n, 1);
         mma_commit_w(&g_empty[n % NST]);
-        DSV_TRACE_POINT(g_trace_kv, n, 3);
+        if (more) issue_sdp(n + 1, 1);
       }
       mma_commit_w(acc_done);
       mbar_wait_warp(acc_done, 0, nullptr, ctl, kid | W_DRAIN);
     }
   } else {
-    // ------------- compute warps: key row kr, W queries of each half -------------
+    // ------------- compute warps: key row kr, W queries of the group -------------
     const int sp = warp & 3;
     const int hf = (warp - 2) >> 2;
     const int kr = sp * 32 + lane;
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     const float scale_log2 = scale * kLog2e;
+    const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+    const uint32_t cs = tmem + lane_off + T::S_COL + hf * W;
+    const uint32_t cp = tmem + lane_off + T::DP_COL + hf * W;
+    const int q0 = hf * W;                         // first query of this warp's columns
     bool ok = true;
-    uint32_t s_tested = 0u;
     for (int n = 0; ok && n < cnt; ++n) {
       const int s = n % NST;
-      if (!mbar_wait_warp(&g_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_GFULL)) {
+      if (!mbar_wait_warp(&g_full[s], (uint32_t)(n / NST) & 1u, abort_flag, ctl, kid | W_GFULL) ||
+          !mbar_wait_warp(s_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_S)) {
         ok = false;
         break;
       }
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        if (!mbar_wait_warp_tested(&s_full[h], (uint32_t)n & 1u, s_tested, abort_flag, ctl, kid | W_S)) {
-          ok = false;
-          break;
-        }
-        if (warp == 2 && lane == 0 && h == 0) DSV_TRACE_POINT(g_trace_kv, n, 4);
-        tc_fence_after();
-        const uint32_t cs = tmem + lane_off + T::st_col(h) + hf * W;
-        const uint32_t cp = tmem + lane_off + T::dpt_col(h) + hf * W;
-        uint32_t xs[W], xp[W];
-        tmem_ld_w<W>(cs, xs);
-        tmem_ld_w<W>(cp, xp);
-        // the next half: (n, 1) after (n, 0), (n + 1, 0) after (n, 1)
-        s_tested = (h == 0 || n + 1 < cnt) ? mbar_test(&s_full[h ^ 1], (uint32_t)(n + h) & 1u) : 0u;
-        const int q0 = h * HALF + hf * W;            // first query of this warp's columns
-        const float4* l4 = reinterpret_cast<const float4*>(sStage + s * T::STAGE_BYTES + 2 * T::B_BYTES) + q0 / 4;
-        const float4* d4 = l4 + BETA / 4;
-        tmem_ld_wait();
-        if (warp == 2 && lane == 0 && h == 0) DSV_TRACE_POINT(g_trace_kv, n, 5);
-        uint32_t pw[W / 2], dw[W / 2];
-        const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+      tc_fence_after();
+      const float4* l4 = reinterpret_cast<const float4*>(sStage + s * T::STAGE_BYTES + 2 * T::B_BYTES) + q0 / 4;
+      const float4* d4 = l4 + BETA / 4;
+      uint32_t x[W];
+      uint64_t p2[W / 2];                          // P^T of this row's W queries, fp32 pairs
+      tmem_ld_w<W>(cs, x);
+      tmem_ld_wait();
+      {
+        uint32_t pw[W / 2];
 #pragma unroll
         for (int q = 0; q < W / 4; ++q) {
-          const float4 L = l4[q], Dd = d4[q];   // -lse*log2(e) and D of four queries
+          const float4 L = l4[q];                  // -lse*log2(e) of four queries
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            // exponent, dP - D and dS on packed fp32 pairs
             const int i0 = 4 * q + 2 * e;
-            float x0, x1, d0, d1;
-            f2_unpack(fma2(f2_pack(__uint_as_float(xs[i0]), __uint_as_float(xs[i0 + 1])), c2,
+            float x0, x1;
+            f2_unpack(fma2(f2_pack(__uint_as_float(x[i0]), __uint_as_float(x[i0 + 1])), c2,
                            e ? f2_pack(L.z, L.w) : f2_pack(L.x, L.y)), x0, x1);
-            const float p0 = ex2(x0), p1 = ex2(x1);
-            const uint64_t t = sub2(f2_pack(__uint_as_float(xp[i0]), __uint_as_float(xp[i0 + 1])),
+            const float a = ex2(x0), b = ex2(x1);
+            p2[2 * q + e] = f2_pack(a, b);
+            pw[2 * q + e] = pack_bf16x2(a, b);
+          }
+        }
+        // each warp overwrites only the TMEM lanes and columns it has just read
+        tmem_st_w<W / 2>(cs, pw);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full);
+      }
+      if (!mbar_wait_warp(dp_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_S)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_ld_w<W>(cp, x);
+      tmem_ld_wait();
+      {
+        uint32_t dw[W / 2];
+#pragma unroll
+        for (int q = 0; q < W / 4; ++q) {
+          const float4 Dd = d4[q];                 // D of four queries
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int i0 = 4 * q + 2 * e;
+            const uint64_t t = sub2(f2_pack(__uint_as_float(x[i0]), __uint_as_float(x[i0 + 1])),
                                     e ? f2_pack(Dd.z, Dd.w) : f2_pack(Dd.x, Dd.y));
-            f2_unpack(mul2(f2_pack(p0, p1), t), d0, d1);
-            pw[2 * q + e] = pack_bf16x2(p0, p1);
+            float d0, d1;
+            f2_unpack(mul2(p2[2 * q + e], t), d0, d1);
             dw[2 * q + e] = pack_bf16x2(d0, d1);
           }
         }
-        if (warp == 2 && lane == 0 && h == 0) DSV_TRACE_POINT(g_trace_kv, n, 6);
-        // each warp overwrites only the TMEM lanes and columns it has just read
-        tmem_st_w<W / 2>(cs, pw);
         tmem_st_w<W / 2>(cp, dw);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&p_full[h]);
-        if (warp == 2 && lane == 0 && h == 0) DSV_TRACE_POINT(g_trace_kv, n, 7);
+        mbar_arrive(ds_full);
       }
     }
     if (ok) ok = mbar_wait_warp(acc_done, 0, abort_flag, ctl, kid | W_ACC);

@@ -325,11 +325,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
-// W consecutive columns (W = 16 or 32) into / out of registers.
+// W consecutive columns (loads: W = 16, 32 or 64; stores: 8, 16 or 32) into /
+// out of registers.
 template <int W>
 __device__ __forceinline__ void tmem_ld_w(uint32_t taddr, uint32_t* r) {
-  static_assert(W == 16 || W == 32, "tmem_ld_w: W must be 16 or 32");
-  if constexpr (W == 32) tmem_ld32(taddr, r); else tmem_ld16(taddr, r);
+  static_assert(W == 16 || W == 32 || W == 64, "tmem_ld_w: W must be 16, 32 or 64");
+  if constexpr (W == 64) {
+    tmem_ld32(taddr, r);
+    tmem_ld32(taddr + 32, r + 32);
+  } else if constexpr (W == 32) {
+    tmem_ld32(taddr, r);
+  } else {
+    tmem_ld16(taddr, r);
+  }
 }
 template <int W>
 __device__ __forceinline__ void tmem_st_w(uint32_t taddr, const uint32_t* r) {
