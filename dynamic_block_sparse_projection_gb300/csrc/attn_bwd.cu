@@ -104,7 +104,7 @@ struct KVTraits {
   static constexpr int NST = 2;
   static constexpr int VEC_BYTES = BETA * 4;       // -lse2_g or D_g
   static constexpr int STAGE_BYTES = (2 * B_BYTES + 2 * VEC_BYTES + 1023) / 1024 * 1024;  // keeps tiles 1024-aligned
-  static constexpr int NBAR = 1 + 2 * NST + 5;
+  static constexpr int NBAR = 1 + 2 * NST + 7;
   static constexpr int SMEM_USED = 1024 + 2 * A_BYTES + NST * STAGE_BYTES + NBAR * 8 + 16;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   // TMEM: S^T (fp32, BETA columns) at 0, dP^T at 128, dV at 256, dK at 256+D.
@@ -118,6 +118,10 @@ struct KVTraits {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int W = BETA / 2;               // columns per compute warp
   __host__ __device__ static constexpr uint32_t packed_col(int q) { return (uint32_t)((q / W) * W + (q % W) / 2); }
+  // The compute warps hand P^T and dS^T over in two chunks (the first and the
+  // second half of each warp's columns, one barrier each), so the tensor core
+  // starts dV and dK on the first while they convert the second.
+  __host__ __device__ static constexpr int chunk_of(int q) { return (q % W) / (W / 2); }
 };
 
 template <int BETA, int D>
@@ -142,9 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* g_empty = g_full + NST;
   uint64_t* s_full = g_empty + NST;               // S^T in TMEM
   uint64_t* dp_full = s_full + 1;                 // dP^T in TMEM
-  uint64_t* p_full = dp_full + 1;                 // P^T written back (bf16)
-  uint64_t* ds_full = p_full + 1;                 // dS^T written back (bf16)
-  uint64_t* acc_done = ds_full + 1;
+  uint64_t* p_full = dp_full + 1;                 // [2] P^T chunk written back (bf16)
+  uint64_t* ds_full = p_full + 2;                 // [2] dS^T chunk written back (bf16)
+  uint64_t* acc_done = ds_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -165,8 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_full, kComputeThreads);
-    mbar_init(ds_full, kComputeThreads);
+    for (int c = 0; c < 2; ++c) {
+      mbar_init(&p_full[c], kComputeThreads);
+      mbar_init(&ds_full[c], kComputeThreads);
+    }
     mbar_init(acc_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -250,59 +256,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       // into dS^T(n), and dK(n), dP^T(n+1) while they turn S^T(n+1) into
       // P^T(n+1).  A product that overwrites a TMEM buffer is issued after
       // the products that read it, and the tensor core runs them in order.
+      // Each barrier is tested half-way through the products issued before
+      // its wait: the MMA queue holds only a few products, so a wait that
+      // sleeps, or pays the test's round trip, lets the tensor core drain.
       constexpr uint32_t ID_S = idesc_bf16_f32(T::BM, BETA, false, false);  // S^T, dP^T: N = BETA queries
       constexpr uint32_t ID_G = idesc_bf16_f32(T::BM, D, false, true);      // dV, dK: B MN-major
       const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t dS0 = sdesc_sw128(smem_u32(sStage), 16, 1024);           // K-major view of a stage
       const uint64_t dSmn0 = sdesc_sw128(smem_u32(sStage), T::B_CHUNK, 1024);  // MN-major view
-      // S^T = K_j Q_g^T (t = 0) or dP^T = V_j dO_g^T (t = 1)
-      auto issue_sdp = [&](int n, int t) {
+      // S^T = K_j Q_g^T (t = 0) or dP^T = V_j dO_g^T (t = 1); returns the test of `probe`
+      auto issue_sdp = [&](int n, int t, uint64_t* probe, uint32_t probe_par) -> uint32_t {
         const uint64_t a0 = t ? dV0 : dK0;
         const uint64_t b0 = desc_off(dS0, (uint32_t)((n % NST) * T::STAGE_BYTES + t * T::B_BYTES));
+        uint32_t r = 0u;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ao = (kk >> 2) * T::A_CHUNK + (kk & 3) * 32;
           const uint32_t bo = (kk >> 2) * T::B_CHUNK + (kk & 3) * 32;
           mma_ss_w(tmem + (t ? T::DP_COL : T::S_COL), desc_off(a0, ao), desc_off(b0, bo), ID_S, kk > 0 ? 1u : 0u);
+          if (kk == D / 32 - 1 && probe != nullptr) r = mbar_test(probe, probe_par);
         }
         mma_commit_w(t ? dp_full : s_full);
+        return r;
       };
-      // dV += P^T dO_g (t = 0) or dK += dS^T Q_g (t = 1)
-      auto issue_grad = [&](int n, int t) {
+      // chunk c of dV += P^T dO_g (t = 0) or dK += dS^T Q_g (t = 1); returns the test of `probe`
+      auto issue_grad = [&](int n, int t, int c, uint64_t* probe, uint32_t probe_par) -> uint32_t {
         const uint64_t b0 = desc_off(dSmn0, (uint32_t)((n % NST) * T::STAGE_BYTES + (t ? 0 : T::B_BYTES)));
+        uint32_t r = 0u;
+        int m = 0;
 #pragma unroll
         for (int kk = 0; kk < BETA / 16; ++kk) {
+          if (T::chunk_of(kk * 16) != c) continue;
           const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
           mma_ts_w(tmem + (t ? T::DK_COL : T::DV_COL), tmem + (t ? T::DP_COL : T::S_COL) + T::packed_col(kk * 16),
                    desc_off(b0, kk * 16 * 128), ID_G, acc);
+          if (++m == BETA / 64 && probe != nullptr) r = mbar_test(probe, probe_par);
         }
+        return r;
       };
       bool ok = mbar_wait_warp(kv_full, 0, abort_flag, ctl, kid | W_KV) &&
                 mbar_wait_warp(&g_full[0], 0, abort_flag, ctl, kid | W_GFULL);
+      uint32_t tp0 = 0u;
       if (ok) {
         tc_fence_after();
-        issue_sdp(0, 0);
-        issue_sdp(0, 1);
+        issue_sdp(0, 0, nullptr, 0u);
+        tp0 = issue_sdp(0, 1, &p_full[0], 0u);
       }
       for (int n = 0; ok && n < cnt; ++n) {
         const bool more = n + 1 < cnt;
+        const uint32_t par = (uint32_t)n & 1u;
         const uint32_t tg = more ? mbar_test(&g_full[(n + 1) % NST], (uint32_t)((n + 1) / NST) & 1u) : 0u;
-        if (!mbar_wait_warp(p_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_P)) break;
+        if (!mbar_wait_warp_tested(&p_full[0], par, tp0, abort_flag, ctl, kid | W_P)) break;
         tc_fence_after();
-        issue_grad(n, 0);
+        const uint32_t tp1 = issue_grad(n, 0, 0, &p_full[1], par);
+        if (!mbar_wait_warp_tested(&p_full[1], par, tp1, abort_flag, ctl, kid | W_P)) break;
+        tc_fence_after();
+        issue_grad(n, 0, 1, nullptr, 0u);
+        uint32_t td0 = 0u;
         if (more) {
           if (!mbar_wait_warp_tested(&g_full[(n + 1) % NST], (uint32_t)((n + 1) / NST) & 1u, tg, abort_flag, ctl,
                                      kid | W_GFULL))
             break;
           tc_fence_after();
-          issue_sdp(n + 1, 0);
+          td0 = issue_sdp(n + 1, 0, &ds_full[0], par);
         }
-        if (!mbar_wait_warp(ds_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_DSFULL)) break;
+        if (!mbar_wait_warp_tested(&ds_full[0], par, td0, abort_flag, ctl, kid | W_DSFULL)) break;
         tc_fence_after();
-        issue_grad(n, 1);
+        const uint32_t td1 = issue_grad(n, 1, 0, &ds_full[1], par);
+        if (!mbar_wait_warp_tested(&ds_full[1], par, td1, abort_flag, ctl, kid | W_DSFULL)) break;
+        tc_fence_after();
+        issue_grad(n, 1, 1, nullptr, 0u);
         mma_commit_w(&g_empty[n % NST]);
-        if (more) issue_sdp(n + 1, 1);
+        if (more) tp0 = issue_sdp(n + 1, 1, &p_full[0], par ^ 1u);
       }
       mma_commit_w(acc_done);
       mbar_wait_warp(acc_done, 0, nullptr, ctl, kid | W_DRAIN);
@@ -333,10 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t p2[W / 2];                          // P^T of this row's W queries, fp32 pairs
       tmem_ld_w<W>(cs, x);
       tmem_ld_wait();
-      {
-        uint32_t pw[W / 2];
 #pragma unroll
-        for (int q = 0; q < W / 4; ++q) {
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pw[W / 4];
+#pragma unroll
+        for (int q = c * (W / 8); q < (c + 1) * (W / 8); ++q) {
           const float4 L = l4[q];                  // -lse*log2(e) of four queries
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
@@ -346,14 +373,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                            e ? f2_pack(L.z, L.w) : f2_pack(L.x, L.y)), x0, x1);
             const float a = ex2(x0), b = ex2(x1);
             p2[2 * q + e] = f2_pack(a, b);
-            pw[2 * q + e] = pack_bf16x2(a, b);
+            pw[2 * q + e - c * (W / 4)] = pack_bf16x2(a, b);
           }
         }
-        // each warp overwrites only the TMEM lanes and columns it has just read
-        tmem_st_w<W / 2>(cs, pw);
+        // each warp overwrites only the TMEM lanes and columns it has read
+        tmem_st_w<W / 4>(cs + c * (W / 4), pw);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full);
+        mbar_arrive(&p_full[c]);
       }
       if (!mbar_wait_warp(dp_full, (uint32_t)n & 1u, abort_flag, ctl, kid | W_S)) {
         ok = false;
@@ -362,10 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       tmem_ld_w<W>(cp, x);
       tmem_ld_wait();
-      {
-        uint32_t dw[W / 2];
 #pragma unroll
-        for (int q = 0; q < W / 4; ++q) {
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dw[W / 4];
+#pragma unroll
+        for (int q = c * (W / 8); q < (c + 1) * (W / 8); ++q) {
           const float4 Dd = d4[q];                 // D of four queries
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
@@ -374,13 +402,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     e ? f2_pack(Dd.z, Dd.w) : f2_pack(Dd.x, Dd.y));
             float d0, d1;
             f2_unpack(mul2(p2[2 * q + e], t), d0, d1);
-            dw[2 * q + e] = pack_bf16x2(d0, d1);
+            dw[2 * q + e - c * (W / 4)] = pack_bf16x2(d0, d1);
           }
         }
-        tmem_st_w<W / 2>(cp, dw);
+        tmem_st_w<W / 4>(cp + c * (W / 4), dw);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(ds_full);
+        mbar_arrive(&ds_full[c]);
       }
     }
     if (ok) ok = mbar_wait_warp(acc_done, 0, abort_flag, ctl, kid | W_ACC);
