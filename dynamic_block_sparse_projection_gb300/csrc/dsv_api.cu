@@ -206,13 +206,14 @@ dsv_status dsv_predict_scores_max(const void* Q, const void* K, const float* Wq,
   dsv_status v = check_shape(s, true);
   if (v != DSV_OK) return v;
   if (empty(s)) return DSV_OK;
-  const long long G = s.N / s.block;
-  if (G * ((G + 15) / 16) >= (1LL << 31)) return DSV_ERR_UNSUPPORTED;   // grid x of the tile kernel
   if (!Q || !K || !Wq || !Wk || !scores || !workspace) return DSV_ERR_INVALID_ARG;
   if (!al16(Q) || !al16(K) || !al16(Wq) || !al16(Wk) || !al16(scores) || !al256(workspace))
     return DSV_ERR_INVALID_ARG;
   if (workspace_bytes < predict_max_ws_bytes(s)) return DSV_ERR_INVALID_ARG;
-  return from_cuda(launch_predict_max(Q, K, Wq, Wk, s, scores, workspace, reinterpret_cast<cudaStream_t>(stream)));
+  Ctl ctl;
+  if (current_ctl(&ctl) != cudaSuccess) return DSV_ERR_CUDA;
+  return from_cuda(
+      launch_predict_max(Q, K, Wq, Wk, s, scores, workspace, ctl, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t dsv_topk_workspace_bytes(dsv_shape s) {

@@ -208,6 +208,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
   return d;
 }
 
+// Shared-memory matrix descriptor without swizzle, K-major: the matrix is a
+// grid of 8-row x 16-byte core matrices, each 128 contiguous bytes; LBO =
+// bytes between core matrices adjacent along K, SBO = bytes between 8-row
+// groups.  Start address 16-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_noswz(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
 // Descriptor of the same matrix `byte_off` bytes further on.  The start
 // address field holds (address >> 4) in 14 bits and shared-memory addresses
 // stay below 2^18, so adding to the low bits never carries into LBO.  Used to
@@ -478,6 +491,7 @@ enum : unsigned int {
   KID_FWD = 1,
   KID_BWD_KV = 2,
   KID_BWD_Q = 3,
+  KID_MAXPOOL = 5,
 };
 
 }  // namespace dsv

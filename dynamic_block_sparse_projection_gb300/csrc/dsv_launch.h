@@ -24,9 +24,10 @@ struct HeadK {
 cudaError_t launch_predict(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s,
                            float* scores, void* ws, cudaStream_t st);
 size_t predict_ws_bytes(const dsv_shape& s);
-// Max-pooled predictor: per-token rank-r projections into `ws`, then the tile-maximum kernel.
+// Max-pooled predictor: per-token rank-r projections, split into bf16 parts in
+// the MMA layout, into `ws`; then the tile-maximum kernel (tcgen05).
 cudaError_t launch_predict_max(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s,
-                               float* scores, void* ws, cudaStream_t st);
+                               float* scores, void* ws, const Ctl& ctl, cudaStream_t st);
 size_t predict_max_ws_bytes(const dsv_shape& s);
 
 // Top-k, transposed lists.

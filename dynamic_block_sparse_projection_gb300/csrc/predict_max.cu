@@ -6,259 +6,483 @@
 // one score; predict.cu takes the mean, this file the largest logit:
 //   S[g, j] = max over i in group g, l in key block j of (Q_i W^Q) . (K_l W^K).
 // A maximum does not commute with pooling, so every token is projected and
-// every tile is formed: block^2 r FMAs per (g, j), on the CUDA cores in fp32.
+// every tile of logits is formed: an [N, N] x r contraction per (b, h), run
+// on the tensor cores.
 //
-// Kernel 1 projects 64 token rows of Q (or K) of one (b, h) per CTA to rank r,
-// the head's W staged once in shared memory, into the workspace
-// ([B*H*N, r] fp32 for each tensor).  Kernel 2 takes one query group and a run
-// of kJPerCta key blocks per CTA: the group's rank-r rows stay in shared
-// memory, each key tile is staged [rank][token] while the next one loads into
-// registers, a thread owns a (block/16) x (block/16) register tile of logits
-// summed by packed two-lane FMAs (per-lane rounding of fmaf), and the tile
-// maximum goes through warp shuffles and one shared-memory step.  fmaxf drops
-// a NaN logit.
+// Kernel 1 projects 64 token rows of Q (or K) of one (b, h) per CTA to rank r
+// in fp32 (the head's W staged once in shared memory) and splits each value
+// into two bf16 parts, v = hi + lo with |v - hi - lo| <= 2^-18 |v|.  Then
+//   q . k = hi_q.hi_k + hi_q.lo_k + lo_q.hi_k   (each term off by ~2^-16 of |q_c k_c|)
+// is ONE bf16 contraction over K = 3r: query rows are stored as [hi | hi | lo]
+// and key rows as [hi | lo | hi], zero-padded to a multiple of 16, in the
+// tensor core's K-major layout without swizzle (8-row x 8-element core
+// matrices of 128 contiguous bytes), one 128-token tile after another.
+//
+// Kernel 2: persistent CTAs; a CTA takes four (for r > 48: two) 128-token
+// query tiles of a (b, h) at a time against a run of key tiles.  Warp 0
+// copies the query tiles and the key tiles through a ring (plain bulk copies:
+// the workspace already holds the MMA layout), warp 1 issues one M=128, N=128, K=3r product (tcgen05,
+// fp32 accumulation) per (query tile, key tile) into one of four TMEM
+// accumulators, and warps 2-9, two groups of four taking alternate products,
+// read each accumulator back (one warp per TMEM lane quarter), take the
+// maximum of every block x block sub-tile and write the scores.  The three-input max.f32 used drops a NaN
+// logit, as fmaxf does.
 #include <cuda_bf16.h>
+#include <limits.h>
 
 #include "dsv_launch.h"
 
 namespace dsv {
 namespace {
 
-constexpr int kProjRows = 64;            // token rows per projection CTA (N is a multiple)
-constexpr int kJPerCta = 16;             // key blocks per tile CTA
+constexpr int kProjRows = 64;            // token rows per projection CTA
+constexpr int kTile = 128;               // tokens per MMA tile (M = N = 128)
 
-// grid (B*H*N / kProjRows, 2): blockIdx.y = 0 projects Q with W^Q, 1 projects K with W^K.
-// Thread t computes row t % 64 and the r/4 columns (t / 64) * r/4 ...
-template <int D, int R>
-__global__ void __launch_bounds__(256) lowrank_project_kernel(const __nv_bfloat16* __restrict__ Q,
-                                                              const __nv_bfloat16* __restrict__ K,
-                                                              const float* __restrict__ Wq,
-                                                              const float* __restrict__ Wk, int H, int N,
-                                                              float* __restrict__ qlr, float* __restrict__ klr) {
-  constexpr int XS = D + 1;              // padded row: a warp's 32 rows hit 32 banks
-  constexpr int RC = R / 4;              // output columns per thread (even: R % 8 == 0)
-  extern __shared__ float4 sm4[];
-  float* w_s = reinterpret_cast<float*>(sm4);   // [D][R]
-  float* x_s = w_s + D * R;                     // [kProjRows][XS]
-  const int t = threadIdx.x;
-  const long long row0 = (long long)blockIdx.x * kProjRows;
-  const int which = blockIdx.y;
-  const int h = (int)((row0 / N) % H);          // 64 rows never straddle a (b, h): N % 64 == 0
-  const uint4* X = reinterpret_cast<const uint4*>((which ? K : Q) + row0 * D);
-  const float4* W = reinterpret_cast<const float4*>((which ? Wk : Wq) + (long long)h * D * R);
-  float* out = (which ? klr : qlr) + row0 * R;
-  for (int i = t; i < D * R / 4; i += 256) reinterpret_cast<float4*>(w_s)[i] = __ldg(W + i);
-  for (int i = t; i < kProjRows * D / 8; i += 256) {
-    const int row = i / (D / 8), c8 = (i - row * (D / 8)) * 8;
-    const uint4 v = __ldcs(X + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      x_s[row * XS + c8 + 2 * e] = __uint_as_float(w[e] << 16);
-      x_s[row * XS + c8 + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-    }
-  }
-  __syncthreads();
-  const int row = t % kProjRows, c0 = (t / kProjRows) * RC;
-  float acc[RC];
-#pragma unroll
-  for (int m = 0; m < RC; ++m) acc[m] = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < D; ++c) {
-    const float x = x_s[row * XS + c];
-    const float2* wr = reinterpret_cast<const float2*>(w_s + c * R + c0);
-#pragma unroll
-    for (int m = 0; m < RC / 2; ++m) {
-      const float2 wv = wr[m];
-      acc[2 * m] = fmaf(x, wv.x, acc[2 * m]);
-      acc[2 * m + 1] = fmaf(x, wv.y, acc[2 * m + 1]);
-    }
-  }
-  float2* dst = reinterpret_cast<float2*>(out + (long long)row * R + c0);
-#pragma unroll
-  for (int m = 0; m < RC / 2; ++m) dst[m] = make_float2(acc[2 * m], acc[2 * m + 1]);
-}
-
-// One [BLOCK, R] fp32 tile of rank-r rows, moved through registers into a
-// [R][BLOCK] shared tile.  Slot i of the tile is row i % BLOCK, ranks
-// 4*(i / BLOCK) .. +3, so a warp's stores cover 32 consecutive rows of one
-// rank: 32 banks.
-template <int BLOCK, int R>
-struct TileIO {
-  static constexpr int NV = BLOCK * R / 4;                 // float4 slots
-  static constexpr int LPT = (NV + 255) / 256;             // slots per thread
-  float4 v[LPT];
-  __device__ __forceinline__ void load(const float4* __restrict__ src) {
-#pragma unroll
-    for (int p = 0; p < LPT; ++p) {
-      const int i = threadIdx.x + 256 * p;
-      if (i < NV) {
-        const int row = i % BLOCK, k4 = (i / BLOCK) * 4;
-        v[p] = __ldg(src + row * (R / 4) + k4 / 4);
-      }
-    }
-  }
-  __device__ __forceinline__ void store(float* __restrict__ dst) const {
-#pragma unroll
-    for (int p = 0; p < LPT; ++p) {
-      const int i = threadIdx.x + 256 * p;
-      if (i < NV) {
-        const int row = i % BLOCK, k4 = (i / BLOCK) * 4;
-        dst[(k4 + 0) * BLOCK + row] = v[p].x;
-        dst[(k4 + 1) * BLOCK + row] = v[p].y;
-        dst[(k4 + 2) * BLOCK + row] = v[p].z;
-        dst[(k4 + 3) * BLOCK + row] = v[p].w;
-      }
-    }
+// Workspace layout of one tensor's split rows.
+template <int R>
+struct MaxLayout {
+  static constexpr int KP = (3 * R + 15) / 16 * 16;   // contraction length, padded to the MMA's K = 16
+  static constexpr int KSTEPS = KP / 16;
+  static constexpr int LBO = 128;                     // bytes between core matrices along K
+  static constexpr int SBO = KP * 16;                 // bytes between 8-row groups
+  static constexpr int TILE_BYTES = kTile * KP * 2;
+  // byte offset of (row i of a tile, element e of the row)
+  __host__ __device__ static constexpr int offset(int i, int e) {
+    return (i >> 3) * SBO + (e >> 3) * 128 + (i & 7) * 16 + (e & 7) * 2;
   }
 };
 
-// grid (G * ceil(G / kJPerCta), 1, B*H).  CTA: query group g = blockIdx.x / chunks,
-// key blocks j0 .. j1-1.  Thread (tr, tc) = (t / 16, t % 16) owns tile rows
-// TM*tr .. TM*tr+TM-1 and columns 4*tc + 64*q .. +3 for q < TN/4.
-template <int BLOCK, int R>
-__global__ void __launch_bounds__(256) tile_max_kernel(const float* __restrict__ qlr, const float* __restrict__ klr,
-                                                       int G, int chunks, float* __restrict__ S) {
-  constexpr int TM = BLOCK / 16;         // rows per thread
-  constexpr int TN = BLOCK / 16;         // columns per thread
-  constexpr int NP = TN / 2;             // packed column pairs per row
+// grid (B*H*NT*kTile / kProjRows, 2): blockIdx.y = 0 projects Q with W^Q and
+// writes [hi | hi | lo], 1 projects K with W^K and writes [hi | lo | hi].
+// Rows past N (the last tile when N % 128 == 64) are written as zeros.
+template <int D, int R>
+__global__ void __launch_bounds__(256) lowrank_split_kernel(const __nv_bfloat16* __restrict__ Q,
+                                                            const __nv_bfloat16* __restrict__ K,
+                                                            const float* __restrict__ Wq,
+                                                            const float* __restrict__ Wk, int H, int N, int NT,
+                                                            uint8_t* __restrict__ qt, uint8_t* __restrict__ kt) {
+  using L = MaxLayout<R>;
+  constexpr int XS = D + 1;              // padded row: a warp's 32 rows hit 32 banks
+  constexpr int RS = R + 1;
+  constexpr int RC = R / 4;              // output columns per thread (even: R % 8 == 0)
   extern __shared__ float4 sm4[];
-  float* qs = reinterpret_cast<float*>(sm4);   // [R][BLOCK]
-  float* ks = qs + R * BLOCK;                  // [R][BLOCK]
-  __shared__ float red[8];
-  __shared__ float s_out[kJPerCta];
-  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const long long bh = blockIdx.z;
-  const int g = (int)(blockIdx.x / chunks);
-  const int j0 = (int)(blockIdx.x - (long long)g * chunks) * kJPerCta;
-  const int j1 = min(G, j0 + kJPerCta);
-  const float4* qsrc = reinterpret_cast<const float4*>(qlr + (bh * G + g) * (long long)BLOCK * R);
-  const float4* kbase = reinterpret_cast<const float4*>(klr + bh * G * (long long)BLOCK * R);
-  {
-    TileIO<BLOCK, R> q;
-    q.load(qsrc);
-    q.store(qs);
-  }
-  TileIO<BLOCK, R> kt;
-  kt.load(kbase + (long long)j0 * (BLOCK * R / 4));
-  const int tc = t & 15, tr = t >> 4;
-  for (int j = j0; j < j1; ++j) {
-    __syncthreads();                       // the previous tile's products are done with ks
-    kt.store(ks);
+  float* w_s = reinterpret_cast<float*>(sm4);   // [D][R]
+  float* x_s = w_s + D * R;                     // [kProjRows][XS], then the results [kProjRows][RS]
+  const int t = threadIdx.x;
+  const int which = blockIdx.y;
+  const long long prow0 = (long long)blockIdx.x * kProjRows;     // row of the padded space (NT * 128 per (b, h))
+  const long long bh = prow0 / ((long long)NT * kTile);
+  const int n0 = (int)(prow0 - bh * NT * kTile);
+  const bool live = n0 < N;              // N % 64 == 0: a 64-row slab is all tokens or all padding
+  if (live) {
+    const int h = (int)(bh % H);
+    const uint4* X = reinterpret_cast<const uint4*>((which ? K : Q) + (bh * N + n0) * D);
+    const float4* W = reinterpret_cast<const float4*>((which ? Wk : Wq) + (long long)h * D * R);
+    for (int i = t; i < D * R / 4; i += 256) reinterpret_cast<float4*>(w_s)[i] = __ldg(W + i);
+    for (int i = t; i < kProjRows * D / 8; i += 256) {
+      const int row = i / (D / 8), c8 = (i - row * (D / 8)) * 8;
+      const uint4 v = __ldcs(X + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x_s[row * XS + c8 + 2 * e] = __uint_as_float(w[e] << 16);
+        x_s[row * XS + c8 + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+      }
+    }
     __syncthreads();
-    if (j + 1 < j1) kt.load(kbase + (long long)(j + 1) * (BLOCK * R / 4));
-    uint64_t acc[TM][NP];
+    const int row = t % kProjRows, c0 = (t / kProjRows) * RC;
+    float acc[RC];
 #pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-      for (int m = 0; m < NP; ++m) acc[i][m] = 0ull;
+    for (int m = 0; m < RC; ++m) acc[m] = 0.f;
 #pragma unroll 4
-    for (int kk = 0; kk < R; ++kk) {
-      float a[TM];
+    for (int c = 0; c < D; ++c) {
+      const float x = x_s[row * XS + c];
+      const float2* wr = reinterpret_cast<const float2*>(w_s + c * R + c0);
 #pragma unroll
-      for (int p = 0; p < TM / 4; ++p) {
-        const float4 av = *reinterpret_cast<const float4*>(qs + kk * BLOCK + tr * TM + 4 * p);
-        a[4 * p] = av.x;
-        a[4 * p + 1] = av.y;
-        a[4 * p + 2] = av.z;
-        a[4 * p + 3] = av.w;
-      }
-      uint64_t b2[NP];
-#pragma unroll
-      for (int q = 0; q < TN / 4; ++q) {
-        const float4 bv = *reinterpret_cast<const float4*>(ks + kk * BLOCK + 64 * q + 4 * tc);
-        b2[2 * q] = f2_pack(bv.x, bv.y);
-        b2[2 * q + 1] = f2_pack(bv.z, bv.w);
-      }
-#pragma unroll
-      for (int i = 0; i < TM; ++i) {
-        const uint64_t a2 = f2_pack(a[i], a[i]);
-#pragma unroll
-        for (int m = 0; m < NP; ++m) acc[i][m] = fma2(a2, b2[m], acc[i][m]);
+      for (int m = 0; m < RC / 2; ++m) {
+        const float2 wv = wr[m];
+        acc[2 * m] = fmaf(x, wv.x, acc[2 * m]);
+        acc[2 * m + 1] = fmaf(x, wv.y, acc[2 * m + 1]);
       }
     }
-    float mx = -INFINITY;
+    __syncthreads();                     // x_s now holds the results
 #pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-      for (int m = 0; m < NP; ++m) {
-        float lo, hi;
-        f2_unpack(acc[i][m], lo, hi);
-        mx = fmaxf(mx, fmaxf(lo, hi));
-      }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red[w] = mx;
-    __syncthreads();
-    if (t == 0) {
-      float r = red[0];
-#pragma unroll
-      for (int q = 1; q < 8; ++q) r = fmaxf(r, red[q]);
-      s_out[j - j0] = r;
-    }
+    for (int m = 0; m < RC; ++m) x_s[row * RS + c0 + m] = acc[m];
   }
   __syncthreads();
-  if (t < j1 - j0) S[(bh * G + g) * (long long)G + j0 + t] = s_out[t];
+  // 16-byte pieces: (row, 8 consecutive elements of the padded row)
+  uint8_t* out = (which ? kt : qt) + (bh * NT + n0 / kTile) * (long long)L::TILE_BYTES;
+  const int i0 = n0 % kTile;
+  for (int it = t; it < kProjRows * (L::KP / 8); it += 256) {
+    const int row = it % kProjRows, grp = it / kProjRows;
+    const int e0 = grp * 8;
+    uint32_t w4[4] = {0u, 0u, 0u, 0u};
+    if (live && e0 < 3 * R) {
+      const int part = e0 / R, c = e0 - part * R;       // R % 8 == 0: a piece lies in one part
+      const bool lo = which ? (part == 1) : (part == 2);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float a = x_s[row * RS + c + 2 * e], b = x_s[row * RS + c + 2 * e + 1];
+        const float ah = __bfloat162float(__float2bfloat16_rn(a)), bhf = __bfloat162float(__float2bfloat16_rn(b));
+        w4[e] = lo ? pack_bf16x2(a - ah, b - bhf) : pack_bf16x2(a, b);
+      }
+    }
+    *reinterpret_cast<uint4*>(out + L::offset(i0 + row, e0)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  }
+}
+
+template <int R>
+struct MaxTraits {
+  using L = MaxLayout<R>;
+  static constexpr int TB = L::TILE_BYTES;
+  static constexpr int ZC = 8;                                   // key tiles per cross-warp combine
+  static constexpr int MISC = 4096;                              // barriers, partial maxima, slots
+  // query tiles per CTA: 4 where they and a two-stage key ring fit (each key
+  // tile copied to shared memory then serves 4 products), else 2
+  static constexpr int NQ = 6 * TB + 1024 + MISC <= 227 * 1024 ? 4 : 2;
+  static constexpr int RING_ROOM = 227 * 1024 - 1024 - NQ * TB - MISC;
+  static constexpr int NSTAGE = RING_ROOM / TB >= 4 ? 4 : RING_ROOM / TB;
+  static constexpr int NACC = 4;                                 // TMEM accumulators of 128 columns
+  static constexpr int SMEM_USED = 1024 + NQ * TB + NSTAGE * TB + MISC;
+  // at least 120 KB, so that one CTA holds an SM (and its whole TMEM)
+  static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  static_assert(NSTAGE >= 2, "tile too large for a two-stage ring");
+};
+
+constexpr int kMaxThreads = 320;         // producer, MMA, two groups of 4 reduction warps
+
+enum : unsigned int { MW_A = 1, MW_BFULL, MW_BEMPTY, MW_TFULL, MW_TEMPTY, MW_DRAIN };
+
+// Order-preserving map of a non-NaN float to a signed integer (and back):
+// negative values have their magnitude bits flipped.
+__device__ __forceinline__ int float_key(float f) {
+  const int b = __float_as_int(f);
+  return b >= 0 ? b : b ^ 0x7FFFFFFF;
+}
+__device__ __forceinline__ float key_float(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7FFFFFFF); }
+
+// Work is a sequence of steps w = ((b*H + h) * NG + tg) * NT + c: query-tile
+// group tg (NQ query tiles from tg*NQ) of head (b, h) against key tile c.
+// Persistent CTAs, one per SM, each take one contiguous range of steps of
+// equal length (so no wave is left partly empty), reloading the query tiles
+// when the range crosses into the next group.
+struct MaxStep {
+  long long bh;
+  int tq0, nq, c;
+  long long item;
+};
+template <int NQ>
+__device__ __forceinline__ MaxStep max_step(long long w, int NT) {
+  const int NG = (NT + NQ - 1) / NQ;
+  MaxStep st;
+  st.item = w / NT;
+  st.c = (int)(w - st.item * NT);
+  st.bh = st.item / NG;
+  st.tq0 = (int)(st.item - st.bh * NG) * NQ;
+  st.nq = NT - st.tq0 < NQ ? NT - st.tq0 : NQ;
+  return st;
 }
 
 template <int BLOCK, int R>
-cudaError_t launch_tile_max(const float* qlr, const float* klr, const dsv_shape& s, float* scores, cudaStream_t st) {
-  const int G = s.N / BLOCK;
-  const int chunks = (G + kJPerCta - 1) / kJPerCta;
-  const int smem = 2 * R * BLOCK * (int)sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(tile_max_kernel<BLOCK, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+__global__ void __launch_bounds__(kMaxThreads, 1)
+    tile_max_mma_kernel(const uint8_t* __restrict__ qt, const uint8_t* __restrict__ kt, int NT, int G,
+                        long long steps, float* __restrict__ S, Ctl ctl) {
+  using T = MaxTraits<R>;
+  using L = typename T::L;
+  constexpr int TB = T::TB, NSTAGE = T::NSTAGE, NQ = T::NQ;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sA = smem_align1024(smem_raw);        // NQ query tiles
+  uint8_t* sB = sA + NQ * TB;                     // NSTAGE key tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + NSTAGE * TB);
+  uint64_t* a_full = bars;
+  uint64_t* a_free = bars + 1;                    // the products on the current query tiles are done
+  uint64_t* b_full = bars + 2;
+  uint64_t* b_empty = b_full + NSTAGE;
+  uint64_t* t_full = b_empty + NSTAGE;            // [NACC]
+  uint64_t* t_empty = t_full + T::NACC;           // [NACC]
+  uint64_t* drain = t_empty + T::NACC;
+  int* part = reinterpret_cast<int*>(drain + 1);  // [2][ZC][NQ][4 quarters][2 halves], ordered keys
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(part + 2 * T::ZC * NQ * 4 * 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long w0 = steps * blockIdx.x / gridDim.x, w1 = steps * (blockIdx.x + 1) / gridDim.x;
+  const unsigned int kid = (unsigned int)KID_MAXPOOL << 8;
+
+  if (threadIdx.x == 0) {
+    mbar_init(a_full, 1);
+    mbar_init(a_free, 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int a = 0; a < T::NACC; ++a) {
+      mbar_init(&t_full[a], 1);
+      mbar_init(&t_empty[a], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- copies ----------------
+      long long cur = -1;
+      int a_loads = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (long long w = w0; ok && w < w1; ++w) {
+        const long long k = w - w0;
+        const MaxStep st = max_step<NQ>(w, NT);
+        if (st.item != cur) {
+          // the query tiles are overwritten once every product reading them is done
+          if (a_loads > 0 &&
+              !mbar_wait(a_free, (uint32_t)(a_loads - 1) & 1u, abort_flag, ctl, kid | MW_A))
+            break;
+          mbar_arrive_expect_tx(a_full, (uint32_t)(st.nq * TB));
+          for (int rt = 0; rt < st.nq; ++rt)
+            bulk_load(sA + rt * TB, qt + (st.bh * NT + st.tq0 + rt) * (long long)TB, TB, a_full);
+          ++a_loads;
+          cur = st.item;
+        }
+        const int s = (int)(k % NSTAGE);
+        if (!mbar_wait(&b_empty[s], ((uint32_t)(k / NSTAGE) & 1u) ^ 1u, abort_flag, ctl, kid | MW_BEMPTY)) break;
+        mbar_arrive_expect_tx(&b_full[s], TB);
+        bulk_load(sB + s * TB, kt + (st.bh * NT + st.c) * (long long)TB, TB, &b_full[s]);
+        issued = k + 1;
+      }
+      // every copy started must land before the CTA exits
+      if (a_loads > 0) mbar_wait(a_full, (uint32_t)(a_loads - 1) & 1u, nullptr, ctl, kid | MW_DRAIN);
+      for (long long k = (issued > NSTAGE ? issued - NSTAGE : 0); k < issued; ++k)
+        mbar_wait(&b_full[k % NSTAGE], (uint32_t)(k / NSTAGE) & 1u, nullptr, ctl, kid | MW_DRAIN);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    // The next key tile's barrier and the next product's accumulator are
+    // tested one step early; a wait whose test found the phase complete is
+    // free.
+    constexpr uint32_t ID = idesc_bf16_f32(kTile, kTile, false, false);
+    const uint64_t a0 = sdesc_noswz(smem_u32(sA), L::LBO, L::SBO);
+    const uint64_t b0 = sdesc_noswz(smem_u32(sB), L::LBO, L::SBO);
+    long long cur = -1;
+    int a_uses = 0;
+    long long p = 0;                                // product number: accumulator p % 4, its use p / 4
+    bool ok = true;
+    uint32_t tb = 0u, te = 1u;                      // product 0's accumulator is free
+    for (long long w = w0; ok && w < w1; ++w) {
+      const long long k = w - w0;
+      const MaxStep st = max_step<NQ>(w, NT);
+      if (st.item != cur) {
+        if (a_uses > 0) mma_commit_w(a_free);
+        if (!mbar_wait_warp(a_full, (uint32_t)a_uses & 1u, abort_flag, ctl, kid | MW_A)) break;
+        ++a_uses;
+        cur = st.item;
+      }
+      const int s = (int)(k % NSTAGE);
+      if (!mbar_wait_warp_tested(&b_full[s], (uint32_t)(k / NSTAGE) & 1u, tb, abort_flag, ctl, kid | MW_BFULL))
+        break;
+      tb = w + 1 < w1 ? mbar_test(&b_full[(k + 1) % NSTAGE], (uint32_t)((k + 1) / NSTAGE) & 1u) : 0u;
+      for (int rt = 0; rt < st.nq; ++rt, ++p) {
+        const int buf = (int)(p & 3);
+        if (!mbar_wait_warp_tested(&t_empty[buf], ((uint32_t)(p >> 2) & 1u) ^ 1u, te, abort_flag, ctl,
+                                   kid | MW_TEMPTY)) {
+          ok = false;
+          break;
+        }
+        te = mbar_test(&t_empty[(p + 1) & 3], ((uint32_t)((p + 1) >> 2) & 1u) ^ 1u);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < L::KSTEPS; ++kk)
+          mma_ss_w(tmem + (uint32_t)(buf * kTile), desc_off(a0, (uint32_t)(rt * TB + kk * 2 * L::LBO)),
+                   desc_off(b0, (uint32_t)(s * TB + kk * 2 * L::LBO)), ID, kk > 0 ? 1u : 0u);
+        mma_commit_w(&t_full[buf]);
+      }
+      if (ok) mma_commit_w(&b_empty[s]);
+    }
+    mma_commit_w(drain);
+    mbar_wait_warp(drain, 0, nullptr, ctl, kid | MW_DRAIN);
+  } else {
+    // ------------- reduction warps: group grp takes the products p with p % 2 == grp; -------------
+    // ------------- warp qd of a group reads TMEM lane quarter qd (tile rows 32*qd .. +31) -----------
+    // Per product: the row maxima over key columns 0..63 and 64..127, then
+    // the warp's maxima (redux on order-preserving integer keys), kept in
+    // shared memory.  Two groups work on alternate products, so that the
+    // latency of one product's waits, loads and reductions overlaps the
+    // other's.  Every ZC steps all eight warps meet at a named barrier and
+    // combine the quarters into scores.  Every warp runs every step and
+    // barrier, also after a wait has given up (then without waits or TMEM
+    // reads), so that no warp is left at the barrier.
+    const int qd = warp & 3, grp = (warp - 2) >> 2;
+    const int tid = threadIdx.x - 64;               // 0 .. 255
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    bool ok = true;
+    long long p = 0;
+    for (long long w = w0; w < w1; ++w) {
+      const long long k = w - w0;
+      const int z = (int)(k % T::ZC), zb = (int)(k / T::ZC) & 1;
+      const int nq = max_step<NQ>(w, NT).nq;
+      for (int rt = 0; rt < nq; ++rt, ++p) {
+        if ((int)(p & 1) != grp) continue;
+        const int buf = (int)(p & 3);
+        if (ok) ok = mbar_wait_warp(&t_full[buf], (uint32_t)(p >> 2) & 1u, abort_flag, ctl, kid | MW_TFULL);
+        int key[2] = {INT_MIN, INT_MIN};
+        if (ok) {
+          tc_fence_after();
+          uint32_t v[128];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_off + (uint32_t)(buf * kTile + 32 * q), v + 32 * q);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&t_empty[buf]);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t* x = v + 64 * hh;
+            float a0 = __uint_as_float(x[0]), a1 = __uint_as_float(x[1]), a2 = __uint_as_float(x[2]),
+                  a3 = __uint_as_float(x[3]);
+#pragma unroll
+            for (int i = 4; i < 60; i += 8) {       // columns 4 .. 59
+              a0 = max3f(a0, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
+              a1 = max3f(a1, __uint_as_float(x[i + 2]), __uint_as_float(x[i + 3]));
+              a2 = max3f(a2, __uint_as_float(x[i + 4]), __uint_as_float(x[i + 5]));
+              a3 = max3f(a3, __uint_as_float(x[i + 6]), __uint_as_float(x[i + 7]));
+            }
+            a0 = max3f(a0, __uint_as_float(x[60]), __uint_as_float(x[61]));
+            a1 = max3f(a1, __uint_as_float(x[62]), __uint_as_float(x[63]));
+            float m = fmaxf(max3f(a0, a1, a2), a3);   // NaN only if all 64 logits are NaN
+            if (m != m) m = -INFINITY;
+            key[hh] = __reduce_max_sync(0xffffffffu, float_key(m));
+          }
+        }
+        if (lane == 0) {
+          int* pp = part + (((zb * T::ZC + z) * NQ + rt) * 4 + qd) * 2;
+          pp[0] = key[0];
+          pp[1] = key[1];
+        }
+      }
+      if (z == T::ZC - 1 || w == w1 - 1) {
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        // one score per thread: (step k - z + zz, query tile rt[, query half ga, key half jb])
+        const int per = BLOCK == 128 ? 1 : 4;
+        const int item = tid / per, sub = tid % per;
+        const int zz = item / NQ, rt = item % NQ;
+        if (ok && zz <= z) {
+          const MaxStep st = max_step<NQ>(w - z + zz, NT);
+          if (rt < st.nq) {
+            const int* pb = part + (((zb * T::ZC + zz) * NQ + rt) * 4) * 2;   // [quarter][half]
+            const int tq = st.tq0 + rt;
+            if (BLOCK == 128) {
+              const int m = max(max(max(pb[0], pb[1]), max(pb[2], pb[3])), max(max(pb[4], pb[5]), max(pb[6], pb[7])));
+              S[(st.bh * G + tq) * (long long)G + st.c] = key_float(m);
+            } else {
+              // rows 0..63 (quarters 0, 1) are group 2*tq, rows 64..127 group 2*tq + 1;
+              // columns 0..63 key block 2*c, 64..127 key block 2*c + 1
+              const int ga = sub >> 1, jb = sub & 1;
+              const int g = 2 * tq + ga, j = 2 * st.c + jb;
+              if (g < G && j < G)
+                S[(st.bh * G + g) * (long long)G + j] =
+                    key_float(max(pb[(2 * ga) * 2 + jb], pb[(2 * ga + 1) * 2 + jb]));
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+template <int R>
+cudaError_t launch_tile_max(const uint8_t* qt, const uint8_t* kt, const dsv_shape& s, int NT, float* scores,
+                            const Ctl& ctl, cudaStream_t st) {
+  const int G = s.N / s.block;
+  auto kern = s.block == 128 ? tile_max_mma_kernel<128, R> : tile_max_mma_kernel<64, R>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, MaxTraits<R>::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((long long)G * chunks), 1, (unsigned)(s.B * s.H));
-  tile_max_kernel<BLOCK, R><<<grid, 256, smem, st>>>(qlr, klr, G, chunks, scores);
+  int dev = 0, nsm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  constexpr int NQ = MaxTraits<R>::NQ;
+  const long long steps = (long long)s.B * s.H * ((NT + NQ - 1) / NQ) * NT;
+  const unsigned grid = (unsigned)(steps < nsm ? steps : nsm);
+  kern<<<grid, kMaxThreads, MaxTraits<R>::SMEM, st>>>(qt, kt, NT, G, steps, scores, ctl);
   return cudaGetLastError();
 }
 
 template <int D, int R>
-cudaError_t launch_project(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s,
-                           float* qlr, float* klr, cudaStream_t st) {
+cudaError_t launch_split(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s, int NT,
+                         uint8_t* qt, uint8_t* kt, cudaStream_t st) {
   const int smem = (D * R + kProjRows * (D + 1)) * (int)sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(lowrank_project_kernel<D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(lowrank_split_kernel<D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long rows = (long long)s.B * s.H * s.N;
+  const long long rows = (long long)s.B * s.H * NT * kTile;
   dim3 grid((unsigned)(rows / kProjRows), 2);
-  lowrank_project_kernel<D, R><<<grid, 256, smem, st>>>(static_cast<const __nv_bfloat16*>(Q),
-                                                        static_cast<const __nv_bfloat16*>(K), Wq, Wk, s.H, s.N, qlr,
-                                                        klr);
+  lowrank_split_kernel<D, R><<<grid, 256, smem, st>>>(static_cast<const __nv_bfloat16*>(Q),
+                                                      static_cast<const __nv_bfloat16*>(K), Wq, Wk, s.H, s.N, NT,
+                                                      qt, kt);
   return cudaGetLastError();
+}
+
+size_t tiles_bytes(const dsv_shape& s, int tile_bytes) {
+  const size_t NT = ((size_t)s.N + kTile - 1) / kTile;
+  return align256((size_t)s.B * s.H * NT * (size_t)tile_bytes);
 }
 
 template <int R>
 cudaError_t launch_predict_max_r(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s,
-                                 float* qlr, float* klr, float* scores, cudaStream_t st) {
-  cudaError_t e = s.d == 128 ? launch_project<128, R>(Q, K, Wq, Wk, s, qlr, klr, st)
-                             : launch_project<64, R>(Q, K, Wq, Wk, s, qlr, klr, st);
+                                 float* scores, void* ws, const Ctl& ctl, cudaStream_t st) {
+  const int NT = (s.N + kTile - 1) / kTile;
+  uint8_t* qt = static_cast<uint8_t*>(ws);
+  uint8_t* kt = qt + tiles_bytes(s, MaxLayout<R>::TILE_BYTES);
+  cudaError_t e = s.d == 128 ? launch_split<128, R>(Q, K, Wq, Wk, s, NT, qt, kt, st)
+                             : launch_split<64, R>(Q, K, Wq, Wk, s, NT, qt, kt, st);
   if (e != cudaSuccess) return e;
-  return s.block == 128 ? launch_tile_max<128, R>(qlr, klr, s, scores, st)
-                        : launch_tile_max<64, R>(qlr, klr, s, scores, st);
+  return launch_tile_max<R>(qt, kt, s, NT, scores, ctl, st);
+}
+
+template <int R>
+size_t ws_bytes_r(const dsv_shape& s) {
+  return 2 * tiles_bytes(s, MaxLayout<R>::TILE_BYTES);
 }
 
 }  // namespace
 
 size_t predict_max_ws_bytes(const dsv_shape& s) {
-  const size_t rows = (size_t)s.B * s.H * (size_t)s.N;
-  return 2 * align256(rows * (size_t)s.r * sizeof(float));
+  switch (s.r) {
+    case 8: return ws_bytes_r<8>(s);
+    case 16: return ws_bytes_r<16>(s);
+    case 24: return ws_bytes_r<24>(s);
+    case 32: return ws_bytes_r<32>(s);
+    case 40: return ws_bytes_r<40>(s);
+    case 48: return ws_bytes_r<48>(s);
+    case 56: return ws_bytes_r<56>(s);
+    default: return ws_bytes_r<64>(s);
+  }
 }
 
 cudaError_t launch_predict_max(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s,
-                               float* scores, void* ws, cudaStream_t st) {
-  const size_t rows = (size_t)s.B * s.H * (size_t)s.N;
-  float* qlr = static_cast<float*>(ws);
-  float* klr = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows * (size_t)s.r * sizeof(float)));
+                               float* scores, void* ws, const Ctl& ctl, cudaStream_t st) {
   switch (s.r) {
-    case 8: return launch_predict_max_r<8>(Q, K, Wq, Wk, s, qlr, klr, scores, st);
-    case 16: return launch_predict_max_r<16>(Q, K, Wq, Wk, s, qlr, klr, scores, st);
-    case 24: return launch_predict_max_r<24>(Q, K, Wq, Wk, s, qlr, klr, scores, st);
-    case 32: return launch_predict_max_r<32>(Q, K, Wq, Wk, s, qlr, klr, scores, st);
-    case 40: return launch_predict_max_r<40>(Q, K, Wq, Wk, s, qlr, klr, scores, st);
-    case 48: return launch_predict_max_r<48>(Q, K, Wq, Wk, s, qlr, klr, scores, st);
-    case 56: return launch_predict_max_r<56>(Q, K, Wq, Wk, s, qlr, klr, scores, st);
-    default: return launch_predict_max_r<64>(Q, K, Wq, Wk, s, qlr, klr, scores, st);
+    case 8: return launch_predict_max_r<8>(Q, K, Wq, Wk, s, scores, ws, ctl, st);
+    case 16: return launch_predict_max_r<16>(Q, K, Wq, Wk, s, scores, ws, ctl, st);
+    case 24: return launch_predict_max_r<24>(Q, K, Wq, Wk, s, scores, ws, ctl, st);
+    case 32: return launch_predict_max_r<32>(Q, K, Wq, Wk, s, scores, ws, ctl, st);
+    case 40: return launch_predict_max_r<40>(Q, K, Wq, Wk, s, scores, ws, ctl, st);
+    case 48: return launch_predict_max_r<48>(Q, K, Wq, Wk, s, scores, ws, ctl, st);
+    case 56: return launch_predict_max_r<56>(Q, K, Wq, Wk, s, scores, ws, ctl, st);
+    default: return launch_predict_max_r<64>(Q, K, Wq, Wk, s, scores, ws, ctl, st);
   }
 }
 

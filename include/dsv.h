@@ -92,13 +92,19 @@ dsv_status dsv_predict_scores(const void* Q, const void* K, const float* Wq, con
  *   scores[b,h,g,j] = max over tokens i of group g and l of key block j of
  *                     (Q[b,h,i] W^Q[h]) . (K[b,h,l] W^K[h])     (fp32, no scale)
  *
- * Every token is projected and every tile formed (block^2 * r FMAs per
- * (g, j), fp32 on the CUDA cores).  A NaN logit is dropped by the maximum.
+ * Every token is projected and every tile formed: an [N, N] x r contraction
+ * per (b, h), on the tensor cores.  Each fp32 projection is split into two
+ * bf16 parts (v = hi + lo to 2^-18 relative) and a logit is taken as
+ * hi.hi + hi.lo + lo.hi, one bf16 contraction of length 3r with fp32
+ * accumulation (~1e-5 of the logit scale against the fp32 value).  A NaN
+ * logit is dropped by the maximum.
  * Arguments and layout as dsv_predict_scores, except:
  * workspace >= dsv_predict_max_workspace_bytes(s) bytes, 256-byte aligned
- *           (holds the rank-r projection of every token of Q and K:
- *           2 * B*H*N*r fp32).
- * DSV_ERR_UNSUPPORTED also when G * ceil(G / 16) >= 2^31.
+ *           (holds every token's split rank-r row of Q and of K in the MMA
+ *           layout: 2 * B*H*ceil(N/128)*128 rows of round_up(3r, 16) bf16).
+ * Waits inside the kernel are bounded like the attention kernels'
+ * (dsv_set_wait_limit_ns); one that runs out is reported as DSV_ERR_TIMEOUT
+ * through dsv_get_device_error.
  * The scores feed dsv_topk_blocks or dsv_topk_mass_blocks unchanged.
  * ------------------------------------------------------------------------ */
 size_t dsv_predict_max_workspace_bytes(dsv_shape s);
