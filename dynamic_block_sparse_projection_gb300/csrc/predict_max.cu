@@ -9,8 +9,8 @@
 // every tile of logits is formed: an [N, N] x r contraction per (b, h), run
 // on the tensor cores.
 //
-// Kernel 1 projects 64 token rows of Q (or K) of one (b, h) per CTA to rank r
-// in fp32 (the head's W staged once in shared memory) and splits each value
+// Kernel 1 projects one 128-token tile of Q (or K) of one (b, h) per CTA to
+// rank r in fp32 (the head's W staged in shared memory) and splits each value
 // into two bf16 parts, v = hi + lo with |v - hi - lo| <= 2^-18 |v|.  Then
 //   q . k = hi_q.hi_k + hi_q.lo_k + lo_q.hi_k   (each term off by ~2^-16 of |q_c k_c|)
 // is ONE bf16 contraction over K = 3r: query rows are stored as [hi | hi | lo]
@@ -35,7 +35,6 @@
 namespace dsv {
 namespace {
 
-constexpr int kProjRows = 64;            // token rows per projection CTA
 constexpr int kTile = 128;               // tokens per MMA tile (M = N = 128)
 
 // Workspace layout of one tensor's split rows.
@@ -52,82 +51,94 @@ struct MaxLayout {
   }
 };
 
-// grid (B*H*NT*kTile / kProjRows, 2): blockIdx.y = 0 projects Q with W^Q and
-// writes [hi | hi | lo], 1 projects K with W^K and writes [hi | lo | hi].
-// Rows past N (the last tile when N % 128 == 64) are written as zeros.
+// grid (B*H*NT, 2), 128 threads: one 128-token tile per CTA, one token row per
+// thread.  blockIdx.y = 0 projects Q with W^Q and writes [hi | hi | lo], 1
+// projects K with W^K and writes [hi | lo | hi].  The head's W sits in shared
+// memory as pairs (W[2m][c], W[2m+1][c]), so that a thread's row (in
+// registers, bf16 pairs) meets it with packed two-lane FMAs; the two lanes of
+// each sum are added at the end.  Rows past N (the last tile when
+// N % 128 == 64) are written as zeros.
 template <int D, int R>
-__global__ void __launch_bounds__(256) lowrank_split_kernel(const __nv_bfloat16* __restrict__ Q,
-                                                            const __nv_bfloat16* __restrict__ K,
-                                                            const float* __restrict__ Wq,
-                                                            const float* __restrict__ Wk, int H, int N, int NT,
-                                                            uint8_t* __restrict__ qt, uint8_t* __restrict__ kt) {
+__global__ void __launch_bounds__(kTile) lowrank_split_kernel(const __nv_bfloat16* __restrict__ Q,
+                                                              const __nv_bfloat16* __restrict__ K,
+                                                              const float* __restrict__ Wq,
+                                                              const float* __restrict__ Wk, int H, int N, int NT,
+                                                              uint8_t* __restrict__ qt, uint8_t* __restrict__ kt) {
   using L = MaxLayout<R>;
-  constexpr int XS = D + 1;              // padded row: a warp's 32 rows hit 32 banks
-  constexpr int RS = R + 1;
-  constexpr int RC = R / 4;              // output columns per thread (even: R % 8 == 0)
   extern __shared__ float4 sm4[];
-  float* w_s = reinterpret_cast<float*>(sm4);   // [D][R]
-  float* x_s = w_s + D * R;                     // [kProjRows][XS], then the results [kProjRows][RS]
+  float2* w2 = reinterpret_cast<float2*>(sm4);  // [D/2][R]: (W[2m][c], W[2m+1][c])
   const int t = threadIdx.x;
   const int which = blockIdx.y;
-  const long long prow0 = (long long)blockIdx.x * kProjRows;     // row of the padded space (NT * 128 per (b, h))
-  const long long bh = prow0 / ((long long)NT * kTile);
-  const int n0 = (int)(prow0 - bh * NT * kTile);
-  const bool live = n0 < N;              // N % 64 == 0: a 64-row slab is all tokens or all padding
-  if (live) {
-    const int h = (int)(bh % H);
-    const uint4* X = reinterpret_cast<const uint4*>((which ? K : Q) + (bh * N + n0) * D);
-    const float4* W = reinterpret_cast<const float4*>((which ? Wk : Wq) + (long long)h * D * R);
-    for (int i = t; i < D * R / 4; i += 256) reinterpret_cast<float4*>(w_s)[i] = __ldg(W + i);
-    for (int i = t; i < kProjRows * D / 8; i += 256) {
-      const int row = i / (D / 8), c8 = (i - row * (D / 8)) * 8;
-      const uint4 v = __ldcs(X + i);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        x_s[row * XS + c8 + 2 * e] = __uint_as_float(w[e] << 16);
-        x_s[row * XS + c8 + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-      }
-    }
-    __syncthreads();
-    const int row = t % kProjRows, c0 = (t / kProjRows) * RC;
-    float acc[RC];
-#pragma unroll
-    for (int m = 0; m < RC; ++m) acc[m] = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < D; ++c) {
-      const float x = x_s[row * XS + c];
-      const float2* wr = reinterpret_cast<const float2*>(w_s + c * R + c0);
-#pragma unroll
-      for (int m = 0; m < RC / 2; ++m) {
-        const float2 wv = wr[m];
-        acc[2 * m] = fmaf(x, wv.x, acc[2 * m]);
-        acc[2 * m + 1] = fmaf(x, wv.y, acc[2 * m + 1]);
-      }
-    }
-    __syncthreads();                     // x_s now holds the results
-#pragma unroll
-    for (int m = 0; m < RC; ++m) x_s[row * RS + c0 + m] = acc[m];
+  const long long tile = blockIdx.x;            // (b*H + h) * NT + tile index
+  const long long bh = tile / NT;
+  const int n = (int)(tile - bh * NT) * kTile + t;
+  const float* W = (which ? Wk : Wq) + (bh % H) * (long long)D * R;
+  for (int i = t; i < D * R / 2; i += kTile) {
+    const int m = i / R, c = i - m * R;
+    w2[i] = make_float2(__ldg(W + (2 * m) * R + c), __ldg(W + (2 * m + 1) * R + c));
   }
   __syncthreads();
-  // 16-byte pieces: (row, 8 consecutive elements of the padded row)
-  uint8_t* out = (which ? kt : qt) + (bh * NT + n0 / kTile) * (long long)L::TILE_BYTES;
-  const int i0 = n0 % kTile;
-  for (int it = t; it < kProjRows * (L::KP / 8); it += 256) {
-    const int row = it % kProjRows, grp = it / kProjRows;
-    const int e0 = grp * 8;
-    uint32_t w4[4] = {0u, 0u, 0u, 0u};
-    if (live && e0 < 3 * R) {
-      const int part = e0 / R, c = e0 - part * R;       // R % 8 == 0: a piece lies in one part
-      const bool lo = which ? (part == 1) : (part == 2);
+  uint8_t* out = (which ? kt : qt) + tile * (long long)L::TILE_BYTES;
+  // outputs per pass (bounds the accumulator registers); divides R, so that a
+  // pass never reads W or writes pieces past column R
+  constexpr int RH = R % 16 == 0 ? 16 : 8;
+  static_assert(R % RH == 0 && RH % 8 == 0, "pass width must divide R");
+  if (n < N) {
+    // the whole row first (16 loads in flight), then the products, RH outputs at a time
+    const uint4* X = reinterpret_cast<const uint4*>((which ? K : Q) + (bh * N + n) * D);
+    uint32_t xw[D / 2];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float a = x_s[row * RS + c + 2 * e], b = x_s[row * RS + c + 2 * e + 1];
-        const float ah = __bfloat162float(__float2bfloat16_rn(a)), bhf = __bfloat162float(__float2bfloat16_rn(b));
-        w4[e] = lo ? pack_bf16x2(a - ah, b - bhf) : pack_bf16x2(a, b);
+    for (int q = 0; q < D / 8; ++q) {
+      const uint4 v = __ldg(X + q);
+      xw[4 * q] = v.x;
+      xw[4 * q + 1] = v.y;
+      xw[4 * q + 2] = v.z;
+      xw[4 * q + 3] = v.w;
+    }
+#pragma unroll 1
+    for (int c0 = 0; c0 < R; c0 += RH) {
+      uint64_t acc[RH];
+#pragma unroll
+      for (int c = 0; c < RH; ++c) acc[c] = 0ull;
+#pragma unroll
+      for (int m = 0; m < D / 2; ++m) {
+        const uint64_t xp = f2_pack(__uint_as_float(xw[m] << 16), __uint_as_float(xw[m] & 0xFFFF0000u));
+        const float4* wr = reinterpret_cast<const float4*>(w2 + m * R + c0);
+#pragma unroll
+        for (int c = 0; c < RH; c += 2) {
+          const float4 ww = wr[c / 2];
+          acc[c] = fma2(xp, f2_pack(ww.x, ww.y), acc[c]);
+          acc[c + 1] = fma2(xp, f2_pack(ww.z, ww.w), acc[c + 1]);
+        }
+      }
+      float v[RH], vl[RH];                        // the values and their low bf16 parts
+#pragma unroll
+      for (int c = 0; c < RH; ++c) {
+        float lo, hi;
+        f2_unpack(acc[c], lo, hi);
+        v[c] = lo + hi;
+        vl[c] = v[c] - __bfloat162float(__float2bfloat16_rn(v[c]));
+      }
+      // 16-byte pieces of the three parts: Q rows [hi | hi | lo], K rows [hi | lo | hi]
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {
+        const float* src = (which ? (part == 1) : (part == 2)) ? vl : v;
+#pragma unroll
+        for (int pc = 0; pc < RH; pc += 8) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) w4[e] = pack_bf16x2(src[pc + 2 * e], src[pc + 2 * e + 1]);
+          *reinterpret_cast<uint4*>(out + L::offset(t, part * R + c0 + pc)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
       }
     }
-    *reinterpret_cast<uint4*>(out + L::offset(i0 + row, e0)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+#pragma unroll
+    for (int e0 = 3 * R; e0 < L::KP; e0 += 8)
+      *reinterpret_cast<uint4*>(out + L::offset(t, e0)) = make_uint4(0u, 0u, 0u, 0u);
+  } else {
+#pragma unroll
+    for (int e0 = 0; e0 < L::KP; e0 += 8)
+      *reinterpret_cast<uint4*>(out + L::offset(t, e0)) = make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -423,15 +434,14 @@ cudaError_t launch_tile_max(const uint8_t* qt, const uint8_t* kt, const dsv_shap
 template <int D, int R>
 cudaError_t launch_split(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s, int NT,
                          uint8_t* qt, uint8_t* kt, cudaStream_t st) {
-  const int smem = (D * R + kProjRows * (D + 1)) * (int)sizeof(float);
+  const int smem = D * R * (int)sizeof(float);
   cudaError_t e =
       cudaFuncSetAttribute(lowrank_split_kernel<D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long rows = (long long)s.B * s.H * NT * kTile;
-  dim3 grid((unsigned)(rows / kProjRows), 2);
-  lowrank_split_kernel<D, R><<<grid, 256, smem, st>>>(static_cast<const __nv_bfloat16*>(Q),
-                                                      static_cast<const __nv_bfloat16*>(K), Wq, Wk, s.H, s.N, NT,
-                                                      qt, kt);
+  dim3 grid((unsigned)((long long)s.B * s.H * NT), 2);
+  lowrank_split_kernel<D, R><<<grid, kTile, smem, st>>>(static_cast<const __nv_bfloat16*>(Q),
+                                                        static_cast<const __nv_bfloat16*>(K), Wq, Wk, s.H, s.N, NT,
+                                                        qt, kt);
   return cudaGetLastError();
 }
 
