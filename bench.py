@@ -39,7 +39,6 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 # fp32 FMA peak of the CUDA cores (152 SMs x 128 lanes x 2 FLOP at the 2.07 GHz maximum SM clock)
-FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def parse_args(argv=None):
@@ -487,14 +486,17 @@ def roofline_entry(dom, per_call, w, hp, peaks, peak_src, bf16_peak=None, bf16_k
                 "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
                 "traffic": traffic, "traffic_source": tnote}
     if dom == "predict" and hp.scores == "max":
-        # every logit of every tile: 2 * r FLOP per (query token, key token) pair, fp32 FMA on the CUDA cores
+        # every logit of every tile: 2 * r FLOP per (query token, key token) pair; the tensor core runs
+        # it as one bf16 contraction of length 3r (hi/lo split of both projections), 3x the FLOPs
         flops = 2.0 * B * H * N * N * w.r
         achieved = flops / (per_call[dom] * 1e-3) / 1e12
-        peak = FP32_FMA_TFLOPS
-        return {"kernel": "dsv_predict_scores_max", "bound": "alu", "achieved": round(achieved, 3), "peak": peak,
+        peak = peaks["bf16_tflops"]
+        return {"kernel": "dsv_predict_scores_max", "bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "algorithmic": f"2*r FLOP per (query, key) token pair x {B * H * N * N} pairs",
-                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz", "traffic": None}
+                "executed_frac": round(3 * achieved / peak, 4),
+                "algorithmic": f"2*r FLOP per (query, key) token pair x {B * H * N * N} pairs (executed: 3x, "
+                               "the bf16 hi/lo split)",
+                "peak_source": f"{peak_src} bf16 burst (cuBLAS)", "traffic": None}
     if dom == "bwd_pre":
         nbytes = 2 * B * H * N * d * 2 + B * H * N * 4 * 3
         kname = KERNEL_OF[dom]
