@@ -29,9 +29,15 @@ def dsv():
     return binding
 
 
-@pytest.mark.parametrize("d,block,r", [(64, 64, 8), (128, 128, 16), (128, 64, 32), (64, 128, 24), (128, 128, 64)])
-def test_maxpool_all_shapes(dsv, d, block, r):
-    B, H, G = 2, 2, 18                     # 18 key blocks: one full run of 16 and a ragged run of 2
+@pytest.mark.parametrize("d,block,r,G", [(64, 64, 8, 18), (128, 128, 16, 18), (128, 64, 32, 18), (64, 128, 24, 18),
+                                         (128, 128, 64, 18), (64, 64, 40, 17), (128, 64, 56, 21), (128, 128, 48, 5)])
+def test_maxpool_all_shapes(dsv, d, block, r, G):
+    """Every rank the kernels are built for and both block sizes; odd G at
+    block 64 leaves the last 128-token tile half empty (rows past N are zero
+    and their scores are not written), r = 56 and 64 take two query tiles per
+    CTA instead of four, and the CTAs' step ranges cross from one query-tile
+    group to the next mid-sweep."""
+    B, H = 2, 2
     N = G * block
     g = torch.Generator(device="cuda").manual_seed(d + block + r)
     Q, K = (torch.randn(B, H, N, d, generator=g, device="cuda").to(torch.bfloat16) * 1.5 for _ in range(2))
