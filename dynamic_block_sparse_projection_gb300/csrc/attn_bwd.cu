@@ -40,12 +40,6 @@
 
 namespace dsv {
 
-#ifdef DSV_TRACE
-static __device__ int g_trace_cta;
-static __device__ unsigned long long g_trace_kv[96 * 16];
-static __device__ unsigned long long g_trace_q[96 * 16];
-#endif
-
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -506,7 +500,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  DSV_TRACE_INIT;
   const int nb = G;
   const unsigned int kid = (unsigned int)KID_BWD_Q << 8;
 
@@ -679,7 +672,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (ok && cnt == 1) mma_commit_w(qd_free);    // the group's last read of dO_g
         for (int n = 0; ok && n < cnt; ++n) {
           const uint32_t gn = gq + (uint32_t)n;
-          DSV_TRACE_POINT(g_trace_q, n, 0);
           uint32_t td = 0u;
           if (n + 1 < cnt) {
             const uint32_t tk = mbar_test(&k_full[(gn + 1) % NK], ((gn + 1) / NK) & 1u);
@@ -696,14 +688,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
             }
             if (n + 2 == cnt) mma_commit_w(qd_free);    // the group's last read of dO_g
           }
-          DSV_TRACE_POINT(g_trace_q, n, 1);
           // ds_full of a group's first pair also means the compute warps have
           // read the previous group's dQ
           if (!mbar_wait_warp_tested(ds_full, gn & 1u, td, abort_flag, ctl, kid | W_DSFULL)) {
             ok = false;
             break;
           }
-          DSV_TRACE_POINT(g_trace_q, n, 2);
           tc_fence_after();
           const int s = (int)(gn % NK);
           const uint64_t kmn = desc_off(dKmn0, (uint32_t)s * T::KV_BYTES);
@@ -714,7 +704,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
           }
           mma_commit_w(&k_empty[s]);
           mma_commit_w(ds_empty);
-          DSV_TRACE_POINT(g_trace_q, n, 3);
         }
         if (!ok) break;
         mma_commit_w(acc_done);
@@ -763,7 +752,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
           ok = false;
           break;
         }
-        if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 4);
         tc_fence_after();
         uint32_t xs[HALF], xp[HALF];
 #pragma unroll
@@ -772,8 +760,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
           tmem_ld32(tmem + lane_off + T::DP_COL + hf * HALF + c * 32, xp + c * 32);
         }
         tmem_ld_wait();
-        if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 5);
-        if (warp > 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 6 + warp);
         tc_fence_before();
         mbar_arrive(sp_free);
         const uint32_t e_tested = mbar_test(ds_empty, (gn & 1u) ^ 1u);
@@ -789,7 +775,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
           f2_unpack(mul2(f2_pack(p0, p1), t), d0, d1);
           dw[i] = pack_bf16x2(d0, d1);
         }
-        if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 6);
         // the single dS buffer is free once dQ of the previous block is done
         if (n + 1 < cnt) s_tested = mbar_test(s_full, (gn + 1) & 1u);
         if (!mbar_wait_warp_tested(ds_empty, (gn & 1u) ^ 1u, e_tested, abort_flag, ctl, kid | W_DSEMPTY)) {
@@ -803,7 +788,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(ds_full);
-        if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_q, n, 7);
       }
       if (ok) ok = mbar_wait_warp(acc_done, (uint32_t)ne & 1u, abort_flag, ctl, kid | W_ACC);
       if (!ok) break;
@@ -1063,16 +1047,3 @@ cudaError_t launch_attn_bwd(const void* Q, const CUtensorMap& tmQ, const CUtenso
 }
 
 }  // namespace dsv
-
-#ifdef DSV_TRACE
-extern "C" int dsv_trace_bwd(int which, int cta, unsigned long long* host) {
-  if (host == nullptr) {
-    static const unsigned long long zero[96 * 16] = {};
-    cudaMemcpyToSymbol(dsv::g_trace_kv, zero, sizeof(zero));
-    cudaMemcpyToSymbol(dsv::g_trace_q, zero, sizeof(zero));
-    return (int)cudaMemcpyToSymbol(dsv::g_trace_cta, &cta, sizeof(int));
-  }
-  return which == 0 ? (int)cudaMemcpyFromSymbol(host, dsv::g_trace_kv, sizeof(dsv::g_trace_kv))
-                    : (int)cudaMemcpyFromSymbol(host, dsv::g_trace_q, sizeof(dsv::g_trace_q));
-}
-#endif

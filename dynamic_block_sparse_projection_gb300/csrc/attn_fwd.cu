@@ -43,11 +43,6 @@
 
 namespace dsv {
 
-#ifdef DSV_TRACE
-static __device__ int g_trace_cta;
-static __device__ unsigned long long g_trace_fwd[96 * 16];
-#endif
-
 namespace {
 
 template <int BETA, int D>
@@ -101,7 +96,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  DSV_TRACE_INIT;
   const unsigned int kid = (unsigned int)KID_FWD << 8;
 
   if (threadIdx.x == 0) {
@@ -218,9 +212,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // S(n) = Q K_n^T into buffer n%3
     auto issue_S = [&](uint32_t gn, int n) -> bool {
       const int s = (int)(gn % NST);
-      DSV_TRACE_POINT(g_trace_fwd, n, 0);
       if (!mbar_wait_warp(&k_full[s], (uint32_t)(gn / NST) & 1u, abort_flag, ctl, kid | W_K)) return false;
-      DSV_TRACE_POINT(g_trace_fwd, n, 1);
       tc_fence_after();
       const uint32_t d_tmem = tmem + (uint32_t)s * T::S_COL;
       const uint64_t kb = desc_off(dK0, (uint32_t)s * T::KV_BYTES);
@@ -230,7 +222,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                  desc_off(kb, (kk >> 2) * T::KV_CHUNK + (kk & 3) * 32), IDS, kk > 0 ? 1u : 0u);
       }
       mma_commit_w(&s_full[s]);
-      DSV_TRACE_POINT(g_trace_fwd, n, 2);
       return true;
     };
     uint32_t gq = 0;
@@ -259,12 +250,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ok = false;
           break;
         }
-        DSV_TRACE_POINT(g_trace_fwd, n, 3);
         if (!mbar_wait_warp_tested(&v_full[s], ph, v_tested, abort_flag, ctl, kid | W_V)) {
           ok = false;
           break;
         }
-        DSV_TRACE_POINT(g_trace_fwd, n, 4);
         tc_fence_after();
         const uint32_t p_tmem = tmem + (uint32_t)s * T::S_COL;
         const uint64_t vb = desc_off(dV0, (uint32_t)s * T::KV_BYTES);
@@ -273,7 +262,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mma_ts_w(tmem + T::O_COL, p_tmem + kk * 8, desc_off(vb, kk * 16 * 128), IDO, (n > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit_w(&o_done[s]);
-        DSV_TRACE_POINT(g_trace_fwd, n, 5);
       }
       if (!ok) break;
       mma_commit_w(o_final);
@@ -318,7 +306,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ok = false;
           break;
         }
-        if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 8);
         tc_fence_after();
         const uint32_t sb = tmem + lane_off + (uint32_t)s * T::S_COL;
         uint32_t xr[BETA];
@@ -326,8 +313,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c = 0; c < BETA / 32; ++c) tmem_ld32(sb + c * 32, xr + c * 32);
         s_tested = (n + 1 < cnt) ? mbar_test(&s_full[(gn + 1) % NST], ((gn + 1) / NST) & 1u) : 0u;
         tmem_ld_wait();
-        if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 9);
-        if (warp == 5 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 6);
         // row max as 8 independent partial maxima (short dependency chains),
         // two new values per three-input max
         float mx8[8];
@@ -384,15 +369,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           f2_unpack(add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3])), a0, a1);
           l += a0 + a1;
         }
-        if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 10);
-        if (warp == 5 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 7);
 #pragma unroll
         for (int c = 0; c < BETA / 32; ++c) tmem_st16(sb + c * 16, pk + c * 16);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_full[s]);
-        if (warp == 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 11);
-        if (warp > 2 && lane == 0) DSV_TRACE_POINT(g_trace_fwd, n, 9 + warp);
       }
       if (ok) ok = mbar_wait_warp(o_final, (uint32_t)ne & 1u, abort_flag, ctl, kid | W_OFINAL);
       if (!ok) break;
@@ -461,14 +442,3 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
 }
 
 }  // namespace dsv
-
-#ifdef DSV_TRACE
-extern "C" int dsv_trace_fwd(int cta, unsigned long long* host) {
-  if (host == nullptr) {
-    static const unsigned long long zero[96 * 16] = {};
-    cudaMemcpyToSymbol(dsv::g_trace_fwd, zero, sizeof(zero));
-    return (int)cudaMemcpyToSymbol(dsv::g_trace_cta, &cta, sizeof(int));
-  }
-  return (int)cudaMemcpyFromSymbol(host, dsv::g_trace_fwd, sizeof(dsv::g_trace_fwd));
-}
-#endif

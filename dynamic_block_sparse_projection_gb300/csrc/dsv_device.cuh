@@ -467,25 +467,6 @@ __device__ __forceinline__ T* align_up_ptr(void* p, uintptr_t a) {
   return reinterpret_cast<T*>((v + a - 1) & ~(a - 1));
 }
 
-// Optional timeline instrumentation, compiled only with -DDSV_TRACE (never in
-// the library build): DSV_TRACE_POINT(buf, step, k) stamps clock64() into
-// buf[step * 16 + k] for the one CTA selected by the translation unit's
-// g_trace_cta (read once by DSV_TRACE_INIT), for the first 96 steps.
-#ifdef DSV_TRACE
-#define DSV_TRACE_INIT const bool dsv_traced = (blockIdx.x == (unsigned)g_trace_cta)
-#define DSV_TRACE_POINT(buf, step, k)                                     \
-  do {                                                                    \
-    if (dsv_traced && (step) < 96) (buf)[(step) * 16 + (k)] = clock64(); \
-  } while (0)
-#else
-#define DSV_TRACE_INIT \
-  do {                 \
-  } while (0)
-#define DSV_TRACE_POINT(buf, step, k) \
-  do {                                \
-  } while (0)
-#endif
-
 // Where a wait gave up (detail word of DSV_ERR_TIMEOUT): kernel id << 8 | wait id.
 enum : unsigned int {
   KID_FWD = 1,
