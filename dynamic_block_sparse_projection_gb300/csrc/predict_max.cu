@@ -146,18 +146,26 @@ template <int R>
 struct MaxTraits {
   using L = MaxLayout<R>;
   static constexpr int TB = L::TILE_BYTES;
-  static constexpr int ZC = 8;                                   // key tiles per cross-warp combine
-  static constexpr int MISC = 4096;                              // barriers, partial maxima, slots
+  // key tiles per product: two (N = 256) when a product is at most three MMAs
+  // (r <= 16), so that the hand-over around each product (barrier round
+  // trips, the accumulator read-back) is paid once per 256 keys
+  static constexpr int KT = L::KSTEPS <= 3 ? 2 : 1;
+  static constexpr int NACC = 4 / KT;                            // TMEM accumulators of 128 * KT columns
+  static constexpr int CG = 2 * KT;                              // 64-column groups of a product
+  static constexpr int SB = KT * TB;                             // bytes of one key step (KT tiles)
+  static constexpr int ZC = 8;                                   // key steps per cross-warp combine
+  static constexpr int MISC = 8192;                              // barriers, partial maxima, slots
   // query tiles per CTA: 4 where they and a two-stage key ring fit (each key
-  // tile copied to shared memory then serves 4 products), else 2
-  static constexpr int NQ = 6 * TB + 1024 + MISC <= 227 * 1024 ? 4 : 2;
+  // step copied to shared memory then serves 4 products), else 2
+  static constexpr int NQ = 4 * TB + 2 * SB + 1024 + MISC <= 227 * 1024 ? 4 : 2;
   static constexpr int RING_ROOM = 227 * 1024 - 1024 - NQ * TB - MISC;
-  static constexpr int NSTAGE = RING_ROOM / TB >= 4 ? 4 : RING_ROOM / TB;
-  static constexpr int NACC = 4;                                 // TMEM accumulators of 128 columns
-  static constexpr int SMEM_USED = 1024 + NQ * TB + NSTAGE * TB + MISC;
+  static constexpr int NSTAGE = RING_ROOM / SB >= 4 ? 4 : RING_ROOM / SB;
+  static constexpr int SMEM_USED = 1024 + NQ * TB + NSTAGE * SB + MISC;
   // at least 120 KB, so that one CTA holds an SM (and its whole TMEM)
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static_assert(NSTAGE >= 2, "tile too large for a two-stage ring");
+  static_assert(2 * ZC * NQ * 4 * CG * 4 + (1 + 2 * NSTAGE + 2 * NACC + 1) * 8 + 16 <= MISC, "misc area");
+  static_assert(ZC * NQ * 4 * KT <= 256, "one combined score per reduction thread");
 };
 
 constexpr int kMaxThreads = 320;         // producer, MMA, two groups of 4 reduction warps
@@ -172,22 +180,24 @@ __device__ __forceinline__ int float_key(float f) {
 }
 __device__ __forceinline__ float key_float(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7FFFFFFF); }
 
-// Work is a sequence of steps w = ((b*H + h) * NG + tg) * NT + c: query-tile
-// group tg (NQ query tiles from tg*NQ) of head (b, h) against key tile c.
-// Persistent CTAs, one per SM, each take one contiguous range of steps of
-// equal length (so no wave is left partly empty), reloading the query tiles
-// when the range crosses into the next group.
+// Work is a sequence of steps w = ((b*H + h) * NG + tg) * NS + c: query-tile
+// group tg (NQ query tiles from tg*NQ) of head (b, h) against key step c (key
+// tiles KT*c .. KT*c + KT - 1; the workspace holds NTP = NS * KT tiles per
+// head, the ones past N zero).  Persistent CTAs, one per SM, each take one
+// contiguous range of steps of equal length (so no wave is left partly
+// empty), reloading the query tiles when the range crosses into the next
+// group.
 struct MaxStep {
   long long bh;
   int tq0, nq, c;
   long long item;
 };
 template <int NQ>
-__device__ __forceinline__ MaxStep max_step(long long w, int NT) {
+__device__ __forceinline__ MaxStep max_step(long long w, int NT, int NS) {
   const int NG = (NT + NQ - 1) / NQ;
   MaxStep st;
-  st.item = w / NT;
-  st.c = (int)(w - st.item * NT);
+  st.item = w / NS;
+  st.c = (int)(w - st.item * NS);
   st.bh = st.item / NG;
   st.tq0 = (int)(st.item - st.bh * NG) * NQ;
   st.nq = NT - st.tq0 < NQ ? NT - st.tq0 : NQ;
@@ -196,28 +206,31 @@ __device__ __forceinline__ MaxStep max_step(long long w, int NT) {
 
 template <int BLOCK, int R>
 __global__ void __launch_bounds__(kMaxThreads, 1)
-    tile_max_mma_kernel(const uint8_t* __restrict__ qt, const uint8_t* __restrict__ kt, int NT, int G,
+    tile_max_mma_kernel(const uint8_t* __restrict__ qt, const uint8_t* __restrict__ kt, int NT, int NS, int G,
                         long long steps, float* __restrict__ S, Ctl ctl) {
   using T = MaxTraits<R>;
   using L = typename T::L;
-  constexpr int TB = T::TB, NSTAGE = T::NSTAGE, NQ = T::NQ;
+  constexpr int TB = T::TB, SB = T::SB, KT = T::KT, NACC = T::NACC, CG = T::CG;
+  constexpr int NSTAGE = T::NSTAGE, NQ = T::NQ;
+  constexpr int NTP_PER_STEP = KT;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sA = smem_align1024(smem_raw);        // NQ query tiles
-  uint8_t* sB = sA + NQ * TB;                     // NSTAGE key tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + NSTAGE * TB);
+  uint8_t* sB = sA + NQ * TB;                     // NSTAGE key steps
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + NSTAGE * SB);
   uint64_t* a_full = bars;
   uint64_t* a_free = bars + 1;                    // the products on the current query tiles are done
   uint64_t* b_full = bars + 2;
   uint64_t* b_empty = b_full + NSTAGE;
   uint64_t* t_full = b_empty + NSTAGE;            // [NACC]
-  uint64_t* t_empty = t_full + T::NACC;           // [NACC]
-  uint64_t* drain = t_empty + T::NACC;
-  int* part = reinterpret_cast<int*>(drain + 1);  // [2][ZC][NQ][4 quarters][2 halves], ordered keys
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(part + 2 * T::ZC * NQ * 4 * 2);
+  uint64_t* t_empty = t_full + NACC;              // [NACC]
+  uint64_t* drain = t_empty + NACC;
+  int* part = reinterpret_cast<int*>(drain + 1);  // [2][ZC][NQ][4 quarters][CG], ordered keys
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(part + 2 * T::ZC * NQ * 4 * CG);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long w0 = steps * blockIdx.x / gridDim.x, w1 = steps * (blockIdx.x + 1) / gridDim.x;
+  const long long NTP = (long long)NS * NTP_PER_STEP;   // tiles per head in the workspace
   const unsigned int kid = (unsigned int)KID_MAXPOOL << 8;
 
   if (threadIdx.x == 0) {
@@ -227,7 +240,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
     }
-    for (int a = 0; a < T::NACC; ++a) {
+    for (int a = 0; a < NACC; ++a) {
       mbar_init(&t_full[a], 1);
       mbar_init(&t_empty[a], 128);
     }
@@ -250,10 +263,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       long long cur = -1;
       int a_loads = 0;
       long long issued = 0;
-      bool ok = true;
-      for (long long w = w0; ok && w < w1; ++w) {
+      for (long long w = w0; w < w1; ++w) {
         const long long k = w - w0;
-        const MaxStep st = max_step<NQ>(w, NT);
+        const MaxStep st = max_step<NQ>(w, NT, NS);
         if (st.item != cur) {
           // the query tiles are overwritten once every product reading them is done
           if (a_loads > 0 &&
@@ -261,14 +273,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             break;
           mbar_arrive_expect_tx(a_full, (uint32_t)(st.nq * TB));
           for (int rt = 0; rt < st.nq; ++rt)
-            bulk_load(sA + rt * TB, qt + (st.bh * NT + st.tq0 + rt) * (long long)TB, TB, a_full);
+            bulk_load(sA + rt * TB, qt + (st.bh * NTP + st.tq0 + rt) * (long long)TB, TB, a_full);
           ++a_loads;
           cur = st.item;
         }
         const int s = (int)(k % NSTAGE);
         if (!mbar_wait(&b_empty[s], ((uint32_t)(k / NSTAGE) & 1u) ^ 1u, abort_flag, ctl, kid | MW_BEMPTY)) break;
-        mbar_arrive_expect_tx(&b_full[s], TB);
-        bulk_load(sB + s * TB, kt + (st.bh * NT + st.c) * (long long)TB, TB, &b_full[s]);
+        mbar_arrive_expect_tx(&b_full[s], SB);
+        bulk_load(sB + s * SB, kt + (st.bh * NTP + (long long)st.c * KT) * (long long)TB, SB, &b_full[s]);
         issued = k + 1;
       }
       // every copy started must land before the CTA exits
@@ -278,20 +290,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    // The next key tile's barrier and the next product's accumulator are
+    // The next key step's barrier and the next product's accumulator are
     // tested one step early; a wait whose test found the phase complete is
     // free.
-    constexpr uint32_t ID = idesc_bf16_f32(kTile, kTile, false, false);
+    constexpr uint32_t ID = idesc_bf16_f32(kTile, kTile * KT, false, false);
     const uint64_t a0 = sdesc_noswz(smem_u32(sA), L::LBO, L::SBO);
     const uint64_t b0 = sdesc_noswz(smem_u32(sB), L::LBO, L::SBO);
     long long cur = -1;
     int a_uses = 0;
-    long long p = 0;                                // product number: accumulator p % 4, its use p / 4
+    long long p = 0;                                // product number: accumulator p % NACC, its use p / NACC
     bool ok = true;
     uint32_t tb = 0u, te = 1u;                      // product 0's accumulator is free
     for (long long w = w0; ok && w < w1; ++w) {
       const long long k = w - w0;
-      const MaxStep st = max_step<NQ>(w, NT);
+      const MaxStep st = max_step<NQ>(w, NT, NS);
       if (st.item != cur) {
         if (a_uses > 0) mma_commit_w(a_free);
         if (!mbar_wait_warp(a_full, (uint32_t)a_uses & 1u, abort_flag, ctl, kid | MW_A)) break;
@@ -303,18 +315,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         break;
       tb = w + 1 < w1 ? mbar_test(&b_full[(k + 1) % NSTAGE], (uint32_t)((k + 1) / NSTAGE) & 1u) : 0u;
       for (int rt = 0; rt < st.nq; ++rt, ++p) {
-        const int buf = (int)(p & 3);
-        if (!mbar_wait_warp_tested(&t_empty[buf], ((uint32_t)(p >> 2) & 1u) ^ 1u, te, abort_flag, ctl,
+        const int buf = (int)(p % NACC);
+        if (!mbar_wait_warp_tested(&t_empty[buf], ((uint32_t)(p / NACC) & 1u) ^ 1u, te, abort_flag, ctl,
                                    kid | MW_TEMPTY)) {
           ok = false;
           break;
         }
-        te = mbar_test(&t_empty[(p + 1) & 3], ((uint32_t)((p + 1) >> 2) & 1u) ^ 1u);
+        te = mbar_test(&t_empty[(p + 1) % NACC], ((uint32_t)((p + 1) / NACC) & 1u) ^ 1u);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < L::KSTEPS; ++kk)
-          mma_ss_w(tmem + (uint32_t)(buf * kTile), desc_off(a0, (uint32_t)(rt * TB + kk * 2 * L::LBO)),
-                   desc_off(b0, (uint32_t)(s * TB + kk * 2 * L::LBO)), ID, kk > 0 ? 1u : 0u);
+          mma_ss_w(tmem + (uint32_t)(buf * kTile * KT), desc_off(a0, (uint32_t)(rt * TB + kk * 2 * L::LBO)),
+                   desc_off(b0, (uint32_t)(s * SB + kk * 2 * L::LBO)), ID, kk > 0 ? 1u : 0u);
         mma_commit_w(&t_full[buf]);
       }
       if (ok) mma_commit_w(&b_empty[s]);
@@ -324,14 +336,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   } else {
     // ------------- reduction warps: group grp takes the products p with p % 2 == grp; -------------
     // ------------- warp qd of a group reads TMEM lane quarter qd (tile rows 32*qd .. +31) -----------
-    // Per product: the row maxima over key columns 0..63 and 64..127, then
-    // the warp's maxima (redux on order-preserving integer keys), kept in
-    // shared memory.  Two groups work on alternate products, so that the
-    // latency of one product's waits, loads and reductions overlaps the
-    // other's.  Every ZC steps all eight warps meet at a named barrier and
-    // combine the quarters into scores.  Every warp runs every step and
-    // barrier, also after a wait has given up (then without waits or TMEM
-    // reads), so that no warp is left at the barrier.
+    // Per product: the row maxima over each 64-column group of the product's
+    // 128 * KT key columns, then the warp's maxima (redux on order-preserving
+    // integer keys), kept in shared memory.  Two groups work on alternate
+    // products, so that the latency of one product's waits, loads and
+    // reductions overlaps the other's.  Every ZC steps all eight warps meet at
+    // a named barrier and combine the quarters into scores.  Every warp runs
+    // every step and barrier, also after a wait has given up (then without
+    // waits or TMEM reads), so that no warp is left at the barrier.
     const int qd = warp & 3, grp = (warp - 2) >> 2;
     const int tid = threadIdx.x - 64;               // 0 .. 255
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
@@ -340,67 +352,78 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     for (long long w = w0; w < w1; ++w) {
       const long long k = w - w0;
       const int z = (int)(k % T::ZC), zb = (int)(k / T::ZC) & 1;
-      const int nq = max_step<NQ>(w, NT).nq;
+      const int nq = max_step<NQ>(w, NT, NS).nq;
       for (int rt = 0; rt < nq; ++rt, ++p) {
         if ((int)(p & 1) != grp) continue;
-        const int buf = (int)(p & 3);
-        if (ok) ok = mbar_wait_warp(&t_full[buf], (uint32_t)(p >> 2) & 1u, abort_flag, ctl, kid | MW_TFULL);
-        int key[2] = {INT_MIN, INT_MIN};
+        const int buf = (int)(p % NACC);
+        if (ok) ok = mbar_wait_warp(&t_full[buf], (uint32_t)(p / NACC) & 1u, abort_flag, ctl, kid | MW_TFULL);
+        int key[CG];
+#pragma unroll
+        for (int cg = 0; cg < CG; ++cg) key[cg] = INT_MIN;
         if (ok) {
           tc_fence_after();
-          uint32_t v[128];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_off + (uint32_t)(buf * kTile + 32 * q), v + 32 * q);
-          tmem_ld_wait();
-          tc_fence_before();
-          mbar_arrive(&t_empty[buf]);
+          for (int kc = 0; kc < KT; ++kc) {
+            uint32_t v[128];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint32_t* x = v + 64 * hh;
-            float a0 = __uint_as_float(x[0]), a1 = __uint_as_float(x[1]), a2 = __uint_as_float(x[2]),
-                  a3 = __uint_as_float(x[3]);
-#pragma unroll
-            for (int i = 4; i < 60; i += 8) {       // columns 4 .. 59
-              a0 = max3f(a0, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
-              a1 = max3f(a1, __uint_as_float(x[i + 2]), __uint_as_float(x[i + 3]));
-              a2 = max3f(a2, __uint_as_float(x[i + 4]), __uint_as_float(x[i + 5]));
-              a3 = max3f(a3, __uint_as_float(x[i + 6]), __uint_as_float(x[i + 7]));
+            for (int q = 0; q < 4; ++q)
+              tmem_ld32(tmem + lane_off + (uint32_t)(buf * kTile * KT + kc * kTile + 32 * q), v + 32 * q);
+            tmem_ld_wait();
+            if (kc == KT - 1) {
+              tc_fence_before();
+              mbar_arrive(&t_empty[buf]);
             }
-            a0 = max3f(a0, __uint_as_float(x[60]), __uint_as_float(x[61]));
-            a1 = max3f(a1, __uint_as_float(x[62]), __uint_as_float(x[63]));
-            float m = fmaxf(max3f(a0, a1, a2), a3);   // NaN only if all 64 logits are NaN
-            if (m != m) m = -INFINITY;
-            key[hh] = __reduce_max_sync(0xffffffffu, float_key(m));
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint32_t* x = v + 64 * hh;
+              float a0 = __uint_as_float(x[0]), a1 = __uint_as_float(x[1]), a2 = __uint_as_float(x[2]),
+                    a3 = __uint_as_float(x[3]);
+#pragma unroll
+              for (int i = 4; i < 60; i += 8) {     // columns 4 .. 59
+                a0 = max3f(a0, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
+                a1 = max3f(a1, __uint_as_float(x[i + 2]), __uint_as_float(x[i + 3]));
+                a2 = max3f(a2, __uint_as_float(x[i + 4]), __uint_as_float(x[i + 5]));
+                a3 = max3f(a3, __uint_as_float(x[i + 6]), __uint_as_float(x[i + 7]));
+              }
+              a0 = max3f(a0, __uint_as_float(x[60]), __uint_as_float(x[61]));
+              a1 = max3f(a1, __uint_as_float(x[62]), __uint_as_float(x[63]));
+              float m = fmaxf(max3f(a0, a1, a2), a3);   // NaN only if all 64 logits are NaN
+              if (m != m) m = -INFINITY;
+              key[2 * kc + hh] = __reduce_max_sync(0xffffffffu, float_key(m));
+            }
           }
         }
         if (lane == 0) {
-          int* pp = part + (((zb * T::ZC + z) * NQ + rt) * 4 + qd) * 2;
-          pp[0] = key[0];
-          pp[1] = key[1];
+          int* pp = part + (((zb * T::ZC + z) * NQ + rt) * 4 + qd) * CG;
+#pragma unroll
+          for (int cg = 0; cg < CG; ++cg) pp[cg] = key[cg];
         }
       }
       if (z == T::ZC - 1 || w == w1 - 1) {
         asm volatile("bar.sync 1, 256;" ::: "memory");
-        // one score per thread: (step k - z + zz, query tile rt[, query half ga, key half jb])
-        const int per = BLOCK == 128 ? 1 : 4;
-        const int item = tid / per, sub = tid % per;
+        // one score per thread: (step k - z + zz, query tile rt, [query half ga,] key block jb)
+        constexpr int PER = BLOCK == 128 ? KT : 4 * KT;
+        const int item = tid / PER, sub = tid % PER;
         const int zz = item / NQ, rt = item % NQ;
         if (ok && zz <= z) {
-          const MaxStep st = max_step<NQ>(w - z + zz, NT);
+          const MaxStep st = max_step<NQ>(w - z + zz, NT, NS);
           if (rt < st.nq) {
-            const int* pb = part + (((zb * T::ZC + zz) * NQ + rt) * 4) * 2;   // [quarter][half]
+            const int* pb = part + (((zb * T::ZC + zz) * NQ + rt) * 4) * CG;   // [quarter][column group]
             const int tq = st.tq0 + rt;
             if (BLOCK == 128) {
-              const int m = max(max(max(pb[0], pb[1]), max(pb[2], pb[3])), max(max(pb[4], pb[5]), max(pb[6], pb[7])));
-              S[(st.bh * G + tq) * (long long)G + st.c] = key_float(m);
+              // key block jb: column groups 2 jb, 2 jb + 1 of all four quarters
+              const int jb = sub, j = st.c * KT + jb;
+              int m = INT_MIN;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) m = max(m, max(pb[q * CG + 2 * jb], pb[q * CG + 2 * jb + 1]));
+              if (j < G) S[(st.bh * G + tq) * (long long)G + j] = key_float(m);
             } else {
               // rows 0..63 (quarters 0, 1) are group 2*tq, rows 64..127 group 2*tq + 1;
-              // columns 0..63 key block 2*c, 64..127 key block 2*c + 1
-              const int ga = sub >> 1, jb = sub & 1;
-              const int g = 2 * tq + ga, j = 2 * st.c + jb;
+              // column group jb is key block 2*KT*c + jb
+              const int ga = sub / (2 * KT), jb = sub % (2 * KT);
+              const int g = 2 * tq + ga, j = 2 * KT * st.c + jb;
               if (g < G && j < G)
-                S[(st.bh * G + g) * (long long)G + j] =
-                    key_float(max(pb[(2 * ga) * 2 + jb], pb[(2 * ga + 1) * 2 + jb]));
+                S[(st.bh * G + g) * (long long)G + j] = key_float(max(pb[(2 * ga) * CG + jb], pb[(2 * ga + 1) * CG + jb]));
             }
           }
         }
@@ -415,7 +438,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 }
 
 template <int R>
-cudaError_t launch_tile_max(const uint8_t* qt, const uint8_t* kt, const dsv_shape& s, int NT, float* scores,
+cudaError_t launch_tile_max(const uint8_t* qt, const uint8_t* kt, const dsv_shape& s, int NT, int NS, float* scores,
                             const Ctl& ctl, cudaStream_t st) {
   const int G = s.N / s.block;
   auto kern = s.block == 128 ? tile_max_mma_kernel<128, R> : tile_max_mma_kernel<64, R>;
@@ -425,46 +448,56 @@ cudaError_t launch_tile_max(const uint8_t* qt, const uint8_t* kt, const dsv_shap
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   constexpr int NQ = MaxTraits<R>::NQ;
-  const long long steps = (long long)s.B * s.H * ((NT + NQ - 1) / NQ) * NT;
+  const long long steps = (long long)s.B * s.H * ((NT + NQ - 1) / NQ) * NS;
   const unsigned grid = (unsigned)(steps < nsm ? steps : nsm);
-  kern<<<grid, kMaxThreads, MaxTraits<R>::SMEM, st>>>(qt, kt, NT, G, steps, scores, ctl);
+  kern<<<grid, kMaxThreads, MaxTraits<R>::SMEM, st>>>(qt, kt, NT, NS, G, steps, scores, ctl);
   return cudaGetLastError();
 }
 
 template <int D, int R>
-cudaError_t launch_split(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s, int NT,
+cudaError_t launch_split(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s, int NTP,
                          uint8_t* qt, uint8_t* kt, cudaStream_t st) {
   const int smem = D * R * (int)sizeof(float);
   cudaError_t e =
       cudaFuncSetAttribute(lowrank_split_kernel<D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((long long)s.B * s.H * NT), 2);
+  dim3 grid((unsigned)((long long)s.B * s.H * NTP), 2);
   lowrank_split_kernel<D, R><<<grid, kTile, smem, st>>>(static_cast<const __nv_bfloat16*>(Q),
-                                                        static_cast<const __nv_bfloat16*>(K), Wq, Wk, s.H, s.N, NT,
+                                                        static_cast<const __nv_bfloat16*>(K), Wq, Wk, s.H, s.N, NTP,
                                                         qt, kt);
   return cudaGetLastError();
 }
 
-size_t tiles_bytes(const dsv_shape& s, int tile_bytes) {
-  const size_t NT = ((size_t)s.N + kTile - 1) / kTile;
-  return align256((size_t)s.B * s.H * NT * (size_t)tile_bytes);
+// 128-token tiles per head in the workspace: ceil(N / 128), rounded up to a
+// whole number of key steps
+template <int R>
+int tiles_per_head(const dsv_shape& s) {
+  constexpr int KT = MaxTraits<R>::KT;
+  const int NT = (s.N + kTile - 1) / kTile;
+  return (NT + KT - 1) / KT * KT;
+}
+
+template <int R>
+size_t tiles_bytes(const dsv_shape& s) {
+  return align256((size_t)s.B * s.H * (size_t)tiles_per_head<R>(s) * (size_t)MaxLayout<R>::TILE_BYTES);
 }
 
 template <int R>
 cudaError_t launch_predict_max_r(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s,
                                  float* scores, void* ws, const Ctl& ctl, cudaStream_t st) {
   const int NT = (s.N + kTile - 1) / kTile;
+  const int NTP = tiles_per_head<R>(s);
   uint8_t* qt = static_cast<uint8_t*>(ws);
-  uint8_t* kt = qt + tiles_bytes(s, MaxLayout<R>::TILE_BYTES);
-  cudaError_t e = s.d == 128 ? launch_split<128, R>(Q, K, Wq, Wk, s, NT, qt, kt, st)
-                             : launch_split<64, R>(Q, K, Wq, Wk, s, NT, qt, kt, st);
+  uint8_t* kt = qt + tiles_bytes<R>(s);
+  cudaError_t e = s.d == 128 ? launch_split<128, R>(Q, K, Wq, Wk, s, NTP, qt, kt, st)
+                             : launch_split<64, R>(Q, K, Wq, Wk, s, NTP, qt, kt, st);
   if (e != cudaSuccess) return e;
-  return launch_tile_max<R>(qt, kt, s, NT, scores, ctl, st);
+  return launch_tile_max<R>(qt, kt, s, NT, NTP / MaxTraits<R>::KT, scores, ctl, st);
 }
 
 template <int R>
 size_t ws_bytes_r(const dsv_shape& s) {
-  return 2 * tiles_bytes(s, MaxLayout<R>::TILE_BYTES);
+  return 2 * tiles_bytes<R>(s);
 }
 
 }  // namespace
