@@ -146,10 +146,10 @@ template <int R>
 struct MaxTraits {
   using L = MaxLayout<R>;
   static constexpr int TB = L::TILE_BYTES;
-  // key tiles per product: two (N = 256) when a product is at most three MMAs
-  // (r <= 16), so that the hand-over around each product (barrier round
-  // trips, the accumulator read-back) is paid once per 256 keys
-  static constexpr int KT = L::KSTEPS <= 3 ? 2 : 1;
+  // key tiles per product: two (N = 256) for r <= 32 (at most six MMAs a
+  // product), so that the hand-over around each product (barrier round trips,
+  // the accumulator read-back) is paid once per 256 keys
+  static constexpr int KT = L::KSTEPS <= 6 ? 2 : 1;
   static constexpr int NACC = 4 / KT;                            // TMEM accumulators of 128 * KT columns
   static constexpr int CG = 2 * KT;                              // 64-column groups of a product
   static constexpr int SB = KT * TB;                             // bytes of one key step (KT tiles)
