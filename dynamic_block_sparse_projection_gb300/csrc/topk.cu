@@ -66,7 +66,7 @@ struct TopkArgs {
 // kept, and the few scores of b* (at most kCandMax) are ranked exactly by
 // (key desc, index asc) unless all of them are kept.  Each thread then writes
 // its own kept indices (ascending) at its prefix position and 32-bit mask
-// words are put together from the threads' 16-bit slot masks.  Value binning
+// words are put together from the threads' E-bit slot masks.  Value binning
 // spreads the scores over the buckets, so the shared-memory atomics rarely
 // collide; radix digits of float bits would pile into the few bins of the
 // common exponents.  Slots outside the row hold NaN: ignored by min / max,
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(RT, select_min_blocks(RT)) topk_select_kernel(
   __shared__ uint32_t s_cnt;
   __shared__ uint32_t candk[kCandMax];
   __shared__ int32_t candi[kCandMax];
-  __shared__ uint32_t gms[RT + 2];       // fast path: kept slots of thread t (bit e = slot e); two zero slots after
+  __shared__ uint32_t gms[RT + 32 / E];  // fast path: kept slots of thread t (bit e = slot e); zero slots after
   __shared__ uint32_t eqw[MAXC];         // fallback: per-chunk words
   __shared__ uint32_t selw[MAXC];
   __shared__ int32_t offw[MAXC];
@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(RT, select_min_blocks(RT)) topk_select_kernel(
   }
   for (int i = 4 * t; i < kBins; i += 4 * RT) *reinterpret_cast<uint4*>(&hist[i]) = make_uint4(0u, 0u, 0u, 0u);
   if (t == 0) s_cnt = 0u;
-  if (t < 2) gms[RT + t] = 0u;
+  if (t < 32 / E) gms[RT + t] = 0u;
   __syncthreads();
 #pragma unroll
   for (int v = 0; v < NW; ++v) {
@@ -344,9 +344,13 @@ __global__ void __launch_bounds__(RT, select_min_blocks(RT)) topk_select_kernel(
         *d++ = i0 + __ffs(gm) - 1;
         gm &= gm - 1u;
       }
-      // mask word m covers indices [32m, 32m + 32): slots 2m .. 2m + 2 shifted by off
+      // mask word m covers indices [32m, 32m + 32): the slot masks of threads
+      // (32/E) m .. (32/E) (m + 1) shifted by off
       for (int m = t; m < words; m += RT) {
-        const uint64_t v = (uint64_t)gms[2 * m] | ((uint64_t)gms[2 * m + 1] << 16) | ((uint64_t)gms[2 * m + 2] << 32);
+        constexpr int SPW = 32 / E;                       // threads per mask word
+        uint64_t v = 0ull;
+#pragma unroll
+        for (int i = 0; i <= SPW; ++i) v |= (uint64_t)gms[SPW * m + i] << (E * i);
         mcol[(long long)m * a.G] = (uint32_t)(v >> off);
       }
     } else {
