@@ -313,8 +313,8 @@ dsv_status dsv_predict_topk_blocks(const void* Q, const void* K, const float* Wq
       make_map_f32x32(&maps.kh, sp + 2 * part, (long long)rows, 128) != cudaSuccess ||
       make_map_f32x32(&maps.kl, sp + 3 * part, (long long)rows, 128) != cudaSuccess)
     return DSV_ERR_CUDA;
-  cudaError_t e = launch_pool_project(Q, K, Wq, Wk, s, qp, kp, st);
-  if (e == cudaSuccess) e = launch_split_tf32(qp, kp, s, split, st);
+  cudaError_t e = launch_pool_project(Q, K, Wq, Wk, s, qp, kp, st, split, split_part_floats(s));
+  if (e == cudaSuccess) e = launch_key_stats(kp, s, split, st);
   if (e == cudaSuccess)
     e = launch_score_select(maps, s, hk, nnz, fwd_ptr, fwd_col, static_cast<uint32_t*>(tws), scores, split, ctl, st);
   if (e == cudaSuccess) e = launch_topk_transpose(s, hk, nnz, bwd_ptr, bwd_col, tws, st);

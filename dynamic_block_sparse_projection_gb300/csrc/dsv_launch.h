@@ -40,9 +40,13 @@ size_t topk_ws_bytes(const dsv_shape& s);
 cudaError_t launch_topk_transpose(const dsv_shape& s, const HeadK& hk, int64_t nnz, int32_t* bwd_ptr,
                                   int32_t* bwd_col, void* ws, cudaStream_t st);
 // Pooled rank-r projections only (qp, kp: [B*H*G, r] fp32), the first kernel of launch_predict.
+// split != null (r <= 32): also the tf32 hi / lo parts of every projected
+// vector, zero-padded to 32 columns: four [B*H*G, 32] fp32 arrays (q hi, q lo,
+// k hi, k lo), `part` floats apart.
 cudaError_t launch_pool_project(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s,
-                                float* qp, float* kp, cudaStream_t st);
-// Fused predictor + top-k: tf32 operand splits of the pooled vectors, then one
+                                float* qp, float* kp, cudaStream_t st, float* split = nullptr, long long part = 0);
+// Fused predictor + top-k: the tf32 operand splits of the pooled vectors
+// (written by launch_pool_project), the per-head key statistics, then one
 // kernel that scores every (group, key block) pair on the tensor cores and
 // selects each group's top k without writing the score matrix (unless
 // `scores` is given); the forward lists and the selection bitmask (in the
@@ -52,7 +56,8 @@ cudaError_t launch_pool_project(const void* Q, const void* K, const float* Wq, c
 struct PredictTopkMaps {
   CUtensorMap qh, ql, kh, kl;
 };
-cudaError_t launch_split_tf32(const float* qp, const float* kp, const dsv_shape& s, float* split, cudaStream_t st);
+long long split_part_floats(const dsv_shape& s);
+cudaError_t launch_key_stats(const float* kp, const dsv_shape& s, float* split, cudaStream_t st);
 cudaError_t launch_score_select(const PredictTopkMaps& maps, const dsv_shape& s, const HeadK& hk, int64_t nnz,
                                 int32_t* fwd_ptr, int32_t* fwd_col, uint32_t* mask, float* scores, const float* split,
                                 const Ctl& ctl, cudaStream_t st);

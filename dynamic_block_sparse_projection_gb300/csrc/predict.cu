@@ -11,7 +11,8 @@
 // Kernel 1 (HBM-bound) streams Q and K once: one CTA per (tensor, b, h, 8
 // consecutive groups) sums each group's `block` rows with 16-byte loads, then
 // projects the 8 means to rank r with the head's W staged once in shared
-// memory.  Kernel 2 writes the G x nb score matrix of each (b, h) from the
+// memory (for the fused predictor + top-k it also writes the tf32 hi / lo
+// parts of each projected vector, the operands of its tensor-core scores).  Kernel 2 writes the G x nb score matrix of each (b, h) from the
 // pooled vectors with r-deep fp32 FMA register tiles (8 x 8 per thread).
 #include <cuda_bf16.h>
 
@@ -25,6 +26,14 @@ namespace {
 
 constexpr int kPoolThreads = 256;
 constexpr int kGPC = 8;                  // groups pooled per CTA (one W load per CTA)
+constexpr int kSplitCols = 32;           // columns of the fused predictor's tf32 operand rows (r <= 32)
+
+// x rounded to tf32 (10 mantissa bits, to nearest, ties away from zero), as fp32 bits
+__device__ __forceinline__ float tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
 
 __device__ __forceinline__ uint4 ld_stream_u4(const uint4* p) {
   uint4 v;
@@ -53,7 +62,8 @@ __global__ void __launch_bounds__(kPoolThreads) pool_project_kernel(const __nv_b
                                                                     const __nv_bfloat16* __restrict__ K,
                                                                     const float* __restrict__ Wq,
                                                                     const float* __restrict__ Wk, int H, int G,
-                                                                    float* __restrict__ qp, float* __restrict__ kp) {
+                                                                    float* __restrict__ qp, float* __restrict__ kp,
+                                                                    float* __restrict__ split, long long split_stride) {
   constexpr int VEC = D / 8;                   // 16-byte vectors per row
   constexpr int RPP = kPoolThreads / VEC;      // rows per pass
   constexpr int PASSES = BLOCK / RPP;
@@ -110,7 +120,25 @@ __global__ void __launch_bounds__(kPoolThreads) pool_project_kernel(const __nv_b
       s0 = fmaf(mean[gi][cc], w_s[cc * R + col], s0);
       s1 = fmaf(mean[gi][cc + 1], w_s[(cc + 1) * R + col], s1);
     }
-    out[(bh * G + g0 + gi) * R + col] = s0 + s1;
+    const float v = s0 + s1;
+    const long long row = bh * G + g0 + gi;
+    out[row * R + col] = v;
+    if (split != nullptr) {
+      // the tf32 parts of the fused predictor: hi = tf32(v), lo = tf32(v - hi),
+      // rows of kSplitCols columns (zero beyond R); parts q hi, q lo, k hi, k lo
+      float* hi = split + (2 * which) * split_stride + row * kSplitCols;
+      const float h = tf32_rna(v);
+      hi[col] = h;
+      hi[split_stride + col] = tf32_rna(v - h);
+    }
+  }
+  if (split != nullptr && R < kSplitCols) {
+    for (int o = threadIdx.x; o < ng * (kSplitCols - R); o += kPoolThreads) {
+      const int gi = o / (kSplitCols - R), col = R + o - gi * (kSplitCols - R);
+      float* hi = split + (2 * which) * split_stride + (bh * G + g0 + gi) * kSplitCols;
+      hi[col] = 0.f;
+      hi[split_stride + col] = 0.f;
+    }
   }
 }
 
@@ -202,13 +230,14 @@ __global__ void __launch_bounds__(256) score_kernel(const float* __restrict__ qp
 
 template <int D, int BLOCK, int R>
 cudaError_t launch_pool(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s, float* qp,
-                        float* kp, cudaStream_t st) {
+                        float* kp, cudaStream_t st, float* split = nullptr, long long part = 0) {
+  if (split != nullptr && R > kSplitCols) return cudaErrorInvalidValue;
   const int G = s.N / s.block;
   const long long ctas = (long long)s.B * s.H * ((G + kGPC - 1) / kGPC);
   dim3 grid((unsigned)ctas, 2);
   pool_project_kernel<D, BLOCK, R><<<grid, kPoolThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(Q),
                                                                   static_cast<const __nv_bfloat16*>(K), Wq, Wk, s.H,
-                                                                  G, qp, kp);
+                                                                  G, qp, kp, split, part);
   return cudaGetLastError();
 }
 
@@ -236,13 +265,13 @@ cudaError_t launch_predict_r(const void* Q, const void* K, const float* Wq, cons
 }  // namespace
 
 cudaError_t launch_pool_project(const void* Q, const void* K, const float* Wq, const float* Wk, const dsv_shape& s,
-                                float* qp, float* kp, cudaStream_t st) {
+                                float* qp, float* kp, cudaStream_t st, float* split, long long part) {
   auto pool = [&](auto rtag) -> cudaError_t {
     constexpr int R = decltype(rtag)::value;
-    if (s.d == 128 && s.block == 128) return launch_pool<128, 128, R>(Q, K, Wq, Wk, s, qp, kp, st);
-    if (s.d == 128 && s.block == 64) return launch_pool<128, 64, R>(Q, K, Wq, Wk, s, qp, kp, st);
-    if (s.d == 64 && s.block == 128) return launch_pool<64, 128, R>(Q, K, Wq, Wk, s, qp, kp, st);
-    return launch_pool<64, 64, R>(Q, K, Wq, Wk, s, qp, kp, st);
+    if (s.d == 128 && s.block == 128) return launch_pool<128, 128, R>(Q, K, Wq, Wk, s, qp, kp, st, split, part);
+    if (s.d == 128 && s.block == 64) return launch_pool<128, 64, R>(Q, K, Wq, Wk, s, qp, kp, st, split, part);
+    if (s.d == 64 && s.block == 128) return launch_pool<64, 128, R>(Q, K, Wq, Wk, s, qp, kp, st, split, part);
+    return launch_pool<64, 64, R>(Q, K, Wq, Wk, s, qp, kp, st, split, part);
   };
   switch (s.r) {
     case 8: return pool(std::integral_constant<int, 8>{});

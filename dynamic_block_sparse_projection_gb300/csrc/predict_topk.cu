@@ -6,8 +6,9 @@
 // block score matrix ([hi] 2B says the same).  Here the pooled rank-r vectors
 // (qbar_g, kbar_j, as in predict.cu) go through:
 //
-//   split_tf32_kernel   every pooled vector x becomes x_hi = tf32(x) and
-//                       x_lo = tf32(x - x_hi), zero-padded to 32 rank columns.
+//   pool_project_kernel (predict.cu) writes, beside each pooled vector x,
+//                       x_hi = tf32(x) and x_lo = tf32(x - x_hi), zero-padded
+//                       to 32 rank columns.
 //   kstats_*_kernel     per head, the mean and covariance of the pooled keys.
 //   score_select_kernel one CTA per (b, h) and 128 consecutive groups.  The
 //                       score tile S[g, j] = qbar_g . kbar_j of 128 groups x
@@ -33,9 +34,10 @@
 //   A row whose bin b* holds more than kCand scores and is only partly kept
 //   (for example a row of equal scores) is finished by an exact radix select
 //   on order-preserving 32-bit keys (five digit passes and an emit pass, run
-//   by the CTA only when one of its rows needs it).  Each thread then writes
-//   its row's ascending list; the bitmask, in the layout of the two-call
-//   top-k's workspace, feeds the same transpose kernels.
+//   by the CTA only when one of its rows needs it).  The four threads of a row
+//   then write its ascending list, each a quarter of the row's bitmask words
+//   after the counts of the quarters before it; the bitmask, in the layout of
+//   the two-call top-k's workspace, feeds the same transpose kernels.
 #include <cuda_runtime.h>
 
 #include <type_traits>
@@ -61,7 +63,7 @@ constexpr int kSelWarps = 4 * kColGroups;
 constexpr int kThreads = 32 * (kSelWarp0 + kSelWarps);
 constexpr int kTileBytes = kRows * kRP * 4;   // one 128 x 32 fp32 operand tile (16 KB)
 constexpr int kNumMain = 3;             // passes 0..2 (pass 0: the row moments, in closed form, no tiles)
-constexpr int kKStatSplits = 16;
+constexpr int kKStatSplits = 64;
 constexpr int kKStat = kRP + kRP * kRP;   // per head: mu[32], then C[32][32]
 constexpr int kNumRadix = 6;            // digit passes of the exact fallback (6, 6, 6, 6, 6, 2 bits)
 constexpr int kRadixBins = 64;
@@ -96,12 +98,6 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-__device__ __forceinline__ float tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
-}
-
 // Instruction descriptor of kind::tf32 with fp32 accumulation, both operands
 // K-major: D format F32 (bits 4-5 = 1), A and B format TF32 (bits 7-9 and
 // 10-12 = 2), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
@@ -123,28 +119,6 @@ __device__ __forceinline__ void mma_tf32_w(uint32_t d_tmem, uint64_t a_desc, uin
 }
 
 // ---------------------------------------------------------------------------
-// tf32 hi / lo parts of the pooled vectors
-// ---------------------------------------------------------------------------
-// grid-stride over 2 * rows * 32 outputs; part 0 = queries, part 1 = keys.
-__global__ void __launch_bounds__(256) split_tf32_kernel(const float* __restrict__ qp, const float* __restrict__ kp,
-                                                         int r, long long rows, float* __restrict__ qh,
-                                                         float* __restrict__ ql, float* __restrict__ kh,
-                                                         float* __restrict__ kl) {
-  const long long n = rows * kRP;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n; i += (long long)gridDim.x * blockDim.x) {
-    const bool keys = i >= n;
-    const long long e = keys ? i - n : i;
-    const long long row = e / kRP;
-    const int c = (int)(e - row * kRP);
-    const float x = c < r ? (keys ? kp : qp)[row * r + c] : 0.f;
-    const float hi = tf32_rna(x);
-    const float lo = tf32_rna(x - hi);
-    (keys ? kh : qh)[e] = hi;
-    (keys ? kl : ql)[e] = lo;
-  }
-}
-
-// ---------------------------------------------------------------------------
 // Per-head statistics of the pooled keys: the mean and covariance of a row of
 // scores are closed forms of them, S[g, .] = qbar_g . kbar_.:
 //   mean_j S[g, j] = qbar_g . mu,   var_j S[g, j] = qbar_g^T C qbar_g,
@@ -153,35 +127,58 @@ __global__ void __launch_bounds__(256) split_tf32_kernel(const float* __restrict
 // fixed order: kKStatSplits partial sums per head, then one reduction.
 // ---------------------------------------------------------------------------
 
-// grid: (B*H, kKStatSplits), 1024 threads: thread (i, j) = (t / 32, t % 32)
-__global__ void __launch_bounds__(1024) kstats_partial_kernel(const float* __restrict__ kp, int r, int G,
-                                                              float* __restrict__ part) {
-  __shared__ float tile[128][kRP + 1];
+// grid: (B*H, kKStatSplits), 256 threads: slice t / 64 of the split's rows,
+// entries i = 4 ib .. 4 ib + 3, j = 4 jb .. 4 jb + 3 with ib = (t / 8) % 8,
+// jb = t % 8 (a 4 x 4 register block: 16 fma per two vector loads); the four
+// slices are summed in shared memory in fixed order.
+constexpr int kStatRows = 64;           // rows of a split staged at a time
+__global__ void __launch_bounds__(256) kstats_partial_kernel(const float* __restrict__ kp, int r, int G,
+                                                             float* __restrict__ part) {
+  __shared__ __align__(16) float tile[kStatRows][kRP];
+  __shared__ float red[4][kKStat];
   __shared__ float k0[kRP];
   const long long bh = blockIdx.x;
-  const int t = threadIdx.x, i = t >> 5, j = t & 31;
+  const int t = threadIdx.x, slice = t >> 6, ib = (t >> 3) & 7, jb = t & 7;
   const float* K = kp + bh * G * (long long)r;
   const int per = (G + kKStatSplits - 1) / kKStatSplits;
   const int g_begin = blockIdx.y * per, g_end = min(G, g_begin + per);
   if (t < kRP) k0[t] = t < r ? K[t] : 0.f;
-  float acc = 0.f, si = 0.f;
-  for (int g0 = g_begin; g0 < g_end; g0 += 128) {
+  float acc[4][4], si[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    si[m] = 0.f;
+#pragma unroll
+    for (int n = 0; n < 4; ++n) acc[m][n] = 0.f;
+  }
+  for (int g0 = g_begin; g0 < g_end; g0 += kStatRows) {
     __syncthreads();
-    for (int e = t; e < 128 * kRP; e += 1024) {
+    for (int e = t; e < kStatRows * kRP; e += 256) {
       const int row = e / kRP, c = e % kRP;
       tile[row][c] = (g0 + row < g_end && c < r) ? K[(long long)(g0 + row) * r + c] - k0[c] : 0.f;
     }
     __syncthreads();
-    const int nrow = min(128, g_end - g0);
-    for (int row = 0; row < nrow; ++row) {
-      const float a = tile[row][i];
-      acc = fmaf(a, tile[row][j], acc);
-      si += a;
+    const int nrow = min(kStatRows, g_end - g0);
+    for (int row = slice; row < nrow; row += 4) {
+      const float4 a = *reinterpret_cast<const float4*>(&tile[row][4 * ib]);
+      const float4 b = *reinterpret_cast<const float4*>(&tile[row][4 * jb]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        si[m] += av[m];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) acc[m][n] = fmaf(av[m], bv[n], acc[m][n]);
+      }
     }
   }
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    if (jb == 0) red[slice][4 * ib + m] = si[m];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) red[slice][kRP + (4 * ib + m) * kRP + 4 * jb + n] = acc[m][n];
+  }
+  __syncthreads();
   float* P = part + (bh * kKStatSplits + blockIdx.y) * (long long)kKStat;
-  if (j == 0) P[i] = si;
-  P[kRP + i * kRP + j] = acc;
+  for (int e = t; e < kKStat; e += 256) P[e] = ((red[0][e] + red[1][e]) + red[2][e]) + red[3][e];
 }
 
 // grid: B*H, 1024 threads: mu and C of each head from its partial sums
@@ -260,6 +257,7 @@ struct RowShared {
   uint32_t kk;           // how many of that bin are kept
   int ccount;            // scores collected from that bin so far
   int fail;              // the row needs the exact fallback
+  int cnt[kColGroups];   // output: kept blocks in each thread's range of words
 };
 
 // bitmask word wi of row r in the shared column region (XOR spread: a warp's
@@ -735,7 +733,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   }
 
   // outputs: the bitmask words (coalesced over consecutive rows), then the
-  // ascending lists, written cooperatively row by row
+  // ascending lists.  After this barrier every failed wait has raised the abort
+  // flag, so out_ok is the same in every thread and the named barriers below
+  // are reached by all selection warps or by none.
+  __syncthreads();
   const bool out_ok = ok && !*abort_flag;
   if (sel && out_ok) {
     if (row_ok && select_all) {
@@ -747,36 +748,38 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
     sel_barrier();                                       // every word of every row is final
     if (row_ok)
       for (int wi = cg; wi < words; wi += kColGroups) a.mask[(bh * words + wi) * (long long)G + g] = hist[word_at(wi, r)];
-    const long long hbase = (long long)b * G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * G;
-    const int cw = warp - kSelWarp0;
-    for (int rr = 0; rr < kRows / kSelWarps; ++rr) {
-      const int r2 = cw * (kRows / kSelWarps) + rr;
-      const int g2 = g0 + r2;
-      if (g2 >= G) break;
-      int32_t* dst = a.fwd_col + hbase + (long long)g2 * k;
-      int run = 0;
-      for (int i = 0; i * 32 < words; ++i) {
-        const int wi = i * 32 + lane;
-        uint32_t m = wi < words ? hist[word_at(wi, r2)] : 0u;
-        const int cnt = __popc(m);
-        int inc = cnt;
+    // the ascending list of row r: thread cg writes the blocks of words
+    // [cg * wpt, (cg + 1) * wpt), after the counts of the row's earlier threads
+    const int wpt = (words + kColGroups - 1) / kColGroups;
+    const int w0 = cg * wpt, w1 = min(words, w0 + wpt);
+    if (row_ok) {
+      int cnt = 0;
+      for (int wi = w0; wi < w1; ++wi) cnt += __popc(hist[word_at(wi, r)]);
+      rs[r].cnt[cg] = cnt;
+    }
+    sel_barrier();
+    if (row_ok) {
+      int pos = 0, total = 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, inc, o);
-          if (lane >= o) inc += v;
-        }
-        int pos = run + inc - cnt;
+      for (int q = 0; q < kColGroups; ++q) {
+        const int c = rs[r].cnt[q];
+        pos += q < cg ? c : 0;
+        total += c;
+      }
+      const long long hbase = (long long)b * G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * G;
+      int32_t* dst = a.fwd_col + hbase + (long long)g * k;
+      for (int wi = w0; wi < w1; ++wi) {
+        uint32_t m = hist[word_at(wi, r)];
         while (m) {
           if (pos < k) dst[pos] = wi * 32 + __ffs(m) - 1;
           ++pos;
           m &= m - 1u;
         }
-        run += __shfl_sync(0xffffffffu, inc, 31);
       }
-      if (lane == 0) {
-        if (run != k) set_error(ctl, DSV_ERR_INTERNAL, (unsigned int)((bh * G + g2) & 0x7fffffff));
-        a.fwd_ptr[bh * G + g2] = (int32_t)(hbase + (long long)g2 * k);
-        if (bh * G + g2 == a.rows - 1) a.fwd_ptr[a.rows] = a.nnz;
+      if (cg == 0) {
+        if (total != k) set_error(ctl, DSV_ERR_INTERNAL, (unsigned int)(grow & 0x7fffffff));
+        a.fwd_ptr[grow] = (int32_t)(hbase + (long long)g * k);
+        if (grow == a.rows - 1) a.fwd_ptr[a.rows] = a.nnz;
       }
     }
   }
@@ -801,20 +804,20 @@ size_t split_tf32_bytes(const dsv_shape& s) {
          align256(bhs * kKStatSplits * kKStat * sizeof(float)) + align256(bhs * kKStat * sizeof(float));
 }
 
-cudaError_t launch_split_tf32(const float* qp, const float* kp, const dsv_shape& s, float* split, cudaStream_t st) {
-  const long long rows = (long long)s.B * s.H * (s.N / s.block);
-  const size_t part = align256((size_t)rows * kRP * sizeof(float)) / sizeof(float);
-  const long long n = 2 * rows * kRP;
-  const unsigned grid = (unsigned)std::min<long long>((n + 255) / 256, 152LL * 16);
-  split_tf32_kernel<<<grid, 256, 0, st>>>(qp, kp, s.r, rows, split, split + part, split + 2 * part, split + 3 * part);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // per-head key statistics after the four parts: partial sums, then mu and C
+long long split_part_floats(const dsv_shape& s) {
+  const size_t rows = (size_t)s.B * s.H * (size_t)(s.N / s.block);
+  return (long long)(align256(rows * kRP * sizeof(float)) / sizeof(float));
+}
+
+cudaError_t launch_key_stats(const float* kp, const dsv_shape& s, float* split, cudaStream_t st) {
+  // per-head key statistics after the four tf32 parts: partial sums, then mu and C
+  const long long part = split_part_floats(s);
   const unsigned bhs = (unsigned)(s.B * s.H);
   float* kpart = split + 4 * part;
   float* kstats = kpart + align256((size_t)bhs * kKStatSplits * kKStat * sizeof(float)) / sizeof(float);
-  kstats_partial_kernel<<<dim3(bhs, kKStatSplits), 1024, 0, st>>>(kp, s.r, s.N / s.block, kpart);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  kstats_partial_kernel<<<dim3(bhs, kKStatSplits), 256, 0, st>>>(kp, s.r, s.N / s.block, kpart);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   kstats_reduce_kernel<<<bhs, 1024, 0, st>>>(kp, s.r, s.N / s.block, kpart, kstats);
   return cudaGetLastError();
 }

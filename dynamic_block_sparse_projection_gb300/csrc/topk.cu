@@ -19,8 +19,9 @@
 //                  mask (stored word column by word column, rows contiguous)
 //                  give each column's population.
 //   topk_scan      per (b, h): exclusive scan of the column counts -> bwd_ptr.
-//   topk_fill      same walk as colcount; each lane appends the set rows of
-//                  its column in ascending g.
+//   topk_fill      same walk as colcount; per column with entries in a
+//                  32-row chunk, one ballot and one coalesced store of
+//                  those rows, in ascending g.
 #include <algorithm>
 
 #include "dsv_launch.h"
@@ -500,7 +501,11 @@ __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
 // rows of segment seg that selected column col.
 constexpr int kSeg = 512;
 
+constexpr int kSegChunks = kSeg / 32;
+
 // grid: (ceil(words / 8), nseg, B*H); warp w handles mask word column blockIdx.x*8 + w.
+// Every mask load of the segment is issued before the first is used (2 KB in
+// flight per warp).
 __global__ void __launch_bounds__(256) topk_colcount_kernel(const uint32_t* __restrict__ mask, int G, int nb,
                                                             int words, int32_t* __restrict__ counts) {
   const int wc = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -509,14 +514,16 @@ __global__ void __launch_bounds__(256) topk_colcount_kernel(const uint32_t* __re
   const int seg = blockIdx.y, nseg = gridDim.y;
   const long long bh = blockIdx.z;
   const uint32_t* M = mask + (bh * words + wc) * (long long)G;   // this word column, rows contiguous
-  const int g1 = min(G, (seg + 1) * kSeg);
-  int cnt = 0;
-#pragma unroll 4
-  for (int g0 = seg * kSeg; g0 < g1; g0 += 32) {
-    const int g = g0 + lane;
-    const uint32_t x = (g < g1) ? M[g] : 0u;
-    cnt += __popc(warp_transpose32(x, lane));
+  const int gs = seg * kSeg, g1 = min(G, gs + kSeg);
+  uint32_t xs[kSegChunks];
+#pragma unroll
+  for (int i = 0; i < kSegChunks; ++i) {
+    const int g = gs + 32 * i + lane;
+    xs[i] = g < g1 ? __ldg(M + g) : 0u;
   }
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < kSegChunks; ++i) cnt += __popc(warp_transpose32(xs[i], lane));
   const int col = wc * 32 + lane;
   if (col < nb) counts[(bh * nseg + seg) * nb + col] = cnt;
 }
@@ -570,57 +577,44 @@ __global__ void __launch_bounds__(1024) topk_scan_kernel(int32_t* __restrict__ c
   if (bh == nslices - 1 && t == 0) bwd_ptr[nslices * nb] = a.row_k ? a.row_ptr[a.rows] : a.nnz;
 }
 
-// Each warp walks the G rows of 32 mask columns (one word column), 32 rows at a
-// time; after a 32x32 bit transpose lane l holds column l's bits.  The rows
-// found are staged per column in shared memory and written out 33..64 at a
-// time by the whole warp (coalesced), not one 4-byte store per lane.
+// Each warp walks the rows of one segment of 32 mask columns (one word column),
+// 32 rows at a time (lane i holds row g0 + i's word).  For every column with an
+// entry among these rows (in ascending order) a ballot gives the rows that
+// selected it, and those lanes store their row at the column's next output
+// positions, consecutive in lane order: one coalesced store per (column,
+// 32-row chunk), however many rows selected the column.  Lane l keeps the next
+// output position of column wc * 32 + l.
 constexpr int kFillWarps = 4;
-constexpr int kFillCap = 64;             // staged entries per column
 // grid: (ceil(words / kFillWarps), nseg, B*H); pos = counts after topk_scan.
 __global__ void __launch_bounds__(kFillWarps * 32) topk_fill_kernel(const uint32_t* __restrict__ mask, int G, int nb,
                                                                     int words, const int32_t* __restrict__ pos,
                                                                     int32_t* __restrict__ bwd_col) {
-  __shared__ int32_t stage[kFillWarps][32][kFillCap + 1];   // +1: lanes at the same depth hit different banks
   const int warp = threadIdx.x >> 5;
   const int wc = blockIdx.x * kFillWarps + warp;
   if (wc >= words) return;
   const int lane = threadIdx.x & 31;
+  const uint32_t below = (1u << lane) - 1u;             // lanes before this one
   const int seg = blockIdx.y, nseg = gridDim.y;
   const long long bh = blockIdx.z;
   const uint32_t* M = mask + (bh * words + wc) * (long long)G;   // this word column, rows contiguous
   const int col = wc * 32 + lane;
-  int32_t (*buf)[kFillCap + 1] = stage[warp];
-  int cur = (col < nb) ? pos[(bh * nseg + seg) * nb + col] : 0;   // next output position of this lane's column
-  int cnt = 0;                                          // staged entries of this lane's column
-  auto flush = [&](unsigned who) {
-    while (who) {
-      const int l = __ffs(who) - 1;
-      who &= who - 1u;
-      const int n = __shfl_sync(0xffffffffu, cnt, l);
-      const int base = __shfl_sync(0xffffffffu, cur, l);
-      for (int i = lane; i < n; i += 32) bwd_col[base + i] = buf[l][i];
-      if (lane == l) {
-        cur += cnt;
-        cnt = 0;
-      }
-    }
-    __syncwarp();
-  };
+  int cur = (col < nb) ? pos[(bh * nseg + seg) * nb + col] : 0;
   const int gs = seg * kSeg, g1 = min(G, gs + kSeg);
   uint32_t xn = (gs + lane < g1) ? M[gs + lane] : 0u;
   for (int g0 = gs; g0 < g1; g0 += 32) {
     const uint32_t x = xn;
     if (g0 + 32 < g1) xn = (g0 + 32 + lane < g1) ? M[g0 + 32 + lane] : 0u;   // next chunk in flight
-    uint32_t t = warp_transpose32(x, lane);
-    flush(__ballot_sync(0xffffffffu, cnt + __popc(t) > kFillCap));
-    while (t) {
-      const int bit = __ffs(t) - 1;
-      buf[lane][cnt++] = g0 + bit;
-      t &= t - 1u;
+    uint32_t cols = __reduce_or_sync(0xffffffffu, x);   // columns with an entry in these rows
+    while (cols) {
+      const int c = __ffs(cols) - 1;
+      cols &= cols - 1u;
+      const bool mine = (x >> c) & 1u;
+      const uint32_t rows = __ballot_sync(0xffffffffu, mine);
+      const int base = __shfl_sync(0xffffffffu, cur, c);
+      if (mine) bwd_col[base + __popc(rows & below)] = g0 + lane;
+      if (lane == c) cur += __popc(rows);
     }
-    __syncwarp();
   }
-  flush(__ballot_sync(0xffffffffu, cnt > 0));
 }
 
 // ---------------------------------------------------------------------------
