@@ -28,6 +28,38 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 dsv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DSV_OK : DSV_ERR_CUDA; }
 
+// A second stream (and two events) per device for the fused predictor +
+// top-k: the transposed lists of the heads whose rows are all selected are
+// built there while the select kernel's last, partly filled wave runs on the
+// caller's stream.  g_fork_mu keeps one call's record / wait / launch
+// sequence on these objects from interleaving with another's.
+struct ForkRes {
+  cudaStream_t side = nullptr;
+  cudaEvent_t main_done = nullptr, side_done = nullptr;
+  int nsm = 0;
+};
+ForkRes g_fork[kMaxDevices];
+std::mutex g_fork_mu;
+
+cudaError_t fork_res(ForkRes** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  ForkRes& f = g_fork[dev];
+  if (f.side == nullptr) {
+    ForkRes n;
+    if ((e = cudaDeviceGetAttribute(&n.nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&n.side, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&n.main_done, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&n.side_done, cudaEventDisableTiming)) != cudaSuccess) return e;
+    f = n;
+  }
+  *out = &f;
+  return cudaSuccess;
+}
+
 // Control block of the current device (error word address, wait limit).
 cudaError_t current_ctl(Ctl* ctl) {
   int dev = 0;
@@ -313,11 +345,31 @@ dsv_status dsv_predict_topk_blocks(const void* Q, const void* K, const float* Wq
       make_map_f32x32(&maps.kh, sp + 2 * part, (long long)rows, 128) != cudaSuccess ||
       make_map_f32x32(&maps.kl, sp + 3 * part, (long long)rows, 128) != cudaSuccess)
     return DSV_ERR_CUDA;
-  cudaError_t e = launch_pool_project(Q, K, Wq, Wk, s, qp, kp, st, split, split_part_floats(s));
+  ForkRes* fr = nullptr;
+  cudaError_t e = fork_res(&fr);
+  if (e == cudaSuccess) e = launch_pool_project(Q, K, Wq, Wk, s, qp, kp, st, split, split_part_floats(s));
   if (e == cudaSuccess) e = launch_key_stats(kp, s, split, st);
-  if (e == cudaSuccess)
-    e = launch_score_select(maps, s, hk, nnz, fwd_ptr, fwd_col, static_cast<uint32_t*>(tws), scores, split, ctl, st);
-  if (e == cudaSuccess) e = launch_topk_transpose(s, hk, nnz, bwd_ptr, bwd_col, tws, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  uint32_t* mask = static_cast<uint32_t*>(tws);
+  // The select kernel runs one CTA per SM; the items of a last, partly filled
+  // wave go into a launch of their own, and the transposes of the heads done
+  // before it run beside it on the side stream.
+  const long long tiles = select_tiles(s), bhs = (long long)s.B * s.H, items = bhs * tiles;
+  const long long tail = items % fr->nsm, n1 = items - tail, heads1 = n1 / tiles;
+  if (tail == 0 || items < 2LL * fr->nsm || heads1 == 0) {
+    e = launch_score_select(maps, s, hk, nnz, fwd_ptr, fwd_col, mask, scores, split, ctl, st);
+    if (e == cudaSuccess) e = launch_topk_transpose(s, hk, nnz, bwd_ptr, bwd_col, tws, st);
+    return from_cuda(e);
+  }
+  std::lock_guard<std::mutex> lock(g_fork_mu);
+  e = launch_score_select(maps, s, hk, nnz, fwd_ptr, fwd_col, mask, scores, split, ctl, st, 0, n1);
+  if (e == cudaSuccess) e = cudaEventRecord(fr->main_done, st);
+  if (e == cudaSuccess) e = launch_score_select(maps, s, hk, nnz, fwd_ptr, fwd_col, mask, scores, split, ctl, st, n1, items);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(fr->side, fr->main_done, 0);
+  if (e == cudaSuccess) e = launch_topk_transpose(s, hk, nnz, bwd_ptr, bwd_col, tws, fr->side, 0, heads1);
+  if (e == cudaSuccess) e = cudaEventRecord(fr->side_done, fr->side);
+  if (e == cudaSuccess) e = launch_topk_transpose(s, hk, nnz, bwd_ptr, bwd_col, tws, st, heads1, -1);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, fr->side_done, 0);
   return from_cuda(e);
 }
 

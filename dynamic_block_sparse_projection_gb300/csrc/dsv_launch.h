@@ -37,8 +37,10 @@ size_t topk_ws_bytes(const dsv_shape& s);
 // The transposed lists only, from a selection bitmask already in `ws` (the
 // layout launch_topk's select kernel writes: word (b, h, w, g) at
 // ((b*H + h) * words + w) * G + g).
+// Heads (slices b*H + h) bh0 .. bh1 - 1 only (bh1 < 0: to the last).
 cudaError_t launch_topk_transpose(const dsv_shape& s, const HeadK& hk, int64_t nnz, int32_t* bwd_ptr,
-                                  int32_t* bwd_col, void* ws, cudaStream_t st);
+                                  int32_t* bwd_col, void* ws, cudaStream_t st, long long bh0 = 0,
+                                  long long bh1 = -1);
 // Pooled rank-r projections only (qp, kp: [B*H*G, r] fp32), the first kernel of launch_predict.
 // split != null (r <= 32): also the tf32 hi / lo parts of every projected
 // vector, zero-padded to 32 columns: four [B*H*G, 32] fp32 arrays (q hi, q lo,
@@ -57,10 +59,14 @@ struct PredictTopkMaps {
   CUtensorMap qh, ql, kh, kl;
 };
 long long split_part_floats(const dsv_shape& s);
+// Score/select items: (b*H + h) * select_tiles(s) + tile, tile = 128 groups; a
+// launch covers items item0 .. item1 - 1 (item1 < 0: to the last).
+long long select_tiles(const dsv_shape& s);
 cudaError_t launch_key_stats(const float* kp, const dsv_shape& s, float* split, cudaStream_t st);
 cudaError_t launch_score_select(const PredictTopkMaps& maps, const dsv_shape& s, const HeadK& hk, int64_t nnz,
                                 int32_t* fwd_ptr, int32_t* fwd_col, uint32_t* mask, float* scores, const float* split,
-                                const Ctl& ctl, cudaStream_t st);
+                                const Ctl& ctl, cudaStream_t st, long long item0 = 0,
+                                long long item1 = -1);
 size_t split_tf32_bytes(const dsv_shape& s);
 // Mass-threshold selection: per row the smallest top set carrying >= tau of
 // the predicted softmax mass (temperature * scores), clamped to [kmin, kmax].

@@ -78,6 +78,7 @@ constexpr unsigned int KID_SEL = 4;
 struct SelArgs {
   CUtensorMap qh, ql, kh, kl;          // [B*H*G, 32] fp32, box 32 x 128, 128-byte swizzle
   int H, G, words, tiles;              // tiles = ceil(G / 128) per (b, h)
+  long long item0;                     // CTA x takes item item0 + x (item = (b*H + h) * tiles + tile)
   long long rows;                      // B*H*G
   int nnz;
   int32_t* fwd_ptr;
@@ -213,13 +214,10 @@ __device__ __forceinline__ float fma_sat(float a, float b, float c) {
   asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-// all ones where a > b, else zero (one instruction)
-__device__ __forceinline__ uint32_t gt_mask(float a, float b) {
-  uint32_t d;
-  asm("set.gt.u32.f32 %0, %1, %2;" : "=r"(d) : "f"(a), "f"(b));
-  return d;
+// (w << 1) | sign bit of d: one funnel shift of the 64-bit value w:d
+__device__ __forceinline__ uint32_t shift_in_sign(uint32_t w, float d) {
+  return __funnelshift_l(__float_as_uint(d), w, 1);
 }
-
 // The bin map of a row: z = clamp(s * sc + c0, 0, 1) (scores below the binned
 // range give 0, above it 1), bin = round(127 z), returned as the float bits
 // B0 + bin (adding 1.5 * 2^23 leaves the rounded value in the low mantissa
@@ -301,8 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   const Ctl& ctl = a.ctl;
   const unsigned int kid = KID_SEL << 8;
   const int G = a.G, nb = a.G, words = a.words;
-  const long long bh = blockIdx.x / a.tiles;
-  const int g0 = (int)(blockIdx.x - bh * a.tiles) * kRows;
+  const long long item = a.item0 + blockIdx.x;
+  const long long bh = item / a.tiles;
+  const int g0 = (int)(item - bh * a.tiles) * kRows;
   const int h = (int)(bh % a.H), b = (int)(bh / a.H);
   const int k = a.hk.k[h];
   const int nc = (nb + kChunk - 1) / kChunk;             // score tiles of a row
@@ -479,13 +478,22 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             } else if constexpr (P == 2) {
               // word: scores above keep_v; above: scores above coll_v (a superset);
               // the threshold bin's scores are the difference
+              // bit e of a word is the sign of (threshold - score e): the difference
+              // is negative exactly when the score is above the threshold (a
+              // rounded difference keeps the sign of the exact one, equal values
+              // give +0, the thresholds are never -0, and a NaN score gives the
+              // canonical NaN, sign clear).  The sign bits are shifted in from the
+              // top, last column first, so that column e lands on bit e.
               uint32_t word = 0u, above = 0u;
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
+              for (int e = 31; e >= 0; --e) {
                 if (FULL || e < nvg) {
                   const float s = __uint_as_float(x[e]);
-                  word |= gt_mask(s, keep_v) & (1u << e);
-                  above |= gt_mask(s, coll_v) & (1u << e);
+                  word = shift_in_sign(word, __fsub_rn(keep_v, s));
+                  above = shift_in_sign(above, __fsub_rn(coll_v, s));
+                } else {
+                  word <<= 1;
+                  above <<= 1;
                 }
               }
               const uint32_t eq = above & ~word;
@@ -666,8 +674,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
           }
           sel_barrier();                                 // decisions out; the histogram region becomes words
           if (row_ok) {
-            keep_v = rs[r].keep_v;
-            coll_v = rs[r].coll_v;
+            keep_v = __fadd_rn(rs[r].keep_v, 0.0f);      // -0 becomes +0
+            coll_v = __fadd_rn(rs[r].coll_v, 0.0f);
             fail = rs[r].fail != 0;
           }
         } else if (pass == 2) {
@@ -804,6 +812,8 @@ size_t split_tf32_bytes(const dsv_shape& s) {
          align256(bhs * kKStatSplits * kKStat * sizeof(float)) + align256(bhs * kKStat * sizeof(float));
 }
 
+long long select_tiles(const dsv_shape& s) { return (s.N / s.block + kRows - 1) / kRows; }
+
 long long split_part_floats(const dsv_shape& s) {
   const size_t rows = (size_t)s.B * s.H * (size_t)(s.N / s.block);
   return (long long)(align256(rows * kRP * sizeof(float)) / sizeof(float));
@@ -824,7 +834,7 @@ cudaError_t launch_key_stats(const float* kp, const dsv_shape& s, float* split, 
 
 cudaError_t launch_score_select(const PredictTopkMaps& maps, const dsv_shape& s, const HeadK& hk, int64_t nnz,
                                 int32_t* fwd_ptr, int32_t* fwd_col, uint32_t* mask, float* scores, const float* split,
-                                const Ctl& ctl, cudaStream_t st) {
+                                const Ctl& ctl, cudaStream_t st, long long item0, long long item1) {
   SelArgs a;
   a.qh = maps.qh;
   a.ql = maps.ql;
@@ -849,8 +859,11 @@ cudaError_t launch_score_select(const PredictTopkMaps& maps, const dsv_shape& s,
   a.ctl = ctl;
   cudaError_t e = cudaFuncSetAttribute(score_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)s.B * s.H * a.tiles;
-  score_select_kernel<<<(unsigned)grid, kThreads, kSelSmem, st>>>(a);
+  const long long items = (long long)s.B * s.H * a.tiles;
+  if (item1 < 0 || item1 > items) item1 = items;
+  if (item0 < 0 || item0 >= item1) return cudaSuccess;
+  a.item0 = item0;
+  score_select_kernel<<<(unsigned)(item1 - item0), kThreads, kSelSmem, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -53,6 +53,8 @@ struct TopkArgs {
   // first entry row_ptr[bh * G] and the total row_ptr[rows]; null: k per head
   const int32_t* row_k;
   const int32_t* row_ptr;
+  // the transposes cover heads bh0 .. bh0 + gridDim - 1 (slices of B*H)
+  long long bh0;
 };
 
 // One CTA of RT threads per row.  Thread t holds kE consecutive scores
@@ -507,12 +509,12 @@ constexpr int kSegChunks = kSeg / 32;
 // Every mask load of the segment is issued before the first is used (2 KB in
 // flight per warp).
 __global__ void __launch_bounds__(256) topk_colcount_kernel(const uint32_t* __restrict__ mask, int G, int nb,
-                                                            int words, int32_t* __restrict__ counts) {
+                                                            int words, int32_t* __restrict__ counts, long long bh0) {
   const int wc = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (wc >= words) return;
   const int lane = threadIdx.x & 31;
   const int seg = blockIdx.y, nseg = gridDim.y;
-  const long long bh = blockIdx.z;
+  const long long bh = bh0 + blockIdx.z;
   const uint32_t* M = mask + (bh * words + wc) * (long long)G;   // this word column, rows contiguous
   const int gs = seg * kSeg, g1 = min(G, gs + kSeg);
   uint32_t xs[kSegChunks];
@@ -535,7 +537,7 @@ __global__ void __launch_bounds__(1024) topk_scan_kernel(int32_t* __restrict__ c
                                                          const __grid_constant__ TopkArgs a,
                                                          int32_t* __restrict__ bwd_ptr, long long nslices) {
   __shared__ int warp_tot[32];
-  const long long bh = blockIdx.x;
+  const long long bh = a.bh0 + blockIdx.x;
   const int h = (int)(bh % a.H), b = (int)(bh / a.H);
   const int nb = a.nb;
   int32_t* C = counts + bh * (long long)nseg * nb;
@@ -588,14 +590,14 @@ constexpr int kFillWarps = 4;
 // grid: (ceil(words / kFillWarps), nseg, B*H); pos = counts after topk_scan.
 __global__ void __launch_bounds__(kFillWarps * 32) topk_fill_kernel(const uint32_t* __restrict__ mask, int G, int nb,
                                                                     int words, const int32_t* __restrict__ pos,
-                                                                    int32_t* __restrict__ bwd_col) {
+                                                                    int32_t* __restrict__ bwd_col, long long bh0) {
   const int warp = threadIdx.x >> 5;
   const int wc = blockIdx.x * kFillWarps + warp;
   if (wc >= words) return;
   const int lane = threadIdx.x & 31;
   const uint32_t below = (1u << lane) - 1u;             // lanes before this one
   const int seg = blockIdx.y, nseg = gridDim.y;
-  const long long bh = blockIdx.z;
+  const long long bh = bh0 + blockIdx.z;
   const uint32_t* M = mask + (bh * words + wc) * (long long)G;   // this word column, rows contiguous
   const int col = wc * 32 + lane;
   int cur = (col < nb) ? pos[(bh * nseg + seg) * nb + col] : 0;
@@ -960,7 +962,7 @@ size_t topk_ws_bytes(const dsv_shape& s) {
 namespace {
 
 cudaError_t run_topk_transpose(const TopkArgs& a, int32_t* bwd_ptr, int32_t* bwd_col, int32_t* counts,
-                               cudaStream_t st);
+                               cudaStream_t st, long long bh1);
 
 // the select kernel and the transposed lists, for fixed (a.row_k == null) or per-row k
 cudaError_t run_topk(const TopkArgs& a, int32_t* bwd_ptr, int32_t* bwd_col, int32_t* counts, cudaStream_t st) {
@@ -977,24 +979,27 @@ cudaError_t run_topk(const TopkArgs& a, int32_t* bwd_ptr, int32_t* bwd_col, int3
   else if (G <= 256 * kE) topk_select_kernel<256><<<grid, 256, 0, st>>>(a);
   else topk_select_kernel<512><<<grid, 512, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  return run_topk_transpose(a, bwd_ptr, bwd_col, counts, st);
+  return run_topk_transpose(a, bwd_ptr, bwd_col, counts, st, -1);
 }
 
 // The transposed lists from the selection bitmask a.mask: per-segment column
 // counts, their scan into bwd_ptr and output positions, then the fill.
+// Heads a.bh0 .. bh1 - 1 only (bh1 < 0: to the last).
 cudaError_t run_topk_transpose(const TopkArgs& a, int32_t* bwd_ptr, int32_t* bwd_col, int32_t* counts,
-                               cudaStream_t st) {
+                               cudaStream_t st, long long bh1) {
   const int G = a.G, words = a.words;
   const long long bhs = a.rows / G;
+  const long long nh = (bh1 < 0 ? bhs : bh1) - a.bh0;
+  if (nh <= 0) return cudaSuccess;
   cudaError_t e;
   const int nseg = (G + kSeg - 1) / kSeg;
-  dim3 g2((unsigned)((words + 7) / 8), (unsigned)nseg, (unsigned)bhs);
-  topk_colcount_kernel<<<g2, 256, 0, st>>>(a.mask, G, G, words, counts);
+  dim3 g2((unsigned)((words + 7) / 8), (unsigned)nseg, (unsigned)nh);
+  topk_colcount_kernel<<<g2, 256, 0, st>>>(a.mask, G, G, words, counts, a.bh0);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  topk_scan_kernel<<<(unsigned)bhs, 1024, 0, st>>>(counts, nseg, a, bwd_ptr, bhs);
+  topk_scan_kernel<<<(unsigned)nh, 1024, 0, st>>>(counts, nseg, a, bwd_ptr, bhs);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  dim3 g3((unsigned)((words + kFillWarps - 1) / kFillWarps), (unsigned)nseg, (unsigned)bhs);
-  topk_fill_kernel<<<g3, kFillWarps * 32, 0, st>>>(a.mask, G, G, words, counts, bwd_col);
+  dim3 g3((unsigned)((words + kFillWarps - 1) / kFillWarps), (unsigned)nseg, (unsigned)nh);
+  topk_fill_kernel<<<g3, kFillWarps * 32, 0, st>>>(a.mask, G, G, words, counts, bwd_col, a.bh0);
   return cudaGetLastError();
 }
 
@@ -1012,6 +1017,7 @@ TopkArgs topk_args(const float* scores, const dsv_shape& s, int32_t* fwd_ptr, in
   a.rows = (long long)s.B * s.H * G;
   a.row_k = nullptr;
   a.row_ptr = nullptr;
+  a.bh0 = 0;
   return a;
 }
 
@@ -1032,11 +1038,12 @@ cudaError_t launch_topk(const float* scores, const dsv_shape& s, const HeadK& hk
 }
 
 cudaError_t launch_topk_transpose(const dsv_shape& s, const HeadK& hk, int64_t nnz, int32_t* bwd_ptr,
-                                  int32_t* bwd_col, void* ws, cudaStream_t st) {
+                                  int32_t* bwd_col, void* ws, cudaStream_t st, long long bh0, long long bh1) {
   TopkArgs a = topk_args(nullptr, s, nullptr, nullptr, ws);
   a.nnz = (int)nnz;
   a.hk = hk;
-  return run_topk_transpose(a, bwd_ptr, bwd_col, topk_counts(ws, s), st);
+  a.bh0 = bh0;
+  return run_topk_transpose(a, bwd_ptr, bwd_col, topk_counts(ws, s), st, bh1);
 }
 
 size_t topk_mass_ws_bytes(const dsv_shape& s) {
