@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(1024) kstats_reduce_kernel(const float* __rest
   const int t = threadIdx.x, i = t >> 5, j = t & 31;
   const float* P = part + bh * kKStatSplits * (long long)kKStat;
   float acc = 0.f, si = 0.f;
+#pragma unroll 16
   for (int q = 0; q < kKStatSplits; ++q) {
     acc += P[q * kKStat + kRP + i * kRP + j];
     if (j == 0) si += P[q * kKStat + i];

@@ -502,6 +502,7 @@ __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
 // column walks below run in parallel: counts[bh][seg][col] is the number of
 // rows of segment seg that selected column col.
 constexpr int kSeg = 512;
+constexpr int kScanBatch = 8;            // segment counts of a column loaded together by the scan
 
 constexpr int kSegChunks = kSeg / 32;
 
@@ -544,9 +545,21 @@ __global__ void __launch_bounds__(1024) topk_scan_kernel(int32_t* __restrict__ c
   const int per = (nb + 1023) / 1024;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int j0 = t * per;
+  // a column's segment counts are loaded kScanBatch at a time (independent
+  // loads in flight), not one dependent add at a time
+  auto batch = [&](int j, int s0, int (&v)[kScanBatch]) {
+#pragma unroll
+    for (int i = 0; i < kScanBatch; ++i) v[i] = s0 + i < nseg ? C[(s0 + i) * nb + j] : 0;
+  };
   int loc = 0;
-  for (int j = j0; j < min(nb, j0 + per); ++j)
-    for (int sg = 0; sg < nseg; ++sg) loc += C[sg * nb + j];
+  for (int j = j0; j < min(nb, j0 + per); ++j) {
+    for (int s0 = 0; s0 < nseg; s0 += kScanBatch) {
+      int v[kScanBatch];
+      batch(j, s0, v);
+#pragma unroll
+      for (int i = 0; i < kScanBatch; ++i) loc += v[i];
+    }
+  }
   int inc = loc;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -570,10 +583,14 @@ __global__ void __launch_bounds__(1024) topk_scan_kernel(int32_t* __restrict__ c
   int run = (int)base + (w > 0 ? warp_tot[w - 1] : 0) + inc - loc;
   for (int j = j0; j < min(nb, j0 + per); ++j) {
     bwd_ptr[bh * nb + j] = run;
-    for (int sg = 0; sg < nseg; ++sg) {
-      const int c = C[sg * nb + j];
-      C[sg * nb + j] = run;
-      run += c;
+    for (int s0 = 0; s0 < nseg; s0 += kScanBatch) {
+      int v[kScanBatch];
+      batch(j, s0, v);
+#pragma unroll
+      for (int i = 0; i < kScanBatch; ++i) {
+        if (s0 + i < nseg) C[(s0 + i) * nb + j] = run;
+        run += v[i];
+      }
     }
   }
   if (bh == nslices - 1 && t == 0) bwd_ptr[nslices * nb] = a.row_k ? a.row_ptr[a.rows] : a.nnz;
