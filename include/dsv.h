@@ -293,6 +293,17 @@ dsv_status dsv_cube_permute(const void* src, void* dst, dsv_shape s, int T, int 
  *               16-byte aligned: the scores the selection used (a check
  *               output; writing it costs the score matrix's HBM traffic).
  * workspace     >= dsv_predict_topk_workspace_bytes(s) bytes, 256-byte aligned.
+ *
+ * Streams: the work is ordered on `stream`.  When the select kernel's items
+ * (one per 128 groups of a head, one CTA per SM) leave a partly filled last
+ * wave, that wave is a launch of its own and the transposed lists of the
+ * heads already selected are built meanwhile on a second, library-owned
+ * stream of the current device.  That stream first waits on an event
+ * recorded in `stream`, and at the end `stream` waits on an event recorded
+ * after its work, so everything enqueued on `stream` after the call runs
+ * after all of the call's work: the call stays stream-ordered (and can be
+ * captured into a CUDA graph).  A host mutex keeps calls from several threads
+ * from interleaving these event records.
  * ------------------------------------------------------------------------ */
 size_t dsv_predict_topk_workspace_bytes(dsv_shape s);
 dsv_status dsv_predict_topk_blocks(const void* Q, const void* K, const float* Wq, const float* Wk, dsv_shape s,

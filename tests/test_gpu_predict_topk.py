@@ -110,6 +110,25 @@ def test_fused_bitwise_repeatable(dsv):
         assert torch.equal(a, b)
 
 
+def test_fused_many_heads_split_launch(dsv):
+    """Enough heads that the select kernel's items (128 groups of one head
+    each) fill two or more waves of one CTA per SM with a partly filled wave
+    left: that wave runs as a launch of its own while the transposed lists of
+    the heads already selected are built on the second stream.  Every list,
+    forward and transposed, must still match the oracle's top-k of the fused
+    scores; G = 260 leaves a 4-group tile at the end of every head."""
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = 3                                                  # ceil(260 / 128)
+    H = -(-2 * nsm // tiles) + 1
+    while (H * tiles) % nsm == 0:
+        H += 1
+    w = wl.scaled(wl.WORKLOADS["latent16k"], name="many_heads", H=H, d=64, T=26, Hl=10, Wl=128)
+    assert w.nb == 260 and H * tiles >= 2 * nsm
+    x = wl.make_inputs(w, device="cuda", with_dO=False)
+    S, lists = _fused(dsv, x, w)
+    _check_lists_exact(S, lists, x.k_per_head, w.nb)
+
+
 FULL = ["latent16k", "latent123k_global", "stress61k", "long518k"]
 
 
