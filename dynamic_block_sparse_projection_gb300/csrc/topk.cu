@@ -15,11 +15,12 @@
 //                  uint32 keys (ties to the lower index), with an MSB-first
 //                  radix select as the fallback.  Each thread writes its kept
 //                  indices (ascending) and the row's bitmask words.
-//   topk_colcount  per (b, h, 32-column slab): 32x32 bit transposes of the
-//                  mask (stored word column by word column, rows contiguous)
-//                  give each column's population.
-//   topk_scan      per (b, h): exclusive scan of the column counts -> bwd_ptr.
-//   topk_fill      same walk as colcount; per column with entries in a
+//   topk_colcount  per (b, h, 32-column slab), down all rows: 32x32 bit
+//                  transposes of the mask (stored word column by word
+//                  column, rows contiguous) give each column's count before
+//                  every 128-row segment and its total.
+//   topk_scan      per (b, h): exclusive scan of the column totals -> bwd_ptr.
+//   topk_fill      per (slab, segment); per column with entries in a
 //                  32-row chunk, one ballot and one coalesced store of
 //                  those rows, in ascending g.
 #include <algorithm>
@@ -500,66 +501,66 @@ __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
 
 // The G rows of a (b, h) slice are cut into segments of kSeg rows so that the
 // column walks below run in parallel: counts[bh][seg][col] is the number of
-// rows of segment seg that selected column col.
-constexpr int kSeg = 512;
-constexpr int kScanBatch = 8;            // segment counts of a column loaded together by the scan
+// rows of segment seg that selected column col.  Short segments keep the walk
+// of a column that most rows select (a hub) short.
+constexpr int kSeg = 128;
 
 constexpr int kSegChunks = kSeg / 32;
 
-// grid: (ceil(words / 8), nseg, B*H); warp w handles mask word column blockIdx.x*8 + w.
-// Every mask load of the segment is issued before the first is used (2 KB in
-// flight per warp).
+// grid: (ceil(words / 8), heads); warp w walks word column blockIdx.x*8 + w of
+// one (b, h) from the first row to the last, segment by segment (the next
+// segment's loads issued before the current one is counted).  Lane l keeps the
+// count of column wc*32 + l so far: counts[bh][seg][col] gets the entries of
+// the column in the segments before seg, tot[bh][col] the column's total.
 __global__ void __launch_bounds__(256) topk_colcount_kernel(const uint32_t* __restrict__ mask, int G, int nb,
-                                                            int words, int32_t* __restrict__ counts, long long bh0) {
+                                                            int words, int nseg, int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ tot, long long bh0) {
   const int wc = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (wc >= words) return;
   const int lane = threadIdx.x & 31;
-  const int seg = blockIdx.y, nseg = gridDim.y;
-  const long long bh = bh0 + blockIdx.z;
+  const long long bh = bh0 + blockIdx.y;
   const uint32_t* M = mask + (bh * words + wc) * (long long)G;   // this word column, rows contiguous
-  const int gs = seg * kSeg, g1 = min(G, gs + kSeg);
-  uint32_t xs[kSegChunks];
-#pragma unroll
-  for (int i = 0; i < kSegChunks; ++i) {
-    const int g = gs + 32 * i + lane;
-    xs[i] = g < g1 ? __ldg(M + g) : 0u;
-  }
-  int cnt = 0;
-#pragma unroll
-  for (int i = 0; i < kSegChunks; ++i) cnt += __popc(warp_transpose32(xs[i], lane));
   const int col = wc * 32 + lane;
-  if (col < nb) counts[(bh * nseg + seg) * nb + col] = cnt;
+  auto load = [&](int seg, uint32_t (&xs)[kSegChunks]) {
+#pragma unroll
+    for (int i = 0; i < kSegChunks; ++i) {
+      const int g = seg * kSeg + 32 * i + lane;
+      xs[i] = g < G ? __ldg(M + g) : 0u;
+    }
+  };
+  uint32_t xn[kSegChunks];
+  load(0, xn);
+  int run = 0;
+  for (int seg = 0; seg < nseg; ++seg) {
+    uint32_t xs[kSegChunks];
+#pragma unroll
+    for (int i = 0; i < kSegChunks; ++i) xs[i] = xn[i];
+    if (seg + 1 < nseg) load(seg + 1, xn);
+    if (col < nb) counts[(bh * nseg + seg) * nb + col] = run;
+#pragma unroll
+    for (int i = 0; i < kSegChunks; ++i) run += __popc(warp_transpose32(xs[i], lane));
+  }
+  if (col < nb) tot[bh * nb + col] = run;
 }
 
 // One CTA (1024 threads) per (b, h): bwd_ptr = slice base + exclusive scan of
-// the column totals; counts[bh][seg][col] becomes the output position of the
-// first entry of segment seg in column col.
-__global__ void __launch_bounds__(1024) topk_scan_kernel(int32_t* __restrict__ counts, int nseg,
+// the column totals (read coalesced into shared memory, scanned there).
+__global__ void __launch_bounds__(1024) topk_scan_kernel(const int32_t* __restrict__ tot,
                                                          const __grid_constant__ TopkArgs a,
                                                          int32_t* __restrict__ bwd_ptr, long long nslices) {
   __shared__ int warp_tot[32];
+  __shared__ int col[kMaxBlocksPerRow];
   const long long bh = a.bh0 + blockIdx.x;
   const int h = (int)(bh % a.H), b = (int)(bh / a.H);
   const int nb = a.nb;
-  int32_t* C = counts + bh * (long long)nseg * nb;
-  const int per = (nb + 1023) / 1024;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const int j0 = t * per;
-  // a column's segment counts are loaded kScanBatch at a time (independent
-  // loads in flight), not one dependent add at a time
-  auto batch = [&](int j, int s0, int (&v)[kScanBatch]) {
-#pragma unroll
-    for (int i = 0; i < kScanBatch; ++i) v[i] = s0 + i < nseg ? C[(s0 + i) * nb + j] : 0;
-  };
+  for (int j = t; j < nb; j += 1024) col[j] = tot[bh * nb + j];
+  __syncthreads();
+  // thread t takes `per` consecutive columns
+  const int per = (nb + 1023) / 1024;
+  const int j0 = t * per, j1 = min(nb, j0 + per);
   int loc = 0;
-  for (int j = j0; j < min(nb, j0 + per); ++j) {
-    for (int s0 = 0; s0 < nseg; s0 += kScanBatch) {
-      int v[kScanBatch];
-      batch(j, s0, v);
-#pragma unroll
-      for (int i = 0; i < kScanBatch; ++i) loc += v[i];
-    }
-  }
+  for (int j = j0; j < j1; ++j) loc += col[j];
   int inc = loc;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -581,18 +582,13 @@ __global__ void __launch_bounds__(1024) topk_scan_kernel(int32_t* __restrict__ c
   const long long base = a.row_k ? (long long)a.row_ptr[bh * a.G]
                                  : (long long)b * a.G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * a.G;
   int run = (int)base + (w > 0 ? warp_tot[w - 1] : 0) + inc - loc;
-  for (int j = j0; j < min(nb, j0 + per); ++j) {
-    bwd_ptr[bh * nb + j] = run;
-    for (int s0 = 0; s0 < nseg; s0 += kScanBatch) {
-      int v[kScanBatch];
-      batch(j, s0, v);
-#pragma unroll
-      for (int i = 0; i < kScanBatch; ++i) {
-        if (s0 + i < nseg) C[(s0 + i) * nb + j] = run;
-        run += v[i];
-      }
-    }
+  for (int j = j0; j < j1; ++j) {
+    const int c = col[j];
+    col[j] = run;
+    run += c;
   }
+  __syncthreads();
+  for (int j = t; j < nb; j += 1024) bwd_ptr[bh * nb + j] = col[j];
   if (bh == nslices - 1 && t == 0) bwd_ptr[nslices * nb] = a.row_k ? a.row_ptr[a.rows] : a.nnz;
 }
 
@@ -604,9 +600,11 @@ __global__ void __launch_bounds__(1024) topk_scan_kernel(int32_t* __restrict__ c
 // 32-row chunk), however many rows selected the column.  Lane l keeps the next
 // output position of column wc * 32 + l.
 constexpr int kFillWarps = 4;
-// grid: (ceil(words / kFillWarps), nseg, B*H); pos = counts after topk_scan.
+// grid: (ceil(words / kFillWarps), nseg, B*H); the column's entries of segment
+// seg start at bwd_ptr[col] + pos[seg][col] (pos = colcount's in-column counts).
 __global__ void __launch_bounds__(kFillWarps * 32) topk_fill_kernel(const uint32_t* __restrict__ mask, int G, int nb,
                                                                     int words, const int32_t* __restrict__ pos,
+                                                                    const int32_t* __restrict__ bwd_ptr,
                                                                     int32_t* __restrict__ bwd_col, long long bh0) {
   const int warp = threadIdx.x >> 5;
   const int wc = blockIdx.x * kFillWarps + warp;
@@ -617,22 +615,25 @@ __global__ void __launch_bounds__(kFillWarps * 32) topk_fill_kernel(const uint32
   const long long bh = bh0 + blockIdx.z;
   const uint32_t* M = mask + (bh * words + wc) * (long long)G;   // this word column, rows contiguous
   const int col = wc * 32 + lane;
-  int cur = (col < nb) ? pos[(bh * nseg + seg) * nb + col] : 0;
+  int cur = (col < nb) ? bwd_ptr[bh * nb + col] + pos[(bh * nseg + seg) * nb + col] : 0;
   const int gs = seg * kSeg, g1 = min(G, gs + kSeg);
   uint32_t xn = (gs + lane < g1) ? M[gs + lane] : 0u;
   for (int g0 = gs; g0 < g1; g0 += 32) {
     const uint32_t x = xn;
     if (g0 + 32 < g1) xn = (g0 + 32 + lane < g1) ? M[g0 + 32 + lane] : 0u;   // next chunk in flight
     uint32_t cols = __reduce_or_sync(0xffffffffu, x);   // columns with an entry in these rows
+    if (cols == 0u) continue;
+    // the columns' positions advance once per chunk (from the transposed bits),
+    // so the per-column steps below do not depend on one another
+    const uint32_t t = warp_transpose32(x, lane);       // lane l: the rows that selected column l
     while (cols) {
       const int c = __ffs(cols) - 1;
       cols &= cols - 1u;
-      const bool mine = (x >> c) & 1u;
-      const uint32_t rows = __ballot_sync(0xffffffffu, mine);
+      const uint32_t rows = __shfl_sync(0xffffffffu, t, c);
       const int base = __shfl_sync(0xffffffffu, cur, c);
-      if (mine) bwd_col[base + __popc(rows & below)] = g0 + lane;
-      if (lane == c) cur += __popc(rows);
+      if ((rows >> lane) & 1u) bwd_col[base + __popc(rows & below)] = g0 + lane;
     }
+    cur += __popc(t);
   }
 }
 
@@ -973,7 +974,8 @@ size_t topk_ws_bytes(const dsv_shape& s) {
   const size_t words = (G + 31) / 32;
   const size_t bhs = (size_t)s.B * s.H;
   const size_t nseg = (G + kSeg - 1) / kSeg;
-  return align256(bhs * G * words * sizeof(uint32_t)) + align256(bhs * nseg * G * sizeof(int32_t));
+  return align256(bhs * G * words * sizeof(uint32_t)) + align256(bhs * nseg * G * sizeof(int32_t)) +
+         align256(bhs * G * sizeof(int32_t));
 }
 
 namespace {
@@ -1010,13 +1012,14 @@ cudaError_t run_topk_transpose(const TopkArgs& a, int32_t* bwd_ptr, int32_t* bwd
   if (nh <= 0) return cudaSuccess;
   cudaError_t e;
   const int nseg = (G + kSeg - 1) / kSeg;
-  dim3 g2((unsigned)((words + 7) / 8), (unsigned)nseg, (unsigned)nh);
-  topk_colcount_kernel<<<g2, 256, 0, st>>>(a.mask, G, G, words, counts, a.bh0);
+  int32_t* tot = counts + align256((size_t)bhs * nseg * G * sizeof(int32_t)) / sizeof(int32_t);
+  dim3 g2((unsigned)((words + 7) / 8), (unsigned)nh);
+  topk_colcount_kernel<<<g2, 256, 0, st>>>(a.mask, G, G, words, nseg, counts, tot, a.bh0);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  topk_scan_kernel<<<(unsigned)nh, 1024, 0, st>>>(counts, nseg, a, bwd_ptr, bhs);
+  topk_scan_kernel<<<(unsigned)nh, 1024, 0, st>>>(tot, a, bwd_ptr, bhs);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   dim3 g3((unsigned)((words + kFillWarps - 1) / kFillWarps), (unsigned)nseg, (unsigned)nh);
-  topk_fill_kernel<<<g3, kFillWarps * 32, 0, st>>>(a.mask, G, G, words, counts, bwd_col, a.bh0);
+  topk_fill_kernel<<<g3, kFillWarps * 32, 0, st>>>(a.mask, G, G, words, counts, bwd_ptr, bwd_col, a.bh0);
   return cudaGetLastError();
 }
 
