@@ -293,8 +293,22 @@ class HotPath:
                           workspace=self.ws_b)
 
 
-KERNELS_PER_STEP = {"predict": 2, "topk": 4, "predict_topk": 8, "fwd": 1, "bwd_pre": 1, "bwd_kv": 2, "bwd_q": 1,
+KERNELS_PER_STEP = {"predict": 2, "topk": 4, "predict_topk": 7, "fwd": 1, "bwd_pre": 1, "bwd_kv": 2, "bwd_q": 1,
                     "cube_in": 4, "cube_out": 4}
+
+
+def predict_topk_launches(w) -> int:
+    """Kernels of one fused predictor + top-k call: pooling, two statistics
+    kernels, the select kernel and three transpose kernels; when the select
+    items (128 groups of one head each, one CTA per SM) leave a partly filled
+    last wave of at least two full ones, the library launches that wave on its
+    own and the transposes in two head ranges (three more launches)."""
+    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    tiles = -(-w.nb // 128)
+    items = w.B * w.H * tiles
+    tail = items % nsm
+    split = tail != 0 and items >= 2 * nsm and (items - tail) // tiles >= 1
+    return KERNELS_PER_STEP["predict_topk"] + (3 if split else 0)
 STAGES = ("predict", "topk", "fwd", "bwd_pre", "bwd_kv", "bwd_q")
 FUSED_STAGES = ("predict_topk", "fwd", "bwd_pre", "bwd_kv", "bwd_q")
 
@@ -445,7 +459,8 @@ def run_ours(args):
         "predictor_topk": hbm_fractions(w, hp, per_call, peaks),
         "speedup_vs_dense": dense,
         "roofline": roofline,
-        "gpu_launches": (sum(KERNELS_PER_STEP[k] for k in stages) + (2 if args.mass else 0)) * args.steps,
+        "gpu_launches": (sum(predict_topk_launches(w) if k == "predict_topk" else KERNELS_PER_STEP[k] for k in stages)
+                         + (2 if args.mass else 0)) * args.steps,
         "clocks": clk.summary(),
         "e2e": e2e,
         "peaks_source": peak_src,
