@@ -303,6 +303,7 @@ def predict_topk_launches(w) -> int:
     items (128 groups of one head each, one CTA per SM) leave a partly filled
     last wave of at least two full ones, the library launches that wave on its
     own and the transposes in two head ranges (three more launches)."""
+    import torch
     nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     tiles = -(-w.nb // 128)
     items = w.B * w.H * tiles
