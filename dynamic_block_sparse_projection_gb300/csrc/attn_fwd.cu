@@ -11,8 +11,10 @@
 //   S = Q K_j^T            tcgen05.mma, A = Q (smem), B = K_j (smem), D in TMEM
 //   P = exp2(S*c - m)      softmax warpgroup, P written back to TMEM as bf16
 //   O += P V_j             tcgen05.mma, A = P (TMEM), B = V_j (smem, MN-major)
-// with an online (running-max) softmax; O is only rescaled when the running
-// max grows by more than 2^8 (values of P then stay below 256).
+// with an online softmax whose reference m is the first block's row maximum:
+// a later block keeps it unless one of its values of P would exceed 2^64 (its
+// block sum tells), and only then are the block's maximum taken, O rescaled
+// and the block redone, so the common path computes no row maximum.
 //
 // Warp roles (224 threads):
 //   warp 0      TMA producer of Q and the K_j ring (one lane).
@@ -315,60 +317,76 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_ld_wait();
         // row max as 8 independent partial maxima (short dependency chains),
         // two new values per three-input max
-        float mx8[8];
+        auto row_max = [&]() -> float {
+          float mx8[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(xr[i]);
+          for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(xr[i]);
 #pragma unroll
-        for (int j = 8; j < BETA; j += 16)
+          for (int j = 8; j < BETA; j += 16)
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            mx8[i] = j + 8 < BETA ? max3f(mx8[i], __uint_as_float(xr[j + i]), __uint_as_float(xr[j + 8 + i]))
-                                  : fmaxf(mx8[i], __uint_as_float(xr[j + i]));
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        const float m_new = fmaxf(m, mx * scale_log2);
-        if (n == 0) {
-          m = m_new;
-        } else if (__any_sync(0xffffffffu, m_new > m + 8.0f)) {
-          // rescale this warp's O rows once the previous PV product has landed
-          const uint32_t gp = gn - 1;
-          if (!mbar_wait_warp(&o_done[gp % NST], (gp / NST) & 1u, abort_flag, ctl, kid | W_O)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const float alpha = ex2(m - m_new);
-          l *= alpha;
-          m = m_new;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_off + T::O_COL + c * 32, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tmem_st32(tmem + lane_off + T::O_COL + c * 32, o);
-          }
-          tmem_st_wait();
-        }
+            for (int i = 0; i < 8; ++i)
+              mx8[i] = j + 8 < BETA ? max3f(mx8[i], __uint_as_float(xr[j + i]), __uint_as_float(xr[j + 8 + i]))
+                                    : fmaxf(mx8[i], __uint_as_float(xr[j + i]));
+          return fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        };
         // P = exp2(S c - m): exponent and row sum on packed fp32 pairs
-        const uint64_t c2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m, -m);
-        uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[BETA / 2];
+        auto exponentiate = [&](float mref) -> float {
+          const uint64_t c2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-mref, -mref);
+          uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-        for (int j = 0; j < BETA / 2; ++j) {
-          float x0, x1;
-          f2_unpack(fma2(f2_pack(__uint_as_float(xr[2 * j]), __uint_as_float(xr[2 * j + 1])), c2, nm2), x0, x1);
-          const float p0 = ex2(x0);
-          const float p1 = ex2(x1);
-          rs2[j & 3] = add2(rs2[j & 3], f2_pack(p0, p1));
-          pk[j] = pack_bf16x2(p0, p1);
-        }
-        {
+          for (int j = 0; j < BETA / 2; ++j) {
+            float x0, x1;
+            f2_unpack(fma2(f2_pack(__uint_as_float(xr[2 * j]), __uint_as_float(xr[2 * j + 1])), c2, nm2), x0, x1);
+            const float p0 = ex2(x0);
+            const float p1 = ex2(x1);
+            rs2[j & 3] = add2(rs2[j & 3], f2_pack(p0, p1));
+            pk[j] = pack_bf16x2(p0, p1);
+          }
           float a0, a1;
           f2_unpack(add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3])), a0, a1);
-          l += a0 + a1;
+          return a0 + a1;
+        };
+        // The running maximum is the first block's; a later block keeps it
+        // unless one of its values would exceed 2^kLazyLog2 (its block sum
+        // tells: every value is at most the sum), in which case the block's
+        // true maximum is taken, O rescaled and the block redone.  l and O stay
+        // far inside the fp32 range (at most 2^kLazyLog2 per value, 4096
+        // blocks of 128), so no row maximum is computed on the common path.
+        constexpr float kLazyLog2 = 64.0f;
+        float bsum;
+        if (n == 0) {
+          m = row_max() * scale_log2;
+          bsum = exponentiate(m);
+        } else {
+          bsum = exponentiate(m);
+          if (__any_sync(0xffffffffu, !(bsum <= 18446744073709551616.0f))) {   // 2^64
+            const float m_new = fmaxf(m, row_max() * scale_log2);
+            // rescale this warp's O rows once the previous PV product has landed
+            const uint32_t gp = gn - 1;
+            if (!mbar_wait_warp(&o_done[gp % NST], (gp / NST) & 1u, abort_flag, ctl, kid | W_O)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const float alpha = ex2(m - m_new);
+            l *= alpha;
+            m = m_new;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tmem + lane_off + T::O_COL + c * 32, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+              tmem_st32(tmem + lane_off + T::O_COL + c * 32, o);
+            }
+            tmem_st_wait();
+            bsum = exponentiate(m);
+          }
         }
+        l += bsum;
 #pragma unroll
         for (int c = 0; c < BETA / 32; ++c) tmem_st16(sb + c * 16, pk + c * 16);
         tmem_st_wait();
