@@ -105,6 +105,35 @@ def test_forward_dense_equals_masked_dense(dsv):
     assert rel_l2(to64(O), O_ref) <= O_REL_L2
 
 
+def test_forward_later_blocks_far_above_the_first(dsv):
+    """The forward's reference maximum is each row's first block's; a later
+    block whose values of P would pass 2^64 must take its own maximum and
+    rescale O.  Key blocks 1, 2, 3 are scaled by 3, 12 and 40 against 0.1 for
+    block 0, so the last blocks' exponents run far past 64 (and past the fp32
+    range) above the first block's maximum; the result must still be the
+    oracle's."""
+    B, H, N, d, block = 1, 2, 256, 64, 64
+    G = N // block
+    g = torch.Generator(device="cuda").manual_seed(11)
+    Qb = (torch.randn(B, H, N, d, generator=g, device="cuda") * 4).to(torch.bfloat16)
+    Kf = torch.randn(B, H, N, d, generator=g, device="cuda")
+    for j, f in enumerate((0.1, 3.0, 12.0, 40.0)):
+        Kf[:, :, j * block:(j + 1) * block] *= f
+    Kb = Kf.to(torch.bfloat16)
+    Vb = torch.randn(B, H, N, d, generator=g, device="cuda").to(torch.bfloat16)
+    fp_ = np.arange(0, B * H * G * G + 1, G)
+    fc_ = np.tile(np.arange(G), B * H * G)                # every row: blocks 0, 1, 2, 3 in this order
+    fp, fc = csr_to_device((fp_, fc_), "cuda")
+    O, lse = dsv.sparse_attn_fwd(Qb, Kb, Vb, fp, fc, block)
+    torch.cuda.synchronize()
+    assert dsv.device_error()[0] == 0
+    O_ref, L_ref = oracle.attn_fwd_groups(to64(Qb), to64(Kb), to64(Vb), fp_, fc_, block)
+    assert np.all(np.isfinite(to64(O))) and np.all(np.isfinite(to64(lse)))
+    assert rel_l2(to64(O), O_ref) <= O_REL_L2
+    assert max_abs_beyond_rounding(to64(O), O_ref) <= O_MAX_ABS
+    assert np.max(np.abs(to64(lse) - L_ref)) <= LSE_MAX_ABS
+
+
 def test_forward_empty_list_and_custom_scale(dsv):
     B, H, N, d, block = 1, 1, 256, 64, 64
     g = torch.Generator(device="cuda").manual_seed(5)
