@@ -215,6 +215,21 @@ __device__ __forceinline__ float fma_sat(float a, float b, float c) {
   asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+// x[e] for an index e that is the same in every lane of the warp (a jump on
+// e, so that x stays in registers)
+__device__ __forceinline__ uint32_t pick32(const uint32_t (&x)[32], int e) {
+  switch (e) {
+    case 0: return x[0];   case 1: return x[1];   case 2: return x[2];   case 3: return x[3];
+    case 4: return x[4];   case 5: return x[5];   case 6: return x[6];   case 7: return x[7];
+    case 8: return x[8];   case 9: return x[9];   case 10: return x[10]; case 11: return x[11];
+    case 12: return x[12]; case 13: return x[13]; case 14: return x[14]; case 15: return x[15];
+    case 16: return x[16]; case 17: return x[17]; case 18: return x[18]; case 19: return x[19];
+    case 20: return x[20]; case 21: return x[21]; case 22: return x[22]; case 23: return x[23];
+    case 24: return x[24]; case 25: return x[25]; case 26: return x[26]; case 27: return x[27];
+    case 28: return x[28]; case 29: return x[29]; case 30: return x[30]; default: return x[31];
+  }
+}
+
 // (w << 1) | sign bit of d: one funnel shift of the 64-bit value w:d
 __device__ __forceinline__ uint32_t shift_in_sign(uint32_t w, float d) {
   return __funnelshift_l(__float_as_uint(d), w, 1);
@@ -467,9 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             if constexpr (P == 1) {
 #pragma unroll
               for (int e = 0; e < 32; ++e)
-                if (FULL || e < nvg)
+                if (work && (FULL || e < nvg))
                   red_shared_add(hbase + (bin_bits(__uint_as_float(x[e]), sc, c0) << 9), 1u);
-              if (a.scores != nullptr) {
+              if (work && a.scores != nullptr) {
                 // check output: the scores this selection uses
                 float* dst = a.scores + grow * (long long)nb + j0;
 #pragma unroll
@@ -497,14 +512,24 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
                   above <<= 1;
                 }
               }
-              const uint32_t eq = above & ~word;
-              hist[word_at(wi, r)] = word;
-              if (eq) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
+              const uint32_t eq = work ? above & ~word : 0u;
+              if (work) hist[word_at(wi, r)] = word;
+              // the threshold bin's scores: one step per column where any row of
+              // the warp has one (every lane of the warp takes part: the pass
+              // runs for all 32 rows, those past the last group with no work),
+              // the score picked from the registers by that column
+              uint32_t ecols = __reduce_or_sync(0xffffffffu, eq);
+              if (ecols) {
+                // this row's slots, reserved at once (the row's four threads add
+                // candidates concurrently)
+                const int cnt = __popc(eq);
+                int pos = cnt ? atomicAdd(&rs[r].ccount, cnt) : 0;
+                while (ecols) {
+                  const int e = __ffs(ecols) - 1;
+                  ecols &= ecols - 1u;
                   if ((eq >> e) & 1u) {
-                    const int pos = atomicAdd(&rs[r].ccount, 1);
-                    if (pos < kCand) cand[pos * kRows + r] = make_uint2(order_key(__uint_as_float(x[e])), (uint32_t)(j0 + e));
+                    if (pos < kCand) cand[pos * kRows + r] = make_uint2(order_key(__uint_as_float(pick32(x, e))), (uint32_t)(j0 + e));
+                    ++pos;
                   }
                 }
               }
@@ -566,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
                 tc_fence_before();
                 mbar_arrive(&t_free[buf]);
               }
-              if (work) run_group(x, tile_of(pass, t), q, pass_tag);
+              run_group(x, tile_of(pass, t), q, pass_tag);   // every lane: pass 2 has warp-wide steps
             }
           }
           n += (uint32_t)nt;
