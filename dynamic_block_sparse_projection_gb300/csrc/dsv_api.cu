@@ -2,7 +2,9 @@
 //
 // Every entry point validates its arguments on the host before any launch
 // (returning DSV_ERR_INVALID_ARG / DSV_ERR_UNSUPPORTED and writing nothing),
-// then enqueues its kernels on the caller's stream without synchronising.
+// then enqueues its kernels on the caller's stream without synchronising
+// (dsv_predict_topk_blocks also forks part of its work onto a library-owned
+// side stream and joins it back with events).
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdint.h>
