@@ -501,15 +501,30 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
               // canonical NaN, sign clear).  The sign bits are shifted in from the
               // top, last column first, so that column e lands on bit e.
               uint32_t word = 0u, above = 0u;
+              if constexpr (FULL) {
+                // two columns per packed subtraction (each lane of it rounds like
+                // a scalar one)
+                const uint64_t kk2 = f2_pack(keep_v, keep_v), cc2 = f2_pack(coll_v, coll_v);
 #pragma unroll
-              for (int e = 31; e >= 0; --e) {
-                if (FULL || e < nvg) {
-                  const float s = __uint_as_float(x[e]);
-                  word = shift_in_sign(word, __fsub_rn(keep_v, s));
-                  above = shift_in_sign(above, __fsub_rn(coll_v, s));
-                } else {
-                  word <<= 1;
-                  above <<= 1;
+                for (int e = 31; e >= 1; e -= 2) {
+                  const uint64_t sv = f2_pack(__uint_as_float(x[e - 1]), __uint_as_float(x[e]));
+                  float dk0, dk1, dc0, dc1;
+                  f2_unpack(sub2(kk2, sv), dk0, dk1);
+                  f2_unpack(sub2(cc2, sv), dc0, dc1);
+                  word = shift_in_sign(shift_in_sign(word, dk1), dk0);
+                  above = shift_in_sign(shift_in_sign(above, dc1), dc0);
+                }
+              } else {
+#pragma unroll
+                for (int e = 31; e >= 0; --e) {
+                  if (e < nvg) {
+                    const float s = __uint_as_float(x[e]);
+                    word = shift_in_sign(word, __fsub_rn(keep_v, s));
+                    above = shift_in_sign(above, __fsub_rn(coll_v, s));
+                  } else {
+                    word <<= 1;
+                    above <<= 1;
+                  }
                 }
               }
               const uint32_t eq = work ? above & ~word : 0u;
