@@ -817,12 +817,18 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       }
       const long long hbase = (long long)b * G * a.hk.kpre[a.H] + (long long)a.hk.kpre[h] * G;
       int32_t* dst = a.fwd_col + hbase + (long long)g * k;
+      uint32_t mn = w0 < w1 ? hist[word_at(w0, r)] : 0u;
       for (int wi = w0; wi < w1; ++wi) {
-        uint32_t m = hist[word_at(wi, r)];
+        uint32_t m = mn;
+        if (wi + 1 < w1) mn = hist[word_at(wi + 1, r)];   // next word in flight
         while (m) {
-          if (pos < k) dst[pos] = wi * 32 + __ffs(m) - 1;
-          ++pos;
+          const int b0 = __ffs(m) - 1;
           m &= m - 1u;
+          const int b1 = __ffs(m) - 1;                    // -1 when m is now empty
+          m &= m - 1u;
+          if (pos < k) dst[pos] = wi * 32 + b0;
+          if (b1 >= 0 && pos + 1 < k) dst[pos + 1] = wi * 32 + b1;
+          pos += b1 >= 0 ? 2 : 1;
         }
       }
       if (cg == 0) {
