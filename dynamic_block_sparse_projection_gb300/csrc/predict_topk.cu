@@ -234,6 +234,7 @@ __device__ __forceinline__ uint32_t pick32(const uint32_t (&x)[32], int e) {
 __device__ __forceinline__ uint32_t shift_in_sign(uint32_t w, float d) {
   return __funnelshift_l(__float_as_uint(d), w, 1);
 }
+
 // The bin map of a row: z = clamp(s * sc + c0, 0, 1) (scores below the binned
 // range give 0, above it 1), bin = round(127 z), returned as the float bits
 // B0 + bin (adding 1.5 * 2^23 leaves the rounded value in the low mantissa
@@ -606,7 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
                 tc_fence_before();
                 mbar_arrive(&t_free[buf]);
               }
-              run_group(x, tile_of(pass, t), q, pass_tag);   // every lane: pass 2 has warp-wide steps
+              run_group(x, tile_of(pass, t), q, pass_tag);   // every lane (rows past G with no work):
+                                                             // pass 2 has warp-wide steps
             }
           }
           n += (uint32_t)nt;
