@@ -255,3 +255,13 @@ def test_host_validation_predict_topk(lib):
     assert L.dsv_predict_topk_blocks(*w4, s, k, *outs, None, FAKE + 16, ws, None) == lib.DSV_ERR_INVALID_ARG
     big = _shape(lib, N=128 * 4097, H=1)
     assert L.dsv_predict_topk_blocks(*w4, big, k, *outs, None, FAKE, 1 << 40, None) == lib.DSV_ERR_UNSUPPORTED
+
+
+def test_noalloc_scratch_holds_every_named_workload(lib):
+    """The allocation-free top-k's fixed 64 MiB scratch must hold the top-k
+    workspace (selection bitmask, per-segment counts, column totals) of every
+    named workload, long518k included (~62 MB)."""
+    from dynamic_block_sparse_projection_gb300 import workloads as wl
+    for w in wl.WORKLOADS.values():
+        need = lib.lib.dsv_topk_workspace_bytes(_shape(lib, B=w.B, H=w.H, N=w.N, d=w.d, block=w.block, r=w.r))
+        assert 0 < need <= (64 << 20), (w.name, need)
